@@ -1,0 +1,490 @@
+#!/usr/bin/env python3
+"""Benchmark of the implicit-GEMM conv2d layer on one or more GPUs.
+
+A step is one pass of the whole hot path -- forward (+ fused ReLU), d_input and
+wgrad (split-K partials + reduction) -- over one batch of seeded synthetic input
+of layer 1 of PufferLib PR #522's encoder in fp32: B=1024, IC=59, OC=128, 11x15
+input, K=5, S=3 -> 3x4, ReLU.  The value is whole-job GFLOP/s (algorithmic
+FLOPs 2*B*P*OC*IC*K*K per operation) with inputs resident in HBM; L2 is flushed
+(a 512 MiB write) between timed steps, outside the timed region.  The JSON line
+also carries per-operation us/iter for both layers in both dtypes, the roofline
+of the dominant kernel, the fp64 oracle's CPU throughput on a bounded sample,
+an end-to-end number through host buffers, and SM clocks sampled during the
+timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU (torchrun): every rank runs the same per-GPU workload (weak scaling,
+independent replicas; the layer needs no exchange for this measurement) and the
+slowest rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "µs/iter and GFLOP/s for conv fwd/dgrad/wgrad at B=1024; % of roofline"
+LAYERS = {
+    "layer1": dict(IC=59, OC=128, H=11, W=15, K=5, S=3, relu=1),
+    "layer2": dict(IC=128, OC=128, H=3, W=4, K=3, S=1, relu=0),
+}
+# PufferLib PR #522 bench output at B=1024 on a GPU the page does not name:
+# (forward us/iter, backward = wgrad + d_input us/iter) of its gemm_fast kernels.
+PR522_US = {("layer1", "f32"): (192.4102, 541.7361), ("layer2", "f32"): (56.8698, 100.2875),
+            ("layer1", "bf16"): (106.4277, 403.5356), ("layer2", "bf16"): (18.4427, 49.1440)}
+FLUSH_BYTES = 512 << 20
+OPS = ("fwd", "dgrad", "wgrad")
+
+
+def flops(B, IC, OC, H, W, K, S, **_):
+    OH, OW = (H - K) // S + 1, (W - K) // S + 1
+    return 2.0 * B * OH * OW * OC * IC * K * K
+
+
+def alg_bytes(op, B, IC, OC, H, W, K, S, relu, esize):
+    """Algorithmic HBM bytes of one operation: each tensor read or written once."""
+    OH, OW = (H - K) // S + 1, (W - K) // S + 1
+    nx, ny, nw = B * IC * H * W, B * OC * OH * OW, OC * IC * K * K
+    if op == "fwd":
+        n = nx + nw + ny
+    elif op == "dgrad":
+        n = ny + nw + nx + (ny if relu else 0)
+    else:
+        n = nx + ny + nw + (ny if relu else 0)
+    return n * esize
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--batch", type=int, default=1024)
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the other-config table, e2e and CPU baseline")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ----------------------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.t:
+                self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------------------
+# reference arm: the fp64 CPU oracle (the only other implementation of this layer)
+# ----------------------------------------------------------------------------------------
+def oracle_step(inp, shape):
+    import oracle
+    y, _ = oracle.conv_fwd(inp["x"], inp["w"], shape["S"], shape["relu"])
+    oracle.conv_bwd_data(inp["dy"], inp["w"], y, shape["H"], shape["W"], shape["S"], shape["relu"])
+    oracle.conv_bwd_filter(inp["x"], inp["dy"], y, shape["K"], shape["S"], shape["relu"])
+
+
+def cpu_baseline(shape, b_sample, min_seconds):
+    import oracle
+    from implicit_gemm_conv2d_gb300 import synth
+    oracle.build()
+    inp = synth.conv_inputs(b_sample, shape["IC"], shape["OC"], shape["H"], shape["W"], shape["K"],
+                            shape["S"], dtype="f32")
+    oracle_step(inp, shape)  # warm-up (page-in, thread start)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle_step(inp, shape)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds:
+            break
+    gflop = 3 * flops(B=b_sample, **shape) * n / 1e9
+    return {"value": gflop / el, "unit": "GFLOP/s", "cores": oracle.default_threads(), "kind": "oracle",
+            "sample": f"{n} step(s) of fwd+dgrad+wgrad on {b_sample} of the 1024 samples "
+                      f"(same shapes and seeded inputs), fp64 direct loops, {el:.1f} s"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    shape = LAYERS["layer1"]
+    b_sample = 8
+    from implicit_gemm_conv2d_gb300 import synth
+    import oracle
+    oracle.build()
+    inp = synth.conv_inputs(b_sample, shape["IC"], shape["OC"], shape["H"], shape["W"], shape["K"],
+                            shape["S"], dtype="f32")
+    for _ in range(args.warmup):
+        oracle_step(inp, shape)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(inp, shape)
+    el = time.perf_counter() - t0
+    value = 3 * flops(B=b_sample, **shape) * args.steps / 1e9 / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "layer-1 conv fwd+dgrad+wgrad, fused ReLU, IC=59 OC=128 11x15 K=5 S=3; "
+                               f"each step a {b_sample}-sample slice of the B=1024 batch",
+                   "l2": "n/a (host)"},
+        "cpu_baseline": {"value": value, "unit": "GFLOP/s", "cores": oracle.default_threads(),
+                         "kind": "oracle", "sample": f"{b_sample} samples per step"},
+        "e2e": {"value": value, "unit": "GFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------------------
+def source_sha(path):
+    h = hashlib.sha256()
+    with open(path, "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def read_traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source
+    it was taken from is unchanged (the sha in the table); else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        line = line.split("#", 1)[0].split()
+        if len(line) == 4 and line[0] == kernel_key:
+            src = os.path.join(ROOT, "implicit_gemm_conv2d_gb300", "csrc", line[3].split(":")[0])
+            if os.path.exists(src) and source_sha(src) == line[3].split(":")[1]:
+                return float(line[1])
+    return None
+
+
+class Workload:
+    def __init__(self, layer, dtype, B, device):
+        import torch
+        from implicit_gemm_conv2d_gb300 import binding, synth
+        self.layer, self.dtype, self.B = layer, dtype, B
+        self.shape = dict(LAYERS[layer])
+        self.tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+        s = self.shape
+        inp = synth.conv_inputs(B, s["IC"], s["OC"], s["H"], s["W"], s["K"], s["S"], dtype=dtype)
+        self.inp = inp
+        self.x = torch.from_numpy(inp["x"]).to(device).to(self.tdt).contiguous()
+        self.w = torch.from_numpy(inp["w"]).to(device).to(self.tdt).contiguous()
+        self.dy = torch.from_numpy(inp["dy"]).to(device).to(self.tdt).contiguous()
+        self.desc = binding.make_desc(B, s["IC"], s["OC"], s["H"], s["W"], s["K"], s["S"], s["relu"], self.tdt)
+        OH, OW = binding.out_dims(self.desc)
+        self.y = torch.empty((B, s["OC"], OH, OW), dtype=self.tdt, device=device)
+        self.dx = torch.empty_like(self.x)
+        self.dw = torch.empty_like(self.w)
+        self.ws = torch.empty(max(16, binding.conv_bwd_filter_workspace_size(self.desc)), dtype=torch.uint8,
+                              device=device)
+        self.flops = flops(B=B, **s)
+        self.launches = sum(binding.conv_query(op, self.desc)["launches"] for op in range(3))
+        self.plans = {name: binding.conv_query(op, self.desc) for op, name in enumerate(OPS)}
+
+    def op(self, name, stream=None):
+        from implicit_gemm_conv2d_gb300 import binding
+        relu_y = self.y if self.shape["relu"] else None
+        if name == "fwd":
+            binding.conv_fwd(self.desc, self.x, self.w, self.y, stream)
+        elif name == "dgrad":
+            binding.conv_bwd_data(self.desc, self.dy, self.w, relu_y, self.dx, stream)
+        else:
+            binding.conv_bwd_filter(self.desc, self.x, self.dy, relu_y, self.dw, self.ws, stream)
+
+
+def time_step(wl, flush_buf, steps, warmup, flush=True):
+    """Per-op device times (ms) for `steps` steps, L2 flushed before each step."""
+    import torch
+    from implicit_gemm_conv2d_gb300 import binding
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        for o in OPS:
+            wl.op(o)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for i in range(steps):
+        if flush:
+            binding.conv_l2_flush(flush_buf)
+        e = ev[i]
+        e[0].record(stream)
+        wl.op("fwd")
+        e[1].record(stream)
+        wl.op("dgrad")
+        e[2].record(stream)
+        wl.op("wgrad")
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    per = {o: [] for o in OPS}
+    total = []
+    for e in ev:
+        for j, o in enumerate(OPS):
+            per[o].append(e[j].elapsed_time(e[j + 1]))
+        total.append(e[0].elapsed_time(e[3]))
+    return per, total
+
+
+def warm_us(wl, iters=200, warmup=50):
+    """PR-style warm timing: back-to-back iterations of one op between two events."""
+    import torch
+    out = {}
+    for o in OPS:
+        for _ in range(warmup):
+            wl.op(o)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(iters):
+            wl.op(o)
+        b.record()
+        torch.cuda.synchronize()
+        out[o] = a.elapsed_time(b) / iters * 1e3
+    return out
+
+
+def e2e(wl, flush_buf, steps):
+    """Same step through the public API with host buffers: pinned host inputs are
+    copied in, the three operations run, the three results are copied out."""
+    import torch
+    from implicit_gemm_conv2d_gb300 import binding
+    xh = wl.x.cpu().pin_memory()
+    wh = wl.w.cpu().pin_memory()
+    dyh = wl.dy.cpu().pin_memory()
+    yh = torch.empty(wl.y.shape, dtype=wl.tdt).pin_memory()
+    dxh = torch.empty(wl.dx.shape, dtype=wl.tdt).pin_memory()
+    dwh = torch.empty(wl.dw.shape, dtype=wl.tdt).pin_memory()
+    stream = torch.cuda.current_stream()
+    times = []
+    for i in range(steps + 3):
+        binding.conv_l2_flush(flush_buf)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        wl.x.copy_(xh, non_blocking=True)
+        wl.w.copy_(wh, non_blocking=True)
+        wl.dy.copy_(dyh, non_blocking=True)
+        for o in OPS:
+            wl.op(o)
+        yh.copy_(wl.y, non_blocking=True)
+        dxh.copy_(wl.dx, non_blocking=True)
+        dwh.copy_(wl.dw, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= 3:
+            times.append(a.elapsed_time(b))
+    ms = statistics.mean(times)
+    esz = wl.x.element_size()
+    return {"value": 3 * wl.flops / (ms * 1e-3) / 1e9, "unit": "GFLOP/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": (wl.x.numel() + wl.w.numel() + wl.dy.numel()) * esz,
+            "d2h_bytes_per_step": (wl.y.numel() + wl.dx.numel() + wl.dw.numel()) * esz}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0}, \
+        "fallback"
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+    from implicit_gemm_conv2d_gb300 import binding, build as libbuild
+    if rank == 0 and not libbuild.up_to_date():
+        libbuild.build()
+    if world > 1:
+        dist.barrier()
+    binding.lib()
+    props = torch.cuda.get_device_properties(device)
+    sms = props.multi_processor_count
+    peaks, peaks_kind = load_peaks()
+
+    flush_buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    wl = Workload("layer1", "f32", args.batch, device)
+
+    # ---- the timed region ----
+    for _ in range(args.warmup):
+        for o in OPS:
+            wl.op(o)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        per, total = time_step(wl, flush_buf, args.steps, 0)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ms_step = sum(total) / len(total)
+    if world > 1:
+        t = torch.tensor([ms_step], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    value = world * 3 * wl.flops / (ms_step * 1e-3) / 1e9
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return 0
+
+    # ---- per-op summary and roofline of the dominant kernel ----
+    op_ms = {o: statistics.mean(per[o]) for o in OPS}
+    clocks = clk.summary()
+    sm_max = clocks["sm_max_mhz"] or peaks.get("sm_max_mhz", 2070.0)
+    ffma_peak = sms * 128 * 2 * sm_max * 1e6 / 1e12  # TFLOP/s: SMs x 128 FP32 lanes x FMA x clock
+    dom = max(OPS, key=lambda o: op_ms[o])
+    plan = wl.plans[dom]
+    achieved = wl.flops / (op_ms[dom] * 1e-3) / 1e12
+    kernel_key = f"{dom}:layer1:f32:B{args.batch}"
+    roofline = {"bound": "alu", "achieved": achieved, "peak": ffma_peak, "unit": "TFLOP/s",
+                "frac": achieved / ffma_peak, "traffic": read_traffic(kernel_key),
+                "kernel": f"{dom} ({plan['algo_name']}, {plan['launches']} launch(es))",
+                "peak_source": f"{sms} SMs x 128 FP32 lanes x 2 FLOP x {sm_max:.0f} MHz (FFMA pipe)"}
+    ops = {}
+    hbm = peaks["hbm_gbs"]
+    for o in OPS:
+        ab = alg_bytes(o, B=args.batch, esize=4, **wl.shape)
+        ops[o] = {"us": op_ms[o] * 1e3, "gflops": wl.flops / (op_ms[o] * 1e-3) / 1e9,
+                  "algo": wl.plans[o]["algo_name"], "launches": wl.plans[o]["launches"],
+                  "frac_alu": wl.flops / (op_ms[o] * 1e-3) / 1e12 / ffma_peak,
+                  "hbm_gbs": ab / (op_ms[o] * 1e-3) / 1e9}
+    pr_fwd, pr_bwd = PR522_US[("layer1", "f32")]
+    pr_gflops = 3 * wl.flops / ((pr_fwd + pr_bwd) * 1e-6) / 1e9 if args.batch == 1024 else None
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": (value / world / pr_gflops) if pr_gflops else None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"layer-1 conv fp32 fwd+dgrad+wgrad, fused ReLU, B={args.batch} IC=59 OC=128 "
+                               "11x15 K=5 S=3 -> 3x4 (PufferLib PR #522 encoder conv1)",
+                   "l2": "flushed (512 MiB write) between timed steps, outside the timed region",
+                   "inputs": "x~N(0,1), w~U(+-1/sqrt(IC*K*K)), dy~N(0,1), SplitMix64 seed 0x5EED2026"},
+        "ops": ops,
+        "roofline": roofline,
+        "gpu_launches": wl.launches * args.steps,
+        "clocks": clocks,
+        "peaks": {"source": peaks_kind, "hbm_gbs": hbm, "bf16_tflops": peaks.get("bf16_tflops")},
+    }
+    if not args.no_extras:
+        line["e2e"] = e2e(wl, flush_buf, min(args.steps, 50))
+        others = {}
+        for layer in ("layer1", "layer2"):
+            for dt in ("f32", "bf16"):
+                w2 = wl if (layer, dt) == ("layer1", "f32") else Workload(layer, dt, args.batch, device)
+                p2, _ = time_step(w2, flush_buf, 50, 5)
+                warm = warm_us(w2)
+                esz = 4 if dt == "f32" else 2
+                entry = {}
+                for o in OPS:
+                    t_ms = statistics.mean(p2[o])
+                    entry[o] = {"us_cold_l2": t_ms * 1e3, "us_warm": warm[o],
+                                "gflops": w2.flops / (t_ms * 1e-3) / 1e9,
+                                "hbm_gbs": alg_bytes(o, B=args.batch, esize=esz, **w2.shape) / (t_ms * 1e-3) / 1e9,
+                                "algo": w2.plans[o]["algo_name"]}
+                if args.batch == 1024:
+                    f, b = PR522_US[(layer, dt)]
+                    entry["pr522_us"] = {"fwd": f, "bwd": b}
+                others[f"{layer}_{dt}"] = entry
+        line["configs_b%d" % args.batch] = others
+        if world == 1:
+            line["cpu_baseline"] = cpu_baseline(LAYERS["layer1"], 128, 10.0)
+    print(json.dumps(line))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

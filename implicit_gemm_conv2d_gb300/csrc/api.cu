@@ -1,0 +1,285 @@
+// api.cu -- the C ABI declared in include/conv.h: argument validation (all on
+// the host, before anything is enqueued), the per-device facts a plan needs,
+// the choice of kernel family, and the launches.
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/conv.h"
+#include "internal.h"
+
+using namespace igc;
+
+namespace {
+
+constexpr int64_t kMaxElems = (int64_t(1) << 31) - 1;
+
+std::atomic<int> g_force[3] = {ALGO_AUTO, ALGO_AUTO, ALGO_AUTO};
+
+struct DevCache {
+    std::mutex mu;
+    DevInfo info[64];
+    bool have[64] = {};
+} g_dev;
+
+int device_info(DevInfo& out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CONV_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return CONV_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_dev.mu);
+    if (!g_dev.have[dev]) {
+        DevInfo d;
+        d.device = dev;
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return CONV_ERR_CUDA;
+        }
+        g_dev.info[dev] = d;
+        g_dev.have[dev] = true;
+    }
+    out = g_dev.info[dev];
+    return CONV_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Descriptor checks and the derived parameter block.  Host only, no CUDA calls.
+int make_params(const conv_desc_t* d, ConvParams& p)
+{
+    if (!d) return CONV_ERR_NULL;
+    if (d->B < 0 || d->IC < 1 || d->OC < 1 || d->K < 1 || d->S < 1 || d->H < d->K ||
+        d->W < d->K || (d->relu != 0 && d->relu != 1) || (d->dtype != CONV_F32 && d->dtype != CONV_BF16))
+        return CONV_ERR_DESC;
+    const int64_t OH = (int64_t(d->H) - d->K) / d->S + 1, OW = (int64_t(d->W) - d->K) / d->S + 1;
+    const int64_t nx = int64_t(d->B) * d->IC * d->H * d->W;
+    const int64_t ny = int64_t(d->B) * d->OC * OH * OW;
+    const int64_t nw = int64_t(d->OC) * d->IC * d->K * d->K;
+    const int64_t per_x = int64_t(d->IC) * d->H * d->W;
+    if (nx > kMaxElems || ny > kMaxElems || nw > kMaxElems || per_x > kMaxElems) return CONV_ERR_UNSUPPORTED;
+    p.B = d->B; p.IC = d->IC; p.OC = d->OC; p.H = d->H; p.W = d->W; p.K = d->K; p.S = d->S;
+    p.OH = int(OH); p.OW = int(OW); p.relu = d->relu;
+    p.P = int(OH * OW);
+    p.KK = d->K * d->K;
+    p.Kred = d->IC * p.KK;
+    p.HW = d->H * d->W;
+    p.IHW = int(per_x);
+    p.OCP = d->OC * p.P;
+    p.N = d->B * p.P;
+    p.dm_P = FastDivmod(uint32_t(p.P));
+    p.dm_OW = FastDivmod(uint32_t(p.OW));
+    p.dm_KK = FastDivmod(uint32_t(p.KK));
+    p.dm_K = FastDivmod(uint32_t(p.K));
+    p.dm_W = FastDivmod(uint32_t(p.W));
+    p.dm_HW = FastDivmod(uint32_t(p.HW));
+    return CONV_OK;
+}
+
+int cuda_status(cudaError_t e)
+{
+    if (e == cudaSuccess) return CONV_OK;
+    cudaGetLastError();
+    return CONV_ERR_CUDA;
+}
+
+// ---- plan selection -------------------------------------------------------------------
+int choose_fwd(const ConvParams& p, int dt, const DevInfo& d, Plan& pl)
+{
+    const int force = g_force[CONV_OP_FWD].load();
+    (void)dt;
+    if (force == ALGO_DIRECT) { pl = plan_fwd_direct(p, d); return CONV_OK; }
+    if (force == ALGO_TC) return CONV_ERR_UNSUPPORTED;
+    if (ffma_fwd_ok(p, d)) { pl = plan_fwd_ffma(p, d); return CONV_OK; }
+    if (force == ALGO_FFMA) return CONV_ERR_UNSUPPORTED;
+    pl = plan_fwd_direct(p, d);
+    return CONV_OK;
+}
+
+int choose_dgrad(const ConvParams& p, int dt, const DevInfo& d, Plan& pl)
+{
+    const int force = g_force[CONV_OP_BWD_DATA].load();
+    (void)dt;
+    if (force == ALGO_DIRECT) { pl = plan_dgrad_direct(p, d); return CONV_OK; }
+    if (force == ALGO_TC) return CONV_ERR_UNSUPPORTED;
+    if (ffma_dgrad_ok(p, d)) { pl = plan_dgrad_ffma(p, d); return CONV_OK; }
+    if (force == ALGO_FFMA) return CONV_ERR_UNSUPPORTED;
+    pl = plan_dgrad_direct(p, d);
+    return CONV_OK;
+}
+
+int choose_wgrad(const ConvParams& p, int dt, const DevInfo& d, Plan& pl)
+{
+    const int force = g_force[CONV_OP_BWD_FILTER].load();
+    (void)dt;
+    if (force == ALGO_DIRECT) { pl = plan_wgrad_direct(p, d); return CONV_OK; }
+    if (force == ALGO_TC) return CONV_ERR_UNSUPPORTED;
+    if (ffma_wgrad_ok(p, d)) { pl = plan_wgrad_ffma(p, d); return CONV_OK; }
+    if (force == ALGO_FFMA) return CONV_ERR_UNSUPPORTED;
+    pl = plan_wgrad_direct(p, d);
+    return CONV_OK;
+}
+
+int choose(int op, const ConvParams& p, int dt, const DevInfo& d, Plan& pl)
+{
+    switch (op) {
+    case CONV_OP_FWD: return choose_fwd(p, dt, d, pl);
+    case CONV_OP_BWD_DATA: return choose_dgrad(p, dt, d, pl);
+    case CONV_OP_BWD_FILTER: return choose_wgrad(p, dt, d, pl);
+    default: return CONV_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* conv_version(void) { return "0.1.0"; }
+
+const char* conv_status_string(int status)
+{
+    switch (status) {
+    case CONV_OK: return "CONV_OK";
+    case CONV_ERR_NULL: return "CONV_ERR_NULL: a required pointer is NULL";
+    case CONV_ERR_DESC: return "CONV_ERR_DESC: invalid descriptor";
+    case CONV_ERR_UNSUPPORTED: return "CONV_ERR_UNSUPPORTED: outside the library's limits";
+    case CONV_ERR_ALIGN: return "CONV_ERR_ALIGN: a pointer is not 16-byte aligned";
+    case CONV_ERR_WORKSPACE: return "CONV_ERR_WORKSPACE: workspace missing or too small";
+    case CONV_ERR_CUDA: return "CONV_ERR_CUDA: a CUDA call or kernel launch failed";
+    default: return "unknown conv status";
+    }
+}
+
+int conv_out_dims(const conv_desc_t* desc, int32_t* OH, int32_t* OW)
+{
+    ConvParams p;
+    const int rc = make_params(desc, p);
+    if (rc != CONV_OK) return rc;
+    if (!OH || !OW) return CONV_ERR_NULL;
+    *OH = p.OH;
+    *OW = p.OW;
+    return CONV_OK;
+}
+
+int conv_set_algo(int op, int algo)
+{
+    if (op < 0 || op > 2 || algo < ALGO_AUTO || algo > ALGO_TC) return CONV_ERR_UNSUPPORTED;
+    g_force[op].store(algo);
+    return CONV_OK;
+}
+
+int conv_query(int op, const conv_desc_t* desc, conv_plan_info_t* info)
+{
+    ConvParams p;
+    int rc = make_params(desc, p);
+    if (rc != CONV_OK) return rc;
+    if (!info) return CONV_ERR_NULL;
+    if (op < 0 || op > 2) return CONV_ERR_UNSUPPORTED;
+    DevInfo d;
+    if ((rc = device_info(d)) != CONV_OK) return rc;
+    Plan pl;
+    if ((rc = choose(op, p, desc->dtype, d, pl)) != CONV_OK) return rc;
+    info->algo = pl.algo;
+    info->launches = pl.launches;
+    info->grid = pl.grid;
+    info->block = pl.block;
+    info->smem_bytes = pl.smem;
+    info->splits = pl.splits;
+    info->workspace = pl.workspace;
+    return CONV_OK;
+}
+
+int conv_fwd(const conv_desc_t* desc, const void* x, const void* w, void* y, conv_stream_t stream)
+{
+    ConvParams p;
+    int rc = make_params(desc, p);
+    if (rc != CONV_OK) return rc;
+    if (p.B == 0) return CONV_OK;
+    if (!x || !w || !y) return CONV_ERR_NULL;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return CONV_ERR_ALIGN;
+    DevInfo d;
+    if ((rc = device_info(d)) != CONV_OK) return rc;
+    Plan pl;
+    if ((rc = choose_fwd(p, desc->dtype, d, pl)) != CONV_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (pl.algo == ALGO_DIRECT) return cuda_status(run_fwd_direct(pl, p, desc->dtype, x, w, y, s));
+    return cuda_status(run_fwd_ffma(pl, p, desc->dtype, x, w, y, s));
+}
+
+int conv_bwd_data(const conv_desc_t* desc, const void* dy, const void* w, const void* y, void* dx,
+                  conv_stream_t stream)
+{
+    ConvParams p;
+    int rc = make_params(desc, p);
+    if (rc != CONV_OK) return rc;
+    if (p.B == 0) return CONV_OK;
+    if (!dy || !w || !dx || (p.relu && !y)) return CONV_ERR_NULL;
+    if (!aligned16(dy) || !aligned16(w) || !aligned16(dx) || (p.relu && !aligned16(y)))
+        return CONV_ERR_ALIGN;
+    DevInfo d;
+    if ((rc = device_info(d)) != CONV_OK) return rc;
+    Plan pl;
+    if ((rc = choose_dgrad(p, desc->dtype, d, pl)) != CONV_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (pl.algo == ALGO_DIRECT) return cuda_status(run_dgrad_direct(pl, p, desc->dtype, dy, w, y, dx, s));
+    return cuda_status(run_dgrad_ffma(pl, p, desc->dtype, dy, w, y, dx, s));
+}
+
+size_t conv_bwd_filter_workspace_size(const conv_desc_t* desc)
+{
+    ConvParams p;
+    if (make_params(desc, p) != CONV_OK) return 0;
+    DevInfo d;
+    if (device_info(d) != CONV_OK) return 0;
+    Plan pl;
+    if (choose_wgrad(p, desc->dtype, d, pl) != CONV_OK) return 0;
+    return pl.workspace;
+}
+
+int conv_bwd_filter(const conv_desc_t* desc, const void* x, const void* dy, const void* y, void* dw,
+                    void* workspace, size_t workspace_bytes, conv_stream_t stream)
+{
+    ConvParams p;
+    int rc = make_params(desc, p);
+    if (rc != CONV_OK) return rc;
+    if (!dw) return CONV_ERR_NULL;
+    if (p.B > 0 && (!x || !dy || (p.relu && !y))) return CONV_ERR_NULL;
+    if (!aligned16(dw) || (p.B > 0 && (!aligned16(x) || !aligned16(dy) || (p.relu && !aligned16(y)))))
+        return CONV_ERR_ALIGN;
+    if (workspace && !aligned16(workspace)) return CONV_ERR_ALIGN;
+    DevInfo d;
+    if ((rc = device_info(d)) != CONV_OK) return rc;
+    Plan pl;
+    if ((rc = choose_wgrad(p, desc->dtype, d, pl)) != CONV_OK) return rc;
+    if (pl.workspace > 0 && (!workspace || workspace_bytes < pl.workspace)) return CONV_ERR_WORKSPACE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (pl.algo == ALGO_DIRECT) return cuda_status(run_wgrad_direct(pl, p, desc->dtype, x, dy, y, dw, s));
+    return cuda_status(run_wgrad_ffma(pl, p, desc->dtype, x, dy, y, dw, workspace, s));
+}
+
+uint64_t conv_fastdivmod_check(uint32_t d, uint32_t lo, uint32_t hi)
+{
+    if (d < 1 || d >= (1u << 31)) return ~uint64_t(0);
+    const FastDivmod f(d);
+    uint64_t bad = 0;
+    if (hi > (1u << 31)) hi = 1u << 31;
+    for (uint32_t n = lo; n < hi; ++n) {
+        uint32_t q, r;
+        f.divmod(n, q, r);
+        bad += (q != n / d) | (r != n % d);
+    }
+    return bad;
+}
+
+int conv_l2_flush(void* buf, size_t bytes, conv_stream_t stream)
+{
+    if (!buf) return CONV_ERR_NULL;
+    if (!aligned16(buf) || (bytes & 15u)) return CONV_ERR_ALIGN;
+    return cuda_status(run_l2_flush(buf, bytes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,79 @@
+// internal.h -- host-side plan and launcher interface between api.cu (the C
+// ABI: validation, dispatch) and the kernel translation units.
+#pragma once
+#include <cstddef>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace igc {
+
+struct DevInfo {
+    int device = -1;
+    int sms = 0;             // streaming multiprocessors
+    int smem_optin = 0;      // max dynamic shared memory per block (opt-in)
+    int cc_major = 0, cc_minor = 0;
+};
+
+// One operation's launch plan.  `algo` uses the conv_algo_t values.
+struct Plan {
+    int algo = 0;
+    int launches = 0;
+    int grid = 0, block = 0, smem = 0;
+    int splits = 0;
+    size_t workspace = 0;
+    int variant = 0;         // kernel-family specific selector
+};
+
+enum { DT_F32 = 0, DT_BF16 = 1 };
+enum { ALGO_AUTO = 0, ALGO_DIRECT = 1, ALGO_FFMA = 2, ALGO_TC = 3 };
+
+// ---- FFMA and direct families (kernels_ffma.cu) ------------------------------------
+bool ffma_fwd_ok(const ConvParams& p, const DevInfo& d);
+bool ffma_dgrad_ok(const ConvParams& p, const DevInfo& d);
+bool ffma_wgrad_ok(const ConvParams& p, const DevInfo& d);
+Plan plan_fwd_ffma(const ConvParams& p, const DevInfo& d);
+Plan plan_dgrad_ffma(const ConvParams& p, const DevInfo& d);
+Plan plan_wgrad_ffma(const ConvParams& p, const DevInfo& d);
+Plan plan_fwd_direct(const ConvParams& p, const DevInfo& d);
+Plan plan_dgrad_direct(const ConvParams& p, const DevInfo& d);
+Plan plan_wgrad_direct(const ConvParams& p, const DevInfo& d);
+
+cudaError_t run_fwd_ffma(const Plan&, const ConvParams&, int dt, const void* x, const void* w,
+                         void* y, cudaStream_t s);
+cudaError_t run_dgrad_ffma(const Plan&, const ConvParams&, int dt, const void* dy, const void* w,
+                           const void* y, void* dx, cudaStream_t s);
+cudaError_t run_wgrad_ffma(const Plan&, const ConvParams&, int dt, const void* x, const void* dy,
+                           const void* y, void* dw, void* ws, cudaStream_t s);
+cudaError_t run_fwd_direct(const Plan&, const ConvParams&, int dt, const void* x, const void* w,
+                           void* y, cudaStream_t s);
+cudaError_t run_dgrad_direct(const Plan&, const ConvParams&, int dt, const void* dy,
+                             const void* w, const void* y, void* dx, cudaStream_t s);
+cudaError_t run_wgrad_direct(const Plan&, const ConvParams&, int dt, const void* x,
+                             const void* dy, const void* y, void* dw, cudaStream_t s);
+// Deterministic split-K sum: dw = sum_{s < splits} ws[s] (fp32 partials, row
+// stride kpad), rounded once to the dtype.  splits == 0 writes zeros.
+cudaError_t run_wgrad_reduce(const ConvParams&, int dt, const float* ws, int splits, int kpad,
+                             void* dw, cudaStream_t s);
+cudaError_t run_l2_flush(void* buf, size_t bytes, cudaStream_t s);
+
+// Dynamic shared memory above 48 KB needs a per-kernel opt-in on every device;
+// done once per (kernel, device) and remembered.
+template <auto Kern>
+cudaError_t ensure_smem(int bytes)
+{
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && configured[dev] >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && dev >= 0 && dev < 64) configured[dev] = bytes;
+    return e;
+}
+
+inline int round_up(int a, int b) { return (a + b - 1) / b * b; }
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+}  // namespace igc

@@ -1,0 +1,160 @@
+/*
+ * conv.h -- C ABI of the implicit-GEMM conv2d library for GB300 (sm_103a).
+ *
+ * One layer type: a 2-D convolution with no padding, a square K x K kernel,
+ * stride S, NCHW activations, computed as an implicit GEMM on the GPU.  The
+ * operations are the three of PufferLib PR #522 ("Speedups to
+ * gemm_conv_forward and gemm_conv_backward kernels"; its bench blocks time a
+ * "forward" with relu=1 on layer 1, and a "backward" made of "wgrad" and
+ * "d_input"):
+ *
+ *   OH = floor((H - K) / S) + 1,   OW = floor((W - K) / S) + 1
+ *   conv_fwd         y[b,oc,oh,ow]   = act(sum_{ic,kh,kw} x[b,ic,oh*S+kh,ow*S+kw] * w[oc,ic,kh,kw])
+ *                    act = max(., 0) (result +0 for a non-positive sum) when relu, else identity
+ *   g                = dy * [y > 0] when relu (y: the forward output), else dy
+ *   conv_bwd_data    dx[b,ic,h,w]    = sum over (oc,kh,kw,oh,ow) with oh*S+kh = h, ow*S+kw = w
+ *                                      of g[b,oc,oh,ow] * w[oc,ic,kh,kw]
+ *   conv_bwd_filter  dw[oc,ic,kh,kw] = sum_{b,oh,ow} g[b,oc,oh,ow] * x[b,ic,oh*S+kh,ow*S+kw]
+ *
+ * Layouts (dense, row-major, no strides): x, dx (B,IC,H,W); y, dy
+ * (B,OC,OH,OW); w, dw (OC,IC,K,K).  Every tensor of a call has the
+ * descriptor's dtype: CONV_F32 (binary32 in and out, fp32 arithmetic) or
+ * CONV_BF16 (bfloat16 in and out, fp32 accumulation, one round-to-nearest-even
+ * rounding of each result).
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers are DEVICE pointers (cudaMalloc'd or equivalent) on the
+ *     current CUDA device, owned by the caller; the library keeps no reference
+ *     after the call returns and allocates no device memory.  Base pointers
+ *     must be 16-byte aligned.  Outputs must not overlap inputs.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream): they
+ *     enqueue kernels and return; they never synchronise.  Each call
+ *     overwrites its whole output (it does not accumulate into it).
+ *   - Results are deterministic: the same inputs give bit-identical outputs,
+ *     run to run (fixed reduction orders, no floating-point atomics).
+ *   - Errors are returned as a conv_status_t.  Argument errors are detected on
+ *     the host before anything is enqueued; CONV_ERR_CUDA reports a failed
+ *     launch (cudaGetLastError) and leaves the output unspecified.
+ *   - A batch of B = 0 is valid: conv_fwd and conv_bwd_data do nothing;
+ *     conv_bwd_filter writes dw = 0.
+ *   - Index arithmetic is 32-bit: every tensor must hold fewer than 2^31
+ *     elements (CONV_ERR_UNSUPPORTED otherwise).
+ */
+#ifndef IGCONV_CONV_H
+#define IGCONV_CONV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so this header needs no CUDA include. */
+struct CUstream_st;
+typedef struct CUstream_st* conv_stream_t;
+
+typedef enum { CONV_F32 = 0, CONV_BF16 = 1 } conv_dtype_t;
+
+/* Shape descriptor.  relu is 0 or 1; dtype is a conv_dtype_t value. */
+typedef struct {
+    int32_t B, IC, OC, H, W, K, S, relu;
+    int32_t dtype;
+} conv_desc_t;
+
+typedef enum {
+    CONV_OK = 0,
+    CONV_ERR_NULL = -1,        /* a required pointer is NULL                         */
+    CONV_ERR_DESC = -2,        /* descriptor invalid: a dim < 1 (B < 0), H or W < K,
+                                  relu not 0/1, dtype unknown                         */
+    CONV_ERR_UNSUPPORTED = -3, /* valid but outside the library's limits (2^31)      */
+    CONV_ERR_ALIGN = -4,       /* a base pointer is not 16-byte aligned              */
+    CONV_ERR_WORKSPACE = -5,   /* workspace NULL or smaller than the queried size    */
+    CONV_ERR_CUDA = -6         /* a CUDA call or kernel launch failed                */
+} conv_status_t;
+
+/* Algorithm families (conv_set_algo / conv_query). */
+typedef enum {
+    CONV_ALGO_AUTO = 0,   /* library choice (default)                                 */
+    CONV_ALGO_DIRECT = 1, /* one thread per output element; any shape                 */
+    CONV_ALGO_FFMA = 2,   /* fp32 FFMA register-tiled implicit GEMM                   */
+    CONV_ALGO_TC = 3      /* tcgen05 tensor cores, TMEM accumulator (bf16)            */
+} conv_algo_t;
+
+typedef enum { CONV_OP_FWD = 0, CONV_OP_BWD_DATA = 1, CONV_OP_BWD_FILTER = 2 } conv_op_t;
+
+/* Forward:  y = act(conv(x, w)).
+ *   x: (B,IC,H,W)   w: (OC,IC,K,K)   y: (B,OC,OH,OW), written.
+ * Returns CONV_OK or an error code (see above). */
+int conv_fwd(const conv_desc_t* desc, const void* x, const void* w, void* y,
+             conv_stream_t stream);
+
+/* Data gradient (d_input):  dx = conv^T(g, w), g = dy masked by y > 0 when relu.
+ *   dy: (B,OC,OH,OW)  w: (OC,IC,K,K)  y: (B,OC,OH,OW) forward output, required
+ *   when desc->relu (the mask source), ignored otherwise (may be NULL)
+ *   dx: (B,IC,H,W), written. */
+int conv_bwd_data(const conv_desc_t* desc, const void* dy, const void* w, const void* y,
+                  void* dx, conv_stream_t stream);
+
+/* Bytes of device workspace conv_bwd_filter needs for this descriptor on the
+ * current device (split-K partial sums), or 0 if it needs none or the
+ * descriptor is invalid.  Host-only; depends on the device's SM count. */
+size_t conv_bwd_filter_workspace_size(const conv_desc_t* desc);
+
+/* Weight gradient (wgrad):  dw = sum over b,oh,ow of g (x) patches(x), as a
+ * split-K reduction over B*OH*OW: a first kernel writes fp32 partial sums of
+ * contiguous ranges of (b,oh,ow) into the workspace, a second sums them in
+ * ascending range order and rounds once to the output dtype.
+ *   x: (B,IC,H,W)  dy: (B,OC,OH,OW)  y: forward output, required when relu
+ *   dw: (OC,IC,K,K), written.
+ *   workspace: device buffer of at least conv_bwd_filter_workspace_size(desc)
+ *   bytes, 16-byte aligned, owned by the caller; contents on entry are
+ *   ignored and on return are unspecified.  May be NULL when the size is 0. */
+int conv_bwd_filter(const conv_desc_t* desc, const void* x, const void* dy, const void* y,
+                    void* dw, void* workspace, size_t workspace_bytes, conv_stream_t stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* conv_status_string(int status);
+
+/* Output spatial size for a descriptor (host-only validation helper). */
+int conv_out_dims(const conv_desc_t* desc, int32_t* OH, int32_t* OW);
+
+/* Launch plan for one operation on the current device, as the next call
+ * with this descriptor would run it. */
+typedef struct {
+    int32_t algo;         /* conv_algo_t actually used                        */
+    int32_t launches;     /* kernels enqueued per call                        */
+    int32_t grid;         /* CTAs of the main kernel                          */
+    int32_t block;        /* threads per CTA of the main kernel               */
+    int32_t smem_bytes;   /* dynamic shared memory of the main kernel         */
+    int32_t splits;       /* wgrad: number of split-K ranges (else 0)         */
+    size_t workspace;     /* wgrad: workspace bytes (else 0)                  */
+} conv_plan_info_t;
+int conv_query(int op, const conv_desc_t* desc, conv_plan_info_t* info);
+
+/* Force an algorithm family for one operation (CONV_ALGO_AUTO restores the
+ * library's choice).  Process-wide, not thread-safe; meant for tests and
+ * benchmarks.  Returns CONV_ERR_UNSUPPORTED for an unknown op or algo.  A
+ * forced family that cannot run a given descriptor makes that call return
+ * CONV_ERR_UNSUPPORTED. */
+int conv_set_algo(int op, int algo);
+
+/* Diagnostics.  conv_fastdivmod_check runs, on the host, the library's
+ * division-by-invariant-integer routine (Granlund & Montgomery, "Division by
+ * invariant integers using multiplication", PLDI 1994) for divisor d over
+ * every dividend in [lo, hi) and returns how many quotients or remainders
+ * differ from '/' and '%'; (uint64_t)-1 if d is outside [1, 2^31). */
+uint64_t conv_fastdivmod_check(uint32_t d, uint32_t lo, uint32_t hi);
+
+/* Write `bytes` bytes of `buf` (device memory, 16-byte aligned, bytes a
+ * multiple of 16) on `stream`, evicting earlier data from L2; benchmarks use
+ * it between timed iterations. */
+int conv_l2_flush(void* buf, size_t bytes, conv_stream_t stream);
+
+/* Library version, e.g. "0.1.0". */
+const char* conv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* IGCONV_CONV_H */

@@ -1,0 +1,147 @@
+"""GPU parity: the library's forward, d_input and wgrad, called through the C
+ABI, against the fp64 oracle on the same seeded inputs, element by element,
+within the normalised-error tolerances of tests/gpu_cases.py.  Covers both
+layers of PufferLib PR #522's encoder at B = 1, a ragged 37 and the full
+1024, both dtypes, every kernel family, odd shapes that exercise tile tails,
+and the degenerate cases (empty batch, 1x1 kernel, kernel as large as the
+input)."""
+import numpy as np
+import pytest
+import torch
+
+from implicit_gemm_conv2d_gb300 import binding
+
+from .gpu_cases import L1, L2, Case, check, to_np
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = {
+    "L1": L1,
+    "L2": L2,
+    "odd": dict(IC=3, OC=5, H=7, W=9, K=2, S=2, relu=True),
+    "wide_oc_p16": dict(IC=4, OC=200, H=6, W=6, K=3, S=1, relu=False),
+    "kk_above_128": dict(IC=2, OC=8, H=13, W=12, K=12, S=1, relu=True),
+    "k1": dict(IC=16, OC=24, H=3, W=5, K=1, S=1, relu=False),
+    "k_eq_input": dict(IC=7, OC=33, H=5, W=5, K=5, S=2, relu=True),
+    "stride_gt_k": dict(IC=5, OC=20, H=10, W=11, K=2, S=3, relu=False),
+}
+
+
+@pytest.fixture(autouse=True)
+def _restore_algo():
+    yield
+    for op in range(3):
+        binding.conv_set_algo(op, binding.ALGO_AUTO)
+
+
+def run_and_check(c: Case, label: str):
+    y = c.gpu_fwd()
+    dx = c.gpu_dgrad(y)
+    dw = c.gpu_wgrad(y)
+    torch.cuda.synchronize()
+    yn = to_np(y)
+    ref, den = c.ref_fwd()
+    e1 = check(yn, ref, den, c.dtype, f"{label} fwd")
+    ref, den = c.ref_dgrad(yn)
+    e2 = check(to_np(dx), ref, den, c.dtype, f"{label} dgrad")
+    ref, den = c.ref_wgrad(yn)
+    e3 = check(to_np(dw), ref, den, c.dtype, f"{label} wgrad")
+    return e1, e2, e3
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("B", [1, 37, 1024])
+@pytest.mark.parametrize("layer", ["L1", "L2"])
+def test_encoder_layers(layer, B, dtype):
+    run_and_check(Case(B, **SHAPES[layer], dtype=dtype), f"{layer} B={B} {dtype}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [s for s in SHAPES if s not in ("L1", "L2")])
+def test_odd_shapes(shape, dtype):
+    run_and_check(Case(5, **SHAPES[shape], dtype=dtype), f"{shape} {dtype}")
+
+
+@pytest.mark.parametrize("algo", [binding.ALGO_DIRECT, binding.ALGO_FFMA])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("layer", ["L1", "L2"])
+def test_each_family(layer, dtype, algo):
+    for op in range(3):
+        binding.conv_set_algo(op, algo)
+    c = Case(29, **SHAPES[layer], dtype=dtype)
+    for op in range(3):
+        assert binding.conv_query(op, c.desc)["algo"] == algo
+    run_and_check(c, f"{layer} {dtype} algo={algo}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("layer", ["L1", "L2"])
+def test_bit_identical_run_to_run(layer, dtype):
+    c = Case(1024, **SHAPES[layer], dtype=dtype)
+    outs = []
+    for _ in range(2):
+        y = c.gpu_fwd()
+        outs.append((y, c.gpu_dgrad(y), c.gpu_wgrad(y)))
+    torch.cuda.synchronize()
+    for a, b in zip(*outs):
+        assert torch.equal(a.view(torch.int16 if a.dtype == torch.bfloat16 else torch.int32),
+                           b.view(torch.int16 if b.dtype == torch.bfloat16 else torch.int32))
+
+
+def test_layer1_unread_column_has_zero_gradient():
+    c = Case(64, **L1, dtype="f32")
+    y = c.gpu_fwd()
+    dx = c.gpu_dgrad(y)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(dx[..., 14]).item() == 0
+    assert torch.count_nonzero(dx[..., :14]).item() > 0
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_empty_batch(dtype):
+    c = Case(1, **L1, dtype=dtype)
+    d0 = binding.make_desc(0, 59, 128, 11, 15, 5, 3, 1, c.x.dtype)
+    dw = torch.full((128, 59, 5, 5), 7.0, dtype=c.x.dtype, device="cuda")
+    n = binding.conv_bwd_filter_workspace_size(d0)
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device="cuda")
+    binding.conv_bwd_filter(d0, c.x[:0], c.dy[:0], c.dy[:0], dw, ws)
+    binding.conv_fwd(d0, c.x[:0], c.w, torch.empty(0, device="cuda", dtype=c.x.dtype))
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(dw).item() == 0
+
+
+def test_workspace_too_small_is_rejected():
+    c = Case(64, **L1, dtype="f32")
+    y = c.gpu_fwd()
+    need = binding.conv_bwd_filter_workspace_size(c.desc)
+    assert need > 0
+    dw = torch.empty((128, 59, 5, 5), device="cuda")
+    small = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(binding.ConvError) as ei:
+        binding.conv_bwd_filter(c.desc, c.x, c.dy, y, dw, small)
+    assert ei.value.status == -5
+    with pytest.raises(binding.ConvError):
+        binding.conv_bwd_filter(c.desc, c.x, c.dy, y, dw, None)
+
+
+def test_query_reports_plan():
+    c = Case(1024, **L1, dtype="f32")
+    q = binding.conv_query(binding.OP_BWD_FILTER, c.desc)
+    assert q["launches"] == 2 and q["splits"] >= 1 and q["workspace"] > 0
+    q = binding.conv_query(binding.OP_FWD, c.desc)
+    assert q["launches"] == 1 and q["grid"] >= 1
+
+
+def test_outputs_fully_overwritten():
+    """Each call overwrites its whole output: pre-fill with NaN and compare."""
+    c = Case(37, **L1, dtype="f32")
+    y = torch.full((37, 128, 3, 4), float("nan"), device="cuda")
+    binding.conv_fwd(c.desc, c.x, c.w, y)
+    dx = torch.full((37, 59, 11, 15), float("nan"), device="cuda")
+    binding.conv_bwd_data(c.desc, c.dy, c.w, y, dx)
+    dw = torch.full((128, 59, 5, 5), float("nan"), device="cuda")
+    ws = torch.full((binding.conv_bwd_filter_workspace_size(c.desc) // 4,), float("nan"), device="cuda")
+    binding.conv_bwd_filter(c.desc, c.x, c.dy, y, dw, ws)
+    torch.cuda.synchronize()
+    for t in (y, dx, dw):
+        assert not torch.isnan(t).any()
