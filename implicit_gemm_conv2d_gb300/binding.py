@@ -51,7 +51,8 @@ class PlanInfo(ctypes.Structure):
 
 EXPORTS = ["conv_fwd", "conv_bwd_data", "conv_bwd_filter_workspace_size", "conv_bwd_filter",
            "conv_status_string", "conv_out_dims", "conv_query", "conv_set_algo",
-           "conv_fastdivmod_check", "conv_l2_flush", "conv_version"]
+           "conv_fastdivmod_check", "conv_l2_flush", "conv_version", "conv_bwd_filter_noalloc"]
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 def library_path() -> str:
@@ -84,6 +85,7 @@ def lib():
         L.conv_fastdivmod_check.restype = ctypes.c_uint64
         L.conv_l2_flush.argtypes = [vp, sz, vp]
         L.conv_version.restype = ctypes.c_char_p
+        L.conv_bwd_filter_noalloc.argtypes = [dp, vp, vp, vp, vp, vp]
         _lib = L
         return L
 
@@ -139,6 +141,14 @@ def conv_bwd_filter(desc: ConvDesc, x, dy, y, dw, workspace, stream=None) -> Non
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().conv_bwd_filter(ctypes.byref(desc), _ptr(x), _ptr(dy), _ptr(y), _ptr(dw),
                                  _ptr(workspace), nbytes, _stream(stream)), "conv_bwd_filter")
+
+
+def conv_bwd_filter_noalloc(desc: ConvDesc, x, dy, y, dw, stream=None) -> None:
+    """Weight gradient with no workspace argument and no allocation: the split-K
+    partials use the library's fixed scratch array (see include/conv.h).  For
+    callers that cannot allocate device memory; concurrent calls race."""
+    _check(lib().conv_bwd_filter_noalloc(ctypes.byref(desc), _ptr(x), _ptr(dy), _ptr(y), _ptr(dw),
+                                         _stream(stream)), "conv_bwd_filter_noalloc")
 
 
 def conv_query(op: int, desc: ConvDesc) -> dict:

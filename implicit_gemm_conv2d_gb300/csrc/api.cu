@@ -11,11 +11,9 @@
 
 using namespace igc;
 
-namespace {
+namespace igc {
 
 constexpr int64_t kMaxElems = (int64_t(1) << 31) - 1;
-
-std::atomic<int> g_force[3] = {ALGO_AUTO, ALGO_AUTO, ALGO_AUTO};
 
 struct DevCache {
     std::mutex mu;
@@ -86,6 +84,12 @@ int cuda_status(cudaError_t e)
     cudaGetLastError();
     return CONV_ERR_CUDA;
 }
+
+}  // namespace igc
+
+namespace {
+
+std::atomic<int> g_force[3] = {ALGO_AUTO, ALGO_AUTO, ALGO_AUTO};
 
 // ---- plan selection -------------------------------------------------------------------
 int choose_fwd(const ConvParams& p, int dt, const DevInfo& d, Plan& pl)

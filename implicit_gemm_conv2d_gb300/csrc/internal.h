@@ -4,6 +4,7 @@
 #include <cstddef>
 #include <cuda_runtime.h>
 
+#include "../../include/conv.h"
 #include "common.cuh"
 
 namespace igc {
@@ -27,6 +28,12 @@ struct Plan {
 
 enum { DT_F32 = 0, DT_BF16 = 1 };
 enum { ALGO_AUTO = 0, ALGO_DIRECT = 1, ALGO_FFMA = 2, ALGO_TC = 3 };
+
+// ---- host helpers shared by the C-ABI translation units (api.cu) --------------------
+int device_info(DevInfo& out);                      // current device, cached; conv_status_t
+int make_params(const conv_desc_t* d, ConvParams& p);  // validation, no CUDA calls
+bool aligned16(const void* p);
+int cuda_status(cudaError_t e);                     // cudaSuccess -> CONV_OK, else CONV_ERR_CUDA
 
 // ---- FFMA and direct families (kernels_ffma.cu) ------------------------------------
 bool ffma_fwd_ok(const ConvParams& p, const DevInfo& d);

@@ -113,6 +113,32 @@ size_t conv_bwd_filter_workspace_size(const conv_desc_t* desc);
 int conv_bwd_filter(const conv_desc_t* desc, const void* x, const void* dy, const void* y,
                     void* dw, void* workspace, size_t workspace_bytes, conv_stream_t stream);
 
+/* Weight gradient that allocates nothing (the paper has no counterpart; this
+ * entry point exists for callers of this library that cannot allocate device
+ * memory: hosts that hand the library only the input and output buffers and own
+ * every other byte, and code that must not allocate while a step runs, where an
+ * allocation can block on the device or fail under memory pressure).
+ *
+ * Computes the same dw as conv_bwd_filter with the same split-K FFMA kernels,
+ * but the fp32 split-K partials live in a scratch array inside the library: a
+ * file-scope __device__ array of CONV_NOALLOC_SCRATCH_BYTES that every GPU which
+ * loads the library holds until the process exits.  The number of split-K
+ * ranges is capped so the partials fit; a descriptor whose single partial
+ * (OC * round_up(IC*K*K, 4) * 4 bytes) exceeds the array is rejected with
+ * CONV_ERR_UNSUPPORTED before anything is enqueued.  No workspace is passed and
+ * the call makes no cudaMalloc / cudaFree and no allocating library call.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call shares the one array: calls that overlap on the GPU
+ * (e.g. on two streams, or from two threads) race and corrupt each other's
+ * result.  Nothing in the array needs to start at zero: every partial the
+ * reduction reads is written first by the same call.
+ *   x, dy, y, dw, stream: as for conv_bwd_filter. */
+#define CONV_NOALLOC_SCRATCH_BYTES (16u << 20)
+int conv_bwd_filter_noalloc(const conv_desc_t* desc, const void* x, const void* dy, const void* y,
+                            void* dw, conv_stream_t stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* conv_status_string(int status);
 
