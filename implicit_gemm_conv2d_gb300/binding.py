@@ -51,7 +51,8 @@ class PlanInfo(ctypes.Structure):
 
 EXPORTS = ["conv_fwd", "conv_bwd_data", "conv_bwd_filter_workspace_size", "conv_bwd_filter",
            "conv_status_string", "conv_out_dims", "conv_query", "conv_set_algo",
-           "conv_fastdivmod_check", "conv_l2_flush", "conv_version", "conv_bwd_filter_noalloc"]
+           "conv_fastdivmod_check", "conv_l2_flush", "conv_version", "conv_bwd_filter_noalloc",
+           "conv_device_status"]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -86,6 +87,7 @@ def lib():
         L.conv_l2_flush.argtypes = [vp, sz, vp]
         L.conv_version.restype = ctypes.c_char_p
         L.conv_bwd_filter_noalloc.argtypes = [dp, vp, vp, vp, vp, vp]
+        L.conv_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
         _lib = L
         return L
 
@@ -170,6 +172,13 @@ def conv_fastdivmod_check(d: int, lo: int, hi: int) -> int:
 def conv_l2_flush(buf, stream=None) -> None:
     _check(lib().conv_l2_flush(_ptr(buf), buf.numel() * buf.element_size(), _stream(stream)),
            "conv_l2_flush")
+
+
+def conv_device_status(reset: bool = False) -> int:
+    """Timeout bits set by the tensor-core kernels (0 = none).  Synchronises."""
+    v = ctypes.c_uint32()
+    _check(lib().conv_device_status(ctypes.byref(v), int(reset)), "conv_device_status")
+    return v.value
 
 
 def conv_version() -> str:

@@ -95,9 +95,11 @@ std::atomic<int> g_force[3] = {ALGO_AUTO, ALGO_AUTO, ALGO_AUTO};
 int choose_fwd(const ConvParams& p, int dt, const DevInfo& d, Plan& pl)
 {
     const int force = g_force[CONV_OP_FWD].load();
-    (void)dt;
     if (force == ALGO_DIRECT) { pl = plan_fwd_direct(p, d); return CONV_OK; }
-    if (force == ALGO_TC) return CONV_ERR_UNSUPPORTED;
+    if (force == ALGO_TC || (force == ALGO_AUTO && dt == DT_BF16)) {
+        if (tc_fwd_ok(p, dt, d)) { pl = plan_fwd_tc(p, dt, d); return CONV_OK; }
+        if (force == ALGO_TC) return CONV_ERR_UNSUPPORTED;
+    }
     if (ffma_fwd_ok(p, d)) { pl = plan_fwd_ffma(p, d); return CONV_OK; }
     if (force == ALGO_FFMA) return CONV_ERR_UNSUPPORTED;
     pl = plan_fwd_direct(p, d);
@@ -119,9 +121,11 @@ int choose_dgrad(const ConvParams& p, int dt, const DevInfo& d, Plan& pl)
 int choose_wgrad(const ConvParams& p, int dt, const DevInfo& d, Plan& pl)
 {
     const int force = g_force[CONV_OP_BWD_FILTER].load();
-    (void)dt;
     if (force == ALGO_DIRECT) { pl = plan_wgrad_direct(p, d); return CONV_OK; }
-    if (force == ALGO_TC) return CONV_ERR_UNSUPPORTED;
+    if (force == ALGO_TC || (force == ALGO_AUTO && dt == DT_BF16)) {
+        if (tc_wgrad_ok(p, dt, d)) { pl = plan_wgrad_tc(p, dt, d); return CONV_OK; }
+        if (force == ALGO_TC) return CONV_ERR_UNSUPPORTED;
+    }
     if (ffma_wgrad_ok(p, d)) { pl = plan_wgrad_ffma(p, d); return CONV_OK; }
     if (force == ALGO_FFMA) return CONV_ERR_UNSUPPORTED;
     pl = plan_wgrad_direct(p, d);
@@ -211,6 +215,7 @@ int conv_fwd(const conv_desc_t* desc, const void* x, const void* w, void* y, con
     if ((rc = choose_fwd(p, desc->dtype, d, pl)) != CONV_OK) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (pl.algo == ALGO_DIRECT) return cuda_status(run_fwd_direct(pl, p, desc->dtype, x, w, y, s));
+    if (pl.algo == ALGO_TC) return cuda_status(run_fwd_tc(pl, p, desc->dtype, x, w, y, s));
     return cuda_status(run_fwd_ffma(pl, p, desc->dtype, x, w, y, s));
 }
 
@@ -262,6 +267,8 @@ int conv_bwd_filter(const conv_desc_t* desc, const void* x, const void* dy, cons
     if (pl.workspace > 0 && (!workspace || workspace_bytes < pl.workspace)) return CONV_ERR_WORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (pl.algo == ALGO_DIRECT) return cuda_status(run_wgrad_direct(pl, p, desc->dtype, x, dy, y, dw, s));
+    if (pl.algo == ALGO_TC)
+        return cuda_status(run_wgrad_tc(pl, p, desc->dtype, x, dy, y, dw, workspace, d.sms, s));
     return cuda_status(run_wgrad_ffma(pl, p, desc->dtype, x, dy, y, dw, workspace, s));
 }
 
@@ -277,6 +284,18 @@ uint64_t conv_fastdivmod_check(uint32_t d, uint32_t lo, uint32_t hi)
         bad += (q != n / d) | (r != n % d);
     }
     return bad;
+}
+
+int conv_device_status(uint32_t* status, int reset)
+{
+    if (!status) return CONV_ERR_NULL;
+    unsigned v = 0;
+    if (tc_read_status(&v, reset != 0) != cudaSuccess) {
+        cudaGetLastError();
+        return CONV_ERR_CUDA;
+    }
+    *status = v;
+    return CONV_OK;
 }
 
 int conv_l2_flush(void* buf, size_t bytes, conv_stream_t stream)

@@ -80,7 +80,19 @@ cudaError_t ensure_smem(int bytes)
     return e;
 }
 
-inline int round_up(int a, int b) { return (a + b - 1) / b * b; }
-inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+// ---- tcgen05 tensor-core family (kernels_tc.cu) -------------------------------------
+bool tc_fwd_ok(const ConvParams& p, int dt, const DevInfo& d);
+Plan plan_fwd_tc(const ConvParams& p, int dt, const DevInfo& d);
+cudaError_t run_fwd_tc(const Plan&, const ConvParams&, int dt, const void* x, const void* w, void* y,
+                       cudaStream_t s);
+bool tc_wgrad_ok(const ConvParams& p, int dt, const DevInfo& d);
+Plan plan_wgrad_tc(const ConvParams& p, int dt, const DevInfo& d);
+cudaError_t run_wgrad_tc(const Plan&, const ConvParams&, int dt, const void* x, const void* dy,
+                         const void* y, void* dw, void* ws, int sms, cudaStream_t s);
+// Error bits the tensor-core kernels set when a bounded wait runs out.
+cudaError_t tc_read_status(unsigned* out, bool reset);
+
+__host__ __device__ inline int round_up(int a, int b) { return (a + b - 1) / b * b; }
+__host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 }  // namespace igc

@@ -172,6 +172,13 @@ int conv_set_algo(int op, int algo);
  * differ from '/' and '%'; (uint64_t)-1 if d is outside [1, 2^31). */
 uint64_t conv_fastdivmod_check(uint32_t d, uint32_t lo, uint32_t hi);
 
+/* Diagnostics: the tensor-core kernels bound every wait on an mbarrier; a wait
+ * that runs out makes the kernel set a bit here, free its tensor memory and
+ * return (its output is then unspecified).  Reads the word into *status
+ * (0 = no timeout since the last reset), and clears it if reset != 0.
+ * Synchronises the device. */
+int conv_device_status(uint32_t* status, int reset);
+
 /* Write `bytes` bytes of `buf` (device memory, 16-byte aligned, bytes a
  * multiple of 16) on `stream`, evicting earlier data from L2; benchmarks use
  * it between timed iterations. */

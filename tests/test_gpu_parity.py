@@ -145,3 +145,53 @@ def test_outputs_fully_overwritten():
     torch.cuda.synchronize()
     for t in (y, dx, dw):
         assert not torch.isnan(t).any()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("B", [3, 200])
+@pytest.mark.parametrize("shape", list(SHAPES))
+def test_tc_forward(shape, B, dtype):
+    """tcgen05 forward (bf16: kind::f16; fp32: 3xTF32) against the oracle."""
+    binding.conv_set_algo(binding.OP_FWD, binding.ALGO_TC)
+    c = Case(B, **SHAPES[shape], dtype=dtype)
+    assert binding.conv_query(binding.OP_FWD, c.desc)["algo"] == binding.ALGO_TC
+    y = c.gpu_fwd()
+    torch.cuda.synchronize()
+    ref, den = c.ref_fwd()
+    check(to_np(y), ref, den, dtype, f"tc fwd {shape} B={B} {dtype}")
+    assert binding.conv_device_status(reset=True) == 0
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("layer", ["L1", "L2"])
+def test_tc_forward_full_batch(layer, dtype):
+    binding.conv_set_algo(binding.OP_FWD, binding.ALGO_TC)
+    c = Case(1024, **SHAPES[layer], dtype=dtype)
+    y = c.gpu_fwd()
+    torch.cuda.synchronize()
+    ref, den = c.ref_fwd()
+    check(to_np(y), ref, den, dtype, f"tc fwd {layer} B=1024 {dtype}")
+    y2 = c.gpu_fwd()
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16 if dtype == "bf16" else torch.int32),
+                       y2.view(torch.int16 if dtype == "bf16" else torch.int32))
+    assert binding.conv_device_status(reset=True) == 0
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("B", [3, 200, 1024])
+@pytest.mark.parametrize("shape", list(SHAPES))
+def test_tc_wgrad(shape, B, dtype):
+    """tcgen05 wgrad split-K partials + reduction against the oracle."""
+    if B == 1024 and shape not in ("L1", "L2"):
+        pytest.skip("full batch only for the encoder layers")
+    binding.conv_set_algo(binding.OP_BWD_FILTER, binding.ALGO_TC)
+    c = Case(B, **SHAPES[shape], dtype=dtype)
+    assert binding.conv_query(binding.OP_BWD_FILTER, c.desc)["algo"] == binding.ALGO_TC
+    y = c.gpu_fwd()
+    dw = c.gpu_wgrad(y)
+    torch.cuda.synchronize()
+    yn = to_np(y)
+    ref, den = c.ref_wgrad(yn)
+    check(to_np(dw), ref, den, dtype, f"tc wgrad {shape} B={B} {dtype}")
+    assert binding.conv_device_status(reset=True) == 0
