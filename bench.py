@@ -72,6 +72,11 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--batch", type=int, default=1024)
+    ap.add_argument("--layer", choices=tuple(LAYERS), default="layer1",
+                    help="workload of the timed step (default: layer 1, the headline)")
+    ap.add_argument("--dtype", choices=("f32", "bf16"), default="f32")
+    ap.add_argument("--no-graphs", action="store_true",
+                    help="launch each operation eagerly instead of replaying a captured CUDA graph")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the other-config table, e2e and CPU baseline")
     return ap.parse_args()
@@ -257,6 +262,32 @@ class Workload:
         self.launches = sum(binding.conv_query(op, self.desc)["launches"] for op in range(3))
         self.plans = {name: binding.conv_query(op, self.desc) for op, name in enumerate(OPS)}
 
+    def capture(self):
+        """One CUDA graph per operation (captured after a warm-up call), so that
+        replays carry no host launch overhead into the timed region."""
+        import torch
+        self.graphs = {}
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for o in OPS:
+                self.op(o)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        for o in OPS:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self.op(o)
+            self.graphs[o] = g
+        torch.cuda.synchronize()
+
+    def run(self, name):
+        g = getattr(self, "graphs", None)
+        if g:
+            g[name].replay()
+        else:
+            self.op(name)
+
     def op(self, name, stream=None):
         from implicit_gemm_conv2d_gb300 import binding
         relu_y = self.y if self.shape["relu"] else None
@@ -275,7 +306,7 @@ def time_step(wl, flush_buf, steps, warmup, flush=True):
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
         for o in OPS:
-            wl.op(o)
+            wl.run(o)
     torch.cuda.synchronize()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
     for i in range(steps):
@@ -283,11 +314,11 @@ def time_step(wl, flush_buf, steps, warmup, flush=True):
             binding.conv_l2_flush(flush_buf)
         e = ev[i]
         e[0].record(stream)
-        wl.op("fwd")
+        wl.run("fwd")
         e[1].record(stream)
-        wl.op("dgrad")
+        wl.run("dgrad")
         e[2].record(stream)
-        wl.op("wgrad")
+        wl.run("wgrad")
         e[3].record(stream)
     torch.cuda.synchronize()
     per = {o: [] for o in OPS}
@@ -305,11 +336,11 @@ def warm_us(wl, iters=200, warmup=50):
     out = {}
     for o in OPS:
         for _ in range(warmup):
-            wl.op(o)
+            wl.run(o)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         for _ in range(iters):
-            wl.op(o)
+            wl.run(o)
         b.record()
         torch.cuda.synchronize()
         out[o] = a.elapsed_time(b) / iters * 1e3
@@ -362,6 +393,41 @@ def load_peaks():
         "fallback"
 
 
+def pipe_peak(algo, dtype, sms, sm_mhz, peaks):
+    """Peak of the pipe an algorithm family runs on, in TFLOP/s of the layer's own
+    (algorithmic) FLOPs, and a description of where it comes from."""
+    if algo == "tc" and dtype == "bf16":
+        return peaks["bf16_tflops"], f"measured dense bf16 tensor peak ({peaks['bf16_tflops']:.0f} TF/s, burst)"
+    if algo == "tc":
+        tf32 = peaks["bf16_tflops"] * (1.1 / 2.25)
+        return tf32 / 3.0, (f"measured bf16 peak x nominal tf32/bf16 ratio (1.1/2.25) = {tf32:.0f} TF/s, "
+                            "/3 for the three tf32 MMAs per fp32 product (3xTF32)")
+    return sms * 128 * 2 * sm_mhz * 1e6 / 1e12, f"{sms} SMs x 128 FP32 lanes x 2 FLOP x {sm_mhz:.0f} MHz (FFMA)"
+
+
+def roofline_of(wl, op, t_ms, sms, sm_mhz, peaks):
+    plan = wl.plans[op]
+    esz = 4 if wl.dtype == "f32" else 2
+    ab = alg_bytes(op, B=wl.B, esize=esz, **wl.shape)
+    pk, src = pipe_peak(plan["algo_name"], wl.dtype, sms, sm_mhz, peaks)
+    t_flop = wl.flops / (pk * 1e12)
+    t_mem = ab / (peaks["hbm_gbs"] * 1e9)
+    t = t_ms * 1e-3
+    if t_flop >= t_mem:
+        bound = "alu" if plan["algo_name"] != "tc" else "tensor"
+        r = {"bound": bound, "achieved": wl.flops / t / 1e12, "peak": pk, "unit": "TFLOP/s"}
+        src_s = src
+    else:
+        r = {"bound": "hbm", "achieved": ab / t / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+        src_s = f"measured HBM copy bandwidth ({peaks['hbm_gbs']:.0f} GB/s)"
+    r["frac"] = r["achieved"] / r["peak"]
+    r["roofline_us"] = max(t_flop, t_mem) * 1e6
+    r["algorithmic_bytes"] = ab
+    r["flops"] = wl.flops
+    r["peak_source"] = src_s
+    return r
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -381,12 +447,14 @@ def run_ours(args):
     peaks, peaks_kind = load_peaks()
 
     flush_buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
-    wl = Workload("layer1", "f32", args.batch, device)
+    wl = Workload(args.layer, args.dtype, args.batch, device)
+    if not args.no_graphs:
+        wl.capture()
 
     # ---- the timed region ----
     for _ in range(args.warmup):
         for o in OPS:
-            wl.op(o)
+            wl.run(o)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -413,65 +481,66 @@ def run_ours(args):
     # ---- per-op summary and roofline of the dominant kernel ----
     op_ms = {o: statistics.mean(per[o]) for o in OPS}
     clocks = clk.summary()
-    sm_max = clocks["sm_max_mhz"] or peaks.get("sm_max_mhz", 2070.0)
-    ffma_peak = sms * 128 * 2 * sm_max * 1e6 / 1e12  # TFLOP/s: SMs x 128 FP32 lanes x FMA x clock
+    sm_mhz = clocks["sm_max_mhz"] or peaks.get("sm_max_mhz", 2070.0)
     dom = max(OPS, key=lambda o: op_ms[o])
     plan = wl.plans[dom]
-    achieved = wl.flops / (op_ms[dom] * 1e-3) / 1e12
-    kernel_key = f"{dom}:layer1:f32:B{args.batch}"
-    roofline = {"bound": "alu", "achieved": achieved, "peak": ffma_peak, "unit": "TFLOP/s",
-                "frac": achieved / ffma_peak, "traffic": read_traffic(kernel_key),
-                "kernel": f"{dom} ({plan['algo_name']}, {plan['launches']} launch(es))",
-                "peak_source": f"{sms} SMs x 128 FP32 lanes x 2 FLOP x {sm_max:.0f} MHz (FFMA pipe)"}
+    roofline = roofline_of(wl, dom, op_ms[dom], sms, sm_mhz, peaks)
+    roofline["kernel"] = f"{dom} ({plan['algo_name']}, {plan['launches']} launch(es))"
+    roofline["traffic"] = read_traffic(f"{dom}:{args.layer}:{args.dtype}:B{args.batch}")
     ops = {}
-    hbm = peaks["hbm_gbs"]
     for o in OPS:
-        ab = alg_bytes(o, B=args.batch, esize=4, **wl.shape)
+        r = roofline_of(wl, o, op_ms[o], sms, sm_mhz, peaks)
         ops[o] = {"us": op_ms[o] * 1e3, "gflops": wl.flops / (op_ms[o] * 1e-3) / 1e9,
                   "algo": wl.plans[o]["algo_name"], "launches": wl.plans[o]["launches"],
-                  "frac_alu": wl.flops / (op_ms[o] * 1e-3) / 1e12 / ffma_peak,
-                  "hbm_gbs": ab / (op_ms[o] * 1e-3) / 1e9}
-    pr_fwd, pr_bwd = PR522_US[("layer1", "f32")]
-    pr_gflops = 3 * wl.flops / ((pr_fwd + pr_bwd) * 1e-6) / 1e9 if args.batch == 1024 else None
+                  "bound": r["bound"], "frac": r["frac"], "roofline_us": r["roofline_us"]}
+    pr = PR522_US.get((args.layer, args.dtype))
+    pr_gflops = 3 * wl.flops / ((pr[0] + pr[1]) * 1e-6) / 1e9 if (pr and args.batch == 1024) else None
+    shp = LAYERS[args.layer]
+    OH, OW = (shp["H"] - shp["K"]) // shp["S"] + 1, (shp["W"] - shp["K"]) // shp["S"] + 1
 
     line = {
         "metric": METRIC, "value": value, "unit": "GFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": (value / world / pr_gflops) if pr_gflops else None,
-        "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"layer-1 conv fp32 fwd+dgrad+wgrad, fused ReLU, B={args.batch} IC=59 OC=128 "
-                               "11x15 K=5 S=3 -> 3x4 (PufferLib PR #522 encoder conv1)",
+        "dtype": args.dtype, "data": "synthetic",
+        "config": {"workload": (f"{args.layer} conv {args.dtype} fwd+dgrad+wgrad"
+                                f"{', fused ReLU' if shp['relu'] else ''}, B={args.batch} IC={shp['IC']} "
+                                f"OC={shp['OC']} {shp['H']}x{shp['W']} K={shp['K']} S={shp['S']} -> {OH}x{OW} "
+                                "(PufferLib PR #522 encoder conv" + ("1)" if args.layer == "layer1" else "2)")),
                    "l2": "flushed (512 MiB write) between timed steps, outside the timed region",
+                   "launch": "each operation replayed from a captured CUDA graph" if not args.no_graphs
+                   else "eager launches",
                    "inputs": "x~N(0,1), w~U(+-1/sqrt(IC*K*K)), dy~N(0,1), SplitMix64 seed 0x5EED2026"},
         "ops": ops,
         "roofline": roofline,
         "gpu_launches": wl.launches * args.steps,
         "clocks": clocks,
-        "peaks": {"source": peaks_kind, "hbm_gbs": hbm, "bf16_tflops": peaks.get("bf16_tflops")},
+        "peaks": {"source": peaks_kind, "hbm_gbs": peaks["hbm_gbs"], "bf16_tflops": peaks.get("bf16_tflops")},
     }
     if not args.no_extras:
         line["e2e"] = e2e(wl, flush_buf, min(args.steps, 50))
         others = {}
         for layer in ("layer1", "layer2"):
             for dt in ("f32", "bf16"):
-                w2 = wl if (layer, dt) == ("layer1", "f32") else Workload(layer, dt, args.batch, device)
+                w2 = wl if (layer, dt) == (args.layer, args.dtype) else Workload(layer, dt, args.batch, device)
+                if not args.no_graphs and not getattr(w2, "graphs", None):
+                    w2.capture()
                 p2, _ = time_step(w2, flush_buf, 50, 5)
                 warm = warm_us(w2)
-                esz = 4 if dt == "f32" else 2
                 entry = {}
                 for o in OPS:
                     t_ms = statistics.mean(p2[o])
+                    r = roofline_of(w2, o, t_ms, sms, sm_mhz, peaks)
                     entry[o] = {"us_cold_l2": t_ms * 1e3, "us_warm": warm[o],
-                                "gflops": w2.flops / (t_ms * 1e-3) / 1e9,
-                                "hbm_gbs": alg_bytes(o, B=args.batch, esize=esz, **w2.shape) / (t_ms * 1e-3) / 1e9,
-                                "algo": w2.plans[o]["algo_name"]}
+                                "gflops": w2.flops / (t_ms * 1e-3) / 1e9, "algo": w2.plans[o]["algo_name"],
+                                "bound": r["bound"], "frac": r["frac"], "roofline_us": r["roofline_us"]}
                 if args.batch == 1024:
                     f, b = PR522_US[(layer, dt)]
                     entry["pr522_us"] = {"fwd": f, "bwd": b}
                 others[f"{layer}_{dt}"] = entry
         line["configs_b%d" % args.batch] = others
         if world == 1:
-            line["cpu_baseline"] = cpu_baseline(LAYERS["layer1"], 128, 10.0)
+            line["cpu_baseline"] = cpu_baseline(LAYERS[args.layer], 128, 10.0)
     print(json.dumps(line))
     if world > 1:
         dist.barrier()

@@ -109,9 +109,11 @@ int choose_fwd(const ConvParams& p, int dt, const DevInfo& d, Plan& pl)
 int choose_dgrad(const ConvParams& p, int dt, const DevInfo& d, Plan& pl)
 {
     const int force = g_force[CONV_OP_BWD_DATA].load();
-    (void)dt;
     if (force == ALGO_DIRECT) { pl = plan_dgrad_direct(p, d); return CONV_OK; }
-    if (force == ALGO_TC) return CONV_ERR_UNSUPPORTED;
+    if (force == ALGO_TC || (force == ALGO_AUTO && dt == DT_BF16)) {
+        if (tc_dgrad_ok(p, dt, d)) { pl = plan_dgrad_tc(p, dt, d); return CONV_OK; }
+        if (force == ALGO_TC) return CONV_ERR_UNSUPPORTED;
+    }
     if (ffma_dgrad_ok(p, d)) { pl = plan_dgrad_ffma(p, d); return CONV_OK; }
     if (force == ALGO_FFMA) return CONV_ERR_UNSUPPORTED;
     pl = plan_dgrad_direct(p, d);
@@ -235,6 +237,7 @@ int conv_bwd_data(const conv_desc_t* desc, const void* dy, const void* w, const 
     if ((rc = choose_dgrad(p, desc->dtype, d, pl)) != CONV_OK) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (pl.algo == ALGO_DIRECT) return cuda_status(run_dgrad_direct(pl, p, desc->dtype, dy, w, y, dx, s));
+    if (pl.algo == ALGO_TC) return cuda_status(run_dgrad_tc(pl, p, desc->dtype, dy, w, y, dx, d.sms, s));
     return cuda_status(run_dgrad_ffma(pl, p, desc->dtype, dy, w, y, dx, s));
 }
 

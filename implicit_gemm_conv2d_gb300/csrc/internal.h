@@ -89,6 +89,10 @@ bool tc_wgrad_ok(const ConvParams& p, int dt, const DevInfo& d);
 Plan plan_wgrad_tc(const ConvParams& p, int dt, const DevInfo& d);
 cudaError_t run_wgrad_tc(const Plan&, const ConvParams&, int dt, const void* x, const void* dy,
                          const void* y, void* dw, void* ws, int sms, cudaStream_t s);
+bool tc_dgrad_ok(const ConvParams& p, int dt, const DevInfo& d);
+Plan plan_dgrad_tc(const ConvParams& p, int dt, const DevInfo& d);
+cudaError_t run_dgrad_tc(const Plan&, const ConvParams&, int dt, const void* dy, const void* w,
+                         const void* y, void* dx, int sms, cudaStream_t s);
 // Error bits the tensor-core kernels set when a bounded wait runs out.
 cudaError_t tc_read_status(unsigned* out, bool reset);
 

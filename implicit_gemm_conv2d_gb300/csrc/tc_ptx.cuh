@@ -45,6 +45,55 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
     return false;
 }
 
+// Same, but gives up early once *abort (set by another thread that already failed)
+// is nonzero.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, const volatile int* abort)
+{
+    for (uint32_t i = 0; i < (1u << 24); ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255) == 255 && *abort) return false;
+        if (i > 64) __nanosleep(64);
+    }
+    return false;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// Arrive once and add `tx` bytes to the barrier's expected transaction count.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t tx)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(tx) : "memory");
+}
+
+// ---- bulk asynchronous copy (TMA engine, no tensor map) ---------------------------------
+// Copy `bytes` (multiple of 16) from global `src` (16-byte aligned) to shared `dst`
+// (16-byte aligned); completion is signalled as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// ---- per-thread asynchronous copies (LSU path) ---------------------------------------------
+// 16-byte global -> shared copy that bypasses L1; bytes [src_bytes, 16) of the
+// destination are zero-filled (src_bytes in [0, 16]), so nothing past a tensor's
+// end is read.  Both addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+// Arrive on `bar` once every cp.async this thread issued so far has landed; counts
+// as one of the barrier's expected arrivals.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // ---- proxies and tcgen05 ordering --------------------------------------------------------
 // Generic-proxy shared-memory writes made visible to the async proxy (the MMA unit).
 __device__ __forceinline__ void fence_proxy_async_smem()

@@ -195,3 +195,26 @@ def test_tc_wgrad(shape, B, dtype):
     ref, den = c.ref_wgrad(yn)
     check(to_np(dw), ref, den, dtype, f"tc wgrad {shape} B={B} {dtype}")
     assert binding.conv_device_status(reset=True) == 0
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("B", [3, 200, 1024])
+@pytest.mark.parametrize("shape", list(SHAPES))
+def test_tc_dgrad(shape, B, dtype):
+    """tcgen05 d_input (resident W^T chunk, TMEM accumulator, shared-memory col2im)."""
+    if B == 1024 and shape not in ("L1", "L2"):
+        pytest.skip("full batch only for the encoder layers")
+    c = Case(B, **SHAPES[shape], dtype=dtype)
+    binding.conv_set_algo(binding.OP_BWD_DATA, binding.ALGO_TC)
+    try:
+        q = binding.conv_query(binding.OP_BWD_DATA, c.desc)
+    except binding.ConvError:
+        pytest.skip("shape outside the tensor-core d_input kernel's limits")
+    assert q["algo"] == binding.ALGO_TC
+    y = c.gpu_fwd()
+    dx = c.gpu_dgrad(y)
+    torch.cuda.synchronize()
+    yn = to_np(y)
+    ref, den = c.ref_dgrad(yn)
+    check(to_np(dx), ref, den, dtype, f"tc dgrad {shape} B={B} {dtype}")
+    assert binding.conv_device_status(reset=True) == 0
