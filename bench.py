@@ -75,6 +75,8 @@ def parse():
     ap.add_argument("--layer", choices=tuple(LAYERS), default="layer1",
                     help="workload of the timed step (default: layer 1, the headline)")
     ap.add_argument("--dtype", choices=("f32", "bf16"), default="f32")
+    ap.add_argument("--algo", choices=("auto", "direct", "ffma", "tc"), default="auto",
+                    help="force one kernel family for all three operations")
     ap.add_argument("--no-graphs", action="store_true",
                     help="launch each operation eagerly instead of replaying a captured CUDA graph")
     ap.add_argument("--no-extras", action="store_true",
@@ -276,7 +278,9 @@ class Workload:
         torch.cuda.synchronize()
         for o in OPS:
             g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
+            # Capture on the stream the warm-up ran on: the library's per-stream
+            # packed-weight buffer already exists there.
+            with torch.cuda.graph(g, stream=s):
                 self.op(o)
             self.graphs[o] = g
         torch.cuda.synchronize()
@@ -442,6 +446,9 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     binding.lib()
+    algo = {"auto": 0, "direct": 1, "ffma": 2, "tc": 3}[args.algo]
+    for op in range(3):
+        binding.conv_set_algo(op, algo)
     props = torch.cuda.get_device_properties(device)
     sms = props.multi_processor_count
     peaks, peaks_kind = load_peaks()
@@ -510,6 +517,7 @@ def run_ours(args):
                    "l2": "flushed (512 MiB write) between timed steps, outside the timed region",
                    "launch": "each operation replayed from a captured CUDA graph" if not args.no_graphs
                    else "eager launches",
+                   "algo": args.algo,
                    "inputs": "x~N(0,1), w~U(+-1/sqrt(IC*K*K)), dy~N(0,1), SplitMix64 seed 0x5EED2026"},
         "ops": ops,
         "roofline": roofline,

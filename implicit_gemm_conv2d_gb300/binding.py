@@ -52,7 +52,7 @@ class PlanInfo(ctypes.Structure):
 EXPORTS = ["conv_fwd", "conv_bwd_data", "conv_bwd_filter_workspace_size", "conv_bwd_filter",
            "conv_status_string", "conv_out_dims", "conv_query", "conv_set_algo",
            "conv_fastdivmod_check", "conv_l2_flush", "conv_version", "conv_bwd_filter_noalloc",
-           "conv_device_status"]
+           "conv_device_status", "conv_release_scratch"]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -88,6 +88,7 @@ def lib():
         L.conv_version.restype = ctypes.c_char_p
         L.conv_bwd_filter_noalloc.argtypes = [dp, vp, vp, vp, vp, vp]
         L.conv_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
+        L.conv_release_scratch.argtypes = []
         _lib = L
         return L
 
@@ -179,6 +180,10 @@ def conv_device_status(reset: bool = False) -> int:
     v = ctypes.c_uint32()
     _check(lib().conv_device_status(ctypes.byref(v), int(reset)), "conv_device_status")
     return v.value
+
+
+def conv_release_scratch() -> None:
+    _check(lib().conv_release_scratch(), "conv_release_scratch")
 
 
 def conv_version() -> str:

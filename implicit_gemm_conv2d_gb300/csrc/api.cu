@@ -85,6 +85,58 @@ int cuda_status(cudaError_t e)
     return CONV_ERR_CUDA;
 }
 
+// Packed-weight scratch, one buffer of kScratchBytes per (device, stream), allocated on
+// the first tensor-core forward / d_input call on that stream.  Work on one stream is
+// ordered, so a buffer is never used by two calls at once.
+namespace {
+struct ScratchEntry {
+    int device;
+    cudaStream_t stream;
+    void* ptr;
+};
+std::mutex g_scratch_mu;
+ScratchEntry g_scratch[256];
+int g_nscratch = 0;
+}  // namespace
+
+void* stream_scratch(int device, cudaStream_t stream)
+{
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    for (int i = 0; i < g_nscratch; ++i)
+        if (g_scratch[i].device == device && g_scratch[i].stream == stream) return g_scratch[i].ptr;
+    if (g_nscratch >= 256) return nullptr;
+    // No allocation inside a stream capture (it would invalidate the capture): the
+    // first call on a stream has to come before capturing on it.
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    void* p = nullptr;
+    if (cudaMalloc(&p, kScratchBytes) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    g_scratch[g_nscratch++] = ScratchEntry{device, stream, p};
+    return p;
+}
+
+int release_scratch()
+{
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    int rc = CONV_OK;
+    for (int i = 0; i < g_nscratch; ++i) {
+        int cur = 0;
+        cudaGetDevice(&cur);
+        cudaSetDevice(g_scratch[i].device);
+        if (cudaDeviceSynchronize() != cudaSuccess || cudaFree(g_scratch[i].ptr) != cudaSuccess) rc = CONV_ERR_CUDA;
+        cudaSetDevice(cur);
+    }
+    g_nscratch = 0;
+    cudaGetLastError();
+    return rc;
+}
+
 }  // namespace igc
 
 namespace {
@@ -96,7 +148,7 @@ int choose_fwd(const ConvParams& p, int dt, const DevInfo& d, Plan& pl)
 {
     const int force = g_force[CONV_OP_FWD].load();
     if (force == ALGO_DIRECT) { pl = plan_fwd_direct(p, d); return CONV_OK; }
-    if (force == ALGO_TC || (force == ALGO_AUTO && dt == DT_BF16)) {
+    if (force == ALGO_TC || force == ALGO_AUTO) {
         if (tc_fwd_ok(p, dt, d)) { pl = plan_fwd_tc(p, dt, d); return CONV_OK; }
         if (force == ALGO_TC) return CONV_ERR_UNSUPPORTED;
     }
@@ -110,7 +162,7 @@ int choose_dgrad(const ConvParams& p, int dt, const DevInfo& d, Plan& pl)
 {
     const int force = g_force[CONV_OP_BWD_DATA].load();
     if (force == ALGO_DIRECT) { pl = plan_dgrad_direct(p, d); return CONV_OK; }
-    if (force == ALGO_TC || (force == ALGO_AUTO && dt == DT_BF16)) {
+    if (force == ALGO_TC || force == ALGO_AUTO) {
         if (tc_dgrad_ok(p, dt, d)) { pl = plan_dgrad_tc(p, dt, d); return CONV_OK; }
         if (force == ALGO_TC) return CONV_ERR_UNSUPPORTED;
     }
@@ -124,7 +176,7 @@ int choose_wgrad(const ConvParams& p, int dt, const DevInfo& d, Plan& pl)
 {
     const int force = g_force[CONV_OP_BWD_FILTER].load();
     if (force == ALGO_DIRECT) { pl = plan_wgrad_direct(p, d); return CONV_OK; }
-    if (force == ALGO_TC || (force == ALGO_AUTO && dt == DT_BF16)) {
+    if (force == ALGO_TC || force == ALGO_AUTO) {
         if (tc_wgrad_ok(p, dt, d)) { pl = plan_wgrad_tc(p, dt, d); return CONV_OK; }
         if (force == ALGO_TC) return CONV_ERR_UNSUPPORTED;
     }
@@ -300,6 +352,8 @@ int conv_device_status(uint32_t* status, int reset)
     *status = v;
     return CONV_OK;
 }
+
+int conv_release_scratch(void) { return release_scratch(); }
 
 int conv_l2_flush(void* buf, size_t bytes, conv_stream_t stream)
 {

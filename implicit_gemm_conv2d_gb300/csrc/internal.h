@@ -35,6 +35,12 @@ int make_params(const conv_desc_t* d, ConvParams& p);  // validation, no CUDA ca
 bool aligned16(const void* p);
 int cuda_status(cudaError_t e);                     // cudaSuccess -> CONV_OK, else CONV_ERR_CUDA
 
+// Library-held scratch for packed weights: one buffer per (device, stream), allocated
+// on first use; nullptr if it cannot be allocated.
+constexpr size_t kScratchBytes = size_t(8) << 20;
+void* stream_scratch(int device, cudaStream_t stream);
+int release_scratch();
+
 // ---- FFMA and direct families (kernels_ffma.cu) ------------------------------------
 bool ffma_fwd_ok(const ConvParams& p, const DevInfo& d);
 bool ffma_dgrad_ok(const ConvParams& p, const DevInfo& d);

@@ -256,71 +256,145 @@ __device__ __forceinline__ unsigned char* align1024(unsigned char* p)
 }
 
 // ======================================================================================
+// Weight packing.  Every call of the tensor-core forward / d_input first rewrites w into
+// the exact shared-memory image of the A operand's K-chunks (128 rows x 128 bytes,
+// 128-byte swizzled, K-major; fp32 as a tf32 hi tile followed by a lo tile), so that the
+// main kernel fetches each chunk with one large bulk copy.
+//   forward: tile (ot, kc) holds A[r][kk] = w[ot*128 + r][kc*KC + kk]
+//   d_input: tile (kt, ch) holds A[r][kk] = w[ch*KC + kk][k0(kt) + r] (W transposed), rows
+//            r < CIC*K*K of input-channel chunk kt
+// ======================================================================================
+template <typename T>
+__global__ void pack_fwd_w_kernel(const ConvParams p, const T* __restrict__ w, unsigned char* __restrict__ out,
+                                  int nchunks, int oc_tiles)
+{
+    using Tr = TcTraits<T>;
+    const int tile_units = TC_M * 8;
+    const size_t total = size_t(oc_tiles) * nchunks * tile_units;
+    const size_t tb = size_t(TC_M) * ROWB * (Tr::split ? 2 : 1);
+    for (size_t u = blockIdx.x * size_t(blockDim.x) + threadIdx.x; u < total; u += size_t(gridDim.x) * blockDim.x) {
+        const int within = int(u % tile_units);
+        const size_t t = u / tile_units;
+        const int kc = int(t % nchunks), ot = int(t / nchunks);
+        const int r = within >> 3, c = within & 7;
+        const int oc = ot * TC_M + r, k = kc * Tr::KC + c * Tr::E;
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < Tr::E; ++i)
+            v[i] = (oc < p.OC && k + i < p.Kred) ? Elem<T>::ldg(w + size_t(oc) * p.Kred + k + i) : 0.f;
+        unsigned char* base = out + t * tb;
+        put_unit<T, 1>(base, base + TC_M * ROWB, r, c, v);
+    }
+}
+
+template <typename T>
+__global__ void pack_dgrad_w_kernel(const ConvParams p, const T* __restrict__ w, unsigned char* __restrict__ out,
+                                    int nkt, int nch, int CIC)
+{
+    using Tr = TcTraits<T>;
+    const int tile_units = TC_M * 8;
+    const size_t total = size_t(nkt) * nch * tile_units;
+    const size_t tb = size_t(TC_M) * ROWB * (Tr::split ? 2 : 1);
+    for (size_t u = blockIdx.x * size_t(blockDim.x) + threadIdx.x; u < total; u += size_t(gridDim.x) * blockDim.x) {
+        const int within = int(u % tile_units);
+        const size_t t = u / tile_units;
+        const int ch = int(t % nch), kt = int(t / nch);
+        const int r = within >> 3, c = within & 7;
+        const int k0 = kt * CIC * p.KK, mrows = min(CIC, p.IC - kt * CIC) * p.KK;
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < Tr::E; ++i) {
+            const int oc = ch * Tr::KC + c * Tr::E + i;
+            v[i] = (r < mrows && oc < p.OC) ? Elem<T>::ldg(w + size_t(oc) * p.Kred + k0 + r) : 0.f;
+        }
+        unsigned char* base = out + t * tb;
+        put_unit<T, 1>(base, base + TC_M * ROWB, r, c, v);
+    }
+}
+
+// ======================================================================================
 // Forward: tile = (128 output channels, NT columns n); K = IC*K*K in chunks of KC.
 // Warp roles (352 threads):
-//   warps 0-1   copy: per chunk, move the raw slabs the chunk needs into a ring of
-//               RAWS shared-memory slots with 16-byte cp.async copies: for each weight
-//               row oc, the segment w[oc, k0 : k0+KC]; for each sample b the tile
-//               touches, the contiguous channels x[b, ic_lo : ic_hi] that k0 .. k0+KC-1
-//               cover.  Sources are rounded down to 16 bytes (the slack is skipped when
-//               read) and the last block of a tensor is zero-filled past its end.
-//               Each copy thread arrives on the slot's barrier when its copies land.
+//   warp 0      x producer: per super-chunk (XG consecutive K-chunks) and per sample the
+//               tile touches, one bulk copy of the contiguous channels x[b, ic_lo : ic_hi]
+//               the super-chunk covers, into one of two raw slots.  Sources are rounded
+//               down to 16 bytes (the slack is skipped when read); bytes of a last
+//               16-byte block that lie past the end of x are copied by plain loads.
+//   warp 1      w producer: per K-chunk, one bulk copy of the packed weight tile (16 KB;
+//               32 KB hi + lo for fp32) straight into the A half of the operand stage.
 //   warp 2      MMA: one thread issues the chunk's tcgen05.mma steps into the TMEM
-//               accumulator and commits to the stage's "empty" barrier, and after a
-//               tile's last chunk to the accumulator barrier.
-//   warps 3-10  formatters: build the A (weights) and B (gathered patches) operand
-//               tiles of the chunk, 128-byte swizzled K-major, from the raw slot into
-//               one of two operand stages; then the tile's epilogue (TMEM -> y).
+//               accumulator, commits to the stage's "empty" barrier and, after a tile's
+//               last chunk, to the accumulator barrier.
+//   warps 3-10  formatters: build the B operand (gathered patches, 128-byte swizzled
+//               K-major) of each chunk from the raw slot; then the tile's epilogue
+//               (TMEM -> ReLU -> y).
 // ======================================================================================
 constexpr int FV_THREADS = 352;
-constexpr int FV_COPY = 64;   // copy threads (warps 0-1)
+constexpr int FV_COPY = 64;   // copy threads of the wgrad kernel (warps 0-1)
 constexpr int FV_MMA_WARP = 2;
 constexpr int FV_FMT0 = 96;   // first formatter thread (warp 3)
 constexpr int FV_OPS = 2;
+constexpr int FV_RAWS = 2;
 
-struct FwdV2Geom {
+constexpr int FV_MAXA = 8;   // max weight-tile slots
+constexpr int FV_MAXB = 4;   // max gathered-operand stages
+
+struct FwdGeom {
     int NT, n_tiles, oc_tiles, tmem_cols;
-    int nchunks;      // round_up(Kred, KC) / KC
-    int raws;         // raw slots in the ring
+    int nchunks;      // K-chunks per tile
+    int xg;           // K-chunks per x super-chunk
+    int na, nbs;      // weight-tile slots, gathered-operand stages
     int nsmax;        // samples a tile can span
     int xs;           // bytes per sample in a raw slot
-    int rw;           // bytes per weight row in a raw slot (KC * esize + 16)
-    int raw_bytes;    // one raw slot: 128 * rw + nsmax * xs (rounded to 128)
-    int op_bytes;     // one operand stage: (128 + NT) * 128 bytes, x2 for split fp32
+    int raw_bytes;    // one raw slot
+    int a_bytes_tile; // one weight tile: 16 KB, 32 KB (hi + lo) for split fp32
+    int b_bytes;      // one gathered-operand stage: NT * 128 bytes, x2 for split fp32
 };
 
-struct FwdV2Bars {
-    uint64_t raw_full[3], raw_empty[3], op_full[FV_OPS], op_empty[FV_OPS], acc_full;
+struct FwdBars {
+    uint64_t raw_full[FV_RAWS], raw_empty[FV_RAWS];
+    uint64_t a_full[FV_MAXA], a_empty[FV_MAXA];
+    uint64_t b_full[FV_MAXB], b_empty[FV_MAXB];
+    uint64_t acc_full;
     uint32_t tslot;
     int abort_flag;
 };
 
 template <typename T>
-inline FwdV2Geom fwd_v2_geom(const ConvParams& p, int NT, int raws)
+inline FwdGeom fwd_geom(const ConvParams& p, int NT, int xg, int na, int nbs)
 {
     using Tr = TcTraits<T>;
     const int es = int(sizeof(T));
-    FwdV2Geom g;
+    FwdGeom g;
     g.NT = NT;
     g.n_tiles = ceil_div(p.N, NT);
     g.oc_tiles = ceil_div(p.OC, TC_M);
     g.tmem_cols = pow2_at_least(NT);
     g.nchunks = round_up(p.Kred, Tr::KC) / Tr::KC;
-    g.raws = raws;
+    g.xg = xg;
     g.nsmax = std::min(p.B, (NT - 1) / p.P + 2);
-    const int chmax = std::min(p.IC, (Tr::KC - 1) / p.KK + 2);
+    const int chmax = std::min(p.IC, (xg * Tr::KC - 1) / p.KK + 2);
     g.xs = round_up(chmax * p.HW * es + 16, 16);
-    g.rw = Tr::KC * es + 16;
-    g.raw_bytes = round_up(TC_M * g.rw + g.nsmax * g.xs, 128);
-    g.op_bytes = (TC_M + NT) * ROWB * (Tr::split ? 2 : 1);
+    g.raw_bytes = round_up(g.nsmax * g.xs, 128);
+    g.na = na;
+    g.nbs = nbs;
+    g.a_bytes_tile = TC_M * ROWB * (Tr::split ? 2 : 1);
+    g.b_bytes = NT * ROWB * (Tr::split ? 2 : 1);
     return g;
 }
 
 template <typename T>
-inline int fwd_v2_smem(const ConvParams& p, const FwdV2Geom& g)
+inline int fwd_smem(const ConvParams& p, const FwdGeom& g)
 {
     const int kred_pad = round_up(p.Kred, TcTraits<T>::KC);
-    return 1024 + FV_OPS * g.op_bytes + g.raws * g.raw_bytes + kred_pad * 4 + int(sizeof(FwdV2Bars)) + 16;
+    return 1024 + g.na * g.a_bytes_tile + g.nbs * g.b_bytes + FV_RAWS * g.raw_bytes + kred_pad * 4 +
+           int(sizeof(FwdBars)) + 16;
+}
+
+template <typename T>
+inline size_t fwd_packed_bytes(const FwdGeom& g)
+{
+    return size_t(g.oc_tiles) * g.nchunks * g.a_bytes_tile;
 }
 
 __device__ __forceinline__ int warp_sum(int v)
@@ -328,17 +402,6 @@ __device__ __forceinline__ int warp_sum(int v)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
-}
-
-// 16 bytes starting at a 2-byte-aligned shared address, as four 32-bit words.
-__device__ __forceinline__ uint4 lds16_unaligned2(const unsigned char* p)
-{
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
-    if ((a & 3) == 0) return make_uint4(w[0], w[1], w[2], w[3]);
-    const uint32_t w0 = w[0], w1 = w[1], w2 = w[2], w3 = w[3], w4 = w[4];
-    return make_uint4(__funnelshift_r(w0, w1, 16), __funnelshift_r(w1, w2, 16), __funnelshift_r(w2, w3, 16),
-                      __funnelshift_r(w3, w4, 16));
 }
 
 template <typename T, int SWZ>
@@ -359,10 +422,21 @@ __device__ __forceinline__ void put_raw_unit(unsigned char* hi, unsigned char* l
     }
 }
 
+// Bulk-copy the global byte range [src, src + bytes) (src 16-byte aligned, bytes a
+// multiple of 16) to shared `dst`, except bytes at or past `end`, which are copied by
+// plain loads from the calling thread (a tensor's last partial 16-byte block).  Returns
+// the bytes that go through the bulk copy, for the barrier's transaction count.
+__device__ __forceinline__ int slab_bytes_bulk(const unsigned char* src, int bytes, const unsigned char* end)
+{
+    const unsigned char* end16 = reinterpret_cast<const unsigned char*>(reinterpret_cast<uintptr_t>(end) & ~uintptr_t(15));
+    if (src + bytes <= end16) return bytes;
+    return end16 > src ? int(end16 - src) : 0;
+}
+
 template <typename T, bool RELU, int SWZ>
 __global__ void __launch_bounds__(FV_THREADS, 1)
-fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict__ w, T* __restrict__ y,
-              const FwdV2Geom geo)
+fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* __restrict__ wpack,
+              T* __restrict__ y, const FwdGeom geo)
 {
     using Tr = TcTraits<T>;
     constexpr int ES = int(sizeof(T));
@@ -370,24 +444,30 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict__
     unsigned char* smem = align1024(smem_raw);
     const int NT = geo.NT;
     const int kred_pad = round_up(p.Kred, Tr::KC);
-    unsigned char* ops = smem;
-    unsigned char* raw = ops + FV_OPS * geo.op_bytes;
-    int* offk = reinterpret_cast<int*>(raw + geo.raws * geo.raw_bytes);
-    FwdV2Bars* bars = reinterpret_cast<FwdV2Bars*>(offk + kred_pad);
+    // Layout: weight-tile slots (hi 16 KB [+ lo 16 KB]) | gathered stages (hi [+ lo]) | raw x slots
+    unsigned char* aring = smem;
+    unsigned char* bring = aring + geo.na * geo.a_bytes_tile;
+    unsigned char* raw = bring + geo.nbs * geo.b_bytes;
+    int* offk = reinterpret_cast<int*>(raw + FV_RAWS * geo.raw_bytes);
+    FwdBars* bars = reinterpret_cast<FwdBars*>(offk + kred_pad);
     volatile int* abort_flag = &bars->abort_flag;
-    const uint32_t a_bytes = TC_M * ROWB;
-    const uint32_t half = (TC_M + NT) * ROWB;
+    const uint32_t a_bytes = TC_M * ROWB;          // one hi (or lo) weight tile
+    const uint32_t b_half = NT * ROWB;             // one hi (or lo) gathered tile
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     for (int k = tid; k < kred_pad; k += FV_THREADS) offk[k] = (k < p.Kred) ? k_offset(p, k) : -1;
     if (tid == 0) {
-        for (int i = 0; i < geo.raws; ++i) {
-            mbar_init(smem_u32(&bars->raw_full[i]), FV_COPY);
+        for (int i = 0; i < FV_RAWS; ++i) {
+            mbar_init(smem_u32(&bars->raw_full[i]), 1);
             mbar_init(smem_u32(&bars->raw_empty[i]), 8);
         }
-        for (int i = 0; i < FV_OPS; ++i) {
-            mbar_init(smem_u32(&bars->op_full[i]), 8);
-            mbar_init(smem_u32(&bars->op_empty[i]), 1);
+        for (int i = 0; i < geo.na; ++i) {
+            mbar_init(smem_u32(&bars->a_full[i]), 1);
+            mbar_init(smem_u32(&bars->a_empty[i]), 1);
+        }
+        for (int i = 0; i < geo.nbs; ++i) {
+            mbar_init(smem_u32(&bars->b_full[i]), 8);
+            mbar_init(smem_u32(&bars->b_empty[i]), 1);
         }
         mbar_init(smem_u32(&bars->acc_full), 1);
         fence_mbar_init();
@@ -399,87 +479,102 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict__
     tc_fence_after();
     const uint32_t tmem = bars->tslot;
     const int total_tiles = geo.n_tiles * geo.oc_tiles;
+    const int nsuper = (geo.nchunks + geo.xg - 1) / geo.xg;
 
-    if (warp < 2) {
-        // ---------------- copy producers ----------------
-        // Thread t copies weight rows t and t + 64 (up to rw/16 blocks each) and blocks
-        // t, t + 64, ... of every sample's channel range.  Per-tile state is hoisted.
-        const unsigned char* wb = reinterpret_cast<const unsigned char*>(w);
+    if (warp == 0) {
+        // ---------------- x producer ----------------
         const unsigned char* xb = reinterpret_cast<const unsigned char*>(x);
-        const unsigned char* w_end = wb + size_t(p.OC) * p.Kred * ES;
         const unsigned char* x_end = xb + size_t(p.B) * p.IHW * ES;
-        uint32_t q = 0;
+        uint32_t xq = 0;
         for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
-            const int n0 = (tile % geo.n_tiles) * NT, oc0 = (tile / geo.n_tiles) * TC_M;
+            const int n0 = (tile % geo.n_tiles) * NT;
             const int n_end = min(n0 + NT, p.N);
             const int b_first = n0 / p.P, nsamp = (n_end - 1) / p.P - b_first + 1;
-            const int rows = min(TC_M, p.OC - oc0);
-            const unsigned char* wrow0 = wb + (size_t(oc0) + tid) * p.Kred * ES;        // row tid
-            const unsigned char* wrow1 = wb + (size_t(oc0) + tid + 64) * p.Kred * ES;   // row tid + 64
-            const bool has0 = tid < rows, has1 = tid + 64 < rows;
-            for (int kc = 0; kc < geo.nchunks; ++kc, ++q) {
-                const int s = q % geo.raws;
-                const uint32_t use = q / geo.raws;
+            for (int sc = 0; sc < nsuper; ++sc, ++xq) {
+                const int s = xq % FV_RAWS;
+                const uint32_t use = xq / FV_RAWS;
                 if (use >= 1 && !mbar_wait_or_abort(smem_u32(&bars->raw_empty[s]), (use - 1) & 1, abort_flag)) {
                     report(const_cast<int*>(abort_flag), 4u);
                     break;
                 }
-                const int k0 = kc * Tr::KC;
-                const int ic_lo = k0 / p.KK, ic_hi = min(p.IC - 1, (k0 + Tr::KC - 1) / p.KK);
-                const int need_w = min(Tr::KC, p.Kred - k0) * ES;
-                const uint32_t slot = smem_u32(raw + s * geo.raw_bytes);
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    if (h == 0 ? !has0 : !has1) continue;
-                    const unsigned char* src = (h == 0 ? wrow0 : wrow1) + k0 * ES;
-                    const int d = int(reinterpret_cast<uintptr_t>(src) & 15);
-                    src -= d;
-                    const int nbk = (d + need_w + 15) >> 4;
-                    const uint32_t dst = slot + (tid + 64 * h) * geo.rw;
-                    for (int blk = 0; blk < nbk; ++blk) {
-                        const long left = long(w_end - src);
-                        cp_async16(dst + blk * 16, src, uint32_t(left < 16 ? left : 16));
-                        src += 16;
-                    }
+                const int sk0 = sc * geo.xg * Tr::KC;
+                const int ic_lo = sk0 / p.KK;
+                const int ic_hi = min(p.IC - 1, (min(sk0 + geo.xg * Tr::KC, p.Kred) - 1) / p.KK);
+                const int need = (ic_hi - ic_lo + 1) * p.HW * ES;
+                unsigned char* slot = raw + s * geo.raw_bytes;
+                // Sample j = lane + 32 i: its source block range and the part that goes by bulk copy.
+                auto piece = [&](int j, const unsigned char*& src, int& bulk) {
+                    const unsigned char* s0 = xb + (size_t(b_first + j) * p.IHW + size_t(ic_lo) * p.HW) * ES;
+                    const int d = int(reinterpret_cast<uintptr_t>(s0) & 15);
+                    src = s0 - d;
+                    const int bytes = round_up(d + need, 16);
+                    bulk = slab_bytes_bulk(src, bytes, x_end);
+                    return bytes;
+                };
+                int tx = 0;
+                for (int j = lane; j < nsamp; j += 32) {
+                    const unsigned char* src;
+                    int bulk;
+                    const int bytes = piece(j, src, bulk);
+                    // Tail past the last 16-byte boundary of x: plain loads.
+                    for (const unsigned char* t = src + bulk; t < src + bytes && t < x_end; ++t)
+                        slot[j * geo.xs + int(t - src)] = *t;
+                    tx += bulk;
                 }
-                const int need_x = (ic_hi - ic_lo + 1) * p.HW * ES;
-                const uint32_t xslot = slot + TC_M * geo.rw;
-                const unsigned char* xs0 = xb + (size_t(b_first) * p.IHW + size_t(ic_lo) * p.HW) * ES;
-                for (int j = 0; j < nsamp; ++j) {
-                    const unsigned char* src = xs0 + size_t(j) * p.IHW * ES;
-                    const int d = int(reinterpret_cast<uintptr_t>(src) & 15);
-                    src -= d;
-                    const int nbk = (d + need_x + 15) >> 4;
-                    const uint32_t dst = xslot + j * geo.xs;
-                    for (int blk = tid; blk < nbk; blk += FV_COPY) {
-                        const unsigned char* sb = src + blk * 16;
-                        const long left = long(x_end - sb);
-                        cp_async16(dst + blk * 16, sb, uint32_t(left < 16 ? left : 16));
-                    }
+                tx = warp_sum(tx);
+                if (lane == 0) mbar_arrive_expect_tx(smem_u32(&bars->raw_full[s]), uint32_t(tx));
+                __syncwarp();
+                for (int j = lane; j < nsamp; j += 32) {
+                    const unsigned char* src;
+                    int bulk;
+                    piece(j, src, bulk);
+                    if (bulk > 0)
+                        bulk_g2s(smem_u32(slot + j * geo.xs), src, uint32_t(bulk), smem_u32(&bars->raw_full[s]));
                 }
-                cp_async_arrive_noinc(smem_u32(&bars->raw_full[s]));
             }
         }
+    } else if (warp == 1) {
+        // ---------------- w producer ----------------
+        if (lane == 0) {
+            uint32_t q = 0;
+            for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
+                const int ot = tile / geo.n_tiles;
+                for (int kc = 0; kc < geo.nchunks; ++kc, ++q) {
+                    const int sl = q % geo.na;
+                    const uint32_t use = q / geo.na;
+                    if (use >= 1 && !mbar_wait_or_abort(smem_u32(&bars->a_empty[sl]), (use - 1) & 1, abort_flag)) {
+                        report(const_cast<int*>(abort_flag), 16u);
+                        break;
+                    }
+                    const uint32_t bar = smem_u32(&bars->a_full[sl]);
+                    mbar_arrive_expect_tx(bar, uint32_t(geo.a_bytes_tile));
+                    const unsigned char* src = wpack + (size_t(ot) * geo.nchunks + kc) * geo.a_bytes_tile;
+                    bulk_g2s(smem_u32(aring + sl * geo.a_bytes_tile), src, uint32_t(geo.a_bytes_tile), bar);
+                }
+            }
+        }
+        __syncwarp();
     } else if (warp == FV_MMA_WARP) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             const uint32_t idesc = instr_desc(Tr::fmt, TC_M, NT);
-            const uint32_t ops_u32 = smem_u32(ops);
+            const uint32_t a_u32 = smem_u32(aring), b_u32 = smem_u32(bring);
             uint32_t q = 0;
             for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
                 bool ok = true;
                 for (int kc = 0; kc < geo.nchunks; ++kc, ++q) {
-                    const int st = q % FV_OPS;
-                    const uint32_t use = q / FV_OPS;
-                    if (!mbar_wait_or_abort(smem_u32(&bars->op_full[st]), use & 1, abort_flag)) {
+                    const int sl = q % geo.na, st = q % geo.nbs;
+                    if (!mbar_wait_or_abort(smem_u32(&bars->a_full[sl]), (q / geo.na) & 1, abort_flag) ||
+                        !mbar_wait_or_abort(smem_u32(&bars->b_full[st]), (q / geo.nbs) & 1, abort_flag)) {
                         report(const_cast<int*>(abort_flag), 8u);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t base = ops_u32 + st * geo.op_bytes;
-                    issue_chunk<T, SWZ>(tmem, base, base + a_bytes, half, half, idesc, kc == 0);
-                    mma_commit(smem_u32(&bars->op_empty[st]));
+                    issue_chunk<T, SWZ>(tmem, a_u32 + sl * geo.a_bytes_tile, b_u32 + st * geo.b_bytes, a_bytes,
+                                        b_half, idesc, kc == 0);
+                    mma_commit(smem_u32(&bars->a_empty[sl]));
+                    mma_commit(smem_u32(&bars->b_empty[st]));
                 }
                 if (!ok) break;
                 mma_commit(smem_u32(&bars->acc_full));
@@ -488,106 +583,72 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict__
         __syncwarp();
     } else {
         // ---------------- formatters + epilogue ----------------
-        // Thread ft owns unit column cfix = ft & 7 of rows (ft >> 3) + 32 i: A rows i < 4,
-        // B rows i < NT / 32.  All per-tile addressing is computed once per tile.
+        // Thread ft owns unit column cfix = ft & 7 of B rows (ft >> 3) + 32 i, i < ceil(NT/32).
         const int ft = tid - FV_FMT0;  // 0 .. 255
         const int fw = warp - 3;       // 0 .. 7
         const int cfix = ft & 7;
-        const int rbase = ft >> 3;     // 0 .. 31
-        const int nbu = (NT + 31) >> 5;  // B rows per thread (the last may fall past NT)
-        constexpr int MAXB = 8;        // NT <= 256
-        uint32_t q = 0, t = 0;
+        const int rbase = ft >> 3;
+        const int nbu = (NT + 31) >> 5;
+        constexpr int MAXB = 8;
+        uint32_t q = 0, xq = 0, t = 0;
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++t) {
             const int n0 = (tile % geo.n_tiles) * NT, oc0 = (tile / geo.n_tiles) * TC_M;
             const int b_first = n0 / p.P;
-            // A: raw-slot byte offset of each owned unit (the row's 16-byte slack is the same
-            // for every chunk because a chunk advances the row by 128 bytes), or -1.
-            int aoff[4];
-            uint32_t adst[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int r = rbase + 32 * i;
-                const int oc = oc0 + r;
-                aoff[i] = oc < p.OC ? r * geo.rw + int(((size_t(oc) * p.Kred) * ES) & 15) + cfix * 16 : -1;
-                adst[i] = unit_off<SWZ>(r, cfix);
-            }
-            // B: per owned row (column n): raw-slot byte offset of the sample's slab plus the
-            // column's window origin, and the slab start's misalignment before the chunk.
             int boff[MAXB], bmis[MAXB];
             uint32_t bdst[MAXB];
 #pragma unroll
             for (int i = 0; i < MAXB; ++i) {
-                boff[i] = -1;
+                boff[i] = -1;  // -1: row past NT (not part of the tile); -2: zero row
                 bmis[i] = 0;
                 bdst[i] = 0;
                 if (i < nbu && rbase + 32 * i < NT) {
                     const int r = rbase + 32 * i;
                     const int n = n0 + r;
                     bdst[i] = unit_off<SWZ>(r, cfix);
-                    boff[i] = -2;  // row inside the tile, column past N: zeros
+                    boff[i] = -2;
                     if (n < p.N) {
                         uint32_t bq, pq, oh, ow;
                         p.dm_P.divmod(uint32_t(n), bq, pq);
                         p.dm_OW.divmod(pq, oh, ow);
-                        boff[i] = TC_M * geo.rw + (int(bq) - b_first) * geo.xs +
-                                  (int(oh) * p.S * p.W + int(ow) * p.S) * ES;
+                        boff[i] = (int(bq) - b_first) * geo.xs + (int(oh) * p.S * p.W + int(ow) * p.S) * ES;
                         bmis[i] = int((size_t(bq) * p.IHW * ES) & 15);
                     }
                 }
             }
             bool ok = true;
+            const unsigned char* slot = raw;
+            int ic_lo = 0, cmis = 0;
             for (int kc = 0; kc < geo.nchunks; ++kc, ++q) {
-                const int s = q % geo.raws;
-                const int st = q % FV_OPS;
-                const uint32_t ruse = q / geo.raws, ouse = q / FV_OPS;
-                if (!mbar_wait_or_abort(smem_u32(&bars->raw_full[s]), ruse & 1, abort_flag) ||
-                    (ouse >= 1 && !mbar_wait_or_abort(smem_u32(&bars->op_empty[st]), (ouse - 1) & 1, abort_flag))) {
+                const int st = q % geo.nbs;
+                const uint32_t ouse = q / geo.nbs;
+                if (kc % geo.xg == 0) {
+                    const int s = xq % FV_RAWS;
+                    if (!mbar_wait_or_abort(smem_u32(&bars->raw_full[s]), (xq / FV_RAWS) & 1, abort_flag)) {
+                        report(const_cast<int*>(abort_flag), 1u);
+                        ok = false;
+                        break;
+                    }
+                    slot = raw + s * geo.raw_bytes;
+                    ic_lo = (kc * Tr::KC) / p.KK;
+                    cmis = (ic_lo * p.HW * ES) & 15;
+                }
+                if (ouse >= 1 && !mbar_wait_or_abort(smem_u32(&bars->b_empty[st]), (ouse - 1) & 1, abort_flag)) {
                     report(const_cast<int*>(abort_flag), 1u);
                     ok = false;
                     break;
                 }
                 const int k0 = kc * Tr::KC;
-                const int ic_lo = k0 / p.KK;
-                const unsigned char* slot = raw + s * geo.raw_bytes;
-                unsigned char* op = ops + st * geo.op_bytes;
-                const int kv = p.Kred - (k0 + cfix * Tr::E);  // valid elements in owned A / B units
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    uint4 v = make_uint4(0, 0, 0, 0);
-                    if (aoff[i] >= 0 && kv > 0) {
-                        const unsigned char* src = slot + aoff[i];
-                        if constexpr (ES == 2) {
-                            v = lds16_unaligned2(src);
-                        } else {
-                            const uint32_t* w4 = reinterpret_cast<const uint32_t*>(src);
-                            v = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                        }
-                        if (kv < Tr::E) {
-                            uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                            for (int e = 0; e < Tr::E; ++e) {
-                                if (e >= kv) {
-                                    if constexpr (ES == 2) wv[e >> 1] &= (e & 1) ? 0x0000FFFFu : 0xFFFF0000u;
-                                    else wv[e] = 0u;
-                                }
-                            }
-                            v = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-                        }
-                    }
-                    put_raw_unit<T, SWZ>(op, op + half, adst[i], v);
-                }
-                // This thread's E k offsets, in bytes from the chunk's first channel.
+                unsigned char* op = bring + st * geo.b_bytes;
                 int ko[Tr::E];
 #pragma unroll
                 for (int e = 0; e < Tr::E; ++e) {
                     const int kk = offk[k0 + cfix * Tr::E + e];
                     ko[e] = kk >= 0 ? (kk - ic_lo * p.HW) * ES : -1;
                 }
-                const int cmis = (ic_lo * p.HW * ES) & 15;
 #pragma unroll
                 for (int i = 0; i < MAXB; ++i) {
                     if (i >= nbu) break;
-                    if (boff[i] == -1) continue;  // row past NT: not part of the tile
+                    if (boff[i] == -1) continue;
                     uint32_t wv[4] = {0, 0, 0, 0};
                     if (boff[i] >= 0) {
                         const unsigned char* src = slot + boff[i] + ((bmis[i] + cmis) & 15);
@@ -603,15 +664,16 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict__
                             }
                         }
                     }
-                    put_raw_unit<T, SWZ>(op + a_bytes, op + half + a_bytes, bdst[i],
-                                         make_uint4(wv[0], wv[1], wv[2], wv[3]));
+                    put_raw_unit<T, SWZ>(op, op + b_half, bdst[i], make_uint4(wv[0], wv[1], wv[2], wv[3]));
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(smem_u32(&bars->op_full[st]));
-                    mbar_arrive(smem_u32(&bars->raw_empty[s]));
+                    mbar_arrive(smem_u32(&bars->b_full[st]));
+                    if (kc % geo.xg == geo.xg - 1 || kc == geo.nchunks - 1)
+                        mbar_arrive(smem_u32(&bars->raw_empty[xq % FV_RAWS]));
                 }
+                if (kc % geo.xg == geo.xg - 1 || kc == geo.nchunks - 1) ++xq;
             }
             if (!ok) break;
             // Epilogue: TMEM -> y.
@@ -1164,28 +1226,31 @@ int tc_swizzle_mode()
 
 }  // namespace
 
-// Tile width NT and raw-ring depth for the forward kernel: the feasible (shared memory)
-// choice minimising (rounds of tiles over the grid) x (NT + 128), where 128 stands for
-// the per-tile cost of the 128 weight rows next to the NT gathered rows; a 3-slot ring
-// is preferred over 2 at equal cost.
+// Tile width NT and x super-chunk length for the forward kernel: the feasible choice
+// (shared memory, packed weights within the scratch buffer) minimising (rounds of tiles
+// over the grid) x (NT + 64), where 64 stands for the per-tile cost of streaming the
+// packed weights next to the NT gathered columns.
 template <typename T>
-static bool pick_fwd_v2(const ConvParams& p, const DevInfo& d, FwdV2Geom& out)
+static bool pick_fwd(const ConvParams& p, const DevInfo& d, FwdGeom& out)
 {
     bool found = false;
     long best = 0;
     const int oct = ceil_div(p.OC, TC_M);
+    // Per NT: the deepest weight ring (then gathered stages, then super-chunk) that fits.
+    static const int cfgs[][3] = {{6, 3, 4}, {6, 2, 4}, {4, 3, 4}, {4, 2, 4}, {4, 2, 2}, {3, 2, 2},
+                                  {3, 2, 1}, {2, 2, 1}};
     for (int nt = 16; nt <= 256; nt += 16) {
-        for (int raws = 3; raws >= 2; --raws) {
-            const FwdV2Geom g = fwd_v2_geom<T>(p, nt, raws);
-            if (fwd_v2_smem<T>(p, g) > d.smem_optin) continue;
+        for (const auto& c : cfgs) {
+            const FwdGeom g = fwd_geom<T>(p, nt, c[2], c[0], c[1]);
+            if (fwd_smem<T>(p, g) > d.smem_optin || fwd_packed_bytes<T>(g) > kScratchBytes) continue;
             const long tiles = long(ceil_div(p.N, nt)) * oct;
-            const long cost = ((tiles + d.sms - 1) / d.sms) * (nt + 128) * (raws == 3 ? 20 : 21);
+            const long cost = ((tiles + d.sms - 1) / d.sms) * (nt + 64) * (16 - c[0]);
             if (!found || cost < best) {
                 best = cost;
                 out = g;
                 found = true;
             }
-            break;  // the deepest feasible ring for this NT
+            break;
         }
     }
     return found;
@@ -1194,22 +1259,22 @@ static bool pick_fwd_v2(const ConvParams& p, const DevInfo& d, FwdV2Geom& out)
 bool tc_fwd_ok(const ConvParams& p, int dt, const DevInfo& d)
 {
     if (d.cc_major != 10 || p.N <= 0) return false;
-    FwdV2Geom g;
-    return dt == DT_BF16 ? pick_fwd_v2<__nv_bfloat16>(p, d, g) : pick_fwd_v2<float>(p, d, g);
+    FwdGeom g;
+    return dt == DT_BF16 ? pick_fwd<__nv_bfloat16>(p, d, g) : pick_fwd<float>(p, d, g);
 }
 
 Plan plan_fwd_tc(const ConvParams& p, int dt, const DevInfo& d)
 {
-    FwdV2Geom g;
-    if (dt == DT_BF16) pick_fwd_v2<__nv_bfloat16>(p, d, g);
-    else pick_fwd_v2<float>(p, d, g);
+    FwdGeom g;
+    if (dt == DT_BF16) pick_fwd<__nv_bfloat16>(p, d, g);
+    else pick_fwd<float>(p, d, g);
     Plan pl;
     pl.algo = ALGO_TC;
-    pl.launches = 1;
+    pl.launches = 2;  // weight packing, then the implicit GEMM
     pl.block = FV_THREADS;
-    pl.variant = g.NT * 4 + g.raws;
+    pl.variant = ((g.NT * 8 + g.xg) * 16 + g.na) * 8 + g.nbs;
     pl.grid = std::min(g.n_tiles * g.oc_tiles, d.sms);
-    pl.smem = dt == DT_BF16 ? fwd_v2_smem<__nv_bfloat16>(p, g) : fwd_v2_smem<float>(p, g);
+    pl.smem = dt == DT_BF16 ? fwd_smem<__nv_bfloat16>(p, g) : fwd_smem<float>(p, g);
     return pl;
 }
 
@@ -1217,14 +1282,23 @@ template <typename T>
 static cudaError_t fwd_tc_t(const Plan& pl, const ConvParams& p, const void* x, const void* w, void* y,
                             cudaStream_t s)
 {
-    const FwdV2Geom g = fwd_v2_geom<T>(p, pl.variant / 4, pl.variant % 4);
-    cudaError_t e = cudaSuccess;
+    const int v = pl.variant;
+    const FwdGeom g = fwd_geom<T>(p, (v / 8 / 16) / 8, (v / 8 / 16) % 8, (v / 8) % 16, v % 8);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    unsigned char* wpack = static_cast<unsigned char*>(stream_scratch(dev, s));
+    if (!wpack) return cudaErrorMemoryAllocation;
+    const size_t units = size_t(g.oc_tiles) * g.nchunks * TC_M * 8;
+    const int pgrid = int(std::min<size_t>((units + 255) / 256, 4096));
+    pack_fwd_w_kernel<T><<<pgrid, 256, 0, s>>>(p, (const T*)w, wpack, g.nchunks, g.oc_tiles);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const bool swz = tc_swizzle_mode() != 0;
 #define IG_LAUNCH_FWD_TC(R, Z)                                                                      \
     do {                                                                                            \
         e = ensure_smem<fwd_tc_kernel<T, R, Z>>(pl.smem);                                           \
         if (e == cudaSuccess)                                                                       \
-            fwd_tc_kernel<T, R, Z><<<pl.grid, pl.block, pl.smem, s>>>(p, (const T*)x, (const T*)w, \
+            fwd_tc_kernel<T, R, Z><<<pl.grid, pl.block, pl.smem, s>>>(p, (const T*)x, wpack,       \
                                                                       (T*)y, g);                    \
     } while (0)
     if (p.relu) {

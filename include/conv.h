@@ -25,8 +25,15 @@
  * Conventions shared by every entry point:
  *   - Pointers are DEVICE pointers (cudaMalloc'd or equivalent) on the
  *     current CUDA device, owned by the caller; the library keeps no reference
- *     after the call returns and allocates no device memory.  Base pointers
- *     must be 16-byte aligned.  Outputs must not overlap inputs.
+ *     after the call returns.  Base pointers must be 16-byte aligned.  Outputs
+ *     must not overlap inputs.
+ *   - Scratch: the tensor-core paths of conv_fwd and conv_bwd_data first
+ *     repack w into the tensor cores' tile layout.  They keep one 8 MiB
+ *     device buffer for that per (device, stream), allocated with cudaMalloc
+ *     on the first such call on that stream and held until
+ *     conv_release_scratch() or process exit; make that first call outside
+ *     stream capture.  Calls on one stream are ordered by the stream, calls
+ *     on different streams use different buffers.  Nothing else allocates.
  *   - Calls are asynchronous on `stream` (0 = legacy default stream): they
  *     enqueue kernels and return; they never synchronise.  Each call
  *     overwrites its whole output (it does not accumulate into it).
@@ -178,6 +185,10 @@ uint64_t conv_fastdivmod_check(uint32_t d, uint32_t lo, uint32_t hi);
  * (0 = no timeout since the last reset), and clears it if reset != 0.
  * Synchronises the device. */
 int conv_device_status(uint32_t* status, int reset);
+
+/* Free the per-(device, stream) packed-weight buffers (synchronises each
+ * device that holds one).  Later calls allocate again as needed. */
+int conv_release_scratch(void);
 
 /* Write `bytes` bytes of `buf` (device memory, 16-byte aligned, bytes a
  * multiple of 16) on `stream`, evicting earlier data from L2; benchmarks use

@@ -1,0 +1,83 @@
+"""The two-layer encoder stack of PufferLib PR #522 end to end in bf16: layer 1
+(11x15 -> 3x4, K=5, S=3, ReLU) feeding layer 2 (3x4 -> 1x2, K=3, S=1), full
+forward + backward chain, over a batch sweep B in {256, 1024, 4096, 16384}.
+
+Each GPU call is checked stage by stage against the oracle fed that call's
+actual GPU inputs (the GPU's y1 feeds layer 2, the GPU's dy1 feeds layer 1's
+backward), within the bf16 tolerance.  At the larger batches the oracle runs
+on a sample of the batch (forward / d_input are per-sample) and on a sample of
+output channels (wgrad's dw[oc] depends only on dy[:, oc])."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from implicit_gemm_conv2d_gb300 import binding, synth
+
+from .gpu_cases import TOL, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+L1 = dict(IC=59, OC=128, H=11, W=15, K=5, S=3)
+L2 = dict(IC=128, OC=128, H=3, W=4, K=3, S=1)
+
+
+def _ws(desc):
+    return torch.empty(max(16, binding.conv_bwd_filter_workspace_size(desc)), dtype=torch.uint8, device="cuda")
+
+
+def _check(out, ref, den, what):
+    err = oracle.normalised_error(out, ref, den)
+    assert err <= TOL["bf16"], f"{what}: normalised error {err:.3e}"
+
+
+@pytest.mark.parametrize("B", [256, 1024, 4096, 16384])
+def test_two_layer_chain_bf16(B):
+    dt = torch.bfloat16
+    i1 = synth.conv_inputs(B, L1["IC"], L1["OC"], L1["H"], L1["W"], L1["K"], L1["S"], dtype="bf16",
+                           need=("x", "w"))
+    w2 = synth.conv_inputs(1, L2["IC"], L2["OC"], L2["H"], L2["W"], L2["K"], L2["S"], dtype="bf16",
+                           w_stream=synth.STREAM_W2, need=("w",))["w"]
+    dy2 = synth.conv_inputs(B, L2["IC"], L2["OC"], L2["H"], L2["W"], L2["K"], L2["S"], dtype="bf16",
+                            need=("dy",))["dy"]
+    x1, W1, W2, DY2 = to_dev(i1["x"], "bf16"), to_dev(i1["w"], "bf16"), to_dev(w2, "bf16"), to_dev(dy2, "bf16")
+    d1 = binding.make_desc(B, **L1, relu=1, dtype=dt)
+    d2 = binding.make_desc(B, **L2, relu=0, dtype=dt)
+    y1 = torch.empty((B, 128, 3, 4), dtype=dt, device="cuda")
+    y2 = torch.empty((B, 128, 1, 2), dtype=dt, device="cuda")
+    dw2 = torch.empty_like(W2)
+    dy1 = torch.empty_like(y1)
+    dw1 = torch.empty_like(W1)
+    dx1 = torch.empty_like(x1)
+    binding.conv_fwd(d1, x1, W1, y1)
+    binding.conv_fwd(d2, y1, W2, y2)
+    binding.conv_bwd_filter(d2, y1, DY2, None, dw2, _ws(d2))
+    binding.conv_bwd_data(d2, DY2, W2, None, dy1)
+    binding.conv_bwd_filter(d1, x1, dy1, y1, dw1, _ws(d1))
+    binding.conv_bwd_data(d1, dy1, W1, y1, dx1)
+    torch.cuda.synchronize()
+    assert binding.conv_device_status(reset=True) == 0
+
+    rng = np.random.default_rng(B)
+    samples = np.arange(B) if B <= 1024 else np.sort(rng.choice(B, 256, replace=False))
+    chans = np.arange(128) if B <= 1024 else np.sort(rng.choice(128, 8, replace=False))
+    x1n, y1n, y2n = i1["x"], to_np(y1), to_np(y2)
+    dy1n = to_np(dy1)
+    # layer-1 forward, layer-2 forward (on the GPU's y1)
+    ref, den = oracle.conv_fwd(x1n[samples], i1["w"], 3, True)
+    _check(y1n[samples], ref, den, f"B={B} layer1 fwd")
+    ref, den = oracle.conv_fwd(y1n[samples], w2, 1, False)
+    _check(y2n[samples], ref, den, f"B={B} layer2 fwd")
+    # layer-2 backward
+    ref, den = oracle.conv_bwd_data(dy2[samples], w2, None, 3, 4, 1, False)
+    _check(dy1n[samples], ref, den, f"B={B} layer2 dgrad")
+    ref, den = oracle.conv_bwd_filter(y1n, dy2[:, chans], None, 3, 1, False)
+    _check(to_np(dw2)[chans], ref, den, f"B={B} layer2 wgrad")
+    # layer-1 backward on the GPU's dy1, masked by the GPU's y1
+    ref, den = oracle.conv_bwd_data(dy1n[samples], i1["w"], y1n[samples], 11, 15, 3, True)
+    st = torch.from_numpy(samples).to("cuda")
+    dx1s = to_np(dx1.index_select(0, st))
+    _check(dx1s, ref, den, f"B={B} layer1 dgrad")
+    ref, den = oracle.conv_bwd_filter(x1n, dy1n[:, chans], y1n[:, chans], 5, 3, True)
+    _check(to_np(dw1)[chans], ref, den, f"B={B} layer1 wgrad")
+    assert np.isfinite(dx1s).all()
