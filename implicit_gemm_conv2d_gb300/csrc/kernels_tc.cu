@@ -1051,65 +1051,122 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
 }
 
 // ======================================================================================
-// d_input: tile = (one chunk of CIC input channels -> M = CIC*K*K <= 128 rows k, NS whole
-// samples -> NS*P columns n); the GEMM's K runs over output channels:
-//   D[k, n] = sum_oc W[oc, k] * g[oc, n]
-// Each CTA keeps its channel chunk's W^T tile (all OC) resident in shared memory and
-// streams its range of samples through the stages.  The epilogue stages D in shared
-// memory as [n][k] fp32 (over the idle stage buffers) and gathers
-//   dx[b, ic, h, w] = sum over (oh, kh) with oh*S + kh = h and (ow, kw) with ow*S + kw = w
-//                     of D[(ic, kh, kw), (b, oh, ow)]
-// in a fixed order: no atomics, bit-reproducible.
+// d_input:  D[k, n] = sum_oc W[oc, k] * g[oc, n]  for k in one chunk of CIC input channels
+// (M = CIC*K*K <= 128 rows, chunk kt) and n the NT columns of NS whole samples, then
+//   dx[b, ic, h, w] = sum over (oh, kh) with oh*S + kh = h, (ow, kw) with ow*S + kw = w of D
+// in a fixed order (no atomics).  Warp roles (352 threads):
+//   warp 0      g producer: per sample tile one bulk copy each of the contiguous dy and y
+//               slabs of its NS samples.
+//   warp 1      w producer: packed W^T tiles (kt, oc chunk), one bulk copy each, into a ring.
+//   warp 2      MMA: per channel chunk kt, the oc-chunk MMAs into one of two TMEM
+//               accumulators (alternating), then a commit to that accumulator's barrier.
+//   warps 3-10  formatters: per sample tile, transpose and ReLU-mask the dy slab into the
+//               B operand [n][oc] (128-byte swizzled, all oc chunks; reused by every
+//               channel chunk); per channel chunk, TMEM -> Ds (fp32 [n][k] in shared
+//               memory) and the col2im gather into dx.  While they gather chunk kt the
+//               MMAs of chunk kt+1 run into the other accumulator.
 // ======================================================================================
+constexpr int DG_MAXA = 6;
+
 struct TcDgradGeom {
-    int NS;         // samples per tile
-    int NT;         // columns per tile = round_up(NS * P, 16) <= 128
-    int CIC;        // input channels per chunk
-    int nkt;        // channel chunks
-    int cpk;        // CTAs per channel chunk
-    int nch;        // reduction chunks over OC
-    int rmax;       // max (oh, kh) pairs per input row = ceil(K / S)
-    int tmem_cols;
+    int NS;          // samples per tile
+    int NT;          // columns per tile = round_up(NS * P, 16) <= 128
+    int CIC;         // input channels per chunk
+    int nkt;         // channel chunks
+    int nch;         // K-chunks over OC
+    int rmax;        // max (oh, kh) pairs per input row = ceil(K / S)
+    int acc_cols;    // TMEM columns per accumulator (power of two >= NT)
+    int na;          // weight-tile ring slots
+    int a_tile;      // bytes of one packed weight tile (16 KB, 32 KB for split fp32)
+    int b_chunk;     // bytes of one B chunk (hi part): NT * 128
+    int b_bytes;     // all B chunks, hi (+ lo)
+    int slab_bytes;  // bytes of one raw slab region (dy or y): NS samples + 16 slack, rounded
+    int ntiles;      // ceil(B / NS)
+    int taps;        // max (kh, kw) taps landing on one input pixel
+};
+
+struct DgBars {
+    uint64_t raw_full, raw_empty, b_full, a_full[DG_MAXA], a_empty[DG_MAXA], acc_full[2], acc_empty[2];
+    uint32_t tslot;
+    int abort_flag;
 };
 
 template <typename T>
-inline int tc_dgrad_smem(const ConvParams& p, const TcDgradGeom& g)
+inline TcDgradGeom dgrad_geom_ns(const ConvParams& p, int NS, int na)
 {
     using Tr = TcTraits<T>;
-    const int a = g.nch * TC_M * ROWB * (Tr::split ? 2 : 1);
-    const int stages = TC_STAGES * g.NT * ROWB * (Tr::split ? 2 : 1);
-    const int region = std::max(stages, g.NT * TC_M * 4);
-    return 1024 + a + region + (p.H + p.W) * (1 + g.rmax) * 8 + int(sizeof(TcTail));
+    const int es = int(sizeof(T));
+    TcDgradGeom g;
+    g.NS = NS;
+    g.NT = std::max(16, round_up(NS * p.P, 16));
+    g.CIC = std::max(1, TC_M / p.KK);
+    g.nkt = ceil_div(p.IC, g.CIC);
+    g.nch = ceil_div(p.OC, Tr::KC);
+    g.rmax = (p.K + p.S - 1) / p.S;
+    g.acc_cols = pow2_at_least(g.NT);
+    g.na = na;
+    g.a_tile = TC_M * ROWB * (Tr::split ? 2 : 1);
+    g.b_chunk = g.NT * ROWB;
+    g.b_bytes = g.nch * g.b_chunk * (Tr::split ? 2 : 1);
+    g.slab_bytes = round_up(NS * p.OCP * es + 32, 128);
+    g.ntiles = ceil_div(p.B, NS);
+    auto axis_max = [](int n, int K, int S, int O) {
+        int m = 0;
+        for (int h = 0; h < n; ++h) {
+            int c = 0;
+            for (int o = 0; o < O; ++o) c += (h - o * S >= 0 && h - o * S < K);
+            m = std::max(m, c);
+        }
+        return m;
+    };
+    g.taps = axis_max(p.H, p.K, p.S, p.OH) * axis_max(p.W, p.K, p.S, p.OW);
+    return g;
+}
+
+constexpr int DG_DSTR = TC_M + 1;  // Ds row stride (floats): spreads the gather over banks
+constexpr int DG_TMAX = 4;         // taps per input pixel handled by the fast gather
+constexpr int DG_PROW = 8;         // ints per pixel row of the tap table (32 bytes, int4-aligned)
+
+template <typename T>
+inline int dgrad_smem(const ConvParams& p, const TcDgradGeom& g)
+{
+    return 1024 + g.na * g.a_tile + g.b_bytes + (p.relu ? 2 : 1) * g.slab_bytes + g.NT * DG_DSTR * 4 +
+           (p.H + p.W) * (1 + g.rmax) * 8 + 16 + p.HW * DG_PROW * 4 + int(sizeof(DgBars)) + 16;
+}
+
+template <typename T>
+inline size_t dgrad_packed_bytes(const TcDgradGeom& g)
+{
+    return size_t(g.nkt) * g.nch * g.a_tile;
 }
 
 template <typename T, bool RELU, int SWZ>
-__global__ void __launch_bounds__(TC_THREADS, 1)
-dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const T* __restrict__ w,
+__global__ void __launch_bounds__(FV_THREADS, 1)
+dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const unsigned char* __restrict__ wpack,
                 const T* __restrict__ y, T* __restrict__ dx, const TcDgradGeom geo)
 {
     using Tr = TcTraits<T>;
+    constexpr int ES = int(sizeof(T));
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = align1024(smem_raw);
     const int NT = geo.NT;
-    const uint32_t a_chunk = TC_M * ROWB;
-    const uint32_t a_total = geo.nch * a_chunk;  // hi parts; lo parts follow for fp32
-    unsigned char* Ares = smem;
-    unsigned char* region = smem + a_total * (Tr::split ? 2 : 1);
-    TcPipe pp;
-    pipe_setup<T>(pp, region, NT, 0);
-    const int rbytes = max(int(TC_STAGES * pp.stage_bytes), NT * TC_M * 4);
-    float* Ds = reinterpret_cast<float*>(region);
+    unsigned char* aring = smem;
+    unsigned char* bt = aring + geo.na * geo.a_tile;              // B chunks (hi), then lo
+    unsigned char* rdy = bt + geo.b_bytes;                         // raw dy slab
+    unsigned char* ry = rdy + geo.slab_bytes;                      // raw y slab (ReLU only)
+    float* Ds = reinterpret_cast<float*>(ry + (RELU ? geo.slab_bytes : 0));
     const int R1 = 1 + geo.rmax;
-    int2* rtab = reinterpret_cast<int2*>(region + rbytes);
+    int2* rtab = reinterpret_cast<int2*>(Ds + NT * DG_DSTR);
     int2* ctab = rtab + p.H * R1;
-    TcTail* tail = reinterpret_cast<TcTail*>(ctab + p.W * R1);
+    // Per input pixel hw: its contributing (p, kh*K + kw) as Ds offsets p*DSTR + kh*K + kw,
+    // then the count (only used when every pixel has <= DG_TMAX taps).
+    int* ptab = reinterpret_cast<int*>((reinterpret_cast<uintptr_t>(ctab + p.W * R1) + 15) & ~uintptr_t(15));
+    DgBars* bars = reinterpret_cast<DgBars*>(ptab + p.HW * DG_PROW);
+    volatile int* abort_flag = &bars->abort_flag;
+    const uint32_t b_lo = uint32_t(geo.nch * geo.b_chunk);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int kt = blockIdx.x % geo.nkt, j = blockIdx.x / geo.nkt;
-    const int ic0 = kt * geo.CIC, nic = min(geo.CIC, p.IC - ic0);
-    const int k0 = ic0 * p.KK, mrows = nic * p.KK;
-
-    for (int h = tid; h < p.H; h += TC_THREADS) {
+    for (int h = tid; h < p.H; h += FV_THREADS) {
         int n = 0;
         for (int oh = 0; oh < p.OH; ++oh) {
             const int kh = h - oh * p.S;
@@ -1117,7 +1174,7 @@ dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const T* __restric
         }
         rtab[h * R1] = make_int2(n, 0);
     }
-    for (int c = tid; c < p.W; c += TC_THREADS) {
+    for (int c = tid; c < p.W; c += FV_THREADS) {
         int n = 0;
         for (int ow = 0; ow < p.OW; ++ow) {
             const int kw = c - ow * p.S;
@@ -1125,88 +1182,268 @@ dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const T* __restric
         }
         ctab[c * R1] = make_int2(n, 0);
     }
-    // Resident A: row m = k0 + m of W^T, all output channels, chunk by chunk.
-    for (int kc = 0; kc < geo.nch; ++kc) {
-        for (int u = tid; u < TC_M * 8; u += TC_THREADS) {
-            const int r = u >> 3, c = u & 7;
-            float v[8];
-#pragma unroll
-            for (int i = 0; i < Tr::E; ++i) {
-                const int oc = kc * Tr::KC + c * Tr::E + i;
-                v[i] = (r < mrows && oc < p.OC) ? Elem<T>::ldg(w + size_t(oc) * p.Kred + k0 + r) : 0.f;
-            }
-            put_unit<T, SWZ>(Ares + kc * a_chunk, Ares + a_total + kc * a_chunk, r, c, v);
+    const bool fast_taps = geo.taps <= DG_TMAX;
+    __syncthreads();  // rtab / ctab complete
+    if (fast_taps) {
+        for (int hw = tid; hw < p.HW; hw += FV_THREADS) {
+            const int h = hw / p.W, ww = hw % p.W;
+            const int2* rr = rtab + h * R1;
+            const int2* cc = ctab + ww * R1;
+            int n = 0;
+            for (int a = 1; a <= rr[0].x; ++a)
+                for (int bq = 1; bq <= cc[0].x; ++bq)
+                    ptab[hw * DG_PROW + n++] = (rr[a].x + cc[bq].x) * DG_DSTR + rr[a].y + cc[bq].y;
+            for (int i = n; i < DG_TMAX; ++i) ptab[hw * DG_PROW + i] = -1;
+            ptab[hw * DG_PROW + DG_TMAX] = n;
         }
     }
-    pipe_start(pp, tail, geo.tmem_cols);
+    if (tid == 0) {
+        mbar_init(smem_u32(&bars->raw_full), 1);
+        mbar_init(smem_u32(&bars->raw_empty), 8);
+        mbar_init(smem_u32(&bars->b_full), 8);
+        for (int i = 0; i < geo.na; ++i) {
+            mbar_init(smem_u32(&bars->a_full[i]), 1);
+            mbar_init(smem_u32(&bars->a_empty[i]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&bars->acc_full[i]), 1);
+            mbar_init(smem_u32(&bars->acc_empty[i]), 8);
+        }
+        fence_mbar_init();
+        bars->abort_flag = 0;
+    }
+    if (warp == 0) tmem_alloc(smem_u32(&bars->tslot), 2 * geo.acc_cols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tslot;
 
-    const int b_lo = int((long long)p.B * j / geo.cpk), b_hi = int((long long)p.B * (j + 1) / geo.cpk);
-    const int span = nic * p.HW;
-    for (int sb = b_lo; sb < b_hi; sb += geo.NS) {
-        const int ns = min(geo.NS, b_hi - sb);
-        const int ncols = ns * p.P;
-        auto fill = [&](unsigned char* st, int kc) {
-            for (int u = tid; u < NT * 8; u += TC_THREADS) {
-                const int r = u >> 3, c = u & 7;
-                float v[8];
-                if (r < ncols) {
-                    uint32_t si, pq;
-                    p.dm_P.divmod(uint32_t(r), si, pq);
-                    const size_t base = size_t(sb + int(si)) * p.OCP + pq;
-#pragma unroll
-                    for (int i = 0; i < Tr::E; ++i) {
-                        const int oc = kc * Tr::KC + c * Tr::E + i;
-                        float g = 0.f;
-                        if (oc < p.OC) {
-                            g = Elem<T>::ldg(dy + base + size_t(oc) * p.P);
-                            if (RELU && !(Elem<T>::ldg(y + base + size_t(oc) * p.P) > 0.f)) g = 0.f;
+    if (warp == 0) {
+        // ---------------- g producer ----------------
+        if (lane == 0) {
+            const unsigned char* gb = reinterpret_cast<const unsigned char*>(dy);
+            const unsigned char* yb = reinterpret_cast<const unsigned char*>(y);
+            const size_t tensor_bytes = size_t(p.B) * p.OCP * ES;
+            uint32_t tl = 0;
+            for (int tile = blockIdx.x; tile < geo.ntiles && !*abort_flag; tile += gridDim.x, ++tl) {
+                if (tl >= 1 && !mbar_wait_or_abort(smem_u32(&bars->raw_empty), (tl - 1) & 1, abort_flag)) {
+                    report(const_cast<int*>(abort_flag), 4u);
+                    break;
+                }
+                const int b0 = tile * geo.NS, ns = min(geo.NS, p.B - b0);
+                const size_t off = size_t(b0) * p.OCP * ES;
+                const int d = int(off & 15);
+                const int bytes = round_up(d + ns * p.OCP * ES, 16);
+                int tx = 0;
+                const int nsl = RELU ? 2 : 1;
+                int bulk[2];
+                for (int i = 0; i < nsl; ++i) {
+                    const unsigned char* base = i == 0 ? gb : yb;
+                    unsigned char* dst = i == 0 ? rdy : ry;
+                    const unsigned char* src = base + off - d;
+                    bulk[i] = slab_bytes_bulk(src, bytes, base + tensor_bytes);
+                    for (const unsigned char* t = src + bulk[i]; t < src + bytes && t < base + tensor_bytes; ++t)
+                        dst[int(t - src)] = *t;
+                    tx += bulk[i];
+                }
+                mbar_arrive_expect_tx(smem_u32(&bars->raw_full), uint32_t(tx));
+                for (int i = 0; i < nsl; ++i)
+                    if (bulk[i] > 0)
+                        bulk_g2s(smem_u32(i == 0 ? rdy : ry), (i == 0 ? gb : yb) + off - d, uint32_t(bulk[i]),
+                                 smem_u32(&bars->raw_full));
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------- w producer ----------------
+        if (lane == 0) {
+            uint32_t q = 0;
+            for (int tile = blockIdx.x; tile < geo.ntiles && !*abort_flag; tile += gridDim.x) {
+                bool ok = true;
+                for (int kt = 0; kt < geo.nkt && ok; ++kt) {
+                    for (int ch = 0; ch < geo.nch; ++ch, ++q) {
+                        const int sl = q % geo.na;
+                        const uint32_t use = q / geo.na;
+                        if (use >= 1 && !mbar_wait_or_abort(smem_u32(&bars->a_empty[sl]), (use - 1) & 1, abort_flag)) {
+                            report(const_cast<int*>(abort_flag), 16u);
+                            ok = false;
+                            break;
                         }
-                        v[i] = g;
+                        const uint32_t bar = smem_u32(&bars->a_full[sl]);
+                        mbar_arrive_expect_tx(bar, uint32_t(geo.a_tile));
+                        bulk_g2s(smem_u32(aring + sl * geo.a_tile), wpack + (size_t(kt) * geo.nch + ch) * geo.a_tile,
+                                 uint32_t(geo.a_tile), bar);
+                    }
+                }
+                if (!ok) break;
+            }
+        }
+        __syncwarp();
+    } else if (warp == FV_MMA_WARP) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            const uint32_t idesc = instr_desc(Tr::fmt, TC_M, NT);
+            const uint32_t a_u32 = smem_u32(aring), b_u32 = smem_u32(bt);
+            uint32_t q = 0, j = 0, tl = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < geo.ntiles && ok && !*abort_flag; tile += gridDim.x, ++tl) {
+                if (!mbar_wait_or_abort(smem_u32(&bars->b_full), tl & 1, abort_flag)) {
+                    report(const_cast<int*>(abort_flag), 8u);
+                    break;
+                }
+                for (int kt = 0; kt < geo.nkt && ok; ++kt, ++j) {
+                    const int buf = j & 1;
+                    if ((j >> 1) >= 1 &&
+                        !mbar_wait_or_abort(smem_u32(&bars->acc_empty[buf]), ((j >> 1) - 1) & 1, abort_flag)) {
+                        report(const_cast<int*>(abort_flag), 8u);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t acc = tmem + uint32_t(buf * geo.acc_cols);
+                    for (int ch = 0; ch < geo.nch; ++ch, ++q) {
+                        const int sl = q % geo.na;
+                        if (!mbar_wait_or_abort(smem_u32(&bars->a_full[sl]), (q / geo.na) & 1, abort_flag)) {
+                            report(const_cast<int*>(abort_flag), 8u);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_chunk<T, SWZ>(acc, a_u32 + sl * geo.a_tile, b_u32 + ch * geo.b_chunk, TC_M * ROWB,
+                                            b_lo, idesc, ch == 0);
+                        mma_commit(smem_u32(&bars->a_empty[sl]));
+                    }
+                    if (!ok) break;
+                    mma_commit(smem_u32(&bars->acc_full[buf]));
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------- formatters + epilogue ----------------
+        const int ft = tid - FV_FMT0;  // 0 .. 255
+        const int fw = warp - 3;       // 0 .. 7
+        const int units_per_row = geo.nch * (Tr::KC / Tr::E);  // 16-byte units of oc per column
+        uint32_t j = 0, tl = 0;
+        for (int tile = blockIdx.x; tile < geo.ntiles; tile += gridDim.x, ++tl) {
+            const int b0 = tile * geo.NS, ns = min(geo.NS, p.B - b0), ncols = ns * p.P;
+            if (!mbar_wait_or_abort(smem_u32(&bars->raw_full), tl & 1, abort_flag)) {
+                report(const_cast<int*>(abort_flag), 1u);
+                break;
+            }
+            // B: unit (column n, oc group og) = E consecutive oc of g[., n]; consecutive threads
+            // take consecutive columns, so their dy reads are consecutive positions.
+            const int d = int((size_t(b0) * p.OCP * ES) & 15);
+            const unsigned char* gsl = rdy + d;
+            const unsigned char* ysl = ry + d;
+            for (int u = ft; u < NT * units_per_row; u += 256) {
+                const int n = u % NT, og = u / NT;
+                uint32_t wv[4] = {0, 0, 0, 0};
+                if (n < ncols) {
+                    uint32_t si, pq;
+                    p.dm_P.divmod(uint32_t(n), si, pq);
+                    const int base = int(si) * p.OCP + int(pq);
+#pragma unroll
+                    for (int e = 0; e < Tr::E; ++e) {
+                        const int oc = og * Tr::E + e;
+                        if (oc < p.OC) {
+                            const int gi = base + oc * p.P;
+                            if constexpr (ES == 2) {
+                                uint32_t h = *reinterpret_cast<const unsigned short*>(gsl + gi * 2);
+                                if (RELU && !(__bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(ysl + gi * 2)) > 0.f))
+                                    h = 0;
+                                wv[e >> 1] |= (e & 1) ? (h << 16) : h;
+                            } else {
+                                uint32_t v = *reinterpret_cast<const uint32_t*>(gsl + gi * 4);
+                                if (RELU && !(*reinterpret_cast<const float*>(ysl + gi * 4) > 0.f)) v = 0;
+                                wv[e] = v;
+                            }
+                        }
+                    }
+                }
+                const int ch = (og * Tr::E) / Tr::KC, c = ((og * Tr::E) % Tr::KC) / Tr::E;
+                unsigned char* dst = bt + ch * geo.b_chunk;
+                put_raw_unit<T, SWZ>(dst, dst + b_lo, unit_off<SWZ>(n, c), make_uint4(wv[0], wv[1], wv[2], wv[3]));
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(smem_u32(&bars->b_full));
+                mbar_arrive(smem_u32(&bars->raw_empty));  // the slab is no longer read
+            }
+            bool ok = true;
+            for (int kt = 0; kt < geo.nkt; ++kt, ++j) {
+                const int buf = j & 1;
+                if (!mbar_wait_or_abort(smem_u32(&bars->acc_full[buf]), (j >> 1) & 1, abort_flag)) {
+                    report(const_cast<int*>(abort_flag), 2u);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int qd = warp & 3, hcols = NT >> 1, c0 = (fw >> 2) * hcols;
+                const int m = qd * 32 + lane;
+                for (int cb = 0; cb < hcols; cb += 8) {
+                    uint32_t r[8];
+                    tmem_ld8(tmem + uint32_t(buf * geo.acc_cols) + (uint32_t(qd * 32) << 16) + uint32_t(c0 + cb), r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) Ds[(c0 + cb + e) * DG_DSTR + m] = __uint_as_float(r[e]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty[buf]));
+                asm volatile("bar.sync 1, 256;" ::: "memory");
+                const int ic0 = kt * geo.CIC, nic = min(geo.CIC, p.IC - ic0);
+                if (fast_taps) {
+                    // Thread owns pixel hw; its <= 4 tap offsets stay in registers while it
+                    // walks every (sample, channel) of the chunk.
+                    for (int hw = ft; hw < p.HW; hw += 256) {
+                        const int4 o = *reinterpret_cast<const int4*>(ptab + hw * DG_PROW);
+                        for (int sI = 0; sI < ns; ++sI) {
+                            T* dxs = dx + size_t(b0 + sI) * p.IHW + size_t(ic0) * p.HW + hw;
+                            const float* ds = Ds + sI * p.P * DG_DSTR;
+                            for (int icl = 0; icl < nic; ++icl) {
+                                const float* dk = ds + icl * p.KK;
+                                float sum = 0.f;
+                                if (o.x >= 0) sum += dk[o.x];
+                                if (o.y >= 0) sum += dk[o.y];
+                                if (o.z >= 0) sum += dk[o.z];
+                                if (o.w >= 0) sum += dk[o.w];
+                                Elem<T>::st(dxs + size_t(icl) * p.HW, sum);
+                            }
+                        }
                     }
                 } else {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) v[i] = 0.f;
+                    const int span = nic * p.HW;
+                    for (int sI = 0; sI < ns; ++sI) {
+                        T* dxs = dx + size_t(b0 + sI) * p.IHW + size_t(ic0) * p.HW;
+                        const float* ds = Ds + sI * p.P * DG_DSTR;
+                        for (int t = ft; t < span; t += 256) {
+                            uint32_t icl, hw, h, ww;
+                            p.dm_HW.divmod(uint32_t(t), icl, hw);
+                            p.dm_W.divmod(hw, h, ww);
+                            const int2* rr = rtab + h * R1;
+                            const int2* cc = ctab + ww * R1;
+                            const int nr = rr[0].x, ncc = cc[0].x;
+                            const int kb = int(icl) * p.KK;
+                            float sum = 0.f;
+                            for (int a = 1; a <= nr; ++a)
+                                for (int bq = 1; bq <= ncc; ++bq)
+                                    sum += ds[(rr[a].x + cc[bq].x) * DG_DSTR + kb + rr[a].y + cc[bq].y];
+                            Elem<T>::st(dxs + t, sum);
+                        }
+                    }
                 }
-                put_unit<T, SWZ>(st, st + pp.half, r, c, v);
+                asm volatile("bar.sync 1, 256;" ::: "memory");  // Ds consumed
             }
-        };
-        if (!pipe_tile<T, SWZ>(pp, geo.nch, fill, smem_u32(Ares), a_total)) break;
-        if (!pipe_wait_acc(pp)) break;
-
-        // TMEM (lane = k row, column = n) -> Ds[n][k].
-        const int q = warp & 3, hcols = NT >> 1, c0 = (warp >> 2) * hcols;
-        const int m = q * 32 + lane;
-        for (int cb = 0; cb < hcols; cb += 8) {
-            uint32_t r[8];
-            tmem_ld8(pp.tmem + (uint32_t(q * 32) << 16) + uint32_t(c0 + cb), r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 8; ++e) Ds[(c0 + cb + e) * TC_M + m] = __uint_as_float(r[e]);
+            if (!ok) break;
         }
-        tc_fence_before();
-        __syncthreads();
-
-        for (int s = 0; s < ns; ++s) {
-            T* dxs = dx + size_t(sb + s) * p.IHW + size_t(ic0) * p.HW;
-            const float* ds = Ds + s * p.P * TC_M;
-            for (int t = tid; t < span; t += TC_THREADS) {
-                uint32_t icl, hw, h, ww;
-                p.dm_HW.divmod(uint32_t(t), icl, hw);
-                p.dm_W.divmod(hw, h, ww);
-                const int2* rr = rtab + h * R1;
-                const int2* cc = ctab + ww * R1;
-                const int nr = rr[0].x, ncc = cc[0].x;
-                const int kb = int(icl) * p.KK;
-                float sum = 0.f;
-                for (int a = 1; a <= nr; ++a)
-                    for (int bq = 1; bq <= ncc; ++bq)
-                        sum += ds[(rr[a].x + cc[bq].x) * TC_M + kb + rr[a].y + cc[bq].y];
-                Elem<T>::st(dxs + t, sum);
-            }
-        }
-        __syncthreads();  // Ds (over the stages) consumed before the next tile's fill
     }
-    pipe_finish(pp, geo.tmem_cols);
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 2 * geo.acc_cols);
+    }
 }
 
 template <typename T> constexpr int dt_of_tc();
@@ -1405,56 +1642,68 @@ cudaError_t run_wgrad_tc(const Plan& pl, const ConvParams& p, int dt, const void
 }
 
 // ---- d_input ------------------------------------------------------------------------
-static TcDgradGeom dgrad_geom(const ConvParams& p, int dt, int sms)
+// Samples per tile: about B / SMs (one tile per CTA at small batches), at most 128 / P;
+// then the deepest weight ring that fits in shared memory.
+template <typename T>
+static bool pick_dgrad(const ConvParams& p, const DevInfo& d, TcDgradGeom& out)
 {
-    TcDgradGeom g;
-    g.CIC = std::max(1, TC_M / p.KK);
-    g.nkt = ceil_div(p.IC, g.CIC);
-    g.cpk = std::max(1, std::min(std::max(1, sms / g.nkt), std::max(1, p.B)));
-    g.rmax = (p.K + p.S - 1) / p.S;
-    const int kc = dt == DT_BF16 ? TcTraits<__nv_bfloat16>::KC : TcTraits<float>::KC;
-    g.nch = ceil_div(p.OC, kc);
-    const int spc = std::max(1, ceil_div(p.B, g.cpk));          // samples per CTA
-    const int ns_max = std::max(1, TC_M / std::max(1, p.P));
-    const int tpc = ceil_div(spc, ns_max);                       // tiles per CTA
-    g.NS = ceil_div(spc, tpc);
-    g.NT = std::max(16, round_up(g.NS * p.P, 16));
-    g.tmem_cols = pow2_at_least(g.NT);
-    return g;
+    if (p.B <= 0 || p.KK > TC_M || p.P > TC_M) return false;
+    const int ns_max = std::max(1, TC_M / p.P);
+    for (int ns = std::min(ns_max, ceil_div(p.B, d.sms)); ns >= 1; --ns) {
+        for (int na = 4; na >= 2; --na) {
+            const TcDgradGeom g = dgrad_geom_ns<T>(p, ns, na);
+            if (g.NT > TC_M || 2 * g.acc_cols > 512) continue;
+            if (dgrad_smem<T>(p, g) <= d.smem_optin && dgrad_packed_bytes<T>(g) <= kScratchBytes) {
+                out = g;
+                return true;
+            }
+        }
+    }
+    return false;
 }
 
 bool tc_dgrad_ok(const ConvParams& p, int dt, const DevInfo& d)
 {
-    if (d.cc_major != 10 || p.B <= 0 || p.KK > TC_M || p.P > TC_M) return false;
-    const TcDgradGeom g = dgrad_geom(p, dt, d.sms);
-    if (g.NT > TC_M) return false;
-    return (dt == DT_BF16 ? tc_dgrad_smem<__nv_bfloat16>(p, g) : tc_dgrad_smem<float>(p, g)) <= d.smem_optin;
+    if (d.cc_major != 10) return false;
+    TcDgradGeom g;
+    return dt == DT_BF16 ? pick_dgrad<__nv_bfloat16>(p, d, g) : pick_dgrad<float>(p, d, g);
 }
 
 Plan plan_dgrad_tc(const ConvParams& p, int dt, const DevInfo& d)
 {
-    const TcDgradGeom g = dgrad_geom(p, dt, d.sms);
+    TcDgradGeom g;
+    if (dt == DT_BF16) pick_dgrad<__nv_bfloat16>(p, d, g);
+    else pick_dgrad<float>(p, d, g);
     Plan pl;
     pl.algo = ALGO_TC;
-    pl.launches = 1;
-    pl.block = TC_THREADS;
-    pl.grid = g.nkt * g.cpk;
-    pl.smem = dt == DT_BF16 ? tc_dgrad_smem<__nv_bfloat16>(p, g) : tc_dgrad_smem<float>(p, g);
+    pl.launches = 2;  // weight packing, then the implicit GEMM + col2im
+    pl.block = FV_THREADS;
+    pl.variant = g.NS * 8 + g.na;
+    pl.grid = std::min(g.ntiles, d.sms);
+    pl.smem = dt == DT_BF16 ? dgrad_smem<__nv_bfloat16>(p, g) : dgrad_smem<float>(p, g);
     return pl;
 }
 
 template <typename T>
 static cudaError_t dgrad_tc_t(const Plan& pl, const ConvParams& p, const void* dy, const void* w,
-                              const void* y, void* dx, int sms, cudaStream_t s)
+                              const void* y, void* dx, int, cudaStream_t s)
 {
-    const TcDgradGeom g = dgrad_geom(p, dt_of_tc<T>(), sms);
-    cudaError_t e = cudaSuccess;
+    const TcDgradGeom g = dgrad_geom_ns<T>(p, pl.variant / 8, pl.variant % 8);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    unsigned char* wpack = static_cast<unsigned char*>(stream_scratch(dev, s));
+    if (!wpack) return cudaErrorMemoryAllocation;
+    const size_t units = size_t(g.nkt) * g.nch * TC_M * 8;
+    const int pgrid = int(std::min<size_t>((units + 255) / 256, 4096));
+    pack_dgrad_w_kernel<T><<<pgrid, 256, 0, s>>>(p, (const T*)w, wpack, g.nkt, g.nch, g.CIC);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const bool swz = tc_swizzle_mode() != 0;
 #define IG_LAUNCH_DG_TC(R, Z)                                                                              \
     do {                                                                                                   \
         e = ensure_smem<dgrad_tc_kernel<T, R, Z>>(pl.smem);                                                \
         if (e == cudaSuccess)                                                                              \
-            dgrad_tc_kernel<T, R, Z><<<pl.grid, pl.block, pl.smem, s>>>(p, (const T*)dy, (const T*)w,      \
+            dgrad_tc_kernel<T, R, Z><<<pl.grid, pl.block, pl.smem, s>>>(p, (const T*)dy, wpack,            \
                                                                         (const T*)y, (T*)dx, g);           \
     } while (0)
     if (p.relu) {

@@ -129,7 +129,8 @@ def test_query_reports_plan():
     q = binding.conv_query(binding.OP_BWD_FILTER, c.desc)
     assert q["launches"] == 2 and q["splits"] >= 1 and q["workspace"] > 0
     q = binding.conv_query(binding.OP_FWD, c.desc)
-    assert q["launches"] == 1 and q["grid"] >= 1
+    # one launch, or two when the tensor-core path first packs the weights
+    assert q["launches"] == (2 if q["algo"] == binding.ALGO_TC else 1) and q["grid"] >= 1
 
 
 def test_outputs_fully_overwritten():
