@@ -756,10 +756,13 @@ inline TcWgradGeom wgrad_v3_geom(const ConvParams& p, int NT, int raws, int spli
     g.tmem_cols = pow2_at_least(NT);
     g.nsc = std::max(1, Tr::KC / std::max(1, p.P));
     g.raws = raws;
+    // Raw slot: [dy region][y region (ReLU)][x region]; dy / y hold the chunk's samples
+    // back to back (one copy when one oc-tile spans all of OC, else one per sample with a
+    // 16-byte-rounded stride gs); x holds each sample's k-tile channels at stride xsb.
     g.gs = round_up(std::min(p.OC, TC_M) * p.P * es + 16, 16);
     const int chk = std::min(p.IC, (NT - 1) / p.KK + 2);
     g.xsb = round_up(chk * p.HW * es + 16, 16);
-    g.raw_bytes = round_up(g.nsc * (g.gs * (p.relu ? 2 : 1) + g.xsb), 128);
+    g.raw_bytes = round_up(g.nsc * (g.gs * (p.relu ? 2 : 1) + g.xsb) + 32, 128);
     g.op_bytes = (TC_M + NT) * ROWB * (Tr::split ? 2 : 1);
     return g;
 }
@@ -802,13 +805,14 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
     volatile int* abort_flag = &bars->abort_flag;
     const uint32_t a_bytes = TC_M * ROWB;
     const uint32_t half = (TC_M + NT) * ROWB;
-    const int gsz = geo.gs, nslab = RELU ? 2 : 1;
-    const int per_sample = gsz * nslab + geo.xsb;
+    const int gregion = geo.nsc * geo.gs + 16;              // bytes of the dy (and of the y) region
+    const int xoff = gregion * (RELU ? 2 : 1);              // start of the x region in a slot
+    const bool gcontig = geo.oc_tiles == 1;                 // dy / y of the chunk are one range
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         for (int i = 0; i < geo.raws; ++i) {
-            mbar_init(smem_u32(&bars->raw_full[i]), FV_COPY);
+            mbar_init(smem_u32(&bars->raw_full[i]), 1);
             mbar_init(smem_u32(&bars->raw_empty[i]), 8);
         }
         for (int i = 0; i < FV_OPS; ++i) {
@@ -846,8 +850,8 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
         return ti;
     };
 
-    if (warp < 2) {
-        // ---------------- copy producers ----------------
+    if (warp == 0) {
+        // ---------------- bulk-copy producer ----------------
         const unsigned char* xb = reinterpret_cast<const unsigned char*>(x);
         const unsigned char* gb = reinterpret_cast<const unsigned char*>(dy);
         const unsigned char* yb = reinterpret_cast<const unsigned char*>(y);
@@ -866,20 +870,64 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
                     report(const_cast<int*>(abort_flag), 4u);
                     break;
                 }
-                const uint32_t slot = smem_u32(raw + s * geo.raw_bytes);
+                unsigned char* slot = raw + s * geo.raw_bytes;
                 const int b0 = ti.s_lo + kc * geo.nsc, nb = min(geo.nsc, ti.s_hi - b0);
-                for (int j = 0; j < nb; ++j) {
-                    const int b = b0 + j;
-                    const size_t go = (size_t(b) * p.OCP + size_t(ti.oc0) * p.P) * ES;
-                    const uint32_t sj = slot + j * per_sample;
-                    copy_range(sj, gb, go, gbytes, g_end, tid, FV_COPY);
-                    if (RELU) copy_range(sj + gsz, yb, go, gbytes, y_end, tid, FV_COPY);
-                    copy_range(sj + gsz * nslab, xb, (size_t(b) * p.IHW + size_t(ti.ic_lo) * p.HW) * ES, xbytes,
-                               x_end, tid, FV_COPY);
+                // Piece i: i < ng -> dy (and y at +gregion), else x of sample i - ng.
+                const int ng = gcontig ? 1 : nb;
+                const int npieces = ng + nb;
+                auto piece = [&](int i, int which, const unsigned char*& src, unsigned char*& dst, int& bytes,
+                                 const unsigned char*& end) {
+                    if (i < ng) {
+                        const int j = i;
+                        const size_t off = (size_t(b0 + j) * p.OCP + size_t(ti.oc0) * p.P) * ES;
+                        const unsigned char* base = which == 0 ? gb : yb;
+                        end = which == 0 ? g_end : y_end;
+                        const int d = int(off & 15);
+                        src = base + off - d;
+                        bytes = round_up(d + (gcontig ? nb * p.OCP * ES : gbytes), 16);
+                        dst = slot + (which == 0 ? 0 : gregion) + (gcontig ? 0 : j * geo.gs);
+                    } else {
+                        const int j = i - ng;
+                        const size_t off = (size_t(b0 + j) * p.IHW + size_t(ti.ic_lo) * p.HW) * ES;
+                        const int d = int(off & 15);
+                        src = xb + off - d;
+                        end = x_end;
+                        bytes = round_up(d + xbytes, 16);
+                        dst = slot + xoff + j * geo.xsb;
+                    }
+                };
+                const int nw = RELU ? 2 : 1;
+                int tx = 0;
+                for (int i = lane; i < npieces; i += 32) {
+                    for (int which = 0; which < (i < ng ? nw : 1); ++which) {
+                        const unsigned char* src;
+                        unsigned char* dst;
+                        int bytes;
+                        const unsigned char* end;
+                        piece(i, which, src, dst, bytes, end);
+                        const int bulk = slab_bytes_bulk(src, bytes, end);
+                        for (const unsigned char* t = src + bulk; t < src + bytes && t < end; ++t) dst[int(t - src)] = *t;
+                        tx += bulk;
+                    }
                 }
-                cp_async_arrive_noinc(smem_u32(&bars->raw_full[s]));
+                tx = warp_sum(tx);
+                if (lane == 0) mbar_arrive_expect_tx(smem_u32(&bars->raw_full[s]), uint32_t(tx));
+                __syncwarp();
+                for (int i = lane; i < npieces; i += 32) {
+                    for (int which = 0; which < (i < ng ? nw : 1); ++which) {
+                        const unsigned char* src;
+                        unsigned char* dst;
+                        int bytes;
+                        const unsigned char* end;
+                        piece(i, which, src, dst, bytes, end);
+                        const int bulk = slab_bytes_bulk(src, bytes, end);
+                        if (bulk > 0) bulk_g2s(smem_u32(dst), src, uint32_t(bulk), smem_u32(&bars->raw_full[s]));
+                    }
+                }
             }
         }
+    } else if (warp == 1) {
+        // idle: the producer of this kernel is warp 0 alone
     } else if (warp == FV_MMA_WARP) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
@@ -954,12 +1002,14 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
                 // 16-byte rounding slack of its copy.
                 const unsigned char* gsrc[Tr::E];
                 const unsigned char* xsrc[Tr::E];
+                const int dg0 = int(((size_t(b0) * p.OCP + size_t(ti.oc0) * p.P) * ES) & 15);
 #pragma unroll
                 for (int e = 0; e < Tr::E; ++e) {
                     const size_t b = size_t(b0 + jj[e]);
-                    const unsigned char* sj = slot + jj[e] * per_sample;
-                    gsrc[e] = sj + int(((b * p.OCP + size_t(ti.oc0) * p.P) * ES) & 15);
-                    xsrc[e] = sj + gsz * nslab + int(((b * p.IHW + size_t(ti.ic_lo) * p.HW) * ES) & 15);
+                    // Element (j, oc row r, p) of dy is at gsrc[e] + (r * P + p) * ES; y is gregion further.
+                    gsrc[e] = gcontig ? slot + dg0 + jj[e] * p.OCP * ES
+                                      : slot + jj[e] * geo.gs + int(((b * p.OCP + size_t(ti.oc0) * p.P) * ES) & 15);
+                    xsrc[e] = slot + xoff + jj[e] * geo.xsb + int(((b * p.IHW + size_t(ti.ic_lo) * p.HW) * ES) & 15);
                 }
                 // A: g rows (oc), 16 bytes of columns per unit.
                 for (int u = ft; u < TC_M * 8; u += 256) {
@@ -975,13 +1025,13 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
                                     uint32_t h = *reinterpret_cast<const unsigned short*>(sj + gi * 2);
                                     if (RELU) {
                                         const float yv = __bfloat162float(
-                                            *reinterpret_cast<const __nv_bfloat16*>(sj + gsz + gi * 2));
+                                            *reinterpret_cast<const __nv_bfloat16*>(sj + gregion + gi * 2));
                                         if (!(yv > 0.f)) h = 0;
                                     }
                                     wv[e >> 1] |= (e & 1) ? (h << 16) : h;
                                 } else {
                                     uint32_t v = *reinterpret_cast<const uint32_t*>(sj + gi * 4);
-                                    if (RELU && !(*reinterpret_cast<const float*>(sj + gsz + gi * 4) > 0.f)) v = 0;
+                                    if (RELU && !(*reinterpret_cast<const float*>(sj + gregion + gi * 4) > 0.f)) v = 0;
                                     wv[e] = v;
                                 }
                             }
