@@ -1,18 +1,19 @@
 // kernels_tc.cu -- tcgen05 tensor-core implicit-GEMM kernels (5th-generation
-// tensor cores, accumulator in tensor memory).
+// tensor cores, accumulator in tensor memory), one per operation:
 //
-// Forward, per CTA tile:  D[oc, n] = sum_k W[oc, k] * X[n, k]   (M = 128 output
-// channels, N = NT columns n = (b, oh, ow), K = IC*K*K padded to the chunk size),
-// X[n, k] = x[col_base(n) + k_offset(k)] gathered on the fly (implicit im2col).
+//   forward  Y[n, oc]  = sum_k X[n, k] * W[oc, k]     X[n, k] = x[col_base(n) + k_offset(k)]
+//   d_input  dX[n, k]  = sum_oc G[n, oc] * W[oc, k]   then col2im into dx
+//   wgrad    dW[oc, k] = sum_n G[n, oc] * X[n, k]     split over n, two-pass reduction
+//
+// with columns n = (b, oh, ow), k = (ic, kh, kw) and G = dy masked by y > 0 when the
+// layer has a fused ReLU (implicit im2col: X and G are gathered on the fly).
 //   bf16: tcgen05.mma kind::f16, bf16 operands, fp32 accumulation.
-//   fp32: three tcgen05.mma kind::tf32 per step (hi*hi + hi*lo + lo*hi with
-//         v = hi + lo, hi = tf32(v), lo = tf32(v - hi)), which keeps about 21
+//   fp32: tcgen05.mma kind::tf32 on split operands (v = hi + lo, hi = tf32(v),
+//         lo = tf32(v - hi)) summing hi*hi + hi*lo + lo*hi, which keeps about 21
 //         significant bits per product: fp32-level accuracy on the tensor pipe.
-// All 256 threads gather the next K-chunk of both operands into shared memory
-// (K-major, 128-byte swizzled core-matrix layout) while one thread issues the
-// MMAs of the current chunk; two stages, one mbarrier per stage signalled by
-// tcgen05.commit.  The epilogue reads the accumulator with tcgen05.ld, applies
-// the ReLU and writes y.  Tiles are scheduled persistently over the grid.
+// Each kernel is warp-specialized: producer warps stage raw input slabs and packed
+// weight chunks with bulk asynchronous copies, formatter warps turn the raw slabs into
+// MMA operands, one thread issues the MMAs, and mbarriers chain the stages.
 //
 // Every mbarrier wait is bounded; a wait that runs out sets a bit in
 // g_tc_status, all threads leave their loops together and the CTA frees its
@@ -31,8 +32,6 @@ namespace {
 
 using namespace tc;
 
-constexpr int TC_THREADS = 256;
-constexpr int TC_STAGES = 2;
 constexpr int TC_M = 128;
 constexpr int ROWB = 128;  // bytes of one operand row per K-chunk
 
@@ -141,115 +140,6 @@ __device__ __forceinline__ void issue_chunk(uint32_t tmem, uint32_t a_addr, uint
     }
 }
 
-// Shared state of one CTA's tensor-core pipeline.  A stage holds the A tile
-// (128 rows) then the B tile (NT rows), 128 bytes per row, followed for split
-// fp32 operands by the lo parts of both (`half` bytes further).
-struct TcPipe {
-    unsigned char* smem;   // stage 0 (1024-byte aligned)
-    uint32_t smem_base;    // its shared-window address
-    uint32_t a_bytes, half, stage_bytes;
-    uint64_t* bars;        // one mbarrier per stage, completed by tcgen05.commit
-    int* abort_flag;
-    uint32_t tmem, idesc;
-    uint32_t g;            // K-chunks issued so far; stage = g & 1
-};
-
-template <typename T>
-__device__ __forceinline__ void pipe_setup(TcPipe& pp, unsigned char* smem, int NT, int a_rows = TC_M)
-{
-    using Tr = TcTraits<T>;
-    pp.smem = smem;
-    pp.smem_base = smem_u32(smem);
-    pp.a_bytes = a_rows * ROWB;
-    pp.half = pp.a_bytes + NT * ROWB;
-    pp.stage_bytes = Tr::split ? 2 * pp.half : pp.half;
-    pp.idesc = instr_desc(Tr::fmt, TC_M, NT);
-    pp.g = 0;
-}
-
-// Tail of the shared-memory carve-up after the stages: barriers, TMEM slot, abort flag.
-struct TcTail {
-    uint64_t bars[TC_STAGES];
-    uint32_t tslot;
-    int abort_flag;
-};
-
-// Barrier init + TMEM allocation.  Call with all threads; ends with a CTA barrier.
-__device__ __forceinline__ void pipe_start(TcPipe& pp, TcTail* tail, int tmem_cols)
-{
-    const int tid = threadIdx.x;
-    if (tid == 0) {
-        for (int s = 0; s < TC_STAGES; ++s) mbar_init(smem_u32(&tail->bars[s]), 1);
-        fence_mbar_init();
-        tail->abort_flag = 0;
-    }
-    if ((tid >> 5) == 0) tmem_alloc(smem_u32(&tail->tslot), tmem_cols);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    pp.bars = tail->bars;
-    pp.abort_flag = &tail->abort_flag;
-    pp.tmem = tail->tslot;
-}
-
-__device__ __forceinline__ void pipe_finish(const TcPipe& pp, int tmem_cols)
-{
-    __syncthreads();
-    if ((threadIdx.x >> 5) == 0) {
-        tc_fence_after();
-        tmem_dealloc(pp.tmem, tmem_cols);
-    }
-}
-
-// One tile's K loop.  fill(stage_ptr, kc) writes chunk kc of A (at stage_ptr) and B
-// (at stage_ptr + a_bytes), plus lo parts at + half, with all threads.  When
-// `a_fixed` is nonzero the MMAs read A from that shared address (+ kc * 16 KB
-// per chunk, lo parts `a_fixed_lo_off` further) instead of the stage.  Returns
-// false if a wait ran out.
-template <typename T, int SWZ, class Fill>
-__device__ __forceinline__ bool pipe_tile(TcPipe& pp, int nchunks, Fill&& fill, uint32_t a_fixed = 0,
-                                          uint32_t a_fixed_lo_off = 0)
-{
-    for (int kc = 0; kc < nchunks; ++kc, ++pp.g) {
-        const int s = pp.g & 1;
-        unsigned char* st = pp.smem + s * pp.stage_bytes;
-        if (pp.g >= 2 && !mbar_wait(smem_u32(&pp.bars[s]), ((pp.g >> 1) - 1) & 1)) report(pp.abort_flag, 1u);
-        fill(st, kc);
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (*pp.abort_flag) return false;
-        if (threadIdx.x == 0) {
-            tc_fence_after();
-            const uint32_t sa = pp.smem_base + s * pp.stage_bytes;
-            if (a_fixed)
-                issue_chunk<T, SWZ>(pp.tmem, a_fixed + kc * (TC_M * ROWB), sa + pp.a_bytes, a_fixed_lo_off,
-                                    pp.half, pp.idesc, kc == 0);
-            else
-                issue_chunk<T, SWZ>(pp.tmem, sa, sa + pp.a_bytes, pp.half, pp.half, pp.idesc, kc == 0);
-            mma_commit(smem_u32(&pp.bars[s]));
-        }
-    }
-    return true;
-}
-
-// Wait until the tile's accumulator is complete.  All threads; false if aborted.
-__device__ __forceinline__ bool pipe_wait_acc(TcPipe& pp)
-{
-    const uint32_t last = pp.g - 1;
-    if (!mbar_wait(smem_u32(&pp.bars[last & 1]), (last >> 1) & 1)) report(pp.abort_flag, 2u);
-    __syncthreads();
-    if (*pp.abort_flag) return false;
-    tc_fence_after();
-    return true;
-}
-
-// End of an epilogue that read TMEM: order the reads before the next tile's MMAs.
-__device__ __forceinline__ void pipe_release_acc()
-{
-    tc_fence_before();
-    __syncthreads();
-}
-
 __device__ __forceinline__ unsigned char* align1024(unsigned char* p)
 {
     return reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -257,33 +147,33 @@ __device__ __forceinline__ unsigned char* align1024(unsigned char* p)
 
 // ======================================================================================
 // Weight packing.  Every call of the tensor-core forward / d_input first rewrites w into
-// the exact shared-memory image of the A operand's K-chunks (128 rows x 128 bytes,
-// 128-byte swizzled, K-major; fp32 as a tf32 hi tile followed by a lo tile), so that the
+// the exact shared-memory image of the weight operand's K-chunks (rows x 128 bytes,
+// 128-byte swizzled, K-major; fp32 as tf32 hi rows followed by lo rows), so that the
 // main kernel fetches each chunk with one large bulk copy.
-//   forward: tile (ot, kc) holds A[r][kk] = w[ot*128 + r][kc*KC + kk]
+//   forward: tile (ot, kc) holds W[r][kk] = w[ot*OTp + r][kc*KC + kk], OTp rows
 //   d_input: tile (kt, ch) holds A[r][kk] = w[ch*KC + kk][k0(kt) + r] (W transposed), rows
 //            r < CIC*K*K of input-channel chunk kt
 // ======================================================================================
 template <typename T>
 __global__ void pack_fwd_w_kernel(const ConvParams p, const T* __restrict__ w, unsigned char* __restrict__ out,
-                                  int nchunks, int oc_tiles)
+                                  int nchunks, int oc_tiles, int OTp)
 {
     using Tr = TcTraits<T>;
-    const int tile_units = TC_M * 8;
+    const int tile_units = OTp * 8;
     const size_t total = size_t(oc_tiles) * nchunks * tile_units;
-    const size_t tb = size_t(TC_M) * ROWB * (Tr::split ? 2 : 1);
+    const size_t tb = size_t(OTp) * ROWB * (Tr::split ? 2 : 1);
     for (size_t u = blockIdx.x * size_t(blockDim.x) + threadIdx.x; u < total; u += size_t(gridDim.x) * blockDim.x) {
         const int within = int(u % tile_units);
         const size_t t = u / tile_units;
         const int kc = int(t % nchunks), ot = int(t / nchunks);
         const int r = within >> 3, c = within & 7;
-        const int oc = ot * TC_M + r, k = kc * Tr::KC + c * Tr::E;
+        const int oc = ot * OTp + r, k = kc * Tr::KC + c * Tr::E;
         float v[8];
 #pragma unroll
         for (int i = 0; i < Tr::E; ++i)
             v[i] = (oc < p.OC && k + i < p.Kred) ? Elem<T>::ldg(w + size_t(oc) * p.Kred + k + i) : 0.f;
         unsigned char* base = out + t * tb;
-        put_unit<T, 1>(base, base + TC_M * ROWB, r, c, v);
+        put_unit<T, 1>(base, base + OTp * ROWB, r, c, v);
     }
 }
 
@@ -313,73 +203,91 @@ __global__ void pack_dgrad_w_kernel(const ConvParams p, const T* __restrict__ w,
 }
 
 // ======================================================================================
-// Forward: tile = (128 output channels, NT columns n); K = IC*K*K in chunks of KC.
-// Warp roles (352 threads):
+// Forward: tile = (128 columns n = (b, oh, ow), OTp output channels); K = IC*K*K in
+// chunks of KC.  The gathered operand X[n, k] is the MMA's A operand and lives in
+// tensor memory (lane m = column n0 + m, K along the TMEM columns); the packed weights
+// are the B operand (N = OTp rows; fp32: the tf32 hi rows followed by the lo rows, so
+// one N = 2*OTp MMA forms X_hi*W_hi and X_hi*W_lo, and a second N = OTp MMA adds
+// X_lo*W_hi into the first half).  Only the weights are read from shared memory by
+// the tensor core.
+// Warp roles (608 threads):
 //   warp 0      x producer: per super-chunk (XG consecutive K-chunks) and per sample the
 //               tile touches, one bulk copy of the contiguous channels x[b, ic_lo : ic_hi]
 //               the super-chunk covers, into one of two raw slots.  Sources are rounded
 //               down to 16 bytes (the slack is skipped when read); bytes of a last
 //               16-byte block that lie past the end of x are copied by plain loads.
-//   warp 1      w producer: per K-chunk, one bulk copy of the packed weight tile (16 KB;
-//               32 KB hi + lo for fp32) straight into the A half of the operand stage.
-//   warp 2      MMA: one thread issues the chunk's tcgen05.mma steps into the TMEM
-//               accumulator, commits to the stage's "empty" barrier and, after a tile's
-//               last chunk, to the accumulator barrier.
-//   warps 3-10  formatters: build the B operand (gathered patches, 128-byte swizzled
-//               K-major) of each chunk from the raw slot; then the tile's epilogue
-//               (TMEM -> ReLU -> y).
+//   warp 1      w producer: per K-chunk, one bulk copy of the packed weight chunk
+//               (OTp rows x 128 bytes; x2 for fp32 hi + lo) into a weight stage.
+//   warp 2      MMA: one thread issues the chunk's tcgen05.mma steps, commits to the
+//               weight stage's and the TMEM operand stage's "empty" barriers and, after
+//               a tile's last chunk, to the accumulator barrier.
+//   warps 3-18  formatters: warp w owns TMEM lanes 32*(w%4) .. +31 (one column each) and
+//               a quarter of each chunk's K; gathers its column's patch values from the
+//               raw slot and writes them with tcgen05.st; then the tile's epilogue
+//               (TMEM -> ReLU -> y), each warp a quarter of the output channels.
 // ======================================================================================
 constexpr int FV_THREADS = 352;
-constexpr int FV_COPY = 64;   // copy threads of the wgrad kernel (warps 0-1)
 constexpr int FV_MMA_WARP = 2;
 constexpr int FV_FMT0 = 96;   // first formatter thread (warp 3)
 constexpr int FV_OPS = 2;
 constexpr int FV_RAWS = 2;
 
-constexpr int FV_MAXA = 8;   // max weight-tile slots
-constexpr int FV_MAXB = 4;   // max gathered-operand stages
+constexpr int FA_TM = 128;    // columns per forward tile (TMEM lanes)
+constexpr int FA_KSPLIT = 4;  // formatter warps per TMEM lane quarter (each a quarter of the chunk's K)
+constexpr int FA_FMTW = 4 * FA_KSPLIT;
+constexpr int FA_THREADS = FV_FMT0 + 32 * FA_FMTW;
+constexpr int FA_MAXW = 6;    // max weight stages
+constexpr int FA_MAXA = 8;    // max TMEM operand stages
+constexpr int FA_TMEM_COLS = 512;
 
 struct FwdGeom {
-    int NT, n_tiles, oc_tiles, tmem_cols;
-    int nchunks;      // K-chunks per tile
-    int xg;           // K-chunks per x super-chunk
-    int na, nbs;      // weight-tile slots, gathered-operand stages
-    int nsmax;        // samples a tile can span
-    int xs;           // bytes per sample in a raw slot
-    int raw_bytes;    // one raw slot
-    int a_bytes_tile; // one weight tile: 16 KB, 32 KB (hi + lo) for split fp32
-    int b_bytes;      // one gathered-operand stage: NT * 128 bytes, x2 for split fp32
+    int OTp, oc_tiles;  // output-channel rows per tile (multiple of 16), tiles over OC
+    int n_tiles;        // column tiles of FA_TM
+    int nchunks;        // K-chunks per tile
+    int xg;             // K-chunks per x super-chunk
+    int nw, na;         // weight stages (shared memory), operand stages (TMEM)
+    int nsmax;          // samples a tile can span
+    int xs;             // bytes per sample in a raw slot
+    int raw_bytes;      // one raw slot
+    int w_bytes;        // one weight stage
+    int dcols;          // accumulator columns (2*OTp for split fp32)
+    int acol0, acols;   // first TMEM column of the operand stages, columns per stage
 };
 
 struct FwdBars {
     uint64_t raw_full[FV_RAWS], raw_empty[FV_RAWS];
-    uint64_t a_full[FV_MAXA], a_empty[FV_MAXA];
-    uint64_t b_full[FV_MAXB], b_empty[FV_MAXB];
-    uint64_t acc_full;
+    uint64_t w_full[FA_MAXW], w_empty[FA_MAXW];
+    uint64_t a_full[FA_MAXA], a_empty[FA_MAXA];
+    uint64_t acc_full, acc_empty;
     uint32_t tslot;
     int abort_flag;
 };
 
 template <typename T>
-inline FwdGeom fwd_geom(const ConvParams& p, int NT, int xg, int na, int nbs)
+inline FwdGeom fwd_geom(const ConvParams& p, int xg, int nw)
 {
     using Tr = TcTraits<T>;
     const int es = int(sizeof(T));
     FwdGeom g;
-    g.NT = NT;
-    g.n_tiles = ceil_div(p.N, NT);
-    g.oc_tiles = ceil_div(p.OC, TC_M);
-    g.tmem_cols = pow2_at_least(NT);
+    const int otmax = Tr::split ? 128 : 256;
+    g.oc_tiles = ceil_div(p.OC, otmax);
+    g.OTp = round_up(ceil_div(p.OC, g.oc_tiles), 16);
+    g.n_tiles = ceil_div(p.N, FA_TM);
     g.nchunks = round_up(p.Kred, Tr::KC) / Tr::KC;
     g.xg = xg;
-    g.nsmax = std::min(p.B, (NT - 1) / p.P + 2);
+    g.nw = nw;
+    g.nsmax = std::min(p.B, (FA_TM - 1) / p.P + 2);
     const int chmax = std::min(p.IC, (xg * Tr::KC - 1) / p.KK + 2);
     g.xs = round_up(chmax * p.HW * es + 16, 16);
+    // Sample stride = 12 words mod 32: the columns of consecutive samples fall on
+    // different banks when a warp gathers one k for 32 columns.
+    while ((g.xs / 4) % 32 != 12) g.xs += 16;
     g.raw_bytes = round_up(g.nsmax * g.xs, 128);
-    g.na = na;
-    g.nbs = nbs;
-    g.a_bytes_tile = TC_M * ROWB * (Tr::split ? 2 : 1);
-    g.b_bytes = NT * ROWB * (Tr::split ? 2 : 1);
+    g.w_bytes = g.OTp * ROWB * (Tr::split ? 2 : 1);
+    g.dcols = g.OTp * (Tr::split ? 2 : 1);
+    g.acol0 = round_up(g.dcols, 32);
+    g.acols = Tr::split ? 2 * Tr::KC : Tr::KC / 2;
+    g.na = std::min(FA_MAXA, (FA_TMEM_COLS - g.acol0) / g.acols);
     return g;
 }
 
@@ -387,14 +295,13 @@ template <typename T>
 inline int fwd_smem(const ConvParams& p, const FwdGeom& g)
 {
     const int kred_pad = round_up(p.Kred, TcTraits<T>::KC);
-    return 1024 + g.na * g.a_bytes_tile + g.nbs * g.b_bytes + FV_RAWS * g.raw_bytes + kred_pad * 4 +
-           int(sizeof(FwdBars)) + 16;
+    return 1024 + g.nw * g.w_bytes + FV_RAWS * g.raw_bytes + kred_pad * 4 + int(sizeof(FwdBars)) + 16;
 }
 
 template <typename T>
 inline size_t fwd_packed_bytes(const FwdGeom& g)
 {
-    return size_t(g.oc_tiles) * g.nchunks * g.a_bytes_tile;
+    return size_t(g.oc_tiles) * g.nchunks * g.w_bytes;
 }
 
 __device__ __forceinline__ int warp_sum(int v)
@@ -433,47 +340,67 @@ __device__ __forceinline__ int slab_bytes_bulk(const unsigned char* src, int byt
     return end16 > src ? int(end16 - src) : 0;
 }
 
+// Position in a ring of n stages: slot i, phase parity ph of its current use, and
+// whether every slot has been used once (from then on a producer waits for "empty").
+struct RingPos {
+    int i = 0;
+    uint32_t ph = 0;
+    bool wrapped = false;
+    __device__ __forceinline__ void next(int n)
+    {
+        if (++i == n) {
+            i = 0;
+            ph ^= 1u;
+            wrapped = true;
+        }
+    }
+};
+
 template <typename T, bool RELU, int SWZ>
-__global__ void __launch_bounds__(FV_THREADS, 1)
+__global__ void __launch_bounds__(FA_THREADS, 1)
 fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* __restrict__ wpack,
               T* __restrict__ y, const FwdGeom geo)
 {
     using Tr = TcTraits<T>;
     constexpr int ES = int(sizeof(T));
+    constexpr int KQ = Tr::KC / FA_KSPLIT;        // K values per formatter warp and chunk
+    constexpr int KQC = Tr::split ? KQ : KQ / 2;  // TMEM columns they fill (per part)
+    static_assert(KQC == 8, "one tcgen05.st of 8 columns per part");
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = align1024(smem_raw);
-    const int NT = geo.NT;
     const int kred_pad = round_up(p.Kred, Tr::KC);
-    // Layout: weight-tile slots (hi 16 KB [+ lo 16 KB]) | gathered stages (hi [+ lo]) | raw x slots
-    unsigned char* aring = smem;
-    unsigned char* bring = aring + geo.na * geo.a_bytes_tile;
-    unsigned char* raw = bring + geo.nbs * geo.b_bytes;
+    // Layout: weight stages | raw x slots | k offsets | barriers
+    unsigned char* wring = smem;
+    unsigned char* raw = wring + geo.nw * geo.w_bytes;
     int* offk = reinterpret_cast<int*>(raw + FV_RAWS * geo.raw_bytes);
     FwdBars* bars = reinterpret_cast<FwdBars*>(offk + kred_pad);
     volatile int* abort_flag = &bars->abort_flag;
-    const uint32_t a_bytes = TC_M * ROWB;          // one hi (or lo) weight tile
-    const uint32_t b_half = NT * ROWB;             // one hi (or lo) gathered tile
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    for (int k = tid; k < kred_pad; k += FV_THREADS) offk[k] = (k < p.Kred) ? k_offset(p, k) : -1;
+    // offk[k]: byte offset of x[., ic, kh, kw] from channel ic_lo of k's super-chunk (0 past Kred).
+    for (int k = tid; k < kred_pad; k += FA_THREADS) {
+        const int sc_ic = (k / (geo.xg * Tr::KC)) * geo.xg * Tr::KC / p.KK;
+        offk[k] = (k < p.Kred) ? (k_offset(p, k) - sc_ic * p.HW) * ES : 0;
+    }
     if (tid == 0) {
         for (int i = 0; i < FV_RAWS; ++i) {
             mbar_init(smem_u32(&bars->raw_full[i]), 1);
-            mbar_init(smem_u32(&bars->raw_empty[i]), 8);
+            mbar_init(smem_u32(&bars->raw_empty[i]), FA_FMTW);
+        }
+        for (int i = 0; i < geo.nw; ++i) {
+            mbar_init(smem_u32(&bars->w_full[i]), 1);
+            mbar_init(smem_u32(&bars->w_empty[i]), 1);
         }
         for (int i = 0; i < geo.na; ++i) {
-            mbar_init(smem_u32(&bars->a_full[i]), 1);
+            mbar_init(smem_u32(&bars->a_full[i]), FA_FMTW);
             mbar_init(smem_u32(&bars->a_empty[i]), 1);
         }
-        for (int i = 0; i < geo.nbs; ++i) {
-            mbar_init(smem_u32(&bars->b_full[i]), 8);
-            mbar_init(smem_u32(&bars->b_empty[i]), 1);
-        }
         mbar_init(smem_u32(&bars->acc_full), 1);
+        mbar_init(smem_u32(&bars->acc_empty), FA_FMTW);
         fence_mbar_init();
         bars->abort_flag = 0;
     }
-    if (warp == 0) tmem_alloc(smem_u32(&bars->tslot), geo.tmem_cols);
+    if (warp == 0) tmem_alloc(smem_u32(&bars->tslot), FA_TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -485,15 +412,14 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
         // ---------------- x producer ----------------
         const unsigned char* xb = reinterpret_cast<const unsigned char*>(x);
         const unsigned char* x_end = xb + size_t(p.B) * p.IHW * ES;
-        uint32_t xq = 0;
+        RingPos rp;
         for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
-            const int n0 = (tile % geo.n_tiles) * NT;
-            const int n_end = min(n0 + NT, p.N);
+            const int n0 = (tile % geo.n_tiles) * FA_TM;
+            const int n_end = min(n0 + FA_TM, p.N);
             const int b_first = n0 / p.P, nsamp = (n_end - 1) / p.P - b_first + 1;
-            for (int sc = 0; sc < nsuper; ++sc, ++xq) {
-                const int s = xq % FV_RAWS;
-                const uint32_t use = xq / FV_RAWS;
-                if (use >= 1 && !mbar_wait_or_abort(smem_u32(&bars->raw_empty[s]), (use - 1) & 1, abort_flag)) {
+            for (int sc = 0; sc < nsuper; ++sc, rp.next(FV_RAWS)) {
+                const int s = rp.i;
+                if (rp.wrapped && !mbar_wait_or_abort(smem_u32(&bars->raw_empty[s]), rp.ph ^ 1u, abort_flag)) {
                     report(const_cast<int*>(abort_flag), 4u);
                     break;
                 }
@@ -536,20 +462,18 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
     } else if (warp == 1) {
         // ---------------- w producer ----------------
         if (lane == 0) {
-            uint32_t q = 0;
+            RingPos wp;
             for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
                 const int ot = tile / geo.n_tiles;
-                for (int kc = 0; kc < geo.nchunks; ++kc, ++q) {
-                    const int sl = q % geo.na;
-                    const uint32_t use = q / geo.na;
-                    if (use >= 1 && !mbar_wait_or_abort(smem_u32(&bars->a_empty[sl]), (use - 1) & 1, abort_flag)) {
+                const unsigned char* src = wpack + size_t(ot) * geo.nchunks * geo.w_bytes;
+                for (int kc = 0; kc < geo.nchunks; ++kc, wp.next(geo.nw), src += geo.w_bytes) {
+                    if (wp.wrapped && !mbar_wait_or_abort(smem_u32(&bars->w_empty[wp.i]), wp.ph ^ 1u, abort_flag)) {
                         report(const_cast<int*>(abort_flag), 16u);
                         break;
                     }
-                    const uint32_t bar = smem_u32(&bars->a_full[sl]);
-                    mbar_arrive_expect_tx(bar, uint32_t(geo.a_bytes_tile));
-                    const unsigned char* src = wpack + (size_t(ot) * geo.nchunks + kc) * geo.a_bytes_tile;
-                    bulk_g2s(smem_u32(aring + sl * geo.a_bytes_tile), src, uint32_t(geo.a_bytes_tile), bar);
+                    const uint32_t bar = smem_u32(&bars->w_full[wp.i]);
+                    mbar_arrive_expect_tx(bar, uint32_t(geo.w_bytes));
+                    bulk_g2s(smem_u32(wring + wp.i * geo.w_bytes), src, uint32_t(geo.w_bytes), bar);
                 }
             }
         }
@@ -557,24 +481,42 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
     } else if (warp == FV_MMA_WARP) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
-            const uint32_t idesc = instr_desc(Tr::fmt, TC_M, NT);
-            const uint32_t a_u32 = smem_u32(aring), b_u32 = smem_u32(bring);
-            uint32_t q = 0;
-            for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
+            // fp32: N = 2*OTp over [W_hi; W_lo], then N = OTp over W_hi; bf16: N = OTp.
+            const uint32_t idesc2 = instr_desc(Tr::fmt, FA_TM, geo.dcols);
+            const uint32_t idesc1 = instr_desc(Tr::fmt, FA_TM, geo.OTp);
+            const uint32_t w_u32 = smem_u32(wring);
+            RingPos wp, ap;
+            uint32_t t = 0;
+            for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x, ++t) {
                 bool ok = true;
-                for (int kc = 0; kc < geo.nchunks; ++kc, ++q) {
-                    const int sl = q % geo.na, st = q % geo.nbs;
-                    if (!mbar_wait_or_abort(smem_u32(&bars->a_full[sl]), (q / geo.na) & 1, abort_flag) ||
-                        !mbar_wait_or_abort(smem_u32(&bars->b_full[st]), (q / geo.nbs) & 1, abort_flag)) {
+                if (t >= 1 && !mbar_wait_or_abort(smem_u32(&bars->acc_empty), (t - 1) & 1, abort_flag)) {
+                    report(const_cast<int*>(abort_flag), 8u);
+                    break;
+                }
+                tc_fence_after();
+                for (int kc = 0; kc < geo.nchunks; ++kc, wp.next(geo.nw), ap.next(geo.na)) {
+                    if (!mbar_wait_or_abort(smem_u32(&bars->w_full[wp.i]), wp.ph, abort_flag) ||
+                        !mbar_wait_or_abort(smem_u32(&bars->a_full[ap.i]), ap.ph, abort_flag)) {
                         report(const_cast<int*>(abort_flag), 8u);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    issue_chunk<T, SWZ>(tmem, a_u32 + sl * geo.a_bytes_tile, b_u32 + st * geo.b_bytes, a_bytes,
-                                        b_half, idesc, kc == 0);
-                    mma_commit(smem_u32(&bars->a_empty[sl]));
-                    mma_commit(smem_u32(&bars->b_empty[st]));
+                    const uint32_t wa = w_u32 + wp.i * geo.w_bytes;
+                    const uint32_t aa = tmem + uint32_t(geo.acol0 + ap.i * geo.acols);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint64_t bd = op_desc<SWZ>(wa + kstep_off<SWZ>(j));
+                        const uint32_t acc = (kc == 0 && j == 0) ? 0u : 1u;
+                        if constexpr (Tr::split) {
+                            mma_tf32_ta(tmem, aa + 8 * j, bd, idesc2, acc);           // hi * [hi; lo]
+                            mma_tf32_ta(tmem, aa + Tr::KC + 8 * j, bd, idesc1, 1u);  // lo * hi
+                        } else {
+                            mma_f16_ta(tmem, aa + 8 * j, bd, idesc1, acc);
+                        }
+                    }
+                    mma_commit(smem_u32(&bars->w_empty[wp.i]));
+                    mma_commit(smem_u32(&bars->a_empty[ap.i]));
                 }
                 if (!ok) break;
                 mma_commit(smem_u32(&bars->acc_full));
@@ -583,130 +525,143 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
         __syncwarp();
     } else {
         // ---------------- formatters + epilogue ----------------
-        // Thread ft owns unit column cfix = ft & 7 of B rows (ft >> 3) + 32 i, i < ceil(NT/32).
-        const int ft = tid - FV_FMT0;  // 0 .. 255
-        const int fw = warp - 3;       // 0 .. 7
-        const int cfix = ft & 7;
-        const int rbase = ft >> 3;
-        const int nbu = (NT + 31) >> 5;
-        constexpr int MAXB = 8;
-        uint32_t q = 0, xq = 0, t = 0;
+        const int fw = warp - 3;            // 0 .. FA_FMTW - 1
+        const int qd = warp & 3;            // TMEM lane quarter this warp may access
+        const int sub = fw >> 2;            // which quarter of each chunk's K
+        const int m = qd * 32 + lane;       // this thread's column within the tile
+        const uint32_t lane_bits = uint32_t(qd * 32) << 16;
+        const uint32_t raw_u32 = smem_u32(raw), offk_u32 = smem_u32(offk) + uint32_t(sub * KQ * 4);
+        const bool ragged_k = (p.Kred % Tr::KC) != 0;
+        RingPos ap, rp;
+        uint32_t t = 0;
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++t) {
-            const int n0 = (tile % geo.n_tiles) * NT, oc0 = (tile / geo.n_tiles) * TC_M;
+            const int n0 = (tile % geo.n_tiles) * FA_TM, ot = tile / geo.n_tiles;
             const int b_first = n0 / p.P;
-            int boff[MAXB], bmis[MAXB];
-            uint32_t bdst[MAXB];
-#pragma unroll
-            for (int i = 0; i < MAXB; ++i) {
-                boff[i] = -1;  // -1: row past NT (not part of the tile); -2: zero row
-                bmis[i] = 0;
-                bdst[i] = 0;
-                if (i < nbu && rbase + 32 * i < NT) {
-                    const int r = rbase + 32 * i;
-                    const int n = n0 + r;
-                    bdst[i] = unit_off<SWZ>(r, cfix);
-                    boff[i] = -2;
-                    if (n < p.N) {
-                        uint32_t bq, pq, oh, ow;
-                        p.dm_P.divmod(uint32_t(n), bq, pq);
-                        p.dm_OW.divmod(pq, oh, ow);
-                        boff[i] = (int(bq) - b_first) * geo.xs + (int(oh) * p.S * p.W + int(ow) * p.S) * ES;
-                        bmis[i] = int((size_t(bq) * p.IHW * ES) & 15);
-                    }
-                }
+            const int n = n0 + m;
+            // Columns past N gather column N-1's values: their accumulator rows are
+            // computed but never stored (rows of D depend only on rows of A).
+            int boff, bmis;
+            {
+                uint32_t bq, pq, oh, ow;
+                p.dm_P.divmod(uint32_t(min(n, p.N - 1)), bq, pq);
+                p.dm_OW.divmod(pq, oh, ow);
+                boff = (int(bq) - b_first) * geo.xs + (int(oh) * p.S * p.W + int(ow) * p.S) * ES;
+                bmis = int((size_t(bq) * p.IHW * ES) & 15);
             }
             bool ok = true;
-            const unsigned char* slot = raw;
-            int ic_lo = 0, cmis = 0;
-            for (int kc = 0; kc < geo.nchunks; ++kc, ++q) {
-                const int st = q % geo.nbs;
-                const uint32_t ouse = q / geo.nbs;
-                if (kc % geo.xg == 0) {
-                    const int s = xq % FV_RAWS;
-                    if (!mbar_wait_or_abort(smem_u32(&bars->raw_full[s]), (xq / FV_RAWS) & 1, abort_flag)) {
+            uint32_t sbase = 0;
+            int xc = 0;  // chunk within the super-chunk
+            for (int kc = 0; kc < geo.nchunks; ++kc, ap.next(geo.na)) {
+                if (xc == 0) {
+                    if (!mbar_wait_or_abort(smem_u32(&bars->raw_full[rp.i]), rp.ph, abort_flag)) {
                         report(const_cast<int*>(abort_flag), 1u);
                         ok = false;
                         break;
                     }
-                    slot = raw + s * geo.raw_bytes;
-                    ic_lo = (kc * Tr::KC) / p.KK;
-                    cmis = (ic_lo * p.HW * ES) & 15;
+                    const int ic_lo = (kc * Tr::KC) / p.KK;
+                    const int cmis = (ic_lo * p.HW * ES) & 15;
+                    sbase = raw_u32 + uint32_t(rp.i * geo.raw_bytes + boff + ((bmis + cmis) & 15));
                 }
-                if (ouse >= 1 && !mbar_wait_or_abort(smem_u32(&bars->b_empty[st]), (ouse - 1) & 1, abort_flag)) {
+                if (ap.wrapped && !mbar_wait_or_abort(smem_u32(&bars->a_empty[ap.i]), ap.ph ^ 1u, abort_flag)) {
                     report(const_cast<int*>(abort_flag), 1u);
                     ok = false;
                     break;
                 }
-                const int k0 = kc * Tr::KC;
-                unsigned char* op = bring + st * geo.b_bytes;
-                int ko[Tr::E];
+                tc_fence_after();
+                const uint32_t oaddr = offk_u32 + uint32_t(kc * Tr::KC * 4);
+                const uint32_t col = tmem + lane_bits + uint32_t(geo.acol0 + ap.i * geo.acols + sub * KQC);
+                // k >= Kred exists only in a ragged last chunk: those values are zeroed.
+                const int kvalid = (ragged_k && kc == geo.nchunks - 1) ? p.Kred - (kc * Tr::KC + sub * KQ) : KQ;
+                int o[KQ];
 #pragma unroll
-                for (int e = 0; e < Tr::E; ++e) {
-                    const int kk = offk[k0 + cfix * Tr::E + e];
-                    ko[e] = kk >= 0 ? (kk - ic_lo * p.HW) * ES : -1;
+                for (int i = 0; i < KQ / 4; ++i) {
+                    const int4 v4 = lds128(oaddr + 16 * i);
+                    o[4 * i] = v4.x;
+                    o[4 * i + 1] = v4.y;
+                    o[4 * i + 2] = v4.z;
+                    o[4 * i + 3] = v4.w;
                 }
+                uint32_t v[KQ];
 #pragma unroll
-                for (int i = 0; i < MAXB; ++i) {
-                    if (i >= nbu) break;
-                    if (boff[i] == -1) continue;
-                    uint32_t wv[4] = {0, 0, 0, 0};
-                    if (boff[i] >= 0) {
-                        const unsigned char* src = slot + boff[i] + ((bmis[i] + cmis) & 15);
+                for (int e = 0; e < KQ; ++e) v[e] = Tr::split ? lds32(sbase + uint32_t(o[e])) : lds16(sbase + uint32_t(o[e]));
+                if (kvalid < KQ) {
 #pragma unroll
-                        for (int e = 0; e < Tr::E; ++e) {
-                            if (ko[e] >= 0) {
-                                if constexpr (ES == 2) {
-                                    const uint32_t h = *reinterpret_cast<const unsigned short*>(src + ko[e]);
-                                    wv[e >> 1] |= (e & 1) ? (h << 16) : h;
-                                } else {
-                                    wv[e] = *reinterpret_cast<const uint32_t*>(src + ko[e]);
-                                }
-                            }
-                        }
+                    for (int e = 0; e < KQ; ++e)
+                        if (e >= kvalid) v[e] = 0;
+                }
+                if constexpr (Tr::split) {
+                    uint32_t hi[8], lo[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        // lo is left unrounded: the MMA reads its tf32 bits (|lo| <= 2^-11 |v|).
+                        const float f = __uint_as_float(v[e]);
+                        const float h = to_tf32(f);
+                        hi[e] = __float_as_uint(h);
+                        lo[e] = __float_as_uint(f - h);
                     }
-                    put_raw_unit<T, SWZ>(op, op + b_half, bdst[i], make_uint4(wv[0], wv[1], wv[2], wv[3]));
+                    tmem_st8(col, hi);
+                    tmem_st8(col + Tr::KC, lo);
+                } else {
+                    uint32_t wv[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) wv[e] = __byte_perm(v[2 * e], v[2 * e + 1], 0x5410);
+                    tmem_st8(col, wv);
                 }
-                fence_proxy_async_smem();
+                tmem_st_wait();
+                tc_fence_before();
                 __syncwarp();
+                const bool sc_end = (++xc == geo.xg) || kc == geo.nchunks - 1;
                 if (lane == 0) {
-                    mbar_arrive(smem_u32(&bars->b_full[st]));
-                    if (kc % geo.xg == geo.xg - 1 || kc == geo.nchunks - 1)
-                        mbar_arrive(smem_u32(&bars->raw_empty[xq % FV_RAWS]));
+                    mbar_arrive(smem_u32(&bars->a_full[ap.i]));
+                    if (sc_end) mbar_arrive(smem_u32(&bars->raw_empty[rp.i]));
                 }
-                if (kc % geo.xg == geo.xg - 1 || kc == geo.nchunks - 1) ++xq;
+                if (sc_end) {
+                    xc = 0;
+                    rp.next(FV_RAWS);
+                }
             }
             if (!ok) break;
-            // Epilogue: TMEM -> y.
+            // Epilogue: TMEM -> y; this warp's lanes, every FA_KSPLIT-th group of 8 channels.
             if (!mbar_wait_or_abort(smem_u32(&bars->acc_full), t & 1, abort_flag)) {
                 report(const_cast<int*>(abort_flag), 2u);
                 break;
             }
             tc_fence_after();
-            const int qd = warp & 3, hcols = NT >> 1, c0 = (fw >> 2) * hcols;
-            const int oc = oc0 + qd * 32 + lane;
-            for (int cb = 0; cb < hcols; cb += 8) {
+            T* yc = nullptr;
+            if (n < p.N) yc = y + col_out(p, n);
+            for (int cb = sub * 8; cb < geo.OTp; cb += 8 * FA_KSPLIT) {
                 uint32_t r[8];
-                tmem_ld8(tmem + (uint32_t(qd * 32) << 16) + uint32_t(c0 + cb), r);
-                tmem_ld_wait();
-                if (oc < p.OC) {
+                tmem_ld8(tmem + lane_bits + uint32_t(cb), r);
+                if constexpr (Tr::split) {
+                    uint32_t r2[8];
+                    tmem_ld8(tmem + lane_bits + uint32_t(geo.OTp + cb), r2);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(r2[e]));
+                } else {
+                    tmem_ld_wait();
+                }
+                if (yc) {
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        const int n = n0 + c0 + cb + e;
-                        if (n < p.N) {
-                            float v = __uint_as_float(r[e]);
-                            if (RELU) v = v > 0.f ? v : 0.f;
-                            Elem<T>::st(y + col_out(p, n) + size_t(oc) * p.P, v);
+                        const int oc = ot * geo.OTp + cb + e;
+                        if (oc < p.OC) {
+                            float f = __uint_as_float(r[e]);
+                            if (RELU) f = f > 0.f ? f : 0.f;
+                            Elem<T>::st(yc + size_t(oc) * p.P, f);
                         }
                     }
                 }
             }
             tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty));
         }
     }
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, geo.tmem_cols);
+        tmem_dealloc(tmem, FA_TMEM_COLS);
     }
 }
 
@@ -773,20 +728,6 @@ inline int wgrad_v3_smem(const TcWgradGeom& g)
     return 1024 + FV_OPS * g.op_bytes + g.raws * g.raw_bytes + g.NT * 4 + int(sizeof(WgBars)) + 16;
 }
 
-// Distribute 16-byte cp.async copies of the global byte range [off, off + bytes) of
-// `base` (rounded out to 16-byte blocks) over threads t, t + nthr, ...; the first block
-// lands at shared address dst.  Blocks are zero-filled past `end`.
-__device__ __forceinline__ void copy_range(uint32_t dst, const unsigned char* base, size_t off, int bytes,
-                                           const unsigned char* end, int t, int nthr)
-{
-    const size_t a = off & ~size_t(15);
-    const int nb = int((off + size_t(bytes) - a + 15) >> 4);
-    for (int i = t; i < nb; i += nthr) {
-        const unsigned char* src = base + a + size_t(i) * 16;
-        const long left = long(end - src);
-        cp_async16(dst + i * 16, src, uint32_t(left < 16 ? left : 16));
-    }
-}
 
 template <typename T, bool RELU, int SWZ>
 __global__ void __launch_bounds__(FV_THREADS, 1)
@@ -1520,27 +1461,15 @@ int tc_swizzle_mode()
 template <typename T>
 static bool pick_fwd(const ConvParams& p, const DevInfo& d, FwdGeom& out)
 {
-    bool found = false;
-    long best = 0;
-    const int oct = ceil_div(p.OC, TC_M);
-    // Per NT: the deepest weight ring (then gathered stages, then super-chunk) that fits.
-    static const int cfgs[][3] = {{6, 3, 4}, {6, 2, 4}, {4, 3, 4}, {4, 2, 4}, {4, 2, 2}, {3, 2, 2},
-                                  {3, 2, 1}, {2, 2, 1}};
-    for (int nt = 16; nt <= 256; nt += 16) {
-        for (const auto& c : cfgs) {
-            const FwdGeom g = fwd_geom<T>(p, nt, c[2], c[0], c[1]);
-            if (fwd_smem<T>(p, g) > d.smem_optin || fwd_packed_bytes<T>(g) > kScratchBytes) continue;
-            const long tiles = long(ceil_div(p.N, nt)) * oct;
-            const long cost = ((tiles + d.sms - 1) / d.sms) * (nt + 64) * (16 - c[0]);
-            if (!found || cost < best) {
-                best = cost;
-                out = g;
-                found = true;
-            }
-            break;
-        }
+    // The deepest weight ring, then the longest x super-chunk, that fits.
+    static const int cfgs[][2] = {{4, 4}, {4, 2}, {3, 4}, {3, 2}, {2, 2}, {2, 1}};
+    for (const auto& c : cfgs) {
+        const FwdGeom g = fwd_geom<T>(p, c[1], c[0]);
+        if (g.na < 2 || fwd_smem<T>(p, g) > d.smem_optin || fwd_packed_bytes<T>(g) > kScratchBytes) continue;
+        out = g;
+        return true;
     }
-    return found;
+    return false;
 }
 
 bool tc_fwd_ok(const ConvParams& p, int dt, const DevInfo& d)
@@ -1558,8 +1487,8 @@ Plan plan_fwd_tc(const ConvParams& p, int dt, const DevInfo& d)
     Plan pl;
     pl.algo = ALGO_TC;
     pl.launches = 2;  // weight packing, then the implicit GEMM
-    pl.block = FV_THREADS;
-    pl.variant = ((g.NT * 8 + g.xg) * 16 + g.na) * 8 + g.nbs;
+    pl.block = FA_THREADS;
+    pl.variant = g.xg * 16 + g.nw;
     pl.grid = std::min(g.n_tiles * g.oc_tiles, d.sms);
     pl.smem = dt == DT_BF16 ? fwd_smem<__nv_bfloat16>(p, g) : fwd_smem<float>(p, g);
     return pl;
@@ -1570,29 +1499,25 @@ static cudaError_t fwd_tc_t(const Plan& pl, const ConvParams& p, const void* x, 
                             cudaStream_t s)
 {
     const int v = pl.variant;
-    const FwdGeom g = fwd_geom<T>(p, (v / 8 / 16) / 8, (v / 8 / 16) % 8, (v / 8) % 16, v % 8);
+    const FwdGeom g = fwd_geom<T>(p, v / 16, v % 16);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     unsigned char* wpack = static_cast<unsigned char*>(stream_scratch(dev, s));
     if (!wpack) return cudaErrorMemoryAllocation;
-    const size_t units = size_t(g.oc_tiles) * g.nchunks * TC_M * 8;
+    const size_t units = size_t(g.oc_tiles) * g.nchunks * g.OTp * 8;
     const int pgrid = int(std::min<size_t>((units + 255) / 256, 4096));
-    pack_fwd_w_kernel<T><<<pgrid, 256, 0, s>>>(p, (const T*)w, wpack, g.nchunks, g.oc_tiles);
+    pack_fwd_w_kernel<T><<<pgrid, 256, 0, s>>>(p, (const T*)w, wpack, g.nchunks, g.oc_tiles, g.OTp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const bool swz = tc_swizzle_mode() != 0;
-#define IG_LAUNCH_FWD_TC(R, Z)                                                                      \
+    // The weight operand is always in the 128-byte swizzled layout the pack kernel writes.
+#define IG_LAUNCH_FWD_TC(R)                                                                         \
     do {                                                                                            \
-        e = ensure_smem<fwd_tc_kernel<T, R, Z>>(pl.smem);                                           \
+        e = ensure_smem<fwd_tc_kernel<T, R, 1>>(pl.smem);                                           \
         if (e == cudaSuccess)                                                                       \
-            fwd_tc_kernel<T, R, Z><<<pl.grid, pl.block, pl.smem, s>>>(p, (const T*)x, wpack,       \
-                                                                      (T*)y, g);                    \
+            fwd_tc_kernel<T, R, 1><<<pl.grid, pl.block, pl.smem, s>>>(p, (const T*)x, wpack, (T*)y, g); \
     } while (0)
-    if (p.relu) {
-        if (swz) IG_LAUNCH_FWD_TC(true, 1); else IG_LAUNCH_FWD_TC(true, 0);
-    } else {
-        if (swz) IG_LAUNCH_FWD_TC(false, 1); else IG_LAUNCH_FWD_TC(false, 0);
-    }
+    if (p.relu) IG_LAUNCH_FWD_TC(true);
+    else IG_LAUNCH_FWD_TC(false);
 #undef IG_LAUNCH_FWD_TC
     return e != cudaSuccess ? e : cudaGetLastError();
 }

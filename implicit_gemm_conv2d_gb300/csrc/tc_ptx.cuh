@@ -67,6 +67,27 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t tx)
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(tx) : "memory");
 }
 
+// ---- shared-memory loads by 32-bit shared-window address ---------------------------------
+// volatile: kept in program order with the mbarrier waits that publish the data.
+__device__ __forceinline__ uint32_t lds32(uint32_t a)
+{
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t a)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ int4 lds128(uint32_t a)
+{
+    int4 v;
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+
 // ---- bulk asynchronous copy (TMA engine, no tensor map) ---------------------------------
 // Copy `bytes` (multiple of 16) from global `src` (16-byte aligned) to shared `dst`
 // (16-byte aligned); completion is signalled as transaction bytes on `bar`.
@@ -139,6 +160,29 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// Same two kinds with the A operand read from tensor memory: `a_tmem` addresses
+// lane 0 of a 128-lane block whose lane m holds row m of A, K along the columns
+// (one tf32 per 32-bit column; two bf16 per column, the even k in the low half).
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_tf32_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 // Arrive once on the mbarrier when every MMA this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar)
 {
@@ -158,6 +202,17 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8])
                  : "memory");
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ---- registers -> TMEM -------------------------------------------------------------------
+// Lane i of warp w writes row 32*(w%4)+i, 8 consecutive 32-bit columns from the address's column.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
+                 "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+// Wait until this thread's tcgen05.st writes are done.
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ---- descriptors ---------------------------------------------------------------------------
 // Shared-memory matrix descriptor, no swizzle, K-major: the operand is stored as
@@ -184,12 +239,16 @@ __host__ __device__ constexpr uint32_t instr_desc(uint32_t fmt, uint32_t M, uint
            | ((M >> 4) << 24);     // M / 16
 }
 
-// fp32 -> tf32 (round to nearest, ties away from zero), kept in an fp32 register.
+// fp32 -> tf32 (10 explicit mantissa bits), kept in an fp32 register: the magnitude
+// is rounded to nearest, ties away from zero, by adding half a unit of the last kept
+// bit (bit 13) to the encoding and clearing the 13 dropped bits; in sign-magnitude
+// form a carry out of the mantissa raises the exponent exactly as rounding the
+// magnitude up does, and Inf stays Inf.  Two integer operations.  (A NaN whose
+// payload lies only in the dropped bits becomes Inf here; the split v = hi + lo
+// below still carries it, as lo = v - hi is then NaN.)
 __device__ __forceinline__ float to_tf32(float v)
 {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
-    return __uint_as_float(r);
+    return __uint_as_float((__float_as_uint(v) + 0x1000u) & 0xFFFFE000u);
 }
 
 }  // namespace tc
