@@ -35,13 +35,6 @@ using namespace tc;
 constexpr int TC_M = 128;
 constexpr int ROWB = 128;  // bytes of one operand row per K-chunk
 
-inline int pow2_at_least(int v)
-{
-    int c = 32;
-    while (c < v) c <<= 1;
-    return c;
-}
-
 template <typename T> struct TcTraits;
 template <> struct TcTraits<__nv_bfloat16> {
     static constexpr int E = 8;        // elements per 16-byte unit
@@ -151,8 +144,8 @@ __device__ __forceinline__ unsigned char* align1024(unsigned char* p)
 // 128-byte swizzled, K-major; fp32 as tf32 hi rows followed by lo rows), so that the
 // main kernel fetches each chunk with one large bulk copy.
 //   forward: tile (ot, kc) holds W[r][kk] = w[ot*OTp + r][kc*KC + kk], OTp rows
-//   d_input: tile (kt, ch) holds A[r][kk] = w[ch*KC + kk][k0(kt) + r] (W transposed), rows
-//            r < CIC*K*K of input-channel chunk kt
+//   d_input: tile (kt, ch) holds W^T[r][kk] = w[ch*KC + kk][k0(kt) + r] (W transposed),
+//            KTp rows, r < CIC*K*K of input-channel chunk kt
 // ======================================================================================
 template <typename T>
 __global__ void pack_fwd_w_kernel(const ConvParams p, const T* __restrict__ w, unsigned char* __restrict__ out,
@@ -179,12 +172,12 @@ __global__ void pack_fwd_w_kernel(const ConvParams p, const T* __restrict__ w, u
 
 template <typename T>
 __global__ void pack_dgrad_w_kernel(const ConvParams p, const T* __restrict__ w, unsigned char* __restrict__ out,
-                                    int nkt, int nch, int CIC)
+                                    int nkt, int nch, int CIC, int KTp)
 {
     using Tr = TcTraits<T>;
-    const int tile_units = TC_M * 8;
+    const int tile_units = KTp * 8;
     const size_t total = size_t(nkt) * nch * tile_units;
-    const size_t tb = size_t(TC_M) * ROWB * (Tr::split ? 2 : 1);
+    const size_t tb = size_t(KTp) * ROWB * (Tr::split ? 2 : 1);
     for (size_t u = blockIdx.x * size_t(blockDim.x) + threadIdx.x; u < total; u += size_t(gridDim.x) * blockDim.x) {
         const int within = int(u % tile_units);
         const size_t t = u / tile_units;
@@ -198,7 +191,7 @@ __global__ void pack_dgrad_w_kernel(const ConvParams p, const T* __restrict__ w,
             v[i] = (r < mrows && oc < p.OC) ? Elem<T>::ldg(w + size_t(oc) * p.Kred + k0 + r) : 0.f;
         }
         unsigned char* base = out + t * tb;
-        put_unit<T, 1>(base, base + TC_M * ROWB, r, c, v);
+        put_unit<T, 1>(base, base + KTp * ROWB, r, c, v);
     }
 }
 
@@ -226,10 +219,8 @@ __global__ void pack_dgrad_w_kernel(const ConvParams p, const T* __restrict__ w,
 //               raw slot and writes them with tcgen05.st; then the tile's epilogue
 //               (TMEM -> ReLU -> y), each warp a quarter of the output channels.
 // ======================================================================================
-constexpr int FV_THREADS = 352;
 constexpr int FV_MMA_WARP = 2;
 constexpr int FV_FMT0 = 96;   // first formatter thread (warp 3)
-constexpr int FV_OPS = 2;
 constexpr int FV_RAWS = 2;
 
 constexpr int FA_TM = 128;    // columns per forward tile (TMEM lanes)
@@ -666,105 +657,142 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
 }
 
 // ======================================================================================
-// wgrad partials: tile = (128 output channels, NT reduction indices k, one split range of
+// wgrad partials: tile = (128 output channels, KTp reduction indices k, one split range of
 // samples); the GEMM's K runs over the split's columns n = (b, oh, ow), a chunk being NSC
-// whole samples (NSC*P <= KC columns, the rest zero):
-//   D[oc, k] = sum_{n in split} g[oc, n] * X[k, n]
-// Same warp roles as the forward kernel.  Per chunk the copy warps bring, for each of
-// the chunk's samples, the contiguous slabs dy[b, oc0 : oc0+128, :], y[b, oc0 : ..] (ReLU
-// mask source) and x[b, ic_lo : ic_hi] (the k-tile's input channels); the formatters
-// build A (g = dy * [y > 0] along n per oc) and B (patches along n per k).  The
-// epilogue stores the fp32 tile to ws[split][oc][k] (row stride kpad).
+// whole samples (NSC*P columns, zero-padded to the MMA step):
+//   D[oc, k] = sum_{n in split} G[n, oc] * X[n, k]
+// G (dy masked by y > 0) is the MMA's A operand in tensor memory (lane = output channel,
+// K = n along the columns); X (the patches) is the shared-memory B operand (N = KTp rows
+// of k, K-major along n; fp32 as tf32 hi rows then lo rows, so one N = 2*KTp MMA forms
+// G_hi*X_hi and G_hi*X_lo and an N = KTp MMA adds G_lo*X_hi).
+// Warp roles (608 threads):
+//   warp 0      bulk-copy producer: per chunk, the contiguous slabs dy[b, oc0 : oc0+128, :],
+//               y[...] (ReLU mask source) and x[b, ic_lo : ic_hi] (the k-tile's input
+//               channels) of the chunk's samples into a raw slot.
+//   warp 2      MMA.
+//   warps 3-6   G formatters: lane = output channel; the chunk's columns, masked and split,
+//               into a TMEM operand stage with tcgen05.st.
+//   warps 7-18  X formatters: 16-byte units (row k, 4 or 8 columns) of the B stage.
+//   warps 3-18  epilogue: the fp32 tile to ws[split][oc][k] (row stride kpad).
+//   warp 1      idle.
 // ======================================================================================
+constexpr int WG_THREADS = FV_FMT0 + 32 * 16;
+constexpr int WG_XTHREADS = 32 * 12;   // X formatter threads
+constexpr int WG_MAXA = 8, WG_MAXB = 4, WG_MAXR = 3;
+// Rows of the B stage one X-formatter thread builds at most (its k offsets stay in registers).
+template <typename T> struct WgRows { static constexpr int value = TcTraits<T>::split ? 4 : 8; };
+
 struct TcWgradGeom {
-    int NT;        // k per tile (multiple of 16, <= 128)
-    int k_tiles;   // ceil(Kred / NT)
+    int KTp;       // k rows per tile (multiple of 32): <= 128 (fp32), <= 256 (bf16)
+    int k_tiles;   // ceil(Kred / KTp)
     int oc_tiles;  // ceil(OC / 128)
     int splits;    // sample ranges
     int kpad;      // workspace row stride (Kred rounded up to 4)
-    int tmem_cols;
     int nsc;       // samples per chunk
+    int cnp;       // columns per chunk, padded to the MMA K-step
     int raws;      // raw slots
     int gs;        // bytes per sample of a dy (or y) slab in a raw slot
     int xsb;       // bytes per sample of the x channels in a raw slot
     int raw_bytes;
-    int op_bytes;
+    int b_bytes;   // one B stage: KTp rows x 128 bytes (x2 for split fp32)
+    int nbs;       // B stages
+    int dcols;     // accumulator columns
+    int acols, na; // TMEM columns per A stage, A stages
 };
 
 struct WgBars {
-    uint64_t raw_full[3], raw_empty[3], op_full[FV_OPS], op_empty[FV_OPS], acc_full;
+    uint64_t raw_full[WG_MAXR], raw_empty[WG_MAXR], a_full[WG_MAXA], a_empty[WG_MAXA];
+    uint64_t b_full[WG_MAXB], b_empty[WG_MAXB], acc_full, acc_empty;
     uint32_t tslot;
     int abort_flag;
 };
 
+// Samples per chunk: as many whole samples as fit in one 128-byte operand row, reduced
+// while that keeps nsc*P a multiple of the MMA K-step (no zero padding), else padded.
+inline int wgrad_nsc(int P, int KC, int ks)
+{
+    const int top = std::max(1, KC / P);
+    for (int m = top; m >= 1; --m)
+        if ((m * P) % ks == 0) return m;
+    return top;
+}
+
 template <typename T>
-inline TcWgradGeom wgrad_v3_geom(const ConvParams& p, int NT, int raws, int splits)
+inline TcWgradGeom wgrad_geom(const ConvParams& p, int KTp, int raws, int nbs, int splits)
 {
     using Tr = TcTraits<T>;
     const int es = int(sizeof(T));
+    const int ks = Tr::KC / 4;  // columns per MMA K-step
     TcWgradGeom g;
-    g.NT = NT;
-    g.k_tiles = ceil_div(p.Kred, NT);
+    g.KTp = KTp;
+    g.k_tiles = ceil_div(p.Kred, KTp);
     g.oc_tiles = ceil_div(p.OC, TC_M);
     g.splits = splits;
     g.kpad = round_up(p.Kred, 4);
-    g.tmem_cols = pow2_at_least(NT);
-    g.nsc = std::max(1, Tr::KC / std::max(1, p.P));
+    g.nsc = wgrad_nsc(p.P, Tr::KC, ks);
+    g.cnp = round_up(g.nsc * p.P, ks);
     g.raws = raws;
     // Raw slot: [dy region][y region (ReLU)][x region]; dy / y hold the chunk's samples
     // back to back (one copy when one oc-tile spans all of OC, else one per sample with a
     // 16-byte-rounded stride gs); x holds each sample's k-tile channels at stride xsb.
     g.gs = round_up(std::min(p.OC, TC_M) * p.P * es + 16, 16);
-    const int chk = std::min(p.IC, (NT - 1) / p.KK + 2);
+    const int chk = std::min(p.IC, (KTp - 1) / p.KK + 2);
     g.xsb = round_up(chk * p.HW * es + 16, 16);
     g.raw_bytes = round_up(g.nsc * (g.gs * (p.relu ? 2 : 1) + g.xsb) + 32, 128);
-    g.op_bytes = (TC_M + NT) * ROWB * (Tr::split ? 2 : 1);
+    g.b_bytes = KTp * ROWB * (Tr::split ? 2 : 1);
+    g.nbs = nbs;
+    g.dcols = KTp * (Tr::split ? 2 : 1);
+    g.acols = Tr::split ? 2 * Tr::KC : Tr::KC / 2;
+    g.na = std::min(WG_MAXA, (512 - round_up(g.dcols, 32)) / g.acols);
     return g;
 }
 
 template <typename T>
-inline int wgrad_v3_smem(const TcWgradGeom& g)
+inline int wgrad_smem(const TcWgradGeom& g)
 {
-    return 1024 + FV_OPS * g.op_bytes + g.raws * g.raw_bytes + g.NT * 4 + int(sizeof(WgBars)) + 16;
+    return 1024 + g.nbs * g.b_bytes + g.raws * g.raw_bytes + int(sizeof(WgBars)) + 16;
 }
 
-
-template <typename T, bool RELU, int SWZ>
-__global__ void __launch_bounds__(FV_THREADS, 1)
+template <typename T, bool RELU>
+__global__ void __launch_bounds__(WG_THREADS, 1)
 wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict__ dy,
                 const T* __restrict__ y, float* __restrict__ ws, const TcWgradGeom geo)
 {
     using Tr = TcTraits<T>;
     constexpr int ES = int(sizeof(T));
+    constexpr int KS = Tr::KC / 4;  // columns per MMA K-step
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = align1024(smem_raw);
-    const int NT = geo.NT;
-    unsigned char* ops = smem;
-    unsigned char* raw = ops + FV_OPS * geo.op_bytes;
-    int* offk = reinterpret_cast<int*>(raw + geo.raws * geo.raw_bytes);  // [NT], per tile
-    WgBars* bars = reinterpret_cast<WgBars*>(offk + NT);
+    const int KTp = geo.KTp;
+    unsigned char* bring = smem;
+    unsigned char* raw = bring + geo.nbs * geo.b_bytes;
+    WgBars* bars = reinterpret_cast<WgBars*>(raw + geo.raws * geo.raw_bytes);
     volatile int* abort_flag = &bars->abort_flag;
-    const uint32_t a_bytes = TC_M * ROWB;
-    const uint32_t half = (TC_M + NT) * ROWB;
     const int gregion = geo.nsc * geo.gs + 16;              // bytes of the dy (and of the y) region
     const int xoff = gregion * (RELU ? 2 : 1);              // start of the x region in a slot
     const bool gcontig = geo.oc_tiles == 1;                 // dy / y of the chunk are one range
+    const int acol0 = round_up(geo.dcols, 32);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         for (int i = 0; i < geo.raws; ++i) {
             mbar_init(smem_u32(&bars->raw_full[i]), 1);
-            mbar_init(smem_u32(&bars->raw_empty[i]), 8);
+            mbar_init(smem_u32(&bars->raw_empty[i]), 16);
         }
-        for (int i = 0; i < FV_OPS; ++i) {
-            mbar_init(smem_u32(&bars->op_full[i]), 8);
-            mbar_init(smem_u32(&bars->op_empty[i]), 1);
+        for (int i = 0; i < geo.na; ++i) {
+            mbar_init(smem_u32(&bars->a_full[i]), 4);
+            mbar_init(smem_u32(&bars->a_empty[i]), 1);
+        }
+        for (int i = 0; i < geo.nbs; ++i) {
+            mbar_init(smem_u32(&bars->b_full[i]), 12);
+            mbar_init(smem_u32(&bars->b_empty[i]), 1);
         }
         mbar_init(smem_u32(&bars->acc_full), 1);
+        mbar_init(smem_u32(&bars->acc_empty), 16);
         fence_mbar_init();
         bars->abort_flag = 0;
     }
-    if (warp == 0) tmem_alloc(smem_u32(&bars->tslot), geo.tmem_cols);
+    if (warp == 0) tmem_alloc(smem_u32(&bars->tslot), 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -780,14 +808,14 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
         TileInfo ti;
         ti.split = tile / per_split;
         const int rem = tile % per_split;
-        ti.k0 = (rem % geo.k_tiles) * NT;
+        ti.k0 = (rem % geo.k_tiles) * KTp;
         ti.oc0 = (rem / geo.k_tiles) * TC_M;
         ti.rows = min(TC_M, p.OC - ti.oc0);
         ti.s_lo = int((long long)p.B * ti.split / geo.splits);
         ti.s_hi = int((long long)p.B * (ti.split + 1) / geo.splits);
         ti.nchunks = (ti.s_hi - ti.s_lo + geo.nsc - 1) / geo.nsc;
         ti.ic_lo = ti.k0 / p.KK;
-        ti.ic_hi = min(p.IC - 1, (min(ti.k0 + NT, p.Kred) - 1) / p.KK);
+        ti.ic_hi = min(p.IC - 1, (min(ti.k0 + KTp, p.Kred) - 1) / p.KK);
         return ti;
     };
 
@@ -799,15 +827,14 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
         const unsigned char* x_end = xb + size_t(p.B) * p.IHW * ES;
         const unsigned char* g_end = gb + size_t(p.B) * p.OCP * ES;
         const unsigned char* y_end = yb + size_t(p.B) * p.OCP * ES;
-        uint32_t q = 0;
+        RingPos rp;
         for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
             const TileInfo ti = decode(tile);
             const int gbytes = ti.rows * p.P * ES;
             const int xbytes = (ti.ic_hi - ti.ic_lo + 1) * p.HW * ES;
-            for (int kc = 0; kc < ti.nchunks; ++kc, ++q) {
-                const int s = q % geo.raws;
-                const uint32_t use = q / geo.raws;
-                if (use >= 1 && !mbar_wait_or_abort(smem_u32(&bars->raw_empty[s]), (use - 1) & 1, abort_flag)) {
+            for (int kc = 0; kc < ti.nchunks; ++kc, rp.next(geo.raws)) {
+                const int s = rp.i;
+                if (rp.wrapped && !mbar_wait_or_abort(smem_u32(&bars->raw_empty[s]), rp.ph ^ 1u, abort_flag)) {
                     report(const_cast<int*>(abort_flag), 4u);
                     break;
                 }
@@ -837,10 +864,10 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
                         dst = slot + xoff + j * geo.xsb;
                     }
                 };
-                const int nw = RELU ? 2 : 1;
+                const int nwh = RELU ? 2 : 1;
                 int tx = 0;
                 for (int i = lane; i < npieces; i += 32) {
-                    for (int which = 0; which < (i < ng ? nw : 1); ++which) {
+                    for (int which = 0; which < (i < ng ? nwh : 1); ++which) {
                         const unsigned char* src;
                         unsigned char* dst;
                         int bytes;
@@ -855,7 +882,7 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
                 if (lane == 0) mbar_arrive_expect_tx(smem_u32(&bars->raw_full[s]), uint32_t(tx));
                 __syncwarp();
                 for (int i = lane; i < npieces; i += 32) {
-                    for (int which = 0; which < (i < ng ? nw : 1); ++which) {
+                    for (int which = 0; which < (i < ng ? nwh : 1); ++which) {
                         const unsigned char* src;
                         unsigned char* dst;
                         int bytes;
@@ -867,162 +894,308 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
                 }
             }
         }
-    } else if (warp == 1) {
-        // idle: the producer of this kernel is warp 0 alone
     } else if (warp == FV_MMA_WARP) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
-            const uint32_t idesc = instr_desc(Tr::fmt, TC_M, NT);
-            const uint32_t ops_u32 = smem_u32(ops);
-            uint32_t q = 0;
-            for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+            const uint32_t idesc2 = instr_desc(Tr::fmt, TC_M, geo.dcols);
+            const uint32_t idesc1 = instr_desc(Tr::fmt, TC_M, KTp);
+            const uint32_t b_u32 = smem_u32(bring);
+            const int ksteps = geo.cnp / KS;
+            RingPos ap, bp;
+            uint32_t t = 0;
+            for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x, ++t) {
                 const TileInfo ti = decode(tile);
                 bool ok = true;
-                for (int kc = 0; kc < ti.nchunks; ++kc, ++q) {
-                    const int st = q % FV_OPS;
-                    const uint32_t use = q / FV_OPS;
-                    if (!mbar_wait_or_abort(smem_u32(&bars->op_full[st]), use & 1, abort_flag)) {
+                if (t >= 1 && !mbar_wait_or_abort(smem_u32(&bars->acc_empty), (t - 1) & 1, abort_flag)) {
+                    report(const_cast<int*>(abort_flag), 8u);
+                    break;
+                }
+                tc_fence_after();
+                for (int kc = 0; kc < ti.nchunks; ++kc, ap.next(geo.na), bp.next(geo.nbs)) {
+                    if (!mbar_wait_or_abort(smem_u32(&bars->a_full[ap.i]), ap.ph, abort_flag) ||
+                        !mbar_wait_or_abort(smem_u32(&bars->b_full[bp.i]), bp.ph, abort_flag)) {
                         report(const_cast<int*>(abort_flag), 8u);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t base = ops_u32 + st * geo.op_bytes;
-                    issue_chunk<T, SWZ>(tmem, base, base + a_bytes, half, half, idesc, kc == 0);
-                    mma_commit(smem_u32(&bars->op_empty[st]));
+                    const uint32_t ba = b_u32 + bp.i * geo.b_bytes;
+                    const uint32_t aa = tmem + uint32_t(acol0 + ap.i * geo.acols);
+                    for (int j = 0; j < ksteps; ++j) {
+                        const uint64_t bd = op_desc<1>(ba + kstep_off<1>(j));
+                        const uint32_t acc = (kc == 0 && j == 0) ? 0u : 1u;
+                        if constexpr (Tr::split) {
+                            mma_tf32_ta(tmem, aa + 8 * j, bd, idesc2, acc);           // hi * [hi; lo]
+                            mma_tf32_ta(tmem, aa + Tr::KC + 8 * j, bd, idesc1, 1u);  // lo * hi
+                        } else {
+                            mma_f16_ta(tmem, aa + 8 * j, bd, idesc1, acc);
+                        }
+                    }
+                    mma_commit(smem_u32(&bars->a_empty[ap.i]));
+                    mma_commit(smem_u32(&bars->b_empty[bp.i]));
                 }
                 if (!ok) break;
                 mma_commit(smem_u32(&bars->acc_full));
             }
         }
         __syncwarp();
-    } else {
-        // ---------------- formatters + epilogue ----------------
-        const int ft = tid - FV_FMT0;
-        const int fw = warp - 3;
-        const int cfix = ft & 7;
-        // This thread's chunk columns n' = cfix*E + e -> (sample j, position pq) never change.
-        int jj[Tr::E], pq[Tr::E], po[Tr::E];
+    } else if (warp >= 3) {
+        const int fw = warp - 3;            // 0 .. 15
+        const int qd = warp & 3;            // TMEM lane quarter
+        const uint32_t lane_bits = uint32_t(qd * 32) << 16;
+        const bool grole = fw < 4;          // G formatter (one warp per lane quarter)
+        // Vector width (elements) of the G loads: P and OC*P multiples of it.
+        const int gvec = (p.P % 4 == 0) ? 4 : (p.P % 2 == 0) ? 2 : 1;
+        const int m = qd * 32 + lane;       // G: output channel within the tile
+        // X role: 16-byte unit column c (E columns) of rows rbase + i*rstep.
+        const int xt = tid - FV_FMT0 - 128;  // 0 .. 383 for the X role
+        const int upr = geo.cnp / Tr::E;     // units per row
+        const int cfix = grole ? 0 : xt % upr;
+        const int rbase = grole ? 0 : xt / upr;
+        const int rstep = WG_XTHREADS / upr;
+        const bool xact = !grole && xt < rstep * upr;
+        constexpr int XMAXR = WgRows<T>::value;  // rows per X thread (checked by the planner)
+        int po[Tr::E], jj[Tr::E];            // column offset and sample of this thread's columns
 #pragma unroll
         for (int e = 0; e < Tr::E; ++e) {
             const int n = cfix * Tr::E + e;
-            uint32_t j, r;
+            uint32_t j, r, oh, ow;
             p.dm_P.divmod(uint32_t(n), j, r);
-            jj[e] = int(j);
-            pq[e] = int(r);
-            uint32_t oh, ow;
             p.dm_OW.divmod(r, oh, ow);
-            po[e] = int(oh) * p.S * p.W + int(ow) * p.S;
+            jj[e] = n < geo.nsc * p.P ? int(j) : 1 << 20;  // padding columns: never a real sample
+            po[e] = (int(oh) * p.S * p.W + int(ow) * p.S) * ES;
         }
-        uint32_t q = 0, t = 0;
+        RingPos rp, ap, bp;
+        uint32_t t = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++t) {
             const TileInfo ti = decode(tile);
-            // k-offset table for this tile (relative to ic_lo); formatters only.
-            asm volatile("bar.sync 1, 256;" ::: "memory");
-            for (int r = ft; r < NT; r += 256) {
+            // X role: byte offsets of this thread's rows k = k0 + rbase + i*rstep (-1: past Kred).
+            int ko[XMAXR];
+#pragma unroll
+            for (int i = 0; i < XMAXR; ++i) {
+                const int r = rbase + i * rstep;
                 const int k = ti.k0 + r;
-                offk[r] = (k < p.Kred) ? k_offset(p, k) - ti.ic_lo * p.HW : -1;
+                ko[i] = (xact && r < KTp && k < p.Kred) ? (k_offset(p, k) - ti.ic_lo * p.HW) * ES : -1;
             }
-            asm volatile("bar.sync 1, 256;" ::: "memory");
             bool ok = true;
-            for (int kc = 0; kc < ti.nchunks; ++kc, ++q) {
-                const int s = q % geo.raws;
-                const int st = q % FV_OPS;
-                const uint32_t ruse = q / geo.raws, ouse = q / FV_OPS;
-                if (!mbar_wait_or_abort(smem_u32(&bars->raw_full[s]), ruse & 1, abort_flag) ||
-                    (ouse >= 1 && !mbar_wait_or_abort(smem_u32(&bars->op_empty[st]), (ouse - 1) & 1, abort_flag))) {
+            for (int kc = 0; kc < ti.nchunks; ++kc, rp.next(geo.raws)) {
+                if (!mbar_wait_or_abort(smem_u32(&bars->raw_full[rp.i]), rp.ph, abort_flag)) {
                     report(const_cast<int*>(abort_flag), 1u);
                     ok = false;
                     break;
                 }
                 const int b0 = ti.s_lo + kc * geo.nsc;
                 const int nb = min(geo.nsc, ti.s_hi - b0);
-                const unsigned char* slot = raw + s * geo.raw_bytes;
-                unsigned char* op = ops + st * geo.op_bytes;
-                // Start of each element's sample slabs in the raw slot, including the
-                // 16-byte rounding slack of its copy.
-                const unsigned char* gsrc[Tr::E];
-                const unsigned char* xsrc[Tr::E];
-                const int dg0 = int(((size_t(b0) * p.OCP + size_t(ti.oc0) * p.P) * ES) & 15);
+                const uint32_t slot = smem_u32(raw + rp.i * geo.raw_bytes);
+                if (grole) {
+                    if (ap.wrapped && !mbar_wait_or_abort(smem_u32(&bars->a_empty[ap.i]), ap.ph ^ 1u, abort_flag)) {
+                        report(const_cast<int*>(abort_flag), 1u);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // Element (sample j, channel m, position pq) of the dy region; y is gregion further.
+                    const int dg0 = int(((size_t(b0) * p.OCP + size_t(ti.oc0) * p.P) * ES) & 15);
+                    const bool live = m < ti.rows;
+                    const uint32_t col = tmem + lane_bits + uint32_t(acol0 + ap.i * geo.acols);
+                    auto gval = [&](int n) -> uint32_t {  // raw bits of G[n, oc0 + m] (0 outside)
+                        uint32_t j, pq;
+                        p.dm_P.divmod(uint32_t(n), j, pq);
+                        if (!live || int(j) >= nb || n >= geo.nsc * p.P) return 0u;
+                        uint32_t a;
+                        if (gcontig) {
+                            a = slot + uint32_t(dg0 + ((int(j) * p.OCP + m * p.P + int(pq)) * ES));
+                        } else {
+                            const size_t b = size_t(b0) + j;
+                            a = slot + uint32_t(int(j) * geo.gs + int(((b * p.OCP + size_t(ti.oc0) * p.P) * ES) & 15) +
+                                                (m * p.P + int(pq)) * ES);
+                        }
+                        if constexpr (ES == 4) {
+                            const uint32_t v = lds32(a);
+                            if (RELU && !(__uint_as_float(lds32(a + gregion)) > 0.f)) return 0u;
+                            return v;
+                        } else {
+                            const uint32_t v = lds16(a);
+                            if (RELU && !(__uint_as_float(lds16(a + gregion) << 16) > 0.f)) return 0u;
+                            return v;
+                        }
+                    };
+                    constexpr int NG = ES == 4 ? 8 : 16;  // columns per tcgen05.st of 8 words
+                    // Fast path (one dy range, P a multiple of the vector): runs of gv
+                    // consecutive positions of one sample are one vector load each.
+                    const int gv = gcontig ? gvec : 0;
+                    const uint32_t gbase = slot + uint32_t(dg0 + m * p.P * ES);
+                    auto gload = [&](int n0, uint32_t (&v)[NG]) {
+                        if (gv == 0) {
 #pragma unroll
-                for (int e = 0; e < Tr::E; ++e) {
-                    const size_t b = size_t(b0 + jj[e]);
-                    // Element (j, oc row r, p) of dy is at gsrc[e] + (r * P + p) * ES; y is gregion further.
-                    gsrc[e] = gcontig ? slot + dg0 + jj[e] * p.OCP * ES
-                                      : slot + jj[e] * geo.gs + int(((b * p.OCP + size_t(ti.oc0) * p.P) * ES) & 15);
-                    xsrc[e] = slot + xoff + jj[e] * geo.xsb + int(((b * p.IHW + size_t(ti.ic_lo) * p.HW) * ES) & 15);
-                }
-                // A: g rows (oc), 16 bytes of columns per unit.
-                for (int u = ft; u < TC_M * 8; u += 256) {
-                    const int r = u >> 3;
-                    uint32_t wv[4] = {0, 0, 0, 0};
-                    if (r < ti.rows) {
+                            for (int e = 0; e < NG; ++e) v[e] = gval(n0 + e);
+                            return;
+                        }
 #pragma unroll
-                        for (int e = 0; e < Tr::E; ++e) {
-                            if (jj[e] < nb) {
-                                const unsigned char* sj = gsrc[e];
-                                const int gi = r * p.P + pq[e];
-                                if constexpr (ES == 2) {
-                                    uint32_t h = *reinterpret_cast<const unsigned short*>(sj + gi * 2);
-                                    if (RELU) {
-                                        const float yv = __bfloat162float(
-                                            *reinterpret_cast<const __nv_bfloat16*>(sj + gregion + gi * 2));
-                                        if (!(yv > 0.f)) h = 0;
+                        for (int e = 0; e < NG; e += 4) {
+                            // 4 columns n0+e .. +3 as 4 / gv loads of gv elements (gv in 4, 2, 1)
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                if (h % gv) continue;
+                                const int n = n0 + e + h;
+                                uint32_t j, pq;
+                                p.dm_P.divmod(uint32_t(n), j, pq);
+                                const bool in = live && int(j) < nb && n < geo.nsc * p.P;
+                                const uint32_t a = gbase + uint32_t((int(j) * p.OCP + int(pq)) * ES);
+                                uint32_t d[4] = {0, 0, 0, 0}, w[4] = {0, 0, 0, 0};
+                                if (in) {
+                                    if constexpr (ES == 4) {
+                                        if (gv == 4) {
+                                            const int4 q4 = lds128(a);
+                                            d[0] = q4.x; d[1] = q4.y; d[2] = q4.z; d[3] = q4.w;
+                                            if (RELU) {
+                                                const int4 r4 = lds128(a + gregion);
+                                                w[0] = r4.x; w[1] = r4.y; w[2] = r4.z; w[3] = r4.w;
+                                            }
+                                        } else if (gv == 2) {
+                                            const uint2 q2 = lds64(a);
+                                            d[0] = q2.x; d[1] = q2.y;
+                                            if (RELU) {
+                                                const uint2 r2 = lds64(a + gregion);
+                                                w[0] = r2.x; w[1] = r2.y;
+                                            }
+                                        } else {
+                                            d[0] = lds32(a);
+                                            if (RELU) w[0] = lds32(a + gregion);
+                                        }
+                                    } else {
+                                        // bf16: gv elements = 8, 4 or 2 bytes, unpacked to one per word
+                                        if (gv == 4) {
+                                            const uint2 q2 = lds64(a);
+                                            d[0] = q2.x & 0xFFFFu; d[1] = q2.x >> 16; d[2] = q2.y & 0xFFFFu; d[3] = q2.y >> 16;
+                                            if (RELU) {
+                                                const uint2 r2 = lds64(a + gregion);
+                                                w[0] = r2.x << 16; w[1] = r2.x & 0xFFFF0000u;
+                                                w[2] = r2.y << 16; w[3] = r2.y & 0xFFFF0000u;
+                                            }
+                                        } else if (gv == 2) {
+                                            const uint32_t q = lds32(a);
+                                            d[0] = q & 0xFFFFu; d[1] = q >> 16;
+                                            if (RELU) {
+                                                const uint32_t r = lds32(a + gregion);
+                                                w[0] = r << 16; w[1] = r & 0xFFFF0000u;
+                                            }
+                                        } else {
+                                            d[0] = lds16(a);
+                                            if (RELU) w[0] = lds16(a + gregion) << 16;
+                                        }
                                     }
-                                    wv[e >> 1] |= (e & 1) ? (h << 16) : h;
-                                } else {
-                                    uint32_t v = *reinterpret_cast<const uint32_t*>(sj + gi * 4);
-                                    if (RELU && !(*reinterpret_cast<const float*>(sj + gregion + gi * 4) > 0.f)) v = 0;
-                                    wv[e] = v;
+                                }
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) {
+                                    if (u >= gv || h + u >= 4) continue;
+                                    // mask words are fp32 patterns (bf16 y in the high half)
+                                    v[e + h + u] = (!RELU || __uint_as_float(w[u]) > 0.f) ? d[u] : 0u;
                                 }
                             }
                         }
+                    };
+                    for (int n0 = 0; n0 < geo.cnp; n0 += NG) {
+                        uint32_t v[NG];
+                        gload(n0, v);
+                        if constexpr (Tr::split) {
+                            uint32_t hi[8], lo[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const float f = __uint_as_float(v[e]);
+                                const float h = to_tf32(f);
+                                hi[e] = __float_as_uint(h);
+                                lo[e] = __float_as_uint(f - h);
+                            }
+                            tmem_st8(col + uint32_t(n0), hi);
+                            tmem_st8(col + uint32_t(Tr::KC + n0), lo);
+                        } else {
+                            uint32_t wv[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) wv[e] = __byte_perm(v[2 * e], v[2 * e + 1], 0x5410);
+                            tmem_st8(col + uint32_t(n0 / 2), wv);
+                        }
                     }
-                    put_raw_unit<T, SWZ>(op, op + half, unit_off<SWZ>(r, cfix), make_uint4(wv[0], wv[1], wv[2], wv[3]));
-                }
-                // B: patch rows (k), 16 bytes of columns per unit.
-                for (int u = ft; u < NT * 8; u += 256) {
-                    const int r = u >> 3;
-                    const int ko = offk[r];
-                    uint32_t wv[4] = {0, 0, 0, 0};
-                    if (ko >= 0) {
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(smem_u32(&bars->a_full[ap.i]));
+                        mbar_arrive(smem_u32(&bars->raw_empty[rp.i]));
+                    }
+                    ap.next(geo.na);
+                } else {
+                    if (bp.wrapped && !mbar_wait_or_abort(smem_u32(&bars->b_empty[bp.i]), bp.ph ^ 1u, abort_flag)) {
+                        report(const_cast<int*>(abort_flag), 1u);
+                        ok = false;
+                        break;
+                    }
+                    unsigned char* op = bring + bp.i * geo.b_bytes;
+                    if (xact) {
+                        // Sample bases of this thread's columns in the x region (with the slack
+                        // of each sample's 16-byte-rounded copy).
+                        uint32_t xs[Tr::E];
 #pragma unroll
                         for (int e = 0; e < Tr::E; ++e) {
-                            if (jj[e] < nb) {
-                                const unsigned char* xs = xsrc[e];
-                                if constexpr (ES == 2) {
-                                    const uint32_t h = *reinterpret_cast<const unsigned short*>(xs + (ko + po[e]) * 2);
-                                    wv[e >> 1] |= (e & 1) ? (h << 16) : h;
-                                } else {
-                                    wv[e] = *reinterpret_cast<const uint32_t*>(xs + (ko + po[e]) * 4);
+                            const int j = min(jj[e], geo.nsc - 1);
+                            const size_t b = size_t(b0 + j);
+                            xs[e] = slot + uint32_t(xoff + j * geo.xsb +
+                                                    int(((b * p.IHW + size_t(ti.ic_lo) * p.HW) * ES) & 15) + po[e]);
+                        }
+#pragma unroll
+                        for (int i = 0; i < XMAXR; ++i) {
+                            const int r = rbase + i * rstep;
+                            if (r >= KTp) break;
+                            uint32_t wv[4] = {0, 0, 0, 0};
+                            if (ko[i] >= 0) {
+#pragma unroll
+                                for (int e = 0; e < Tr::E; ++e) {
+                                    if (jj[e] < nb) {
+                                        if constexpr (ES == 2) {
+                                            const uint32_t h = lds16(xs[e] + uint32_t(ko[i]));
+                                            wv[e >> 1] |= (e & 1) ? (h << 16) : h;
+                                        } else {
+                                            wv[e] = lds32(xs[e] + uint32_t(ko[i]));
+                                        }
+                                    }
                                 }
                             }
+                            put_raw_unit<T, 1>(op, op + KTp * ROWB, unit_off<1>(r, cfix),
+                                               make_uint4(wv[0], wv[1], wv[2], wv[3]));
                         }
                     }
-                    put_raw_unit<T, SWZ>(op + a_bytes, op + half + a_bytes, unit_off<SWZ>(r, cfix),
-                                         make_uint4(wv[0], wv[1], wv[2], wv[3]));
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(smem_u32(&bars->op_full[st]));
-                    mbar_arrive(smem_u32(&bars->raw_empty[s]));
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(smem_u32(&bars->b_full[bp.i]));
+                        mbar_arrive(smem_u32(&bars->raw_empty[rp.i]));
+                    }
+                    bp.next(geo.nbs);
                 }
             }
             if (!ok) break;
+            // Epilogue: D[oc][k] -> ws; this warp's lanes, a quarter of the k columns.
             if (!mbar_wait_or_abort(smem_u32(&bars->acc_full), t & 1, abort_flag)) {
                 report(const_cast<int*>(abort_flag), 2u);
                 break;
             }
             tc_fence_after();
-            const int qd = warp & 3, hcols = NT >> 1, c0 = (fw >> 2) * hcols;
-            const int oc = ti.oc0 + qd * 32 + lane;
-            for (int cb = 0; cb < hcols; cb += 8) {
+            const int oc = ti.oc0 + m;
+            const int kq = KTp / 4, c0 = (fw >> 2) * kq;
+            for (int cb = c0; cb < c0 + kq; cb += 8) {
                 uint32_t r[8];
-                tmem_ld8(tmem + (uint32_t(qd * 32) << 16) + uint32_t(c0 + cb), r);
-                tmem_ld_wait();
-                const int k = ti.k0 + c0 + cb;
-                if (oc < p.OC && k < geo.kpad) {
+                tmem_ld8(tmem + lane_bits + uint32_t(cb), r);
+                if constexpr (Tr::split) {
+                    uint32_t r2[8];
+                    tmem_ld8(tmem + lane_bits + uint32_t(KTp + cb), r2);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(r2[e]));
+                } else {
+                    tmem_ld_wait();
+                }
+                const int k = ti.k0 + cb;
+                if (oc < p.OC && m < ti.rows && k < geo.kpad) {
                     float* dst = ws + (size_t(ti.split) * p.OC + oc) * geo.kpad + k;
                     *reinterpret_cast<float4*>(dst) = make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]),
                                                                   __uint_as_float(r[2]), __uint_as_float(r[3]));
@@ -1032,75 +1205,88 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
                 }
             }
             tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty));
         }
     }
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, geo.tmem_cols);
+        tmem_dealloc(tmem, 512);
     }
 }
 
 // ======================================================================================
-// d_input:  D[k, n] = sum_oc W[oc, k] * g[oc, n]  for k in one chunk of CIC input channels
-// (M = CIC*K*K <= 128 rows, chunk kt) and n the NT columns of NS whole samples, then
-//   dx[b, ic, h, w] = sum over (oh, kh) with oh*S + kh = h, (ow, kw) with ow*S + kw = w of D
-// in a fixed order (no atomics).  Warp roles (352 threads):
-//   warp 0      g producer: per sample tile one bulk copy each of the contiguous dy and y
-//               slabs of its NS samples.
+// d_input:  D[n, k] = sum_oc G[n, oc] * W[oc, k]  for the 128 columns n of NS whole
+// samples (TMEM lanes) and k in one k-tile of CIC input channels (KTp >= CIC*K*K rows),
+// then  dx[b, ic, h, w] = sum over (oh, kh) with oh*S + kh = h, (ow, kw) with
+// ow*S + kw = w of D, in a fixed order (no atomics).  G = dy masked by y > 0 is the
+// MMA's A operand in tensor memory (K = output channels along the TMEM columns), built
+// once per sample tile; the packed W^T tiles are the shared-memory B operand.
+// Warp roles (608 threads):
 //   warp 1      w producer: packed W^T tiles (kt, oc chunk), one bulk copy each, into a ring.
-//   warp 2      MMA: per channel chunk kt, the oc-chunk MMAs into one of two TMEM
-//               accumulators (alternating), then a commit to that accumulator's barrier.
-//   warps 3-10  formatters: per sample tile, transpose and ReLU-mask the dy slab into the
-//               B operand [n][oc] (128-byte swizzled, all oc chunks; reused by every
-//               channel chunk); per channel chunk, TMEM -> Ds (fp32 [n][k] in shared
-//               memory) and the col2im gather into dx.  While they gather chunk kt the
-//               MMAs of chunk kt+1 run into the other accumulator.
+//   warp 2      MMA: per k-tile, the oc-chunk MMAs into an accumulator buffer, then a
+//               commit to that buffer's barrier (two buffers for bf16: the MMAs of k-tile
+//               kt+1 run while k-tile kt is read out).
+//   warps 3-18  formatters: per sample tile, load dy (and y) of their lane's column and
+//               a quarter of the output channels from global memory, mask, split (fp32)
+//               and store G to TMEM; per k-tile, TMEM -> Ds (fp32 [n][k] in shared
+//               memory), then the col2im gather into dx with all 512 threads.
+//   warp 0      idle after set-up.
 // ======================================================================================
-constexpr int DG_MAXA = 6;
+constexpr int DG_FMTW = 16;
+constexpr int DG_THREADS = FV_FMT0 + 32 * DG_FMTW;
+constexpr int DG_NFT = 32 * DG_FMTW;  // formatter threads
+constexpr int DG_MAXW = 6;
+constexpr int DG_TM = 128;             // columns per sample tile (TMEM lanes)
 
 struct TcDgradGeom {
-    int NS;          // samples per tile
-    int NT;          // columns per tile = round_up(NS * P, 16) <= 128
-    int CIC;         // input channels per chunk
-    int nkt;         // channel chunks
+    int NS;          // samples per tile (NS * P <= 128)
+    int CIC;         // input channels per k-tile
+    int KTp;         // k rows per k-tile: CIC*K*K rounded up to 32
+    int nkt;         // k-tiles
     int nch;         // K-chunks over OC
     int rmax;        // max (oh, kh) pairs per input row = ceil(K / S)
-    int acc_cols;    // TMEM columns per accumulator (power of two >= NT)
-    int na;          // weight-tile ring slots
-    int a_tile;      // bytes of one packed weight tile (16 KB, 32 KB for split fp32)
-    int b_chunk;     // bytes of one B chunk (hi part): NT * 128
-    int b_bytes;     // all B chunks, hi (+ lo)
-    int slab_bytes;  // bytes of one raw slab region (dy or y): NS samples + 16 slack, rounded
-    int ntiles;      // ceil(B / NS)
     int taps;        // max (kh, kw) taps landing on one input pixel
+    int nw;          // weight ring stages
+    int w_tile;      // bytes of one packed tile: KTp rows x 128 (x2 for split fp32)
+    int dcols;       // accumulator columns per buffer: KTp (x2 for split fp32)
+    int ndb;         // accumulator buffers
+    int acol0;       // first TMEM column of the G buffers
+    int acols;       // TMEM columns of one G buffer
+    int nab;         // G buffers
+    int ntiles;      // ceil(B / NS)
 };
 
 struct DgBars {
-    uint64_t raw_full, raw_empty, b_full, a_full[DG_MAXA], a_empty[DG_MAXA], acc_full[2], acc_empty[2];
+    uint64_t w_full[DG_MAXW], w_empty[DG_MAXW], a_full[2], a_empty[2], acc_full[2], acc_empty[2];
+    uint64_t fbar;  // formatter-warp barrier (Ds written / Ds read)
     uint32_t tslot;
     int abort_flag;
 };
 
 template <typename T>
-inline TcDgradGeom dgrad_geom_ns(const ConvParams& p, int NS, int na)
+inline TcDgradGeom dgrad_geom(const ConvParams& p, int CIC, int nw)
 {
     using Tr = TcTraits<T>;
-    const int es = int(sizeof(T));
     TcDgradGeom g;
-    g.NS = NS;
-    g.NT = std::max(16, round_up(NS * p.P, 16));
-    g.CIC = std::max(1, TC_M / p.KK);
-    g.nkt = ceil_div(p.IC, g.CIC);
+    g.NS = std::max(1, DG_TM / p.P);
+    g.CIC = CIC;
+    g.KTp = round_up(CIC * p.KK, 32);
+    g.nkt = ceil_div(p.IC, CIC);
     g.nch = ceil_div(p.OC, Tr::KC);
     g.rmax = (p.K + p.S - 1) / p.S;
-    g.acc_cols = pow2_at_least(g.NT);
-    g.na = na;
-    g.a_tile = TC_M * ROWB * (Tr::split ? 2 : 1);
-    g.b_chunk = g.NT * ROWB;
-    g.b_bytes = g.nch * g.b_chunk * (Tr::split ? 2 : 1);
-    g.slab_bytes = round_up(NS * p.OCP * es + 32, 128);
-    g.ntiles = ceil_div(p.B, NS);
+    g.nw = nw;
+    g.w_tile = g.KTp * ROWB * (Tr::split ? 2 : 1);
+    g.dcols = g.KTp * (Tr::split ? 2 : 1);
+    g.acols = Tr::split ? 2 * g.nch * Tr::KC : g.nch * Tr::KC / 2;
+    // Two accumulator and two G buffers when they fit in the 512 TMEM columns.
+    g.ndb = 2;
+    g.nab = 2;
+    if (2 * g.dcols + 2 * g.acols > 512) g.nab = 1;
+    if (2 * g.dcols + g.acols > 512) g.ndb = 1;
+    g.acol0 = g.ndb * g.dcols;
+    g.ntiles = ceil_div(p.B, g.NS);
     auto axis_max = [](int n, int K, int S, int O) {
         int m = 0;
         for (int h = 0; h < n; ++h) {
@@ -1114,50 +1300,45 @@ inline TcDgradGeom dgrad_geom_ns(const ConvParams& p, int NS, int na)
     return g;
 }
 
-constexpr int DG_DSTR = TC_M + 1;  // Ds row stride (floats): spreads the gather over banks
-constexpr int DG_TMAX = 4;         // taps per input pixel handled by the fast gather
-constexpr int DG_PROW = 8;         // ints per pixel row of the tap table (32 bytes, int4-aligned)
+constexpr int DG_DSTR = DG_TM + 4;  // Ds row stride (floats): 16-byte rows, 4 banks apart
+constexpr int DG_TMAX = 4;          // taps per input pixel handled by the fast gather
+constexpr int DG_PROW = 8;          // ints per pixel row of the tap table (32 bytes, int4-aligned)
 
 template <typename T>
 inline int dgrad_smem(const ConvParams& p, const TcDgradGeom& g)
 {
-    return 1024 + g.na * g.a_tile + g.b_bytes + (p.relu ? 2 : 1) * g.slab_bytes + g.NT * DG_DSTR * 4 +
-           (p.H + p.W) * (1 + g.rmax) * 8 + 16 + p.HW * DG_PROW * 4 + int(sizeof(DgBars)) + 16;
+    return 1024 + g.nw * g.w_tile + DG_TM * DG_DSTR * 4 + 16 + (p.H + p.W) * (1 + g.rmax) * 8 + 16 +
+           p.HW * DG_PROW * 4 + int(sizeof(DgBars)) + 16;
 }
 
 template <typename T>
 inline size_t dgrad_packed_bytes(const TcDgradGeom& g)
 {
-    return size_t(g.nkt) * g.nch * g.a_tile;
+    return size_t(g.nkt) * g.nch * g.w_tile;
 }
 
 template <typename T, bool RELU, int SWZ>
-__global__ void __launch_bounds__(FV_THREADS, 1)
+__global__ void __launch_bounds__(DG_THREADS, 1)
 dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const unsigned char* __restrict__ wpack,
                 const T* __restrict__ y, T* __restrict__ dx, const TcDgradGeom geo)
 {
     using Tr = TcTraits<T>;
-    constexpr int ES = int(sizeof(T));
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = align1024(smem_raw);
-    const int NT = geo.NT;
-    unsigned char* aring = smem;
-    unsigned char* bt = aring + geo.na * geo.a_tile;              // B chunks (hi), then lo
-    unsigned char* rdy = bt + geo.b_bytes;                         // raw dy slab
-    unsigned char* ry = rdy + geo.slab_bytes;                      // raw y slab (ReLU only)
-    float* Ds = reinterpret_cast<float*>(ry + (RELU ? geo.slab_bytes : 0));
+    unsigned char* wring = smem;
+    float* Ds = reinterpret_cast<float*>(wring + geo.nw * geo.w_tile);
     const int R1 = 1 + geo.rmax;
-    int2* rtab = reinterpret_cast<int2*>(Ds + NT * DG_DSTR);
+    int2* rtab = reinterpret_cast<int2*>(Ds + DG_TM * DG_DSTR + 4);  // 4 floats: the zero word
     int2* ctab = rtab + p.H * R1;
     // Per input pixel hw: its contributing (p, kh*K + kw) as Ds offsets p*DSTR + kh*K + kw,
     // then the count (only used when every pixel has <= DG_TMAX taps).
     int* ptab = reinterpret_cast<int*>((reinterpret_cast<uintptr_t>(ctab + p.W * R1) + 15) & ~uintptr_t(15));
     DgBars* bars = reinterpret_cast<DgBars*>(ptab + p.HW * DG_PROW);
     volatile int* abort_flag = &bars->abort_flag;
-    const uint32_t b_lo = uint32_t(geo.nch * geo.b_chunk);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    for (int h = tid; h < p.H; h += FV_THREADS) {
+    if (tid < 4) Ds[DG_TM * DG_DSTR + tid] = 0.f;
+    for (int h = tid; h < p.H; h += DG_THREADS) {
         int n = 0;
         for (int oh = 0; oh < p.OH; ++oh) {
             const int kh = h - oh * p.S;
@@ -1165,7 +1346,7 @@ dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const unsigned cha
         }
         rtab[h * R1] = make_int2(n, 0);
     }
-    for (int c = tid; c < p.W; c += FV_THREADS) {
+    for (int c = tid; c < p.W; c += DG_THREADS) {
         int n = 0;
         for (int ow = 0; ow < p.OW; ++ow) {
             const int kw = c - ow * p.S;
@@ -1176,7 +1357,7 @@ dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const unsigned cha
     const bool fast_taps = geo.taps <= DG_TMAX;
     __syncthreads();  // rtab / ctab complete
     if (fast_taps) {
-        for (int hw = tid; hw < p.HW; hw += FV_THREADS) {
+        for (int hw = tid; hw < p.HW; hw += DG_THREADS) {
             const int h = hw / p.W, ww = hw % p.W;
             const int2* rr = rtab + h * R1;
             const int2* cc = ctab + ww * R1;
@@ -1189,218 +1370,263 @@ dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const unsigned cha
         }
     }
     if (tid == 0) {
-        mbar_init(smem_u32(&bars->raw_full), 1);
-        mbar_init(smem_u32(&bars->raw_empty), 8);
-        mbar_init(smem_u32(&bars->b_full), 8);
-        for (int i = 0; i < geo.na; ++i) {
-            mbar_init(smem_u32(&bars->a_full[i]), 1);
-            mbar_init(smem_u32(&bars->a_empty[i]), 1);
+        for (int i = 0; i < geo.nw; ++i) {
+            mbar_init(smem_u32(&bars->w_full[i]), 1);
+            mbar_init(smem_u32(&bars->w_empty[i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&bars->a_full[i]), DG_FMTW);
+            mbar_init(smem_u32(&bars->a_empty[i]), 1);
             mbar_init(smem_u32(&bars->acc_full[i]), 1);
-            mbar_init(smem_u32(&bars->acc_empty[i]), 8);
+            mbar_init(smem_u32(&bars->acc_empty[i]), DG_FMTW);
         }
+        mbar_init(smem_u32(&bars->fbar), DG_FMTW);
         fence_mbar_init();
         bars->abort_flag = 0;
     }
-    if (warp == 0) tmem_alloc(smem_u32(&bars->tslot), 2 * geo.acc_cols);
+    if (warp == 0) tmem_alloc(smem_u32(&bars->tslot), 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tslot;
 
-    if (warp == 0) {
-        // ---------------- g producer ----------------
-        if (lane == 0) {
-            const unsigned char* gb = reinterpret_cast<const unsigned char*>(dy);
-            const unsigned char* yb = reinterpret_cast<const unsigned char*>(y);
-            const size_t tensor_bytes = size_t(p.B) * p.OCP * ES;
-            uint32_t tl = 0;
-            for (int tile = blockIdx.x; tile < geo.ntiles && !*abort_flag; tile += gridDim.x, ++tl) {
-                if (tl >= 1 && !mbar_wait_or_abort(smem_u32(&bars->raw_empty), (tl - 1) & 1, abort_flag)) {
-                    report(const_cast<int*>(abort_flag), 4u);
-                    break;
-                }
-                const int b0 = tile * geo.NS, ns = min(geo.NS, p.B - b0);
-                const size_t off = size_t(b0) * p.OCP * ES;
-                const int d = int(off & 15);
-                const int bytes = round_up(d + ns * p.OCP * ES, 16);
-                int tx = 0;
-                const int nsl = RELU ? 2 : 1;
-                int bulk[2];
-                for (int i = 0; i < nsl; ++i) {
-                    const unsigned char* base = i == 0 ? gb : yb;
-                    unsigned char* dst = i == 0 ? rdy : ry;
-                    const unsigned char* src = base + off - d;
-                    bulk[i] = slab_bytes_bulk(src, bytes, base + tensor_bytes);
-                    for (const unsigned char* t = src + bulk[i]; t < src + bytes && t < base + tensor_bytes; ++t)
-                        dst[int(t - src)] = *t;
-                    tx += bulk[i];
-                }
-                mbar_arrive_expect_tx(smem_u32(&bars->raw_full), uint32_t(tx));
-                for (int i = 0; i < nsl; ++i)
-                    if (bulk[i] > 0)
-                        bulk_g2s(smem_u32(i == 0 ? rdy : ry), (i == 0 ? gb : yb) + off - d, uint32_t(bulk[i]),
-                                 smem_u32(&bars->raw_full));
-            }
-        }
-        __syncwarp();
-    } else if (warp == 1) {
+    if (warp == 1) {
         // ---------------- w producer ----------------
         if (lane == 0) {
-            uint32_t q = 0;
-            for (int tile = blockIdx.x; tile < geo.ntiles && !*abort_flag; tile += gridDim.x) {
-                bool ok = true;
-                for (int kt = 0; kt < geo.nkt && ok; ++kt) {
-                    for (int ch = 0; ch < geo.nch; ++ch, ++q) {
-                        const int sl = q % geo.na;
-                        const uint32_t use = q / geo.na;
-                        if (use >= 1 && !mbar_wait_or_abort(smem_u32(&bars->a_empty[sl]), (use - 1) & 1, abort_flag)) {
-                            report(const_cast<int*>(abort_flag), 16u);
-                            ok = false;
-                            break;
-                        }
-                        const uint32_t bar = smem_u32(&bars->a_full[sl]);
-                        mbar_arrive_expect_tx(bar, uint32_t(geo.a_tile));
-                        bulk_g2s(smem_u32(aring + sl * geo.a_tile), wpack + (size_t(kt) * geo.nch + ch) * geo.a_tile,
-                                 uint32_t(geo.a_tile), bar);
+            RingPos wp;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < geo.ntiles && ok && !*abort_flag; tile += gridDim.x) {
+                const unsigned char* src = wpack;
+                for (int i = 0; i < geo.nkt * geo.nch; ++i, wp.next(geo.nw), src += geo.w_tile) {
+                    if (wp.wrapped && !mbar_wait_or_abort(smem_u32(&bars->w_empty[wp.i]), wp.ph ^ 1u, abort_flag)) {
+                        report(const_cast<int*>(abort_flag), 16u);
+                        ok = false;
+                        break;
                     }
+                    const uint32_t bar = smem_u32(&bars->w_full[wp.i]);
+                    mbar_arrive_expect_tx(bar, uint32_t(geo.w_tile));
+                    bulk_g2s(smem_u32(wring + wp.i * geo.w_tile), src, uint32_t(geo.w_tile), bar);
                 }
-                if (!ok) break;
             }
         }
         __syncwarp();
     } else if (warp == FV_MMA_WARP) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
-            const uint32_t idesc = instr_desc(Tr::fmt, TC_M, NT);
-            const uint32_t a_u32 = smem_u32(aring), b_u32 = smem_u32(bt);
-            uint32_t q = 0, j = 0, tl = 0;
+            const uint32_t idesc2 = instr_desc(Tr::fmt, DG_TM, geo.dcols);
+            const uint32_t idesc1 = instr_desc(Tr::fmt, DG_TM, geo.KTp);
+            const uint32_t w_u32 = smem_u32(wring);
+            RingPos wp, abp, dbp;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < geo.ntiles && ok && !*abort_flag; tile += gridDim.x, ++tl) {
-                if (!mbar_wait_or_abort(smem_u32(&bars->b_full), tl & 1, abort_flag)) {
+            for (int tile = blockIdx.x; tile < geo.ntiles && ok && !*abort_flag; tile += gridDim.x, abp.next(geo.nab)) {
+                if (!mbar_wait_or_abort(smem_u32(&bars->a_full[abp.i]), abp.ph, abort_flag)) {
                     report(const_cast<int*>(abort_flag), 8u);
                     break;
                 }
-                for (int kt = 0; kt < geo.nkt && ok; ++kt, ++j) {
-                    const int buf = j & 1;
-                    if ((j >> 1) >= 1 &&
-                        !mbar_wait_or_abort(smem_u32(&bars->acc_empty[buf]), ((j >> 1) - 1) & 1, abort_flag)) {
+                const uint32_t ga = tmem + uint32_t(geo.acol0 + abp.i * geo.acols);
+                for (int kt = 0; kt < geo.nkt && ok; ++kt, dbp.next(geo.ndb)) {
+                    if (dbp.wrapped &&
+                        !mbar_wait_or_abort(smem_u32(&bars->acc_empty[dbp.i]), dbp.ph ^ 1u, abort_flag)) {
                         report(const_cast<int*>(abort_flag), 8u);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t acc = tmem + uint32_t(buf * geo.acc_cols);
-                    for (int ch = 0; ch < geo.nch; ++ch, ++q) {
-                        const int sl = q % geo.na;
-                        if (!mbar_wait_or_abort(smem_u32(&bars->a_full[sl]), (q / geo.na) & 1, abort_flag)) {
+                    const uint32_t acc = tmem + uint32_t(dbp.i * geo.dcols);
+                    for (int ch = 0; ch < geo.nch; ++ch, wp.next(geo.nw)) {
+                        if (!mbar_wait_or_abort(smem_u32(&bars->w_full[wp.i]), wp.ph, abort_flag)) {
                             report(const_cast<int*>(abort_flag), 8u);
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        issue_chunk<T, SWZ>(acc, a_u32 + sl * geo.a_tile, b_u32 + ch * geo.b_chunk, TC_M * ROWB,
-                                            b_lo, idesc, ch == 0);
-                        mma_commit(smem_u32(&bars->a_empty[sl]));
+                        const uint32_t wa = w_u32 + wp.i * geo.w_tile;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint64_t bd = op_desc<SWZ>(wa + kstep_off<SWZ>(j));
+                            const uint32_t first = (ch == 0 && j == 0) ? 0u : 1u;
+                            const uint32_t col = uint32_t(ch * 32 + 8 * j);  // oc columns of this step
+                            if constexpr (Tr::split) {
+                                mma_tf32_ta(acc, ga + col, bd, idesc2, first);                          // hi*[hi;lo]
+                                mma_tf32_ta(acc, ga + uint32_t(geo.nch * Tr::KC) + col, bd, idesc1, 1u);  // lo*hi
+                            } else {
+                                mma_f16_ta(acc, ga + col, bd, idesc1, first);
+                            }
+                        }
+                        mma_commit(smem_u32(&bars->w_empty[wp.i]));
                     }
                     if (!ok) break;
-                    mma_commit(smem_u32(&bars->acc_full[buf]));
+                    mma_commit(smem_u32(&bars->acc_full[dbp.i]));
                 }
+                if (!ok) break;
+                mma_commit(smem_u32(&bars->a_empty[abp.i]));
             }
         }
         __syncwarp();
-    } else {
-        // ---------------- formatters + epilogue ----------------
-        const int ft = tid - FV_FMT0;  // 0 .. 255
-        const int fw = warp - 3;       // 0 .. 7
-        const int units_per_row = geo.nch * (Tr::KC / Tr::E);  // 16-byte units of oc per column
-        uint32_t j = 0, tl = 0;
-        for (int tile = blockIdx.x; tile < geo.ntiles; tile += gridDim.x, ++tl) {
-            const int b0 = tile * geo.NS, ns = min(geo.NS, p.B - b0), ncols = ns * p.P;
-            if (!mbar_wait_or_abort(smem_u32(&bars->raw_full), tl & 1, abort_flag)) {
+    } else if (warp >= 3) {
+        // ---------------- formatters + col2im ----------------
+        const int ft = tid - FV_FMT0;       // 0 .. 511
+        const uint32_t ds_u32 = smem_u32(Ds);
+        const int fw = warp - 3;            // 0 .. 15
+        const int qd = warp & 3;            // TMEM lane quarter
+        const int sub = fw >> 2;            // quarter of the oc range (G) / of the k range (D)
+        const int m = qd * 32 + lane;       // column within the tile
+        const uint32_t lane_bits = uint32_t(qd * 32) << 16;
+        const int ocq = geo.nch * Tr::KC / 4;  // output channels per formatter warp
+        // G rows of sample tile `tile` into G buffer `ab`: dy (masked) of column m, channels
+        // [sub*ocq, (sub+1)*ocq); zeros past the batch or past OC.
+        auto build_g = [&](int tile, const RingPos& ab) -> bool {
+            if (ab.wrapped && !mbar_wait_or_abort(smem_u32(&bars->a_empty[ab.i]), ab.ph ^ 1u, abort_flag)) {
                 report(const_cast<int*>(abort_flag), 1u);
-                break;
+                return false;
             }
-            // B: unit (column n, oc group og) = E consecutive oc of g[., n]; consecutive threads
-            // take consecutive columns, so their dy reads are consecutive positions.
-            const int d = int((size_t(b0) * p.OCP * ES) & 15);
-            const unsigned char* gsl = rdy + d;
-            const unsigned char* ysl = ry + d;
-            for (int u = ft; u < NT * units_per_row; u += 256) {
-                const int n = u % NT, og = u / NT;
-                uint32_t wv[4] = {0, 0, 0, 0};
-                if (n < ncols) {
-                    uint32_t si, pq;
-                    p.dm_P.divmod(uint32_t(n), si, pq);
-                    const int base = int(si) * p.OCP + int(pq);
+            tc_fence_after();
+            const int b0 = tile * geo.NS, ns = min(geo.NS, p.B - b0);
+            const bool valid = m < ns * p.P;
+            uint32_t si = 0, pq = 0;
+            p.dm_P.divmod(uint32_t(valid ? m : 0), si, pq);
+            const size_t base = (size_t(b0) + si) * p.OCP + pq;  // si = 0, pq = 0 for invalid lanes
+            const uint32_t gcol = tmem + lane_bits + uint32_t(geo.acol0 + ab.i * geo.acols);
+            // Batches of 16 channels: every load of a batch is issued before the first use.
+            for (int o0 = sub * ocq; o0 < (sub + 1) * ocq; o0 += 16) {
+                // Unconditional loads from clamped addresses (invalid lanes and channels
+                // past OC read a valid element), zeroed afterwards.
+                float v[16], yv[16];
+                const T* dyp = dy + base;
+                const T* yp = y + base;
 #pragma unroll
-                    for (int e = 0; e < Tr::E; ++e) {
-                        const int oc = og * Tr::E + e;
-                        if (oc < p.OC) {
-                            const int gi = base + oc * p.P;
-                            if constexpr (ES == 2) {
-                                uint32_t h = *reinterpret_cast<const unsigned short*>(gsl + gi * 2);
-                                if (RELU && !(__bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(ysl + gi * 2)) > 0.f))
-                                    h = 0;
-                                wv[e >> 1] |= (e & 1) ? (h << 16) : h;
-                            } else {
-                                uint32_t v = *reinterpret_cast<const uint32_t*>(gsl + gi * 4);
-                                if (RELU && !(*reinterpret_cast<const float*>(ysl + gi * 4) > 0.f)) v = 0;
-                                wv[e] = v;
-                            }
+                for (int e = 0; e < 16; ++e) {
+                    const int oc = min(o0 + e, p.OC - 1);
+                    v[e] = Elem<T>::ldg(dyp + oc * p.P);
+                    if (RELU) yv[e] = Elem<T>::ldg(yp + oc * p.P);
+                }
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int oc = o0 + e;
+                    bool keep = valid && oc < p.OC && oc < (sub + 1) * ocq;
+                    if (RELU) keep = keep && yv[e] > 0.f;
+                    if (!keep) v[e] = 0.f;
+                }
+                const int nb = min(16, (sub + 1) * ocq - o0);  // multiple of 8 (fp32) / 16 (bf16)
+                if constexpr (Tr::split) {
+#pragma unroll
+                    for (int g8 = 0; g8 < 2; ++g8) {
+                        if (8 * g8 >= nb) break;
+                        uint32_t hi[8], lo[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float f = v[8 * g8 + e];
+                            const float h = to_tf32(f);
+                            hi[e] = __float_as_uint(h);
+                            lo[e] = __float_as_uint(f - h);
                         }
+                        tmem_st8(gcol + uint32_t(o0 + 8 * g8), hi);
+                        tmem_st8(gcol + uint32_t(geo.nch * Tr::KC + o0 + 8 * g8), lo);
+                    }
+                } else {
+#pragma unroll
+                    for (int g16 = 0; g16 < 1; ++g16) {
+                        uint32_t wv[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            wv[e] = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(v[16 * g16 + 2 * e]))) |
+                                    (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(v[16 * g16 + 2 * e + 1]))) << 16);
+                        tmem_st8(gcol + uint32_t((o0 + 16 * g16) / 2), wv);
                     }
                 }
-                const int ch = (og * Tr::E) / Tr::KC, c = ((og * Tr::E) % Tr::KC) / Tr::E;
-                unsigned char* dst = bt + ch * geo.b_chunk;
-                put_raw_unit<T, SWZ>(dst, dst + b_lo, unit_off<SWZ>(n, c), make_uint4(wv[0], wv[1], wv[2], wv[3]));
             }
-            fence_proxy_async_smem();
+            tmem_st_wait();
+            tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(smem_u32(&bars->b_full));
-                mbar_arrive(smem_u32(&bars->raw_empty));  // the slab is no longer read
-            }
-            bool ok = true;
-            for (int kt = 0; kt < geo.nkt; ++kt, ++j) {
-                const int buf = j & 1;
-                if (!mbar_wait_or_abort(smem_u32(&bars->acc_full[buf]), (j >> 1) & 1, abort_flag)) {
+            if (lane == 0) mbar_arrive(smem_u32(&bars->a_full[ab.i]));
+            return true;
+        };
+        // Barrier of the 16 formatter warps (bounded wait, unlike bar.sync).
+        uint32_t fph = 0;
+        auto fmt_sync = [&]() -> bool {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->fbar));
+            const bool done = mbar_wait_or_abort(smem_u32(&bars->fbar), fph, abort_flag);
+            fph ^= 1u;
+            if (!done) report(const_cast<int*>(abort_flag), 2u);
+            return done;
+        };
+        RingPos abp, dbp;
+        bool ok = true;
+        const int first = blockIdx.x;
+        if (first < geo.ntiles) ok = build_g(first, abp);
+        for (int tile = first; tile < geo.ntiles && ok; tile += gridDim.x) {
+            RingPos nab = abp;
+            nab.next(geo.nab);
+            const int next = tile + int(gridDim.x);
+            // With two G buffers the next tile's G is written before this tile's k-tiles
+            // are read out, so the MMAs move on to it without waiting.
+            if (geo.nab == 2 && next < geo.ntiles && !(ok = build_g(next, nab))) break;
+            const int b0 = tile * geo.NS, ns = min(geo.NS, p.B - b0);
+            for (int kt = 0; kt < geo.nkt; ++kt, dbp.next(geo.ndb)) {
+                if (!mbar_wait_or_abort(smem_u32(&bars->acc_full[dbp.i]), dbp.ph, abort_flag)) {
                     report(const_cast<int*>(abort_flag), 2u);
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const int qd = warp & 3, hcols = NT >> 1, c0 = (fw >> 2) * hcols;
-                const int m = qd * 32 + lane;
-                for (int cb = 0; cb < hcols; cb += 8) {
-                    uint32_t r[8];
-                    tmem_ld8(tmem + uint32_t(buf * geo.acc_cols) + (uint32_t(qd * 32) << 16) + uint32_t(c0 + cb), r);
-                    tmem_ld_wait();
+                // TMEM -> Ds: this warp's lanes, k columns [sub*KTp/4, (sub+1)*KTp/4) (a
+                // multiple of 8), two 8-column loads per wait, then 16-byte shared stores.
+                {
+                    const uint32_t acc = tmem + lane_bits + uint32_t(dbp.i * geo.dcols);
+                    const int kq = geo.KTp / 4, c0 = sub * kq;
+                    const uint32_t drow = ds_u32 + uint32_t((m * DG_DSTR + c0) * 4);
+                    for (int c = 0; c < kq; c += 16) {
+                        const bool two = c + 8 < kq;
+                        uint32_t r[2][8], r2[2][8];
+                        tmem_ld8(acc + uint32_t(c0 + c), r[0]);
+                        if (two) tmem_ld8(acc + uint32_t(c0 + c + 8), r[1]);
+                        if constexpr (Tr::split) {
+                            tmem_ld8(acc + uint32_t(geo.KTp + c0 + c), r2[0]);
+                            if (two) tmem_ld8(acc + uint32_t(geo.KTp + c0 + c + 8), r2[1]);
+                        }
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) Ds[(c0 + cb + e) * DG_DSTR + m] = __uint_as_float(r[e]);
+                        for (int i = 0; i < 2; ++i) {
+                            if (i == 1 && !two) break;
+                            if constexpr (Tr::split) {
+#pragma unroll
+                                for (int e = 0; e < 8; ++e)
+                                    r[i][e] = __float_as_uint(__uint_as_float(r[i][e]) + __uint_as_float(r2[i][e]));
+                            }
+                            sts128(drow + uint32_t(4 * (c + 8 * i)), r[i][0], r[i][1], r[i][2], r[i][3]);
+                            sts128(drow + uint32_t(4 * (c + 8 * i)) + 16, r[i][4], r[i][5], r[i][6], r[i][7]);
+                        }
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty[buf]));
-                asm volatile("bar.sync 1, 256;" ::: "memory");
+                if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty[dbp.i]));
+                if (!fmt_sync()) {
+                    ok = false;
+                    break;
+                }
                 const int ic0 = kt * geo.CIC, nic = min(geo.CIC, p.IC - ic0);
                 if (fast_taps) {
-                    // Thread owns pixel hw; its <= 4 tap offsets stay in registers while it
-                    // walks every (sample, channel) of the chunk.
-                    for (int hw = ft; hw < p.HW; hw += 256) {
+                    // Thread owns (pixel hw, a subset of the samples); its <= 4 tap offsets
+                    // stay in registers while it walks the chunk's channels.
+                    const int nsplit = max(1, DG_NFT / p.HW);
+                    for (int it = ft; it < p.HW * nsplit; it += DG_NFT) {
+                        const int hw = it % p.HW, part = it / p.HW;
                         const int4 o = *reinterpret_cast<const int4*>(ptab + hw * DG_PROW);
-                        for (int sI = 0; sI < ns; ++sI) {
+                        // Absent taps read the zero word kept past the Ds rows.
+                        const uint32_t zero = ds_u32 + uint32_t(DG_TM * DG_DSTR * 4);
+                        for (int sI = part; sI < ns; sI += nsplit) {
                             T* dxs = dx + size_t(b0 + sI) * p.IHW + size_t(ic0) * p.HW + hw;
-                            const float* ds = Ds + sI * p.P * DG_DSTR;
+                            const uint32_t ds = ds_u32 + uint32_t(sI * p.P * DG_DSTR * 4);
+#pragma unroll 4
                             for (int icl = 0; icl < nic; ++icl) {
-                                const float* dk = ds + icl * p.KK;
-                                float sum = 0.f;
-                                if (o.x >= 0) sum += dk[o.x];
-                                if (o.y >= 0) sum += dk[o.y];
-                                if (o.z >= 0) sum += dk[o.z];
-                                if (o.w >= 0) sum += dk[o.w];
-                                Elem<T>::st(dxs + size_t(icl) * p.HW, sum);
+                                const uint32_t dk = ds + uint32_t(icl * p.KK * 4);
+                                const float a0 = __uint_as_float(lds32(o.x >= 0 ? dk + uint32_t(o.x * 4) : zero));
+                                const float a1 = __uint_as_float(lds32(o.y >= 0 ? dk + uint32_t(o.y * 4) : zero));
+                                const float a2 = __uint_as_float(lds32(o.z >= 0 ? dk + uint32_t(o.z * 4) : zero));
+                                const float a3 = __uint_as_float(lds32(o.w >= 0 ? dk + uint32_t(o.w * 4) : zero));
+                                Elem<T>::st(dxs + size_t(icl) * p.HW, ((a0 + a1) + a2) + a3);
                             }
                         }
                     }
@@ -1409,7 +1635,7 @@ dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const unsigned cha
                     for (int sI = 0; sI < ns; ++sI) {
                         T* dxs = dx + size_t(b0 + sI) * p.IHW + size_t(ic0) * p.HW;
                         const float* ds = Ds + sI * p.P * DG_DSTR;
-                        for (int t = ft; t < span; t += 256) {
+                        for (int t = ft; t < span; t += DG_NFT) {
                             uint32_t icl, hw, h, ww;
                             p.dm_HW.divmod(uint32_t(t), icl, hw);
                             p.dm_W.divmod(hw, h, ww);
@@ -1425,15 +1651,20 @@ dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const unsigned cha
                         }
                     }
                 }
-                asm volatile("bar.sync 1, 256;" ::: "memory");  // Ds consumed
+                if (!fmt_sync()) {  // Ds consumed
+                    ok = false;
+                    break;
+                }
             }
             if (!ok) break;
+            if (geo.nab == 1 && next < geo.ntiles && !(ok = build_g(next, nab))) break;
+            abp = nab;
         }
     }
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, 2 * geo.acc_cols);
+        tmem_dealloc(tmem, 512);
     }
 }
 
@@ -1443,14 +1674,6 @@ template <> constexpr int dt_of_tc<__nv_bfloat16>() { return DT_BF16; }
 
 
 
-int tc_swizzle_mode()
-{
-    static const int mode = [] {
-        const char* e = getenv("IGC_TC_SWIZZLE");
-        return (e && e[0] == '0') ? 0 : 1;
-    }();
-    return mode;
-}
 
 }  // namespace
 
@@ -1529,24 +1752,30 @@ cudaError_t run_fwd_tc(const Plan& pl, const ConvParams& p, int dt, const void* 
 }
 
 // ---- wgrad ------------------------------------------------------------------------------
-// Split count: enough tiles to cover the SMs, at least two chunks per split.
+// k rows per tile: the largest the accumulator allows (128 for fp32 hi + lo, 256 for
+// bf16), shrunk to K*K*IC rounded up to 32; splits: enough tiles to cover the SMs, at least two
+// chunks per split; then the deepest raw / B rings that fit.
 template <typename T>
-static bool pick_wgrad_v3(const ConvParams& p, const DevInfo& d, TcWgradGeom& out)
+static bool pick_wgrad(const ConvParams& p, const DevInfo& d, TcWgradGeom& out)
 {
-    if (p.P > TcTraits<T>::KC || p.B <= 0) return false;
-    for (int nt : {128, 64, 32}) {
-        const int tiles = ceil_div(p.Kred, nt) * ceil_div(p.OC, TC_M);
-        const int nsc = std::max(1, TcTraits<T>::KC / p.P);
-        int splits = std::max(1, d.sms / tiles);
-        splits = std::min(splits, std::max(1, p.B / (2 * nsc)));
+    using Tr = TcTraits<T>;
+    if (p.P > Tr::KC || p.B <= 0) return false;
+    const int ktmax = Tr::split ? 128 : 256;
+    const int ktp = std::min(ktmax, round_up(p.Kred, 32));  // epilogue quarters of 8-column loads
+    const int upr = round_up(wgrad_nsc(p.P, Tr::KC, Tr::KC / 4) * p.P, Tr::KC / 4) / Tr::E;
+    if (ceil_div(ktp, WG_XTHREADS / upr) > WgRows<T>::value) return false;  // rows per X thread
+    const int tiles = ceil_div(p.Kred, ktp) * ceil_div(p.OC, TC_M);
+    const int nsc = wgrad_nsc(p.P, Tr::KC, Tr::KC / 4);
+    int splits = std::max(1, d.sms / tiles);
+    splits = std::min(splits, std::max(1, p.B / (2 * nsc)));
+    for (int nbs = 3; nbs >= 2; --nbs)
         for (int raws = 3; raws >= 2; --raws) {
-            const TcWgradGeom g = wgrad_v3_geom<T>(p, nt, raws, splits);
-            if (wgrad_v3_smem<T>(g) <= d.smem_optin) {
+            const TcWgradGeom g = wgrad_geom<T>(p, ktp, raws, nbs, splits);
+            if (g.na >= 2 && wgrad_smem<T>(g) <= d.smem_optin) {
                 out = g;
                 return true;
             }
         }
-    }
     return false;
 }
 
@@ -1555,14 +1784,14 @@ bool tc_wgrad_ok(const ConvParams& p, int dt, const DevInfo& d)
     if (d.cc_major != 10) return false;
     if (p.N == 0) return true;
     TcWgradGeom g;
-    return dt == DT_BF16 ? pick_wgrad_v3<__nv_bfloat16>(p, d, g) : pick_wgrad_v3<float>(p, d, g);
+    return dt == DT_BF16 ? pick_wgrad<__nv_bfloat16>(p, d, g) : pick_wgrad<float>(p, d, g);
 }
 
 Plan plan_wgrad_tc(const ConvParams& p, int dt, const DevInfo& d)
 {
     Plan pl;
     pl.algo = ALGO_TC;
-    pl.block = FV_THREADS;
+    pl.block = WG_THREADS;
     if (p.N == 0) {
         pl.launches = 1;  // the reduction alone writes zeros
         pl.splits = 0;
@@ -1570,11 +1799,11 @@ Plan plan_wgrad_tc(const ConvParams& p, int dt, const DevInfo& d)
         return pl;
     }
     TcWgradGeom g;
-    if (dt == DT_BF16) pick_wgrad_v3<__nv_bfloat16>(p, d, g);
-    else pick_wgrad_v3<float>(p, d, g);
-    pl.smem = dt == DT_BF16 ? wgrad_v3_smem<__nv_bfloat16>(g) : wgrad_v3_smem<float>(g);
+    if (dt == DT_BF16) pick_wgrad<__nv_bfloat16>(p, d, g);
+    else pick_wgrad<float>(p, d, g);
+    pl.smem = dt == DT_BF16 ? wgrad_smem<__nv_bfloat16>(g) : wgrad_smem<float>(g);
     pl.splits = g.splits;
-    pl.variant = g.NT * 4 + g.raws;
+    pl.variant = (g.KTp * 4 + g.raws) * 4 + g.nbs;
     pl.launches = 2;
     pl.grid = std::min(g.k_tiles * g.oc_tiles * g.splits, d.sms);
     pl.workspace = size_t(g.splits) * p.OC * g.kpad * sizeof(float);
@@ -1588,20 +1817,17 @@ static cudaError_t wgrad_tc_t(const Plan& pl, const ConvParams& p, const void* x
     cudaError_t e = cudaSuccess;
     const int kpad = round_up(p.Kred, 4);
     if (pl.splits > 0) {
-        const TcWgradGeom g = wgrad_v3_geom<T>(p, pl.variant / 4, pl.variant % 4, pl.splits);
-        const bool swz = tc_swizzle_mode() != 0;
-#define IG_LAUNCH_WG_TC(R, Z)                                                                              \
+        const int v = pl.variant;
+        const TcWgradGeom g = wgrad_geom<T>(p, v / 16, (v / 4) % 4, v % 4, pl.splits);
+#define IG_LAUNCH_WG_TC(R)                                                                                 \
     do {                                                                                                   \
-        e = ensure_smem<wgrad_tc_kernel<T, R, Z>>(pl.smem);                                                \
+        e = ensure_smem<wgrad_tc_kernel<T, R>>(pl.smem);                                                   \
         if (e == cudaSuccess)                                                                              \
-            wgrad_tc_kernel<T, R, Z><<<pl.grid, pl.block, pl.smem, s>>>(p, (const T*)x, (const T*)dy,      \
-                                                                        (const T*)y, (float*)ws, g);       \
+            wgrad_tc_kernel<T, R><<<pl.grid, pl.block, pl.smem, s>>>(p, (const T*)x, (const T*)dy,         \
+                                                                     (const T*)y, (float*)ws, g);          \
     } while (0)
-        if (p.relu) {
-            if (swz) IG_LAUNCH_WG_TC(true, 1); else IG_LAUNCH_WG_TC(true, 0);
-        } else {
-            if (swz) IG_LAUNCH_WG_TC(false, 1); else IG_LAUNCH_WG_TC(false, 0);
-        }
+        if (p.relu) IG_LAUNCH_WG_TC(true);
+        else IG_LAUNCH_WG_TC(false);
 #undef IG_LAUNCH_WG_TC
         if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -1617,17 +1843,16 @@ cudaError_t run_wgrad_tc(const Plan& pl, const ConvParams& p, int dt, const void
 }
 
 // ---- d_input ------------------------------------------------------------------------
-// Samples per tile: about B / SMs (one tile per CTA at small batches), at most 128 / P;
-// then the deepest weight ring that fits in shared memory.
+// Channels per k-tile: as many as keep KTp within the accumulator limit (128 rows; the fp32
+// accumulator holds hi and lo halves), then the deepest weight ring that fits.
 template <typename T>
 static bool pick_dgrad(const ConvParams& p, const DevInfo& d, TcDgradGeom& out)
 {
-    if (p.B <= 0 || p.KK > TC_M || p.P > TC_M) return false;
-    const int ns_max = std::max(1, TC_M / p.P);
-    for (int ns = std::min(ns_max, ceil_div(p.B, d.sms)); ns >= 1; --ns) {
-        for (int na = 4; na >= 2; --na) {
-            const TcDgradGeom g = dgrad_geom_ns<T>(p, ns, na);
-            if (g.NT > TC_M || 2 * g.acc_cols > 512) continue;
+    if (p.B <= 0 || p.KK > 128 || p.P > DG_TM) return false;
+    for (int cic = std::min(p.IC, 128 / p.KK); cic >= 1; --cic) {
+        for (int nw = 4; nw >= 2; --nw) {
+            const TcDgradGeom g = dgrad_geom<T>(p, cic, nw);
+            if (g.dcols * g.ndb + g.acols * g.nab > 512) continue;
             if (dgrad_smem<T>(p, g) <= d.smem_optin && dgrad_packed_bytes<T>(g) <= kScratchBytes) {
                 out = g;
                 return true;
@@ -1652,8 +1877,8 @@ Plan plan_dgrad_tc(const ConvParams& p, int dt, const DevInfo& d)
     Plan pl;
     pl.algo = ALGO_TC;
     pl.launches = 2;  // weight packing, then the implicit GEMM + col2im
-    pl.block = FV_THREADS;
-    pl.variant = g.NS * 8 + g.na;
+    pl.block = DG_THREADS;
+    pl.variant = g.CIC * 8 + g.nw;
     pl.grid = std::min(g.ntiles, d.sms);
     pl.smem = dt == DT_BF16 ? dgrad_smem<__nv_bfloat16>(p, g) : dgrad_smem<float>(p, g);
     return pl;
@@ -1663,29 +1888,26 @@ template <typename T>
 static cudaError_t dgrad_tc_t(const Plan& pl, const ConvParams& p, const void* dy, const void* w,
                               const void* y, void* dx, int, cudaStream_t s)
 {
-    const TcDgradGeom g = dgrad_geom_ns<T>(p, pl.variant / 8, pl.variant % 8);
+    const TcDgradGeom g = dgrad_geom<T>(p, pl.variant / 8, pl.variant % 8);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     unsigned char* wpack = static_cast<unsigned char*>(stream_scratch(dev, s));
     if (!wpack) return cudaErrorMemoryAllocation;
-    const size_t units = size_t(g.nkt) * g.nch * TC_M * 8;
+    const size_t units = size_t(g.nkt) * g.nch * g.KTp * 8;
     const int pgrid = int(std::min<size_t>((units + 255) / 256, 4096));
-    pack_dgrad_w_kernel<T><<<pgrid, 256, 0, s>>>(p, (const T*)w, wpack, g.nkt, g.nch, g.CIC);
+    pack_dgrad_w_kernel<T><<<pgrid, 256, 0, s>>>(p, (const T*)w, wpack, g.nkt, g.nch, g.CIC, g.KTp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const bool swz = tc_swizzle_mode() != 0;
-#define IG_LAUNCH_DG_TC(R, Z)                                                                              \
+    // The weight operand is always in the 128-byte swizzled layout the pack kernel writes.
+#define IG_LAUNCH_DG_TC(R)                                                                                 \
     do {                                                                                                   \
-        e = ensure_smem<dgrad_tc_kernel<T, R, Z>>(pl.smem);                                                \
+        e = ensure_smem<dgrad_tc_kernel<T, R, 1>>(pl.smem);                                                \
         if (e == cudaSuccess)                                                                              \
-            dgrad_tc_kernel<T, R, Z><<<pl.grid, pl.block, pl.smem, s>>>(p, (const T*)dy, wpack,            \
+            dgrad_tc_kernel<T, R, 1><<<pl.grid, pl.block, pl.smem, s>>>(p, (const T*)dy, wpack,            \
                                                                         (const T*)y, (T*)dx, g);           \
     } while (0)
-    if (p.relu) {
-        if (swz) IG_LAUNCH_DG_TC(true, 1); else IG_LAUNCH_DG_TC(true, 0);
-    } else {
-        if (swz) IG_LAUNCH_DG_TC(false, 1); else IG_LAUNCH_DG_TC(false, 0);
-    }
+    if (p.relu) IG_LAUNCH_DG_TC(true);
+    else IG_LAUNCH_DG_TC(false);
 #undef IG_LAUNCH_DG_TC
     return e != cudaSuccess ? e : cudaGetLastError();
 }
