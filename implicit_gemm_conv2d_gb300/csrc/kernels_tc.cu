@@ -670,17 +670,25 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
 //               y[...] (ReLU mask source) and x[b, ic_lo : ic_hi] (the k-tile's input
 //               channels) of the chunk's samples into a raw slot.
 //   warp 2      MMA.
-//   warps 3-6   G formatters: lane = output channel; the chunk's columns, masked and split,
-//               into a TMEM operand stage with tcgen05.st.
-//   warps 7-18  X formatters: 16-byte units (row k, 4 or 8 columns) of the B stage.
+//   G warps     (the first 8 formatter warps for fp32, 4 for bf16) lane = output channel;
+//               the chunk's columns, masked and split, into a TMEM operand stage with
+//               tcgen05.st.
+//   X warps     (the other formatter warps) 16-byte units (row k, 4 or 8 columns) of the
+//               B stage.
 //   warps 3-18  epilogue: the fp32 tile to ws[split][oc][k] (row stride kpad).
 //   warp 1      idle.
 // ======================================================================================
 constexpr int WG_THREADS = FV_FMT0 + 32 * 16;
-constexpr int WG_XTHREADS = 32 * 12;   // X formatter threads
 constexpr int WG_MAXA = 8, WG_MAXB = 4, WG_MAXR = 3;
-// Rows of the B stage one X-formatter thread builds at most (its k offsets stay in registers).
-template <typename T> struct WgRows { static constexpr int value = TcTraits<T>::split ? 4 : 8; };
+// Formatter roles: G warps (a multiple of 4, one or more per TMEM lane quarter) and X
+// warps; the column groups of 8 words one G thread writes; the B-stage rows one X thread
+// builds (its k offsets stay in registers).  fp32 splits the warps evenly (G and X are
+// both 128 rows); bf16 gives X three quarters (its KTp is up to 256 rows).
+template <typename T> struct WgRoles {
+    static constexpr int g_warps = TcTraits<T>::split ? 8 : 4;
+    static constexpr int g_groups = TcTraits<T>::split ? 2 : 4;
+    static constexpr int x_rows = TcTraits<T>::split ? 4 : 6;
+};
 
 struct TcWgradGeom {
     int KTp;       // k rows per tile (multiple of 32): <= 128 (fp32), <= 256 (bf16)
@@ -750,7 +758,7 @@ inline TcWgradGeom wgrad_geom(const ConvParams& p, int KTp, int raws, int nbs, i
 template <typename T>
 inline int wgrad_smem(const TcWgradGeom& g)
 {
-    return 1024 + g.nbs * g.b_bytes + g.raws * g.raw_bytes + int(sizeof(WgBars)) + 16;
+    return 1024 + g.nbs * g.b_bytes + g.raws * g.raw_bytes + int(sizeof(WgBars)) + 8 * g.cnp + 16;
 }
 
 template <typename T, bool RELU>
@@ -767,24 +775,31 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
     unsigned char* bring = smem;
     unsigned char* raw = bring + geo.nbs * geo.b_bytes;
     WgBars* bars = reinterpret_cast<WgBars*>(raw + geo.raws * geo.raw_bytes);
+    // Column table of a chunk: column n -> (sample j, byte offset of (j, pq) in the dy
+    // region from channel row 0); padding columns get a sample no chunk has.
+    int* gtab = reinterpret_cast<int*>(bars + 1);
     volatile int* abort_flag = &bars->abort_flag;
     const int gregion = geo.nsc * geo.gs + 16;              // bytes of the dy (and of the y) region
     const int xoff = gregion * (RELU ? 2 : 1);              // start of the x region in a slot
-    const bool gcontig = geo.oc_tiles == 1;                 // dy / y of the chunk are one range
     const int acol0 = round_up(geo.dcols, 32);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int n = tid; n < geo.cnp; n += WG_THREADS) {
+        const int j = n / p.P, pq = n % p.P;
+        gtab[2 * n] = n < geo.nsc * p.P ? j : 1 << 20;
+        gtab[2 * n + 1] = (j * p.OCP + pq) * ES;
+    }
     if (tid == 0) {
         for (int i = 0; i < geo.raws; ++i) {
             mbar_init(smem_u32(&bars->raw_full[i]), 1);
             mbar_init(smem_u32(&bars->raw_empty[i]), 16);
         }
         for (int i = 0; i < geo.na; ++i) {
-            mbar_init(smem_u32(&bars->a_full[i]), 4);
+            mbar_init(smem_u32(&bars->a_full[i]), WgRoles<T>::g_warps);
             mbar_init(smem_u32(&bars->a_empty[i]), 1);
         }
         for (int i = 0; i < geo.nbs; ++i) {
-            mbar_init(smem_u32(&bars->b_full[i]), 12);
+            mbar_init(smem_u32(&bars->b_full[i]), 16 - WgRoles<T>::g_warps);
             mbar_init(smem_u32(&bars->b_empty[i]), 1);
         }
         mbar_init(smem_u32(&bars->acc_full), 1);
@@ -801,8 +816,12 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
     const int total = per_split * geo.splits;
 
     // Tile decode shared by all roles.
+    // The k-tiles of one split read the same dy / y chunks: each starts at a different
+    // chunk (a fixed rotation, so the summation order is fixed) so that they do not all
+    // request the same lines at once.
     struct TileInfo {
-        int split, k0, oc0, rows, s_lo, s_hi, nchunks, ic_lo, ic_hi;
+        int split, k0, oc0, rows, s_lo, s_hi, nchunks, ic_lo, ic_hi, rot;
+        __device__ int chunk(int kc) const { return kc + rot < nchunks ? kc + rot : kc + rot - nchunks; }
     };
     auto decode = [&](int tile) {
         TileInfo ti;
@@ -816,84 +835,73 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
         ti.nchunks = (ti.s_hi - ti.s_lo + geo.nsc - 1) / geo.nsc;
         ti.ic_lo = ti.k0 / p.KK;
         ti.ic_hi = min(p.IC - 1, (min(ti.k0 + KTp, p.Kred) - 1) / p.KK);
+        ti.rot = (rem % geo.k_tiles) * ti.nchunks / geo.k_tiles;
         return ti;
     };
 
     if (warp == 0) {
-        // ---------------- bulk-copy producer ----------------
-        const unsigned char* xb = reinterpret_cast<const unsigned char*>(x);
-        const unsigned char* gb = reinterpret_cast<const unsigned char*>(dy);
-        const unsigned char* yb = reinterpret_cast<const unsigned char*>(y);
-        const unsigned char* x_end = xb + size_t(p.B) * p.IHW * ES;
-        const unsigned char* g_end = gb + size_t(p.B) * p.OCP * ES;
-        const unsigned char* y_end = yb + size_t(p.B) * p.OCP * ES;
-        RingPos rp;
-        for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
-            const TileInfo ti = decode(tile);
-            const int gbytes = ti.rows * p.P * ES;
-            const int xbytes = (ti.ic_hi - ti.ic_lo + 1) * p.HW * ES;
-            for (int kc = 0; kc < ti.nchunks; ++kc, rp.next(geo.raws)) {
-                const int s = rp.i;
-                if (rp.wrapped && !mbar_wait_or_abort(smem_u32(&bars->raw_empty[s]), rp.ph ^ 1u, abort_flag)) {
-                    report(const_cast<int*>(abort_flag), 4u);
-                    break;
-                }
-                unsigned char* slot = raw + s * geo.raw_bytes;
-                const int b0 = ti.s_lo + kc * geo.nsc, nb = min(geo.nsc, ti.s_hi - b0);
-                // Piece i: i < ng -> dy (and y at +gregion), else x of sample i - ng.
-                const int ng = gcontig ? 1 : nb;
-                const int npieces = ng + nb;
-                auto piece = [&](int i, int which, const unsigned char*& src, unsigned char*& dst, int& bytes,
-                                 const unsigned char*& end) {
-                    if (i < ng) {
-                        const int j = i;
-                        const size_t off = (size_t(b0 + j) * p.OCP + size_t(ti.oc0) * p.P) * ES;
-                        const unsigned char* base = which == 0 ? gb : yb;
-                        end = which == 0 ? g_end : y_end;
-                        const int d = int(off & 15);
-                        src = base + off - d;
-                        bytes = round_up(d + (gcontig ? nb * p.OCP * ES : gbytes), 16);
-                        dst = slot + (which == 0 ? 0 : gregion) + (gcontig ? 0 : j * geo.gs);
-                    } else {
-                        const int j = i - ng;
-                        const size_t off = (size_t(b0 + j) * p.IHW + size_t(ti.ic_lo) * p.HW) * ES;
-                        const int d = int(off & 15);
-                        src = xb + off - d;
-                        end = x_end;
-                        bytes = round_up(d + xbytes, 16);
-                        dst = slot + xoff + j * geo.xsb;
+        // ---------------- bulk-copy producer (lane 0) ----------------
+        // Per chunk: one copy of dy[b0 : b0+nb] (all channels, contiguous), one of y, and
+        // per sample one of x[b, ic_lo : ic_hi].  Sources are rounded down to 16 bytes (the
+        // slack is skipped when read); bytes of a last 16-byte block past the end of a
+        // tensor are copied by plain loads.
+        if (lane == 0) {
+            const unsigned char* xb = reinterpret_cast<const unsigned char*>(x);
+            const unsigned char* gb = reinterpret_cast<const unsigned char*>(dy);
+            const unsigned char* yb = reinterpret_cast<const unsigned char*>(y);
+            const unsigned char* x_end = xb + size_t(p.B) * p.IHW * ES;
+            const unsigned char* g_end = gb + size_t(p.B) * p.OCP * ES;
+            const unsigned char* y_end = yb + size_t(p.B) * p.OCP * ES;
+            const size_t xstride = size_t(p.IHW) * ES, gstride = size_t(p.OCP) * ES;
+            // A copy of [src, src + bytes) (src 16-byte aligned, bytes a multiple of 16): the
+            // bytes at or past the last 16-byte boundary before `end` by plain loads (done
+            // before the barrier's arrival releases them), the rest by one bulk copy.
+            auto tail = [&](unsigned char* dstp, const unsigned char* src, int bytes, const unsigned char* end) -> int {
+                const int bulk = slab_bytes_bulk(src, bytes, end);
+                for (const unsigned char* t = src + bulk; t < src + bytes && t < end; ++t) dstp[int(t - src)] = *t;
+                return bulk;
+            };
+            RingPos rp;
+            for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+                const TileInfo ti = decode(tile);
+                const int xbytes = (ti.ic_hi - ti.ic_lo + 1) * p.HW * ES;
+                for (int kc = 0; kc < ti.nchunks; ++kc, rp.next(geo.raws)) {
+                    const int s = rp.i;
+                    if (rp.wrapped && !mbar_wait_or_abort(smem_u32(&bars->raw_empty[s]), rp.ph ^ 1u, abort_flag)) {
+                        report(const_cast<int*>(abort_flag), 4u);
+                        break;
                     }
-                };
-                const int nwh = RELU ? 2 : 1;
-                int tx = 0;
-                for (int i = lane; i < npieces; i += 32) {
-                    for (int which = 0; which < (i < ng ? nwh : 1); ++which) {
-                        const unsigned char* src;
-                        unsigned char* dst;
-                        int bytes;
-                        const unsigned char* end;
-                        piece(i, which, src, dst, bytes, end);
-                        const int bulk = slab_bytes_bulk(src, bytes, end);
-                        for (const unsigned char* t = src + bulk; t < src + bytes && t < end; ++t) dst[int(t - src)] = *t;
-                        tx += bulk;
+                    unsigned char* slot = raw + s * geo.raw_bytes;
+                    const uint32_t slot_u32 = smem_u32(slot), bar = smem_u32(&bars->raw_full[s]);
+                    const int b0 = ti.s_lo + ti.chunk(kc) * geo.nsc, nb = min(geo.nsc, ti.s_hi - b0);
+                    const size_t goff = size_t(b0) * gstride;
+                    const int gd = int(goff & 15);
+                    const int gbytes = round_up(gd + nb * int(gstride), 16);
+                    const size_t xoff0 = size_t(b0) * xstride + size_t(ti.ic_lo) * p.HW * ES;
+                    // Plain-load tails and transaction bytes, then the arrival, then the copies.
+                    const int gbulk = tail(slot, gb + goff - gd, gbytes, g_end);
+                    int tx = gbulk;
+                    if (RELU) tx += tail(slot + gregion, yb + goff - gd, gbytes, y_end);
+                    for (int j = 0; j < nb; ++j) {
+                        const size_t xo = xoff0 + size_t(j) * xstride;
+                        const int xd = int(xo & 15);
+                        tx += tail(slot + xoff + j * geo.xsb, xb + xo - xd, round_up(xd + xbytes, 16), x_end);
                     }
-                }
-                tx = warp_sum(tx);
-                if (lane == 0) mbar_arrive_expect_tx(smem_u32(&bars->raw_full[s]), uint32_t(tx));
-                __syncwarp();
-                for (int i = lane; i < npieces; i += 32) {
-                    for (int which = 0; which < (i < ng ? nwh : 1); ++which) {
-                        const unsigned char* src;
-                        unsigned char* dst;
-                        int bytes;
-                        const unsigned char* end;
-                        piece(i, which, src, dst, bytes, end);
-                        const int bulk = slab_bytes_bulk(src, bytes, end);
-                        if (bulk > 0) bulk_g2s(smem_u32(dst), src, uint32_t(bulk), smem_u32(&bars->raw_full[s]));
+                    mbar_arrive_expect_tx(bar, uint32_t(tx));
+                    if (gbulk > 0) {
+                        bulk_g2s(slot_u32, gb + goff - gd, uint32_t(gbulk), bar);
+                        if (RELU) bulk_g2s(slot_u32 + gregion, yb + goff - gd, uint32_t(gbulk), bar);
+                    }
+                    for (int j = 0; j < nb; ++j) {
+                        const size_t xo = xoff0 + size_t(j) * xstride;
+                        const int xd = int(xo & 15);
+                        const int xbulk = slab_bytes_bulk(xb + xo - xd, round_up(xd + xbytes, 16), x_end);
+                        if (xbulk > 0) bulk_g2s(slot_u32 + uint32_t(xoff + j * geo.xsb), xb + xo - xd, uint32_t(xbulk), bar);
                     }
                 }
             }
         }
+        __syncwarp();
     } else if (warp == FV_MMA_WARP) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
@@ -943,51 +951,79 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
         const int fw = warp - 3;            // 0 .. 15
         const int qd = warp & 3;            // TMEM lane quarter
         const uint32_t lane_bits = uint32_t(qd * 32) << 16;
-        const bool grole = fw < 4;          // G formatter (one warp per lane quarter)
-        // Vector width (elements) of the G loads: P and OC*P multiples of it.
-        const int gvec = (p.P % 4 == 0) ? 4 : (p.P % 2 == 0) ? 2 : 1;
-        const int m = qd * 32 + lane;       // G: output channel within the tile
-        // X role: 16-byte unit column c (E columns) of rows rbase + i*rstep.
-        const int xt = tid - FV_FMT0 - 128;  // 0 .. 383 for the X role
-        const int upr = geo.cnp / Tr::E;     // units per row
-        const int cfix = grole ? 0 : xt % upr;
-        const int rbase = grole ? 0 : xt / upr;
-        const int rstep = WG_XTHREADS / upr;
-        const bool xact = !grole && xt < rstep * upr;
-        constexpr int XMAXR = WgRows<T>::value;  // rows per X thread (checked by the planner)
-        int po[Tr::E], jj[Tr::E];            // column offset and sample of this thread's columns
-#pragma unroll
-        for (int e = 0; e < Tr::E; ++e) {
-            const int n = cfix * Tr::E + e;
-            uint32_t j, r, oh, ow;
-            p.dm_P.divmod(uint32_t(n), j, r);
-            p.dm_OW.divmod(r, oh, ow);
-            jj[e] = n < geo.nsc * p.P ? int(j) : 1 << 20;  // padding columns: never a real sample
-            po[e] = (int(oh) * p.S * p.W + int(ow) * p.S) * ES;
-        }
-        RingPos rp, ap, bp;
-        uint32_t t = 0;
-        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++t) {
-            const TileInfo ti = decode(tile);
-            // X role: byte offsets of this thread's rows k = k0 + rbase + i*rstep (-1: past Kred).
-            int ko[XMAXR];
-#pragma unroll
-            for (int i = 0; i < XMAXR; ++i) {
-                const int r = rbase + i * rstep;
-                const int k = ti.k0 + r;
-                ko[i] = (xact && r < KTp && k < p.Kred) ? (k_offset(p, k) - ti.ic_lo * p.HW) * ES : -1;
+        constexpr int NGW = WgRoles<T>::g_warps;
+        const int m = qd * 32 + lane;       // output channel within the tile (G, epilogue)
+        // Epilogue of tile t: D[oc][k] -> ws; this warp's lanes, a quarter of the k columns.
+        auto epilogue = [&](const TileInfo& ti, uint32_t t) -> bool {
+            if (!mbar_wait_or_abort(smem_u32(&bars->acc_full), t & 1, abort_flag)) {
+                report(const_cast<int*>(abort_flag), 2u);
+                return false;
             }
-            bool ok = true;
-            for (int kc = 0; kc < ti.nchunks; ++kc, rp.next(geo.raws)) {
-                if (!mbar_wait_or_abort(smem_u32(&bars->raw_full[rp.i]), rp.ph, abort_flag)) {
-                    report(const_cast<int*>(abort_flag), 1u);
-                    ok = false;
-                    break;
+            tc_fence_after();
+            const int oc = ti.oc0 + m;
+            const int kq = KTp / 4, c0 = (fw >> 2) * kq;
+            for (int cb = c0; cb < c0 + kq; cb += 8) {
+                uint32_t r[8];
+                tmem_ld8(tmem + lane_bits + uint32_t(cb), r);
+                if constexpr (Tr::split) {
+                    uint32_t r2[8];
+                    tmem_ld8(tmem + lane_bits + uint32_t(KTp + cb), r2);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(r2[e]));
+                } else {
+                    tmem_ld_wait();
                 }
-                const int b0 = ti.s_lo + kc * geo.nsc;
-                const int nb = min(geo.nsc, ti.s_hi - b0);
-                const uint32_t slot = smem_u32(raw + rp.i * geo.raw_bytes);
-                if (grole) {
+                const int k = ti.k0 + cb;
+                if (oc < p.OC && m < ti.rows && k < geo.kpad) {
+                    float* dst = ws + (size_t(ti.split) * p.OC + oc) * geo.kpad + k;
+                    *reinterpret_cast<float4*>(dst) = make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]),
+                                                                  __uint_as_float(r[2]), __uint_as_float(r[3]));
+                    if (k + 4 < geo.kpad)
+                        *reinterpret_cast<float4*>(dst + 4) = make_float4(
+                            __uint_as_float(r[4]), __uint_as_float(r[5]), __uint_as_float(r[6]), __uint_as_float(r[7]));
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty));
+            return true;
+        };
+        if (fw < NGW) {
+            // ---------------- G formatters ----------------
+            const int gsub = fw >> 2;           // which of the NGW/4 warps of its lane quarter
+            constexpr int NG = ES == 4 ? 8 : 16;       // columns per tcgen05.st of 8 words
+            constexpr int MAXG = WgRoles<T>::g_groups;  // column groups per thread
+            const int ngroups = geo.cnp / NG;
+            // Fast path: P a multiple of 4 -> runs of 4 positions of one
+            // sample are one vector load; per group of NG columns the byte offsets (from the
+            // thread's channel row) and samples of its NG/4 vectors never change.
+            const bool gfast = p.P % 4 == 0;
+            int goff[MAXG][NG / 4], gsj[MAXG][NG / 4];
+#pragma unroll
+            for (int gi = 0; gi < MAXG; ++gi)
+#pragma unroll
+                for (int vi = 0; vi < NG / 4; ++vi) {
+                    const int n = (gsub + gi * (NGW / 4)) * NG + vi * 4;
+                    uint32_t j, pq;
+                    p.dm_P.divmod(uint32_t(n), j, pq);
+                    goff[gi][vi] = (int(j) * p.OCP + int(pq)) * ES;
+                    gsj[gi][vi] = n < geo.nsc * p.P ? int(j) : 1 << 20;  // padding: never a real sample
+                }
+            RingPos rp, ap;
+            uint32_t t = 0;
+            for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++t) {
+                const TileInfo ti = decode(tile);
+                bool ok = true;
+                for (int kc = 0; kc < ti.nchunks; ++kc, rp.next(geo.raws)) {
+                    if (!mbar_wait_or_abort(smem_u32(&bars->raw_full[rp.i]), rp.ph, abort_flag)) {
+                        report(const_cast<int*>(abort_flag), 1u);
+                        ok = false;
+                        break;
+                    }
+                    const int b0 = ti.s_lo + ti.chunk(kc) * geo.nsc;
+                    const int nb = min(geo.nsc, ti.s_hi - b0);
+                    const uint32_t slot = smem_u32(raw + rp.i * geo.raw_bytes);
                     if (ap.wrapped && !mbar_wait_or_abort(smem_u32(&bars->a_empty[ap.i]), ap.ph ^ 1u, abort_flag)) {
                         report(const_cast<int*>(abort_flag), 1u);
                         ok = false;
@@ -998,106 +1034,67 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
                     const int dg0 = int(((size_t(b0) * p.OCP + size_t(ti.oc0) * p.P) * ES) & 15);
                     const bool live = m < ti.rows;
                     const uint32_t col = tmem + lane_bits + uint32_t(acol0 + ap.i * geo.acols);
-                    auto gval = [&](int n) -> uint32_t {  // raw bits of G[n, oc0 + m] (0 outside)
-                        uint32_t j, pq;
-                        p.dm_P.divmod(uint32_t(n), j, pq);
-                        if (!live || int(j) >= nb || n >= geo.nsc * p.P) return 0u;
-                        uint32_t a;
-                        if (gcontig) {
-                            a = slot + uint32_t(dg0 + ((int(j) * p.OCP + m * p.P + int(pq)) * ES));
-                        } else {
-                            const size_t b = size_t(b0) + j;
-                            a = slot + uint32_t(int(j) * geo.gs + int(((b * p.OCP + size_t(ti.oc0) * p.P) * ES) & 15) +
-                                                (m * p.P + int(pq)) * ES);
-                        }
-                        if constexpr (ES == 4) {
-                            const uint32_t v = lds32(a);
-                            if (RELU && !(__uint_as_float(lds32(a + gregion)) > 0.f)) return 0u;
-                            return v;
-                        } else {
-                            const uint32_t v = lds16(a);
-                            if (RELU && !(__uint_as_float(lds16(a + gregion) << 16) > 0.f)) return 0u;
-                            return v;
-                        }
-                    };
-                    constexpr int NG = ES == 4 ? 8 : 16;  // columns per tcgen05.st of 8 words
-                    // Fast path (one dy range, P a multiple of the vector): runs of gv
-                    // consecutive positions of one sample are one vector load each.
-                    const int gv = gcontig ? gvec : 0;
                     const uint32_t gbase = slot + uint32_t(dg0 + m * p.P * ES);
-                    auto gload = [&](int n0, uint32_t (&v)[NG]) {
-                        if (gv == 0) {
+                    const uint32_t gtab_u32 = smem_u32(gtab);
 #pragma unroll
-                            for (int e = 0; e < NG; ++e) v[e] = gval(n0 + e);
-                            return;
-                        }
+                    for (int gi = 0; gi < MAXG; ++gi) {
+                        const int g = gsub + gi * (NGW / 4);
+                        if (g >= ngroups) break;
+                        uint32_t v[NG];
+                        if (gfast) {
+                            uint32_t d[NG], w[NG];
 #pragma unroll
-                        for (int e = 0; e < NG; e += 4) {
-                            // 4 columns n0+e .. +3 as 4 / gv loads of gv elements (gv in 4, 2, 1)
-#pragma unroll
-                            for (int h = 0; h < 4; ++h) {
-                                if (h % gv) continue;
-                                const int n = n0 + e + h;
-                                uint32_t j, pq;
-                                p.dm_P.divmod(uint32_t(n), j, pq);
-                                const bool in = live && int(j) < nb && n < geo.nsc * p.P;
-                                const uint32_t a = gbase + uint32_t((int(j) * p.OCP + int(pq)) * ES);
-                                uint32_t d[4] = {0, 0, 0, 0}, w[4] = {0, 0, 0, 0};
-                                if (in) {
-                                    if constexpr (ES == 4) {
-                                        if (gv == 4) {
-                                            const int4 q4 = lds128(a);
-                                            d[0] = q4.x; d[1] = q4.y; d[2] = q4.z; d[3] = q4.w;
-                                            if (RELU) {
-                                                const int4 r4 = lds128(a + gregion);
-                                                w[0] = r4.x; w[1] = r4.y; w[2] = r4.z; w[3] = r4.w;
-                                            }
-                                        } else if (gv == 2) {
-                                            const uint2 q2 = lds64(a);
-                                            d[0] = q2.x; d[1] = q2.y;
-                                            if (RELU) {
-                                                const uint2 r2 = lds64(a + gregion);
-                                                w[0] = r2.x; w[1] = r2.y;
-                                            }
-                                        } else {
-                                            d[0] = lds32(a);
-                                            if (RELU) w[0] = lds32(a + gregion);
-                                        }
-                                    } else {
-                                        // bf16: gv elements = 8, 4 or 2 bytes, unpacked to one per word
-                                        if (gv == 4) {
-                                            const uint2 q2 = lds64(a);
-                                            d[0] = q2.x & 0xFFFFu; d[1] = q2.x >> 16; d[2] = q2.y & 0xFFFFu; d[3] = q2.y >> 16;
-                                            if (RELU) {
-                                                const uint2 r2 = lds64(a + gregion);
-                                                w[0] = r2.x << 16; w[1] = r2.x & 0xFFFF0000u;
-                                                w[2] = r2.y << 16; w[3] = r2.y & 0xFFFF0000u;
-                                            }
-                                        } else if (gv == 2) {
-                                            const uint32_t q = lds32(a);
-                                            d[0] = q & 0xFFFFu; d[1] = q >> 16;
-                                            if (RELU) {
-                                                const uint32_t r = lds32(a + gregion);
-                                                w[0] = r << 16; w[1] = r & 0xFFFF0000u;
-                                            }
-                                        } else {
-                                            d[0] = lds16(a);
-                                            if (RELU) w[0] = lds16(a + gregion) << 16;
-                                        }
+                            for (int vi = 0; vi < NG / 4; ++vi) {
+                                // Only real rows and samples are read (the rest of the
+                                // region may lie past the slot).
+                                const uint32_t a = gbase + uint32_t(goff[gi][vi]);
+                                d[4 * vi] = d[4 * vi + 1] = d[4 * vi + 2] = d[4 * vi + 3] = 0u;
+                                w[4 * vi] = w[4 * vi + 1] = w[4 * vi + 2] = w[4 * vi + 3] = 0u;
+                                if (!live || gsj[gi][vi] >= nb) continue;
+                                if constexpr (ES == 4) {
+                                    const int4 q = lds128(a);
+                                    d[4 * vi] = q.x; d[4 * vi + 1] = q.y; d[4 * vi + 2] = q.z; d[4 * vi + 3] = q.w;
+                                    if (RELU) {
+                                        const int4 r = lds128(a + gregion);
+                                        w[4 * vi] = r.x; w[4 * vi + 1] = r.y; w[4 * vi + 2] = r.z; w[4 * vi + 3] = r.w;
+                                    }
+                                } else {
+                                    const uint2 q = lds64(a);
+                                    d[4 * vi] = q.x & 0xFFFFu; d[4 * vi + 1] = q.x >> 16;
+                                    d[4 * vi + 2] = q.y & 0xFFFFu; d[4 * vi + 3] = q.y >> 16;
+                                    if (RELU) {
+                                        const uint2 r = lds64(a + gregion);
+                                        w[4 * vi] = r.x << 16; w[4 * vi + 1] = r.x & 0xFFFF0000u;
+                                        w[4 * vi + 2] = r.y << 16; w[4 * vi + 3] = r.y & 0xFFFF0000u;
                                     }
                                 }
+                            }
 #pragma unroll
-                                for (int u = 0; u < 4; ++u) {
-                                    if (u >= gv || h + u >= 4) continue;
-                                    // mask words are fp32 patterns (bf16 y in the high half)
-                                    v[e + h + u] = (!RELU || __uint_as_float(w[u]) > 0.f) ? d[u] : 0u;
+                            for (int e = 0; e < NG; ++e) {
+                                // mask words are fp32 patterns (bf16 y in the high half)
+                                const bool keep = live && gsj[gi][e / 4] < nb && (!RELU || __uint_as_float(w[e]) > 0.f);
+                                v[e] = keep ? d[e] : 0u;
+                            }
+                        } else {
+                            // Element by element through the column table (sample, byte offset).
+#pragma unroll
+                            for (int e = 0; e < NG; ++e) {
+                                const int n = g * NG + e;
+                                const int j = int(lds32(gtab_u32 + 8 * n)), off = int(lds32(gtab_u32 + 8 * n + 4));
+                                uint32_t d = 0u;
+                                if (live && j < nb) {
+                                    const uint32_t a = gbase + uint32_t(off);
+                                    if constexpr (ES == 4) {
+                                        d = lds32(a);
+                                        if (RELU && !(__uint_as_float(lds32(a + gregion)) > 0.f)) d = 0u;
+                                    } else {
+                                        d = lds16(a);
+                                        if (RELU && !(__uint_as_float(lds16(a + gregion) << 16) > 0.f)) d = 0u;
+                                    }
                                 }
+                                v[e] = d;
                             }
                         }
-                    };
-                    for (int n0 = 0; n0 < geo.cnp; n0 += NG) {
-                        uint32_t v[NG];
-                        gload(n0, v);
                         if constexpr (Tr::split) {
                             uint32_t hi[8], lo[8];
 #pragma unroll
@@ -1107,13 +1104,13 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
                                 hi[e] = __float_as_uint(h);
                                 lo[e] = __float_as_uint(f - h);
                             }
-                            tmem_st8(col + uint32_t(n0), hi);
-                            tmem_st8(col + uint32_t(Tr::KC + n0), lo);
+                            tmem_st8(col + uint32_t(g * NG), hi);
+                            tmem_st8(col + uint32_t(Tr::KC + g * NG), lo);
                         } else {
                             uint32_t wv[8];
 #pragma unroll
                             for (int e = 0; e < 8; ++e) wv[e] = __byte_perm(v[2 * e], v[2 * e + 1], 0x5410);
-                            tmem_st8(col + uint32_t(n0 / 2), wv);
+                            tmem_st8(col + uint32_t(g * NG / 2), wv);
                         }
                     }
                     tmem_st_wait();
@@ -1124,7 +1121,55 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
                         mbar_arrive(smem_u32(&bars->raw_empty[rp.i]));
                     }
                     ap.next(geo.na);
-                } else {
+                }
+                if (!ok || !epilogue(ti, t)) break;
+            }
+        } else {
+            // ---------------- X formatters ----------------
+            // 16-byte unit column c (E columns) of rows rbase + i*rstep.
+            const int xthreads = 32 * (16 - NGW);
+            const int xt = tid - FV_FMT0 - 32 * NGW;
+            const int upr = geo.cnp / Tr::E;     // units per row
+            const int cfix = xt % upr;
+            const int rbase = xt / upr;
+            const int rstep = xthreads / upr;
+            const bool xact = xt < rstep * upr;
+            constexpr int XMAXR = WgRoles<T>::x_rows;  // rows per thread (checked by the planner)
+            int po[Tr::E], jj[Tr::E];            // column offset and sample of this thread's columns
+#pragma unroll
+            for (int e = 0; e < Tr::E; ++e) {
+                const int n = cfix * Tr::E + e;
+                uint32_t j, r, oh, ow;
+                p.dm_P.divmod(uint32_t(n), j, r);
+                p.dm_OW.divmod(r, oh, ow);
+                jj[e] = n < geo.nsc * p.P ? int(j) : 1 << 20;  // padding columns: never a real sample
+                po[e] = (int(oh) * p.S * p.W + int(ow) * p.S) * ES;
+            }
+            uint32_t uo[XMAXR];                  // unit offsets of this thread's rows in a B stage
+#pragma unroll
+            for (int i = 0; i < XMAXR; ++i) uo[i] = unit_off<1>(rbase + i * rstep, cfix);
+            RingPos rp, bp;
+            uint32_t t = 0;
+            for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++t) {
+                const TileInfo ti = decode(tile);
+                // Byte offsets of this thread's rows k = k0 + rbase + i*rstep (-1: past Kred).
+                int ko[XMAXR];
+#pragma unroll
+                for (int i = 0; i < XMAXR; ++i) {
+                    const int r = rbase + i * rstep;
+                    const int k = ti.k0 + r;
+                    ko[i] = (xact && r < KTp && k < p.Kred) ? (k_offset(p, k) - ti.ic_lo * p.HW) * ES : -1;
+                }
+                bool ok = true;
+                for (int kc = 0; kc < ti.nchunks; ++kc, rp.next(geo.raws)) {
+                    if (!mbar_wait_or_abort(smem_u32(&bars->raw_full[rp.i]), rp.ph, abort_flag)) {
+                        report(const_cast<int*>(abort_flag), 1u);
+                        ok = false;
+                        break;
+                    }
+                    const int b0 = ti.s_lo + ti.chunk(kc) * geo.nsc;
+                    const int nb = min(geo.nsc, ti.s_hi - b0);
+                    const uint32_t slot = smem_u32(raw + rp.i * geo.raw_bytes);
                     if (bp.wrapped && !mbar_wait_or_abort(smem_u32(&bars->b_empty[bp.i]), bp.ph ^ 1u, abort_flag)) {
                         report(const_cast<int*>(abort_flag), 1u);
                         ok = false;
@@ -1160,8 +1205,7 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
                                     }
                                 }
                             }
-                            put_raw_unit<T, 1>(op, op + KTp * ROWB, unit_off<1>(r, cfix),
-                                               make_uint4(wv[0], wv[1], wv[2], wv[3]));
+                            put_raw_unit<T, 1>(op, op + KTp * ROWB, uo[i], make_uint4(wv[0], wv[1], wv[2], wv[3]));
                         }
                     }
                     fence_proxy_async_smem();
@@ -1171,42 +1215,9 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
                         mbar_arrive(smem_u32(&bars->raw_empty[rp.i]));
                     }
                     bp.next(geo.nbs);
-                }
+                                }
+                if (!ok || !epilogue(ti, t)) break;
             }
-            if (!ok) break;
-            // Epilogue: D[oc][k] -> ws; this warp's lanes, a quarter of the k columns.
-            if (!mbar_wait_or_abort(smem_u32(&bars->acc_full), t & 1, abort_flag)) {
-                report(const_cast<int*>(abort_flag), 2u);
-                break;
-            }
-            tc_fence_after();
-            const int oc = ti.oc0 + m;
-            const int kq = KTp / 4, c0 = (fw >> 2) * kq;
-            for (int cb = c0; cb < c0 + kq; cb += 8) {
-                uint32_t r[8];
-                tmem_ld8(tmem + lane_bits + uint32_t(cb), r);
-                if constexpr (Tr::split) {
-                    uint32_t r2[8];
-                    tmem_ld8(tmem + lane_bits + uint32_t(KTp + cb), r2);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(r2[e]));
-                } else {
-                    tmem_ld_wait();
-                }
-                const int k = ti.k0 + cb;
-                if (oc < p.OC && m < ti.rows && k < geo.kpad) {
-                    float* dst = ws + (size_t(ti.split) * p.OC + oc) * geo.kpad + k;
-                    *reinterpret_cast<float4*>(dst) = make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]),
-                                                                  __uint_as_float(r[2]), __uint_as_float(r[3]));
-                    if (k + 4 < geo.kpad)
-                        *reinterpret_cast<float4*>(dst + 4) = make_float4(
-                            __uint_as_float(r[4]), __uint_as_float(r[5]), __uint_as_float(r[6]), __uint_as_float(r[7]));
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty));
         }
     }
     __syncthreads();
@@ -1759,11 +1770,14 @@ template <typename T>
 static bool pick_wgrad(const ConvParams& p, const DevInfo& d, TcWgradGeom& out)
 {
     using Tr = TcTraits<T>;
-    if (p.P > Tr::KC || p.B <= 0) return false;
+    if (p.P > Tr::KC || p.B <= 0 || p.OC > TC_M) return false;  // one dy range of all OC per chunk
     const int ktmax = Tr::split ? 128 : 256;
     const int ktp = std::min(ktmax, round_up(p.Kred, 32));  // epilogue quarters of 8-column loads
-    const int upr = round_up(wgrad_nsc(p.P, Tr::KC, Tr::KC / 4) * p.P, Tr::KC / 4) / Tr::E;
-    if (ceil_div(ktp, WG_XTHREADS / upr) > WgRows<T>::value) return false;  // rows per X thread
+    const int cnp = round_up(wgrad_nsc(p.P, Tr::KC, Tr::KC / 4) * p.P, Tr::KC / 4);
+    const int upr = cnp / Tr::E;
+    if (ceil_div(ktp, 32 * (16 - WgRoles<T>::g_warps) / upr) > WgRoles<T>::x_rows) return false;  // rows per X thread
+    const int ng = Tr::split ? 8 : 16;  // G columns per group
+    if (ceil_div(cnp / ng, WgRoles<T>::g_warps / 4) > WgRoles<T>::g_groups) return false;
     const int tiles = ceil_div(p.Kred, ktp) * ceil_div(p.OC, TC_M);
     const int nsc = wgrad_nsc(p.P, Tr::KC, Tr::KC / 4);
     int splits = std::max(1, d.sms / tiles);

@@ -34,14 +34,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
         : "memory");
     return ok != 0;
 }
-// Bounded wait for the phase with the given parity to complete.  Returns false
-// (and the caller reports an error and unwinds) if it never does.
+// Same with a suspend-time hint: the thread sleeps in hardware until the phase completes
+// or about `ns` nanoseconds pass, instead of spinning on issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for the phase with the given parity to complete: up to 4096 hardware
+// sleeps of at most 1 ms (about 4 s).  Returns false (and the caller reports an error
+// and unwinds) if it never does.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
 {
-    for (uint32_t i = 0; i < (1u << 24); ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (i > 64) __nanosleep(64);
-    }
+    for (uint32_t i = 0; i < 4096u; ++i)
+        if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
     return false;
 }
 
@@ -49,10 +62,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
 // is nonzero.
 __device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, const volatile int* abort)
 {
-    for (uint32_t i = 0; i < (1u << 24); ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255) == 255 && *abort) return false;
-        if (i > 64) __nanosleep(64);
+    for (uint32_t i = 0; i < 4096u; ++i) {
+        if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
+        if (*abort) return false;
     }
     return false;
 }
