@@ -666,9 +666,9 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
 // of k, K-major along n; fp32 as tf32 hi rows then lo rows, so one N = 2*KTp MMA forms
 // G_hi*X_hi and G_hi*X_lo and an N = KTp MMA adds G_lo*X_hi).
 // Warp roles (608 threads):
-//   warp 0      bulk-copy producer: per chunk, the contiguous slabs dy[b, oc0 : oc0+128, :],
-//               y[...] (ReLU mask source) and x[b, ic_lo : ic_hi] (the k-tile's input
-//               channels) of the chunk's samples into a raw slot.
+//   warps 0, 1  bulk-copy producers (lane 0 each): per chunk, the contiguous slab
+//               dy[b0 : b0+nb] (and y, the ReLU mask source) by warp 0, and x[b, ic_lo :
+//               ic_hi] (the k-tile's input channels) of each sample by warp 1, into a raw slot.
 //   warp 2      MMA.
 //   G warps     (the first 8 formatter warps for fp32, 4 for bf16) lane = output channel;
 //               the chunk's columns, masked and split, into a TMEM operand stage with
@@ -676,7 +676,6 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
 //   X warps     (the other formatter warps) 16-byte units (row k, 4 or 8 columns) of the
 //               B stage.
 //   warps 3-18  epilogue: the fp32 tile to ws[split][oc][k] (row stride kpad).
-//   warp 1      idle.
 // ======================================================================================
 constexpr int WG_THREADS = FV_FMT0 + 32 * 16;
 constexpr int WG_MAXA = 8, WG_MAXB = 4, WG_MAXR = 3;
@@ -791,7 +790,7 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
     }
     if (tid == 0) {
         for (int i = 0; i < geo.raws; ++i) {
-            mbar_init(smem_u32(&bars->raw_full[i]), 1);
+            mbar_init(smem_u32(&bars->raw_full[i]), 2);  // the two producers' arrivals
             mbar_init(smem_u32(&bars->raw_empty[i]), 16);
         }
         for (int i = 0; i < geo.na; ++i) {
@@ -839,13 +838,16 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
         return ti;
     };
 
-    if (warp == 0) {
-        // ---------------- bulk-copy producer (lane 0) ----------------
-        // Per chunk: one copy of dy[b0 : b0+nb] (all channels, contiguous), one of y, and
-        // per sample one of x[b, ic_lo : ic_hi].  Sources are rounded down to 16 bytes (the
-        // slack is skipped when read); bytes of a last 16-byte block past the end of a
-        // tensor are copied by plain loads.
+    if (warp <= 1) {
+        // ---------------- bulk-copy producers ----------------
+        // Lane 0 of warp 0 copies dy[b0 : b0+nb] (all channels, contiguous) and y; lane 0
+        // of warp 1 copies x[b, ic_lo : ic_hi] of each sample: two threads on two SM
+        // sub-partitions, each arriving once (with its transaction bytes) on the slot's
+        // barrier.  Sources are rounded down to 16 bytes (the slack is skipped when read);
+        // bytes of a last 16-byte block past the end of a tensor are copied by plain loads
+        // before the arrival that releases them.
         if (lane == 0) {
+            const bool gside = warp == 0;
             const unsigned char* xb = reinterpret_cast<const unsigned char*>(x);
             const unsigned char* gb = reinterpret_cast<const unsigned char*>(dy);
             const unsigned char* yb = reinterpret_cast<const unsigned char*>(y);
@@ -853,9 +855,6 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
             const unsigned char* g_end = gb + size_t(p.B) * p.OCP * ES;
             const unsigned char* y_end = yb + size_t(p.B) * p.OCP * ES;
             const size_t xstride = size_t(p.IHW) * ES, gstride = size_t(p.OCP) * ES;
-            // A copy of [src, src + bytes) (src 16-byte aligned, bytes a multiple of 16): the
-            // bytes at or past the last 16-byte boundary before `end` by plain loads (done
-            // before the barrier's arrival releases them), the rest by one bulk copy.
             auto tail = [&](unsigned char* dstp, const unsigned char* src, int bytes, const unsigned char* end) -> int {
                 const int bulk = slab_bytes_bulk(src, bytes, end);
                 for (const unsigned char* t = src + bulk; t < src + bytes && t < end; ++t) dstp[int(t - src)] = *t;
@@ -874,29 +873,33 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
                     unsigned char* slot = raw + s * geo.raw_bytes;
                     const uint32_t slot_u32 = smem_u32(slot), bar = smem_u32(&bars->raw_full[s]);
                     const int b0 = ti.s_lo + ti.chunk(kc) * geo.nsc, nb = min(geo.nsc, ti.s_hi - b0);
-                    const size_t goff = size_t(b0) * gstride;
-                    const int gd = int(goff & 15);
-                    const int gbytes = round_up(gd + nb * int(gstride), 16);
-                    const size_t xoff0 = size_t(b0) * xstride + size_t(ti.ic_lo) * p.HW * ES;
-                    // Plain-load tails and transaction bytes, then the arrival, then the copies.
-                    const int gbulk = tail(slot, gb + goff - gd, gbytes, g_end);
-                    int tx = gbulk;
-                    if (RELU) tx += tail(slot + gregion, yb + goff - gd, gbytes, y_end);
-                    for (int j = 0; j < nb; ++j) {
-                        const size_t xo = xoff0 + size_t(j) * xstride;
-                        const int xd = int(xo & 15);
-                        tx += tail(slot + xoff + j * geo.xsb, xb + xo - xd, round_up(xd + xbytes, 16), x_end);
-                    }
-                    mbar_arrive_expect_tx(bar, uint32_t(tx));
-                    if (gbulk > 0) {
-                        bulk_g2s(slot_u32, gb + goff - gd, uint32_t(gbulk), bar);
-                        if (RELU) bulk_g2s(slot_u32 + gregion, yb + goff - gd, uint32_t(gbulk), bar);
-                    }
-                    for (int j = 0; j < nb; ++j) {
-                        const size_t xo = xoff0 + size_t(j) * xstride;
-                        const int xd = int(xo & 15);
-                        const int xbulk = slab_bytes_bulk(xb + xo - xd, round_up(xd + xbytes, 16), x_end);
-                        if (xbulk > 0) bulk_g2s(slot_u32 + uint32_t(xoff + j * geo.xsb), xb + xo - xd, uint32_t(xbulk), bar);
+                    if (gside) {
+                        const size_t goff = size_t(b0) * gstride;
+                        const int gd = int(goff & 15);
+                        const int gbytes = round_up(gd + nb * int(gstride), 16);
+                        const int gbulk = tail(slot, gb + goff - gd, gbytes, g_end);
+                        if (RELU) tail(slot + gregion, yb + goff - gd, gbytes, y_end);
+                        mbar_arrive_expect_tx(bar, uint32_t(gbulk * (RELU ? 2 : 1)));
+                        if (gbulk > 0) {
+                            bulk_g2s(slot_u32, gb + goff - gd, uint32_t(gbulk), bar);
+                            if (RELU) bulk_g2s(slot_u32 + gregion, yb + goff - gd, uint32_t(gbulk), bar);
+                        }
+                    } else {
+                        const unsigned char* xs = xb + size_t(b0) * xstride + size_t(ti.ic_lo) * p.HW * ES;
+                        int tx = 0;
+                        for (int j = 0; j < nb; ++j) {
+                            const int xd = int(reinterpret_cast<uintptr_t>(xs + size_t(j) * xstride) & 15);
+                            tx += tail(slot + xoff + j * geo.xsb, xs + size_t(j) * xstride - xd, round_up(xd + xbytes, 16),
+                                       x_end);
+                        }
+                        mbar_arrive_expect_tx(bar, uint32_t(tx));
+                        for (int j = 0; j < nb; ++j) {
+                            const unsigned char* src = xs + size_t(j) * xstride;
+                            const int xd = int(reinterpret_cast<uintptr_t>(src) & 15);
+                            const int xbulk = slab_bytes_bulk(src - xd, round_up(xd + xbytes, 16), x_end);
+                            if (xbulk > 0)
+                                bulk_g2s(slot_u32 + uint32_t(xoff + j * geo.xsb), src - xd, uint32_t(xbulk), bar);
+                        }
                     }
                 }
             }
