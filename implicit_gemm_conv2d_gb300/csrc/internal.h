@@ -2,6 +2,7 @@
 // ABI: validation, dispatch) and the kernel translation units.
 #pragma once
 #include <cstddef>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "../../include/conv.h"
@@ -65,9 +66,10 @@ cudaError_t run_dgrad_direct(const Plan&, const ConvParams&, int dt, const void*
 cudaError_t run_wgrad_direct(const Plan&, const ConvParams&, int dt, const void* x,
                              const void* dy, const void* y, void* dw, cudaStream_t s);
 // Deterministic split-K sum: dw = sum_{s < splits} ws[s] (fp32 partials, row
-// stride kpad), rounded once to the dtype.  splits == 0 writes zeros.
+// stride kpad), rounded once to the dtype.  splits == 0 writes zeros.  `overlapped`:
+// launched to overlap the kernel that writes ws (it waits for that kernel itself).
 cudaError_t run_wgrad_reduce(const ConvParams&, int dt, const float* ws, int splits, int kpad,
-                             void* dw, cudaStream_t s);
+                             void* dw, cudaStream_t s, bool overlapped = false);
 cudaError_t run_l2_flush(void* buf, size_t bytes, cudaStream_t s);
 
 // Dynamic shared memory above 48 KB needs a per-kernel opt-in on every device;
@@ -84,6 +86,27 @@ cudaError_t ensure_smem(int bytes)
     e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e == cudaSuccess && dev >= 0 && dev < 64) configured[dev] = bytes;
     return e;
+}
+
+// Launch `Kern` so that it may start while the previous kernel on the stream is still
+// running (programmatic dependent launch): the kernel must execute griddepcontrol.wait
+// before it reads anything that kernel writes.  Use only for the second kernel of a pair
+// whose first kernel was launched in plain stream order.
+template <class... KArgs, class... Args>
+cudaError_t launch_overlapped(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 // ---- tcgen05 tensor-core family (kernels_tc.cu) -------------------------------------

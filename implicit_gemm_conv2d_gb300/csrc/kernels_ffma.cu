@@ -459,6 +459,8 @@ template <typename T>
 __global__ void wgrad_reduce_kernel(const float* __restrict__ ws, int splits, int kpad, int OC,
                                     int Kred, FastDivmod dm_kred, T* __restrict__ dw)
 {
+    // When launched to overlap the partials kernel: wait for it (at once otherwise).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int total = OC * Kred;
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
         uint32_t oc, k;
@@ -731,11 +733,18 @@ cudaError_t run_wgrad_ffma(const Plan& pl, const ConvParams& p, int dt, const vo
 }
 
 cudaError_t run_wgrad_reduce(const ConvParams& p, int dt, const float* ws, int splits, int kpad,
-                             void* dw, cudaStream_t s)
+                             void* dw, cudaStream_t s, bool overlapped)
 {
     const int total = p.OC * p.Kred;
     const int grid = std::max(1, std::min(4096, ceil_div(total, 256)));
     const FastDivmod dm(uint32_t(p.Kred));
+    if (overlapped) {
+        return dt == DT_F32
+                   ? launch_overlapped(wgrad_reduce_kernel<float>, dim3(grid), dim3(256), 0, s, ws, splits, kpad,
+                                       p.OC, p.Kred, dm, (float*)dw)
+                   : launch_overlapped(wgrad_reduce_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, s, ws, splits,
+                                       kpad, p.OC, p.Kred, dm, (__nv_bfloat16*)dw);
+    }
     if (dt == DT_F32)
         wgrad_reduce_kernel<float><<<grid, 256, 0, s>>>(ws, splits, kpad, p.OC, p.Kred, dm, (float*)dw);
     else

@@ -151,6 +151,7 @@ template <typename T>
 __global__ void pack_fwd_w_kernel(const ConvParams p, const T* __restrict__ w, unsigned char* __restrict__ out,
                                   int nchunks, int oc_tiles, int OTp)
 {
+    grid_dep_launch();  // the implicit GEMM may start its prologue meanwhile
     using Tr = TcTraits<T>;
     const int tile_units = OTp * 8;
     const size_t total = size_t(oc_tiles) * nchunks * tile_units;
@@ -174,6 +175,7 @@ template <typename T>
 __global__ void pack_dgrad_w_kernel(const ConvParams p, const T* __restrict__ w, unsigned char* __restrict__ out,
                                     int nkt, int nch, int CIC, int KTp)
 {
+    grid_dep_launch();  // the implicit GEMM may start its prologue meanwhile
     using Tr = TcTraits<T>;
     const int tile_units = KTp * 8;
     const size_t total = size_t(nkt) * nch * tile_units;
@@ -453,6 +455,7 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
     } else if (warp == 1) {
         // ---------------- w producer ----------------
         if (lane == 0) {
+            grid_dep_wait();  // the packed weights come from the kernel launched just before
             RingPos wp;
             for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
                 const int ot = tile / geo.n_tiles;
@@ -1223,6 +1226,7 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
             }
         }
     }
+    grid_dep_launch();  // the split reduction may be scheduled now (it waits for this grid)
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
@@ -1407,6 +1411,7 @@ dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const unsigned cha
     if (warp == 1) {
         // ---------------- w producer ----------------
         if (lane == 0) {
+            grid_dep_wait();  // the packed weights come from the kernel launched just before
             RingPos wp;
             bool ok = true;
             for (int tile = blockIdx.x; tile < geo.ntiles && ok && !*abort_flag; tile += gridDim.x) {
@@ -1751,7 +1756,8 @@ static cudaError_t fwd_tc_t(const Plan& pl, const ConvParams& p, const void* x, 
     do {                                                                                            \
         e = ensure_smem<fwd_tc_kernel<T, R, 1>>(pl.smem);                                           \
         if (e == cudaSuccess)                                                                       \
-            fwd_tc_kernel<T, R, 1><<<pl.grid, pl.block, pl.smem, s>>>(p, (const T*)x, wpack, (T*)y, g); \
+            e = launch_overlapped(fwd_tc_kernel<T, R, 1>, dim3(pl.grid), dim3(pl.block), pl.smem, s, p,   \
+                                  (const T*)x, (const unsigned char*)wpack, (T*)y, g);                       \
     } while (0)
     if (p.relu) IG_LAUNCH_FWD_TC(true);
     else IG_LAUNCH_FWD_TC(false);
@@ -1849,7 +1855,7 @@ static cudaError_t wgrad_tc_t(const Plan& pl, const ConvParams& p, const void* x
         if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    return run_wgrad_reduce(p, dt_of_tc<T>(), (const float*)ws, pl.splits, kpad, dw, s);
+    return run_wgrad_reduce(p, dt_of_tc<T>(), (const float*)ws, pl.splits, kpad, dw, s, pl.splits > 0);
 }
 
 cudaError_t run_wgrad_tc(const Plan& pl, const ConvParams& p, int dt, const void* x, const void* dy,
@@ -1920,8 +1926,8 @@ static cudaError_t dgrad_tc_t(const Plan& pl, const ConvParams& p, const void* d
     do {                                                                                                   \
         e = ensure_smem<dgrad_tc_kernel<T, R, 1>>(pl.smem);                                                \
         if (e == cudaSuccess)                                                                              \
-            dgrad_tc_kernel<T, R, 1><<<pl.grid, pl.block, pl.smem, s>>>(p, (const T*)dy, wpack,            \
-                                                                        (const T*)y, (T*)dx, g);           \
+            e = launch_overlapped(dgrad_tc_kernel<T, R, 1>, dim3(pl.grid), dim3(pl.block), pl.smem, s, p, \
+                                  (const T*)dy, (const unsigned char*)wpack, (const T*)y, (T*)dx, g);      \
     } while (0)
     if (p.relu) IG_LAUNCH_DG_TC(true);
     else IG_LAUNCH_DG_TC(false);

@@ -138,6 +138,13 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar)
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// ---- programmatic dependent launch ---------------------------------------------------------
+// Wait until the kernel this one was launched to overlap has finished and its writes are
+// visible (returns at once when there is none).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next kernel (launched to overlap this one) be scheduled now.
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---- proxies and tcgen05 ordering --------------------------------------------------------
 // Generic-proxy shared-memory writes made visible to the async proxy (the MMA unit).
 __device__ __forceinline__ void fence_proxy_async_smem()
