@@ -1633,19 +1633,29 @@ dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const unsigned cha
                     for (int it = ft; it < p.HW * nsplit; it += DG_NFT) {
                         const int hw = it % p.HW, part = it / p.HW;
                         const int4 o = *reinterpret_cast<const int4*>(ptab + hw * DG_PROW);
-                        // Absent taps read the zero word kept past the Ds rows.
+                        // Absent taps read the zero word kept past the Ds rows and do not move
+                        // with the channel; present ones step by one channel's K*K values.
                         const uint32_t zero = ds_u32 + uint32_t(DG_TM * DG_DSTR * 4);
+                        const uint32_t kstep = uint32_t(p.KK * 4);
+                        const uint32_t d0 = o.x >= 0 ? kstep : 0u, d1 = o.y >= 0 ? kstep : 0u;
+                        const uint32_t d2 = o.z >= 0 ? kstep : 0u, d3 = o.w >= 0 ? kstep : 0u;
                         for (int sI = part; sI < ns; sI += nsplit) {
                             T* dxs = dx + size_t(b0 + sI) * p.IHW + size_t(ic0) * p.HW + hw;
                             const uint32_t ds = ds_u32 + uint32_t(sI * p.P * DG_DSTR * 4);
+                            uint32_t a0 = o.x >= 0 ? ds + uint32_t(o.x * 4) : zero;
+                            uint32_t a1 = o.y >= 0 ? ds + uint32_t(o.y * 4) : zero;
+                            uint32_t a2 = o.z >= 0 ? ds + uint32_t(o.z * 4) : zero;
+                            uint32_t a3 = o.w >= 0 ? ds + uint32_t(o.w * 4) : zero;
 #pragma unroll 4
                             for (int icl = 0; icl < nic; ++icl) {
-                                const uint32_t dk = ds + uint32_t(icl * p.KK * 4);
-                                const float a0 = __uint_as_float(lds32(o.x >= 0 ? dk + uint32_t(o.x * 4) : zero));
-                                const float a1 = __uint_as_float(lds32(o.y >= 0 ? dk + uint32_t(o.y * 4) : zero));
-                                const float a2 = __uint_as_float(lds32(o.z >= 0 ? dk + uint32_t(o.z * 4) : zero));
-                                const float a3 = __uint_as_float(lds32(o.w >= 0 ? dk + uint32_t(o.w * 4) : zero));
-                                Elem<T>::st(dxs + size_t(icl) * p.HW, ((a0 + a1) + a2) + a3);
+                                const float v0 = __uint_as_float(lds32(a0)), v1 = __uint_as_float(lds32(a1));
+                                const float v2 = __uint_as_float(lds32(a2)), v3 = __uint_as_float(lds32(a3));
+                                Elem<T>::st(dxs, ((v0 + v1) + v2) + v3);
+                                dxs += p.HW;
+                                a0 += d0;
+                                a1 += d1;
+                                a2 += d2;
+                                a3 += d3;
                             }
                         }
                     }
