@@ -1713,8 +1713,9 @@ template <> constexpr int dt_of_tc<__nv_bfloat16>() { return DT_BF16; }
 template <typename T>
 static bool pick_fwd(const ConvParams& p, const DevInfo& d, FwdGeom& out)
 {
-    // The deepest weight ring, then the longest x super-chunk, that fits.
-    static const int cfgs[][2] = {{4, 4}, {4, 2}, {3, 4}, {3, 2}, {2, 2}, {2, 1}};
+    // The deepest weight ring, then the longest x super-chunk (fewer, larger slab copies),
+    // that fits.
+    static const int cfgs[][2] = {{4, 8}, {4, 6}, {4, 4}, {4, 2}, {3, 4}, {3, 2}, {2, 2}, {2, 1}};
     for (const auto& c : cfgs) {
         const FwdGeom g = fwd_geom<T>(p, c[1], c[0]);
         if (g.na < 2 || fwd_smem<T>(p, g) > d.smem_optin || fwd_packed_bytes<T>(g) > kScratchBytes) continue;
