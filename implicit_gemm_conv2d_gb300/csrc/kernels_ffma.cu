@@ -462,11 +462,22 @@ __global__ void wgrad_reduce_kernel(const float* __restrict__ ws, int splits, in
     // When launched to overlap the partials kernel: wait for it (at once otherwise).
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int total = OC * Kred;
+    const size_t sstride = size_t(OC) * kpad;
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
         uint32_t oc, k;
         dm_kred.divmod(uint32_t(i), oc, k);
+        const float* src = ws + size_t(oc) * kpad + k;
+        // Loads in groups of 8 issued together, added in ascending split order.
         float s = 0.f;
-        for (int sp = 0; sp < splits; ++sp) s += ws[(size_t(sp) * OC + oc) * kpad + k];
+        int sp = 0;
+        for (; sp + 8 <= splits; sp += 8) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = __ldcg(src + size_t(sp + u) * sstride);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) s += v[u];
+        }
+        for (; sp < splits; ++sp) s += __ldcg(src + size_t(sp) * sstride);
         Elem<T>::st(dw + i, s);
     }
 }

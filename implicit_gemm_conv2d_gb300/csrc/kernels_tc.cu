@@ -681,7 +681,7 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
 //   warps 3-18  epilogue: the fp32 tile to ws[split][oc][k] (row stride kpad).
 // ======================================================================================
 constexpr int WG_THREADS = FV_FMT0 + 32 * 16;
-constexpr int WG_MAXA = 8, WG_MAXB = 4, WG_MAXR = 3;
+constexpr int WG_MAXA = 8, WG_MAXB = 4, WG_MAXR = 5;
 // Formatter roles: G warps (a multiple of 4, one or more per TMEM lane quarter) and X
 // warps; the column groups of 8 words one G thread writes; the B-stage rows one X thread
 // builds (its k offsets stay in registers).  fp32 splits the warps evenly (G and X are
@@ -880,8 +880,9 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
                         const size_t goff = size_t(b0) * gstride;
                         const int gd = int(goff & 15);
                         const int gbytes = round_up(gd + nb * int(gstride), 16);
-                        const int gbulk = tail(slot, gb + goff - gd, gbytes, g_end);
-                        if (RELU) tail(slot + gregion, yb + goff - gd, gbytes, y_end);
+                        const bool at_end = b0 + nb == p.B;  // only then can a copy reach dy's end
+                        const int gbulk = at_end ? tail(slot, gb + goff - gd, gbytes, g_end) : gbytes;
+                        if (RELU && at_end) tail(slot + gregion, yb + goff - gd, gbytes, y_end);
                         mbar_arrive_expect_tx(bar, uint32_t(gbulk * (RELU ? 2 : 1)));
                         if (gbulk > 0) {
                             bulk_g2s(slot_u32, gb + goff - gd, uint32_t(gbulk), bar);
@@ -889,17 +890,20 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
                         }
                     } else {
                         const unsigned char* xs = xb + size_t(b0) * xstride + size_t(ti.ic_lo) * p.HW * ES;
+                        const bool at_end = b0 + nb == p.B;  // only then can a copy reach x's end
                         int tx = 0;
                         for (int j = 0; j < nb; ++j) {
                             const int xd = int(reinterpret_cast<uintptr_t>(xs + size_t(j) * xstride) & 15);
-                            tx += tail(slot + xoff + j * geo.xsb, xs + size_t(j) * xstride - xd, round_up(xd + xbytes, 16),
-                                       x_end);
+                            const int bytes = round_up(xd + xbytes, 16);
+                            tx += at_end ? tail(slot + xoff + j * geo.xsb, xs + size_t(j) * xstride - xd, bytes, x_end)
+                                         : bytes;
                         }
                         mbar_arrive_expect_tx(bar, uint32_t(tx));
                         for (int j = 0; j < nb; ++j) {
                             const unsigned char* src = xs + size_t(j) * xstride;
                             const int xd = int(reinterpret_cast<uintptr_t>(src) & 15);
-                            const int xbulk = slab_bytes_bulk(src - xd, round_up(xd + xbytes, 16), x_end);
+                            const int bytes = round_up(xd + xbytes, 16);
+                            const int xbulk = at_end ? slab_bytes_bulk(src - xd, bytes, x_end) : bytes;
                             if (xbulk > 0)
                                 bulk_g2s(slot_u32 + uint32_t(xoff + j * geo.xsb), src - xd, uint32_t(xbulk), bar);
                         }
@@ -1802,14 +1806,16 @@ static bool pick_wgrad(const ConvParams& p, const DevInfo& d, TcWgradGeom& out)
     const int nsc = wgrad_nsc(p.P, Tr::KC, Tr::KC / 4);
     int splits = std::max(1, d.sms / tiles);
     splits = std::min(splits, std::max(1, p.B / (2 * nsc)));
-    for (int nbs = 3; nbs >= 2; --nbs)
-        for (int raws = 3; raws >= 2; --raws) {
-            const TcWgradGeom g = wgrad_geom<T>(p, ktp, raws, nbs, splits);
-            if (g.na >= 2 && wgrad_smem<T>(g) <= d.smem_optin) {
-                out = g;
-                return true;
-            }
+    // The raw ring hides the bulk copies' latency (about 1.5k clocks from issue to landing),
+    // so it gets the deeper ring; two B stages suffice.
+    static const int cfgs[][2] = {{5, 2}, {4, 2}, {3, 3}, {3, 2}, {2, 2}};  // {raws, nbs}
+    for (const auto& c : cfgs) {
+        const TcWgradGeom g = wgrad_geom<T>(p, ktp, c[0], c[1], splits);
+        if (g.na >= 2 && wgrad_smem<T>(g) <= d.smem_optin) {
+            out = g;
+            return true;
         }
+    }
     return false;
 }
 
@@ -1837,7 +1843,7 @@ Plan plan_wgrad_tc(const ConvParams& p, int dt, const DevInfo& d)
     else pick_wgrad<float>(p, d, g);
     pl.smem = dt == DT_BF16 ? wgrad_smem<__nv_bfloat16>(g) : wgrad_smem<float>(g);
     pl.splits = g.splits;
-    pl.variant = (g.KTp * 4 + g.raws) * 4 + g.nbs;
+    pl.variant = (g.KTp * 8 + g.raws) * 4 + g.nbs;
     pl.launches = 2;
     pl.grid = std::min(g.k_tiles * g.oc_tiles * g.splits, d.sms);
     pl.workspace = size_t(g.splits) * p.OC * g.kpad * sizeof(float);
@@ -1852,7 +1858,7 @@ static cudaError_t wgrad_tc_t(const Plan& pl, const ConvParams& p, const void* x
     const int kpad = round_up(p.Kred, 4);
     if (pl.splits > 0) {
         const int v = pl.variant;
-        const TcWgradGeom g = wgrad_geom<T>(p, v / 16, (v / 4) % 4, v % 4, pl.splits);
+        const TcWgradGeom g = wgrad_geom<T>(p, v / 32, (v / 4) % 8, v % 4, pl.splits);
 #define IG_LAUNCH_WG_TC(R)                                                                                 \
     do {                                                                                                   \
         e = ensure_smem<wgrad_tc_kernel<T, R>>(pl.smem);                                                   \
