@@ -245,6 +245,8 @@ struct FwdGeom {
     int w_bytes;        // one weight stage
     int dcols;          // accumulator columns (2*OTp for split fp32)
     int acol0, acols;   // first TMEM column of the operand stages, columns per stage
+    int splits;         // K ranges (split-K when there are too few column tiles)
+    int kc_per;         // K-chunks per range (a multiple of xg)
 };
 
 struct FwdBars {
@@ -281,7 +283,25 @@ inline FwdGeom fwd_geom(const ConvParams& p, int xg, int nw)
     g.acol0 = round_up(g.dcols, 32);
     g.acols = Tr::split ? 2 * Tr::KC : Tr::KC / 2;
     g.na = std::min(FA_MAXA, (FA_TMEM_COLS - g.acol0) / g.acols);
+    g.splits = 1;
+    g.kc_per = g.nchunks;
     return g;
+}
+
+// K ranges for a forward with fewer column tiles than half the SMs: enough ranges to
+// cover the SMs, each a whole number of x super-chunks, their fp32 partials fitting in
+// the scratch buffer beside the packed weights.
+inline void fwd_set_splits(FwdGeom& g, const ConvParams& p, int sms, size_t packed, size_t scratch)
+{
+    const int tiles = g.n_tiles * g.oc_tiles;
+    if (2 * tiles >= sms || g.nchunks < 2 * g.xg) return;
+    const size_t part = size_t(p.N) * g.oc_tiles * g.OTp * 4;  // one range's partials
+    const size_t room = scratch > packed + 256 ? scratch - round_up(packed, 256) : 0;
+    int want = std::min(sms / tiles, int(room / part));
+    want = std::min(want, g.nchunks / g.xg);
+    if (want < 2) return;
+    g.kc_per = round_up(ceil_div(g.nchunks, want), g.xg);
+    g.splits = ceil_div(g.nchunks, g.kc_per);
 }
 
 template <typename T>
@@ -352,7 +372,7 @@ struct RingPos {
 template <typename T, bool RELU, int SWZ>
 __global__ void __launch_bounds__(FA_THREADS, 1)
 fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* __restrict__ wpack,
-              T* __restrict__ y, const FwdGeom geo)
+              T* __restrict__ y, float* __restrict__ part, const FwdGeom geo)
 {
     using Tr = TcTraits<T>;
     constexpr int ES = int(sizeof(T));
@@ -398,8 +418,13 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tslot;
-    const int total_tiles = geo.n_tiles * geo.oc_tiles;
-    const int nsuper = (geo.nchunks + geo.xg - 1) / geo.xg;
+    // Tile = (column tile, oc tile, K range); K range sp covers chunks [sp*kc_per, ...).
+    const int ctiles = geo.n_tiles * geo.oc_tiles;
+    const int total_tiles = ctiles * geo.splits;
+    auto krange = [&](int tile, int& lo, int& hi) {
+        lo = (tile / ctiles) * geo.kc_per;
+        hi = min(geo.nchunks, lo + geo.kc_per);
+    };
 
     if (warp == 0) {
         // ---------------- x producer ----------------
@@ -410,7 +435,9 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
             const int n0 = (tile % geo.n_tiles) * FA_TM;
             const int n_end = min(n0 + FA_TM, p.N);
             const int b_first = n0 / p.P, nsamp = (n_end - 1) / p.P - b_first + 1;
-            for (int sc = 0; sc < nsuper; ++sc, rp.next(FV_RAWS)) {
+            int kc_lo, kc_hi;
+            krange(tile, kc_lo, kc_hi);
+            for (int sc = kc_lo / geo.xg; sc < (kc_hi + geo.xg - 1) / geo.xg; ++sc, rp.next(FV_RAWS)) {
                 const int s = rp.i;
                 if (rp.wrapped && !mbar_wait_or_abort(smem_u32(&bars->raw_empty[s]), rp.ph ^ 1u, abort_flag)) {
                     report(const_cast<int*>(abort_flag), 4u);
@@ -458,9 +485,11 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
             grid_dep_wait();  // the packed weights come from the kernel launched just before
             RingPos wp;
             for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
-                const int ot = tile / geo.n_tiles;
-                const unsigned char* src = wpack + size_t(ot) * geo.nchunks * geo.w_bytes;
-                for (int kc = 0; kc < geo.nchunks; ++kc, wp.next(geo.nw), src += geo.w_bytes) {
+                const int ot = (tile / geo.n_tiles) % geo.oc_tiles;
+                int kc_lo, kc_hi;
+                krange(tile, kc_lo, kc_hi);
+                const unsigned char* src = wpack + (size_t(ot) * geo.nchunks + kc_lo) * geo.w_bytes;
+                for (int kc = kc_lo; kc < kc_hi; ++kc, wp.next(geo.nw), src += geo.w_bytes) {
                     if (wp.wrapped && !mbar_wait_or_abort(smem_u32(&bars->w_empty[wp.i]), wp.ph ^ 1u, abort_flag)) {
                         report(const_cast<int*>(abort_flag), 16u);
                         break;
@@ -488,7 +517,9 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
                     break;
                 }
                 tc_fence_after();
-                for (int kc = 0; kc < geo.nchunks; ++kc, wp.next(geo.nw), ap.next(geo.na)) {
+                int kc_lo, kc_hi;
+                krange(tile, kc_lo, kc_hi);
+                for (int kc = kc_lo; kc < kc_hi; ++kc, wp.next(geo.nw), ap.next(geo.na)) {
                     if (!mbar_wait_or_abort(smem_u32(&bars->w_full[wp.i]), wp.ph, abort_flag) ||
                         !mbar_wait_or_abort(smem_u32(&bars->a_full[ap.i]), ap.ph, abort_flag)) {
                         report(const_cast<int*>(abort_flag), 8u);
@@ -501,7 +532,7 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const uint64_t bd = op_desc<SWZ>(wa + kstep_off<SWZ>(j));
-                        const uint32_t acc = (kc == 0 && j == 0) ? 0u : 1u;
+                        const uint32_t acc = (kc == kc_lo && j == 0) ? 0u : 1u;
                         if constexpr (Tr::split) {
                             mma_tf32_ta(tmem, aa + 8 * j, bd, idesc2, acc);           // hi * [hi; lo]
                             mma_tf32_ta(tmem, aa + Tr::KC + 8 * j, bd, idesc1, 1u);  // lo * hi
@@ -529,9 +560,11 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
         RingPos ap, rp;
         uint32_t t = 0;
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++t) {
-            const int n0 = (tile % geo.n_tiles) * FA_TM, ot = tile / geo.n_tiles;
+            const int n0 = (tile % geo.n_tiles) * FA_TM, ot = (tile / geo.n_tiles) % geo.oc_tiles;
             const int b_first = n0 / p.P;
             const int n = n0 + m;
+            int kc_lo, kc_hi;
+            krange(tile, kc_lo, kc_hi);
             // Columns past N gather column N-1's values: their accumulator rows are
             // computed but never stored (rows of D depend only on rows of A).
             int boff, bmis;
@@ -545,7 +578,7 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
             bool ok = true;
             uint32_t sbase = 0;
             int xc = 0;  // chunk within the super-chunk
-            for (int kc = 0; kc < geo.nchunks; ++kc, ap.next(geo.na)) {
+            for (int kc = kc_lo; kc < kc_hi; ++kc, ap.next(geo.na)) {
                 if (xc == 0) {
                     if (!mbar_wait_or_abort(smem_u32(&bars->raw_full[rp.i]), rp.ph, abort_flag)) {
                         report(const_cast<int*>(abort_flag), 1u);
@@ -604,7 +637,7 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                const bool sc_end = (++xc == geo.xg) || kc == geo.nchunks - 1;
+                const bool sc_end = (++xc == geo.xg) || kc == kc_hi - 1;
                 if (lane == 0) {
                     mbar_arrive(smem_u32(&bars->a_full[ap.i]));
                     if (sc_end) mbar_arrive(smem_u32(&bars->raw_empty[rp.i]));
@@ -615,14 +648,19 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
                 }
             }
             if (!ok) break;
-            // Epilogue: TMEM -> y; this warp's lanes, every FA_KSPLIT-th group of 8 channels.
+            // Epilogue: TMEM -> y (or, with K ranges, -> this range's fp32 partials); this
+            // warp's lanes, every FA_KSPLIT-th group of 8 channels.
             if (!mbar_wait_or_abort(smem_u32(&bars->acc_full), t & 1, abort_flag)) {
                 report(const_cast<int*>(abort_flag), 2u);
                 break;
             }
             tc_fence_after();
             T* yc = nullptr;
-            if (n < p.N) yc = y + col_out(p, n);
+            float* pc = nullptr;
+            if (n < p.N) {
+                if (geo.splits == 1) yc = y + col_out(p, n);
+                else pc = part + (size_t(tile / ctiles) * p.N + n) * (geo.oc_tiles * geo.OTp) + ot * geo.OTp;
+            }
             for (int cb = sub * 8; cb < geo.OTp; cb += 8 * FA_KSPLIT) {
                 uint32_t r[8];
                 tmem_ld8(tmem + lane_bits + uint32_t(cb), r);
@@ -645,6 +683,11 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
                             Elem<T>::st(yc + size_t(oc) * p.P, f);
                         }
                     }
+                } else if (pc) {
+                    *reinterpret_cast<float4*>(pc + cb) = make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]),
+                                                                      __uint_as_float(r[2]), __uint_as_float(r[3]));
+                    *reinterpret_cast<float4*>(pc + cb + 4) = make_float4(
+                        __uint_as_float(r[4]), __uint_as_float(r[5]), __uint_as_float(r[6]), __uint_as_float(r[7]));
                 }
             }
             tc_fence_before();
@@ -656,6 +699,24 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, FA_TMEM_COLS);
+    }
+}
+
+// Sum of the forward's K-range partials in ascending range order, then ReLU, into y.
+template <typename T, bool RELU>
+__global__ void fwd_reduce_kernel(const ConvParams p, const float* __restrict__ part, int splits, int ocp,
+                                  T* __restrict__ y)
+{
+    grid_dep_wait();  // the partials come from the kernel launched just before
+    const size_t total = size_t(p.N) * p.OC;
+    const size_t sstride = size_t(p.N) * ocp;
+    for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < total; i += size_t(gridDim.x) * blockDim.x) {
+        const int n = int(i / p.OC), oc = int(i % p.OC);
+        const float* src = part + size_t(n) * ocp + oc;
+        float s = 0.f;
+        for (int sp = 0; sp < splits; ++sp) s += __ldcg(src + size_t(sp) * sstride);
+        if (RELU) s = s > 0.f ? s : 0.f;
+        Elem<T>::st(y + col_out(p, n) + size_t(oc) * p.P, s);
     }
 }
 
@@ -1719,12 +1780,21 @@ static bool pick_fwd(const ConvParams& p, const DevInfo& d, FwdGeom& out)
 {
     // The deepest weight ring, then the longest x super-chunk (fewer, larger slab copies),
     // that fits.
+    // With too few column tiles for the SMs the K ranges matter more: short super-chunks
+    // first, so that K splits into more ranges.
     static const int cfgs[][2] = {{4, 8}, {4, 6}, {4, 4}, {4, 2}, {3, 4}, {3, 2}, {2, 2}, {2, 1}};
-    for (const auto& c : cfgs) {
-        const FwdGeom g = fwd_geom<T>(p, c[1], c[0]);
-        if (g.na < 2 || fwd_smem<T>(p, g) > d.smem_optin || fwd_packed_bytes<T>(g) > kScratchBytes) continue;
-        out = g;
-        return true;
+    static const int cfgs_split[][2] = {{4, 2}, {3, 2}, {2, 2}, {4, 1}, {2, 1}};
+    const bool few = 2 * ceil_div(p.N, FA_TM) * ceil_div(p.OC, TcTraits<T>::split ? 128 : 256) < d.sms;
+    for (int pass = few ? 0 : 1; pass < 2; ++pass) {
+        const int ncfg = pass == 0 ? 5 : 8;
+        for (int i = 0; i < ncfg; ++i) {
+            const int* c = pass == 0 ? cfgs_split[i] : cfgs[i];
+            FwdGeom g = fwd_geom<T>(p, c[1], c[0]);
+            if (g.na < 2 || fwd_smem<T>(p, g) > d.smem_optin || fwd_packed_bytes<T>(g) > kScratchBytes) continue;
+            fwd_set_splits(g, p, d.sms, fwd_packed_bytes<T>(g), kScratchBytes);
+            out = g;
+            return true;
+        }
     }
     return false;
 }
@@ -1743,10 +1813,12 @@ Plan plan_fwd_tc(const ConvParams& p, int dt, const DevInfo& d)
     else pick_fwd<float>(p, d, g);
     Plan pl;
     pl.algo = ALGO_TC;
-    pl.launches = 2;  // weight packing, then the implicit GEMM
+    // weight packing, the implicit GEMM, and with K ranges the sum of their partials
+    pl.launches = g.splits > 1 ? 3 : 2;
     pl.block = FA_THREADS;
-    pl.variant = g.xg * 16 + g.nw;
-    pl.grid = std::min(g.n_tiles * g.oc_tiles, d.sms);
+    pl.splits = g.splits;
+    pl.variant = (g.kc_per * 16 + g.xg) * 16 + g.nw;
+    pl.grid = std::min(g.n_tiles * g.oc_tiles * g.splits, d.sms);
     pl.smem = dt == DT_BF16 ? fwd_smem<__nv_bfloat16>(p, g) : fwd_smem<float>(p, g);
     return pl;
 }
@@ -1756,7 +1828,9 @@ static cudaError_t fwd_tc_t(const Plan& pl, const ConvParams& p, const void* x, 
                             cudaStream_t s)
 {
     const int v = pl.variant;
-    const FwdGeom g = fwd_geom<T>(p, v / 16, v % 16);
+    FwdGeom g = fwd_geom<T>(p, (v / 16) % 16, v % 16);
+    g.kc_per = v / 256;
+    g.splits = ceil_div(g.nchunks, g.kc_per);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -1767,12 +1841,19 @@ static cudaError_t fwd_tc_t(const Plan& pl, const ConvParams& p, const void* x, 
     pack_fwd_w_kernel<T><<<pgrid, 256, 0, s>>>(p, (const T*)w, wpack, g.nchunks, g.oc_tiles, g.OTp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // The weight operand is always in the 128-byte swizzled layout the pack kernel writes.
+    float* part = reinterpret_cast<float*>(wpack + round_up(fwd_packed_bytes<T>(g), size_t(256)));
 #define IG_LAUNCH_FWD_TC(R)                                                                         \
     do {                                                                                            \
         e = ensure_smem<fwd_tc_kernel<T, R, 1>>(pl.smem);                                           \
         if (e == cudaSuccess)                                                                       \
             e = launch_overlapped(fwd_tc_kernel<T, R, 1>, dim3(pl.grid), dim3(pl.block), pl.smem, s, p,   \
-                                  (const T*)x, (const unsigned char*)wpack, (T*)y, g);                       \
+                                  (const T*)x, (const unsigned char*)wpack, (T*)y, part, g);                 \
+        if (e == cudaSuccess && g.splits > 1) {                                                     \
+            const size_t total = size_t(p.N) * p.OC;                                                \
+            const int rgrid = int(std::min<size_t>((total + 255) / 256, 4096));                     \
+            e = launch_overlapped(fwd_reduce_kernel<T, R>, dim3(rgrid), dim3(256), 0, s, p,           \
+                                  (const float*)part, g.splits, g.oc_tiles * g.OTp, (T*)y);            \
+        }                                                                                           \
     } while (0)
     if (p.relu) IG_LAUNCH_FWD_TC(true);
     else IG_LAUNCH_FWD_TC(false);
