@@ -1339,6 +1339,8 @@ struct TcDgradGeom {
     int acols;       // TMEM columns of one G buffer
     int nab;         // G buffers
     int ntiles;      // ceil(B / NS)
+    int ktsplit;     // k-tile ranges per sample tile (more work items when the tiles are few)
+    int kt_per;      // k-tiles per range
 };
 
 struct DgBars {
@@ -1370,6 +1372,8 @@ inline TcDgradGeom dgrad_geom(const ConvParams& p, int CIC, int nw)
     if (2 * g.dcols + g.acols > 512) g.ndb = 1;
     g.acol0 = g.ndb * g.dcols;
     g.ntiles = ceil_div(p.B, g.NS);
+    g.ktsplit = 1;
+    g.kt_per = g.nkt;
     auto axis_max = [](int n, int K, int S, int O) {
         int m = 0;
         for (int h = 0; h < n; ++h) {
@@ -1472,6 +1476,12 @@ dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const unsigned cha
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tslot;
+    // Work item wi = (sample tile wi % ntiles, k-tile range wi / ntiles).
+    const int nwork = geo.ntiles * geo.ktsplit;
+    auto ktrange = [&](int wi, int& lo, int& hi) {
+        lo = (wi / geo.ntiles) * geo.kt_per;
+        hi = min(geo.nkt, lo + geo.kt_per);
+    };
 
     if (warp == 1) {
         // ---------------- w producer ----------------
@@ -1479,9 +1489,11 @@ dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const unsigned cha
             grid_dep_wait();  // the packed weights come from the kernel launched just before
             RingPos wp;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < geo.ntiles && ok && !*abort_flag; tile += gridDim.x) {
-                const unsigned char* src = wpack;
-                for (int i = 0; i < geo.nkt * geo.nch; ++i, wp.next(geo.nw), src += geo.w_tile) {
+            for (int wi = blockIdx.x; wi < nwork && ok && !*abort_flag; wi += gridDim.x) {
+                int kt_lo, kt_hi;
+                ktrange(wi, kt_lo, kt_hi);
+                const unsigned char* src = wpack + size_t(kt_lo) * geo.nch * geo.w_tile;
+                for (int i = 0; i < (kt_hi - kt_lo) * geo.nch; ++i, wp.next(geo.nw), src += geo.w_tile) {
                     if (wp.wrapped && !mbar_wait_or_abort(smem_u32(&bars->w_empty[wp.i]), wp.ph ^ 1u, abort_flag)) {
                         report(const_cast<int*>(abort_flag), 16u);
                         ok = false;
@@ -1502,13 +1514,15 @@ dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const unsigned cha
             const uint32_t w_u32 = smem_u32(wring);
             RingPos wp, abp, dbp;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < geo.ntiles && ok && !*abort_flag; tile += gridDim.x, abp.next(geo.nab)) {
+            for (int wi = blockIdx.x; wi < nwork && ok && !*abort_flag; wi += gridDim.x, abp.next(geo.nab)) {
+                int kt_lo, kt_hi;
+                ktrange(wi, kt_lo, kt_hi);
                 if (!mbar_wait_or_abort(smem_u32(&bars->a_full[abp.i]), abp.ph, abort_flag)) {
                     report(const_cast<int*>(abort_flag), 8u);
                     break;
                 }
                 const uint32_t ga = tmem + uint32_t(geo.acol0 + abp.i * geo.acols);
-                for (int kt = 0; kt < geo.nkt && ok; ++kt, dbp.next(geo.ndb)) {
+                for (int kt = kt_lo; kt < kt_hi && ok; ++kt, dbp.next(geo.ndb)) {
                     if (dbp.wrapped &&
                         !mbar_wait_or_abort(smem_u32(&bars->acc_empty[dbp.i]), dbp.ph ^ 1u, abort_flag)) {
                         report(const_cast<int*>(abort_flag), 8u);
@@ -1638,16 +1652,19 @@ dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const unsigned cha
         RingPos abp, dbp;
         bool ok = true;
         const int first = blockIdx.x;
-        if (first < geo.ntiles) ok = build_g(first, abp);
-        for (int tile = first; tile < geo.ntiles && ok; tile += gridDim.x) {
+        if (first < nwork) ok = build_g(first % geo.ntiles, abp);
+        for (int wi = first; wi < nwork && ok; wi += gridDim.x) {
+            const int tile = wi % geo.ntiles;
+            int kt_lo, kt_hi;
+            ktrange(wi, kt_lo, kt_hi);
             RingPos nab = abp;
             nab.next(geo.nab);
-            const int next = tile + int(gridDim.x);
+            const int next = wi + int(gridDim.x);
             // With two G buffers the next tile's G is written before this tile's k-tiles
             // are read out, so the MMAs move on to it without waiting.
-            if (geo.nab == 2 && next < geo.ntiles && !(ok = build_g(next, nab))) break;
+            if (geo.nab == 2 && next < nwork && !(ok = build_g(next % geo.ntiles, nab))) break;
             const int b0 = tile * geo.NS, ns = min(geo.NS, p.B - b0);
-            for (int kt = 0; kt < geo.nkt; ++kt, dbp.next(geo.ndb)) {
+            for (int kt = kt_lo; kt < kt_hi; ++kt, dbp.next(geo.ndb)) {
                 if (!mbar_wait_or_abort(smem_u32(&bars->acc_full[dbp.i]), dbp.ph, abort_flag)) {
                     report(const_cast<int*>(abort_flag), 2u);
                     ok = false;
@@ -1751,7 +1768,7 @@ dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const unsigned cha
                 }
             }
             if (!ok) break;
-            if (geo.nab == 1 && next < geo.ntiles && !(ok = build_g(next, nab))) break;
+            if (geo.nab == 1 && next < nwork && !(ok = build_g(next % geo.ntiles, nab))) break;
             abp = nab;
         }
     }
@@ -1972,9 +1989,14 @@ static bool pick_dgrad(const ConvParams& p, const DevInfo& d, TcDgradGeom& out)
     if (p.B <= 0 || p.KK > 128 || p.P > DG_TM) return false;
     for (int cic = std::min(p.IC, 128 / p.KK); cic >= 1; --cic) {
         for (int nw = 4; nw >= 2; --nw) {
-            const TcDgradGeom g = dgrad_geom<T>(p, cic, nw);
+            TcDgradGeom g = dgrad_geom<T>(p, cic, nw);
             if (g.dcols * g.ndb + g.acols * g.nab > 512) continue;
             if (dgrad_smem<T>(p, g) <= d.smem_optin && dgrad_packed_bytes<T>(g) <= kScratchBytes) {
+                if (2 * g.ntiles < d.sms) {  // few sample tiles: split the k-tiles too
+                    const int want = std::min(g.nkt, d.sms / g.ntiles);
+                    g.kt_per = ceil_div(g.nkt, want);
+                    g.ktsplit = ceil_div(g.nkt, g.kt_per);
+                }
                 out = g;
                 return true;
             }
@@ -1999,8 +2021,8 @@ Plan plan_dgrad_tc(const ConvParams& p, int dt, const DevInfo& d)
     pl.algo = ALGO_TC;
     pl.launches = 2;  // weight packing, then the implicit GEMM + col2im
     pl.block = DG_THREADS;
-    pl.variant = g.CIC * 8 + g.nw;
-    pl.grid = std::min(g.ntiles, d.sms);
+    pl.variant = (g.kt_per * 128 + g.CIC) * 8 + g.nw;
+    pl.grid = std::min(g.ntiles * g.ktsplit, d.sms);
     pl.smem = dt == DT_BF16 ? dgrad_smem<__nv_bfloat16>(p, g) : dgrad_smem<float>(p, g);
     return pl;
 }
@@ -2009,7 +2031,9 @@ template <typename T>
 static cudaError_t dgrad_tc_t(const Plan& pl, const ConvParams& p, const void* dy, const void* w,
                               const void* y, void* dx, int, cudaStream_t s)
 {
-    const TcDgradGeom g = dgrad_geom<T>(p, pl.variant / 8, pl.variant % 8);
+    TcDgradGeom g = dgrad_geom<T>(p, (pl.variant / 8) % 128, pl.variant % 8);
+    g.kt_per = pl.variant / 1024;
+    g.ktsplit = ceil_div(g.nkt, g.kt_per);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
