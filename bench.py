@@ -84,6 +84,33 @@ def parse():
     return ap.parse_args()
 
 
+def combine_ranks(ms_step, world, device):
+    """The slowest rank's step time (every rank gets it): replicas finish together only as
+    fast as the slowest one."""
+    if world == 1:
+        return ms_step
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms_step)], device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(ms_step_max, world, flops_per_op):
+    """Whole-job GFLOP/s: every rank runs the full three-operation step on its own batch."""
+    return world * 3 * flops_per_op / (ms_step_max * 1e-3) / 1e9
+
+
+def workload_config(layer, dtype, batch):
+    shp = LAYERS[layer]
+    OH, OW = (shp["H"] - shp["K"]) // shp["S"] + 1, (shp["W"] - shp["K"]) // shp["S"] + 1
+    return {"workload": (f"{layer} conv {dtype} fwd+dgrad+wgrad"
+                         f"{', fused ReLU' if shp['relu'] else ''}, B={batch} IC={shp['IC']} "
+                         f"OC={shp['OC']} {shp['H']}x{shp['W']} K={shp['K']} S={shp['S']} -> {OH}x{OW} "
+                         "(PufferLib PR #522 encoder conv" + ("1)" if layer == "layer1" else "2)")),
+            "inputs": "x~N(0,1), w~U(+-1/sqrt(IC*K*K)), dy~N(0,1), SplitMix64 seed 0x5EED2026"}
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -220,11 +247,11 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": "layer-1 conv fwd+dgrad+wgrad, fused ReLU, IC=59 OC=128 11x15 K=5 S=3; "
-                               f"each step a {b_sample}-sample slice of the B=1024 batch",
-                   "l2": "n/a (host)"},
+        "config": workload_config("layer1", "f32", 1024),
         "cpu_baseline": {"value": value, "unit": "GFLOP/s", "cores": oracle.default_threads(),
-                         "kind": "oracle", "sample": f"{b_sample} samples per step"},
+                         "kind": "oracle",
+                         "sample": f"each step the fp64 oracle on {b_sample} of the 1024 samples (the same "
+                                   "shapes and seeded inputs); GFLOP/s counts the sample's FLOPs"},
         "e2e": {"value": value, "unit": "GFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -490,12 +517,8 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    ms_step = sum(total) / len(total)
-    if world > 1:
-        t = torch.tensor([ms_step], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
-    value = world * 3 * wl.flops / (ms_step * 1e-3) / 1e9
+    ms_step = combine_ranks(sum(total) / len(total), world, device)
+    value = job_value(ms_step, world, wl.flops)
 
     if rank != 0:
         if world > 1:
@@ -520,23 +543,16 @@ def run_ours(args):
                   "bound": r["bound"], "frac": r["frac"], "roofline_us": r["roofline_us"]}
     pr = PR522_US.get((args.layer, args.dtype))
     pr_gflops = 3 * wl.flops / ((pr[0] + pr[1]) * 1e-6) / 1e9 if (pr and args.batch == 1024) else None
-    shp = LAYERS[args.layer]
-    OH, OW = (shp["H"] - shp["K"]) // shp["S"] + 1, (shp["W"] - shp["K"]) // shp["S"] + 1
-
     line = {
         "metric": METRIC, "value": value, "unit": "GFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": (value / world / pr_gflops) if pr_gflops else None,
         "dtype": args.dtype, "data": "synthetic",
-        "config": {"workload": (f"{args.layer} conv {args.dtype} fwd+dgrad+wgrad"
-                                f"{', fused ReLU' if shp['relu'] else ''}, B={args.batch} IC={shp['IC']} "
-                                f"OC={shp['OC']} {shp['H']}x{shp['W']} K={shp['K']} S={shp['S']} -> {OH}x{OW} "
-                                "(PufferLib PR #522 encoder conv" + ("1)" if args.layer == "layer1" else "2)")),
-                   "l2": "flushed (512 MiB write) between timed steps, outside the timed region",
-                   "launch": "each operation replayed from a captured CUDA graph" if not args.no_graphs
-                   else "eager launches",
-                   "algo": args.algo,
-                   "inputs": "x~N(0,1), w~U(+-1/sqrt(IC*K*K)), dy~N(0,1), SplitMix64 seed 0x5EED2026"},
+        "config": dict(workload_config(args.layer, args.dtype, args.batch),
+                       l2="flushed (512 MiB write) between timed steps, outside the timed region",
+                       launch=("each operation replayed from a captured CUDA graph" if not args.no_graphs
+                               else "eager launches"),
+                       algo=args.algo),
         "ops": ops,
         "roofline": roofline,
         "gpu_launches": wl.launches * args.steps,
