@@ -1,4 +1,5 @@
-"""fp64 CPU oracle for the conv2d layer (forward + ReLU, d_input, wgrad).
+"""fp64 CPU oracle for the conv2d layer (forward + bias + ReLU, d_input, wgrad,
+bias grad).
 
 TEST INFRASTRUCTURE ONLY.  The product path never imports this package; only
 the tests, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg do.
@@ -8,7 +9,10 @@ module builds it with gcc on first use and marshals numpy arrays in and out.
 Definitions follow PufferLib PR #522 ("Speedups to gemm_conv_forward and
 gemm_conv_backward kernels"), whose layer-1 and layer-2 bench blocks name the
 forward, "backward wgrad" and "backward d_input" results and print the shapes
-11x15 K=5 S=3 -> 3x4 (relu=1) and 3x4 K=3 S=1 -> 1x2 (relu=0).
+11x15 K=5 S=3 -> 3x4 (relu=1) and 3x4 K=3 S=1 -> 1x2 (relu=0); the bias is the
+per-output-channel conv bias whose gradient the same PR's "n3_conv_bias_grad"
+blocks time (added before the activation in the forward; its gradient is the
+sum of the masked output gradient over batch and positions).
 
 Every function returns ``(out, den)`` where ``den`` holds, per output element,
 the sum of |term| over the products that element sums; the normalised error of
@@ -60,7 +64,10 @@ def bind(path: str):
     lib.oracle_conv_fwd.argtypes = [sp, dp, dp, dp, dp, ctypes.c_int]
     lib.oracle_conv_bwd_data.argtypes = [sp, dp, dp, dp, dp, dp, ctypes.c_int]
     lib.oracle_conv_bwd_filter.argtypes = [sp, dp, dp, dp, dp, dp, ctypes.c_int]
-    for f in (lib.oracle_conv_fwd, lib.oracle_conv_bwd_data, lib.oracle_conv_bwd_filter):
+    lib.oracle_conv_fwd_bias.argtypes = [sp, dp, dp, dp, dp, dp, ctypes.c_int]
+    lib.oracle_conv_bwd_bias.argtypes = [sp, dp, dp, dp, dp, ctypes.c_int]
+    for f in (lib.oracle_conv_fwd, lib.oracle_conv_bwd_data, lib.oracle_conv_bwd_filter,
+              lib.oracle_conv_fwd_bias, lib.oracle_conv_bwd_bias):
         f.restype = ctypes.c_int
     lib.oracle_out_dim.argtypes = [ctypes.c_int64] * 3
     lib.oracle_out_dim.restype = ctypes.c_int64
@@ -99,8 +106,9 @@ def _shape(B, IC, OC, H, W, K, S, relu):
     return _Shape(B, IC, OC, H, W, K, S, 1 if relu else 0)
 
 
-def conv_fwd(x, w, S: int, relu: bool, nthreads: int | None = None, lib=None):
-    """y = act(conv(x, w)) with x (B,IC,H,W), w (OC,IC,K,K).  Returns (y, den)."""
+def conv_fwd(x, w, S: int, relu: bool, nthreads: int | None = None, lib=None, bias=None):
+    """y = act(conv(x, w) + bias) with x (B,IC,H,W), w (OC,IC,K,K), bias (OC,) or None
+    (no bias term).  Returns (y, den); den includes |bias[oc]|."""
     x, w = _f64(x), _f64(w)
     B, IC, H, W = x.shape
     OC, IC2, K, K2 = w.shape
@@ -108,9 +116,16 @@ def conv_fwd(x, w, S: int, relu: bool, nthreads: int | None = None, lib=None):
     OH, OW = out_dim(H, K, S), out_dim(W, K, S)
     y = np.empty((B, OC, OH, OW))
     den = np.empty_like(y)
-    rc = (lib or _load()).oracle_conv_fwd(ctypes.byref(_shape(B, IC, OC, H, W, K, S, relu)),
-                                 _ptr(x), _ptr(w), _ptr(y), _ptr(den),
+    lib = lib or _load()
+    shape = ctypes.byref(_shape(B, IC, OC, H, W, K, S, relu))
+    if bias is None:
+        rc = lib.oracle_conv_fwd(shape, _ptr(x), _ptr(w), _ptr(y), _ptr(den),
                                  nthreads or default_threads())
+    else:
+        bias = _f64(bias)
+        assert bias.shape == (OC,)
+        rc = lib.oracle_conv_fwd_bias(shape, _ptr(x), _ptr(w), _ptr(bias), _ptr(y), _ptr(den),
+                                      nthreads or default_threads())
     if rc != 0:
         raise ValueError(f"oracle_conv_fwd rejected the arguments (rc={rc})")
     return y, den
@@ -150,6 +165,23 @@ def conv_bwd_filter(x, dy, y, K: int, S: int, relu: bool, nthreads: int | None =
     if rc != 0:
         raise ValueError(f"oracle_conv_bwd_filter rejected the arguments (rc={rc})")
     return dw, den
+
+
+def conv_bwd_bias(dy, y, relu: bool, nthreads: int | None = None, lib=None):
+    """db (OC,) = sum over b, oh, ow of dy (B,OC,OH,OW), masked by y > 0 when relu.
+    Returns (db, den)."""
+    dy = _f64(dy)
+    y = _f64(y) if (relu and y is not None) else None
+    B, OC, OH, OW = dy.shape
+    db = np.empty((OC,))
+    den = np.empty_like(db)
+    # The shape record wants a window; K = S = 1 over an OH x OW input reproduces OH x OW.
+    rc = (lib or _load()).oracle_conv_bwd_bias(ctypes.byref(_shape(B, 1, OC, OH, OW, 1, 1, relu)),
+                                      _ptr(dy), _ptr(y), _ptr(db), _ptr(den),
+                                      nthreads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle_conv_bwd_bias rejected the arguments (rc={rc})")
+    return db, den
 
 
 def normalised_error(out, ref, den) -> float:

@@ -24,6 +24,13 @@
  *                              ow*S+kw = w of g[b,oc,oh,ow] * w[oc,ic,kh,kw]
  *   wgrad     dw[oc,ic,kh,kw] = sum_{b,oh,ow} g[b,oc,oh,ow] * x[b,ic,oh*S+kh,ow*S+kw]
  *
+ * The layer's bias (the same PR's "n3_conv_bias_grad" bench blocks time the
+ * gradient of a per-output-channel conv bias, conv1: OC=128 x 12 positions,
+ * conv2: OC=128 x 2): the bias is added to the sum before the activation,
+ *
+ *   forward+bias  y[b,oc,oh,ow] = act( bias[oc] + sum_{ic,kh,kw} ... as above )
+ *   bias grad     db[oc]        = sum_{b,oh,ow} g[b,oc,oh,ow]
+ *
  * Each output is accumulated in fp64 by direct loops in a fixed order, and
  * its "denominator" D = sum of |term| over the same terms is returned beside
  * it, so that a caller can form the normalised error |out - ref| / D.
@@ -34,10 +41,11 @@
  * Threads: every output element is computed start-to-finish by one thread
  * in the same order, so results do not depend on the thread count.
  *
- * Parity pins: brute force against an independent im2col-matrix formulation,
- * the 1x1/stride-1 matmul special case, the delta-input case, the adjoint
- * identity, central finite differences and the printed output sizes (tests in
- * tests/test_oracle.py).
+ * Parity pins: brute force against an independent im2col-matrix formulation
+ * (with the bias as an extra row of ones), the 1x1/stride-1 matmul special
+ * case, the delta-input case, the zero-weight case (y = act(bias)), the
+ * adjoint identity, central finite differences (in x, w and the bias) and the
+ * printed output sizes (tests in tests/test_oracle.py).
  */
 #include <math.h>
 #include <pthread.h>
@@ -68,7 +76,7 @@ typedef struct {
     int64_t lo, hi;          /* range of the outermost loop index */
 } ref_job_t;
 
-/* ---- forward: outer index b ------------------------------------------------ */
+/* ---- forward: outer index b; j->c is the bias (OC) or NULL ---------------- */
 static void* ref_fwd_range(void* arg)
 {
     const ref_job_t* j = (const ref_job_t*)arg;
@@ -90,6 +98,11 @@ static void* ref_fwd_range(void* arg)
                                 acc += t;
                                 den += fabs(t);
                             }
+                    if (j->c) { /* bias, added to the finished sum */
+                        const double bv = j->c[oc];
+                        acc += bv;
+                        den += fabs(bv);
+                    }
                     const int64_t o = ((b * s->OC + oc) * OH + oh) * OW + ow;
                     j->out[o] = (s->relu && !(acc > 0.0)) ? 0.0 : acc;
                     if (j->den) j->den[o] = den;
@@ -165,6 +178,29 @@ static void* ref_wgrad_range(void* arg)
     return NULL;
 }
 
+/* ---- bias grad: outer index oc -------------------------------------------- */
+static void* ref_bgrad_range(void* arg)
+{
+    const ref_job_t* j = (const ref_job_t*)arg;
+    const ref_shape_t* s = j->s;
+    const double* dy = j->a;
+    const double* y = j->c;
+    const int64_t OH = ref_out_dim(s->H, s->K, s->S), OW = ref_out_dim(s->W, s->K, s->S);
+    for (int64_t oc = j->lo; oc < j->hi; ++oc) {
+        double acc = 0.0, den = 0.0;
+        for (int64_t b = 0; b < s->B; ++b)
+            for (int64_t oh = 0; oh < OH; ++oh)
+                for (int64_t ow = 0; ow < OW; ++ow) {
+                    const double t = ref_g(s, dy, y, ((b * s->OC + oc) * OH + oh) * OW + ow);
+                    acc += t;
+                    den += fabs(t);
+                }
+        j->out[oc] = acc;
+        if (j->den) j->den[oc] = den;
+    }
+    return NULL;
+}
+
 /* Split [0, n) into nthreads contiguous ranges and run fn on each. */
 static int ref_run(void* (*fn)(void*), ref_job_t proto, int64_t n, int nthreads)
 {
@@ -223,4 +259,22 @@ int oracle_conv_bwd_filter(const ref_shape_t* s, const double* x, const double* 
     if (!ref_valid(s) || !x || !dy || !dw || (s->relu && !y)) return -1;
     ref_job_t p = {s, x, dy, y, dw, den, 0, 0};
     return ref_run(ref_wgrad_range, p, s->OC, nthreads);
+}
+
+/* y, den: (B,OC,OH,OW); bias: (OC), required.  den may be NULL. */
+int oracle_conv_fwd_bias(const ref_shape_t* s, const double* x, const double* w,
+                         const double* bias, double* y, double* den, int nthreads)
+{
+    if (!ref_valid(s) || !x || !w || !bias || !y) return -1;
+    ref_job_t p = {s, x, w, bias, y, den, 0, 0};
+    return ref_run(ref_fwd_range, p, s->B, nthreads);
+}
+
+/* db, den: (OC).  y is required when s->relu, ignored otherwise. */
+int oracle_conv_bwd_bias(const ref_shape_t* s, const double* dy, const double* y, double* db,
+                         double* den, int nthreads)
+{
+    if (!ref_valid(s) || !dy || !db || (s->relu && !y)) return -1;
+    ref_job_t p = {s, dy, NULL, y, db, den, 0, 0};
+    return ref_run(ref_bgrad_range, p, s->OC, nthreads);
 }

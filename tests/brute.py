@@ -1,7 +1,8 @@
 """Independent second formulation of the conv2d layer, used only to pin the
 oracle: the patch matrix (im2col) is materialised by strided slicing and
 multiplied with numpy matmul; d_input scatters the patch-matrix gradient back
-by the transpose of the same slicing.  No loop order, index formula or helper
+by the transpose of the same slicing; the bias rides in the matmul as a row of
+ones, and its gradient is a product with vectors of ones.  No loop order, index formula or helper
 is shared with oracle/conv_ref.c.
 """
 import numpy as np
@@ -34,14 +35,21 @@ def unpatch(cols, IC, H, W, K, S):
     return dx
 
 
-def fwd(x, w, S, relu):
+def fwd(x, w, S, relu, bias=None):
+    """With a bias, the patch matrix gets an extra row of ones and the weight
+    matrix an extra column holding the bias, so the bias rides in the matmul."""
     x = np.asarray(x, np.float64)
     w = np.asarray(w, np.float64)
     B, IC, H, W = x.shape
     OC, _, K, _ = w.shape
     OH, OW = out_hw(H, W, K, S)
-    pre = np.matmul(w.reshape(OC, -1), patches(x, K, S)).reshape(B, OC, OH, OW)
-    den = np.matmul(np.abs(w).reshape(OC, -1), np.abs(patches(x, K, S))).reshape(B, OC, OH, OW)
+    cols = patches(x, K, S)
+    wm = w.reshape(OC, -1)
+    if bias is not None:
+        cols = np.concatenate([cols, np.ones((B, 1, OH * OW))], axis=1)
+        wm = np.concatenate([wm, np.asarray(bias, np.float64).reshape(OC, 1)], axis=1)
+    pre = np.matmul(wm, cols).reshape(B, OC, OH, OW)
+    den = np.matmul(np.abs(wm), np.abs(cols)).reshape(B, OC, OH, OW)
     y = np.where(pre > 0, pre, 0.0) if relu else pre
     return y, den, pre
 
@@ -73,3 +81,15 @@ def wgrad(x, dy, y, K, S, relu):
     dw = np.matmul(gm, cols.transpose(0, 2, 1)).sum(axis=0)
     den = np.matmul(np.abs(gm), np.abs(cols).transpose(0, 2, 1)).sum(axis=0)
     return dw.reshape(OC, IC, K, K), den.reshape(OC, IC, K, K)
+
+
+def bgrad(dy, y, relu):
+    """db[oc] = 1_B^T (G 1_P): both contractions as matmuls with vectors of ones."""
+    g = grad_in(dy, y, relu)
+    B, OC = g.shape[:2]
+    gm = g.reshape(B, OC, -1)
+    onesp = np.ones(gm.shape[2])
+    onesb = np.ones(B)
+    db = np.matmul(onesb, np.matmul(gm, onesp))
+    den = np.matmul(onesb, np.matmul(np.abs(gm), onesp))
+    return db, den

@@ -6,13 +6,17 @@ planted-mistake tests can run the same pins against a mutated oracle.
 Pins, per the layer's definitions (PufferLib PR #522, layer-1/layer-2 bench
 blocks) and the mathematics of a linear map:
   brute      exact agreement with an independent im2col-matrix formulation on
-             small integer inputs (tests/brute.py), outputs and denominators;
+             small integer inputs (tests/brute.py), outputs and denominators,
+             with and without the bias, and the bias gradient;
   matmul     K=1, S=1 reduces to y[b,:,p] = w[:,:,0,0] @ x[b,:,p];
   delta      a one-hot input returns the (flipped-window) kernel entries;
   adjoint    <conv(x,w), g> = <x, dgrad(g,w)> = <w, wgrad(x,g)> (and the
              ReLU-masked form of it);
-  fd         central finite differences of L = <relu(conv(x,w)), dy>;
-  shapes     the output sizes printed on the page (tests/golden);
+  fd         central finite differences of L = <relu(conv(x,w) + bias), dy>
+             in x, w and the bias;
+  zero_w     with w = 0 the forward is act(bias) at every sample and position;
+  shapes     the output sizes printed on the page (tests/golden), and the
+             bias-gradient sizes its bias blocks print;
   unread     layer 1's input column w=14 is never read: dx is exactly 0
              there and changing x there changes nothing.
 """
@@ -66,6 +70,16 @@ def pin_brute(lib=None, cases=None):
         dwb, wdenb = brute.wgrad(x, dy, y, K, S, relu)
         assert np.array_equal(dw, dwb), ("wgrad", B, IC, OC, H, W, K, S, relu)
         assert np.array_equal(wden, wdenb), ("wgrad den", B, IC, OC, H, W, K, S, relu)
+        # The bias: forward with it, and its gradient (masked by the biased output).
+        bias = _ints(rng, (OC,), -4, 4)
+        yb_, den_ = oracle.conv_fwd(x, w, S, relu, nthreads=2, lib=lib, bias=bias)
+        ybb, denbb, _ = brute.fwd(x, w, S, relu, bias=bias)
+        assert np.array_equal(yb_, ybb), ("fwd bias", B, IC, OC, H, W, K, S, relu)
+        assert np.array_equal(den_, denbb), ("fwd bias den", B, IC, OC, H, W, K, S, relu)
+        db, bden = oracle.conv_bwd_bias(dy, yb_, relu, nthreads=2, lib=lib)
+        dbb, bdenb = brute.bgrad(dy, yb_, relu)
+        assert np.array_equal(db, dbb), ("bias grad", B, IC, OC, H, W, K, S, relu)
+        assert np.array_equal(bden, bdenb), ("bias grad den", B, IC, OC, H, W, K, S, relu)
 
 
 def pin_matmul(lib=None):
@@ -97,6 +111,26 @@ def pin_delta(lib=None):
             assert np.array_equal(y, want), "delta input does not return the kernel"
 
 
+def pin_zero_weight(lib=None):
+    """w = 0 leaves only the bias: y[b, oc, p] = act(bias[oc]) exactly, den = |bias[oc]|;
+    the bias gradient of an all-ones dy is then B*P where bias > 0 (relu) or everywhere."""
+    rng = np.random.default_rng(17)
+    for B, IC, OC, H, W, K, S in [(3, 2, 5, 11, 15, 5, 3), (2, 4, 3, 3, 4, 3, 1)]:
+        x = rng.standard_normal((B, IC, H, W))
+        w = np.zeros((OC, IC, K, K))
+        bias = rng.standard_normal(OC)
+        bias[0] = 0.0
+        OH, OW = (H - K) // S + 1, (W - K) // S + 1
+        for relu in (False, True):
+            y, den = oracle.conv_fwd(x, w, S, relu, lib=lib, bias=bias)
+            act = np.where(bias > 0, bias, 0.0) if relu else bias
+            assert np.array_equal(y, np.broadcast_to(act[None, :, None, None], y.shape)), "w=0: y != act(bias)"
+            assert np.array_equal(den, np.broadcast_to(np.abs(bias)[None, :, None, None], y.shape))
+            db, bden = oracle.conv_bwd_bias(np.ones_like(y), y, relu, lib=lib)
+            want = np.where((bias > 0) | (not relu), float(B * OH * OW), 0.0)
+            assert np.array_equal(db, want) and np.array_equal(bden, want), "bias grad of ones"
+
+
 def pin_adjoint(lib=None):
     rng = np.random.default_rng(9)
     for (B, IC, OC, H, W, K, S) in [(3, 4, 5, 11, 15, 5, 3), (4, 6, 5, 3, 4, 3, 1), (2, 3, 2, 9, 8, 3, 2)]:
@@ -113,6 +147,15 @@ def pin_adjoint(lib=None):
             scale = float(np.sum(np.abs(y * dy))) + 1e-300
             assert abs(lhs - a) <= 1e-12 * scale, ("adjoint <y,dy> vs <x,dx>", relu, lhs, a)
             assert abs(lhs - c) <= 1e-12 * scale, ("adjoint <y,dy> vs <w,dw>", relu, lhs, c)
+            # The bias enters as a broadcast over (b, oh, ow); its adjoint is the sum
+            # over them: <broadcast(v), g> = <v, bias_grad(g)> for any v.
+            v = rng.standard_normal(OC)
+            g = dy * (y > 0) if relu else dy
+            db, _ = oracle.conv_bwd_bias(dy, y, relu, lib=lib)
+            lhs = float(np.sum(v[None, :, None, None] * g))
+            rhs = float(np.sum(v * db))
+            scale = float(np.sum(np.abs(v[None, :, None, None] * g))) + 1e-300
+            assert abs(lhs - rhs) <= 1e-12 * scale, ("adjoint of the bias broadcast", relu, lhs, rhs)
 
 
 def pin_fd(lib=None):
@@ -153,6 +196,23 @@ def pin_fd(lib=None):
         assert abs(fd - dw[idx]) <= 1e-6 * (1 + abs(dw[idx])), ("fd dw", idx, fd, dw[idx])
         checked += 1
     assert checked == 48
+    # The bias: L(bias) = <relu(conv(x,w) + bias), dy> with its gradient from the oracle.
+    bias = rng.standard_normal(OC) * 0.05
+    pre_b, _ = oracle.conv_fwd(x, w, S, False, lib=lib, bias=bias)
+    assert np.min(np.abs(pre_b)) > 1e-3, "seed gives a biased pre-activation too close to the kink"
+    yb, _ = oracle.conv_fwd(x, w, S, True, lib=lib, bias=bias)
+    db, _ = oracle.conv_bwd_bias(dy, yb, True, lib=lib)
+
+    def loss_b(bb):
+        yy, _ = oracle.conv_fwd(x, w, S, True, lib=lib, bias=bb)
+        return float(np.sum(yy * dy))
+
+    for oc in range(OC):
+        bp, bm = bias.copy(), bias.copy()
+        bp[oc] += h
+        bm[oc] -= h
+        fd = (loss_b(bp) - loss_b(bm)) / (2 * h)
+        assert abs(fd - db[oc]) <= 1e-6 * (1 + abs(db[oc])), ("fd db", oc, fd, db[oc])
 
 
 def printed_shapes():
@@ -177,6 +237,28 @@ def pin_shapes(lib=None):
         assert y.shape == (2, OC, OH, OW)
 
 
+def pin_bias_grad_shapes(lib=None):
+    """The page's bias-gradient headers name each layer's OC and OH*OW and the element
+    count of the gradient; the layer shapes above must produce exactly those, and the
+    oracle's bias gradient must take that gradient to one value per output channel."""
+    layers = {i + 1: row for i, row in enumerate(printed_shapes())}
+    rows = []
+    with open(os.path.join(GOLDEN, "pr522_bias_grad_shapes.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                rows.append(tuple(int(t) for t in line.split()))
+    assert len(rows) == 2
+    rng = np.random.default_rng(19)
+    for layer, B, OC, spatial, elems in rows:
+        _, IC, OC_l, H, W, K, S, OH, OW, relu = layers[layer]
+        OHo, OWo = oracle.out_dim(H, K, S), oracle.out_dim(W, K, S)
+        assert OC == OC_l and OHo * OWo == spatial and B * OC * spatial == elems
+        dy = rng.standard_normal((2, OC, OHo, OWo))
+        db, _ = oracle.conv_bwd_bias(dy, None, False, lib=lib)
+        assert db.shape == (OC,)
+
+
 def pin_unread(lib=None):
     """Layer 1 (11x15, K=5, S=3): windows start at w = 0, 3, 6, 9 and end at 13,
     so column 14 feeds no output."""
@@ -196,4 +278,5 @@ def pin_unread(lib=None):
     assert np.all(den[..., :14] > 0)  # without the mask every other column is reached
 
 
-ALL_PINS = [pin_brute, pin_matmul, pin_delta, pin_adjoint, pin_fd, pin_shapes, pin_unread]
+ALL_PINS = [pin_brute, pin_matmul, pin_delta, pin_zero_weight, pin_adjoint, pin_fd, pin_shapes,
+            pin_bias_grad_shapes, pin_unread]

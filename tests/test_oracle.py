@@ -20,6 +20,10 @@ def test_delta_input_returns_kernel():
     pins.pin_delta()
 
 
+def test_zero_weight_leaves_bias():
+    pins.pin_zero_weight()
+
+
 def test_adjoint_identity():
     pins.pin_adjoint()
 
@@ -30,6 +34,10 @@ def test_finite_differences():
 
 def test_printed_output_sizes():
     pins.pin_shapes()
+
+
+def test_printed_bias_grad_sizes():
+    pins.pin_bias_grad_shapes()
 
 
 def test_layer1_column14_unread():

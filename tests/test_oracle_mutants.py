@@ -36,6 +36,17 @@ MUTANTS = [
     ("mask: gradient passes at y == 0", "if (s->relu && !(y[i] > 0.0)) return 0.0;",
      "if (s->relu && !(y[i] >= 0.0)) return 0.0;", 0),
     ("mask: ignored", "if (s->relu && !(y[i] > 0.0)) return 0.0;", "", 0),
+    ("fwd bias: one channel's bias for all", "const double bv = j->c[oc];",
+     "const double bv = j->c[0];", 0),
+    ("fwd bias: subtracted", "acc += bv;", "acc -= bv;", 0),
+    ("fwd bias: denominator term dropped", "den += fabs(bv);", "", 0),
+    ("fwd bias: added after the ReLU", "j->out[o] = (s->relu && !(acc > 0.0)) ? 0.0 : acc;",
+     "j->out[o] = (s->relu && !(acc - (j->c ? j->c[oc] : 0.0) > 0.0)) ? (j->c ? j->c[oc] : 0.0) : acc;",
+     0),
+    ("bias grad: mask ignored", "const double t = ref_g(s, dy, y, ((b * s->OC + oc) * OH + oh) * OW + ow);",
+     "const double t = dy[((b * s->OC + oc) * OH + oh) * OW + ow];", 0),
+    ("bias grad: last sample dropped", "for (int64_t b = 0; b < s->B; ++b)",
+     "for (int64_t b = 0; b + 1 < s->B; ++b)", 1),
 ]
 
 
