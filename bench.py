@@ -43,6 +43,10 @@ LAYERS = {
 # (forward us/iter, backward = wgrad + d_input us/iter) of its gemm_fast kernels.
 PR522_US = {("layer1", "f32"): (192.4102, 541.7361), ("layer2", "f32"): (56.8698, 100.2875),
             ("layer1", "bf16"): (106.4277, 403.5356), ("layer2", "bf16"): (18.4427, 49.1440)}
+# The same PR's "n3_conv_bias_grad" blocks: bias-gradient us/iter of its fast kernel at
+# B=32768, OC=128 (conv1: 12 positions, 50.3 M gradient elements; conv2: 2 positions).
+PR522_BIAS_GRAD_US = {"layer1": 136.5968, "layer2": 40.9008}
+BIAS_GRAD_BATCH = 32768
 FLUSH_BYTES = 512 << 20
 OPS = ("fwd", "dgrad", "wgrad")
 
@@ -430,6 +434,108 @@ def e2e(wl, flush_buf, steps):
             "d2h_bytes_per_step": (wl.y.numel() + wl.dx.numel() + wl.dw.numel()) * esz}
 
 
+_SIDE = []
+
+
+def graphed(fn):
+    """Capture fn (a sequence of library calls) into a CUDA graph on a side stream, after
+    a warm-up call there (the library's per-stream scratch exists before capture)."""
+    import torch
+    if not _SIDE:
+        _SIDE.append(torch.cuda.Stream())
+    s = _SIDE[0]
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(g, flush_buf=None, iters=50, warmup=5):
+    """Mean device ms of one replay: cold (L2 flushed before each, one event pair per
+    replay) when flush_buf is given, else warm (iters back-to-back replays)."""
+    import torch
+    from implicit_gemm_conv2d_gb300 import binding
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    if flush_buf is None:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(iters):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / iters
+    evs = []
+    for _ in range(iters):
+        binding.conv_l2_flush(flush_buf)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+
+def bias_extras(wls, flush_buf, peaks, device):
+    """The per-channel bias: forward with the bias against the plain forward, and the bias
+    gradient, for each layer / dtype workload at the bench batch; then the bias gradient at
+    the PR's bias-grad batch (B=32768, no mask, as its blocks time it), warm and cold L2."""
+    import torch
+    from implicit_gemm_conv2d_gb300 import binding, synth
+    hbm = peaks["hbm_gbs"]
+    out = {}
+    for key, wl in wls.items():
+        s = wl.shape
+        b_np = synth.conv_inputs(wl.B, s["IC"], s["OC"], s["H"], s["W"], s["K"], s["S"], dtype=wl.dtype,
+                                 need=("bias",))["bias"]
+        bias = torch.from_numpy(b_np).to(device).to(wl.tdt)
+        db = torch.empty_like(bias)
+        relu_y = wl.y if s["relu"] else None
+        g_fb = graphed(lambda: binding.conv_fwd_bias(wl.desc, wl.x, wl.w, bias, wl.y))
+        g_f = graphed(lambda: binding.conv_fwd(wl.desc, wl.x, wl.w, wl.y))
+        g_db = graphed(lambda: binding.conv_bwd_bias(wl.desc, wl.dy, relu_y, db))
+        esz = wl.x.element_size()
+        nbytes = (wl.dy.numel() * (2 if s["relu"] else 1) + db.numel()) * esz
+        t_db = time_graph(g_db, flush_buf)
+        plan = binding.conv_query(binding.OP_BWD_BIAS, wl.desc)
+        out[key] = {"fwd_us_cold_l2": time_graph(g_f, flush_buf) * 1e3,
+                    "fwd_bias_us_cold_l2": time_graph(g_fb, flush_buf) * 1e3,
+                    "bias_grad_us_cold_l2": t_db * 1e3, "bias_grad_us_warm": time_graph(g_db, None, 200, 50) * 1e3,
+                    "bias_grad_bytes": nbytes, "bias_grad_gbs": nbytes / (t_db * 1e-3) / 1e9,
+                    "bias_grad_frac_hbm": nbytes / (t_db * 1e-3) / 1e9 / hbm,
+                    "bias_grad_plan": {k: plan[k] for k in ("algo_name", "launches", "grid", "block", "splits")}}
+    big = {}
+    for layer in ("layer1", "layer2"):
+        s = LAYERS[layer]
+        for dt in ("f32", "bf16"):
+            tdt = torch.float32 if dt == "f32" else torch.bfloat16
+            dy_np = synth.conv_inputs(BIAS_GRAD_BATCH, s["IC"], s["OC"], s["H"], s["W"], s["K"], s["S"], dtype=dt,
+                                      need=("dy",))["dy"]
+            dy = torch.from_numpy(dy_np).to(device).to(tdt)
+            del dy_np
+            db = torch.empty((s["OC"],), dtype=tdt, device=device)
+            desc = binding.bias_desc(tuple(dy.shape), False, tdt)
+            g = graphed(lambda: binding.conv_bwd_bias(desc, dy, None, db))
+            nbytes = (dy.numel() + db.numel()) * dy.element_size()
+            warm = time_graph(g, None, 200, 50)
+            cold = time_graph(g, flush_buf, 50, 5)
+            big[f"{layer}_{dt}"] = {"grad_elems": dy.numel(), "us_warm": warm * 1e3, "us_cold_l2": cold * 1e3,
+                                    "gbs_cold_l2": nbytes / (cold * 1e-3) / 1e9,
+                                    "frac_hbm_cold_l2": nbytes / (cold * 1e-3) / 1e9 / hbm,
+                                    "pr522_fast_us": PR522_BIAS_GRAD_US[layer]}
+            del dy, g
+    out[f"bias_grad_b{BIAS_GRAD_BATCH}_norelu"] = big
+    return out
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -562,9 +668,11 @@ def run_ours(args):
     if not args.no_extras:
         line["e2e"] = e2e(wl, flush_buf, min(args.steps, 50))
         others = {}
+        wls = {}
         for layer in ("layer1", "layer2"):
             for dt in ("f32", "bf16"):
                 w2 = wl if (layer, dt) == (args.layer, args.dtype) else Workload(layer, dt, args.batch, device)
+                wls[f"{layer}_{dt}"] = w2
                 if not args.no_graphs and not getattr(w2, "graphs", None):
                     w2.capture()
                 p2, _ = time_step(w2, flush_buf, 50, 5)
@@ -581,6 +689,7 @@ def run_ours(args):
                     entry["pr522_us"] = {"fwd": f, "bwd": b}
                 others[f"{layer}_{dt}"] = entry
         line["configs_b%d" % args.batch] = others
+        line["bias"] = bias_extras(wls, flush_buf, peaks, device)
         if world == 1:
             line["cpu_baseline"] = cpu_baseline(LAYERS[args.layer], 128, 10.0)
     print(json.dumps(line))

@@ -22,7 +22,7 @@ from . import build as _build
 
 F32, BF16 = 0, 1
 ALGO_AUTO, ALGO_DIRECT, ALGO_FFMA, ALGO_TC = 0, 1, 2, 3
-OP_FWD, OP_BWD_DATA, OP_BWD_FILTER = 0, 1, 2
+OP_FWD, OP_BWD_DATA, OP_BWD_FILTER, OP_BWD_BIAS = 0, 1, 2, 3
 ALGO_NAMES = {0: "auto", 1: "direct", 2: "ffma", 3: "tc"}
 
 _DT = {torch.float32: F32, torch.bfloat16: BF16}
@@ -52,7 +52,7 @@ class PlanInfo(ctypes.Structure):
 EXPORTS = ["conv_fwd", "conv_bwd_data", "conv_bwd_filter_workspace_size", "conv_bwd_filter",
            "conv_status_string", "conv_out_dims", "conv_query", "conv_set_algo",
            "conv_fastdivmod_check", "conv_l2_flush", "conv_version", "conv_bwd_filter_noalloc",
-           "conv_device_status", "conv_release_scratch"]
+           "conv_device_status", "conv_release_scratch", "conv_fwd_bias", "conv_bwd_bias"]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -89,6 +89,8 @@ def lib():
         L.conv_bwd_filter_noalloc.argtypes = [dp, vp, vp, vp, vp, vp]
         L.conv_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
         L.conv_release_scratch.argtypes = []
+        L.conv_fwd_bias.argtypes = [dp, vp, vp, vp, vp, vp]
+        L.conv_bwd_bias.argtypes = [dp, vp, vp, vp, vp]
         _lib = L
         return L
 
@@ -129,6 +131,16 @@ def out_dims(desc: ConvDesc):
 
 def conv_fwd(desc: ConvDesc, x, w, y, stream=None) -> None:
     _check(lib().conv_fwd(ctypes.byref(desc), _ptr(x), _ptr(w), _ptr(y), _stream(stream)), "conv_fwd")
+
+
+def conv_fwd_bias(desc: ConvDesc, x, w, bias, y, stream=None) -> None:
+    _check(lib().conv_fwd_bias(ctypes.byref(desc), _ptr(x), _ptr(w), _ptr(bias), _ptr(y), _stream(stream)),
+           "conv_fwd_bias")
+
+
+def conv_bwd_bias(desc: ConvDesc, dy, y, db, stream=None) -> None:
+    _check(lib().conv_bwd_bias(ctypes.byref(desc), _ptr(dy), _ptr(y), _ptr(db), _stream(stream)),
+           "conv_bwd_bias")
 
 
 def conv_bwd_data(desc: ConvDesc, dy, w, y, dx, stream=None) -> None:
@@ -199,12 +211,29 @@ def _desc_from(x_shape, w_shape, S, relu, dtype):
     return make_desc(B, IC, OC, H, W, K, S, relu, dtype)
 
 
-def fwd(x, w, S: int, relu: bool, stream=None):
+def fwd(x, w, S: int, relu: bool, stream=None, bias=None):
     desc = _desc_from(x.shape, w.shape, S, relu, x.dtype)
     oh, ow = out_dims(desc)
     y = torch.empty((x.shape[0], w.shape[0], oh, ow), dtype=x.dtype, device=x.device)
-    conv_fwd(desc, x, w, y, stream)
+    if bias is None:
+        conv_fwd(desc, x, w, y, stream)
+    else:
+        conv_fwd_bias(desc, x, w, bias, y, stream)
     return y
+
+
+def bias_desc(dy_shape, relu: bool, dtype) -> ConvDesc:
+    """A descriptor for the bias gradient of an output of shape (B, OC, OH, OW): the
+    reduction needs only those sizes, so a 1x1, stride-1 window over an OH x OW input
+    stands for the layer."""
+    B, OC, OH, OW = dy_shape
+    return make_desc(B, 1, OC, OH, OW, 1, 1, relu, dtype)
+
+
+def bwd_bias(dy, y, relu: bool, stream=None):
+    db = torch.empty((dy.shape[1],), dtype=dy.dtype, device=dy.device)
+    conv_bwd_bias(bias_desc(dy.shape, relu, dy.dtype), dy, y if relu else None, db, stream)
+    return db
 
 
 def bwd_data(dy, w, y, H: int, W: int, S: int, relu: bool, stream=None):

@@ -141,7 +141,7 @@ int release_scratch()
 
 namespace {
 
-std::atomic<int> g_force[3] = {ALGO_AUTO, ALGO_AUTO, ALGO_AUTO};
+std::atomic<int> g_force[4] = {ALGO_AUTO, ALGO_AUTO, ALGO_AUTO, ALGO_AUTO};
 
 // ---- plan selection -------------------------------------------------------------------
 int choose_fwd(const ConvParams& p, int dt, const DevInfo& d, Plan& pl)
@@ -186,14 +186,40 @@ int choose_wgrad(const ConvParams& p, int dt, const DevInfo& d, Plan& pl)
     return CONV_OK;
 }
 
+int choose_bgrad(const ConvParams& p, int dt, const DevInfo& d, Plan& pl)
+{
+    pl = plan_bgrad(p, dt, d, g_force[CONV_OP_BWD_BIAS].load() == ALGO_DIRECT);
+    return CONV_OK;
+}
+
 int choose(int op, const ConvParams& p, int dt, const DevInfo& d, Plan& pl)
 {
     switch (op) {
     case CONV_OP_FWD: return choose_fwd(p, dt, d, pl);
     case CONV_OP_BWD_DATA: return choose_dgrad(p, dt, d, pl);
     case CONV_OP_BWD_FILTER: return choose_wgrad(p, dt, d, pl);
+    case CONV_OP_BWD_BIAS: return choose_bgrad(p, dt, d, pl);
     default: return CONV_ERR_UNSUPPORTED;
     }
+}
+
+int fwd_impl(const conv_desc_t* desc, const void* x, const void* w, const void* bias, void* y,
+             conv_stream_t stream)
+{
+    ConvParams p;
+    int rc = make_params(desc, p);
+    if (rc != CONV_OK) return rc;
+    if (p.B == 0) return CONV_OK;
+    if (!x || !w || !y) return CONV_ERR_NULL;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (bias && !aligned16(bias))) return CONV_ERR_ALIGN;
+    DevInfo d;
+    if ((rc = device_info(d)) != CONV_OK) return rc;
+    Plan pl;
+    if ((rc = choose_fwd(p, desc->dtype, d, pl)) != CONV_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (pl.algo == ALGO_DIRECT) return cuda_status(run_fwd_direct(pl, p, desc->dtype, x, w, bias, y, s));
+    if (pl.algo == ALGO_TC) return cuda_status(run_fwd_tc(pl, p, desc->dtype, x, w, bias, y, s));
+    return cuda_status(run_fwd_ffma(pl, p, desc->dtype, x, w, bias, y, s));
 }
 
 }  // namespace
@@ -229,7 +255,8 @@ int conv_out_dims(const conv_desc_t* desc, int32_t* OH, int32_t* OW)
 
 int conv_set_algo(int op, int algo)
 {
-    if (op < 0 || op > 2 || algo < ALGO_AUTO || algo > ALGO_TC) return CONV_ERR_UNSUPPORTED;
+    if (op < 0 || op > 3 || algo < ALGO_AUTO || algo > ALGO_TC) return CONV_ERR_UNSUPPORTED;
+    if (op == CONV_OP_BWD_BIAS && algo != ALGO_AUTO && algo != ALGO_DIRECT) return CONV_ERR_UNSUPPORTED;
     g_force[op].store(algo);
     return CONV_OK;
 }
@@ -240,7 +267,7 @@ int conv_query(int op, const conv_desc_t* desc, conv_plan_info_t* info)
     int rc = make_params(desc, p);
     if (rc != CONV_OK) return rc;
     if (!info) return CONV_ERR_NULL;
-    if (op < 0 || op > 2) return CONV_ERR_UNSUPPORTED;
+    if (op < 0 || op > 3) return CONV_ERR_UNSUPPORTED;
     DevInfo d;
     if ((rc = device_info(d)) != CONV_OK) return rc;
     Plan pl;
@@ -257,20 +284,32 @@ int conv_query(int op, const conv_desc_t* desc, conv_plan_info_t* info)
 
 int conv_fwd(const conv_desc_t* desc, const void* x, const void* w, void* y, conv_stream_t stream)
 {
+    return fwd_impl(desc, x, w, nullptr, y, stream);
+}
+
+int conv_fwd_bias(const conv_desc_t* desc, const void* x, const void* w, const void* bias, void* y,
+                  conv_stream_t stream)
+{
+    ConvParams p;
+    const int rc = make_params(desc, p);
+    if (rc != CONV_OK) return rc;
+    if (p.B > 0 && !bias) return CONV_ERR_NULL;
+    return fwd_impl(desc, x, w, bias, y, stream);
+}
+
+int conv_bwd_bias(const conv_desc_t* desc, const void* dy, const void* y, void* db, conv_stream_t stream)
+{
     ConvParams p;
     int rc = make_params(desc, p);
     if (rc != CONV_OK) return rc;
-    if (p.B == 0) return CONV_OK;
-    if (!x || !w || !y) return CONV_ERR_NULL;
-    if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return CONV_ERR_ALIGN;
+    if (!db) return CONV_ERR_NULL;
+    if (p.B > 0 && (!dy || (p.relu && !y))) return CONV_ERR_NULL;
+    if (!aligned16(db) || (p.B > 0 && (!aligned16(dy) || (p.relu && !aligned16(y))))) return CONV_ERR_ALIGN;
     DevInfo d;
     if ((rc = device_info(d)) != CONV_OK) return rc;
     Plan pl;
-    if ((rc = choose_fwd(p, desc->dtype, d, pl)) != CONV_OK) return rc;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (pl.algo == ALGO_DIRECT) return cuda_status(run_fwd_direct(pl, p, desc->dtype, x, w, y, s));
-    if (pl.algo == ALGO_TC) return cuda_status(run_fwd_tc(pl, p, desc->dtype, x, w, y, s));
-    return cuda_status(run_fwd_ffma(pl, p, desc->dtype, x, w, y, s));
+    if ((rc = choose_bgrad(p, desc->dtype, d, pl)) != CONV_OK) return rc;
+    return cuda_status(run_bgrad(pl, p, desc->dtype, dy, y, db, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int conv_bwd_data(const conv_desc_t* desc, const void* dy, const void* w, const void* y, void* dx,

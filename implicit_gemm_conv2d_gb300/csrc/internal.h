@@ -53,14 +53,16 @@ Plan plan_fwd_direct(const ConvParams& p, const DevInfo& d);
 Plan plan_dgrad_direct(const ConvParams& p, const DevInfo& d);
 Plan plan_wgrad_direct(const ConvParams& p, const DevInfo& d);
 
+// Forward launchers: `bias` (OC values of the dtype) is added to each finished sum before the
+// activation; nullptr = no bias.
 cudaError_t run_fwd_ffma(const Plan&, const ConvParams&, int dt, const void* x, const void* w,
-                         void* y, cudaStream_t s);
+                         const void* bias, void* y, cudaStream_t s);
 cudaError_t run_dgrad_ffma(const Plan&, const ConvParams&, int dt, const void* dy, const void* w,
                            const void* y, void* dx, cudaStream_t s);
 cudaError_t run_wgrad_ffma(const Plan&, const ConvParams&, int dt, const void* x, const void* dy,
                            const void* y, void* dw, void* ws, cudaStream_t s);
 cudaError_t run_fwd_direct(const Plan&, const ConvParams&, int dt, const void* x, const void* w,
-                           void* y, cudaStream_t s);
+                           const void* bias, void* y, cudaStream_t s);
 cudaError_t run_dgrad_direct(const Plan&, const ConvParams&, int dt, const void* dy,
                              const void* w, const void* y, void* dx, cudaStream_t s);
 cudaError_t run_wgrad_direct(const Plan&, const ConvParams&, int dt, const void* x,
@@ -112,8 +114,8 @@ cudaError_t launch_overlapped(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 // ---- tcgen05 tensor-core family (kernels_tc.cu) -------------------------------------
 bool tc_fwd_ok(const ConvParams& p, int dt, const DevInfo& d);
 Plan plan_fwd_tc(const ConvParams& p, int dt, const DevInfo& d);
-cudaError_t run_fwd_tc(const Plan&, const ConvParams&, int dt, const void* x, const void* w, void* y,
-                       cudaStream_t s);
+cudaError_t run_fwd_tc(const Plan&, const ConvParams&, int dt, const void* x, const void* w,
+                       const void* bias, void* y, cudaStream_t s);
 bool tc_wgrad_ok(const ConvParams& p, int dt, const DevInfo& d);
 Plan plan_wgrad_tc(const ConvParams& p, int dt, const DevInfo& d);
 cudaError_t run_wgrad_tc(const Plan&, const ConvParams&, int dt, const void* x, const void* dy,
@@ -122,6 +124,13 @@ bool tc_dgrad_ok(const ConvParams& p, int dt, const DevInfo& d);
 Plan plan_dgrad_tc(const ConvParams& p, int dt, const DevInfo& d);
 cudaError_t run_dgrad_tc(const Plan&, const ConvParams&, int dt, const void* dy, const void* w,
                          const void* y, void* dx, int sms, cudaStream_t s);
+// ---- bias gradient (kernels_bias.cu) ------------------------------------------------
+// `direct`: the one-warp-per-channel kernel (any shape); else the column-sum kernel and its
+// reduce, when the shape allows.
+Plan plan_bgrad(const ConvParams& p, int dt, const DevInfo& d, bool direct);
+cudaError_t run_bgrad(const Plan&, const ConvParams&, int dt, const void* dy, const void* y, void* db,
+                      cudaStream_t s);
+
 // Error bits the tensor-core kernels set when a bounded wait runs out.
 cudaError_t tc_read_status(unsigned* out, bool reset);
 

@@ -38,7 +38,7 @@ inline int fw_smem(const ConvParams& p)
 template <typename T, bool RELU>
 __global__ void __launch_bounds__(FW_THREADS, 1)
 fwd_ffma_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict__ w,
-                T* __restrict__ y)
+                const T* __restrict__ bias, T* __restrict__ y)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int kred_pad = fw_kred_pad(p.Kred);
@@ -133,6 +133,7 @@ fwd_ffma_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
                     const int oc = oc0 + lane + 32 * j;
                     if (oc < p.OC) {
                         float v = acc[j][c];
+                        if (bias) v += Elem<T>::ldg(bias + oc);
                         if (RELU) v = v > 0.f ? v : 0.f;
                         Elem<T>::st(y + ob + size_t(oc) * p.P, v);
                     }
@@ -487,7 +488,7 @@ __global__ void wgrad_reduce_kernel(const float* __restrict__ ws, int splits, in
 // ======================================================================================
 template <typename T, bool RELU>
 __global__ void fwd_direct_kernel(const ConvParams p, const T* __restrict__ x,
-                                  const T* __restrict__ w, T* __restrict__ y)
+                                  const T* __restrict__ w, const T* __restrict__ bias, T* __restrict__ y)
 {
     const int total = p.B * p.OCP;
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
@@ -502,6 +503,7 @@ __global__ void fwd_direct_kernel(const ConvParams p, const T* __restrict__ x,
                 for (int kw = 0; kw < p.K; ++kw)
                     acc = fmaf(Elem<T>::ldg(wo + (ic * p.K + kh) * p.K + kw),
                                Elem<T>::ldg(xb + ic * p.HW + kh * p.W + kw), acc);
+        if (bias) acc += Elem<T>::ldg(bias + oc);
         if (RELU) acc = acc > 0.f ? acc : 0.f;
         Elem<T>::st(y + i, acc);
     }
@@ -672,7 +674,7 @@ Plan plan_wgrad_direct(const ConvParams& p, const DevInfo& d)
 
 template <typename T>
 static cudaError_t fwd_ffma_t(const Plan& pl, const ConvParams& p, const void* x, const void* w,
-                              void* y, cudaStream_t s)
+                              const void* bias, void* y, cudaStream_t s)
 {
     const int oct = ceil_div(p.OC, FW_OCT);
     dim3 grid(pl.grid / oct, oct);
@@ -680,17 +682,18 @@ static cudaError_t fwd_ffma_t(const Plan& pl, const ConvParams& p, const void* x
     IG_DISPATCH_RELU(p.relu, {
         e = ensure_smem<fwd_ffma_kernel<T, R>>(pl.smem);
         if (e == cudaSuccess)
-            fwd_ffma_kernel<T, R><<<grid, pl.block, pl.smem, s>>>(p, (const T*)x, (const T*)w, (T*)y);
+            fwd_ffma_kernel<T, R><<<grid, pl.block, pl.smem, s>>>(p, (const T*)x, (const T*)w, (const T*)bias,
+                                                                  (T*)y);
     });
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t run_fwd_ffma(const Plan& pl, const ConvParams& p, int dt, const void* x, const void* w,
-                         void* y, cudaStream_t s)
+                         const void* bias, void* y, cudaStream_t s)
 {
     if (pl.launches == 0) return cudaSuccess;
-    return dt == DT_F32 ? fwd_ffma_t<float>(pl, p, x, w, y, s)
-                        : fwd_ffma_t<__nv_bfloat16>(pl, p, x, w, y, s);
+    return dt == DT_F32 ? fwd_ffma_t<float>(pl, p, x, w, bias, y, s)
+                        : fwd_ffma_t<__nv_bfloat16>(pl, p, x, w, bias, y, s);
 }
 
 template <typename T>
@@ -769,8 +772,9 @@ static cudaError_t direct_t(int op, const Plan& pl, const ConvParams& p, const v
                             const void* b, const void* c, void* out, cudaStream_t s)
 {
     IG_DISPATCH_RELU(p.relu, {
-        if (op == 0)
-            fwd_direct_kernel<T, R><<<pl.grid, pl.block, 0, s>>>(p, (const T*)a, (const T*)b, (T*)out);
+        if (op == 0)  // c: the bias or nullptr
+            fwd_direct_kernel<T, R><<<pl.grid, pl.block, 0, s>>>(p, (const T*)a, (const T*)b, (const T*)c,
+                                                                 (T*)out);
         else if (op == 1)
             dgrad_direct_kernel<T, R><<<pl.grid, pl.block, 0, s>>>(p, (const T*)a, (const T*)b,
                                                                    (const T*)c, (T*)out);
@@ -782,11 +786,11 @@ static cudaError_t direct_t(int op, const Plan& pl, const ConvParams& p, const v
 }
 
 cudaError_t run_fwd_direct(const Plan& pl, const ConvParams& p, int dt, const void* x,
-                           const void* w, void* y, cudaStream_t s)
+                           const void* w, const void* bias, void* y, cudaStream_t s)
 {
     if (pl.launches == 0) return cudaSuccess;
-    return dt == DT_F32 ? direct_t<float>(0, pl, p, x, w, nullptr, y, s)
-                        : direct_t<__nv_bfloat16>(0, pl, p, x, w, nullptr, y, s);
+    return dt == DT_F32 ? direct_t<float>(0, pl, p, x, w, bias, y, s)
+                        : direct_t<__nv_bfloat16>(0, pl, p, x, w, bias, y, s);
 }
 cudaError_t run_dgrad_direct(const Plan& pl, const ConvParams& p, int dt, const void* dy,
                              const void* w, const void* y, void* dx, cudaStream_t s)

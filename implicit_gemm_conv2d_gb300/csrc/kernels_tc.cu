@@ -372,7 +372,7 @@ struct RingPos {
 template <typename T, bool RELU, int SWZ>
 __global__ void __launch_bounds__(FA_THREADS, 1)
 fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* __restrict__ wpack,
-              T* __restrict__ y, float* __restrict__ part, const FwdGeom geo)
+              const T* __restrict__ bias, T* __restrict__ y, float* __restrict__ part, const FwdGeom geo)
 {
     using Tr = TcTraits<T>;
     constexpr int ES = int(sizeof(T));
@@ -648,7 +648,8 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
                 }
             }
             if (!ok) break;
-            // Epilogue: TMEM -> y (or, with K ranges, -> this range's fp32 partials); this
+            // Epilogue: TMEM -> y, plus the bias if given, then ReLU (or, with K ranges, -> this
+            // range's fp32 partials, the bias and ReLU left to the reduce kernel); this
             // warp's lanes, every FA_KSPLIT-th group of 8 channels.
             if (!mbar_wait_or_abort(smem_u32(&bars->acc_full), t & 1, abort_flag)) {
                 report(const_cast<int*>(abort_flag), 2u);
@@ -679,6 +680,7 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
                         const int oc = ot * geo.OTp + cb + e;
                         if (oc < p.OC) {
                             float f = __uint_as_float(r[e]);
+                            if (bias) f += Elem<T>::ldg(bias + oc);
                             if (RELU) f = f > 0.f ? f : 0.f;
                             Elem<T>::st(yc + size_t(oc) * p.P, f);
                         }
@@ -702,10 +704,11 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
     }
 }
 
-// Sum of the forward's K-range partials in ascending range order, then ReLU, into y.
+// Sum of the forward's K-range partials in ascending range order, then the bias (if any) and
+// ReLU, into y.
 template <typename T, bool RELU>
 __global__ void fwd_reduce_kernel(const ConvParams p, const float* __restrict__ part, int splits, int ocp,
-                                  T* __restrict__ y)
+                                  const T* __restrict__ bias, T* __restrict__ y)
 {
     grid_dep_wait();  // the partials come from the kernel launched just before
     const size_t total = size_t(p.N) * p.OC;
@@ -715,6 +718,7 @@ __global__ void fwd_reduce_kernel(const ConvParams p, const float* __restrict__ 
         const float* src = part + size_t(n) * ocp + oc;
         float s = 0.f;
         for (int sp = 0; sp < splits; ++sp) s += __ldcg(src + size_t(sp) * sstride);
+        if (bias) s += Elem<T>::ldg(bias + oc);
         if (RELU) s = s > 0.f ? s : 0.f;
         Elem<T>::st(y + col_out(p, n) + size_t(oc) * p.P, s);
     }
@@ -1841,8 +1845,8 @@ Plan plan_fwd_tc(const ConvParams& p, int dt, const DevInfo& d)
 }
 
 template <typename T>
-static cudaError_t fwd_tc_t(const Plan& pl, const ConvParams& p, const void* x, const void* w, void* y,
-                            cudaStream_t s)
+static cudaError_t fwd_tc_t(const Plan& pl, const ConvParams& p, const void* x, const void* w,
+                            const void* bias, void* y, cudaStream_t s)
 {
     const int v = pl.variant;
     FwdGeom g = fwd_geom<T>(p, (v / 16) % 16, v % 16);
@@ -1864,12 +1868,13 @@ static cudaError_t fwd_tc_t(const Plan& pl, const ConvParams& p, const void* x, 
         e = ensure_smem<fwd_tc_kernel<T, R, 1>>(pl.smem);                                           \
         if (e == cudaSuccess)                                                                       \
             e = launch_overlapped(fwd_tc_kernel<T, R, 1>, dim3(pl.grid), dim3(pl.block), pl.smem, s, p,   \
-                                  (const T*)x, (const unsigned char*)wpack, (T*)y, part, g);                 \
+                                  (const T*)x, (const unsigned char*)wpack, (const T*)bias, (T*)y, part, g); \
         if (e == cudaSuccess && g.splits > 1) {                                                     \
             const size_t total = size_t(p.N) * p.OC;                                                \
             const int rgrid = int(std::min<size_t>((total + 255) / 256, 4096));                     \
             e = launch_overlapped(fwd_reduce_kernel<T, R>, dim3(rgrid), dim3(256), 0, s, p,           \
-                                  (const float*)part, g.splits, g.oc_tiles * g.OTp, (T*)y);            \
+                                  (const float*)part, g.splits, g.oc_tiles * g.OTp, (const T*)bias,   \
+                                  (T*)y);                                                             \
         }                                                                                           \
     } while (0)
     if (p.relu) IG_LAUNCH_FWD_TC(true);
@@ -1878,10 +1883,11 @@ static cudaError_t fwd_tc_t(const Plan& pl, const ConvParams& p, const void* x, 
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-cudaError_t run_fwd_tc(const Plan& pl, const ConvParams& p, int dt, const void* x, const void* w, void* y,
-                       cudaStream_t s)
+cudaError_t run_fwd_tc(const Plan& pl, const ConvParams& p, int dt, const void* x, const void* w,
+                       const void* bias, void* y, cudaStream_t s)
 {
-    return dt == DT_F32 ? fwd_tc_t<float>(pl, p, x, w, y, s) : fwd_tc_t<__nv_bfloat16>(pl, p, x, w, y, s);
+    return dt == DT_F32 ? fwd_tc_t<float>(pl, p, x, w, bias, y, s)
+                        : fwd_tc_t<__nv_bfloat16>(pl, p, x, w, bias, y, s);
 }
 
 // ---- wgrad ------------------------------------------------------------------------------

@@ -13,6 +13,7 @@ synthetic value recipe used throughout this project):
   x  ~ N(0, 1)                            stream 1
   w  ~ U(-a, a),  a = 1 / sqrt(IC*K*K)    stream 2
   dy ~ N(0, 1)                            stream 3
+  bias ~ U(-a, a), the same a              stream 7 (only when asked for)
 Values are rounded to fp32 (round-to-nearest-even); bf16 inputs round those
 fp32 values once more to bf16 with round-to-nearest-even.  The arrays returned
 are float32 holding exactly the values the layer receives in either dtype.
@@ -29,7 +30,7 @@ _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 _CHUNK = 1 << 22
 
-STREAM_X, STREAM_W, STREAM_DY, STREAM_SUB_X, STREAM_SUB_W, STREAM_W2 = 1, 2, 3, 4, 5, 6
+STREAM_X, STREAM_W, STREAM_DY, STREAM_SUB_X, STREAM_SUB_W, STREAM_W2, STREAM_BIAS = 1, 2, 3, 4, 5, 6, 7
 
 
 def _mix(z: np.ndarray) -> np.ndarray:
@@ -153,4 +154,7 @@ def conv_inputs(B: int, IC: int, OC: int, H: int, W: int, K: int, S: int, dtype:
     if "dy" in need:
         dy = normal(seed, STREAM_DY, B * OC * OH * OW)
         out["dy"] = to_dtype_values(dy, dtype).reshape(B, OC, OH, OW)
+    if "bias" in need:
+        a = 1.0 / math.sqrt(IC * K * K)
+        out["bias"] = to_dtype_values(uniform_pm(seed, STREAM_BIAS, OC, a) * scale, dtype)
     return out

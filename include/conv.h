@@ -16,8 +16,15 @@
  *                                      of g[b,oc,oh,ow] * w[oc,ic,kh,kw]
  *   conv_bwd_filter  dw[oc,ic,kh,kw] = sum_{b,oh,ow} g[b,oc,oh,ow] * x[b,ic,oh*S+kh,ow*S+kw]
  *
+ * and the layer's per-output-channel bias (the same PR's "n3_conv_bias_grad"
+ * bench blocks time its gradient for both conv layers, conv1 with 12 output
+ * positions and conv2 with 2, OC = 128, B = 32768):
+ *
+ *   conv_fwd_bias    y[b,oc,oh,ow]   = act(bias[oc] + sum_{ic,kh,kw} ... as conv_fwd)
+ *   conv_bwd_bias    db[oc]          = sum_{b,oh,ow} g[b,oc,oh,ow]
+ *
  * Layouts (dense, row-major, no strides): x, dx (B,IC,H,W); y, dy
- * (B,OC,OH,OW); w, dw (OC,IC,K,K).  Every tensor of a call has the
+ * (B,OC,OH,OW); w, dw (OC,IC,K,K); bias, db (OC).  Every tensor of a call has the
  * descriptor's dtype: CONV_F32 (binary32 in and out, fp32 arithmetic) or
  * CONV_BF16 (bfloat16 in and out, fp32 accumulation, one round-to-nearest-even
  * rounding of each result).
@@ -28,7 +35,8 @@
  *     after the call returns.  Base pointers must be 16-byte aligned.  Outputs
  *     must not overlap inputs.
  *   - Scratch: the tensor-core paths of conv_fwd and conv_bwd_data first
- *     repack w into the tensor cores' tile layout.  They keep one 8 MiB
+ *     repack w into the tensor cores' tile layout, and conv_bwd_bias keeps its
+ *     per-block partial sums.  They keep one 8 MiB
  *     device buffer for that per (device, stream), allocated with cudaMalloc
  *     on the first such call on that stream and held until
  *     conv_release_scratch() or process exit; make that first call outside
@@ -83,18 +91,29 @@ typedef enum {
 /* Algorithm families (conv_set_algo / conv_query). */
 typedef enum {
     CONV_ALGO_AUTO = 0,   /* library choice (default)                                 */
-    CONV_ALGO_DIRECT = 1, /* one thread per output element; any shape                 */
-    CONV_ALGO_FFMA = 2,   /* fp32 FFMA register-tiled implicit GEMM                   */
-    CONV_ALGO_TC = 3      /* tcgen05 tensor cores, TMEM accumulator (bf16)            */
+    CONV_ALGO_DIRECT = 1, /* one thread (bias grad: one warp) per output element; any
+                             shape                                                    */
+    CONV_ALGO_FFMA = 2,   /* fp32 CUDA-core tiled kernels: FFMA register-tiled
+                             implicit GEMM; for the bias grad, the column-sum kernel  */
+    CONV_ALGO_TC = 3      /* tcgen05 tensor cores, TMEM accumulator (bf16 operands,
+                             or fp32 as three tf32 products)                          */
 } conv_algo_t;
 
-typedef enum { CONV_OP_FWD = 0, CONV_OP_BWD_DATA = 1, CONV_OP_BWD_FILTER = 2 } conv_op_t;
+typedef enum { CONV_OP_FWD = 0, CONV_OP_BWD_DATA = 1, CONV_OP_BWD_FILTER = 2, CONV_OP_BWD_BIAS = 3 } conv_op_t;
 
 /* Forward:  y = act(conv(x, w)).
  *   x: (B,IC,H,W)   w: (OC,IC,K,K)   y: (B,OC,OH,OW), written.
  * Returns CONV_OK or an error code (see above). */
 int conv_fwd(const conv_desc_t* desc, const void* x, const void* w, void* y,
              conv_stream_t stream);
+
+/* Forward with the per-channel bias:  y = act(conv(x, w) + bias), the bias
+ * added in fp32 to the finished sum, before the activation and the one
+ * rounding to the output dtype.  Same kernels, plans and conventions as
+ * conv_fwd (conv_query / conv_set_algo with CONV_OP_FWD cover both).
+ *   bias: (OC) in the descriptor's dtype, required (use conv_fwd for none). */
+int conv_fwd_bias(const conv_desc_t* desc, const void* x, const void* w, const void* bias, void* y,
+                  conv_stream_t stream);
 
 /* Data gradient (d_input):  dx = conv^T(g, w), g = dy masked by y > 0 when relu.
  *   dy: (B,OC,OH,OW)  w: (OC,IC,K,K)  y: (B,OC,OH,OW) forward output, required
@@ -119,6 +138,24 @@ size_t conv_bwd_filter_workspace_size(const conv_desc_t* desc);
  *   ignored and on return are unspecified.  May be NULL when the size is 0. */
 int conv_bwd_filter(const conv_desc_t* desc, const void* x, const void* dy, const void* y,
                     void* dw, void* workspace, size_t workspace_bytes, conv_stream_t stream);
+
+/* Bias gradient:  db[oc] = sum over b, oh, ow of g (g = dy masked by y > 0 when
+ * relu), accumulated in fp32 and rounded once to the dtype.  Two kernels: the
+ * first gives each CTA a contiguous range of samples and sums, per output
+ * position (oc, oh, ow), down its rows in ascending b, then over the positions
+ * of each channel in ascending (oh, ow); the second adds the CTAs' per-channel
+ * sums in a fixed order (strided by 32 in ascending order, then a fixed
+ * butterfly).  The partial sums live in the per-stream scratch buffer (see
+ * Scratch above; this call allocates it if it is the first on its stream).
+ * A shape whose OC*OH*OW row is too long for the first kernel's shared-memory
+ * window (more than 12288 positions per output channel) runs a one-warp-per-
+ * channel kernel instead (the same result up to summation order).
+ *   dy: (B,OC,OH,OW)  y: forward output, required when desc->relu, ignored
+ *   otherwise (may be NULL)  db: (OC), written (zeros when B = 0).
+ * conv_query(CONV_OP_BWD_BIAS, ...) reports the plan; conv_set_algo accepts
+ * CONV_ALGO_AUTO and CONV_ALGO_DIRECT (the one-warp-per-channel kernel) for it. */
+int conv_bwd_bias(const conv_desc_t* desc, const void* dy, const void* y, void* db,
+                  conv_stream_t stream);
 
 /* Weight gradient that allocates nothing (the paper has no counterpart; this
  * entry point exists for callers of this library that cannot allocate device
@@ -167,9 +204,9 @@ int conv_query(int op, const conv_desc_t* desc, conv_plan_info_t* info);
 
 /* Force an algorithm family for one operation (CONV_ALGO_AUTO restores the
  * library's choice).  Process-wide, not thread-safe; meant for tests and
- * benchmarks.  Returns CONV_ERR_UNSUPPORTED for an unknown op or algo.  A
- * forced family that cannot run a given descriptor makes that call return
- * CONV_ERR_UNSUPPORTED. */
+ * benchmarks.  Returns CONV_ERR_UNSUPPORTED for an unknown op or algo, and for
+ * CONV_ALGO_FFMA / CONV_ALGO_TC with CONV_OP_BWD_BIAS.  A forced family that
+ * cannot run a given descriptor makes that call return CONV_ERR_UNSUPPORTED. */
 int conv_set_algo(int op, int algo);
 
 /* Diagnostics.  conv_fastdivmod_check runs, on the host, the library's

@@ -64,6 +64,8 @@ def test_invalid_descriptor(L, bad):
     assert L.conv_bwd_data(ctypes.byref(d), fake, fake, fake, fake, None) == -2
     assert L.conv_bwd_filter(ctypes.byref(d), fake, fake, fake, fake, fake, 1 << 30, None) == -2
     assert L.conv_bwd_filter_workspace_size(ctypes.byref(d)) == 0
+    assert L.conv_fwd_bias(ctypes.byref(d), fake, fake, fake, fake, None) == -2
+    assert L.conv_bwd_bias(ctypes.byref(d), fake, fake, fake, None) == -2
     oh, ow = ctypes.c_int32(), ctypes.c_int32()
     assert L.conv_out_dims(ctypes.byref(d), ctypes.byref(oh), ctypes.byref(ow)) == -2
 
@@ -88,18 +90,37 @@ def test_null_and_alignment_checked_before_cuda(L):
     assert L.conv_bwd_filter(ctypes.byref(d), ok, ok, ok, ok, odd, 1 << 30, None) == -4
     d0 = desc(relu=0)
     assert L.conv_bwd_data(ctypes.byref(d0), ok, ok, None, None, None) == -1
+    # The bias entry points.
+    assert L.conv_fwd_bias(ctypes.byref(d), ok, ok, None, ok, None) == -1   # bias required
+    assert L.conv_fwd_bias(ctypes.byref(d), ok, ok, odd, ok, None) == -4
+    assert L.conv_fwd_bias(ctypes.byref(d), None, ok, ok, ok, None) == -1
+    assert L.conv_bwd_bias(None, ok, ok, ok, None) == -1
+    assert L.conv_bwd_bias(ctypes.byref(d), ok, ok, None, None) == -1      # db required
+    assert L.conv_bwd_bias(ctypes.byref(d), ok, None, ok, None) == -1      # relu needs y
+    assert L.conv_bwd_bias(ctypes.byref(d), None, ok, ok, None) == -1
+    assert L.conv_bwd_bias(ctypes.byref(d), ok, ok, odd, None) == -4
+    assert L.conv_bwd_bias(ctypes.byref(d), odd, ok, ok, None) == -4
+    assert L.conv_bwd_bias(ctypes.byref(d), ok, odd, ok, None) == -4
 
 
 def test_empty_batch_is_a_no_op(L):
     d = desc(B=0)
     assert L.conv_fwd(ctypes.byref(d), None, None, None, None) == 0
     assert L.conv_bwd_data(ctypes.byref(d), None, None, None, None, None) == 0
+    assert L.conv_fwd_bias(ctypes.byref(d), None, None, None, None, None) == 0
+    assert L.conv_bwd_bias(ctypes.byref(d), None, None, None, None) == -1  # db is still written
 
 
 def test_set_algo_validation(L):
-    assert L.conv_set_algo(3, 0) == -3
+    assert L.conv_set_algo(4, 0) == -3
+    assert L.conv_set_algo(-1, 0) == -3
     assert L.conv_set_algo(0, 9) == -3
     assert L.conv_set_algo(0, 0) == 0
+    # The bias gradient has the column-sum kernel (auto) and the direct kernel only.
+    assert L.conv_set_algo(3, 2) == -3
+    assert L.conv_set_algo(3, 3) == -3
+    assert L.conv_set_algo(3, 1) == 0
+    assert L.conv_set_algo(3, 0) == 0
 
 
 # Divisors the two layers use: P, OW, K*K, K, W, H*W and IC*K*K for

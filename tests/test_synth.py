@@ -39,6 +39,19 @@ def test_determinism_and_streams_differ():
     assert not np.array_equal(a["x"].reshape(-1)[:60], a["dy"].reshape(-1)[:60])
 
 
+def test_bias_is_optional_and_its_own_stream():
+    base = synth.conv_inputs(4, 3, 5, 11, 15, 5, 3)
+    withb = synth.conv_inputs(4, 3, 5, 11, 15, 5, 3, need=("x", "w", "dy", "bias"))
+    assert "bias" not in base and withb["bias"].shape == (5,)
+    for k in base:  # asking for the bias changes none of the other tensors
+        assert base[k].tobytes() == withb[k].tobytes()
+    a = 1 / math.sqrt(3 * 25)
+    assert np.all(np.abs(withb["bias"]) < a)
+    assert not np.array_equal(withb["bias"], withb["w"].reshape(-1)[:5])
+    bf = synth.conv_inputs(4, 3, 5, 11, 15, 5, 3, dtype="bf16", need=("bias",))["bias"]
+    assert np.array_equal(bf, synth.to_dtype_values(withb["bias"].astype(np.float64), "bf16"))
+
+
 def test_distributions():
     n = 1 << 20
     x = synth.normal(synth.SEED, 1, n)
