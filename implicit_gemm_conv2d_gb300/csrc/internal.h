@@ -36,9 +36,9 @@ int make_params(const conv_desc_t* d, ConvParams& p);  // validation, no CUDA ca
 bool aligned16(const void* p);
 int cuda_status(cudaError_t e);                     // cudaSuccess -> CONV_OK, else CONV_ERR_CUDA
 
-// Library-held scratch for packed weights: one buffer per (device, stream), allocated
-// on first use; nullptr if it cannot be allocated.
-constexpr size_t kScratchBytes = size_t(8) << 20;
+// Library-held scratch for packed weights and the forward's / bias gradient's partial sums:
+// one buffer per (device, stream), allocated on first use; nullptr if it cannot be allocated.
+constexpr size_t kScratchBytes = size_t(48) << 20;
 void* stream_scratch(int device, cudaStream_t stream);
 int release_scratch();
 

@@ -82,18 +82,19 @@ bias_colsum_kernel(const ConvParams p, const T* __restrict__ dy, const T* __rest
         for (int e = 0; e < V; ++e) acc[e] = 0.f;
         const size_t col = size_t(c0) + size_t(cg) * V;
         int b = b_lo + r;
-        // Four rows' loads in flight, added in ascending b.
+        // U rows' loads in flight (eight 16-byte loads), added in ascending b.
+        constexpr int U = RELU ? 4 : 8;
 #pragma unroll 1
-        for (; b + 3 * R < b_hi; b += 4 * R) {
-            float v[4][V], m[4][V];
+        for (; b + (U - 1) * R < b_hi; b += U * R) {
+            float v[U][V], m[U][V];
             const size_t off0 = size_t(b) * p.OCP + col;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < U; ++u) {
                 VecLd<T, V>::ld(dy + off0 + u * rstep, v[u]);
                 if (RELU) VecLd<T, V>::ld(y + off0 + u * rstep, m[u]);
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int u = 0; u < U; ++u)
 #pragma unroll
                 for (int e = 0; e < V; ++e) acc[e] += (!RELU || m[u][e] > 0.f) ? v[u][e] : 0.f;
         }
@@ -130,8 +131,18 @@ bias_reduce_kernel(const float* __restrict__ part, int nsplit, int OC, T* __rest
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int oc = blockIdx.x * 32 + lane;
     float s = 0.f;
-    if (oc < OC)
-        for (int i = warp; i < nsplit; i += BG_RED_WARPS) s += __ldcg(part + size_t(i) * OC + oc);
+    if (oc < OC) {
+        // Loads in groups of eight issued together, added in ascending range order.
+        int i = warp;
+        for (; i + 7 * BG_RED_WARPS < nsplit; i += 8 * BG_RED_WARPS) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = __ldcg(part + size_t(i + u * BG_RED_WARPS) * OC + oc);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) s += v[u];
+        }
+        for (; i < nsplit; i += BG_RED_WARPS) s += __ldcg(part + size_t(i) * OC + oc);
+    }
     red[warp][lane] = s;
     __syncthreads();
     if (warp == 0 && oc < OC) {

@@ -291,17 +291,40 @@ inline FwdGeom fwd_geom(const ConvParams& p, int xg, int nw)
 // K ranges for a forward with fewer column tiles than half the SMs: enough ranges to
 // cover the SMs, each a whole number of x super-chunks, their fp32 partials fitting in
 // the scratch buffer beside the packed weights.
-inline void fwd_set_splits(FwdGeom& g, const ConvParams& p, int sms, size_t packed, size_t scratch)
+// Estimated forward time in chunk steps of one CTA (about a microsecond each): rounds of
+// work items over the SMs x chunks per item, plus, with K ranges, the reduce kernel (a launch
+// and one pass over the fp32 partials).
+inline double fwd_cost(int tiles, int sms, int splits, int kc, size_t part)
+{
+    return double(ceil_div(tiles * splits, sms)) * kc +
+           (splits > 1 ? 1.5 + double(splits) * double(part) / 8e6 : 0.0);
+}
+
+// K ranges, only when the column tiles fill fewer than half the SMs (with more, a range's
+// fixed cost -- its own x slabs, pipeline fill and partial sums -- outweighs the gain; layer 1
+// at B = 1024, 96 tiles, ran 8 % slower in fp32 and 40 % slower in bf16 with three ranges):
+// the split of the nchunks K-chunks (kc_per of them, a multiple of xg, per range) with the
+// lowest estimated time, within the scratch buffer's room for partials.  Returns that estimate.
+inline double fwd_set_splits(FwdGeom& g, const ConvParams& p, int sms, size_t packed, size_t scratch)
 {
     const int tiles = g.n_tiles * g.oc_tiles;
-    if (2 * tiles >= sms || g.nchunks < 2 * g.xg) return;
+    double best = fwd_cost(tiles, sms, 1, g.nchunks, 0);
+    if (2 * tiles >= sms || g.nchunks < 2 * g.xg) return best;
     const size_t part = size_t(p.N) * g.oc_tiles * g.OTp * 4;  // one range's partials
-    const size_t room = scratch > packed + 256 ? scratch - round_up(packed, 256) : 0;
-    int want = std::min(sms / tiles, int(room / part));
-    want = std::min(want, g.nchunks / g.xg);
-    if (want < 2) return;
-    g.kc_per = round_up(ceil_div(g.nchunks, want), g.xg);
-    g.splits = ceil_div(g.nchunks, g.kc_per);
+    const size_t room = scratch > packed + 256 ? scratch - round_up(packed, size_t(256)) : 0;
+    const int smax = int(std::min<size_t>(std::min<size_t>(room / part, size_t(g.nchunks / g.xg)), 16));
+    for (int want = 2; want <= smax; ++want) {
+        const int kc = round_up(ceil_div(g.nchunks, want), g.xg);
+        const int splits = ceil_div(g.nchunks, kc);
+        if (splits < 2) continue;
+        const double c = fwd_cost(tiles, sms, splits, kc, part);
+        if (c < best) {
+            best = c;
+            g.kc_per = kc;
+            g.splits = splits;
+        }
+    }
+    return best;
 }
 
 template <typename T>
@@ -1792,32 +1815,35 @@ template <> constexpr int dt_of_tc<__nv_bfloat16>() { return DT_BF16; }
 
 }  // namespace
 
-// Tile width NT and x super-chunk length for the forward kernel: the feasible choice
-// (shared memory, packed weights within the scratch buffer) minimising (rounds of tiles
-// over the grid) x (NT + 64), where 64 stands for the per-tile cost of streaming the
-// packed weights next to the NT gathered columns.
+// Weight-ring depth, x super-chunk length and K ranges of the forward kernel: feasible
+// (shared memory, packed weights and partials within the scratch buffer) and of the lowest
+// estimated time (fwd_cost).
 template <typename T>
 static bool pick_fwd(const ConvParams& p, const DevInfo& d, FwdGeom& out)
 {
-    // The deepest weight ring, then the longest x super-chunk (fewer, larger slab copies),
-    // that fits.
-    // With too few column tiles for the SMs the K ranges matter more: short super-chunks
-    // first, so that K splits into more ranges.
+    // Per list, the first that fits: the deepest weight ring, then the longest x super-chunk
+    // (fewer, larger slab copies); or short super-chunks first, so that K splits into more
+    // ranges.  Of the two, the lower estimated time (ties: the first list).
     static const int cfgs[][2] = {{4, 8}, {4, 6}, {4, 4}, {4, 2}, {3, 4}, {3, 2}, {2, 2}, {2, 1}};
     static const int cfgs_split[][2] = {{4, 2}, {3, 2}, {2, 2}, {4, 1}, {2, 1}};
-    const bool few = 2 * ceil_div(p.N, FA_TM) * ceil_div(p.OC, TcTraits<T>::split ? 128 : 256) < d.sms;
-    for (int pass = few ? 0 : 1; pass < 2; ++pass) {
-        const int ncfg = pass == 0 ? 5 : 8;
+    bool found = false;
+    double best = 0.0;
+    for (int pass = 0; pass < 2; ++pass) {
+        const int ncfg = pass == 0 ? 8 : 5;
         for (int i = 0; i < ncfg; ++i) {
-            const int* c = pass == 0 ? cfgs_split[i] : cfgs[i];
+            const int* c = pass == 0 ? cfgs[i] : cfgs_split[i];
             FwdGeom g = fwd_geom<T>(p, c[1], c[0]);
             if (g.na < 2 || fwd_smem<T>(p, g) > d.smem_optin || fwd_packed_bytes<T>(g) > kScratchBytes) continue;
-            fwd_set_splits(g, p, d.sms, fwd_packed_bytes<T>(g), kScratchBytes);
-            out = g;
-            return true;
+            const double t = fwd_set_splits(g, p, d.sms, fwd_packed_bytes<T>(g), kScratchBytes);
+            if (!found || t < best) {
+                out = g;
+                best = t;
+                found = true;
+            }
+            break;
         }
     }
-    return false;
+    return found;
 }
 
 bool tc_fwd_ok(const ConvParams& p, int dt, const DevInfo& d)

@@ -35,8 +35,9 @@
  *     after the call returns.  Base pointers must be 16-byte aligned.  Outputs
  *     must not overlap inputs.
  *   - Scratch: the tensor-core paths of conv_fwd and conv_bwd_data first
- *     repack w into the tensor cores' tile layout, and conv_bwd_bias keeps its
- *     per-block partial sums.  They keep one 8 MiB
+ *     repack w into the tensor cores' tile layout (and conv_fwd, when it
+ *     splits K, keeps its fp32 partial sums there), and conv_bwd_bias keeps its
+ *     per-block partial sums.  They keep one 48 MiB
  *     device buffer for that per (device, stream), allocated with cudaMalloc
  *     on the first such call on that stream and held until
  *     conv_release_scratch() or process exit; make that first call outside

@@ -86,15 +86,18 @@ def test_encoder_layers_with_bias(layer, B, dtype):
     fwd_and_bgrad(BiasCase(B, **SHAPES[layer], dtype=dtype), f"{layer} B={B} {dtype}")
 
 
-def test_bias_reaches_both_tensor_core_forward_paths():
-    """On 152 SMs, layer 1 at B = 1024 has enough column tiles for the tensor-core
-    forward to run without K ranges (the bias is added in its epilogue), while layer 2
-    splits K (the bias is added by the reduce kernel); test_encoder_layers_with_bias
-    checks both results."""
-    q1 = binding.conv_query(binding.OP_FWD, BiasCase(1024, **L1, need=("dy",)).desc)
-    q2 = binding.conv_query(binding.OP_FWD, BiasCase(1024, **L2, need=("dy",)).desc)
-    assert q1["algo"] == binding.ALGO_TC and q1["launches"] == 2
-    assert q2["algo"] == binding.ALGO_TC and q2["launches"] == 3
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_bias_in_tensor_core_epilogue(dtype):
+    """On 152 SMs, layer 1 at B = 1024 and 4096 has enough column tiles for the tensor-core
+    forward to run without K ranges, so the bias is added in its epilogue; layer 2 at
+    B = 1024 splits K and the reduce kernel adds it (both checked by
+    test_encoder_layers_with_bias at B = 1024; here layer 1 at B = 4096 too)."""
+    c = BiasCase(4096, **L1, dtype=dtype)
+    q = binding.conv_query(binding.OP_FWD, c.desc)
+    assert q["algo"] == binding.ALGO_TC and q["launches"] == 2 and q["splits"] == 1
+    assert binding.conv_query(binding.OP_FWD, BiasCase(1024, **L1, dtype=dtype, need=("dy",)).desc)["launches"] == 2
+    assert binding.conv_query(binding.OP_FWD, BiasCase(1024, **L2, dtype=dtype, need=("dy",)).desc)["launches"] == 3
+    fwd_and_bgrad(c, f"L1 B=4096 {dtype}")
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
