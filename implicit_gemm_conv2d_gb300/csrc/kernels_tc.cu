@@ -223,7 +223,7 @@ __global__ void pack_dgrad_w_kernel(const ConvParams p, const T* __restrict__ w,
 // ======================================================================================
 constexpr int FV_MMA_WARP = 2;
 constexpr int FV_FMT0 = 96;   // first formatter thread (warp 3)
-constexpr int FV_RAWS = 2;
+constexpr int FV_MAXRAWS = 4;  // max raw x slots of the forward
 
 constexpr int FA_TM = 128;    // columns per forward tile (TMEM lanes)
 constexpr int FA_KSPLIT = 4;  // formatter warps per TMEM lane quarter (each a quarter of the chunk's K)
@@ -238,6 +238,7 @@ struct FwdGeom {
     int n_tiles;        // column tiles of FA_TM
     int nchunks;        // K-chunks per tile
     int xg;             // K-chunks per x super-chunk
+    int nraw;           // raw x slots (shared memory), one super-chunk each
     int nw, na;         // weight stages (shared memory), operand stages (TMEM)
     int nsmax;          // samples a tile can span
     int xs;             // bytes per sample in a raw slot
@@ -250,7 +251,7 @@ struct FwdGeom {
 };
 
 struct FwdBars {
-    uint64_t raw_full[FV_RAWS], raw_empty[FV_RAWS];
+    uint64_t raw_full[FV_MAXRAWS], raw_empty[FV_MAXRAWS];
     uint64_t w_full[FA_MAXW], w_empty[FA_MAXW];
     uint64_t a_full[FA_MAXA], a_empty[FA_MAXA];
     uint64_t acc_full, acc_empty;
@@ -259,7 +260,7 @@ struct FwdBars {
 };
 
 template <typename T>
-inline FwdGeom fwd_geom(const ConvParams& p, int xg, int nw)
+inline FwdGeom fwd_geom(const ConvParams& p, int xg, int nw, int nraw)
 {
     using Tr = TcTraits<T>;
     const int es = int(sizeof(T));
@@ -271,6 +272,7 @@ inline FwdGeom fwd_geom(const ConvParams& p, int xg, int nw)
     g.nchunks = round_up(p.Kred, Tr::KC) / Tr::KC;
     g.xg = xg;
     g.nw = nw;
+    g.nraw = nraw;
     g.nsmax = std::min(p.B, (FA_TM - 1) / p.P + 2);
     const int chmax = std::min(p.IC, (xg * Tr::KC - 1) / p.KK + 2);
     g.xs = round_up(chmax * p.HW * es + 16, 16);
@@ -288,9 +290,6 @@ inline FwdGeom fwd_geom(const ConvParams& p, int xg, int nw)
     return g;
 }
 
-// K ranges for a forward with fewer column tiles than half the SMs: enough ranges to
-// cover the SMs, each a whole number of x super-chunks, their fp32 partials fitting in
-// the scratch buffer beside the packed weights.
 // Estimated forward time in chunk steps of one CTA (about a microsecond each): rounds of
 // work items over the SMs x chunks per item, plus, with K ranges, the reduce kernel (a launch
 // and one pass over the fp32 partials).
@@ -331,7 +330,7 @@ template <typename T>
 inline int fwd_smem(const ConvParams& p, const FwdGeom& g)
 {
     const int kred_pad = round_up(p.Kred, TcTraits<T>::KC);
-    return 1024 + g.nw * g.w_bytes + FV_RAWS * g.raw_bytes + kred_pad * 4 + int(sizeof(FwdBars)) + 16;
+    return 1024 + g.nw * g.w_bytes + g.nraw * g.raw_bytes + kred_pad * 4 + int(sizeof(FwdBars)) + 16;
 }
 
 template <typename T>
@@ -408,7 +407,7 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
     // Layout: weight stages | raw x slots | k offsets | barriers
     unsigned char* wring = smem;
     unsigned char* raw = wring + geo.nw * geo.w_bytes;
-    int* offk = reinterpret_cast<int*>(raw + FV_RAWS * geo.raw_bytes);
+    int* offk = reinterpret_cast<int*>(raw + geo.nraw * geo.raw_bytes);
     FwdBars* bars = reinterpret_cast<FwdBars*>(offk + kred_pad);
     volatile int* abort_flag = &bars->abort_flag;
 
@@ -419,7 +418,7 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
         offk[k] = (k < p.Kred) ? (k_offset(p, k) - sc_ic * p.HW) * ES : 0;
     }
     if (tid == 0) {
-        for (int i = 0; i < FV_RAWS; ++i) {
+        for (int i = 0; i < geo.nraw; ++i) {
             mbar_init(smem_u32(&bars->raw_full[i]), 1);
             mbar_init(smem_u32(&bars->raw_empty[i]), FA_FMTW);
         }
@@ -460,7 +459,7 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
             const int b_first = n0 / p.P, nsamp = (n_end - 1) / p.P - b_first + 1;
             int kc_lo, kc_hi;
             krange(tile, kc_lo, kc_hi);
-            for (int sc = kc_lo / geo.xg; sc < (kc_hi + geo.xg - 1) / geo.xg; ++sc, rp.next(FV_RAWS)) {
+            for (int sc = kc_lo / geo.xg; sc < (kc_hi + geo.xg - 1) / geo.xg; ++sc, rp.next(geo.nraw)) {
                 const int s = rp.i;
                 if (rp.wrapped && !mbar_wait_or_abort(smem_u32(&bars->raw_empty[s]), rp.ph ^ 1u, abort_flag)) {
                     report(const_cast<int*>(abort_flag), 4u);
@@ -667,7 +666,7 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
                 }
                 if (sc_end) {
                     xc = 0;
-                    rp.next(FV_RAWS);
+                    rp.next(geo.nraw);
                 }
             }
             if (!ok) break;
@@ -1824,15 +1823,17 @@ static bool pick_fwd(const ConvParams& p, const DevInfo& d, FwdGeom& out)
     // Per list, the first that fits: the deepest weight ring, then the longest x super-chunk
     // (fewer, larger slab copies); or short super-chunks first, so that K splits into more
     // ranges.  Of the two, the lower estimated time (ties: the first list).
-    static const int cfgs[][2] = {{4, 8}, {4, 6}, {4, 4}, {4, 2}, {3, 4}, {3, 2}, {2, 2}, {2, 1}};
-    static const int cfgs_split[][2] = {{4, 2}, {3, 2}, {2, 2}, {4, 1}, {2, 1}};
+    // {weight stages, chunks per x super-chunk, raw x slots}
+    static const int cfgs[][3] = {{4, 8, 2}, {4, 6, 2}, {4, 4, 2}, {4, 2, 2}, {3, 4, 2}, {3, 2, 2}, {2, 2, 2},
+                                  {2, 1, 2}};
+    static const int cfgs_split[][3] = {{4, 2, 2}, {3, 2, 2}, {2, 2, 2}, {4, 1, 2}, {2, 1, 2}};
     bool found = false;
     double best = 0.0;
     for (int pass = 0; pass < 2; ++pass) {
         const int ncfg = pass == 0 ? 8 : 5;
         for (int i = 0; i < ncfg; ++i) {
             const int* c = pass == 0 ? cfgs[i] : cfgs_split[i];
-            FwdGeom g = fwd_geom<T>(p, c[1], c[0]);
+            FwdGeom g = fwd_geom<T>(p, c[1], c[0], c[2]);
             if (g.na < 2 || fwd_smem<T>(p, g) > d.smem_optin || fwd_packed_bytes<T>(g) > kScratchBytes) continue;
             const double t = fwd_set_splits(g, p, d.sms, fwd_packed_bytes<T>(g), kScratchBytes);
             if (!found || t < best) {
@@ -1864,7 +1865,7 @@ Plan plan_fwd_tc(const ConvParams& p, int dt, const DevInfo& d)
     pl.launches = g.splits > 1 ? 3 : 2;
     pl.block = FA_THREADS;
     pl.splits = g.splits;
-    pl.variant = (g.kc_per * 16 + g.xg) * 16 + g.nw;
+    pl.variant = ((g.kc_per * 16 + g.xg) * 16 + g.nw) * 8 + g.nraw;
     pl.grid = std::min(g.n_tiles * g.oc_tiles * g.splits, d.sms);
     pl.smem = dt == DT_BF16 ? fwd_smem<__nv_bfloat16>(p, g) : fwd_smem<float>(p, g);
     return pl;
@@ -1875,8 +1876,8 @@ static cudaError_t fwd_tc_t(const Plan& pl, const ConvParams& p, const void* x, 
                             const void* bias, void* y, cudaStream_t s)
 {
     const int v = pl.variant;
-    FwdGeom g = fwd_geom<T>(p, (v / 16) % 16, v % 16);
-    g.kc_per = v / 256;
+    FwdGeom g = fwd_geom<T>(p, (v / 128) % 16, (v / 8) % 16, v % 8);
+    g.kc_per = v / 2048;
     g.splits = ceil_div(g.nchunks, g.kc_per);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
