@@ -265,41 +265,58 @@ def run_reference(args):
 # ----------------------------------------------------------------------------------------
 # our arm
 # ----------------------------------------------------------------------------------------
-def source_sha(path):
+def source_sha(paths):
+    """First 16 hex digits of the SHA-256 of the concatenated files."""
     h = hashlib.sha256()
-    with open(path, "rb") as f:
-        h.update(f.read())
+    for path in paths:
+        with open(path, "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def read_traffic(kernel_key):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel source
-    it was taken from is unchanged (the sha in the table); else None."""
+    """DRAM bytes per launch from the committed ncu summary, if the kernel sources it was
+    taken from are unchanged (their '+'-joined names and sha in the table); else None."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
     for line in open(path):
         line = line.split("#", 1)[0].split()
         if len(line) == 4 and line[0] == kernel_key:
-            src = os.path.join(ROOT, "implicit_gemm_conv2d_gb300", "csrc", line[3].split(":")[0])
-            if os.path.exists(src) and source_sha(src) == line[3].split(":")[1]:
+            names, sha = line[3].split(":")
+            srcs = [os.path.join(ROOT, "implicit_gemm_conv2d_gb300", "csrc", n) for n in names.split("+")]
+            if all(os.path.exists(x) for x in srcs) and source_sha(srcs) == sha:
                 return float(line[1])
     return None
 
 
 class Workload:
-    def __init__(self, layer, dtype, B, device):
+    def __init__(self, layer, dtype, B, device, on_device=False):
+        """on_device: draw the inputs with a seeded torch generator on the GPU (same
+        distributions as synth.conv_inputs, other values) instead of the host generator;
+        for timing-only sweeps at large B, where host generation would take minutes."""
         import torch
         from implicit_gemm_conv2d_gb300 import binding, synth
         self.layer, self.dtype, self.B = layer, dtype, B
         self.shape = dict(LAYERS[layer])
         self.tdt = torch.float32 if dtype == "f32" else torch.bfloat16
         s = self.shape
-        inp = synth.conv_inputs(B, s["IC"], s["OC"], s["H"], s["W"], s["K"], s["S"], dtype=dtype)
-        self.inp = inp
-        self.x = torch.from_numpy(inp["x"]).to(device).to(self.tdt).contiguous()
-        self.w = torch.from_numpy(inp["w"]).to(device).to(self.tdt).contiguous()
-        self.dy = torch.from_numpy(inp["dy"]).to(device).to(self.tdt).contiguous()
+        OH, OW = (s["H"] - s["K"]) // s["S"] + 1, (s["W"] - s["K"]) // s["S"] + 1
+        if on_device:
+            g = torch.Generator(device=device)
+            g.manual_seed(synth.SEED)
+            a = 1.0 / math.sqrt(s["IC"] * s["K"] * s["K"])
+            self.inp = None
+            self.x = torch.randn((B, s["IC"], s["H"], s["W"]), generator=g, device=device).to(self.tdt)
+            self.w = ((torch.rand((s["OC"], s["IC"], s["K"], s["K"]), generator=g, device=device) * 2 - 1) * a).to(
+                self.tdt)
+            self.dy = torch.randn((B, s["OC"], OH, OW), generator=g, device=device).to(self.tdt)
+        else:
+            inp = synth.conv_inputs(B, s["IC"], s["OC"], s["H"], s["W"], s["K"], s["S"], dtype=dtype)
+            self.inp = inp
+            self.x = torch.from_numpy(inp["x"]).to(device).to(self.tdt).contiguous()
+            self.w = torch.from_numpy(inp["w"]).to(device).to(self.tdt).contiguous()
+            self.dy = torch.from_numpy(inp["dy"]).to(device).to(self.tdt).contiguous()
         self.desc = binding.make_desc(B, s["IC"], s["OC"], s["H"], s["W"], s["K"], s["S"], s["relu"], self.tdt)
         OH, OW = binding.out_dims(self.desc)
         self.y = torch.empty((B, s["OC"], OH, OW), dtype=self.tdt, device=device)
@@ -536,6 +553,35 @@ def bias_extras(wls, flush_buf, peaks, device):
     return out
 
 
+SWEEP_BATCHES = (256, 1024, 4096, 16384)
+
+
+def batch_sweep(flush_buf, sms, sm_mhz, peaks, device):
+    """Per-operation cold-L2 time, throughput and roofline fraction of both layers in both
+    dtypes over a range of batch sizes (the plans the library picks for each), inputs drawn
+    on the device."""
+    import torch
+    out = {}
+    for layer in ("layer1", "layer2"):
+        for dt in ("f32", "bf16"):
+            for B in SWEEP_BATCHES:
+                wl = Workload(layer, dt, B, device, on_device=True)
+                wl.capture()
+                per, _ = time_step(wl, flush_buf, 30, 3)
+                entry = {}
+                for o in OPS:
+                    t_ms = statistics.mean(per[o])
+                    r = roofline_of(wl, o, t_ms, sms, sm_mhz, peaks)
+                    pl = wl.plans[o]
+                    entry[o] = {"us_cold_l2": t_ms * 1e3, "tflops": wl.flops / (t_ms * 1e-3) / 1e12,
+                                "bound": r["bound"], "frac": r["frac"], "algo": pl["algo_name"],
+                                "grid": pl["grid"], "splits": pl["splits"], "launches": pl["launches"]}
+                out[f"{layer}_{dt}_B{B}"] = entry
+                del wl
+                torch.cuda.empty_cache()
+    return out
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -690,6 +736,7 @@ def run_ours(args):
                 others[f"{layer}_{dt}"] = entry
         line["configs_b%d" % args.batch] = others
         line["bias"] = bias_extras(wls, flush_buf, peaks, device)
+        line["batch_sweep"] = batch_sweep(flush_buf, sms, sm_mhz, peaks, device)
         if world == 1:
             line["cpu_baseline"] = cpu_baseline(LAYERS[args.layer], 128, 10.0)
     print(json.dumps(line))

@@ -48,11 +48,27 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
         : "memory");
     return ok != 0;
 }
-// Bounded wait for the phase with the given parity to complete: up to 4096 hardware
-// sleeps of at most 1 ms (about 4 s).  Returns false (and the caller reports an error
-// and unwinds) if it never does.
+// Non-blocking test of the phase with the given parity: true if it has completed.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity to complete: a non-blocking test
+// first (a phase that completed long ago costs no suspend round trip), then up to 4096
+// hardware sleeps of at most 1 ms (about 4 s).  Returns false (and the caller reports an
+// error and unwinds) if it never does.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
 {
+    if (mbar_test_wait(bar, parity)) return true;
     for (uint32_t i = 0; i < 4096u; ++i)
         if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
     return false;
@@ -62,6 +78,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
 // is nonzero.
 __device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, const volatile int* abort)
 {
+    if (mbar_test_wait(bar, parity)) return true;
     for (uint32_t i = 0; i < 4096u; ++i) {
         if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
         if (*abort) return false;
