@@ -52,7 +52,9 @@ class PlanInfo(ctypes.Structure):
 EXPORTS = ["conv_fwd", "conv_bwd_data", "conv_bwd_filter_workspace_size", "conv_bwd_filter",
            "conv_status_string", "conv_out_dims", "conv_query", "conv_set_algo",
            "conv_fastdivmod_check", "conv_l2_flush", "conv_version", "conv_bwd_filter_noalloc",
-           "conv_device_status", "conv_release_scratch", "conv_fwd_bias", "conv_bwd_bias"]
+           "conv_device_status", "conv_release_scratch", "conv_fwd_bias", "conv_bwd_bias",
+           "conv_wait_selftest"]
+STATUS_WAIT_SELFTEST = 1 << 30
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -91,6 +93,7 @@ def lib():
         L.conv_release_scratch.argtypes = []
         L.conv_fwd_bias.argtypes = [dp, vp, vp, vp, vp, vp]
         L.conv_bwd_bias.argtypes = [dp, vp, vp, vp, vp]
+        L.conv_wait_selftest.argtypes = [ctypes.c_uint32, vp]
         _lib = L
         return L
 
@@ -192,6 +195,12 @@ def conv_device_status(reset: bool = False) -> int:
     v = ctypes.c_uint32()
     _check(lib().conv_device_status(ctypes.byref(v), int(reset)), "conv_device_status")
     return v.value
+
+
+def conv_wait_selftest(max_sleeps: int, stream=None) -> None:
+    """Run the bounded-wait self-test kernel (see include/conv.h); its timeout sets
+    STATUS_WAIT_SELFTEST in conv_device_status()."""
+    _check(lib().conv_wait_selftest(int(max_sleeps), _stream(stream)), "conv_wait_selftest")
 
 
 def conv_release_scratch() -> None:

@@ -383,13 +383,19 @@ uint64_t conv_fastdivmod_check(uint32_t d, uint32_t lo, uint32_t hi)
 int conv_device_status(uint32_t* status, int reset)
 {
     if (!status) return CONV_ERR_NULL;
-    unsigned v = 0;
-    if (tc_read_status(&v, reset != 0) != cudaSuccess) {
+    unsigned v = 0, w = 0;
+    if (tc_read_status(&v, reset != 0) != cudaSuccess || diag_read_status(&w, reset != 0) != cudaSuccess) {
         cudaGetLastError();
         return CONV_ERR_CUDA;
     }
-    *status = v;
+    *status = v | w;
     return CONV_OK;
+}
+
+int conv_wait_selftest(uint32_t max_sleeps, conv_stream_t stream)
+{
+    if (max_sleeps < 1 || max_sleeps > 1000000u) return CONV_ERR_UNSUPPORTED;
+    return cuda_status(run_wait_selftest(max_sleeps, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int conv_release_scratch(void) { return release_scratch(); }

@@ -133,6 +133,10 @@ cudaError_t run_bgrad(const Plan&, const ConvParams&, int dt, const void* dy, co
 
 // Error bits the tensor-core kernels set when a bounded wait runs out.
 cudaError_t tc_read_status(unsigned* out, bool reset);
+// Bounded-wait self-test (kernels_diag.cu): a one-CTA kernel whose wait on a never-completed
+// mbarrier runs out and sets CONV_STATUS_WAIT_SELFTEST in its own status word.
+cudaError_t run_wait_selftest(unsigned max_sleeps, cudaStream_t s);
+cudaError_t diag_read_status(unsigned* out, bool reset);
 
 __host__ __device__ inline int round_up(int a, int b) { return (a + b - 1) / b * b; }
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }

@@ -224,6 +224,15 @@ uint64_t conv_fastdivmod_check(uint32_t d, uint32_t lo, uint32_t hi);
  * Synchronises the device. */
 int conv_device_status(uint32_t* status, int reset);
 
+/* Diagnostics: the timeout path of those waits, without a fault or a hang.  Enqueues on
+ * `stream` one CTA whose thread waits on an mbarrier that nothing completes, through a
+ * bounded loop of at most `max_sleeps` hardware sleeps of up to 1 microsecond each (the
+ * kernels' own waits allow 4096 sleeps of up to 1 ms); when the loop runs out it sets bit 30
+ * (CONV_STATUS_WAIT_SELFTEST) of the status word and returns normally, so the context stays
+ * usable.  max_sleeps must be in [1, 10^6] (CONV_ERR_UNSUPPORTED otherwise). */
+#define CONV_STATUS_WAIT_SELFTEST (1u << 30)
+int conv_wait_selftest(uint32_t max_sleeps, conv_stream_t stream);
+
 /* Free the per-(device, stream) packed-weight buffers (synchronises each
  * device that holds one).  Later calls allocate again as needed. */
 int conv_release_scratch(void);

@@ -111,6 +111,11 @@ def test_empty_batch_is_a_no_op(L):
     assert L.conv_bwd_bias(ctypes.byref(d), None, None, None, None) == -1  # db is still written
 
 
+def test_wait_selftest_arguments_checked_before_cuda(L):
+    assert L.conv_wait_selftest(0, None) == -3
+    assert L.conv_wait_selftest(1000001, None) == -3
+
+
 def test_set_algo_validation(L):
     assert L.conv_set_algo(4, 0) == -3
     assert L.conv_set_algo(-1, 0) == -3
