@@ -158,7 +158,7 @@ int conv_bwd_filter(const conv_desc_t* desc, const void* x, const void* dy, cons
 int conv_bwd_bias(const conv_desc_t* desc, const void* dy, const void* y, void* db,
                   conv_stream_t stream);
 
-/* Weight gradient that allocates nothing (the paper has no counterpart; this
+/* Weight gradient that allocates nothing (PufferLib PR #522 has no counterpart; this
  * entry point exists for callers of this library that cannot allocate device
  * memory: hosts that hand the library only the input and output buffers and own
  * every other byte, and code that must not allocate while a step runs, where an
