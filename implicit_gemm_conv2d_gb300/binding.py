@@ -53,7 +53,7 @@ EXPORTS = ["conv_fwd", "conv_bwd_data", "conv_bwd_filter_workspace_size", "conv_
            "conv_status_string", "conv_out_dims", "conv_query", "conv_set_algo",
            "conv_fastdivmod_check", "conv_l2_flush", "conv_version", "conv_bwd_filter_noalloc",
            "conv_device_status", "conv_release_scratch", "conv_fwd_bias", "conv_bwd_bias",
-           "conv_wait_selftest"]
+           "conv_wait_selftest", "conv_query_for_device"]
 STATUS_WAIT_SELFTEST = 1 << 30
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -94,6 +94,7 @@ def lib():
         L.conv_fwd_bias.argtypes = [dp, vp, vp, vp, vp, vp]
         L.conv_bwd_bias.argtypes = [dp, vp, vp, vp, vp]
         L.conv_wait_selftest.argtypes = [ctypes.c_uint32, vp]
+        L.conv_query_for_device.argtypes = [ctypes.c_int, dp] + [ctypes.c_int] * 4 + [ctypes.POINTER(PlanInfo)]
         _lib = L
         return L
 
@@ -172,6 +173,20 @@ def conv_bwd_filter_noalloc(desc: ConvDesc, x, dy, y, dw, stream=None) -> None:
 def conv_query(op: int, desc: ConvDesc) -> dict:
     info = PlanInfo()
     _check(lib().conv_query(int(op), ctypes.byref(desc), ctypes.byref(info)), "conv_query")
+    d = info.as_dict()
+    d["algo_name"] = ALGO_NAMES.get(d["algo"], "?")
+    return d
+
+
+GB300 = dict(sms=152, smem_optin=232448, cc_major=10, cc_minor=3)
+
+
+def conv_query_for_device(op: int, desc: ConvDesc, sms: int, smem_optin: int, cc_major: int,
+                          cc_minor: int) -> dict:
+    """The plan for a device described by its properties (host only, no CUDA call)."""
+    info = PlanInfo()
+    _check(lib().conv_query_for_device(int(op), ctypes.byref(desc), int(sms), int(smem_optin), int(cc_major),
+                                       int(cc_minor), ctypes.byref(info)), "conv_query_for_device")
     d = info.as_dict()
     d["algo_name"] = ALGO_NAMES.get(d["algo"], "?")
     return d

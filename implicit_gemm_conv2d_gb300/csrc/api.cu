@@ -261,15 +261,13 @@ int conv_set_algo(int op, int algo)
     return CONV_OK;
 }
 
-int conv_query(int op, const conv_desc_t* desc, conv_plan_info_t* info)
+static int query_on(int op, const conv_desc_t* desc, const DevInfo& d, conv_plan_info_t* info)
 {
     ConvParams p;
     int rc = make_params(desc, p);
     if (rc != CONV_OK) return rc;
     if (!info) return CONV_ERR_NULL;
     if (op < 0 || op > 3) return CONV_ERR_UNSUPPORTED;
-    DevInfo d;
-    if ((rc = device_info(d)) != CONV_OK) return rc;
     Plan pl;
     if ((rc = choose(op, p, desc->dtype, d, pl)) != CONV_OK) return rc;
     info->algo = pl.algo;
@@ -280,6 +278,31 @@ int conv_query(int op, const conv_desc_t* desc, conv_plan_info_t* info)
     info->splits = pl.splits;
     info->workspace = pl.workspace;
     return CONV_OK;
+}
+
+int conv_query(int op, const conv_desc_t* desc, conv_plan_info_t* info)
+{
+    ConvParams p;
+    int rc = make_params(desc, p);
+    if (rc != CONV_OK) return rc;
+    if (!info) return CONV_ERR_NULL;
+    if (op < 0 || op > 3) return CONV_ERR_UNSUPPORTED;
+    DevInfo d;
+    if ((rc = device_info(d)) != CONV_OK) return rc;
+    return query_on(op, desc, d, info);
+}
+
+int conv_query_for_device(int op, const conv_desc_t* desc, int sms, int smem_optin, int cc_major, int cc_minor,
+                          conv_plan_info_t* info)
+{
+    if (sms < 1 || smem_optin < 1 || cc_major < 1 || cc_minor < 0) return CONV_ERR_UNSUPPORTED;
+    DevInfo d;
+    d.device = -1;
+    d.sms = sms;
+    d.smem_optin = smem_optin;
+    d.cc_major = cc_major;
+    d.cc_minor = cc_minor;
+    return query_on(op, desc, d, info);
 }
 
 int conv_fwd(const conv_desc_t* desc, const void* x, const void* w, void* y, conv_stream_t stream)

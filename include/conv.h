@@ -203,6 +203,15 @@ typedef struct {
 } conv_plan_info_t;
 int conv_query(int op, const conv_desc_t* desc, conv_plan_info_t* info);
 
+/* The same plan for a device described by its properties instead of the current one,
+ * computed on the host with no CUDA call (capacity planning; tests without a GPU).
+ * sms: streaming multiprocessors; smem_optin: opt-in dynamic shared memory per block in
+ * bytes; cc_major / cc_minor: compute capability (the tensor-core family needs
+ * cc_major == 10).  The algorithm forced with conv_set_algo applies.  Returns
+ * CONV_ERR_UNSUPPORTED for a property below 1 (cc_minor below 0). */
+int conv_query_for_device(int op, const conv_desc_t* desc, int sms, int smem_optin, int cc_major, int cc_minor,
+                          conv_plan_info_t* info);
+
 /* Force an algorithm family for one operation (CONV_ALGO_AUTO restores the
  * library's choice).  Process-wide, not thread-safe; meant for tests and
  * benchmarks.  Returns CONV_ERR_UNSUPPORTED for an unknown op or algo, and for

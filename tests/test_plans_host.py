@@ -1,0 +1,118 @@
+"""The planner on the host, for a described GB300 (152 SMs, 227 KB opt-in shared memory,
+compute capability 10.3) and for devices without the tensor-core family: every plan the
+library would launch stays inside the hardware limits and the scratch buffer, the
+tensor-core forward splits K only when its column tiles fill fewer than half the SMs, and
+forcing a family is honoured.  No GPU: conv_query_for_device makes no CUDA call."""
+import pytest
+
+from implicit_gemm_conv2d_gb300 import binding
+
+GB300 = binding.GB300
+SCRATCH = 48 << 20
+OPS = (binding.OP_FWD, binding.OP_BWD_DATA, binding.OP_BWD_FILTER, binding.OP_BWD_BIAS)
+
+SHAPES = {
+    "L1": (59, 128, 11, 15, 5, 3, 1),
+    "L2": (128, 128, 3, 4, 3, 1, 0),
+    "odd": (3, 5, 7, 9, 2, 2, 1),
+    "wide_oc_p16": (4, 200, 6, 6, 3, 1, 0),
+    "kk_above_128": (2, 8, 13, 12, 12, 1, 1),
+    "k1": (16, 24, 3, 5, 1, 1, 0),
+    "k_eq_input": (7, 33, 5, 5, 5, 2, 1),
+    "stride_gt_k": (5, 20, 10, 11, 2, 3, 0),
+    "long_rows": (1, 3, 120, 120, 1, 1, 0),
+}
+BATCHES = (1, 37, 256, 1024, 4096, 16384, 32768)
+
+
+@pytest.fixture(autouse=True)
+def _restore_algo():
+    yield
+    for op in OPS:
+        binding.conv_set_algo(op, binding.ALGO_AUTO)
+
+
+def plan(op, B, shape, dtype, dev=GB300):
+    IC, OC, H, W, K, S, relu = shape
+    return binding.conv_query_for_device(op, binding.make_desc(B, IC, OC, H, W, K, S, relu, dtype), **dev)
+
+
+@pytest.mark.parametrize("dtype", [binding.F32, binding.BF16])
+@pytest.mark.parametrize("name", list(SHAPES))
+def test_plans_within_limits(name, dtype):
+    IC, OC, H, W, K, S, relu = SHAPES[name]
+    OH, OW = (H - K) // S + 1, (W - K) // S + 1
+    for B in BATCHES:
+        if B * IC * H * W >= 2 ** 31:
+            continue
+        for op in OPS:
+            q = plan(op, B, SHAPES[name], dtype)
+            where = (name, dtype, B, op, q)
+            assert q["launches"] >= 1, where
+            assert 32 <= q["block"] <= 1024 and q["block"] % 32 == 0, where
+            assert 0 <= q["smem_bytes"] <= GB300["smem_optin"], where
+            assert q["grid"] >= 1, where
+            if q["algo"] == binding.ALGO_TC:
+                assert q["grid"] <= GB300["sms"], where
+            if op == binding.OP_FWD and q["algo"] == binding.ALGO_TC:
+                assert q["splits"] >= 1 and q["launches"] == (3 if q["splits"] > 1 else 2), where
+            if op == binding.OP_BWD_FILTER and q["splits"] > 0:
+                assert q["workspace"] >= q["splits"] * OC * IC * K * K * 4, where
+            if op == binding.OP_BWD_BIAS:
+                if q["algo"] == binding.ALGO_FFMA:
+                    assert q["block"] <= 512 and q["smem_bytes"] <= 48 * 1024, where
+                    assert 1 <= q["splits"] <= 1024 and q["splits"] * OC * 4 <= SCRATCH, where
+                    assert q["launches"] == 2, where
+                else:
+                    assert q["algo"] == binding.ALGO_DIRECT and OH * OW > 12288, where
+
+
+def test_encoder_layers_use_tensor_cores_on_gb300():
+    for name in ("L1", "L2"):
+        for dtype in (binding.F32, binding.BF16):
+            for op in (binding.OP_FWD, binding.OP_BWD_DATA, binding.OP_BWD_FILTER):
+                assert plan(op, 1024, SHAPES[name], dtype)["algo"] == binding.ALGO_TC, (name, dtype, op)
+
+
+@pytest.mark.parametrize("dtype", [binding.F32, binding.BF16])
+def test_forward_k_ranges_only_with_few_column_tiles(dtype):
+    # layer 1 at B = 1024: 12288 columns = 96 tiles of 128, more than half of 152 SMs
+    q = plan(binding.OP_FWD, 1024, SHAPES["L1"], dtype)
+    assert q["splits"] == 1 and q["grid"] == 96
+    # layer 2 at B = 1024: 2048 columns = 16 tiles: K splits, the work items fill the SMs
+    q = plan(binding.OP_FWD, 1024, SHAPES["L2"], dtype)
+    assert q["splits"] > 1 and 16 * q["splits"] >= GB300["sms"] // 2
+    # large batches never split
+    for name in ("L1", "L2"):
+        assert plan(binding.OP_FWD, 16384, SHAPES[name], dtype)["splits"] == 1
+
+
+def test_no_tensor_core_plan_without_the_hardware():
+    hopper = dict(sms=132, smem_optin=232448, cc_major=9, cc_minor=0)
+    small = dict(sms=152, smem_optin=48 * 1024, cc_major=10, cc_minor=3)
+    for op in (binding.OP_FWD, binding.OP_BWD_DATA, binding.OP_BWD_FILTER):
+        for name in SHAPES:
+            q = plan(op, 1024, SHAPES[name], binding.F32, hopper)
+            assert q["algo"] in (binding.ALGO_FFMA, binding.ALGO_DIRECT), (op, name, q)
+            q = plan(op, 1024, SHAPES[name], binding.F32, small)
+            assert q["smem_bytes"] <= small["smem_optin"], (op, name, q)
+            if name in ("L1", "L2"):  # their tensor-core stages need more than 48 KB
+                assert q["algo"] != binding.ALGO_TC, (op, name, q)
+
+
+def test_forced_family_is_honoured():
+    for op in OPS:
+        binding.conv_set_algo(op, binding.ALGO_DIRECT)
+        assert plan(op, 1024, SHAPES["L1"], binding.F32)["algo"] == binding.ALGO_DIRECT
+        binding.conv_set_algo(op, binding.ALGO_AUTO)
+    binding.conv_set_algo(binding.OP_FWD, binding.ALGO_TC)
+    with pytest.raises(binding.ConvError):  # no tensor cores on this device: the forced family cannot run
+        plan(binding.OP_FWD, 1024, SHAPES["L1"], binding.F32, dict(sms=132, smem_optin=232448, cc_major=9,
+                                                                   cc_minor=0))
+
+
+def test_device_properties_checked():
+    d = binding.make_desc(8, 59, 128, 11, 15, 5, 3, 1, binding.F32)
+    for bad in (dict(GB300, sms=0), dict(GB300, smem_optin=0), dict(GB300, cc_major=0), dict(GB300, cc_minor=-1)):
+        with pytest.raises(binding.ConvError):
+            binding.conv_query_for_device(binding.OP_FWD, d, **bad)
