@@ -142,12 +142,14 @@ int conv_bwd_filter(const conv_desc_t* desc, const void* x, const void* dy, cons
 
 /* Bias gradient:  db[oc] = sum over b, oh, ow of g (g = dy masked by y > 0 when
  * relu), accumulated in fp32 and rounded once to the dtype.  Two kernels: the
- * first gives each CTA a contiguous range of samples and sums, per output
- * position (oc, oh, ow), down its rows in ascending b, then over the positions
- * of each channel in ascending (oh, ow); the second adds the CTAs' per-channel
- * sums in a fixed order (strided by 32 in ascending order, then a fixed
- * butterfly).  The partial sums live in the per-stream scratch buffer (see
- * Scratch above; this call allocates it if it is the first on its stream).
+ * first gives each CTA a contiguous range of samples and sums each output
+ * position (oc, oh, ow) down its rows (in R interleaved row lanes, each in
+ * ascending b), then adds, per channel, its positions in ascending (oh, ow),
+ * each over the row lanes in ascending order; the second adds the CTAs'
+ * per-channel sums in a fixed order (warp w of 32 takes ranges w, w + 32, ...
+ * in ascending order, then the 32 warp sums are added in ascending order).  The
+ * partial sums live in the per-stream scratch buffer (see Scratch above; this
+ * call allocates it if it is the first on its stream).
  * A shape whose OC*OH*OW row is too long for the first kernel's shared-memory
  * window (more than 12288 positions per output channel) runs a one-warp-per-
  * channel kernel instead (the same result up to summation order).
