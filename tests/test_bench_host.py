@@ -66,3 +66,23 @@ def test_pipe_peaks():
     assert pk == pytest.approx(1920.6 * 1.1 / 2.25 / 3)
     pk, _ = bench.pipe_peak("ffma", "f32", 152, 2070.0, peaks)
     assert pk == pytest.approx(152 * 128 * 2 * 2070e6 / 1e12)
+
+
+def test_reference_arm_prints_one_contract_line():
+    """`bench.py --impl reference` times the oracle on the host cores and prints one JSON
+    line with the contract's keys (no GPU needed)."""
+    import json
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["value"] > 0 and d["steps"] == 1
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["e2e"]["value"] == d["value"]
