@@ -9,8 +9,9 @@
 // layer has a fused ReLU (implicit im2col: X and G are gathered on the fly).
 //   bf16: tcgen05.mma kind::f16, bf16 operands, fp32 accumulation.
 //   fp32: tcgen05.mma kind::tf32 on split operands (v = hi + lo, hi = tf32(v),
-//         lo = tf32(v - hi)) summing hi*hi + hi*lo + lo*hi, which keeps about 21
-//         significant bits per product: fp32-level accuracy on the tensor pipe.
+//         lo = v - hi, of which the MMA reads the leading tf32 bits) summing
+//         hi*hi + hi*lo + lo*hi, which keeps about 21 significant bits per product:
+//         fp32-level accuracy on the tensor pipe.
 // Each kernel is warp-specialized: producer warps stage raw input slabs and packed
 // weight chunks with bulk asynchronous copies, formatter warps turn the raw slabs into
 // MMA operands, one thread issues the MMAs, and mbarriers chain the stages.
