@@ -136,6 +136,7 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
+        self.oneshot = []
         self.t = None
         self.t0 = self.t1 = None
 
@@ -157,11 +158,24 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append((time.monotonic(), line.strip()))
 
+    def query_once(self):
+        """One nvidia-smi query now (the timed region of a short run can fall between two
+        100 ms samples; a query right before and right after it always lands)."""
+        try:
+            r = subprocess.run(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=10)
+            if r.returncode == 0 and r.stdout.strip():
+                self.oneshot.append((time.monotonic(), r.stdout.strip().splitlines()[0]))
+        except (OSError, subprocess.TimeoutExpired):
+            pass
+
     def mark_start(self):
+        self.query_once()
         self.t0 = time.monotonic()
 
     def mark_end(self):
         self.t1 = time.monotonic()
+        self.query_once()
 
     def __exit__(self, *exc):
         if self.proc:
@@ -176,11 +190,10 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for ts, ln in self.lines:
-            if self.t0 is not None and ts < self.t0:
-                continue
-            if self.t1 is not None and ts > self.t1 + 0.1:
-                continue
+        inside = [(ts, ln) for ts, ln in self.lines
+                  if not (self.t0 is not None and ts < self.t0) and not (self.t1 is not None and ts > self.t1 + 0.1)]
+        n_inside = len(inside)
+        for ts, ln in inside + self.oneshot:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -192,10 +205,13 @@ class ClockSampler:
             for name, val in zip(names, parts[5:9]):
                 if val.lower() == "active":
                     reasons.add(name)
+        how = ("nvidia-smi: one query right before and one right after the timed region, plus "
+               "100 ms samples inside it")
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "samples_inside": 0,
+                    "how": how}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "samples_inside": n_inside, "how": how}
 
 
 # ----------------------------------------------------------------------------------------
@@ -251,7 +267,9 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": workload_config("layer1", "f32", 1024),
+        "config": dict(workload_config("layer1", "f32", b_sample),
+                       sample=f"each step runs the fp64 oracle on B={b_sample} samples of the B=1024 "
+                              "workload (same shapes, seeded inputs); the value counts those samples' FLOPs"),
         "cpu_baseline": {"value": value, "unit": "GFLOP/s", "cores": oracle.default_threads(),
                          "kind": "oracle",
                          "sample": f"each step the fp64 oracle on {b_sample} of the 1024 samples (the same "
@@ -324,9 +342,17 @@ class Workload:
         self.dw = torch.empty_like(self.w)
         self.ws = torch.empty(max(16, binding.conv_bwd_filter_workspace_size(self.desc)), dtype=torch.uint8,
                               device=device)
+        # The step runs the workspace-taking forward and d_input (weights packed once per call into
+        # these caller-owned buffers); "fwd_plain" / "dgrad_plain" are the no-workspace entry points.
+        self.ws_fwd = torch.empty(max(16, binding.conv_fwd_workspace_size(self.desc)), dtype=torch.uint8, device=device)
+        self.ws_dgrad = torch.empty(max(16, binding.conv_bwd_data_workspace_size(self.desc)), dtype=torch.uint8,
+                                    device=device)
         self.flops = flops(B=B, **s)
-        self.launches = sum(binding.conv_query(op, self.desc)["launches"] for op in range(3))
-        self.plans = {name: binding.conv_query(op, self.desc) for op, name in enumerate(OPS)}
+        step_ops = (binding.OP_FWD_WS, binding.OP_BWD_DATA_WS, binding.OP_BWD_FILTER)
+        self.launches = sum(binding.conv_query(op, self.desc)["launches"] for op in step_ops)
+        self.plans = {name: binding.conv_query(op, self.desc) for op, name in zip(step_ops, OPS)}
+        self.plans["fwd_plain"] = binding.conv_query(binding.OP_FWD, self.desc)
+        self.plans["dgrad_plain"] = binding.conv_query(binding.OP_BWD_DATA, self.desc)
 
     def capture(self):
         """One CUDA graph per operation (captured after a warm-up call), so that
@@ -336,14 +362,12 @@ class Workload:
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
-            for o in OPS:
+            for o in OPS + ("fwd_plain", "dgrad_plain"):
                 self.op(o)
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
-        for o in OPS:
+        for o in OPS + ("fwd_plain", "dgrad_plain"):
             g = torch.cuda.CUDAGraph()
-            # Capture on the stream the warm-up ran on: the library's per-stream
-            # packed-weight buffer already exists there.
             with torch.cuda.graph(g, stream=s):
                 self.op(o)
             self.graphs[o] = g
@@ -360,8 +384,12 @@ class Workload:
         from implicit_gemm_conv2d_gb300 import binding
         relu_y = self.y if self.shape["relu"] else None
         if name == "fwd":
-            binding.conv_fwd(self.desc, self.x, self.w, self.y, stream)
+            binding.conv_fwd_ws(self.desc, self.x, self.w, None, self.y, self.ws_fwd, stream)
         elif name == "dgrad":
+            binding.conv_bwd_data_ws(self.desc, self.dy, self.w, relu_y, self.dx, self.ws_dgrad, stream)
+        elif name == "fwd_plain":
+            binding.conv_fwd(self.desc, self.x, self.w, self.y, stream)
+        elif name == "dgrad_plain":
             binding.conv_bwd_data(self.desc, self.dy, self.w, relu_y, self.dx, stream)
         else:
             binding.conv_bwd_filter(self.desc, self.x, self.dy, relu_y, self.dw, self.ws, stream)
@@ -415,32 +443,80 @@ def warm_us(wl, iters=200, warmup=50):
     return out
 
 
-def e2e(wl, flush_buf, steps):
-    """Same step through the public API with host buffers: pinned host inputs are
-    copied in, the three operations run, the three results are copied out."""
+def e2e(wl, flush_buf, steps, chunks=4):
+    """Same step through the public API with host buffers: every step copies the pinned host
+    inputs in and the three results out.  The batch is cut into `chunks` sample ranges so
+    that copies overlap compute: per range, x and dy go in on a copy-in stream, the forward and
+    d_input of that range run on the compute stream, and y and dx come out on a copy-out
+    stream; wgrad runs once on the whole batch when every range is in, then dw comes out.
+    Events order the three streams; the timed region runs from the first copy's start to the
+    last copy's end."""
     import torch
     from implicit_gemm_conv2d_gb300 import binding
+    B = wl.B
+    chunks = max(1, min(chunks, B))
+    bounds = [B * i // chunks for i in range(chunks + 1)]
+    s = wl.shape
+    relu = s["relu"]
+    descs = [binding.make_desc(bounds[i + 1] - bounds[i], s["IC"], s["OC"], s["H"], s["W"], s["K"], s["S"],
+                               relu, wl.tdt) for i in range(chunks)]
+    ws_f = [torch.empty(max(16, binding.conv_fwd_workspace_size(d)), dtype=torch.uint8, device=wl.x.device)
+            for d in descs]
+    ws_d = [torch.empty(max(16, binding.conv_bwd_data_workspace_size(d)), dtype=torch.uint8, device=wl.x.device)
+            for d in descs]
     xh = wl.x.cpu().pin_memory()
     wh = wl.w.cpu().pin_memory()
     dyh = wl.dy.cpu().pin_memory()
     yh = torch.empty(wl.y.shape, dtype=wl.tdt).pin_memory()
     dxh = torch.empty(wl.dx.shape, dtype=wl.tdt).pin_memory()
     dwh = torch.empty(wl.dw.shape, dtype=wl.tdt).pin_memory()
-    stream = torch.cuda.current_stream()
+    main = torch.cuda.current_stream()
+    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+
+    def step():
+        s_in.wait_stream(main)
+        s_cmp.wait_stream(main)
+        s_out.wait_stream(main)
+        with torch.cuda.stream(s_in):
+            wl.w.copy_(wh, non_blocking=True)
+        ins = []
+        for i in range(chunks):
+            a, b = bounds[i], bounds[i + 1]
+            with torch.cuda.stream(s_in):
+                wl.x[a:b].copy_(xh[a:b], non_blocking=True)
+                wl.dy[a:b].copy_(dyh[a:b], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(s_in)
+                ins.append(ev)
+        for i in range(chunks):
+            a, b = bounds[i], bounds[i + 1]
+            s_cmp.wait_event(ins[i])
+            binding.conv_fwd_ws(descs[i], wl.x[a:b], wl.w, None, wl.y[a:b], ws_f[i], s_cmp)
+            binding.conv_bwd_data_ws(descs[i], wl.dy[a:b], wl.w, wl.y[a:b] if relu else None, wl.dx[a:b], ws_d[i],
+                                     s_cmp)
+            done = torch.cuda.Event()
+            done.record(s_cmp)
+            s_out.wait_event(done)
+            with torch.cuda.stream(s_out):
+                yh[a:b].copy_(wl.y[a:b], non_blocking=True)
+                dxh[a:b].copy_(wl.dx[a:b], non_blocking=True)
+        binding.conv_bwd_filter(wl.desc, wl.x, wl.dy, wl.y if relu else None, wl.dw, wl.ws, s_cmp)
+        done = torch.cuda.Event()
+        done.record(s_cmp)
+        s_out.wait_event(done)
+        with torch.cuda.stream(s_out):
+            dwh.copy_(wl.dw, non_blocking=True)
+        main.wait_stream(s_out)
+        main.wait_stream(s_in)
+        main.wait_stream(s_cmp)
+
     times = []
     for i in range(steps + 3):
         binding.conv_l2_flush(flush_buf)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        wl.x.copy_(xh, non_blocking=True)
-        wl.w.copy_(wh, non_blocking=True)
-        wl.dy.copy_(dyh, non_blocking=True)
-        for o in OPS:
-            wl.op(o)
-        yh.copy_(wl.y, non_blocking=True)
-        dxh.copy_(wl.dx, non_blocking=True)
-        dwh.copy_(wl.dw, non_blocking=True)
-        b.record(stream)
+        a.record(main)
+        step()
+        b.record(main)
         b.synchronize()
         if i >= 3:
             times.append(a.elapsed_time(b))
@@ -448,7 +524,8 @@ def e2e(wl, flush_buf, steps):
     esz = wl.x.element_size()
     return {"value": 3 * wl.flops / (ms * 1e-3) / 1e9, "unit": "GFLOP/s", "ms_per_step": ms,
             "h2d_bytes_per_step": (wl.x.numel() + wl.w.numel() + wl.dy.numel()) * esz,
-            "d2h_bytes_per_step": (wl.y.numel() + wl.dx.numel() + wl.dw.numel()) * esz}
+            "d2h_bytes_per_step": (wl.y.numel() + wl.dx.numel() + wl.dw.numel()) * esz,
+            "overlap": f"{chunks} sample ranges; copy-in, compute and copy-out on three streams"}
 
 
 _SIDE = []
@@ -687,12 +764,23 @@ def run_ours(args):
     roofline = roofline_of(wl, dom, op_ms[dom], sms, sm_mhz, peaks)
     roofline["kernel"] = f"{dom} ({plan['algo_name']}, {plan['launches']} launch(es))"
     roofline["traffic"] = read_traffic(f"{dom}:{args.layer}:{args.dtype}:B{args.batch}")
+    roofline["traffic_note"] = ("dram__bytes_read.sum + dram__bytes_write.sum per call (sum over its launches) from "
+                                "one ncu capture of the same kernel source, L2 flushed before the step; output "
+                                "lines still dirty in L2 when the kernel ends are not in dram__bytes_write, so "
+                                "the figure is mostly reads; null when the kernel source changed since")
     ops = {}
     for o in OPS:
         r = roofline_of(wl, o, op_ms[o], sms, sm_mhz, peaks)
         ops[o] = {"us": op_ms[o] * 1e3, "gflops": wl.flops / (op_ms[o] * 1e-3) / 1e9,
                   "algo": wl.plans[o]["algo_name"], "launches": wl.plans[o]["launches"],
                   "bound": r["bound"], "frac": r["frac"], "roofline_us": r["roofline_us"]}
+    # The no-workspace entry points (weights formatted inside the kernels), same workload, cold L2.
+    plain = {}
+    if getattr(wl, "graphs", None):
+        for o, name in (("fwd", "fwd_plain"), ("dgrad", "dgrad_plain")):
+            t_ms = time_graph(wl.graphs[name], flush_buf, 50, 5)
+            plain[o] = {"us": t_ms * 1e3, "gflops": wl.flops / (t_ms * 1e-3) / 1e9,
+                        "launches": wl.plans[name]["launches"]}
     pr = PR522_US.get((args.layer, args.dtype))
     pr_gflops = 3 * wl.flops / ((pr[0] + pr[1]) * 1e-6) / 1e9 if (pr and args.batch == 1024) else None
     line = {
@@ -702,10 +790,12 @@ def run_ours(args):
         "dtype": args.dtype, "data": "synthetic",
         "config": dict(workload_config(args.layer, args.dtype, args.batch),
                        l2="flushed (512 MiB write) between timed steps, outside the timed region",
+                       calls="conv_fwd_ws, conv_bwd_data_ws (caller-owned workspaces), conv_bwd_filter",
                        launch=("each operation replayed from a captured CUDA graph" if not args.no_graphs
                                else "eager launches"),
                        algo=args.algo),
         "ops": ops,
+        "ops_no_workspace": plain,
         "roofline": roofline,
         "gpu_launches": wl.launches * args.steps,
         "clocks": clocks,

@@ -22,7 +22,7 @@ from . import build as _build
 
 F32, BF16 = 0, 1
 ALGO_AUTO, ALGO_DIRECT, ALGO_FFMA, ALGO_TC = 0, 1, 2, 3
-OP_FWD, OP_BWD_DATA, OP_BWD_FILTER, OP_BWD_BIAS = 0, 1, 2, 3
+OP_FWD, OP_BWD_DATA, OP_BWD_FILTER, OP_BWD_BIAS, OP_FWD_WS, OP_BWD_DATA_WS = 0, 1, 2, 3, 4, 5
 ALGO_NAMES = {0: "auto", 1: "direct", 2: "ffma", 3: "tc"}
 
 _DT = {torch.float32: F32, torch.bfloat16: BF16}
@@ -52,8 +52,9 @@ class PlanInfo(ctypes.Structure):
 EXPORTS = ["conv_fwd", "conv_bwd_data", "conv_bwd_filter_workspace_size", "conv_bwd_filter",
            "conv_status_string", "conv_out_dims", "conv_query", "conv_set_algo",
            "conv_fastdivmod_check", "conv_l2_flush", "conv_version", "conv_bwd_filter_noalloc",
-           "conv_device_status", "conv_release_scratch", "conv_fwd_bias", "conv_bwd_bias",
-           "conv_wait_selftest", "conv_query_for_device"]
+           "conv_device_status", "conv_fwd_bias", "conv_bwd_bias",
+           "conv_wait_selftest", "conv_query_for_device", "conv_fwd_workspace_size", "conv_fwd_ws",
+           "conv_bwd_data_workspace_size", "conv_bwd_data_ws"]
 STATUS_WAIT_SELFTEST = 1 << 30
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -90,11 +91,16 @@ def lib():
         L.conv_version.restype = ctypes.c_char_p
         L.conv_bwd_filter_noalloc.argtypes = [dp, vp, vp, vp, vp, vp]
         L.conv_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
-        L.conv_release_scratch.argtypes = []
         L.conv_fwd_bias.argtypes = [dp, vp, vp, vp, vp, vp]
         L.conv_bwd_bias.argtypes = [dp, vp, vp, vp, vp]
         L.conv_wait_selftest.argtypes = [ctypes.c_uint32, vp]
         L.conv_query_for_device.argtypes = [ctypes.c_int, dp] + [ctypes.c_int] * 4 + [ctypes.POINTER(PlanInfo)]
+        L.conv_fwd_workspace_size.argtypes = [dp]
+        L.conv_fwd_workspace_size.restype = sz
+        L.conv_fwd_ws.argtypes = [dp, vp, vp, vp, vp, vp, sz, vp]
+        L.conv_bwd_data_workspace_size.argtypes = [dp]
+        L.conv_bwd_data_workspace_size.restype = sz
+        L.conv_bwd_data_ws.argtypes = [dp, vp, vp, vp, vp, vp, sz, vp]
         _lib = L
         return L
 
@@ -150,6 +156,28 @@ def conv_bwd_bias(desc: ConvDesc, dy, y, db, stream=None) -> None:
 def conv_bwd_data(desc: ConvDesc, dy, w, y, dx, stream=None) -> None:
     _check(lib().conv_bwd_data(ctypes.byref(desc), _ptr(dy), _ptr(w), _ptr(y), _ptr(dx), _stream(stream)),
            "conv_bwd_data")
+
+
+def conv_fwd_workspace_size(desc: ConvDesc) -> int:
+    return int(lib().conv_fwd_workspace_size(ctypes.byref(desc)))
+
+
+def conv_fwd_ws(desc: ConvDesc, x, w, bias, y, workspace, stream=None) -> None:
+    """The forward with a caller-provided workspace (bias may be None)."""
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().conv_fwd_ws(ctypes.byref(desc), _ptr(x), _ptr(w), _ptr(bias), _ptr(y), _ptr(workspace), nbytes,
+                             _stream(stream)), "conv_fwd_ws")
+
+
+def conv_bwd_data_workspace_size(desc: ConvDesc) -> int:
+    return int(lib().conv_bwd_data_workspace_size(ctypes.byref(desc)))
+
+
+def conv_bwd_data_ws(desc: ConvDesc, dy, w, y, dx, workspace, stream=None) -> None:
+    """d_input with a caller-provided workspace."""
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().conv_bwd_data_ws(ctypes.byref(desc), _ptr(dy), _ptr(w), _ptr(y), _ptr(dx), _ptr(workspace),
+                                  nbytes, _stream(stream)), "conv_bwd_data_ws")
 
 
 def conv_bwd_filter_workspace_size(desc: ConvDesc) -> int:
@@ -216,10 +244,6 @@ def conv_wait_selftest(max_sleeps: int, stream=None) -> None:
     """Run the bounded-wait self-test kernel (see include/conv.h); its timeout sets
     STATUS_WAIT_SELFTEST in conv_device_status()."""
     _check(lib().conv_wait_selftest(int(max_sleeps), _stream(stream)), "conv_wait_selftest")
-
-
-def conv_release_scratch() -> None:
-    _check(lib().conv_release_scratch(), "conv_release_scratch")
 
 
 def conv_version() -> str:

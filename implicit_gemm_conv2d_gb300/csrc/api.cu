@@ -85,58 +85,6 @@ int cuda_status(cudaError_t e)
     return CONV_ERR_CUDA;
 }
 
-// Packed-weight scratch, one buffer of kScratchBytes per (device, stream), allocated on
-// the first tensor-core forward / d_input call on that stream.  Work on one stream is
-// ordered, so a buffer is never used by two calls at once.
-namespace {
-struct ScratchEntry {
-    int device;
-    cudaStream_t stream;
-    void* ptr;
-};
-std::mutex g_scratch_mu;
-ScratchEntry g_scratch[256];
-int g_nscratch = 0;
-}  // namespace
-
-void* stream_scratch(int device, cudaStream_t stream)
-{
-    std::lock_guard<std::mutex> lk(g_scratch_mu);
-    for (int i = 0; i < g_nscratch; ++i)
-        if (g_scratch[i].device == device && g_scratch[i].stream == stream) return g_scratch[i].ptr;
-    if (g_nscratch >= 256) return nullptr;
-    // No allocation inside a stream capture (it would invalidate the capture): the
-    // first call on a stream has to come before capturing on it.
-    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
-        cudaGetLastError();
-        return nullptr;
-    }
-    void* p = nullptr;
-    if (cudaMalloc(&p, kScratchBytes) != cudaSuccess) {
-        cudaGetLastError();
-        return nullptr;
-    }
-    g_scratch[g_nscratch++] = ScratchEntry{device, stream, p};
-    return p;
-}
-
-int release_scratch()
-{
-    std::lock_guard<std::mutex> lk(g_scratch_mu);
-    int rc = CONV_OK;
-    for (int i = 0; i < g_nscratch; ++i) {
-        int cur = 0;
-        cudaGetDevice(&cur);
-        cudaSetDevice(g_scratch[i].device);
-        if (cudaDeviceSynchronize() != cudaSuccess || cudaFree(g_scratch[i].ptr) != cudaSuccess) rc = CONV_ERR_CUDA;
-        cudaSetDevice(cur);
-    }
-    g_nscratch = 0;
-    cudaGetLastError();
-    return rc;
-}
-
 }  // namespace igc
 
 namespace {
@@ -144,12 +92,13 @@ namespace {
 std::atomic<int> g_force[4] = {ALGO_AUTO, ALGO_AUTO, ALGO_AUTO, ALGO_AUTO};
 
 // ---- plan selection -------------------------------------------------------------------
-int choose_fwd(const ConvParams& p, int dt, const DevInfo& d, Plan& pl)
+// `packed`: the plan of the workspace-taking entry point (conv_fwd_ws / conv_bwd_data_ws).
+int choose_fwd(const ConvParams& p, int dt, const DevInfo& d, bool packed, Plan& pl)
 {
     const int force = g_force[CONV_OP_FWD].load();
     if (force == ALGO_DIRECT) { pl = plan_fwd_direct(p, d); return CONV_OK; }
     if (force == ALGO_TC || force == ALGO_AUTO) {
-        if (tc_fwd_ok(p, dt, d)) { pl = plan_fwd_tc(p, dt, d); return CONV_OK; }
+        if (tc_fwd_ok(p, dt, d, packed)) { pl = plan_fwd_tc(p, dt, d, packed); return CONV_OK; }
         if (force == ALGO_TC) return CONV_ERR_UNSUPPORTED;
     }
     if (ffma_fwd_ok(p, d)) { pl = plan_fwd_ffma(p, d); return CONV_OK; }
@@ -158,12 +107,12 @@ int choose_fwd(const ConvParams& p, int dt, const DevInfo& d, Plan& pl)
     return CONV_OK;
 }
 
-int choose_dgrad(const ConvParams& p, int dt, const DevInfo& d, Plan& pl)
+int choose_dgrad(const ConvParams& p, int dt, const DevInfo& d, bool packed, Plan& pl)
 {
     const int force = g_force[CONV_OP_BWD_DATA].load();
     if (force == ALGO_DIRECT) { pl = plan_dgrad_direct(p, d); return CONV_OK; }
     if (force == ALGO_TC || force == ALGO_AUTO) {
-        if (tc_dgrad_ok(p, dt, d)) { pl = plan_dgrad_tc(p, dt, d); return CONV_OK; }
+        if (tc_dgrad_ok(p, dt, d, packed)) { pl = plan_dgrad_tc(p, dt, d, packed); return CONV_OK; }
         if (force == ALGO_TC) return CONV_ERR_UNSUPPORTED;
     }
     if (ffma_dgrad_ok(p, d)) { pl = plan_dgrad_ffma(p, d); return CONV_OK; }
@@ -195,31 +144,71 @@ int choose_bgrad(const ConvParams& p, int dt, const DevInfo& d, Plan& pl)
 int choose(int op, const ConvParams& p, int dt, const DevInfo& d, Plan& pl)
 {
     switch (op) {
-    case CONV_OP_FWD: return choose_fwd(p, dt, d, pl);
-    case CONV_OP_BWD_DATA: return choose_dgrad(p, dt, d, pl);
+    case CONV_OP_FWD: return choose_fwd(p, dt, d, false, pl);
+    case CONV_OP_BWD_DATA: return choose_dgrad(p, dt, d, false, pl);
     case CONV_OP_BWD_FILTER: return choose_wgrad(p, dt, d, pl);
     case CONV_OP_BWD_BIAS: return choose_bgrad(p, dt, d, pl);
+    case CONV_OP_FWD_WS: return choose_fwd(p, dt, d, true, pl);
+    case CONV_OP_BWD_DATA_WS: return choose_dgrad(p, dt, d, true, pl);
     default: return CONV_ERR_UNSUPPORTED;
     }
 }
 
-int fwd_impl(const conv_desc_t* desc, const void* x, const void* w, const void* bias, void* y,
-             conv_stream_t stream)
+// The forward, with (ws != nullptr: the workspace path) or without a workspace.
+int fwd_impl(const conv_desc_t* desc, const void* x, const void* w, const void* bias, void* y, void* ws,
+             size_t ws_bytes, bool with_ws, conv_stream_t stream)
 {
     ConvParams p;
     int rc = make_params(desc, p);
     if (rc != CONV_OK) return rc;
     if (p.B == 0) return CONV_OK;
     if (!x || !w || !y) return CONV_ERR_NULL;
-    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (bias && !aligned16(bias))) return CONV_ERR_ALIGN;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (bias && !aligned16(bias)) || (ws && !aligned16(ws)))
+        return CONV_ERR_ALIGN;
     DevInfo d;
     if ((rc = device_info(d)) != CONV_OK) return rc;
     Plan pl;
-    if ((rc = choose_fwd(p, desc->dtype, d, pl)) != CONV_OK) return rc;
+    if ((rc = choose_fwd(p, desc->dtype, d, with_ws, pl)) != CONV_OK) return rc;
+    if (pl.workspace > 0 && (!ws || ws_bytes < pl.workspace)) return CONV_ERR_WORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (pl.algo == ALGO_DIRECT) return cuda_status(run_fwd_direct(pl, p, desc->dtype, x, w, bias, y, s));
-    if (pl.algo == ALGO_TC) return cuda_status(run_fwd_tc(pl, p, desc->dtype, x, w, bias, y, s));
+    if (pl.algo == ALGO_TC)
+        return cuda_status(run_fwd_tc(pl, p, desc->dtype, x, w, bias, y, pl.workspace > 0 ? ws : nullptr, s));
     return cuda_status(run_fwd_ffma(pl, p, desc->dtype, x, w, bias, y, s));
+}
+
+int dgrad_impl(const conv_desc_t* desc, const void* dy, const void* w, const void* y, void* dx, void* ws,
+               size_t ws_bytes, bool with_ws, conv_stream_t stream)
+{
+    ConvParams p;
+    int rc = make_params(desc, p);
+    if (rc != CONV_OK) return rc;
+    if (p.B == 0) return CONV_OK;
+    if (!dy || !w || !dx || (p.relu && !y)) return CONV_ERR_NULL;
+    if (!aligned16(dy) || !aligned16(w) || !aligned16(dx) || (p.relu && !aligned16(y)) || (ws && !aligned16(ws)))
+        return CONV_ERR_ALIGN;
+    DevInfo d;
+    if ((rc = device_info(d)) != CONV_OK) return rc;
+    Plan pl;
+    if ((rc = choose_dgrad(p, desc->dtype, d, with_ws, pl)) != CONV_OK) return rc;
+    if (pl.workspace > 0 && (!ws || ws_bytes < pl.workspace)) return CONV_ERR_WORKSPACE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (pl.algo == ALGO_DIRECT) return cuda_status(run_dgrad_direct(pl, p, desc->dtype, dy, w, y, dx, s));
+    if (pl.algo == ALGO_TC)
+        return cuda_status(run_dgrad_tc(pl, p, desc->dtype, dy, w, y, dx, pl.workspace > 0 ? ws : nullptr, s));
+    return cuda_status(run_dgrad_ffma(pl, p, desc->dtype, dy, w, y, dx, s));
+}
+
+// Workspace bytes of an operation's plan on the current device (0: none, or invalid).
+size_t plan_workspace(int op, const conv_desc_t* desc)
+{
+    ConvParams p;
+    if (make_params(desc, p) != CONV_OK) return 0;
+    DevInfo d;
+    if (device_info(d) != CONV_OK) return 0;
+    Plan pl;
+    if (choose(op, p, desc->dtype, d, pl) != CONV_OK) return 0;
+    return pl.workspace;
 }
 
 }  // namespace
@@ -255,8 +244,11 @@ int conv_out_dims(const conv_desc_t* desc, int32_t* OH, int32_t* OW)
 
 int conv_set_algo(int op, int algo)
 {
-    if (op < 0 || op > 3 || algo < ALGO_AUTO || algo > ALGO_TC) return CONV_ERR_UNSUPPORTED;
+    if (op < 0 || op > 5 || algo < ALGO_AUTO || algo > ALGO_TC) return CONV_ERR_UNSUPPORTED;
     if (op == CONV_OP_BWD_BIAS && algo != ALGO_AUTO && algo != ALGO_DIRECT) return CONV_ERR_UNSUPPORTED;
+    // the workspace-taking entry points share the choice of their operation
+    if (op == CONV_OP_FWD_WS) op = CONV_OP_FWD;
+    if (op == CONV_OP_BWD_DATA_WS) op = CONV_OP_BWD_DATA;
     g_force[op].store(algo);
     return CONV_OK;
 }
@@ -267,7 +259,7 @@ static int query_on(int op, const conv_desc_t* desc, const DevInfo& d, conv_plan
     int rc = make_params(desc, p);
     if (rc != CONV_OK) return rc;
     if (!info) return CONV_ERR_NULL;
-    if (op < 0 || op > 3) return CONV_ERR_UNSUPPORTED;
+    if (op < 0 || op > 5) return CONV_ERR_UNSUPPORTED;
     Plan pl;
     if ((rc = choose(op, p, desc->dtype, d, pl)) != CONV_OK) return rc;
     info->algo = pl.algo;
@@ -286,7 +278,7 @@ int conv_query(int op, const conv_desc_t* desc, conv_plan_info_t* info)
     int rc = make_params(desc, p);
     if (rc != CONV_OK) return rc;
     if (!info) return CONV_ERR_NULL;
-    if (op < 0 || op > 3) return CONV_ERR_UNSUPPORTED;
+    if (op < 0 || op > 5) return CONV_ERR_UNSUPPORTED;
     DevInfo d;
     if ((rc = device_info(d)) != CONV_OK) return rc;
     return query_on(op, desc, d, info);
@@ -307,7 +299,7 @@ int conv_query_for_device(int op, const conv_desc_t* desc, int sms, int smem_opt
 
 int conv_fwd(const conv_desc_t* desc, const void* x, const void* w, void* y, conv_stream_t stream)
 {
-    return fwd_impl(desc, x, w, nullptr, y, stream);
+    return fwd_impl(desc, x, w, nullptr, y, nullptr, 0, false, stream);
 }
 
 int conv_fwd_bias(const conv_desc_t* desc, const void* x, const void* w, const void* bias, void* y,
@@ -317,7 +309,23 @@ int conv_fwd_bias(const conv_desc_t* desc, const void* x, const void* w, const v
     const int rc = make_params(desc, p);
     if (rc != CONV_OK) return rc;
     if (p.B > 0 && !bias) return CONV_ERR_NULL;
-    return fwd_impl(desc, x, w, bias, y, stream);
+    return fwd_impl(desc, x, w, bias, y, nullptr, 0, false, stream);
+}
+
+size_t conv_fwd_workspace_size(const conv_desc_t* desc) { return plan_workspace(CONV_OP_FWD_WS, desc); }
+
+int conv_fwd_ws(const conv_desc_t* desc, const void* x, const void* w, const void* bias, void* y, void* workspace,
+                size_t workspace_bytes, conv_stream_t stream)
+{
+    return fwd_impl(desc, x, w, bias, y, workspace, workspace_bytes, true, stream);
+}
+
+size_t conv_bwd_data_workspace_size(const conv_desc_t* desc) { return plan_workspace(CONV_OP_BWD_DATA_WS, desc); }
+
+int conv_bwd_data_ws(const conv_desc_t* desc, const void* dy, const void* w, const void* y, void* dx,
+                     void* workspace, size_t workspace_bytes, conv_stream_t stream)
+{
+    return dgrad_impl(desc, dy, w, y, dx, workspace, workspace_bytes, true, stream);
 }
 
 int conv_bwd_bias(const conv_desc_t* desc, const void* dy, const void* y, void* db, conv_stream_t stream)
@@ -338,21 +346,7 @@ int conv_bwd_bias(const conv_desc_t* desc, const void* dy, const void* y, void* 
 int conv_bwd_data(const conv_desc_t* desc, const void* dy, const void* w, const void* y, void* dx,
                   conv_stream_t stream)
 {
-    ConvParams p;
-    int rc = make_params(desc, p);
-    if (rc != CONV_OK) return rc;
-    if (p.B == 0) return CONV_OK;
-    if (!dy || !w || !dx || (p.relu && !y)) return CONV_ERR_NULL;
-    if (!aligned16(dy) || !aligned16(w) || !aligned16(dx) || (p.relu && !aligned16(y)))
-        return CONV_ERR_ALIGN;
-    DevInfo d;
-    if ((rc = device_info(d)) != CONV_OK) return rc;
-    Plan pl;
-    if ((rc = choose_dgrad(p, desc->dtype, d, pl)) != CONV_OK) return rc;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (pl.algo == ALGO_DIRECT) return cuda_status(run_dgrad_direct(pl, p, desc->dtype, dy, w, y, dx, s));
-    if (pl.algo == ALGO_TC) return cuda_status(run_dgrad_tc(pl, p, desc->dtype, dy, w, y, dx, d.sms, s));
-    return cuda_status(run_dgrad_ffma(pl, p, desc->dtype, dy, w, y, dx, s));
+    return dgrad_impl(desc, dy, w, y, dx, nullptr, 0, false, stream);
 }
 
 size_t conv_bwd_filter_workspace_size(const conv_desc_t* desc)
@@ -420,8 +414,6 @@ int conv_wait_selftest(uint32_t max_sleeps, conv_stream_t stream)
     if (max_sleeps < 1 || max_sleeps > 1000000u) return CONV_ERR_UNSUPPORTED;
     return cuda_status(run_wait_selftest(max_sleeps, reinterpret_cast<cudaStream_t>(stream)));
 }
-
-int conv_release_scratch(void) { return release_scratch(); }
 
 int conv_l2_flush(void* buf, size_t bytes, conv_stream_t stream)
 {

@@ -36,11 +36,8 @@ int make_params(const conv_desc_t* d, ConvParams& p);  // validation, no CUDA ca
 bool aligned16(const void* p);
 int cuda_status(cudaError_t e);                     // cudaSuccess -> CONV_OK, else CONV_ERR_CUDA
 
-// Library-held scratch for packed weights and the forward's / bias gradient's partial sums:
-// one buffer per (device, stream), allocated on first use; nullptr if it cannot be allocated.
-constexpr size_t kScratchBytes = size_t(48) << 20;
-void* stream_scratch(int device, cudaStream_t stream);
-int release_scratch();
+// Largest thread-block cluster the kernels use (the portable limit).
+constexpr int kMaxCluster = 8;
 
 // ---- FFMA and direct families (kernels_ffma.cu) ------------------------------------
 bool ffma_fwd_ok(const ConvParams& p, const DevInfo& d);
@@ -111,19 +108,52 @@ cudaError_t launch_overlapped(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
+// Launch `Kern` with a 1-D thread-block cluster of `cluster` CTAs (1 = none; the grid must be a
+// multiple of it), and optionally as a programmatic dependent launch (see launch_overlapped; the
+// kernel then executes griddepcontrol.wait before its first global-memory access).
+template <class... KArgs, class... Args>
+cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, int cluster,
+                      bool pdl, Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = unsigned(cluster);
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 // ---- tcgen05 tensor-core family (kernels_tc.cu) -------------------------------------
-bool tc_fwd_ok(const ConvParams& p, int dt, const DevInfo& d);
-Plan plan_fwd_tc(const ConvParams& p, int dt, const DevInfo& d);
+// `packed` / `ws`: the workspace path (weights packed once per call into the caller's
+// workspace, bulk-copied by the main kernel); else the main kernel formats them itself.
+bool tc_fwd_ok(const ConvParams& p, int dt, const DevInfo& d, bool packed);
+Plan plan_fwd_tc(const ConvParams& p, int dt, const DevInfo& d, bool packed);
 cudaError_t run_fwd_tc(const Plan&, const ConvParams&, int dt, const void* x, const void* w,
-                       const void* bias, void* y, cudaStream_t s);
+                       const void* bias, void* y, void* ws, cudaStream_t s);
 bool tc_wgrad_ok(const ConvParams& p, int dt, const DevInfo& d);
 Plan plan_wgrad_tc(const ConvParams& p, int dt, const DevInfo& d);
 cudaError_t run_wgrad_tc(const Plan&, const ConvParams&, int dt, const void* x, const void* dy,
                          const void* y, void* dw, void* ws, int sms, cudaStream_t s);
-bool tc_dgrad_ok(const ConvParams& p, int dt, const DevInfo& d);
-Plan plan_dgrad_tc(const ConvParams& p, int dt, const DevInfo& d);
+bool tc_dgrad_ok(const ConvParams& p, int dt, const DevInfo& d, bool packed);
+Plan plan_dgrad_tc(const ConvParams& p, int dt, const DevInfo& d, bool packed);
 cudaError_t run_dgrad_tc(const Plan&, const ConvParams&, int dt, const void* dy, const void* w,
-                         const void* y, void* dx, int sms, cudaStream_t s);
+                         const void* y, void* dx, void* ws, cudaStream_t s);
 // ---- bias gradient (kernels_bias.cu) ------------------------------------------------
 // `direct`: the one-warp-per-channel kernel (any shape); else the column-sum kernel and its
 // reduce, when the shape allows.

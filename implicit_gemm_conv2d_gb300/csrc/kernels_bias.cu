@@ -6,33 +6,29 @@
 // It is a memory-bound reduction: dy is B rows of OC*P contiguous values (P = OH*OW), read
 // once (with y beside it under relu) and reduced to OC numbers.
 //
-// Column-sum kernel: each CTA owns a window of whole channels (all OC unless a row is longer
-// than the shared-memory window) and a contiguous range of samples.  Its threads read the
-// rows with coalesced 16-byte loads, each thread summing its own columns (oc, oh, ow) down
-// its rows in ascending b; a narrow window (few columns) gets several row lanes, thread lane r
-// taking rows r, r + R, ...  Then each channel's P columns are added in ascending (oh, ow),
-// each over the row lanes in ascending order, into one fp32 partial per (range, channel),
-// kept in the per-stream scratch buffer.
-// Reduce kernel: 32 warps per 32 channels; warp w adds ranges w, w + 32, ... in ascending
-// order, then one warp adds the 32 warp sums in ascending order and rounds once.
+// One kernel, no global scratch.  CTA (w, r) owns a window of ocw whole channels -- the
+// window's OCW*P values of a sample are contiguous in dy -- and the r-th of R contiguous
+// sample ranges; the R CTAs of a window form one thread-block cluster.  Threads read the
+// window's rows with coalesced 16-byte loads (8 rows in flight, 4 with the mask), each
+// summing its own columns (oc, oh, ow) down its rows in ascending b; a narrow window gets
+// several row lanes, thread lane q taking rows q, q + Q, ...  Then each channel's P columns
+// are added in ascending (oh, ow), each over the row lanes in ascending order, into one fp32
+// sum per channel in shared memory; after a cluster barrier the rank-0 CTA adds the R
+// ranges' sums in ascending rank order through distributed shared memory and rounds once.
 // No atomics: the result depends only on the plan (shape and SM count).
 #include <algorithm>
 
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace igc {
 
 namespace {
 
-constexpr int BG_MAXT = 512;        // threads of a column-sum CTA
+constexpr int BG_THREADS = 256;     // threads of a CTA (at most)
 constexpr int BG_WIN = 12288;       // fp32 column sums in a CTA's shared-memory window (48 KB)
-constexpr int BG_REGS = 64;         // registers per thread the column-sum kernel is built for
-constexpr int BG_MINROWS = 4;       // rows per thread of a sample range, at least (when B allows)
-constexpr int BG_MAXSPLIT = 1024;   // sample ranges, at most (the reduce adds 32 per warp lane)
-constexpr int BG_RED_WARPS = 32;    // warps of a reduce CTA (one CTA per 32 channels)
-
-__device__ __forceinline__ void dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+constexpr int BG_MINROWS = 16;      // rows per sample range, at least (when B allows)
+constexpr int BG_MINBYTES = 64;     // bytes of a window's row, at least (when OC allows)
 
 // V consecutive elements widened to fp32: one 16-byte load for V * sizeof(T) == 16.
 template <typename T, int V> struct VecLd;
@@ -59,33 +55,38 @@ template <> struct VecLd<__nv_bfloat16, 8> {
     }
 };
 
+// CTA blockIdx.x = window * R + range (cluster of R along x).  Thread (q, c) = (threadIdx.x /
+// lanes_c, threadIdx.x % lanes_c): column groups c, c + lanes_c, ... of the window, rows
+// b_lo + q, b_lo + q + Q, ... of the range (Q = blockDim.x / lanes_c row lanes).
 template <typename T, bool RELU, int V>
-__global__ void __launch_bounds__(BG_MAXT, 65536 / (BG_MAXT * BG_REGS))
-bias_colsum_kernel(const ConvParams p, const T* __restrict__ dy, const T* __restrict__ y,
-                   float* __restrict__ part, int nsplit, int ocw, int lanes_c)
+__global__ void __launch_bounds__(BG_THREADS)
+bias_grad_kernel(const ConvParams p, const T* __restrict__ dy, const T* __restrict__ y, T* __restrict__ db,
+                 int ocw, int R, int lanes_c)
 {
-    // Thread (r, c) = (threadIdx.x / lanes_c, threadIdx.x % lanes_c): column groups c, c + lanes_c, ...
-    // of the window, rows b_lo + r, b_lo + r + R, ... of the range (R = blockDim.x / lanes_c).
-    extern __shared__ float colsum[];  // [R][ocw * P] column sums
-    const int R = blockDim.x / lanes_c, r = threadIdx.x / lanes_c, c = threadIdx.x % lanes_c;
-    const int oc0 = blockIdx.x * ocw;
-    const int noc = min(ocw, p.OC - oc0);
+    extern __shared__ float sm[];  // [Q][ocw * P] column sums, then [ocw] channel sums
+    const int Q = blockDim.x / lanes_c, q = threadIdx.x / lanes_c, c = threadIdx.x % lanes_c;
     const int wcols = ocw * p.P;
-    const int c0 = oc0 * p.P, ncg = noc * p.P / V;  // window columns [c0, c0 + noc*P), V per group
-    const int s = blockIdx.y;
-    const int b_lo = int(int64_t(p.B) * s / nsplit), b_hi = int(int64_t(p.B) * (s + 1) / nsplit);
-    const size_t rstep = size_t(R) * p.OCP;
+    float* colsum = sm;
+    float* csum = sm + Q * wcols;
+    const int win = blockIdx.x / R;
+    const int rank = R > 1 ? int(tc::cluster_rank()) : 0;
+    const int oc0 = win * ocw;
+    const int noc = min(ocw, p.OC - oc0);
+    const int ncg = noc * p.P / V;
+    const int b_lo = int(int64_t(p.B) * rank / R), b_hi = int(int64_t(p.B) * (rank + 1) / R);
+    const size_t rstep = size_t(Q) * p.OCP;
+    tc::grid_dep_wait();  // the previous kernel on the stream may still be writing dy / y
 #pragma unroll 1
     for (int cg = c; cg < ncg; cg += lanes_c) {
         float acc[V];
 #pragma unroll
         for (int e = 0; e < V; ++e) acc[e] = 0.f;
-        const size_t col = size_t(c0) + size_t(cg) * V;
-        int b = b_lo + r;
-        // U rows' loads in flight (eight 16-byte loads), added in ascending b.
+        const size_t col = size_t(oc0) * p.P + size_t(cg) * V;
+        int b = b_lo + q;
+        // U rows' loads in flight, added in ascending b.
         constexpr int U = RELU ? 4 : 8;
 #pragma unroll 1
-        for (; b + (U - 1) * R < b_hi; b += U * R) {
+        for (; b + (U - 1) * Q < b_hi; b += U * Q) {
             float v[U][V], m[U][V];
             const size_t off0 = size_t(b) * p.OCP + col;
 #pragma unroll
@@ -98,7 +99,7 @@ bias_colsum_kernel(const ConvParams p, const T* __restrict__ dy, const T* __rest
 #pragma unroll
                 for (int e = 0; e < V; ++e) acc[e] += (!RELU || m[u][e] > 0.f) ? v[u][e] : 0.f;
         }
-        for (; b < b_hi; b += R) {
+        for (; b < b_hi; b += Q) {
             float v[V], m[V];
             const size_t off = size_t(b) * p.OCP + col;
             VecLd<T, V>::ld(dy + off, v);
@@ -107,50 +108,32 @@ bias_colsum_kernel(const ConvParams p, const T* __restrict__ dy, const T* __rest
             for (int e = 0; e < V; ++e) acc[e] += (!RELU || m[e] > 0.f) ? v[e] : 0.f;
         }
 #pragma unroll
-        for (int e = 0; e < V; ++e) colsum[r * wcols + cg * V + e] = acc[e];
+        for (int e = 0; e < V; ++e) colsum[q * wcols + cg * V + e] = acc[e];
     }
     __syncthreads();
     // Channel j of the window: its P columns in ascending (oh, ow), each over the row lanes
-    // in ascending r.
+    // in ascending q.
     for (int j = threadIdx.x; j < noc; j += blockDim.x) {
         float t = 0.f;
-        for (int q = 0; q < p.P; ++q)
-            for (int rr = 0; rr < R; ++rr) t += colsum[rr * wcols + j * p.P + q];
-        part[size_t(s) * p.OC + oc0 + j] = t;
+        for (int pq = 0; pq < p.P; ++pq)
+            for (int qq = 0; qq < Q; ++qq) t += colsum[qq * wcols + j * p.P + pq];
+        csum[j] = t;
     }
-    dep_launch();
-}
-
-// db[oc] = sum of the nsplit partials part[s][oc]; nsplit == 0 writes zeros.
-template <typename T>
-__global__ void __launch_bounds__(BG_RED_WARPS * 32)
-bias_reduce_kernel(const float* __restrict__ part, int nsplit, int OC, T* __restrict__ db)
-{
-    __shared__ float red[BG_RED_WARPS][33];
-    dep_wait();  // the partials come from the kernel launched just before
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int oc = blockIdx.x * 32 + lane;
-    float s = 0.f;
-    if (oc < OC) {
-        // Loads in groups of eight issued together, added in ascending range order.
-        int i = warp;
-        for (; i + 7 * BG_RED_WARPS < nsplit; i += 8 * BG_RED_WARPS) {
-            float v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = __ldcg(part + size_t(i + u * BG_RED_WARPS) * OC + oc);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) s += v[u];
+    tc::grid_dep_launch();
+    if (R == 1) {
+        for (int j = threadIdx.x; j < noc; j += blockDim.x) Elem<T>::st(db + oc0 + j, csum[j]);
+        return;
+    }
+    tc::cluster_sync();  // every range's channel sums are in its CTA's shared memory
+    if (rank == 0) {
+        const uint32_t cs = tc::smem_u32(csum);
+        for (int j = threadIdx.x; j < noc; j += blockDim.x) {
+            float t = 0.f;
+            for (int r = 0; r < R; ++r) t += tc::ld_dsmem_f32(tc::dsmem_addr(cs + uint32_t(4 * j), uint32_t(r)));
+            Elem<T>::st(db + oc0 + j, t);
         }
-        for (; i < nsplit; i += BG_RED_WARPS) s += __ldcg(part + size_t(i) * OC + oc);
     }
-    red[warp][lane] = s;
-    __syncthreads();
-    if (warp == 0 && oc < OC) {
-        float t = 0.f;
-#pragma unroll
-        for (int w = 0; w < BG_RED_WARPS; ++w) t += red[w][lane];
-        Elem<T>::st(db + oc, t);
-    }
+    tc::cluster_sync();  // no CTA leaves while rank 0 still reads its shared memory
 }
 
 // Any shape: one warp per channel; lane l adds the elements l, l + 32, ... of the channel's
@@ -177,18 +160,11 @@ __global__ void bias_direct_kernel(const ConvParams p, const T* __restrict__ dy,
     }
 }
 
-// Plan fields: grid = column-sum CTAs (windows x ranges), block = its threads (column lanes x row
-// lanes), smem = its column sums, splits = sample ranges, variant = (channels per window * 1024 +
-// column lanes) * 16 + V.
-int vec_width(const ConvParams& p, int dt)
-{
-    const int v = dt == DT_F32 ? 4 : 8;  // 16 bytes
-    // One window holding every channel, rows 16-byte aligned (OC*P a multiple of V).
-    return (p.OCP <= BG_WIN && p.OCP % v == 0) ? v : 1;
-}
-
 }  // namespace
 
+// Plan fields: grid = CTAs (windows x ranges), block = threads (column lanes x row lanes),
+// smem = column and channel sums, splits = sample ranges R (the cluster size), variant =
+// (channels per window * 1024 + column lanes) * 16 + V.
 Plan plan_bgrad(const ConvParams& p, int dt, const DevInfo& d, bool direct)
 {
     Plan pl;
@@ -200,31 +176,40 @@ Plan plan_bgrad(const ConvParams& p, int dt, const DevInfo& d, bool direct)
         return pl;
     }
     pl.algo = ALGO_FFMA;
-    const int v = vec_width(p, dt);
-    const int ocw = v > 1 ? p.OC : std::min(p.OC, BG_WIN / p.P);
-    const int wcols = ocw * p.P;
-    const int nwin = ceil_div(p.OC, ocw);
-    const int lanes_c = std::min(BG_MAXT, round_up(wcols / v, 32));
-    // Row lanes: enough for 256 threads when the window is narrow, within the thread and
-    // shared-memory limits.
-    const int lanes_r = std::max(1, std::min({256 / lanes_c, BG_MAXT / lanes_c, BG_WIN / wcols}));
-    pl.block = lanes_c * lanes_r;
-    pl.smem = lanes_r * wcols * 4;
-    if (p.B == 0) {
-        pl.launches = 1;  // the reduce writes zeros
-        pl.splits = 0;
-        pl.grid = 0;
-    } else {
-        // One wave of resident CTAs (threads, registers and shared memory per SM).
-        const int per_sm = std::max(1, std::min({2048 / pl.block, 65536 / (BG_REGS * pl.block),
-                                                 (200 * 1024) / (pl.smem + 1024), 32}));
-        int nsplit = std::max(1, d.sms * per_sm / nwin);
-        nsplit = std::min(nsplit, std::max(1, p.B / (BG_MINROWS * lanes_r)));
-        nsplit = std::min({nsplit, BG_MAXSPLIT, int(kScratchBytes / (sizeof(float) * size_t(p.OC)))});
-        pl.splits = std::max(1, nsplit);
-        pl.grid = nwin * pl.splits;
-        pl.launches = 2;
+    pl.launches = 1;
+    const int es = dt == DT_F32 ? 4 : 2;
+    const int vw = 16 / es;
+    // Sample ranges: the largest power of two up to the cluster limit that leaves every range
+    // BG_MINROWS rows.
+    int R = 1;
+    while (R < kMaxCluster && p.B / (2 * R) >= BG_MINROWS) R *= 2;
+    // Channels per window: enough windows for about two CTAs per SM, a row of at least
+    // BG_MINBYTES, then rounded up so that windows start on 16-byte boundaries (vector loads).
+    const int nwin_target = std::max(1, ceil_div(2 * d.sms, R));
+    int ocw = std::max(1, ceil_div(p.OC, nwin_target));
+    while (ocw < p.OC && ocw * p.P * es < BG_MINBYTES) ++ocw;
+    int v = 1;
+    if (p.OCP % vw == 0) {
+        int o = ocw;
+        while (o <= p.OC && (o * p.P) % vw != 0) ++o;
+        if (o <= p.OC && o * p.P <= BG_WIN) {
+            ocw = o;
+            v = vw;
+        }
     }
+    ocw = std::min(ocw, std::max(1, BG_WIN / p.P));
+    // Column lanes: the window's column groups, rounded up to a power of two below a warp and
+    // to whole warps above (the surplus lanes idle), so that blocks are whole warps.
+    const int ncg = ocw * p.P / v;
+    int lanes_c = 1;
+    while (lanes_c < ncg && lanes_c < 32) lanes_c *= 2;
+    if (ncg > 32) lanes_c = std::min(BG_THREADS, round_up(ncg, 32));
+    int lanes_r = std::max(1, std::min(BG_THREADS / lanes_c, BG_WIN / (ocw * p.P)));
+    while (lanes_r > 1 && (lanes_c * lanes_r) % 32 != 0) --lanes_r;
+    pl.block = lanes_c * lanes_r;
+    pl.smem = (lanes_r * ocw * p.P + ocw) * 4;
+    pl.splits = R;
+    pl.grid = ceil_div(p.OC, ocw) * R;
     pl.variant = (ocw * 1024 + lanes_c) * 16 + v;
     return pl;
 }
@@ -235,7 +220,6 @@ template <typename T>
 cudaError_t bgrad_t(const Plan& pl, const ConvParams& p, const void* dy, const void* y, void* db,
                     cudaStream_t s)
 {
-    cudaError_t e = cudaSuccess;
     if (pl.algo == ALGO_DIRECT) {
         if (p.relu)
             bias_direct_kernel<T, true><<<pl.grid, pl.block, 0, s>>>(p, (const T*)dy, (const T*)y, (T*)db);
@@ -244,30 +228,24 @@ cudaError_t bgrad_t(const Plan& pl, const ConvParams& p, const void* dy, const v
         return cudaGetLastError();
     }
     const int ocw = pl.variant / 16 / 1024, lanes_c = pl.variant / 16 % 1024, v = pl.variant % 16;
-    if (pl.splits > 0) {
-        int dev = 0;
-        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-        float* part = static_cast<float*>(stream_scratch(dev, s));
-        if (!part) return cudaErrorMemoryAllocation;
-        const dim3 grid(ceil_div(p.OC, ocw), pl.splits);
-#define IG_BG_LAUNCH(R, V)                                                                              \
-    bias_colsum_kernel<T, R, V><<<grid, pl.block, pl.smem, s>>>(p, (const T*)dy, (const T*)y, part, pl.splits, ocw, \
-                                                                 lanes_c)
-        constexpr int VW = sizeof(T) == 4 ? 4 : 8;
-        if (p.relu) {
-            if (v == VW) IG_BG_LAUNCH(true, VW);
-            else IG_BG_LAUNCH(true, 1);
-        } else {
-            if (v == VW) IG_BG_LAUNCH(false, VW);
-            else IG_BG_LAUNCH(false, 1);
-        }
-#undef IG_BG_LAUNCH
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        return launch_overlapped(bias_reduce_kernel<T>, dim3(ceil_div(p.OC, 32)), dim3(BG_RED_WARPS * 32), 0, s,
-                                 (const float*)part, pl.splits, p.OC, (T*)db);
+    cudaError_t e = cudaSuccess;
+#define IG_BG_LAUNCH(RL, V)                                                                                 \
+    do {                                                                                                    \
+        e = ensure_smem<bias_grad_kernel<T, RL, V>>(pl.smem);                                               \
+        if (e == cudaSuccess)                                                                               \
+            e = launch_ex(bias_grad_kernel<T, RL, V>, dim3(pl.grid), dim3(pl.block), pl.smem, s, pl.splits, \
+                          true, p, (const T*)dy, (const T*)y, (T*)db, ocw, pl.splits, lanes_c);             \
+    } while (0)
+    constexpr int VW = sizeof(T) == 4 ? 4 : 8;
+    if (p.relu) {
+        if (v == VW) IG_BG_LAUNCH(true, VW);
+        else IG_BG_LAUNCH(true, 1);
+    } else {
+        if (v == VW) IG_BG_LAUNCH(false, VW);
+        else IG_BG_LAUNCH(false, 1);
     }
-    bias_reduce_kernel<T><<<ceil_div(p.OC, 32), BG_RED_WARPS * 32, 0, s>>>(nullptr, 0, p.OC, (T*)db);  // B = 0
-    return cudaGetLastError();
+#undef IG_BG_LAUNCH
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

@@ -84,152 +84,298 @@ __device__ __forceinline__ void report(int* abort_flag, unsigned code)
     atomicOr(&g_tc_status, code);
 }
 
-// Write one unit of 4 fp32 values as tf32 hi and lo parts, or of 8 bf16 values.
-template <typename T, int SWZ>
-__device__ __forceinline__ void put_unit(unsigned char* hi, unsigned char* lo, int r, int c, const float (&v)[8])
-{
-    const uint32_t off = unit_off<SWZ>(r, c);
-    if constexpr (TcTraits<T>::split) {
-        float h[4], l[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            h[i] = to_tf32(v[i]);
-            l[i] = to_tf32(v[i] - h[i]);
-        }
-        st_unit(hi, off, __float_as_uint(h[0]), __float_as_uint(h[1]), __float_as_uint(h[2]), __float_as_uint(h[3]));
-        st_unit(lo, off, __float_as_uint(l[0]), __float_as_uint(l[1]), __float_as_uint(l[2]), __float_as_uint(l[3]));
-    } else {
-        uint32_t q[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(v[2 * i]));
-            const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(v[2 * i + 1]));
-            q[i] = a | (b << 16);
-        }
-        st_unit(hi, off, q[0], q[1], q[2], q[3]);
-    }
-}
-
-// Issue the MMAs of one K-chunk (4 steps of 32 bytes of K) from operand tiles at
-// the given shared addresses (hi parts; the lo parts of a split fp32 operand
-// sit `lo_off` bytes further).
-template <typename T, int SWZ>
-__device__ __forceinline__ void issue_chunk(uint32_t tmem, uint32_t a_addr, uint32_t b_addr, uint32_t a_lo_off,
-                                            uint32_t b_lo_off, uint32_t idesc, bool first)
-{
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint64_t ad = op_desc<SWZ>(a_addr + kstep_off<SWZ>(j));
-        const uint64_t bd = op_desc<SWZ>(b_addr + kstep_off<SWZ>(j));
-        const uint32_t acc = (first && j == 0) ? 0u : 1u;
-        if constexpr (TcTraits<T>::split) {
-            const uint64_t al = op_desc<SWZ>(a_addr + a_lo_off + kstep_off<SWZ>(j));
-            const uint64_t bl = op_desc<SWZ>(b_addr + b_lo_off + kstep_off<SWZ>(j));
-            mma_tf32(tmem, ad, bd, idesc, acc);
-            mma_tf32(tmem, ad, bl, idesc, 1u);
-            mma_tf32(tmem, al, bd, idesc, 1u);
-        } else {
-            mma_f16(tmem, ad, bd, idesc, acc);
-        }
-    }
-}
-
 __device__ __forceinline__ unsigned char* align1024(unsigned char* p)
 {
     return reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// ======================================================================================
-// Weight packing.  Every call of the tensor-core forward / d_input first rewrites w into
-// the exact shared-memory image of the weight operand's K-chunks (rows x 128 bytes,
-// 128-byte swizzled, K-major; fp32 as tf32 hi rows followed by lo rows), so that the
-// main kernel fetches each chunk with one large bulk copy.
-//   forward: tile (ot, kc) holds W[r][kk] = w[ot*OTp + r][kc*KC + kk], OTp rows
-//   d_input: tile (kt, ch) holds W^T[r][kk] = w[ch*KC + kk][k0(kt) + r] (W transposed),
-//            KTp rows, r < CIC*K*K of input-channel chunk kt
-// ======================================================================================
+// Raw bits of one element of w (zero-extended for bf16).
 template <typename T>
-__global__ void pack_fwd_w_kernel(const ConvParams p, const T* __restrict__ w, unsigned char* __restrict__ out,
-                                  int nchunks, int oc_tiles, int OTp)
+__device__ __forceinline__ uint32_t ld_bits(const T* p)
 {
-    grid_dep_launch();  // the implicit GEMM may start its prologue meanwhile
+    if constexpr (sizeof(T) == 4) return __ldg(reinterpret_cast<const unsigned int*>(p));
+    else return __ldg(reinterpret_cast<const unsigned short*>(p));
+}
+
+// The fp32 split of the 3xTF32 products: hi = tf32(v) (round to nearest), lo = v - hi (exact
+// in fp32; the MMA reads its leading tf32 bits).  Every operand of the fp32 path is split so.
+__device__ __forceinline__ void split_tf32(uint32_t bits, uint32_t& hi, uint32_t& lo)
+{
+    const float f = __uint_as_float(bits);
+    const float h = to_tf32(f);
+    hi = __float_as_uint(h);
+    lo = __float_as_uint(f - h);
+}
+
+// ======================================================================================
+// Weight operand stages, formatted inside the kernels from w as the caller passes it
+// (OC x IC*K*K, row-major; 16-byte aligned base): 128-byte rows, 128-byte swizzled, K-major,
+// fp32 as tf32 hi rows followed (lo_off bytes further) by lo rows.  Dedicated weight-formatter
+// warps do it in two steps per stage, one stage apart:
+//   stage_*   each lane issues 16-byte cp.async copies of the aligned blocks that cover the
+//             pieces of w the warp itself will format, into a raw slot of the warp's own
+//             (no register holds the data in flight; copies past OC or past the end of w
+//             are zero-filled); the copies of one stage form one cp.async group;
+//   format_*  after cp.async.wait_group and __syncwarp, the warp reads its raw slot
+//             (conflict-free 32-lane runs), splits fp32 into tf32 hi / lo, and stores the
+//             operand stage; the caller fences the stores for the tensor core and arrives.
+// A warp copies exactly what it formats, so no other warp waits on its copies.
+// ======================================================================================
+constexpr int NWF = 4;      // weight-formatter warps of the forward
+constexpr int DG_NWF = 2;   // weight-formatter warps of d_input (608 threads: up to 96 registers each)
+constexpr int WRAW = 2;     // raw slots per warp: the next stage's copies fly while one is formatted
+constexpr int WRB = 144;    // bytes of a raw row piece: 128 bytes of w plus 16 of alignment slack
+
+// Forward stage: row r = output channel oc0 + r (r < OTp), K = k0 .. k0 + KC - 1 (128 bytes of
+// one row of w).  Warp wf owns rows wf, wf + NWF, ...; its raw slot holds them at WRB-byte
+// strides, each as the 9 aligned blocks covering [&w[oc][k0], +128).
+inline __host__ __device__ int fwd_wraw_warp_bytes(int OTp) { return ((OTp + NWF - 1) / NWF) * WRB; }
+
+template <typename T>
+__device__ __forceinline__ void stage_w_fwd(uint32_t slot, const T* __restrict__ w, const ConvParams& p, int oc0,
+                                            int k0, int OTp, int wf, int lane)
+{
+    const char* wb = reinterpret_cast<const char*>(w);
+    const char* wend = wb + size_t(p.OC) * p.Kred * sizeof(T);
+    const int nrw = (OTp - wf + NWF - 1) / NWF;
+    for (int q = lane; q < nrw * 9; q += 32) {
+        const int i = q / 9, j = q - 9 * (q / 9);
+        const int oc = oc0 + wf + NWF * i;
+        const char* a = wb + (size_t(oc) * p.Kred + k0) * sizeof(T);
+        const char* s = reinterpret_cast<const char*>(reinterpret_cast<uintptr_t>(a) & ~uintptr_t(15)) + 16 * j;
+        const int n = (oc < p.OC && s < wend) ? int(min(ptrdiff_t(16), wend - s)) : 0;
+        cp_async16(slot + uint32_t(i * WRB + 16 * j), n > 0 ? s : wb, uint32_t(n));
+    }
+}
+
+// Lane L stores K value L (+ 32 for bf16) of each of the warp's rows: every read is a
+// 32-lane run of one raw row, every store one 128-byte row of the stage (all banks).  The
+// warp's rows r = wf + NWF*i have r & 7 = wf + 4 (i & 1) and r >> 3 = i >> 1, and their raw
+// pieces start at one of two misalignments (even / odd i), so the loop carries no address
+// arithmetic.  Rows past OC were zero-filled by the copies; K values past Kred (the last,
+// ragged chunk) are zeroed here.
+template <typename T>
+__device__ __forceinline__ void format_w_fwd(uint32_t stage, uint32_t lo_off, uint32_t slot, const ConvParams& p,
+                                             int oc0, int k0, int OTp, int wf, int lane)
+{
     using Tr = TcTraits<T>;
-    const int tile_units = OTp * 8;
-    const size_t total = size_t(oc_tiles) * nchunks * tile_units;
-    const size_t tb = size_t(OTp) * ROWB * (Tr::split ? 2 : 1);
-    for (size_t u = blockIdx.x * size_t(blockDim.x) + threadIdx.x; u < total; u += size_t(gridDim.x) * blockDim.x) {
-        const int within = int(u % tile_units);
-        const size_t t = u / tile_units;
-        const int kc = int(t % nchunks), ot = int(t / nchunks);
-        const int r = within >> 3, c = within & 7;
-        const int oc = ot * OTp + r, k = kc * Tr::KC + c * Tr::E;
-        float v[8];
+    constexpr int EPL = Tr::KC / 32;  // K values per lane and row
+    constexpr int ES = int(sizeof(T));
+    const int nrw = OTp / NWF;        // even: OTp is a multiple of 16
+    uint32_t src[2], soff[2][EPL];
+    bool kval[EPL];
 #pragma unroll
-        for (int i = 0; i < Tr::E; ++i)
-            v[i] = (oc < p.OC && k + i < p.Kred) ? Elem<T>::ldg(w + size_t(oc) * p.Kred + k + i) : 0.f;
-        unsigned char* base = out + t * tb;
-        put_unit<T, 1>(base, base + OTp * ROWB, r, c, v);
+    for (int t = 0; t < 2; ++t) {
+        const int d = int(((size_t(oc0 + wf + NWF * t) * p.Kred + k0) * ES) & 15);
+        src[t] = slot + uint32_t(t * WRB + d + lane * ES);
+        const int r7 = wf + 4 * t;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+            const int kk = lane + 32 * e;
+            soff[t][e] = stage + uint32_t(r7 * 128 + (((kk / Tr::E) ^ r7) << 4) + (kk % Tr::E) * ES);
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) kval[e] = k0 + lane + 32 * e < p.Kred;
+#pragma unroll 4
+    for (int i2 = 0; i2 < nrw / 2; ++i2) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const uint32_t s = src[t] + uint32_t(i2 * 2 * WRB);
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) {
+                uint32_t v = ES == 4 ? lds32(s + uint32_t(64 * e)) : lds16(s + uint32_t(64 * e));
+                if (!kval[e]) v = 0u;
+                const uint32_t a = soff[t][e] + uint32_t(i2 * 1024);
+                if constexpr (Tr::split) {
+                    uint32_t hi, lo;
+                    split_tf32(v, hi, lo);
+                    sts32(a, hi);
+                    sts32(a + lo_off, lo);
+                } else {
+                    sts16(a, v);
+                }
+            }
+        }
+    }
+}
+
+// d_input stage (W transposed): row r = k0 + r of the reduction index (r < mrows; zero rows
+// up to KTp), K = output channels oc0 .. oc0 + KC - 1.  Warp wf owns the 32-row groups
+// g = wf, wf + DG_NWF, ...; for each of them and each of the KC channels its raw slot holds the
+// aligned blocks covering w[oc][k0 + 32 g .. +32) (9 blocks for fp32, 5 for bf16).
+template <typename T> struct DgRaw {
+    static constexpr int blocks = sizeof(T) == 4 ? 9 : 5;  // aligned 16-byte blocks per (group, channel)
+    static constexpr int rb = 16 * blocks;
+};
+template <typename T>
+inline __host__ __device__ int dgrad_wraw_warp_bytes(int KTp)
+{
+    return ((KTp / 32 + DG_NWF - 1) / DG_NWF) * TcTraits<T>::KC * DgRaw<T>::rb;
+}
+
+template <typename T>
+__device__ __forceinline__ void stage_wt_dgrad(uint32_t slot, const T* __restrict__ w, const ConvParams& p, int k0,
+                                               int oc0, int KTp, int wf, int lane)
+{
+    using Tr = TcTraits<T>;
+    constexpr int NB = DgRaw<T>::blocks, RB = DgRaw<T>::rb;
+    const char* wb = reinterpret_cast<const char*>(w);
+    const char* wend = wb + size_t(p.OC) * p.Kred * sizeof(T);
+    const int ngw = (KTp / 32 - wf + DG_NWF - 1) / DG_NWF;
+    for (int q = lane; q < ngw * Tr::KC * NB; q += 32) {
+        const int gi = q / (Tr::KC * NB), rem = q - gi * (Tr::KC * NB);
+        const int jj = rem / NB, b = rem - NB * (rem / NB);
+        const int oc = oc0 + jj, g = wf + DG_NWF * gi;
+        const char* a = wb + (size_t(oc) * p.Kred + k0 + 32 * g) * sizeof(T);
+        const char* s = reinterpret_cast<const char*>(reinterpret_cast<uintptr_t>(a) & ~uintptr_t(15)) + 16 * b;
+        const int n = (oc < p.OC && s < wend) ? int(min(ptrdiff_t(16), wend - s)) : 0;
+        cp_async16(slot + uint32_t((gi * Tr::KC + jj) * RB + 16 * b), n > 0 ? s : wb, uint32_t(n));
+    }
+}
+
+// Lane L builds row 32 g + L of each of the warp's groups: per 16-byte unit, E channels read
+// from E raw runs (32-lane runs, conflict-free) and one 16-byte store (the swizzle spreads the
+// warp's 32 rows over all banks).  Channel oc0 + c*E + e starts its run at a misalignment
+// that depends on e only, so the loop carries no address arithmetic.  Channels past OC were
+// zero-filled by the copies; rows past mrows are zeroed here.
+template <typename T>
+__device__ __forceinline__ void format_wt_dgrad(uint32_t stage, uint32_t lo_off, uint32_t slot, const ConvParams& p,
+                                                int k0, int mrows, int oc0, int KTp, int wf, int lane)
+{
+    using Tr = TcTraits<T>;
+    constexpr int E = Tr::E, ES = int(sizeof(T)), RB = DgRaw<T>::rb;
+    const int ngw = (KTp / 32 - wf + DG_NWF - 1) / DG_NWF;
+    uint32_t d[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) d[e] = uint32_t(((size_t(oc0 + e) * p.Kred + k0) * ES) & 15) + uint32_t(lane * ES);
+    const uint32_t rbase = uint32_t((lane >> 3) * 1024 + (lane & 7) * 128);
+    for (int gi = 0; gi < ngw; ++gi) {
+        const int g = wf + DG_NWF * gi, r = 32 * g + lane;
+        const bool rv = r < mrows;
+        const uint32_t gslot = slot + uint32_t(gi * Tr::KC * RB);
+        const uint32_t gst = stage + uint32_t(4 * g * 1024) + rbase;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            uint32_t v[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                v[e] = ES == 4 ? lds32(gslot + uint32_t((c * E + e) * RB) + d[e])
+                               : lds16(gslot + uint32_t((c * E + e) * RB) + d[e]);
+                if (!rv) v[e] = 0u;
+            }
+            const uint32_t a = gst + uint32_t((c ^ (lane & 7)) << 4);
+            if constexpr (Tr::split) {
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) split_tf32(v[e], hi[e], lo[e]);
+                sts128(a, hi[0], hi[1], hi[2], hi[3]);
+                sts128(a + lo_off, lo[0], lo[1], lo[2], lo[3]);
+            } else {
+                sts128(a, v[0] | (v[1] << 16), v[2] | (v[3] << 16), v[4] | (v[5] << 16), v[6] | (v[7] << 16));
+            }
+        }
+    }
+}
+
+// Workspace path: the same stages packed once per call into the caller's workspace, so that
+// the main kernel fetches each with one bulk copy instead of formatting it in every CTA.
+// The images are byte-identical to what in-kernel formatting produces (same split, same
+// zeros), so both paths give bit-identical results.  Grid (units / 256, chunks, tiles), one
+// 16-byte unit (hi and lo for fp32) per thread: no division.
+//   forward: tile (ot, kc) at index ot*nchunks + kc, OTp rows
+//   d_input: tile (kt, ch) at index kt*nch + ch, KTp rows (W transposed)
+template <typename T>
+__device__ __forceinline__ void put_unit(unsigned char* hi, unsigned char* lo, uint32_t off,
+                                         const uint32_t (&v)[TcTraits<T>::E])
+{
+    if constexpr (TcTraits<T>::split) {
+        uint32_t h[4], l[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) split_tf32(v[e], h[e], l[e]);
+        *reinterpret_cast<uint4*>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+    } else {
+        *reinterpret_cast<uint4*>(hi + off) =
+            make_uint4(v[0] | (v[1] << 16), v[2] | (v[3] << 16), v[4] | (v[5] << 16), v[6] | (v[7] << 16));
     }
 }
 
 template <typename T>
-__global__ void pack_dgrad_w_kernel(const ConvParams p, const T* __restrict__ w, unsigned char* __restrict__ out,
-                                    int nkt, int nch, int CIC, int KTp)
+__global__ void pack_fwd_w_kernel(const ConvParams p, const T* __restrict__ w, unsigned char* __restrict__ out,
+                                  int nchunks, int OTp)
 {
     grid_dep_launch();  // the implicit GEMM may start its prologue meanwhile
     using Tr = TcTraits<T>;
-    const int tile_units = KTp * 8;
-    const size_t total = size_t(nkt) * nch * tile_units;
-    const size_t tb = size_t(KTp) * ROWB * (Tr::split ? 2 : 1);
-    for (size_t u = blockIdx.x * size_t(blockDim.x) + threadIdx.x; u < total; u += size_t(gridDim.x) * blockDim.x) {
-        const int within = int(u % tile_units);
-        const size_t t = u / tile_units;
-        const int ch = int(t % nch), kt = int(t / nch);
-        const int r = within >> 3, c = within & 7;
-        const int k0 = kt * CIC * p.KK, mrows = min(CIC, p.IC - kt * CIC) * p.KK;
-        float v[8];
+    const int u = blockIdx.x * blockDim.x + threadIdx.x;
+    if (u >= OTp * 8) return;
+    const int kc = blockIdx.y, ot = blockIdx.z, r = u >> 3, c = u & 7;
+    const int oc = ot * OTp + r, k = kc * Tr::KC + c * Tr::E;
+    uint32_t v[Tr::E];
 #pragma unroll
-        for (int i = 0; i < Tr::E; ++i) {
-            const int oc = ch * Tr::KC + c * Tr::E + i;
-            v[i] = (r < mrows && oc < p.OC) ? Elem<T>::ldg(w + size_t(oc) * p.Kred + k0 + r) : 0.f;
-        }
-        unsigned char* base = out + t * tb;
-        put_unit<T, 1>(base, base + KTp * ROWB, r, c, v);
+    for (int e = 0; e < Tr::E; ++e) v[e] = (oc < p.OC && k + e < p.Kred) ? ld_bits(w + size_t(oc) * p.Kred + k + e) : 0u;
+    unsigned char* base = out + (size_t(ot) * nchunks + kc) * (size_t(OTp) * ROWB * (Tr::split ? 2 : 1));
+    put_unit<T>(base, base + OTp * ROWB, unit_off<1>(r, c), v);
+}
+
+template <typename T>
+__global__ void pack_dgrad_w_kernel(const ConvParams p, const T* __restrict__ w, unsigned char* __restrict__ out,
+                                    int nch, int CIC, int KTp)
+{
+    grid_dep_launch();  // the implicit GEMM may start its prologue meanwhile
+    using Tr = TcTraits<T>;
+    const int u = blockIdx.x * blockDim.x + threadIdx.x;
+    if (u >= KTp * 8) return;
+    const int ch = blockIdx.y, kt = blockIdx.z, r = u >> 3, c = u & 7;
+    const int k0 = kt * CIC * p.KK, mrows = min(CIC, p.IC - kt * CIC) * p.KK;
+    uint32_t v[Tr::E];
+#pragma unroll
+    for (int e = 0; e < Tr::E; ++e) {
+        const int oc = ch * Tr::KC + c * Tr::E + e;
+        v[e] = (r < mrows && oc < p.OC) ? ld_bits(w + size_t(oc) * p.Kred + k0 + r) : 0u;
     }
+    unsigned char* base = out + (size_t(kt) * nch + ch) * (size_t(KTp) * ROWB * (Tr::split ? 2 : 1));
+    put_unit<T>(base, base + KTp * ROWB, unit_off<1>(r, c), v);
 }
 
 // ======================================================================================
 // Forward: tile = (128 columns n = (b, oh, ow), OTp output channels); K = IC*K*K in
 // chunks of KC.  The gathered operand X[n, k] is the MMA's A operand and lives in
-// tensor memory (lane m = column n0 + m, K along the TMEM columns); the packed weights
-// are the B operand (N = OTp rows; fp32: the tf32 hi rows followed by the lo rows, so
-// one N = 2*OTp MMA forms X_hi*W_hi and X_hi*W_lo, and a second N = OTp MMA adds
-// X_lo*W_hi into the first half).  Only the weights are read from shared memory by
-// the tensor core.
-// Warp roles (608 threads):
+// tensor memory (lane m = column n0 + m, K along the TMEM columns); the weights are the
+// B operand in shared memory (N = OTp rows; fp32: the tf32 hi rows followed by the lo rows,
+// so one N = 2*OTp MMA forms X_hi*W_hi and X_hi*W_lo, and a second N = OTp MMA adds
+// X_lo*W_hi into the first half).  Only the weights are read from shared memory by the
+// tensor core.
+// Warp roles (704 threads):
 //   warp 0      x producer: per super-chunk (XG consecutive K-chunks) and per sample the
 //               tile touches, one bulk copy of the contiguous channels x[b, ic_lo : ic_hi]
-//               the super-chunk covers, into one of two raw slots.  Sources are rounded
+//               the super-chunk covers, into one of the raw slots.  Sources are rounded
 //               down to 16 bytes (the slack is skipped when read); bytes of a last
 //               16-byte block that lie past the end of x are copied by plain loads.
-//   warp 1      w producer: per K-chunk, one bulk copy of the packed weight chunk
-//               (OTp rows x 128 bytes; x2 for fp32 hi + lo) into a weight stage.
-//   warp 2      MMA: one thread issues the chunk's tcgen05.mma steps, commits to the
+//   warp 1      MMA: one thread issues the chunk's tcgen05.mma steps, commits to the
 //               weight stage's and the TMEM operand stage's "empty" barriers and, after
 //               a tile's last chunk, to the accumulator barrier.
-//   warps 3-18  formatters: warp w owns TMEM lanes 32*(w%4) .. +31 (one column each) and
-//               a quarter of each chunk's K; gathers its column's patch values from the
+//   warps 2-5   weight formatters: each K-chunk's weight stage from w (stage_w_fwd, format_w_fwd).
+//   warps 6-21  gather formatters: warp w owns TMEM lanes 32*(w%4) .. +31 (one column each)
+//               and a quarter of each chunk's K; gathers its column's patch values from the
 //               raw slot and writes them with tcgen05.st; then the tile's epilogue
-//               (TMEM -> ReLU -> y), each warp a quarter of the output channels.
+//               (TMEM -> bias -> ReLU -> y), each warp a quarter of the output channels.
+// K ranges: with fewer column tiles than half the SMs, the K-chunks of a tile split into
+// R ranges computed by the R CTAs of one thread-block cluster.  Each CTA writes its fp32
+// partial tile into its own shared memory; after a cluster barrier CTA q sums rows
+// [q*128/R, (q+1)*128/R) of the R partials in ascending rank order through distributed
+// shared memory, adds the bias, applies the ReLU and writes y.  No global scratch.
 // ======================================================================================
-constexpr int FV_MMA_WARP = 2;
-constexpr int FV_FMT0 = 96;   // first formatter thread (warp 3)
 constexpr int FV_MAXRAWS = 4;  // max raw x slots of the forward
 
+constexpr int FA_XWARP = 0;    // x producer
+constexpr int FA_MMAWARP = 1;  // MMA issuer
+constexpr int FA_WF0 = 2;      // first weight-formatter warp
+constexpr int FA_FMT0 = 32 * (FA_WF0 + NWF);  // first gather-formatter thread (warp 6)
 constexpr int FA_TM = 128;    // columns per forward tile (TMEM lanes)
 constexpr int FA_KSPLIT = 4;  // formatter warps per TMEM lane quarter (each a quarter of the chunk's K)
 constexpr int FA_FMTW = 4 * FA_KSPLIT;
-constexpr int FA_THREADS = FV_FMT0 + 32 * FA_FMTW;
+constexpr int FA_THREADS = FA_FMT0 + 32 * FA_FMTW;
 constexpr int FA_MAXW = 6;    // max weight stages
 constexpr int FA_MAXA = 8;    // max TMEM operand stages
 constexpr int FA_TMEM_COLS = 512;
@@ -247,8 +393,9 @@ struct FwdGeom {
     int w_bytes;        // one weight stage
     int dcols;          // accumulator columns (2*OTp for split fp32)
     int acol0, acols;   // first TMEM column of the operand stages, columns per stage
-    int splits;         // K ranges (split-K when there are too few column tiles)
+    int splits;         // K ranges = cluster size (1: no split)
     int kc_per;         // K-chunks per range (a multiple of xg)
+    int packed;         // 1: weight stages bulk-copied from a packed image in the workspace
 };
 
 struct FwdBars {
@@ -259,6 +406,10 @@ struct FwdBars {
     uint32_t tslot;
     int abort_flag;
 };
+
+// Row stride (floats) of a CTA's partial tile in the K-range reduction: 16-byte rows whose
+// first words fall 4 banks apart.
+inline __host__ __device__ int fwd_red_stride(int OTp) { return OTp + 4; }
 
 template <typename T>
 inline FwdGeom fwd_geom(const ConvParams& p, int xg, int nw, int nraw)
@@ -288,36 +439,35 @@ inline FwdGeom fwd_geom(const ConvParams& p, int xg, int nw, int nraw)
     g.na = std::min(FA_MAXA, (FA_TMEM_COLS - g.acol0) / g.acols);
     g.splits = 1;
     g.kc_per = g.nchunks;
+    g.packed = 0;
     return g;
 }
 
 // Estimated forward time in chunk steps of one CTA (about a microsecond each): rounds of
-// work items over the SMs x chunks per item, plus, with K ranges, the reduce kernel (a launch
-// and one pass over the fp32 partials).
-inline double fwd_cost(int tiles, int sms, int splits, int kc, size_t part)
+// work items over the SMs x chunks per item, plus, with K ranges, the in-cluster reduction
+// (a cluster barrier and R distributed-shared-memory reads per output).
+inline double fwd_cost(int tiles, int sms, int splits, int kc)
 {
-    return double(ceil_div(tiles * splits, sms)) * kc +
-           (splits > 1 ? 1.5 + double(splits) * double(part) / 8e6 : 0.0);
+    return double(ceil_div(tiles * splits, sms)) * kc + (splits > 1 ? 0.5 + 0.05 * splits : 0.0);
 }
 
 // K ranges, only when the column tiles fill fewer than half the SMs (with more, a range's
-// fixed cost -- its own x slabs, pipeline fill and partial sums -- outweighs the gain; layer 1
-// at B = 1024, 96 tiles, ran 8 % slower in fp32 and 40 % slower in bf16 with three ranges):
-// the split of the nchunks K-chunks (kc_per of them, a multiple of xg, per range) with the
-// lowest estimated time, within the scratch buffer's room for partials.  Returns that estimate.
-inline double fwd_set_splits(FwdGeom& g, const ConvParams& p, int sms, size_t packed, size_t scratch)
+// fixed cost -- its own x slabs and pipeline fill -- outweighs the gain; layer 1 at B = 1024,
+// 96 tiles, ran 8 % slower in fp32 and 40 % slower in bf16 with three ranges): the split of
+// the nchunks K-chunks (kc_per of them, a multiple of xg, per range) into R <= kMaxCluster
+// ranges, one cluster of R CTAs per tile, with the lowest estimated time.  Returns that
+// estimate.
+inline double fwd_set_splits(FwdGeom& g, int sms)
 {
     const int tiles = g.n_tiles * g.oc_tiles;
-    double best = fwd_cost(tiles, sms, 1, g.nchunks, 0);
+    double best = fwd_cost(tiles, sms, 1, g.nchunks);
     if (2 * tiles >= sms || g.nchunks < 2 * g.xg) return best;
-    const size_t part = size_t(p.N) * g.oc_tiles * g.OTp * 4;  // one range's partials
-    const size_t room = scratch > packed + 256 ? scratch - round_up(packed, size_t(256)) : 0;
-    const int smax = int(std::min<size_t>(std::min<size_t>(room / part, size_t(g.nchunks / g.xg)), 16));
+    const int smax = std::min(g.nchunks / g.xg, kMaxCluster);
     for (int want = 2; want <= smax; ++want) {
         const int kc = round_up(ceil_div(g.nchunks, want), g.xg);
         const int splits = ceil_div(g.nchunks, kc);
-        if (splits < 2) continue;
-        const double c = fwd_cost(tiles, sms, splits, kc, part);
+        if (splits < 2 || tiles * splits > sms) continue;  // one work item per CTA
+        const double c = fwd_cost(tiles, sms, splits, kc);
         if (c < best) {
             best = c;
             g.kc_per = kc;
@@ -327,17 +477,26 @@ inline double fwd_set_splits(FwdGeom& g, const ConvParams& p, int sms, size_t pa
     return best;
 }
 
+// Raw w slots of the weight formatters (none on the workspace path).
+inline __host__ __device__ int fwd_wraw_bytes(const FwdGeom& g)
+{
+    return g.packed ? 0 : NWF * WRAW * fwd_wraw_warp_bytes(g.OTp);
+}
+
 template <typename T>
 inline int fwd_smem(const ConvParams& p, const FwdGeom& g)
 {
     const int kred_pad = round_up(p.Kred, TcTraits<T>::KC);
-    return 1024 + g.nw * g.w_bytes + g.nraw * g.raw_bytes + kred_pad * 4 + int(sizeof(FwdBars)) + 16;
+    return 1024 + g.nw * g.w_bytes + g.nraw * g.raw_bytes + fwd_wraw_bytes(g) + kred_pad * 4 + int(sizeof(FwdBars)) +
+           16;
 }
 
-template <typename T>
-inline size_t fwd_packed_bytes(const FwdGeom& g)
+// With K ranges the partial tile (128 rows x fwd_red_stride(OTp) floats) reuses the weight
+// stages and raw slots once the tile's MMAs are done.
+inline bool fwd_red_fits(const FwdGeom& g)
 {
-    return size_t(g.oc_tiles) * g.nchunks * g.w_bytes;
+    return g.splits <= 1 || size_t(FA_TM) * fwd_red_stride(g.OTp) * 4 <= size_t(g.nw) * g.w_bytes +
+                                                                           size_t(g.nraw) * g.raw_bytes;
 }
 
 __device__ __forceinline__ int warp_sum(int v)
@@ -347,19 +506,18 @@ __device__ __forceinline__ int warp_sum(int v)
     return v;
 }
 
+// Store the 16-byte unit `v` of a B operand stage: as tf32 hi and lo parts (fp32), or as is (bf16).
 template <typename T, int SWZ>
 __device__ __forceinline__ void put_raw_unit(unsigned char* hi, unsigned char* lo, uint32_t off, uint4 v)
 {
     if constexpr (TcTraits<T>::split) {
-        float h[4], l[4];
-        const float f[4] = {__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w)};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            h[i] = to_tf32(f[i]);
-            l[i] = to_tf32(f[i] - h[i]);
-        }
-        st_unit(hi, off, __float_as_uint(h[0]), __float_as_uint(h[1]), __float_as_uint(h[2]), __float_as_uint(h[3]));
-        st_unit(lo, off, __float_as_uint(l[0]), __float_as_uint(l[1]), __float_as_uint(l[2]), __float_as_uint(l[3]));
+        uint32_t h[4], l[4];
+        split_tf32(v.x, h[0], l[0]);
+        split_tf32(v.y, h[1], l[1]);
+        split_tf32(v.z, h[2], l[2]);
+        split_tf32(v.w, h[3], l[3]);
+        st_unit(hi, off, h[0], h[1], h[2], h[3]);
+        st_unit(lo, off, l[0], l[1], l[2], l[3]);
     } else {
         st_unit(hi, off, v.x, v.y, v.z, v.w);
     }
@@ -392,10 +550,10 @@ struct RingPos {
     }
 };
 
-template <typename T, bool RELU, int SWZ>
+template <typename T, bool RELU>
 __global__ void __launch_bounds__(FA_THREADS, 1)
-fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* __restrict__ wpack,
-              const T* __restrict__ bias, T* __restrict__ y, float* __restrict__ part, const FwdGeom geo)
+fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict__ w,
+              const unsigned char* __restrict__ wpack, const T* __restrict__ bias, T* __restrict__ y, const FwdGeom geo)
 {
     using Tr = TcTraits<T>;
     constexpr int ES = int(sizeof(T));
@@ -405,10 +563,11 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = align1024(smem_raw);
     const int kred_pad = round_up(p.Kred, Tr::KC);
-    // Layout: weight stages | raw x slots | k offsets | barriers
+    // Layout: weight stages | raw x slots | raw w slots (NWF warps x WRAW) | k offsets | barriers
     unsigned char* wring = smem;
     unsigned char* raw = wring + geo.nw * geo.w_bytes;
-    int* offk = reinterpret_cast<int*>(raw + geo.nraw * geo.raw_bytes);
+    unsigned char* wraw = raw + geo.nraw * geo.raw_bytes;
+    int* offk = reinterpret_cast<int*>(wraw + fwd_wraw_bytes(geo));
     FwdBars* bars = reinterpret_cast<FwdBars*>(offk + kred_pad);
     volatile int* abort_flag = &bars->abort_flag;
 
@@ -424,7 +583,7 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
             mbar_init(smem_u32(&bars->raw_empty[i]), FA_FMTW);
         }
         for (int i = 0; i < geo.nw; ++i) {
-            mbar_init(smem_u32(&bars->w_full[i]), 1);
+            mbar_init(smem_u32(&bars->w_full[i]), geo.packed ? 1 : NWF);
             mbar_init(smem_u32(&bars->w_empty[i]), 1);
         }
         for (int i = 0; i < geo.na; ++i) {
@@ -441,25 +600,32 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tslot;
-    // Tile = (column tile, oc tile, K range); K range sp covers chunks [sp*kc_per, ...).
+    // Nothing above touches global memory: the previous kernel on the stream may still run.
+    grid_dep_wait();
+    // Work item = (column tile, oc tile, K range).  Without K ranges the CTAs stride over the
+    // tiles; with them the grid is one CTA per item and the R CTAs of a cluster share a tile.
+    const int R = geo.splits;
     const int ctiles = geo.n_tiles * geo.oc_tiles;
-    const int total_tiles = ctiles * geo.splits;
-    auto krange = [&](int tile, int& lo, int& hi) {
-        lo = (tile / ctiles) * geo.kc_per;
-        hi = min(geo.nchunks, lo + geo.kc_per);
+    const int total_items = ctiles * R;
+    auto decode = [&](int item, int& ntile, int& ot, int& kc_lo, int& kc_hi) {
+        const int ct = item / R, range = item % R;
+        ntile = ct % geo.n_tiles;
+        ot = ct / geo.n_tiles;
+        kc_lo = range * geo.kc_per;
+        kc_hi = min(geo.nchunks, kc_lo + geo.kc_per);
     };
 
-    if (warp == 0) {
+    if (warp == FA_XWARP) {
         // ---------------- x producer ----------------
         const unsigned char* xb = reinterpret_cast<const unsigned char*>(x);
         const unsigned char* x_end = xb + size_t(p.B) * p.IHW * ES;
         RingPos rp;
-        for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
-            const int n0 = (tile % geo.n_tiles) * FA_TM;
+        for (int item = blockIdx.x; item < total_items && !*abort_flag; item += gridDim.x) {
+            int ntile, ot, kc_lo, kc_hi;
+            decode(item, ntile, ot, kc_lo, kc_hi);
+            const int n0 = ntile * FA_TM;
             const int n_end = min(n0 + FA_TM, p.N);
             const int b_first = n0 / p.P, nsamp = (n_end - 1) / p.P - b_first + 1;
-            int kc_lo, kc_hi;
-            krange(tile, kc_lo, kc_hi);
             for (int sc = kc_lo / geo.xg; sc < (kc_hi + geo.xg - 1) / geo.xg; ++sc, rp.next(geo.nraw)) {
                 const int s = rp.i;
                 if (rp.wrapped && !mbar_wait_or_abort(smem_u32(&bars->raw_empty[s]), rp.ph ^ 1u, abort_flag)) {
@@ -491,6 +657,7 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
                     tx += bulk;
                 }
                 tx = warp_sum(tx);
+                __syncwarp();  // every lane's tail stores happen before lane 0's (releasing) arrive
                 if (lane == 0) mbar_arrive_expect_tx(smem_u32(&bars->raw_full[s]), uint32_t(tx));
                 __syncwarp();
                 for (int j = lane; j < nsamp; j += 32) {
@@ -502,29 +669,78 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
                 }
             }
         }
-    } else if (warp == 1) {
-        // ---------------- w producer ----------------
-        if (lane == 0) {
-            grid_dep_wait();  // the packed weights come from the kernel launched just before
+    } else if (warp >= FA_WF0 && warp < FA_WF0 + NWF && geo.packed) {
+        // ---------------- weight stages from the packed image (workspace path) ----------------
+        if (warp == FA_WF0 && lane == 0) {
             RingPos wp;
-            for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
-                const int ot = (tile / geo.n_tiles) % geo.oc_tiles;
-                int kc_lo, kc_hi;
-                krange(tile, kc_lo, kc_hi);
+            for (int item = blockIdx.x; item < total_items && !*abort_flag; item += gridDim.x) {
+                int ntile, ot, kc_lo, kc_hi;
+                decode(item, ntile, ot, kc_lo, kc_hi);
                 const unsigned char* src = wpack + (size_t(ot) * geo.nchunks + kc_lo) * geo.w_bytes;
+                bool ok = true;
                 for (int kc = kc_lo; kc < kc_hi; ++kc, wp.next(geo.nw), src += geo.w_bytes) {
                     if (wp.wrapped && !mbar_wait_or_abort(smem_u32(&bars->w_empty[wp.i]), wp.ph ^ 1u, abort_flag)) {
                         report(const_cast<int*>(abort_flag), 16u);
+                        ok = false;
                         break;
                     }
                     const uint32_t bar = smem_u32(&bars->w_full[wp.i]);
                     mbar_arrive_expect_tx(bar, uint32_t(geo.w_bytes));
                     bulk_g2s(smem_u32(wring + wp.i * geo.w_bytes), src, uint32_t(geo.w_bytes), bar);
                 }
+                if (!ok) break;
             }
         }
         __syncwarp();
-    } else if (warp == FV_MMA_WARP) {
+    } else if (warp >= FA_WF0 && warp < FA_WF0 + NWF) {
+        // ---------------- weight formatters ----------------
+        // The warp's chunk sequence (item, kc) over this CTA's work items; the copies of the
+        // next chunk are in flight while the current one is formatted.
+        const int wf = warp - FA_WF0;
+        const uint32_t w_u32 = smem_u32(wring), lo_off = uint32_t(geo.OTp * ROWB);
+        const uint32_t slot0 = smem_u32(wraw) + uint32_t(wf * WRAW * fwd_wraw_warp_bytes(geo.OTp));
+        const uint32_t slot_bytes = uint32_t(fwd_wraw_warp_bytes(geo.OTp));
+        struct Seq { int item, kc, hi, ot; };
+        auto first = [&](Seq& s, int item) -> bool {
+            if (item >= total_items) return false;
+            int ntile, lo;
+            decode(item, ntile, s.ot, lo, s.hi);
+            s.item = item;
+            s.kc = lo;
+            return true;
+        };
+        auto advance = [&](Seq& s) -> bool { return ++s.kc < s.hi || first(s, s.item + int(gridDim.x)); };
+        Seq cur;
+        bool have = first(cur, int(blockIdx.x));
+        if (have) stage_w_fwd<T>(slot0, w, p, cur.ot * geo.OTp, cur.kc * Tr::KC, geo.OTp, wf, lane);
+        cp_async_commit();
+        uint32_t slot = 0;
+        RingPos wp;
+        while (have && !*abort_flag) {
+            Seq nxt = cur;
+            const bool have_nxt = advance(nxt);
+            if (have_nxt)
+                stage_w_fwd<T>(slot0 + (slot ^ 1u) * slot_bytes, w, p, nxt.ot * geo.OTp, nxt.kc * Tr::KC, geo.OTp, wf,
+                               lane);
+            cp_async_commit();
+            cp_async_wait<1>();  // this lane's copies of the current chunk have landed
+            __syncwarp();        // ... and every lane's are visible to the warp
+            if (wp.wrapped && !mbar_wait_or_abort(smem_u32(&bars->w_empty[wp.i]), wp.ph ^ 1u, abort_flag)) {
+                report(const_cast<int*>(abort_flag), 16u);
+                break;
+            }
+            format_w_fwd<T>(w_u32 + uint32_t(wp.i * geo.w_bytes), lo_off, slot0 + slot * slot_bytes, p,
+                            cur.ot * geo.OTp, cur.kc * Tr::KC, geo.OTp, wf, lane);
+            fence_proxy_async_smem();  // the generic-proxy stores, for the tensor core
+            __syncwarp();              // also: every lane is done reading this raw slot
+            if (lane == 0) mbar_arrive(smem_u32(&bars->w_full[wp.i]));
+            wp.next(geo.nw);
+            cur = nxt;
+            have = have_nxt;
+            slot ^= 1u;
+        }
+        cp_async_wait<0>();  // no copy may land after the CTA's shared memory is reused or released
+    } else if (warp == FA_MMAWARP) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             // fp32: N = 2*OTp over [W_hi; W_lo], then N = OTp over W_hi; bf16: N = OTp.
@@ -533,15 +749,15 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
             const uint32_t w_u32 = smem_u32(wring);
             RingPos wp, ap;
             uint32_t t = 0;
-            for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x, ++t) {
+            for (int item = blockIdx.x; item < total_items && !*abort_flag; item += gridDim.x, ++t) {
+                int ntile, ot, kc_lo, kc_hi;
+                decode(item, ntile, ot, kc_lo, kc_hi);
                 bool ok = true;
                 if (t >= 1 && !mbar_wait_or_abort(smem_u32(&bars->acc_empty), (t - 1) & 1, abort_flag)) {
                     report(const_cast<int*>(abort_flag), 8u);
                     break;
                 }
                 tc_fence_after();
-                int kc_lo, kc_hi;
-                krange(tile, kc_lo, kc_hi);
                 for (int kc = kc_lo; kc < kc_hi; ++kc, wp.next(geo.nw), ap.next(geo.na)) {
                     if (!mbar_wait_or_abort(smem_u32(&bars->w_full[wp.i]), wp.ph, abort_flag) ||
                         !mbar_wait_or_abort(smem_u32(&bars->a_full[ap.i]), ap.ph, abort_flag)) {
@@ -554,7 +770,7 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
                     const uint32_t aa = tmem + uint32_t(geo.acol0 + ap.i * geo.acols);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const uint64_t bd = op_desc<SWZ>(wa + kstep_off<SWZ>(j));
+                        const uint64_t bd = op_desc<1>(wa + kstep_off<1>(j));
                         const uint32_t acc = (kc == kc_lo && j == 0) ? 0u : 1u;
                         if constexpr (Tr::split) {
                             mma_tf32_ta(tmem, aa + 8 * j, bd, idesc2, acc);           // hi * [hi; lo]
@@ -571,23 +787,23 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
             }
         }
         __syncwarp();
-    } else {
-        // ---------------- formatters + epilogue ----------------
-        const int fw = warp - 3;            // 0 .. FA_FMTW - 1
-        const int qd = warp & 3;            // TMEM lane quarter this warp may access
-        const int sub = fw >> 2;            // which quarter of each chunk's K
-        const int m = qd * 32 + lane;       // this thread's column within the tile
+    } else if (warp >= FA_FMT0 / 32) {
+        // ---------------- gather formatters + epilogue ----------------
+        const int fw = warp - FA_FMT0 / 32;  // 0 .. FA_FMTW - 1
+        const int qd = warp & 3;             // TMEM lane quarter this warp may access
+        const int sub = fw >> 2;             // which quarter of each chunk's K
+        const int m = qd * 32 + lane;        // this thread's column within the tile
         const uint32_t lane_bits = uint32_t(qd * 32) << 16;
         const uint32_t raw_u32 = smem_u32(raw), offk_u32 = smem_u32(offk) + uint32_t(sub * KQ * 4);
         const bool ragged_k = (p.Kred % Tr::KC) != 0;
         RingPos ap, rp;
         uint32_t t = 0;
-        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++t) {
-            const int n0 = (tile % geo.n_tiles) * FA_TM, ot = (tile / geo.n_tiles) % geo.oc_tiles;
+        for (int item = blockIdx.x; item < total_items; item += gridDim.x, ++t) {
+            int ntile, ot, kc_lo, kc_hi;
+            decode(item, ntile, ot, kc_lo, kc_hi);
+            const int n0 = ntile * FA_TM;
             const int b_first = n0 / p.P;
             const int n = n0 + m;
-            int kc_lo, kc_hi;
-            krange(tile, kc_lo, kc_hi);
             // Columns past N gather column N-1's values: their accumulator rows are
             // computed but never stored (rows of D depend only on rows of A).
             int boff, bmis;
@@ -642,13 +858,7 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
                 if constexpr (Tr::split) {
                     uint32_t hi[8], lo[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        // lo is left unrounded: the MMA reads its tf32 bits (|lo| <= 2^-11 |v|).
-                        const float f = __uint_as_float(v[e]);
-                        const float h = to_tf32(f);
-                        hi[e] = __float_as_uint(h);
-                        lo[e] = __float_as_uint(f - h);
-                    }
+                    for (int e = 0; e < 8; ++e) split_tf32(v[e], hi[e], lo[e]);
                     tmem_st8(col, hi);
                     tmem_st8(col + Tr::KC, lo);
                 } else {
@@ -671,20 +881,17 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
                 }
             }
             if (!ok) break;
-            // Epilogue: TMEM -> y, plus the bias if given, then ReLU (or, with K ranges, -> this
-            // range's fp32 partials, the bias and ReLU left to the reduce kernel); this
-            // warp's lanes, every FA_KSPLIT-th group of 8 channels.
+            // Epilogue: TMEM -> y, plus the bias if given, then ReLU; with K ranges -> this
+            // CTA's fp32 partial tile in shared memory (row m, the tile's OTp channels), reduced
+            // across the cluster below.  This warp's lanes, every FA_KSPLIT-th group of 8 channels.
             if (!mbar_wait_or_abort(smem_u32(&bars->acc_full), t & 1, abort_flag)) {
                 report(const_cast<int*>(abort_flag), 2u);
                 break;
             }
             tc_fence_after();
-            T* yc = nullptr;
-            float* pc = nullptr;
-            if (n < p.N) {
-                if (geo.splits == 1) yc = y + col_out(p, n);
-                else pc = part + (size_t(tile / ctiles) * p.N + n) * (geo.oc_tiles * geo.OTp) + ot * geo.OTp;
-            }
+            if (R == 1) grid_dep_launch();  // the last tile: the next kernel may be scheduled now
+            T* yc = (R == 1 && n < p.N) ? y + col_out(p, n) : nullptr;
+            const uint32_t red_row = smem_u32(smem) + uint32_t(m * fwd_red_stride(geo.OTp) * 4);
             for (int cb = sub * 8; cb < geo.OTp; cb += 8 * FA_KSPLIT) {
                 uint32_t r[8];
                 tmem_ld8(tmem + lane_bits + uint32_t(cb), r);
@@ -708,11 +915,9 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
                             Elem<T>::st(yc + size_t(oc) * p.P, f);
                         }
                     }
-                } else if (pc) {
-                    *reinterpret_cast<float4*>(pc + cb) = make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]),
-                                                                      __uint_as_float(r[2]), __uint_as_float(r[3]));
-                    *reinterpret_cast<float4*>(pc + cb + 4) = make_float4(
-                        __uint_as_float(r[4]), __uint_as_float(r[5]), __uint_as_float(r[6]), __uint_as_float(r[7]));
+                } else if (R > 1) {
+                    sts128(red_row + uint32_t(cb * 4), r[0], r[1], r[2], r[3]);
+                    sts128(red_row + uint32_t(cb * 4 + 16), r[4], r[5], r[6], r[7]);
                 }
             }
             tc_fence_before();
@@ -725,25 +930,49 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const unsigned char* 
         tc_fence_after();
         tmem_dealloc(tmem, FA_TMEM_COLS);
     }
-}
-
-// Sum of the forward's K-range partials in ascending range order, then the bias (if any) and
-// ReLU, into y.
-template <typename T, bool RELU>
-__global__ void fwd_reduce_kernel(const ConvParams p, const float* __restrict__ part, int splits, int ocp,
-                                  const T* __restrict__ bias, T* __restrict__ y)
-{
-    grid_dep_wait();  // the partials come from the kernel launched just before
-    const size_t total = size_t(p.N) * p.OC;
-    const size_t sstride = size_t(p.N) * ocp;
-    for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < total; i += size_t(gridDim.x) * blockDim.x) {
-        const int n = int(i / p.OC), oc = int(i % p.OC);
-        const float* src = part + size_t(n) * ocp + oc;
-        float s = 0.f;
-        for (int sp = 0; sp < splits; ++sp) s += __ldcg(src + size_t(sp) * sstride);
-        if (bias) s += Elem<T>::ldg(bias + oc);
-        if (RELU) s = s > 0.f ? s : 0.f;
-        Elem<T>::st(y + col_out(p, n) + size_t(oc) * p.P, s);
+    if (R > 1) {
+        // K-range reduction across the cluster (every thread of every CTA passes both cluster
+        // barriers exactly once, also after an aborted wait: the status word then already
+        // holds the error and the output is unspecified).
+        grid_dep_launch();
+        cluster_sync();  // every CTA's partial tile is in its shared memory
+        const int rank = int(cluster_rank());
+        int ntile, ot, kc_lo, kc_hi;
+        decode(int(blockIdx.x), ntile, ot, kc_lo, kc_hi);
+        const int rows = ceil_div(FA_TM, R);  // tile rows (columns n) this CTA finishes
+        const int r0 = rank * rows, r1 = min(FA_TM, r0 + rows);
+        const int q4 = geo.OTp / 4;           // 16-byte groups of channels per row
+        const int RS = fwd_red_stride(geo.OTp);
+        const uint32_t base = smem_u32(smem);
+        uint32_t peer[kMaxCluster];
+#pragma unroll
+        for (int q = 0; q < kMaxCluster; ++q) peer[q] = q < R ? dsmem_addr(base, uint32_t(q)) : 0u;
+        for (int it = tid; it < (r1 - r0) * q4; it += FA_THREADS) {
+            const int mm = r0 + it % (r1 - r0), g4 = it / (r1 - r0);  // consecutive threads: consecutive columns
+            const int n = ntile * FA_TM + mm;
+            if (n >= p.N) continue;
+            const uint32_t off = uint32_t((mm * RS + g4 * 4) * 4);
+            float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < kMaxCluster; ++q) {
+                if (q >= R) break;
+                const float4 v = ld_dsmem_f4(peer[q] + off);
+                s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+            }
+            const float f4[4] = {s.x, s.y, s.z, s.w};
+            T* yc = y + col_out(p, n);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int oc = ot * geo.OTp + g4 * 4 + e;
+                if (oc < p.OC) {
+                    float f = f4[e];
+                    if (bias) f += Elem<T>::ldg(bias + oc);
+                    if (RELU) f = f > 0.f ? f : 0.f;
+                    Elem<T>::st(yc + size_t(oc) * p.P, f);
+                }
+            }
+        }
+        cluster_sync();  // no CTA leaves while a peer still reads its shared memory
     }
 }
 
@@ -768,7 +997,9 @@ __global__ void fwd_reduce_kernel(const ConvParams p, const float* __restrict__ 
 //               B stage.
 //   warps 3-18  epilogue: the fp32 tile to ws[split][oc][k] (row stride kpad).
 // ======================================================================================
-constexpr int WG_THREADS = FV_FMT0 + 32 * 16;
+constexpr int WG_MMA_WARP = 2;
+constexpr int WG_FMT0 = 96;  // first formatter thread (warp 3)
+constexpr int WG_THREADS = WG_FMT0 + 32 * 16;
 constexpr int WG_MAXA = 8, WG_MAXB = 4, WG_MAXR = 5;
 // Formatter roles: G warps (a multiple of 4, one or more per TMEM lane quarter) and X
 // warps; the column groups of 8 words one G thread writes; the B-stage rows one X thread
@@ -902,6 +1133,8 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tslot;
+    // Nothing above touches global memory: the previous kernel on the stream may still run.
+    grid_dep_wait();
     const int per_split = geo.k_tiles * geo.oc_tiles;
     const int total = per_split * geo.splits;
 
@@ -1000,7 +1233,7 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
             }
         }
         __syncwarp();
-    } else if (warp == FV_MMA_WARP) {
+    } else if (warp == WG_MMA_WARP) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             const uint32_t idesc2 = instr_desc(Tr::fmt, TC_M, geo.dcols);
@@ -1226,7 +1459,7 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
             // ---------------- X formatters ----------------
             // 16-byte unit column c (E columns) of rows rbase + i*rstep.
             const int xthreads = 32 * (16 - NGW);
-            const int xt = tid - FV_FMT0 - 32 * NGW;
+            const int xt = tid - WG_FMT0 - 32 * NGW;
             const int upr = geo.cnp / Tr::E;     // units per row
             const int cfix = xt % upr;
             const int rbase = xt / upr;
@@ -1332,20 +1565,24 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
 // then  dx[b, ic, h, w] = sum over (oh, kh) with oh*S + kh = h, (ow, kw) with
 // ow*S + kw = w of D, in a fixed order (no atomics).  G = dy masked by y > 0 is the
 // MMA's A operand in tensor memory (K = output channels along the TMEM columns), built
-// once per sample tile; the packed W^T tiles are the shared-memory B operand.
+// once per sample tile; the W^T tiles are the shared-memory B operand, formatted in the
+// kernel from w.
 // Warp roles (608 threads):
-//   warp 1      w producer: packed W^T tiles (kt, oc chunk), one bulk copy each, into a ring.
-//   warp 2      MMA: per k-tile, the oc-chunk MMAs into an accumulator buffer, then a
+//   warp 0      MMA: per k-tile, the oc-chunk MMAs into an accumulator buffer, then a
 //               commit to that buffer's barrier (two buffers for bf16: the MMAs of k-tile
 //               kt+1 run while k-tile kt is read out).
+//   warps 1-2   weight formatters: the W^T tiles (kt, oc chunk) from w into a ring of
+//               stages (stage_wt_dgrad, format_wt_dgrad).
 //   warps 3-18  formatters: per sample tile, load dy (and y) of their lane's column and
 //               a quarter of the output channels from global memory, mask, split (fp32)
 //               and store G to TMEM; per k-tile, TMEM -> Ds (fp32 [n][k] in shared
 //               memory), then the col2im gather into dx with all 512 threads.
-//   warp 0      idle after set-up.
 // ======================================================================================
+constexpr int DG_MMA_WARP = 0;
+constexpr int DG_WF0 = 1;                     // first weight-formatter warp
+constexpr int DG_FMT0 = 32 * (DG_WF0 + DG_NWF);  // first formatter thread (warp 3)
 constexpr int DG_FMTW = 16;
-constexpr int DG_THREADS = FV_FMT0 + 32 * DG_FMTW;
+constexpr int DG_THREADS = DG_FMT0 + 32 * DG_FMTW;
 constexpr int DG_NFT = 32 * DG_FMTW;  // formatter threads
 constexpr int DG_MAXW = 6;
 constexpr int DG_TM = 128;             // columns per sample tile (TMEM lanes)
@@ -1368,6 +1605,7 @@ struct TcDgradGeom {
     int ntiles;      // ceil(B / NS)
     int ktsplit;     // k-tile ranges per sample tile (more work items when the tiles are few)
     int kt_per;      // k-tiles per range
+    int packed;      // 1: W^T stages bulk-copied from a packed image in the workspace
 };
 
 struct DgBars {
@@ -1401,6 +1639,7 @@ inline TcDgradGeom dgrad_geom(const ConvParams& p, int CIC, int nw)
     g.ntiles = ceil_div(p.B, g.NS);
     g.ktsplit = 1;
     g.kt_per = g.nkt;
+    g.packed = 0;
     auto axis_max = [](int n, int K, int S, int O) {
         int m = 0;
         for (int h = 0; h < n; ++h) {
@@ -1418,29 +1657,33 @@ constexpr int DG_DSTR = DG_TM + 4;  // Ds row stride (floats): 16-byte rows, 4 b
 constexpr int DG_TMAX = 4;          // taps per input pixel handled by the fast gather
 constexpr int DG_PROW = 8;          // ints per pixel row of the tap table (32 bytes, int4-aligned)
 
+// Raw w slots of the weight formatters (none on the workspace path).
+template <typename T>
+inline __host__ __device__ int dgrad_wraw_bytes(const TcDgradGeom& g)
+{
+    return g.packed ? 0 : DG_NWF * WRAW * dgrad_wraw_warp_bytes<T>(g.KTp);
+}
+
 template <typename T>
 inline int dgrad_smem(const ConvParams& p, const TcDgradGeom& g)
 {
-    return 1024 + g.nw * g.w_tile + DG_TM * DG_DSTR * 4 + 16 + (p.H + p.W) * (1 + g.rmax) * 8 + 16 +
-           p.HW * DG_PROW * 4 + int(sizeof(DgBars)) + 16;
+    return 1024 + g.nw * g.w_tile + dgrad_wraw_bytes<T>(g) + DG_TM * DG_DSTR * 4 + 16 + (p.H + p.W) * (1 + g.rmax) * 8 +
+           16 + p.HW * DG_PROW * 4 + int(sizeof(DgBars)) + 16;
 }
 
-template <typename T>
-inline size_t dgrad_packed_bytes(const TcDgradGeom& g)
-{
-    return size_t(g.nkt) * g.nch * g.w_tile;
-}
-
-template <typename T, bool RELU, int SWZ>
+template <typename T, bool RELU>
 __global__ void __launch_bounds__(DG_THREADS, 1)
-dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const unsigned char* __restrict__ wpack,
-                const T* __restrict__ y, T* __restrict__ dx, const TcDgradGeom geo)
+dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const T* __restrict__ w,
+                const unsigned char* __restrict__ wpack, const T* __restrict__ y, T* __restrict__ dx,
+                const TcDgradGeom geo)
 {
     using Tr = TcTraits<T>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = align1024(smem_raw);
+    // Layout: weight stages | raw w slots (DG_NWF warps x WRAW) | Ds | row, column, pixel tap tables | barriers
     unsigned char* wring = smem;
-    float* Ds = reinterpret_cast<float*>(wring + geo.nw * geo.w_tile);
+    unsigned char* wraw = wring + geo.nw * geo.w_tile;
+    float* Ds = reinterpret_cast<float*>(wraw + dgrad_wraw_bytes<T>(geo));
     const int R1 = 1 + geo.rmax;
     int2* rtab = reinterpret_cast<int2*>(Ds + DG_TM * DG_DSTR + 4);  // 4 floats: the zero word
     int2* ctab = rtab + p.H * R1;
@@ -1485,7 +1728,7 @@ dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const unsigned cha
     }
     if (tid == 0) {
         for (int i = 0; i < geo.nw; ++i) {
-            mbar_init(smem_u32(&bars->w_full[i]), 1);
+            mbar_init(smem_u32(&bars->w_full[i]), geo.packed ? 1 : DG_NWF);
             mbar_init(smem_u32(&bars->w_empty[i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -1503,6 +1746,8 @@ dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const unsigned cha
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tslot;
+    // Nothing above touches global memory: the previous kernel on the stream may still run.
+    grid_dep_wait();
     // Work item wi = (sample tile wi % ntiles, k-tile range wi / ntiles).
     const int nwork = geo.ntiles * geo.ktsplit;
     auto ktrange = [&](int wi, int& lo, int& hi) {
@@ -1510,10 +1755,9 @@ dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const unsigned cha
         hi = min(geo.nkt, lo + geo.kt_per);
     };
 
-    if (warp == 1) {
-        // ---------------- w producer ----------------
-        if (lane == 0) {
-            grid_dep_wait();  // the packed weights come from the kernel launched just before
+    if (warp >= DG_WF0 && warp < DG_WF0 + DG_NWF && geo.packed) {
+        // ---------------- W^T stages from the packed image (workspace path) ----------------
+        if (warp == DG_WF0 && lane == 0) {
             RingPos wp;
             bool ok = true;
             for (int wi = blockIdx.x; wi < nwork && ok && !*abort_flag; wi += gridDim.x) {
@@ -1533,7 +1777,62 @@ dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const unsigned cha
             }
         }
         __syncwarp();
-    } else if (warp == FV_MMA_WARP) {
+    } else if (warp >= DG_WF0 && warp < DG_WF0 + DG_NWF) {
+        // ---------------- weight formatters ----------------
+        // The warp's tile sequence (work item, k-tile, oc chunk); the copies of the next tile
+        // are in flight while the current one is formatted.
+        const int wf = warp - DG_WF0;
+        const uint32_t w_u32 = smem_u32(wring), lo_off = uint32_t(geo.KTp * ROWB);
+        const uint32_t slot_bytes = uint32_t(dgrad_wraw_warp_bytes<T>(geo.KTp));
+        const uint32_t slot0 = smem_u32(wraw) + uint32_t(wf * WRAW) * slot_bytes;
+        struct Seq { int wi, kt, kt_hi, ch; };
+        auto first = [&](Seq& s, int wi) -> bool {
+            if (wi >= nwork) return false;
+            int lo;
+            ktrange(wi, lo, s.kt_hi);
+            s.wi = wi;
+            s.kt = lo;
+            s.ch = 0;
+            return true;
+        };
+        auto advance = [&](Seq& s) -> bool {
+            if (++s.ch < geo.nch) return true;
+            s.ch = 0;
+            return ++s.kt < s.kt_hi || first(s, s.wi + int(gridDim.x));
+        };
+        auto k0_of = [&](const Seq& s) { return s.kt * geo.CIC * p.KK; };
+        Seq cur;
+        bool have = first(cur, int(blockIdx.x));
+        if (have) stage_wt_dgrad<T>(slot0, w, p, k0_of(cur), cur.ch * Tr::KC, geo.KTp, wf, lane);
+        cp_async_commit();
+        uint32_t slot = 0;
+        RingPos wp;
+        while (have && !*abort_flag) {
+            Seq nxt = cur;
+            const bool have_nxt = advance(nxt);
+            if (have_nxt)
+                stage_wt_dgrad<T>(slot0 + (slot ^ 1u) * slot_bytes, w, p, k0_of(nxt), nxt.ch * Tr::KC, geo.KTp, wf,
+                                  lane);
+            cp_async_commit();
+            cp_async_wait<1>();  // this lane's copies of the current tile have landed
+            __syncwarp();        // ... and every lane's are visible to the warp
+            if (wp.wrapped && !mbar_wait_or_abort(smem_u32(&bars->w_empty[wp.i]), wp.ph ^ 1u, abort_flag)) {
+                report(const_cast<int*>(abort_flag), 16u);
+                break;
+            }
+            const int mrows = min(geo.CIC, p.IC - cur.kt * geo.CIC) * p.KK;
+            format_wt_dgrad<T>(w_u32 + uint32_t(wp.i * geo.w_tile), lo_off, slot0 + slot * slot_bytes, p, k0_of(cur),
+                               mrows, cur.ch * Tr::KC, geo.KTp, wf, lane);
+            fence_proxy_async_smem();  // the generic-proxy stores, for the tensor core
+            __syncwarp();              // also: every lane is done reading this raw slot
+            if (lane == 0) mbar_arrive(smem_u32(&bars->w_full[wp.i]));
+            wp.next(geo.nw);
+            cur = nxt;
+            have = have_nxt;
+            slot ^= 1u;
+        }
+        cp_async_wait<0>();  // no copy may land after the CTA's shared memory is released
+    } else if (warp == DG_MMA_WARP) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             const uint32_t idesc2 = instr_desc(Tr::fmt, DG_TM, geo.dcols);
@@ -1568,7 +1867,7 @@ dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const unsigned cha
                         const uint32_t wa = w_u32 + wp.i * geo.w_tile;
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            const uint64_t bd = op_desc<SWZ>(wa + kstep_off<SWZ>(j));
+                            const uint64_t bd = op_desc<1>(wa + kstep_off<1>(j));
                             const uint32_t first = (ch == 0 && j == 0) ? 0u : 1u;
                             const uint32_t col = uint32_t(ch * 32 + 8 * j);  // oc columns of this step
                             if constexpr (Tr::split) {
@@ -1588,11 +1887,11 @@ dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const unsigned cha
             }
         }
         __syncwarp();
-    } else if (warp >= 3) {
+    } else if (warp >= DG_FMT0 / 32) {
         // ---------------- formatters + col2im ----------------
-        const int ft = tid - FV_FMT0;       // 0 .. 511
+        const int ft = tid - DG_FMT0;       // 0 .. 511
         const uint32_t ds_u32 = smem_u32(Ds);
-        const int fw = warp - 3;            // 0 .. 15
+        const int fw = warp - DG_FMT0 / 32; // 0 .. 15
         const int qd = warp & 3;            // TMEM lane quarter
         const int sub = fw >> 2;            // quarter of the oc range (G) / of the k range (D)
         const int m = qd * 32 + lane;       // column within the tile
@@ -1816,10 +2115,11 @@ template <> constexpr int dt_of_tc<__nv_bfloat16>() { return DT_BF16; }
 }  // namespace
 
 // Weight-ring depth, x super-chunk length and K ranges of the forward kernel: feasible
-// (shared memory, packed weights and partials within the scratch buffer) and of the lowest
-// estimated time (fwd_cost).
+// (shared memory, including the K-range reduction's partial tile) and of the lowest estimated
+// time (fwd_cost).  `packed`: the workspace path (weight stages bulk-copied from the packed
+// image, no raw w slots).
 template <typename T>
-static bool pick_fwd(const ConvParams& p, const DevInfo& d, FwdGeom& out)
+static bool pick_fwd(const ConvParams& p, const DevInfo& d, bool packed, FwdGeom& out)
 {
     // Per list, the first that fits: the deepest weight ring, then the longest x super-chunk
     // (fewer, larger slab copies); or short super-chunks first, so that K splits into more
@@ -1835,11 +2135,17 @@ static bool pick_fwd(const ConvParams& p, const DevInfo& d, FwdGeom& out)
         for (int i = 0; i < ncfg; ++i) {
             const int* c = pass == 0 ? cfgs[i] : cfgs_split[i];
             FwdGeom g = fwd_geom<T>(p, c[1], c[0], c[2]);
-            if (g.na < 2 || fwd_smem<T>(p, g) > d.smem_optin || fwd_packed_bytes<T>(g) > kScratchBytes) continue;
-            const double t = fwd_set_splits(g, p, d.sms, fwd_packed_bytes<T>(g), kScratchBytes);
-            if (!found || t < best) {
+            g.packed = packed ? 1 : 0;
+            if (g.na < 2 || fwd_smem<T>(p, g) > d.smem_optin) continue;
+            const double t = fwd_set_splits(g, d.sms);
+            if (!fwd_red_fits(g)) {
+                g.splits = 1;
+                g.kc_per = g.nchunks;
+            }
+            const double tt = g.splits > 1 ? t : fwd_cost(g.n_tiles * g.oc_tiles, d.sms, 1, g.nchunks);
+            if (!found || tt < best) {
                 out = g;
-                best = t;
+                best = tt;
                 found = true;
             }
             break;
@@ -1848,62 +2154,53 @@ static bool pick_fwd(const ConvParams& p, const DevInfo& d, FwdGeom& out)
     return found;
 }
 
-bool tc_fwd_ok(const ConvParams& p, int dt, const DevInfo& d)
+bool tc_fwd_ok(const ConvParams& p, int dt, const DevInfo& d, bool packed)
 {
     if (d.cc_major != 10 || p.N <= 0) return false;
     FwdGeom g;
-    return dt == DT_BF16 ? pick_fwd<__nv_bfloat16>(p, d, g) : pick_fwd<float>(p, d, g);
+    return dt == DT_BF16 ? pick_fwd<__nv_bfloat16>(p, d, packed, g) : pick_fwd<float>(p, d, packed, g);
 }
 
-Plan plan_fwd_tc(const ConvParams& p, int dt, const DevInfo& d)
+Plan plan_fwd_tc(const ConvParams& p, int dt, const DevInfo& d, bool packed)
 {
     FwdGeom g;
-    if (dt == DT_BF16) pick_fwd<__nv_bfloat16>(p, d, g);
-    else pick_fwd<float>(p, d, g);
+    if (dt == DT_BF16) pick_fwd<__nv_bfloat16>(p, d, packed, g);
+    else pick_fwd<float>(p, d, packed, g);
     Plan pl;
     pl.algo = ALGO_TC;
-    // weight packing, the implicit GEMM, and with K ranges the sum of their partials
-    pl.launches = g.splits > 1 ? 3 : 2;
+    // one launch (weights formatted in the kernel, K ranges reduced inside each cluster); the
+    // workspace path first packs the weights into the workspace
+    pl.launches = packed ? 2 : 1;
     pl.block = FA_THREADS;
     pl.splits = g.splits;
     pl.variant = ((g.kc_per * 16 + g.xg) * 16 + g.nw) * 8 + g.nraw;
-    pl.grid = std::min(g.n_tiles * g.oc_tiles * g.splits, d.sms);
+    pl.grid = g.splits > 1 ? g.n_tiles * g.oc_tiles * g.splits : std::min(g.n_tiles * g.oc_tiles, d.sms);
     pl.smem = dt == DT_BF16 ? fwd_smem<__nv_bfloat16>(p, g) : fwd_smem<float>(p, g);
+    if (packed) pl.workspace = size_t(g.oc_tiles) * g.nchunks * g.w_bytes;
     return pl;
 }
 
 template <typename T>
 static cudaError_t fwd_tc_t(const Plan& pl, const ConvParams& p, const void* x, const void* w,
-                            const void* bias, void* y, cudaStream_t s)
+                            const void* bias, void* y, void* ws, cudaStream_t s)
 {
     const int v = pl.variant;
     FwdGeom g = fwd_geom<T>(p, (v / 128) % 16, (v / 8) % 16, v % 8);
     g.kc_per = v / 2048;
     g.splits = ceil_div(g.nchunks, g.kc_per);
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    unsigned char* wpack = static_cast<unsigned char*>(stream_scratch(dev, s));
-    if (!wpack) return cudaErrorMemoryAllocation;
-    const size_t units = size_t(g.oc_tiles) * g.nchunks * g.OTp * 8;
-    const int pgrid = int(std::min<size_t>((units + 255) / 256, 4096));
-    pack_fwd_w_kernel<T><<<pgrid, 256, 0, s>>>(p, (const T*)w, wpack, g.nchunks, g.oc_tiles, g.OTp);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    // The weight operand is always in the 128-byte swizzled layout the pack kernel writes.
-    float* part = reinterpret_cast<float*>(wpack + round_up(fwd_packed_bytes<T>(g), size_t(256)));
-#define IG_LAUNCH_FWD_TC(R)                                                                         \
-    do {                                                                                            \
-        e = ensure_smem<fwd_tc_kernel<T, R, 1>>(pl.smem);                                           \
-        if (e == cudaSuccess)                                                                       \
-            e = launch_overlapped(fwd_tc_kernel<T, R, 1>, dim3(pl.grid), dim3(pl.block), pl.smem, s, p,   \
-                                  (const T*)x, (const unsigned char*)wpack, (const T*)bias, (T*)y, part, g); \
-        if (e == cudaSuccess && g.splits > 1) {                                                     \
-            const size_t total = size_t(p.N) * p.OC;                                                \
-            const int rgrid = int(std::min<size_t>((total + 255) / 256, 4096));                     \
-            e = launch_overlapped(fwd_reduce_kernel<T, R>, dim3(rgrid), dim3(256), 0, s, p,           \
-                                  (const float*)part, g.splits, g.oc_tiles * g.OTp, (const T*)bias,   \
-                                  (T*)y);                                                             \
-        }                                                                                           \
+    g.packed = ws ? 1 : 0;
+    cudaError_t e = cudaSuccess;
+    if (ws) {
+        const dim3 pgrid(ceil_div(g.OTp * 8, 256), g.nchunks, g.oc_tiles);
+        pack_fwd_w_kernel<T><<<pgrid, 256, 0, s>>>(p, (const T*)w, (unsigned char*)ws, g.nchunks, g.OTp);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+#define IG_LAUNCH_FWD_TC(R)                                                                                  \
+    do {                                                                                                     \
+        e = ensure_smem<fwd_tc_kernel<T, R>>(pl.smem);                                                       \
+        if (e == cudaSuccess)                                                                                \
+            e = launch_ex(fwd_tc_kernel<T, R>, dim3(pl.grid), dim3(pl.block), pl.smem, s, g.splits, true, p, \
+                          (const T*)x, (const T*)w, (const unsigned char*)ws, (const T*)bias, (T*)y, g);     \
     } while (0)
     if (p.relu) IG_LAUNCH_FWD_TC(true);
     else IG_LAUNCH_FWD_TC(false);
@@ -1912,10 +2209,10 @@ static cudaError_t fwd_tc_t(const Plan& pl, const ConvParams& p, const void* x, 
 }
 
 cudaError_t run_fwd_tc(const Plan& pl, const ConvParams& p, int dt, const void* x, const void* w,
-                       const void* bias, void* y, cudaStream_t s)
+                       const void* bias, void* y, void* ws, cudaStream_t s)
 {
-    return dt == DT_F32 ? fwd_tc_t<float>(pl, p, x, w, bias, y, s)
-                        : fwd_tc_t<__nv_bfloat16>(pl, p, x, w, bias, y, s);
+    return dt == DT_F32 ? fwd_tc_t<float>(pl, p, x, w, bias, y, ws, s)
+                        : fwd_tc_t<__nv_bfloat16>(pl, p, x, w, bias, y, ws, s);
 }
 
 // ---- wgrad ------------------------------------------------------------------------------
@@ -1995,8 +2292,8 @@ static cudaError_t wgrad_tc_t(const Plan& pl, const ConvParams& p, const void* x
     do {                                                                                                   \
         e = ensure_smem<wgrad_tc_kernel<T, R>>(pl.smem);                                                   \
         if (e == cudaSuccess)                                                                              \
-            wgrad_tc_kernel<T, R><<<pl.grid, pl.block, pl.smem, s>>>(p, (const T*)x, (const T*)dy,         \
-                                                                     (const T*)y, (float*)ws, g);          \
+            e = launch_ex(wgrad_tc_kernel<T, R>, dim3(pl.grid), dim3(pl.block), pl.smem, s, 1, true, p,       \
+                          (const T*)x, (const T*)dy, (const T*)y, (float*)ws, g);                          \
     } while (0)
         if (p.relu) IG_LAUNCH_WG_TC(true);
         else IG_LAUNCH_WG_TC(false);
@@ -2016,16 +2313,18 @@ cudaError_t run_wgrad_tc(const Plan& pl, const ConvParams& p, int dt, const void
 
 // ---- d_input ------------------------------------------------------------------------
 // Channels per k-tile: as many as keep KTp within the accumulator limit (128 rows; the fp32
-// accumulator holds hi and lo halves), then the deepest weight ring that fits.
+// accumulator holds hi and lo halves), then the deepest weight ring that fits.  `packed`: the
+// workspace path (no raw w slots).
 template <typename T>
-static bool pick_dgrad(const ConvParams& p, const DevInfo& d, TcDgradGeom& out)
+static bool pick_dgrad(const ConvParams& p, const DevInfo& d, bool packed, TcDgradGeom& out)
 {
     if (p.B <= 0 || p.KK > 128 || p.P > DG_TM) return false;
     for (int cic = std::min(p.IC, 128 / p.KK); cic >= 1; --cic) {
         for (int nw = 4; nw >= 2; --nw) {
             TcDgradGeom g = dgrad_geom<T>(p, cic, nw);
+            g.packed = packed ? 1 : 0;
             if (g.dcols * g.ndb + g.acols * g.nab > 512) continue;
-            if (dgrad_smem<T>(p, g) <= d.smem_optin && dgrad_packed_bytes<T>(g) <= kScratchBytes) {
+            if (dgrad_smem<T>(p, g) <= d.smem_optin) {
                 if (2 * g.ntiles < d.sms) {  // few sample tiles: split the k-tiles too
                     const int want = std::min(g.nkt, d.sms / g.ntiles);
                     g.kt_per = ceil_div(g.nkt, want);
@@ -2039,51 +2338,51 @@ static bool pick_dgrad(const ConvParams& p, const DevInfo& d, TcDgradGeom& out)
     return false;
 }
 
-bool tc_dgrad_ok(const ConvParams& p, int dt, const DevInfo& d)
+bool tc_dgrad_ok(const ConvParams& p, int dt, const DevInfo& d, bool packed)
 {
     if (d.cc_major != 10) return false;
     TcDgradGeom g;
-    return dt == DT_BF16 ? pick_dgrad<__nv_bfloat16>(p, d, g) : pick_dgrad<float>(p, d, g);
+    return dt == DT_BF16 ? pick_dgrad<__nv_bfloat16>(p, d, packed, g) : pick_dgrad<float>(p, d, packed, g);
 }
 
-Plan plan_dgrad_tc(const ConvParams& p, int dt, const DevInfo& d)
+Plan plan_dgrad_tc(const ConvParams& p, int dt, const DevInfo& d, bool packed)
 {
     TcDgradGeom g;
-    if (dt == DT_BF16) pick_dgrad<__nv_bfloat16>(p, d, g);
-    else pick_dgrad<float>(p, d, g);
+    if (dt == DT_BF16) pick_dgrad<__nv_bfloat16>(p, d, packed, g);
+    else pick_dgrad<float>(p, d, packed, g);
     Plan pl;
     pl.algo = ALGO_TC;
-    pl.launches = 2;  // weight packing, then the implicit GEMM + col2im
+    // the implicit GEMM + col2im (weights formatted in the kernel); the workspace path first
+    // packs W^T into the workspace
+    pl.launches = packed ? 2 : 1;
     pl.block = DG_THREADS;
     pl.variant = (g.kt_per * 128 + g.CIC) * 8 + g.nw;
     pl.grid = std::min(g.ntiles * g.ktsplit, d.sms);
     pl.smem = dt == DT_BF16 ? dgrad_smem<__nv_bfloat16>(p, g) : dgrad_smem<float>(p, g);
+    if (packed) pl.workspace = size_t(g.nkt) * g.nch * g.w_tile;
     return pl;
 }
 
 template <typename T>
 static cudaError_t dgrad_tc_t(const Plan& pl, const ConvParams& p, const void* dy, const void* w,
-                              const void* y, void* dx, int, cudaStream_t s)
+                              const void* y, void* dx, void* ws, cudaStream_t s)
 {
     TcDgradGeom g = dgrad_geom<T>(p, (pl.variant / 8) % 128, pl.variant % 8);
     g.kt_per = pl.variant / 1024;
     g.ktsplit = ceil_div(g.nkt, g.kt_per);
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    unsigned char* wpack = static_cast<unsigned char*>(stream_scratch(dev, s));
-    if (!wpack) return cudaErrorMemoryAllocation;
-    const size_t units = size_t(g.nkt) * g.nch * g.KTp * 8;
-    const int pgrid = int(std::min<size_t>((units + 255) / 256, 4096));
-    pack_dgrad_w_kernel<T><<<pgrid, 256, 0, s>>>(p, (const T*)w, wpack, g.nkt, g.nch, g.CIC, g.KTp);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    // The weight operand is always in the 128-byte swizzled layout the pack kernel writes.
-#define IG_LAUNCH_DG_TC(R)                                                                                 \
-    do {                                                                                                   \
-        e = ensure_smem<dgrad_tc_kernel<T, R, 1>>(pl.smem);                                                \
-        if (e == cudaSuccess)                                                                              \
-            e = launch_overlapped(dgrad_tc_kernel<T, R, 1>, dim3(pl.grid), dim3(pl.block), pl.smem, s, p, \
-                                  (const T*)dy, (const unsigned char*)wpack, (const T*)y, (T*)dx, g);      \
+    g.packed = ws ? 1 : 0;
+    cudaError_t e = cudaSuccess;
+    if (ws) {
+        const dim3 pgrid(ceil_div(g.KTp * 8, 256), g.nch, g.nkt);
+        pack_dgrad_w_kernel<T><<<pgrid, 256, 0, s>>>(p, (const T*)w, (unsigned char*)ws, g.nch, g.CIC, g.KTp);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+#define IG_LAUNCH_DG_TC(R)                                                                                   \
+    do {                                                                                                     \
+        e = ensure_smem<dgrad_tc_kernel<T, R>>(pl.smem);                                                     \
+        if (e == cudaSuccess)                                                                                \
+            e = launch_ex(dgrad_tc_kernel<T, R>, dim3(pl.grid), dim3(pl.block), pl.smem, s, 1, true, p,      \
+                          (const T*)dy, (const T*)w, (const unsigned char*)ws, (const T*)y, (T*)dx, g);      \
     } while (0)
     if (p.relu) IG_LAUNCH_DG_TC(true);
     else IG_LAUNCH_DG_TC(false);
@@ -2092,10 +2391,10 @@ static cudaError_t dgrad_tc_t(const Plan& pl, const ConvParams& p, const void* d
 }
 
 cudaError_t run_dgrad_tc(const Plan& pl, const ConvParams& p, int dt, const void* dy, const void* w,
-                         const void* y, void* dx, int sms, cudaStream_t s)
+                         const void* y, void* dx, void* ws, cudaStream_t s)
 {
-    return dt == DT_F32 ? dgrad_tc_t<float>(pl, p, dy, w, y, dx, sms, s)
-                        : dgrad_tc_t<__nv_bfloat16>(pl, p, dy, w, y, dx, sms, s);
+    return dt == DT_F32 ? dgrad_tc_t<float>(pl, p, dy, w, y, dx, ws, s)
+                        : dgrad_tc_t<__nv_bfloat16>(pl, p, dy, w, y, dx, ws, s);
 }
 
 cudaError_t tc_read_status(unsigned* out, bool reset)

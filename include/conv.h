@@ -34,15 +34,13 @@
  *     current CUDA device, owned by the caller; the library keeps no reference
  *     after the call returns.  Base pointers must be 16-byte aligned.  Outputs
  *     must not overlap inputs.
- *   - Scratch: the tensor-core paths of conv_fwd and conv_bwd_data first
- *     repack w into the tensor cores' tile layout (and conv_fwd, when it
- *     splits K, keeps its fp32 partial sums there), and conv_bwd_bias keeps its
- *     per-block partial sums.  They keep one 48 MiB
- *     device buffer for that per (device, stream), allocated with cudaMalloc
- *     on the first such call on that stream and held until
- *     conv_release_scratch() or process exit; make that first call outside
- *     stream capture.  Calls on one stream are ordered by the stream, calls
- *     on different streams use different buffers.  Nothing else allocates.
+ *   - Memory: no entry point allocates.  conv_fwd, conv_fwd_bias, conv_bwd_data
+ *     and conv_bwd_bias use no memory beyond their arguments (their kernels
+ *     format the weights on chip and reduce split sums inside thread-block
+ *     clusters through distributed shared memory); conv_fwd_ws,
+ *     conv_bwd_data_ws and conv_bwd_filter use a workspace the caller sizes with
+ *     the matching *_workspace_size query and owns; conv_bwd_filter_noalloc uses
+ *     a fixed array inside the library.
  *   - Calls are asynchronous on `stream` (0 = legacy default stream): they
  *     enqueue kernels and return; they never synchronise.  Each call
  *     overwrites its whole output (it does not accumulate into it).
@@ -100,7 +98,11 @@ typedef enum {
                              or fp32 as three tf32 products)                          */
 } conv_algo_t;
 
-typedef enum { CONV_OP_FWD = 0, CONV_OP_BWD_DATA = 1, CONV_OP_BWD_FILTER = 2, CONV_OP_BWD_BIAS = 3 } conv_op_t;
+typedef enum {
+    CONV_OP_FWD = 0, CONV_OP_BWD_DATA = 1, CONV_OP_BWD_FILTER = 2, CONV_OP_BWD_BIAS = 3,
+    CONV_OP_FWD_WS = 4,      /* conv_fwd_ws / conv_fwd_bias with a workspace (conv_query only) */
+    CONV_OP_BWD_DATA_WS = 5  /* conv_bwd_data_ws (conv_query only)                           */
+} conv_op_t;
 
 /* Forward:  y = act(conv(x, w)).
  *   x: (B,IC,H,W)   w: (OC,IC,K,K)   y: (B,OC,OH,OW), written.
@@ -116,12 +118,35 @@ int conv_fwd(const conv_desc_t* desc, const void* x, const void* w, void* y,
 int conv_fwd_bias(const conv_desc_t* desc, const void* x, const void* w, const void* bias, void* y,
                   conv_stream_t stream);
 
+/* The forward with a workspace: the same result as conv_fwd / conv_fwd_bias, bit for bit
+ * (bias may be NULL: no bias).  With a workspace the tensor-core path first packs w once
+ * into the operand tiles' exact shared-memory image (a small kernel), and the implicit GEMM
+ * then fetches each tile with one bulk copy instead of formatting w in every CTA, which is
+ * faster whenever the CTAs together would format w many times over (PufferLib PR #522's
+ * layer-1 shape at B = 1024 and above).
+ *   workspace: device buffer of at least conv_fwd_workspace_size(desc) bytes, 16-byte
+ *   aligned, owned by the caller; contents on entry are ignored and on return are
+ *   unspecified.  May be NULL when the size is 0 (then the call is conv_fwd's).
+ *   CONV_ERR_WORKSPACE if it is NULL or smaller than the queried size. */
+size_t conv_fwd_workspace_size(const conv_desc_t* desc);
+int conv_fwd_ws(const conv_desc_t* desc, const void* x, const void* w, const void* bias, void* y,
+                void* workspace, size_t workspace_bytes, conv_stream_t stream);
+
 /* Data gradient (d_input):  dx = conv^T(g, w), g = dy masked by y > 0 when relu.
  *   dy: (B,OC,OH,OW)  w: (OC,IC,K,K)  y: (B,OC,OH,OW) forward output, required
  *   when desc->relu (the mask source), ignored otherwise (may be NULL)
  *   dx: (B,IC,H,W), written. */
 int conv_bwd_data(const conv_desc_t* desc, const void* dy, const void* w, const void* y,
                   void* dx, conv_stream_t stream);
+
+/* d_input with a workspace: the same result as conv_bwd_data, bit for bit; the tensor-core
+ * path packs w^T once into the workspace (see conv_fwd_ws).
+ *   workspace: at least conv_bwd_data_workspace_size(desc) bytes, 16-byte aligned, owned by
+ *   the caller, contents ignored on entry and unspecified on return; may be NULL when the
+ *   size is 0.  CONV_ERR_WORKSPACE if it is NULL or too small. */
+size_t conv_bwd_data_workspace_size(const conv_desc_t* desc);
+int conv_bwd_data_ws(const conv_desc_t* desc, const void* dy, const void* w, const void* y, void* dx,
+                     void* workspace, size_t workspace_bytes, conv_stream_t stream);
 
 /* Bytes of device workspace conv_bwd_filter needs for this descriptor on the
  * current device (split-K partial sums), or 0 if it needs none or the
@@ -141,21 +166,19 @@ int conv_bwd_filter(const conv_desc_t* desc, const void* x, const void* dy, cons
                     void* dw, void* workspace, size_t workspace_bytes, conv_stream_t stream);
 
 /* Bias gradient:  db[oc] = sum over b, oh, ow of g (g = dy masked by y > 0 when
- * relu), accumulated in fp32 and rounded once to the dtype.  Two kernels: the
- * first gives each CTA a contiguous range of samples and sums each output
- * position (oc, oh, ow) down its rows (in R interleaved row lanes, each in
- * ascending b), then adds, per channel, its positions in ascending (oh, ow),
- * each over the row lanes in ascending order; the second adds the CTAs'
- * per-channel sums in a fixed order (warp w of 32 takes ranges w, w + 32, ...
- * in ascending order, then the 32 warp sums are added in ascending order).  The
- * partial sums live in the per-stream scratch buffer (see Scratch above; this
- * call allocates it if it is the first on its stream).
- * A shape whose OC*OH*OW row is too long for the first kernel's shared-memory
- * window (more than 12288 positions per output channel) runs a one-warp-per-
- * channel kernel instead (the same result up to summation order).
+ * relu), accumulated in fp32 and rounded once to the dtype.  One kernel: the
+ * channels are cut into windows and the batch into R contiguous sample ranges
+ * (R a power of two, at most 8); the CTA of (window, range) sums each output
+ * position (oc, oh, ow) of its window down its rows (in interleaved row lanes,
+ * each in ascending b), then adds, per channel, its positions in ascending
+ * (oh, ow), each over the row lanes in ascending order; the R CTAs of a window
+ * form a thread-block cluster whose rank-0 CTA adds the R per-channel sums in
+ * ascending range order through distributed shared memory.  No global scratch.
+ * A shape whose OH*OW is longer than 12288 positions runs a one-warp-per-channel
+ * kernel instead (the same result up to summation order).
  *   dy: (B,OC,OH,OW)  y: forward output, required when desc->relu, ignored
  *   otherwise (may be NULL)  db: (OC), written (zeros when B = 0).
- * conv_query(CONV_OP_BWD_BIAS, ...) reports the plan; conv_set_algo accepts
+ * conv_query(CONV_OP_BWD_BIAS, ...) reports the plan (splits = R); conv_set_algo accepts
  * CONV_ALGO_AUTO and CONV_ALGO_DIRECT (the one-warp-per-channel kernel) for it. */
 int conv_bwd_bias(const conv_desc_t* desc, const void* dy, const void* y, void* db,
                   conv_stream_t stream);
@@ -243,10 +266,6 @@ int conv_device_status(uint32_t* status, int reset);
  * usable.  max_sleeps must be in [1, 10^6] (CONV_ERR_UNSUPPORTED otherwise). */
 #define CONV_STATUS_WAIT_SELFTEST (1u << 30)
 int conv_wait_selftest(uint32_t max_sleeps, conv_stream_t stream);
-
-/* Free the per-(device, stream) packed-weight buffers (synchronises each
- * device that holds one).  Later calls allocate again as needed. */
-int conv_release_scratch(void);
 
 /* Write `bytes` bytes of `buf` (device memory, 16-byte aligned, bytes a
  * multiple of 16) on `stream`, evicting earlier data from L2; benchmarks use

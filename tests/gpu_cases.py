@@ -54,6 +54,20 @@ class Case:
         binding.conv_bwd_data(self.desc, self.dy, self.w, y if self.relu else None, dx)
         return dx
 
+    def gpu_fwd_ws(self):
+        """conv_fwd_ws: the forward with a caller-provided workspace (packed weights)."""
+        OH, OW = binding.out_dims(self.desc)
+        y = torch.empty((self.B, self.OC, OH, OW), dtype=TORCH_DT[self.dtype], device="cuda")
+        ws = torch.empty(max(binding.conv_fwd_workspace_size(self.desc), 16), dtype=torch.uint8, device="cuda")
+        binding.conv_fwd_ws(self.desc, self.x, self.w, None, y, ws)
+        return y
+
+    def gpu_dgrad_ws(self, y):
+        dx = torch.empty((self.B, self.IC, self.H, self.W), dtype=TORCH_DT[self.dtype], device="cuda")
+        ws = torch.empty(max(binding.conv_bwd_data_workspace_size(self.desc), 16), dtype=torch.uint8, device="cuda")
+        binding.conv_bwd_data_ws(self.desc, self.dy, self.w, y if self.relu else None, dx, ws)
+        return dx
+
     def gpu_wgrad(self, y):
         dw = torch.empty((self.OC, self.IC, self.K, self.K), dtype=TORCH_DT[self.dtype], device="cuda")
         n = binding.conv_bwd_filter_workspace_size(self.desc)

@@ -66,6 +66,10 @@ def test_invalid_descriptor(L, bad):
     assert L.conv_bwd_filter_workspace_size(ctypes.byref(d)) == 0
     assert L.conv_fwd_bias(ctypes.byref(d), fake, fake, fake, fake, None) == -2
     assert L.conv_bwd_bias(ctypes.byref(d), fake, fake, fake, None) == -2
+    assert L.conv_fwd_ws(ctypes.byref(d), fake, fake, None, fake, fake, 1 << 30, None) == -2
+    assert L.conv_bwd_data_ws(ctypes.byref(d), fake, fake, fake, fake, fake, 1 << 30, None) == -2
+    assert L.conv_fwd_workspace_size(ctypes.byref(d)) == 0
+    assert L.conv_bwd_data_workspace_size(ctypes.byref(d)) == 0
     oh, ow = ctypes.c_int32(), ctypes.c_int32()
     assert L.conv_out_dims(ctypes.byref(d), ctypes.byref(oh), ctypes.byref(ow)) == -2
 
@@ -101,6 +105,12 @@ def test_null_and_alignment_checked_before_cuda(L):
     assert L.conv_bwd_bias(ctypes.byref(d), ok, ok, odd, None) == -4
     assert L.conv_bwd_bias(ctypes.byref(d), odd, ok, ok, None) == -4
     assert L.conv_bwd_bias(ctypes.byref(d), ok, odd, ok, None) == -4
+    # The workspace-taking forward / d_input: the same checks, plus the workspace's alignment.
+    assert L.conv_fwd_ws(ctypes.byref(d), None, ok, None, ok, ok, 1 << 30, None) == -1
+    assert L.conv_fwd_ws(ctypes.byref(d), ok, ok, None, ok, odd, 1 << 30, None) == -4
+    assert L.conv_fwd_ws(ctypes.byref(d), ok, ok, odd, ok, ok, 1 << 30, None) == -4
+    assert L.conv_bwd_data_ws(ctypes.byref(d), ok, ok, None, ok, ok, 1 << 30, None) == -1  # relu needs y
+    assert L.conv_bwd_data_ws(ctypes.byref(d), ok, ok, ok, ok, odd, 1 << 30, None) == -4
 
 
 def test_empty_batch_is_a_no_op(L):
@@ -117,7 +127,9 @@ def test_wait_selftest_arguments_checked_before_cuda(L):
 
 
 def test_set_algo_validation(L):
-    assert L.conv_set_algo(4, 0) == -3
+    assert L.conv_set_algo(6, 0) == -3
+    assert L.conv_set_algo(4, 0) == 0   # the workspace-taking forward shares the forward's choice
+    assert L.conv_set_algo(5, 0) == 0   # ... and d_input's
     assert L.conv_set_algo(-1, 0) == -3
     assert L.conv_set_algo(0, 9) == -3
     assert L.conv_set_algo(0, 0) == 0

@@ -1,15 +1,19 @@
 """The planner on the host, for a described GB300 (152 SMs, 227 KB opt-in shared memory,
 compute capability 10.3) and for devices without the tensor-core family: every plan the
-library would launch stays inside the hardware limits and the scratch buffer, the
-tensor-core forward splits K only when its column tiles fill fewer than half the SMs, and
-forcing a family is honoured.  No GPU: conv_query_for_device makes no CUDA call."""
+library would launch stays inside the hardware limits, only wgrad asks for memory beyond its
+arguments (the caller's workspace), the tensor-core forward splits K only when its column
+tiles fill fewer than half the SMs and then into one thread-block cluster of at most 8 CTAs
+per tile, and forcing a family is honoured.  No GPU: conv_query_for_device makes no CUDA
+call."""
 import pytest
 
 from implicit_gemm_conv2d_gb300 import binding
 
 GB300 = binding.GB300
-SCRATCH = 48 << 20
-OPS = (binding.OP_FWD, binding.OP_BWD_DATA, binding.OP_BWD_FILTER, binding.OP_BWD_BIAS)
+MAX_CLUSTER = 8
+OPS = (binding.OP_FWD, binding.OP_BWD_DATA, binding.OP_BWD_FILTER, binding.OP_BWD_BIAS, binding.OP_FWD_WS,
+       binding.OP_BWD_DATA_WS)
+WS_OPS = (binding.OP_BWD_FILTER, binding.OP_FWD_WS, binding.OP_BWD_DATA_WS)
 
 SHAPES = {
     "L1": (59, 128, 11, 15, 5, 3, 1),
@@ -54,15 +58,28 @@ def test_plans_within_limits(name, dtype):
             assert q["grid"] >= 1, where
             if q["algo"] == binding.ALGO_TC:
                 assert q["grid"] <= GB300["sms"], where
+            if op not in WS_OPS:
+                assert q["workspace"] == 0, where
+            if op in (binding.OP_FWD_WS, binding.OP_BWD_DATA_WS):
+                # the workspace path packs the weights into the workspace, then the main kernel
+                if q["algo"] == binding.ALGO_TC:
+                    assert q["launches"] == 2 and q["workspace"] > 0, where
+                else:
+                    assert q["workspace"] == 0, where
             if op == binding.OP_FWD and q["algo"] == binding.ALGO_TC:
-                assert q["splits"] >= 1 and q["launches"] == (3 if q["splits"] > 1 else 2), where
+                # one launch: weights formatted in the kernel, K ranges reduced in a cluster
+                assert q["launches"] == 1 and 1 <= q["splits"] <= MAX_CLUSTER, where
+                if q["splits"] > 1:
+                    assert q["grid"] % q["splits"] == 0, where
+            if op == binding.OP_BWD_DATA and q["algo"] == binding.ALGO_TC:
+                assert q["launches"] == 1, where
             if op == binding.OP_BWD_FILTER and q["splits"] > 0:
                 assert q["workspace"] >= q["splits"] * OC * IC * K * K * 4, where
             if op == binding.OP_BWD_BIAS:
                 if q["algo"] == binding.ALGO_FFMA:
-                    assert q["block"] <= 512 and q["smem_bytes"] <= 48 * 1024, where
-                    assert 1 <= q["splits"] <= 1024 and q["splits"] * OC * 4 <= SCRATCH, where
-                    assert q["launches"] == 2, where
+                    assert q["block"] <= 256 and q["smem_bytes"] <= 48 * 1024, where
+                    assert q["splits"] in (1, 2, 4, 8) and q["grid"] % q["splits"] == 0, where
+                    assert q["launches"] == 1, where
                 else:
                     assert q["algo"] == binding.ALGO_DIRECT and OH * OW > 12288, where
 
@@ -79,9 +96,10 @@ def test_forward_k_ranges_only_with_few_column_tiles(dtype):
     # layer 1 at B = 1024: 12288 columns = 96 tiles of 128, more than half of 152 SMs
     q = plan(binding.OP_FWD, 1024, SHAPES["L1"], dtype)
     assert q["splits"] == 1 and q["grid"] == 96
-    # layer 2 at B = 1024: 2048 columns = 16 tiles: K splits, the work items fill the SMs
+    # layer 2 at B = 1024: 2048 columns = 16 tiles: K splits into a cluster of ranges per
+    # tile, one CTA per (tile, range), and the work items fill at least half the SMs
     q = plan(binding.OP_FWD, 1024, SHAPES["L2"], dtype)
-    assert q["splits"] > 1 and 16 * q["splits"] >= GB300["sms"] // 2
+    assert 1 < q["splits"] <= MAX_CLUSTER and q["grid"] == 16 * q["splits"] >= GB300["sms"] // 2
     # large batches never split
     for name in ("L1", "L2"):
         assert plan(binding.OP_FWD, 16384, SHAPES[name], dtype)["splits"] == 1
@@ -98,6 +116,18 @@ def test_no_tensor_core_plan_without_the_hardware():
             assert q["smem_bytes"] <= small["smem_optin"], (op, name, q)
             if name in ("L1", "L2"):  # their tensor-core stages need more than 48 KB
                 assert q["algo"] != binding.ALGO_TC, (op, name, q)
+
+
+def test_workspace_path_matches_the_plain_plan():
+    # the same family (the packed stages need no raw w slots, so the workspace path may pick a
+    # deeper ring), with a workspace for the packed image
+    for name in ("L1", "L2"):
+        for dtype in (binding.F32, binding.BF16):
+            for B in (37, 1024, 16384):
+                for plain_op, ws_op in ((binding.OP_FWD, binding.OP_FWD_WS), (binding.OP_BWD_DATA, binding.OP_BWD_DATA_WS)):
+                    a, b = plan(plain_op, B, SHAPES[name], dtype), plan(ws_op, B, SHAPES[name], dtype)
+                    assert a["algo"] == b["algo"] == binding.ALGO_TC, (name, dtype, B, a, b)
+                    assert b["workspace"] > 0 and a["workspace"] == 0, (name, dtype, B, a, b)
 
 
 def test_forced_family_is_honoured():
