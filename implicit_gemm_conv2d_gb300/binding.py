@@ -54,7 +54,7 @@ EXPORTS = ["conv_fwd", "conv_bwd_data", "conv_bwd_filter_workspace_size", "conv_
            "conv_fastdivmod_check", "conv_l2_flush", "conv_version", "conv_bwd_filter_noalloc",
            "conv_device_status", "conv_fwd_bias", "conv_bwd_bias",
            "conv_wait_selftest", "conv_query_for_device", "conv_fwd_workspace_size", "conv_fwd_ws",
-           "conv_bwd_data_workspace_size", "conv_bwd_data_ws"]
+           "conv_bwd_data_workspace_size", "conv_bwd_data_ws", "conv_bwd_filter_bias"]
 STATUS_WAIT_SELFTEST = 1 << 30
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -101,6 +101,7 @@ def lib():
         L.conv_bwd_data_workspace_size.argtypes = [dp]
         L.conv_bwd_data_workspace_size.restype = sz
         L.conv_bwd_data_ws.argtypes = [dp, vp, vp, vp, vp, vp, sz, vp]
+        L.conv_bwd_filter_bias.argtypes = [dp, vp, vp, vp, vp, vp, vp, sz, vp]
         _lib = L
         return L
 
@@ -188,6 +189,13 @@ def conv_bwd_filter(desc: ConvDesc, x, dy, y, dw, workspace, stream=None) -> Non
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().conv_bwd_filter(ctypes.byref(desc), _ptr(x), _ptr(dy), _ptr(y), _ptr(dw),
                                  _ptr(workspace), nbytes, _stream(stream)), "conv_bwd_filter")
+
+
+def conv_bwd_filter_bias(desc: ConvDesc, x, dy, y, dw, db, workspace, stream=None) -> None:
+    """Weight and bias gradients in one pass over g (the same workspace as conv_bwd_filter)."""
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().conv_bwd_filter_bias(ctypes.byref(desc), _ptr(x), _ptr(dy), _ptr(y), _ptr(dw), _ptr(db),
+                                      _ptr(workspace), nbytes, _stream(stream)), "conv_bwd_filter_bias")
 
 
 def conv_bwd_filter_noalloc(desc: ConvDesc, x, dy, y, dw, stream=None) -> None:

@@ -360,15 +360,20 @@ size_t conv_bwd_filter_workspace_size(const conv_desc_t* desc)
     return pl.workspace;
 }
 
-int conv_bwd_filter(const conv_desc_t* desc, const void* x, const void* dy, const void* y, void* dw,
-                    void* workspace, size_t workspace_bytes, conv_stream_t stream)
+namespace {
+
+// Weight gradient, and with db != nullptr the bias gradient too (fused into the tensor-core
+// wgrad: one read of dy and y for both; the other families run the bias-gradient kernel after).
+int wgrad_impl(const conv_desc_t* desc, const void* x, const void* dy, const void* y, void* dw, void* db,
+               void* workspace, size_t workspace_bytes, conv_stream_t stream)
 {
     ConvParams p;
     int rc = make_params(desc, p);
     if (rc != CONV_OK) return rc;
     if (!dw) return CONV_ERR_NULL;
     if (p.B > 0 && (!x || !dy || (p.relu && !y))) return CONV_ERR_NULL;
-    if (!aligned16(dw) || (p.B > 0 && (!aligned16(x) || !aligned16(dy) || (p.relu && !aligned16(y)))))
+    if (!aligned16(dw) || (db && !aligned16(db)) ||
+        (p.B > 0 && (!aligned16(x) || !aligned16(dy) || (p.relu && !aligned16(y)))))
         return CONV_ERR_ALIGN;
     if (workspace && !aligned16(workspace)) return CONV_ERR_ALIGN;
     DevInfo d;
@@ -377,10 +382,31 @@ int conv_bwd_filter(const conv_desc_t* desc, const void* x, const void* dy, cons
     if ((rc = choose_wgrad(p, desc->dtype, d, pl)) != CONV_OK) return rc;
     if (pl.workspace > 0 && (!workspace || workspace_bytes < pl.workspace)) return CONV_ERR_WORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (pl.algo == ALGO_DIRECT) return cuda_status(run_wgrad_direct(pl, p, desc->dtype, x, dy, y, dw, s));
     if (pl.algo == ALGO_TC)
-        return cuda_status(run_wgrad_tc(pl, p, desc->dtype, x, dy, y, dw, workspace, d.sms, s));
-    return cuda_status(run_wgrad_ffma(pl, p, desc->dtype, x, dy, y, dw, workspace, s));
+        return cuda_status(run_wgrad_tc(pl, p, desc->dtype, x, dy, y, dw, workspace, db, s));
+    cudaError_t e = pl.algo == ALGO_DIRECT ? run_wgrad_direct(pl, p, desc->dtype, x, dy, y, dw, s)
+                                           : run_wgrad_ffma(pl, p, desc->dtype, x, dy, y, dw, workspace, s);
+    if (e == cudaSuccess && db) {
+        Plan bp;
+        if ((rc = choose_bgrad(p, desc->dtype, d, bp)) != CONV_OK) return rc;
+        e = run_bgrad(bp, p, desc->dtype, dy, y, db, s);
+    }
+    return cuda_status(e);
+}
+
+}  // namespace
+
+int conv_bwd_filter(const conv_desc_t* desc, const void* x, const void* dy, const void* y, void* dw,
+                    void* workspace, size_t workspace_bytes, conv_stream_t stream)
+{
+    return wgrad_impl(desc, x, dy, y, dw, nullptr, workspace, workspace_bytes, stream);
+}
+
+int conv_bwd_filter_bias(const conv_desc_t* desc, const void* x, const void* dy, const void* y, void* dw, void* db,
+                         void* workspace, size_t workspace_bytes, conv_stream_t stream)
+{
+    if (!db && desc) return CONV_ERR_NULL;
+    return wgrad_impl(desc, x, dy, y, dw, db, workspace, workspace_bytes, stream);
 }
 
 uint64_t conv_fastdivmod_check(uint32_t d, uint32_t lo, uint32_t hi)

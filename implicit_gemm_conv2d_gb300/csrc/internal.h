@@ -66,9 +66,11 @@ cudaError_t run_wgrad_direct(const Plan&, const ConvParams&, int dt, const void*
                              const void* dy, const void* y, void* dw, cudaStream_t s);
 // Deterministic split-K sum: dw = sum_{s < splits} ws[s] (fp32 partials, row
 // stride kpad), rounded once to the dtype.  splits == 0 writes zeros.  `overlapped`:
-// launched to overlap the kernel that writes ws (it waits for that kernel itself).
+// launched to overlap the kernel that writes ws (it waits for that kernel itself).  With db:
+// also db[oc] = sum_{q < nbp} bpart[q][oc] (nbp == 0 writes zeros).
 cudaError_t run_wgrad_reduce(const ConvParams&, int dt, const float* ws, int splits, int kpad,
-                             void* dw, cudaStream_t s, bool overlapped = false);
+                             void* dw, cudaStream_t s, bool overlapped = false, const float* bpart = nullptr,
+                             int nbp = 0, void* db = nullptr);
 cudaError_t run_l2_flush(void* buf, size_t bytes, cudaStream_t s);
 
 // Dynamic shared memory above 48 KB needs a per-kernel opt-in on every device;
@@ -148,8 +150,10 @@ cudaError_t run_fwd_tc(const Plan&, const ConvParams&, int dt, const void* x, co
                        const void* bias, void* y, void* ws, cudaStream_t s);
 bool tc_wgrad_ok(const ConvParams& p, int dt, const DevInfo& d);
 Plan plan_wgrad_tc(const ConvParams& p, int dt, const DevInfo& d);
+// db != nullptr: also the bias gradient, from the same loads of g (its partial channel sums go
+// to the workspace's tail, see plan_wgrad_tc).
 cudaError_t run_wgrad_tc(const Plan&, const ConvParams&, int dt, const void* x, const void* dy,
-                         const void* y, void* dw, void* ws, int sms, cudaStream_t s);
+                         const void* y, void* dw, void* ws, void* db, cudaStream_t s);
 bool tc_dgrad_ok(const ConvParams& p, int dt, const DevInfo& d, bool packed);
 Plan plan_dgrad_tc(const ConvParams& p, int dt, const DevInfo& d, bool packed);
 cudaError_t run_dgrad_tc(const Plan&, const ConvParams&, int dt, const void* dy, const void* w,

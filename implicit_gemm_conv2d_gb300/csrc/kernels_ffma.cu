@@ -456,12 +456,24 @@ wgrad_ffma_kernel(const ConvParams p, const T* __restrict__ x, const T* __restri
     }
 }
 
+// Also, when db is given, the bias gradient: db[oc] = sum of the nbp per-(split, lane group)
+// partial channel sums bpart[q][oc] in ascending q (the tensor-core wgrad accumulates them
+// from the masked g it already loads).
 template <typename T>
 __global__ void wgrad_reduce_kernel(const float* __restrict__ ws, int splits, int kpad, int OC,
-                                    int Kred, FastDivmod dm_kred, T* __restrict__ dw)
+                                    int Kred, FastDivmod dm_kred, T* __restrict__ dw, const float* __restrict__ bpart,
+                                    int nbp, T* __restrict__ db)
 {
     // When launched to overlap the partials kernel: wait for it (at once otherwise).
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (db) {
+        const int oc = blockIdx.x * blockDim.x + threadIdx.x;  // the grid covers OC*Kred >= OC threads
+        if (oc < OC) {
+            float s = 0.f;
+            for (int q = 0; q < nbp; ++q) s += __ldcg(bpart + size_t(q) * OC + oc);
+            Elem<T>::st(db + oc, s);
+        }
+    }
     const int total = OC * Kred;
     const size_t sstride = size_t(OC) * kpad;
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
@@ -747,24 +759,16 @@ cudaError_t run_wgrad_ffma(const Plan& pl, const ConvParams& p, int dt, const vo
 }
 
 cudaError_t run_wgrad_reduce(const ConvParams& p, int dt, const float* ws, int splits, int kpad,
-                             void* dw, cudaStream_t s, bool overlapped)
+                             void* dw, cudaStream_t s, bool overlapped, const float* bpart, int nbp, void* db)
 {
     const int total = p.OC * p.Kred;
     const int grid = std::max(1, std::min(4096, ceil_div(total, 256)));
     const FastDivmod dm(uint32_t(p.Kred));
-    if (overlapped) {
-        return dt == DT_F32
-                   ? launch_overlapped(wgrad_reduce_kernel<float>, dim3(grid), dim3(256), 0, s, ws, splits, kpad,
-                                       p.OC, p.Kred, dm, (float*)dw)
-                   : launch_overlapped(wgrad_reduce_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, s, ws, splits,
-                                       kpad, p.OC, p.Kred, dm, (__nv_bfloat16*)dw);
-    }
     if (dt == DT_F32)
-        wgrad_reduce_kernel<float><<<grid, 256, 0, s>>>(ws, splits, kpad, p.OC, p.Kred, dm, (float*)dw);
-    else
-        wgrad_reduce_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(ws, splits, kpad, p.OC, p.Kred, dm,
-                                                               (__nv_bfloat16*)dw);
-    return cudaGetLastError();
+        return launch_ex(wgrad_reduce_kernel<float>, dim3(grid), dim3(256), 0, s, 1, overlapped, ws, splits, kpad,
+                         p.OC, p.Kred, dm, (float*)dw, bpart, nbp, (float*)db);
+    return launch_ex(wgrad_reduce_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, s, 1, overlapped, ws, splits,
+                     kpad, p.OC, p.Kred, dm, (__nv_bfloat16*)dw, bpart, nbp, (__nv_bfloat16*)db);
 }
 
 template <typename T>

@@ -1085,7 +1085,7 @@ inline int wgrad_smem(const TcWgradGeom& g)
 template <typename T, bool RELU>
 __global__ void __launch_bounds__(WG_THREADS, 1)
 wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict__ dy,
-                const T* __restrict__ y, float* __restrict__ ws, const TcWgradGeom geo)
+                const T* __restrict__ y, float* __restrict__ ws, float* __restrict__ bpart, const TcWgradGeom geo)
 {
     using Tr = TcTraits<T>;
     constexpr int ES = int(sizeof(T));
@@ -1345,6 +1345,11 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
             uint32_t t = 0;
             for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++t) {
                 const TileInfo ti = decode(tile);
+                // The bias gradient rides on the first k-tile of each split (one per (split, oc
+                // tile)): the sum of this thread's masked g values, chunk by chunk in ascending
+                // order (k-tile 0 starts at chunk 0), each chunk's values in ascending column.
+                const bool bias_tile = bpart != nullptr && ti.k0 == 0;
+                float bsum = 0.f;
                 bool ok = true;
                 for (int kc = 0; kc < ti.nchunks; ++kc, rp.next(geo.raws)) {
                     if (!mbar_wait_or_abort(smem_u32(&bars->raw_full[rp.i]), rp.ph, abort_flag)) {
@@ -1426,15 +1431,14 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
                                 v[e] = d;
                             }
                         }
+                        if (bias_tile) {
+#pragma unroll
+                            for (int e = 0; e < NG; ++e) bsum += __uint_as_float(ES == 4 ? v[e] : (v[e] << 16));
+                        }
                         if constexpr (Tr::split) {
                             uint32_t hi[8], lo[8];
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const float f = __uint_as_float(v[e]);
-                                const float h = to_tf32(f);
-                                hi[e] = __float_as_uint(h);
-                                lo[e] = __float_as_uint(f - h);
-                            }
+                            for (int e = 0; e < 8; ++e) split_tf32(v[e], hi[e], lo[e]);
                             tmem_st8(col + uint32_t(g * NG), hi);
                             tmem_st8(col + uint32_t(Tr::KC + g * NG), lo);
                         } else {
@@ -1453,6 +1457,8 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
                     }
                     ap.next(geo.na);
                 }
+                if (ok && bias_tile && m < ti.rows)
+                    bpart[(size_t(ti.split) * (NGW / 4) + gsub) * p.OC + ti.oc0 + m] = bsum;
                 if (!ok || !epilogue(ti, t)) break;
             }
         } else {
@@ -2275,16 +2281,22 @@ Plan plan_wgrad_tc(const ConvParams& p, int dt, const DevInfo& d)
     pl.variant = (g.KTp * 8 + g.raws) * 4 + g.nbs;
     pl.launches = 2;
     pl.grid = std::min(g.k_tiles * g.oc_tiles * g.splits, d.sms);
-    pl.workspace = size_t(g.splits) * p.OC * g.kpad * sizeof(float);
+    // the split-K partials, then room for the bias gradient's partial channel sums (two G lane
+    // groups per split at most), so that conv_bwd_filter and conv_bwd_filter_bias share the size
+    pl.workspace = size_t(g.splits) * p.OC * g.kpad * sizeof(float) + size_t(g.splits) * 2 * p.OC * sizeof(float);
     return pl;
 }
 
 template <typename T>
 static cudaError_t wgrad_tc_t(const Plan& pl, const ConvParams& p, const void* x, const void* dy,
-                              const void* y, void* dw, void* ws, int, cudaStream_t s)
+                              const void* y, void* dw, void* ws, void* db, cudaStream_t s)
 {
     cudaError_t e = cudaSuccess;
     const int kpad = round_up(p.Kred, 4);
+    float* bpart = db ? reinterpret_cast<float*>(static_cast<unsigned char*>(ws) +
+                                                 size_t(pl.splits) * p.OC * kpad * sizeof(float))
+                      : nullptr;
+    const int nbp = pl.splits * (WgRoles<T>::g_warps / 4);
     if (pl.splits > 0) {
         const int v = pl.variant;
         const TcWgradGeom g = wgrad_geom<T>(p, v / 32, (v / 4) % 8, v % 4, pl.splits);
@@ -2293,7 +2305,7 @@ static cudaError_t wgrad_tc_t(const Plan& pl, const ConvParams& p, const void* x
         e = ensure_smem<wgrad_tc_kernel<T, R>>(pl.smem);                                                   \
         if (e == cudaSuccess)                                                                              \
             e = launch_ex(wgrad_tc_kernel<T, R>, dim3(pl.grid), dim3(pl.block), pl.smem, s, 1, true, p,       \
-                          (const T*)x, (const T*)dy, (const T*)y, (float*)ws, g);                          \
+                          (const T*)x, (const T*)dy, (const T*)y, (float*)ws, bpart, g);                   \
     } while (0)
         if (p.relu) IG_LAUNCH_WG_TC(true);
         else IG_LAUNCH_WG_TC(false);
@@ -2301,14 +2313,15 @@ static cudaError_t wgrad_tc_t(const Plan& pl, const ConvParams& p, const void* x
         if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    return run_wgrad_reduce(p, dt_of_tc<T>(), (const float*)ws, pl.splits, kpad, dw, s, pl.splits > 0);
+    return run_wgrad_reduce(p, dt_of_tc<T>(), (const float*)ws, pl.splits, kpad, dw, s, pl.splits > 0, bpart,
+                            pl.splits > 0 ? nbp : 0, db);
 }
 
 cudaError_t run_wgrad_tc(const Plan& pl, const ConvParams& p, int dt, const void* x, const void* dy,
-                         const void* y, void* dw, void* ws, int sms, cudaStream_t s)
+                         const void* y, void* dw, void* ws, void* db, cudaStream_t s)
 {
-    return dt == DT_F32 ? wgrad_tc_t<float>(pl, p, x, dy, y, dw, ws, sms, s)
-                        : wgrad_tc_t<__nv_bfloat16>(pl, p, x, dy, y, dw, ws, sms, s);
+    return dt == DT_F32 ? wgrad_tc_t<float>(pl, p, x, dy, y, dw, ws, db, s)
+                        : wgrad_tc_t<__nv_bfloat16>(pl, p, x, dy, y, dw, ws, db, s);
 }
 
 // ---- d_input ------------------------------------------------------------------------

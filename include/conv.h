@@ -165,6 +165,19 @@ size_t conv_bwd_filter_workspace_size(const conv_desc_t* desc);
 int conv_bwd_filter(const conv_desc_t* desc, const void* x, const void* dy, const void* y,
                     void* dw, void* workspace, size_t workspace_bytes, conv_stream_t stream);
 
+/* Weight and bias gradients in one pass over g:  dw as conv_bwd_filter (bit for bit) and
+ * db[oc] = sum over b, oh, ow of g (as conv_bwd_bias, up to summation order).  On the
+ * tensor-core path the bias gradient is fused into wgrad: the threads that load and mask g
+ * for the first k-tile of each split also sum it per output channel (each thread its
+ * channel's values, chunk by chunk, in ascending column order), write one fp32 partial per
+ * (split, lane group) after the split-K partials in the workspace, and the split reduction
+ * adds them in ascending order -- so dy and y are read once for both gradients.  The other
+ * families run the bias-gradient kernel after the weight gradient.
+ *   x, dy, y, dw, workspace, workspace_bytes: as conv_bwd_filter (the same workspace size,
+ *   conv_bwd_filter_workspace_size, serves both)   db: (OC), written. */
+int conv_bwd_filter_bias(const conv_desc_t* desc, const void* x, const void* dy, const void* y, void* dw,
+                         void* db, void* workspace, size_t workspace_bytes, conv_stream_t stream);
+
 /* Bias gradient:  db[oc] = sum over b, oh, ow of g (g = dy masked by y > 0 when
  * relu), accumulated in fp32 and rounded once to the dtype.  One kernel: the
  * channels are cut into windows and the batch into R contiguous sample ranges

@@ -68,6 +68,7 @@ def test_invalid_descriptor(L, bad):
     assert L.conv_bwd_bias(ctypes.byref(d), fake, fake, fake, None) == -2
     assert L.conv_fwd_ws(ctypes.byref(d), fake, fake, None, fake, fake, 1 << 30, None) == -2
     assert L.conv_bwd_data_ws(ctypes.byref(d), fake, fake, fake, fake, fake, 1 << 30, None) == -2
+    assert L.conv_bwd_filter_bias(ctypes.byref(d), fake, fake, fake, fake, fake, fake, 1 << 30, None) == -2
     assert L.conv_fwd_workspace_size(ctypes.byref(d)) == 0
     assert L.conv_bwd_data_workspace_size(ctypes.byref(d)) == 0
     oh, ow = ctypes.c_int32(), ctypes.c_int32()
@@ -105,6 +106,10 @@ def test_null_and_alignment_checked_before_cuda(L):
     assert L.conv_bwd_bias(ctypes.byref(d), ok, ok, odd, None) == -4
     assert L.conv_bwd_bias(ctypes.byref(d), odd, ok, ok, None) == -4
     assert L.conv_bwd_bias(ctypes.byref(d), ok, odd, ok, None) == -4
+    # The fused weight + bias gradients: db required and aligned.
+    assert L.conv_bwd_filter_bias(ctypes.byref(d), ok, ok, ok, ok, None, ok, 1 << 30, None) == -1
+    assert L.conv_bwd_filter_bias(ctypes.byref(d), ok, ok, ok, ok, odd, ok, 1 << 30, None) == -4
+    assert L.conv_bwd_filter_bias(ctypes.byref(d), ok, ok, None, ok, ok, ok, 1 << 30, None) == -1  # relu needs y
     # The workspace-taking forward / d_input: the same checks, plus the workspace's alignment.
     assert L.conv_fwd_ws(ctypes.byref(d), None, ok, None, ok, ok, 1 << 30, None) == -1
     assert L.conv_fwd_ws(ctypes.byref(d), ok, ok, None, ok, odd, 1 << 30, None) == -4

@@ -185,3 +185,64 @@ def test_zero_bias_matches_plain_forward():
     b = c.gpu_fwd(bias=False)
     torch.cuda.synchronize()
     assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def _bits(t):
+    return t.view(torch.int16 if t.dtype == torch.bfloat16 else torch.int32)
+
+
+def wgrad_and_bias(c: BiasCase, label: str, y=None):
+    """conv_bwd_filter_bias: dw bit for bit as conv_bwd_filter, db against the oracle."""
+    y = c.gpu_fwd() if y is None else y
+    ym = y if c.relu else None
+    d = c.dev
+    ws = torch.empty(max(16, binding.conv_bwd_filter_workspace_size(c.desc)), dtype=torch.uint8, device="cuda")
+    dw_ref = torch.empty((c.OC, c.IC, c.K, c.K), dtype=TORCH_DT[c.dtype], device="cuda")
+    binding.conv_bwd_filter(c.desc, d["x"], d["dy"], ym, dw_ref, ws)
+    dw = torch.full_like(dw_ref, float("nan"))
+    db = torch.full((c.OC,), float("nan"), dtype=TORCH_DT[c.dtype], device="cuda")
+    binding.conv_bwd_filter_bias(c.desc, d["x"], d["dy"], ym, dw, db, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(_bits(dw), _bits(dw_ref)), f"{label}: dw differs from conv_bwd_filter's"
+    ref, den = c.ref_bgrad(to_np(y))
+    check(to_np(db), ref, den, c.dtype, f"{label} fused bias grad")
+    assert binding.conv_device_status(reset=True) == 0
+    return db
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("B", [1, 37, 1024])
+@pytest.mark.parametrize("layer", ["L1", "L2"])
+def test_bias_grad_fused_into_wgrad(layer, B, dtype):
+    c = BiasCase(B, **SHAPES[layer], dtype=dtype)
+    assert binding.conv_query(binding.OP_BWD_FILTER, c.desc)["algo"] == binding.ALGO_TC
+    db = wgrad_and_bias(c, f"{layer} B={B} {dtype}")
+    # run to run: bit-identical
+    db2 = wgrad_and_bias(c, f"{layer} B={B} {dtype} again")
+    assert torch.equal(_bits(db), _bits(db2))
+
+
+@pytest.mark.parametrize("shape", ["odd", "wide_oc_p16", "k1", "stride_gt_k", "two_windows"])
+def test_bias_grad_fused_odd_shapes(shape):
+    wgrad_and_bias(BiasCase(5, **SHAPES[shape], dtype="f32"), shape)
+
+
+@pytest.mark.parametrize("algo", [binding.ALGO_FFMA, binding.ALGO_DIRECT])
+def test_bias_grad_with_other_wgrad_families(algo):
+    """The FFMA and direct wgrad families run the bias-gradient kernel after the weight gradient."""
+    binding.conv_set_algo(binding.OP_BWD_FILTER, algo)
+    c = BiasCase(29, **L1, dtype="f32")
+    assert binding.conv_query(binding.OP_BWD_FILTER, c.desc)["algo"] == algo
+    wgrad_and_bias(c, f"L1 algo={algo}")
+
+
+def test_bias_grad_fused_empty_batch():
+    c = BiasCase(1, **L1, dtype="f32")
+    d0 = binding.make_desc(0, 59, 128, 11, 15, 5, 3, 1, torch.float32)
+    dw = torch.full((128, 59, 5, 5), 7.0, device="cuda")
+    db = torch.full((128,), 7.0, device="cuda")
+    e = torch.empty(0, device="cuda")
+    ws = torch.empty(max(16, binding.conv_bwd_filter_workspace_size(d0)), dtype=torch.uint8, device="cuda")
+    binding.conv_bwd_filter_bias(d0, e, e, e, dw, db, ws)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(dw).item() == 0 and torch.count_nonzero(db).item() == 0
