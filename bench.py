@@ -85,6 +85,8 @@ def parse():
                     help="launch each operation eagerly instead of replaying a captured CUDA graph")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the other-config table, e2e and CPU baseline")
+    ap.add_argument("--chain-only", action="store_true",
+                    help="time only the fused two-layer forward chain against the two forward calls")
     return ap.parse_args()
 
 
@@ -630,6 +632,44 @@ def bias_extras(wls, flush_buf, peaks, device):
     return out
 
 
+def chain_extras(flush_buf, device, batches=(256, 1024, 4096, 16384)):
+    """The encoder's two-layer forward fused (conv_fwd_chain2: layer 1's output tile stays in
+    shared memory as layer 2's input) against the two layers' forward calls one after the other
+    (conv_fwd_ws each), cold L2; layer 2's share of the chain = chain - layer 1 alone."""
+    import torch
+    from implicit_gemm_conv2d_gb300 import binding
+    out = {}
+    s1, s2 = LAYERS["layer1"], LAYERS["layer2"]
+    for dt in ("bf16", "f32"):
+        tdt = torch.float32 if dt == "f32" else torch.bfloat16
+        for B in batches:
+            g = torch.Generator(device=device)
+            g.manual_seed(7)
+            x = torch.randn((B, s1["IC"], s1["H"], s1["W"]), generator=g, device=device).to(tdt)
+            w1 = ((torch.rand((s1["OC"], s1["IC"], s1["K"], s1["K"]), generator=g, device=device) * 2 - 1)
+                  / math.sqrt(s1["IC"] * s1["K"] ** 2)).to(tdt)
+            w2 = ((torch.rand((s2["OC"], s2["IC"], s2["K"], s2["K"]), generator=g, device=device) * 2 - 1)
+                  / math.sqrt(s2["IC"] * s2["K"] ** 2)).to(tdt)
+            d1 = binding.make_desc(B, *(s1[k] for k in ("IC", "OC", "H", "W", "K", "S", "relu")), tdt)
+            d2 = binding.make_desc(B, *(s2[k] for k in ("IC", "OC", "H", "W", "K", "S", "relu")), tdt)
+            y1 = torch.empty((B, 128, 3, 4), dtype=tdt, device=device)
+            y2 = torch.empty((B, 128, 1, 2), dtype=tdt, device=device)
+            wsc = torch.empty(max(16, binding.conv_fwd_chain2_workspace_size(d1, d2)), dtype=torch.uint8, device=device)
+            ws1 = torch.empty(max(16, binding.conv_fwd_workspace_size(d1)), dtype=torch.uint8, device=device)
+            ws2 = torch.empty(max(16, binding.conv_fwd_workspace_size(d2)), dtype=torch.uint8, device=device)
+            gc = graphed(lambda: binding.conv_fwd_chain2(d1, d2, x, w1, None, w2, None, y1, y2, wsc))
+            g1 = graphed(lambda: binding.conv_fwd_ws(d1, x, w1, None, y1, ws1))
+            g2 = graphed(lambda: binding.conv_fwd_ws(d2, y1, w2, None, y2, ws2))
+            tc, t1, t2 = (time_graph(gg, flush_buf, 30, 3) * 1e3 for gg in (gc, g1, g2))
+            q = binding.conv_query_chain2(d1, d2)
+            out[f"{dt}_B{B}"] = {"chain_us_cold_l2": tc, "layer1_fwd_us_cold_l2": t1, "layer2_fwd_us_cold_l2": t2,
+                                 "unfused_us": t1 + t2, "layer2_share_of_chain_us": tc - t1,
+                                 "chain_plan": {k: q[k] for k in ("algo_name", "launches", "grid", "block")}}
+            del gc, g1, g2, x, y1, y2
+            torch.cuda.empty_cache()
+    return out
+
+
 SWEEP_BATCHES = (256, 1024, 4096, 16384)
 
 
@@ -726,6 +766,9 @@ def run_ours(args):
     peaks, peaks_kind = load_peaks()
 
     flush_buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    if args.chain_only:
+        print(json.dumps({"chain_fwd": chain_extras(flush_buf, device)}))
+        return 0
     wl = Workload(args.layer, args.dtype, args.batch, device)
     if not args.no_graphs:
         wl.capture()
@@ -826,6 +869,7 @@ def run_ours(args):
                 others[f"{layer}_{dt}"] = entry
         line["configs_b%d" % args.batch] = others
         line["bias"] = bias_extras(wls, flush_buf, peaks, device)
+        line["chain_fwd"] = chain_extras(flush_buf, device)
         line["batch_sweep"] = batch_sweep(flush_buf, sms, sm_mhz, peaks, device)
         if world == 1:
             line["cpu_baseline"] = cpu_baseline(LAYERS[args.layer], 128, 10.0)

@@ -54,7 +54,8 @@ EXPORTS = ["conv_fwd", "conv_bwd_data", "conv_bwd_filter_workspace_size", "conv_
            "conv_fastdivmod_check", "conv_l2_flush", "conv_version", "conv_bwd_filter_noalloc",
            "conv_device_status", "conv_fwd_bias", "conv_bwd_bias",
            "conv_wait_selftest", "conv_query_for_device", "conv_fwd_workspace_size", "conv_fwd_ws",
-           "conv_bwd_data_workspace_size", "conv_bwd_data_ws", "conv_bwd_filter_bias"]
+           "conv_bwd_data_workspace_size", "conv_bwd_data_ws", "conv_bwd_filter_bias",
+           "conv_fwd_chain2_workspace_size", "conv_fwd_chain2", "conv_query_chain2"]
 STATUS_WAIT_SELFTEST = 1 << 30
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -102,6 +103,10 @@ def lib():
         L.conv_bwd_data_workspace_size.restype = sz
         L.conv_bwd_data_ws.argtypes = [dp, vp, vp, vp, vp, vp, sz, vp]
         L.conv_bwd_filter_bias.argtypes = [dp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.conv_fwd_chain2_workspace_size.argtypes = [dp, dp]
+        L.conv_fwd_chain2_workspace_size.restype = sz
+        L.conv_fwd_chain2.argtypes = [dp, dp] + [vp] * 8 + [sz, vp]
+        L.conv_query_chain2.argtypes = [dp, dp, ctypes.POINTER(PlanInfo)]
         _lib = L
         return L
 
@@ -196,6 +201,26 @@ def conv_bwd_filter_bias(desc: ConvDesc, x, dy, y, dw, db, workspace, stream=Non
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().conv_bwd_filter_bias(ctypes.byref(desc), _ptr(x), _ptr(dy), _ptr(y), _ptr(dw), _ptr(db),
                                       _ptr(workspace), nbytes, _stream(stream)), "conv_bwd_filter_bias")
+
+
+def conv_fwd_chain2_workspace_size(d1: ConvDesc, d2: ConvDesc) -> int:
+    return int(lib().conv_fwd_chain2_workspace_size(ctypes.byref(d1), ctypes.byref(d2)))
+
+
+def conv_fwd_chain2(d1: ConvDesc, d2: ConvDesc, x, w1, bias1, w2, bias2, y1, y2, workspace, stream=None) -> None:
+    """Two-layer forward chain (layer 2's input is layer 1's output); biases may be None."""
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().conv_fwd_chain2(ctypes.byref(d1), ctypes.byref(d2), _ptr(x), _ptr(w1), _ptr(bias1), _ptr(w2),
+                                 _ptr(bias2), _ptr(y1), _ptr(y2), _ptr(workspace), nbytes, _stream(stream)),
+           "conv_fwd_chain2")
+
+
+def conv_query_chain2(d1: ConvDesc, d2: ConvDesc) -> dict:
+    info = PlanInfo()
+    _check(lib().conv_query_chain2(ctypes.byref(d1), ctypes.byref(d2), ctypes.byref(info)), "conv_query_chain2")
+    d = info.as_dict()
+    d["algo_name"] = ALGO_NAMES.get(d["algo"], "?")
+    return d
 
 
 def conv_bwd_filter_noalloc(desc: ConvDesc, x, dy, y, dw, stream=None) -> None:

@@ -409,6 +409,90 @@ int conv_bwd_filter_bias(const conv_desc_t* desc, const void* x, const void* dy,
     return wgrad_impl(desc, x, dy, y, dw, db, workspace, workspace_bytes, stream);
 }
 
+namespace {
+
+// Two descriptors that chain: layer 2's input is layer 1's output.
+int chain_params(const conv_desc_t* d1, const conv_desc_t* d2, ConvParams& p1, ConvParams& p2)
+{
+    int rc = make_params(d1, p1);
+    if (rc != CONV_OK) return rc;
+    if ((rc = make_params(d2, p2)) != CONV_OK) return rc;
+    if (d1->B != d2->B || d1->dtype != d2->dtype || d2->IC != d1->OC || d2->H != p1.OH || d2->W != p1.OW)
+        return CONV_ERR_DESC;
+    return CONV_OK;
+}
+
+int chain_plan(const ConvParams& p1, const ConvParams& p2, int dt, const DevInfo& d, Plan& pl)
+{
+    const int f = g_force[CONV_OP_FWD].load();
+    if ((f == ALGO_AUTO || f == ALGO_TC) && tc_chain_ok(p1, p2, dt, d)) {
+        pl = plan_chain_tc(p1, p2, dt, d);
+        return CONV_OK;
+    }
+    pl = Plan();
+    pl.algo = ALGO_AUTO;  // not fused: two forward calls
+    return CONV_OK;
+}
+
+}  // namespace
+
+size_t conv_fwd_chain2_workspace_size(const conv_desc_t* d1, const conv_desc_t* d2)
+{
+    ConvParams p1, p2;
+    if (chain_params(d1, d2, p1, p2) != CONV_OK) return 0;
+    DevInfo d;
+    if (device_info(d) != CONV_OK) return 0;
+    Plan pl;
+    chain_plan(p1, p2, d1->dtype, d, pl);
+    return pl.workspace;
+}
+
+int conv_fwd_chain2(const conv_desc_t* d1, const conv_desc_t* d2, const void* x, const void* w1, const void* bias1,
+                    const void* w2, const void* bias2, void* y1, void* y2, void* workspace, size_t workspace_bytes,
+                    conv_stream_t stream)
+{
+    if (!d1 || !d2) return CONV_ERR_NULL;
+    ConvParams p1, p2;
+    int rc = chain_params(d1, d2, p1, p2);
+    if (rc != CONV_OK) return rc;
+    if (p1.B == 0) return CONV_OK;
+    if (!x || !w1 || !w2 || !y1 || !y2) return CONV_ERR_NULL;
+    if (!aligned16(x) || !aligned16(w1) || !aligned16(w2) || !aligned16(y1) || !aligned16(y2) ||
+        (bias1 && !aligned16(bias1)) || (bias2 && !aligned16(bias2)) || (workspace && !aligned16(workspace)))
+        return CONV_ERR_ALIGN;
+    DevInfo d;
+    if ((rc = device_info(d)) != CONV_OK) return rc;
+    Plan pl;
+    chain_plan(p1, p2, d1->dtype, d, pl);
+    if (pl.algo != ALGO_TC) {  // the two layers one after the other
+        if ((rc = fwd_impl(d1, x, w1, bias1, y1, nullptr, 0, false, stream)) != CONV_OK) return rc;
+        return fwd_impl(d2, y1, w2, bias2, y2, nullptr, 0, false, stream);
+    }
+    if (!workspace || workspace_bytes < pl.workspace) return CONV_ERR_WORKSPACE;
+    return cuda_status(run_chain_tc(pl, p1, p2, d1->dtype, x, w1, bias1, w2, bias2, y1, y2, workspace,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int conv_query_chain2(const conv_desc_t* d1, const conv_desc_t* d2, conv_plan_info_t* info)
+{
+    ConvParams p1, p2;
+    int rc = chain_params(d1, d2, p1, p2);
+    if (rc != CONV_OK) return rc;
+    if (!info) return CONV_ERR_NULL;
+    DevInfo d;
+    if ((rc = device_info(d)) != CONV_OK) return rc;
+    Plan pl;
+    chain_plan(p1, p2, d1->dtype, d, pl);
+    info->algo = pl.algo;
+    info->launches = pl.launches;
+    info->grid = pl.grid;
+    info->block = pl.block;
+    info->smem_bytes = pl.smem;
+    info->splits = pl.splits;
+    info->workspace = pl.workspace;
+    return CONV_OK;
+}
+
 uint64_t conv_fastdivmod_check(uint32_t d, uint32_t lo, uint32_t hi)
 {
     if (d < 1 || d >= (1u << 31)) return ~uint64_t(0);

@@ -158,6 +158,13 @@ bool tc_dgrad_ok(const ConvParams& p, int dt, const DevInfo& d, bool packed);
 Plan plan_dgrad_tc(const ConvParams& p, int dt, const DevInfo& d, bool packed);
 cudaError_t run_dgrad_tc(const Plan&, const ConvParams&, int dt, const void* dy, const void* w,
                          const void* y, void* dx, void* ws, cudaStream_t s);
+// Two-layer forward chain (layer 2's input = layer 1's output), one kernel after packing both
+// weight images into the workspace.
+bool tc_chain_ok(const ConvParams& p1, const ConvParams& p2, int dt, const DevInfo& d);
+Plan plan_chain_tc(const ConvParams& p1, const ConvParams& p2, int dt, const DevInfo& d);
+cudaError_t run_chain_tc(const Plan&, const ConvParams& p1, const ConvParams& p2, int dt, const void* x,
+                         const void* w1, const void* b1, const void* w2, const void* b2, void* y1, void* y2, void* ws,
+                         cudaStream_t s);
 // ---- bias gradient (kernels_bias.cu) ------------------------------------------------
 // `direct`: the one-warp-per-channel kernel (any shape); else the column-sum kernel and its
 // reduce, when the shape allows.

@@ -2111,6 +2111,405 @@ dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const T* __restric
     }
 }
 
+// ======================================================================================
+// Two-layer forward chain: y1 = act1(conv1(x) + b1), y2 = act2(conv2(y1) + b2), where conv2's
+// input is conv1's output (IC2 = OC1, H2 x W2 = OH1 x OW1) -- the encoder of PufferLib PR #522
+// (layer 1 -> 3x4 -> layer 2).  A work item is a group of NS whole samples (NS*P1 <= 128
+// layer-1 columns).  Phase 1 is layer 1's forward tile for the group, as in fwd_tc_kernel;
+// its epilogue writes y1 to global memory (the backward needs it) and into a shared-memory
+// slab laid out as conv2's NCHW input.  Phase 2 is layer 2's forward for the same samples
+// (NS*P2 columns), gathered from that slab: y1 never makes a round trip through memory between
+// the layers, and one launch does both.  Both phases share the weight ring (packed images in
+// the caller's workspace, one bulk copy per chunk), the TMEM operand ring and the accumulator.
+// Warp roles (608 threads): warp 0 x producer (phase 1), warp 1 weight producer (W1 chunks,
+// then W2 chunks), warp 2 MMA, warps 3-18 formatters (gather + epilogue of both phases).
+// ======================================================================================
+constexpr int CH_THREADS = 96 + 32 * FA_FMTW;
+
+struct ChainGeom {
+    FwdGeom g1;              // layer 1 (tile = NS*P1 columns, OTp1 rows); nw / nraw / xg of the ring
+    int ns, ngroups;         // samples per group, groups
+    int OTp2, oc_tiles2;     // layer 2 rows (a single oc tile)
+    int nchunks2;            // layer 2 K-chunks
+    int w_bytes2;            // one layer-2 weight stage
+    int stage_bytes;         // weight ring stage = max(w_bytes1, w_bytes2)
+    int dcols;               // accumulator columns = max of the two layers'
+    int acol0;               // first TMEM column of the operand stages
+    int xs2;                 // bytes per sample in the y1 slab
+    int slab_bytes;
+    size_t wpack2_off;       // byte offset of the packed W2 image in the workspace
+    int relu1, relu2;
+};
+
+struct ChainBars {
+    uint64_t raw_full[FV_MAXRAWS], raw_empty[FV_MAXRAWS];
+    uint64_t w_full[FA_MAXW], w_empty[FA_MAXW];
+    uint64_t a_full[FA_MAXA], a_empty[FA_MAXA];
+    uint64_t acc_full, acc_empty;
+    uint64_t slab_full;      // the 16 formatter warps' y1 slab writes of the current group
+    uint32_t tslot;
+    int abort_flag;
+};
+
+template <typename T>
+inline int chain_smem(const ConvParams& p1, const ConvParams& p2, const ChainGeom& c)
+{
+    using Tr = TcTraits<T>;
+    return 1024 + c.g1.nw * c.stage_bytes + c.g1.nraw * c.g1.raw_bytes + c.slab_bytes + round_up(p1.Kred, Tr::KC) * 4 +
+           round_up(p2.Kred, Tr::KC) * 4 + int(sizeof(ChainBars)) + 16;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(CH_THREADS, 1)
+fwd_chain_kernel(const ConvParams p1, const ConvParams p2, const T* __restrict__ x,
+                 const unsigned char* __restrict__ wpack, const T* __restrict__ bias1,
+                 const T* __restrict__ bias2, T* __restrict__ y1, T* __restrict__ y2, const ChainGeom cg)
+{
+    using Tr = TcTraits<T>;
+    constexpr int ES = int(sizeof(T));
+    constexpr int KQ = Tr::KC / FA_KSPLIT;
+    constexpr int KQC = Tr::split ? KQ : KQ / 2;
+    static_assert(KQC == 8, "one tcgen05.st of 8 columns per part");
+    const FwdGeom& g1 = cg.g1;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = align1024(smem_raw);
+    const int kred1 = round_up(p1.Kred, Tr::KC), kred2 = round_up(p2.Kred, Tr::KC);
+    // Layout: weight stages | raw x slots | y1 slab | k offsets (layer 1, layer 2) | barriers
+    unsigned char* wring = smem;
+    unsigned char* raw = wring + g1.nw * cg.stage_bytes;
+    unsigned char* slab = raw + g1.nraw * g1.raw_bytes;
+    int* offk1 = reinterpret_cast<int*>(slab + cg.slab_bytes);
+    int* offk2 = offk1 + kred1;
+    ChainBars* bars = reinterpret_cast<ChainBars*>(offk2 + kred2);
+    volatile int* abort_flag = &bars->abort_flag;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int k = tid; k < kred1; k += CH_THREADS) {
+        const int sc_ic = (k / (g1.xg * Tr::KC)) * g1.xg * Tr::KC / p1.KK;
+        offk1[k] = (k < p1.Kred) ? (k_offset(p1, k) - sc_ic * p1.HW) * ES : 0;
+    }
+    for (int k = tid; k < kred2; k += CH_THREADS) offk2[k] = (k < p2.Kred) ? k_offset(p2, k) * ES : 0;
+    if (tid == 0) {
+        for (int i = 0; i < g1.nraw; ++i) {
+            mbar_init(smem_u32(&bars->raw_full[i]), 1);
+            mbar_init(smem_u32(&bars->raw_empty[i]), FA_FMTW);
+        }
+        for (int i = 0; i < g1.nw; ++i) {
+            mbar_init(smem_u32(&bars->w_full[i]), 1);
+            mbar_init(smem_u32(&bars->w_empty[i]), 1);
+        }
+        for (int i = 0; i < g1.na; ++i) {
+            mbar_init(smem_u32(&bars->a_full[i]), FA_FMTW);
+            mbar_init(smem_u32(&bars->a_empty[i]), 1);
+        }
+        mbar_init(smem_u32(&bars->acc_full), 1);
+        mbar_init(smem_u32(&bars->acc_empty), FA_FMTW);
+        mbar_init(smem_u32(&bars->slab_full), FA_FMTW);
+        fence_mbar_init();
+        bars->abort_flag = 0;
+    }
+    if (warp == 0) tmem_alloc(smem_u32(&bars->tslot), FA_TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tslot;
+    grid_dep_wait();  // the packed weights come from the kernels launched just before
+
+    if (warp == 0) {
+        // ---------------- x producer (phase 1) ----------------
+        const unsigned char* xb = reinterpret_cast<const unsigned char*>(x);
+        const unsigned char* x_end = xb + size_t(p1.B) * p1.IHW * ES;
+        RingPos rp;
+        for (int grp = blockIdx.x; grp < cg.ngroups && !*abort_flag; grp += gridDim.x) {
+            const int b_first = grp * cg.ns, nsamp = min(cg.ns, p1.B - b_first);
+            for (int sc = 0; sc < (g1.nchunks + g1.xg - 1) / g1.xg; ++sc, rp.next(g1.nraw)) {
+                const int s = rp.i;
+                if (rp.wrapped && !mbar_wait_or_abort(smem_u32(&bars->raw_empty[s]), rp.ph ^ 1u, abort_flag)) {
+                    report(const_cast<int*>(abort_flag), 4u);
+                    break;
+                }
+                const int sk0 = sc * g1.xg * Tr::KC;
+                const int ic_lo = sk0 / p1.KK;
+                const int ic_hi = min(p1.IC - 1, (min(sk0 + g1.xg * Tr::KC, p1.Kred) - 1) / p1.KK);
+                const int need = (ic_hi - ic_lo + 1) * p1.HW * ES;
+                unsigned char* slot = raw + s * g1.raw_bytes;
+                auto piece = [&](int j, const unsigned char*& src, int& bulk) {
+                    const unsigned char* s0 = xb + (size_t(b_first + j) * p1.IHW + size_t(ic_lo) * p1.HW) * ES;
+                    const int d = int(reinterpret_cast<uintptr_t>(s0) & 15);
+                    src = s0 - d;
+                    const int bytes = round_up(d + need, 16);
+                    bulk = slab_bytes_bulk(src, bytes, x_end);
+                    return bytes;
+                };
+                int tx = 0;
+                for (int j = lane; j < nsamp; j += 32) {
+                    const unsigned char* src;
+                    int bulk;
+                    const int bytes = piece(j, src, bulk);
+                    for (const unsigned char* t = src + bulk; t < src + bytes && t < x_end; ++t)
+                        slot[j * g1.xs + int(t - src)] = *t;
+                    tx += bulk;
+                }
+                tx = warp_sum(tx);
+                __syncwarp();
+                if (lane == 0) mbar_arrive_expect_tx(smem_u32(&bars->raw_full[s]), uint32_t(tx));
+                __syncwarp();
+                for (int j = lane; j < nsamp; j += 32) {
+                    const unsigned char* src;
+                    int bulk;
+                    piece(j, src, bulk);
+                    if (bulk > 0)
+                        bulk_g2s(smem_u32(slot + j * g1.xs), src, uint32_t(bulk), smem_u32(&bars->raw_full[s]));
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- weight producer: W1 chunks, then W2 chunks, per group ----------------
+        if (lane == 0) {
+            RingPos wp;
+            bool ok = true;
+            for (int grp = blockIdx.x; grp < cg.ngroups && ok && !*abort_flag; grp += gridDim.x) {
+                for (int ph = 0; ph < 2 && ok; ++ph) {
+                    const int n = ph == 0 ? g1.nchunks : cg.nchunks2;
+                    const int wb = ph == 0 ? g1.w_bytes : cg.w_bytes2;
+                    const unsigned char* src = wpack + (ph == 0 ? size_t(0) : cg.wpack2_off);
+                    for (int kc = 0; kc < n; ++kc, wp.next(g1.nw), src += wb) {
+                        if (wp.wrapped && !mbar_wait_or_abort(smem_u32(&bars->w_empty[wp.i]), wp.ph ^ 1u, abort_flag)) {
+                            report(const_cast<int*>(abort_flag), 16u);
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t bar = smem_u32(&bars->w_full[wp.i]);
+                        mbar_arrive_expect_tx(bar, uint32_t(wb));
+                        bulk_g2s(smem_u32(wring + wp.i * cg.stage_bytes), src, uint32_t(wb), bar);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // ---------------- MMA issuer: phase 1 then phase 2 of each group ----------------
+        if (lane == 0) {
+            const uint32_t w_u32 = smem_u32(wring);
+            RingPos wp, ap;
+            uint32_t t = 0;
+            bool ok = true;
+            for (int grp = blockIdx.x; grp < cg.ngroups && ok && !*abort_flag; grp += gridDim.x) {
+                for (int ph = 0; ph < 2 && ok; ++ph, ++t) {
+                    const int OTp = ph == 0 ? g1.OTp : cg.OTp2;
+                    const uint32_t idesc2 = instr_desc(Tr::fmt, FA_TM, Tr::split ? 2 * OTp : OTp);
+                    const uint32_t idesc1 = instr_desc(Tr::fmt, FA_TM, OTp);
+                    const int n = ph == 0 ? g1.nchunks : cg.nchunks2;
+                    if (t >= 1 && !mbar_wait_or_abort(smem_u32(&bars->acc_empty), (t - 1) & 1, abort_flag)) {
+                        report(const_cast<int*>(abort_flag), 8u);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    for (int kc = 0; kc < n; ++kc, wp.next(g1.nw), ap.next(g1.na)) {
+                        if (!mbar_wait_or_abort(smem_u32(&bars->w_full[wp.i]), wp.ph, abort_flag) ||
+                            !mbar_wait_or_abort(smem_u32(&bars->a_full[ap.i]), ap.ph, abort_flag)) {
+                            report(const_cast<int*>(abort_flag), 8u);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t wa = w_u32 + wp.i * cg.stage_bytes;
+                        const uint32_t aa = tmem + uint32_t(cg.acol0 + ap.i * g1.acols);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint64_t bd = op_desc<1>(wa + kstep_off<1>(j));
+                            const uint32_t acc = (kc == 0 && j == 0) ? 0u : 1u;
+                            if constexpr (Tr::split) {
+                                mma_tf32_ta(tmem, aa + 8 * j, bd, idesc2, acc);
+                                mma_tf32_ta(tmem, aa + Tr::KC + 8 * j, bd, idesc1, 1u);
+                            } else {
+                                mma_f16_ta(tmem, aa + 8 * j, bd, idesc1, acc);
+                            }
+                        }
+                        mma_commit(smem_u32(&bars->w_empty[wp.i]));
+                        mma_commit(smem_u32(&bars->a_empty[ap.i]));
+                    }
+                    if (!ok) break;
+                    mma_commit(smem_u32(&bars->acc_full));
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp >= 3) {
+        // ---------------- formatters: gather + epilogue, both phases ----------------
+        const int fw = warp - 3;
+        const int qd = warp & 3;
+        const int sub = fw >> 2;
+        const int m = qd * 32 + lane;
+        const uint32_t lane_bits = uint32_t(qd * 32) << 16;
+        const uint32_t raw_u32 = smem_u32(raw), slab_u32 = smem_u32(slab);
+        const uint32_t offk1_u32 = smem_u32(offk1) + uint32_t(sub * KQ * 4);
+        const uint32_t offk2_u32 = smem_u32(offk2) + uint32_t(sub * KQ * 4);
+        RingPos ap, rp;
+        uint32_t t = 0, sph = 0;
+        bool ok = true;
+        for (int grp = blockIdx.x; grp < cg.ngroups && ok; grp += gridDim.x) {
+            const int b_first = grp * cg.ns, nsamp = min(cg.ns, p1.B - b_first);
+            for (int ph = 0; ph < 2 && ok; ++ph, ++t) {
+                const ConvParams& p = ph == 0 ? p1 : p2;
+                const int n = ph == 0 ? g1.nchunks : cg.nchunks2;
+                const int cols = nsamp * p.P;  // valid columns of this phase
+                // This thread's column within the group (columns past `cols` gather the last
+                // valid column's values: their accumulator rows are computed but never stored).
+                int boff, bmis = 0;
+                {
+                    uint32_t bq, pq, oh, ow;
+                    p.dm_P.divmod(uint32_t(min(m, cols - 1)), bq, pq);
+                    p.dm_OW.divmod(pq, oh, ow);
+                    boff = int(bq) * (ph == 0 ? g1.xs : cg.xs2) + (int(oh) * p.S * p.W + int(ow) * p.S) * ES;
+                    if (ph == 0) bmis = int((size_t(b_first + int(bq)) * p1.IHW * ES) & 15);
+                }
+                if (ph == 1) {
+                    // the slab holds this group's y1: wait for every formatter warp's writes
+                    if (!mbar_wait_or_abort(smem_u32(&bars->slab_full), sph, abort_flag)) {
+                        report(const_cast<int*>(abort_flag), 32u);
+                        ok = false;
+                        break;
+                    }
+                    sph ^= 1u;
+                }
+                const bool ragged_k = (p.Kred % Tr::KC) != 0;
+                uint32_t sbase = 0;
+                int xc = 0;
+                for (int kc = 0; kc < n; ++kc, ap.next(g1.na)) {
+                    if (ph == 0 && xc == 0) {
+                        if (!mbar_wait_or_abort(smem_u32(&bars->raw_full[rp.i]), rp.ph, abort_flag)) {
+                            report(const_cast<int*>(abort_flag), 1u);
+                            ok = false;
+                            break;
+                        }
+                        const int ic_lo = (kc * Tr::KC) / p1.KK;
+                        const int cmis = (ic_lo * p1.HW * ES) & 15;
+                        sbase = raw_u32 + uint32_t(rp.i * g1.raw_bytes + boff + ((bmis + cmis) & 15));
+                    }
+                    if (ph == 1) sbase = slab_u32 + uint32_t(boff);
+                    if (ap.wrapped && !mbar_wait_or_abort(smem_u32(&bars->a_empty[ap.i]), ap.ph ^ 1u, abort_flag)) {
+                        report(const_cast<int*>(abort_flag), 1u);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t oaddr = (ph == 0 ? offk1_u32 : offk2_u32) + uint32_t(kc * Tr::KC * 4);
+                    const uint32_t col = tmem + lane_bits + uint32_t(cg.acol0 + ap.i * g1.acols + sub * KQC);
+                    const int kvalid = (ragged_k && kc == n - 1) ? p.Kred - (kc * Tr::KC + sub * KQ) : KQ;
+                    int o[KQ];
+#pragma unroll
+                    for (int i = 0; i < KQ / 4; ++i) {
+                        const int4 v4 = lds128(oaddr + 16 * i);
+                        o[4 * i] = v4.x;
+                        o[4 * i + 1] = v4.y;
+                        o[4 * i + 2] = v4.z;
+                        o[4 * i + 3] = v4.w;
+                    }
+                    uint32_t v[KQ];
+#pragma unroll
+                    for (int e = 0; e < KQ; ++e)
+                        v[e] = Tr::split ? lds32(sbase + uint32_t(o[e])) : lds16(sbase + uint32_t(o[e]));
+                    if (kvalid < KQ) {
+#pragma unroll
+                        for (int e = 0; e < KQ; ++e)
+                            if (e >= kvalid) v[e] = 0;
+                    }
+                    if constexpr (Tr::split) {
+                        uint32_t hi[8], lo[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) split_tf32(v[e], hi[e], lo[e]);
+                        tmem_st8(col, hi);
+                        tmem_st8(col + Tr::KC, lo);
+                    } else {
+                        uint32_t wv[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) wv[e] = __byte_perm(v[2 * e], v[2 * e + 1], 0x5410);
+                        tmem_st8(col, wv);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    const bool sc_end = ph == 0 && ((++xc == g1.xg) || kc == n - 1);
+                    if (lane == 0) {
+                        mbar_arrive(smem_u32(&bars->a_full[ap.i]));
+                        if (sc_end) mbar_arrive(smem_u32(&bars->raw_empty[rp.i]));
+                    }
+                    if (sc_end) {
+                        xc = 0;
+                        rp.next(g1.nraw);
+                    }
+                }
+                if (!ok) break;
+                // Epilogue: TMEM -> bias -> activation -> y (and, in phase 1, the y1 slab).
+                if (!mbar_wait_or_abort(smem_u32(&bars->acc_full), t & 1, abort_flag)) {
+                    report(const_cast<int*>(abort_flag), 2u);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int OTp = ph == 0 ? g1.OTp : cg.OTp2;
+                const T* bias = ph == 0 ? bias1 : bias2;
+                const bool relu = (ph == 0 ? cg.relu1 : cg.relu2) != 0;
+                T* yc = nullptr;
+                uint32_t srow = 0;
+                if (m < cols) {
+                    const int nglob = b_first * p.P + m;
+                    yc = (ph == 0 ? y1 : y2) + col_out(p, nglob);
+                    if (ph == 0) {
+                        uint32_t s1, q1;
+                        p1.dm_P.divmod(uint32_t(m), s1, q1);
+                        srow = slab_u32 + uint32_t(int(s1) * cg.xs2 + int(q1) * ES);  // + oc * P1 * ES
+                    }
+                }
+                for (int cb = sub * 8; cb < OTp; cb += 8 * FA_KSPLIT) {
+                    uint32_t r[8];
+                    tmem_ld8(tmem + lane_bits + uint32_t(cb), r);
+                    if constexpr (Tr::split) {
+                        uint32_t r2[8];
+                        tmem_ld8(tmem + lane_bits + uint32_t(OTp + cb), r2);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(r2[e]));
+                    } else {
+                        tmem_ld_wait();
+                    }
+                    if (yc) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int oc = cb + e;
+                            if (oc < p.OC) {
+                                float f = __uint_as_float(r[e]);
+                                if (bias) f += Elem<T>::ldg(bias + oc);
+                                if (relu) f = f > 0.f ? f : 0.f;
+                                Elem<T>::st(yc + size_t(oc) * p.P, f);
+                                if (ph == 0) {
+                                    // the slab holds exactly the value y1 holds (rounded to T)
+                                    const uint32_t a = srow + uint32_t(oc * p1.P * ES);
+                                    if constexpr (ES == 4) sts32(a, __float_as_uint(f));
+                                    else sts16(a, __bfloat16_as_ushort(__float2bfloat16_rn(f)));
+                                }
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(smem_u32(&bars->acc_empty));
+                    if (ph == 0) mbar_arrive(smem_u32(&bars->slab_full));  // this warp's slab writes are done
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, FA_TMEM_COLS);
+    }
+}
+
 template <typename T> constexpr int dt_of_tc();
 template <> constexpr int dt_of_tc<float>() { return DT_F32; }
 template <> constexpr int dt_of_tc<__nv_bfloat16>() { return DT_BF16; }
@@ -2408,6 +2807,107 @@ cudaError_t run_dgrad_tc(const Plan& pl, const ConvParams& p, int dt, const void
 {
     return dt == DT_F32 ? dgrad_tc_t<float>(pl, p, dy, w, y, dx, ws, s)
                         : dgrad_tc_t<__nv_bfloat16>(pl, p, dy, w, y, dx, ws, s);
+}
+
+// ---- two-layer forward chain ----------------------------------------------------------
+// Samples per group: as many whole samples as fit the 128 TMEM lanes in both layers (layer 1
+// usually decides: 10 samples of 3x4); then the deepest weight ring and longest x super-chunk
+// that fit, with the y1 slab of the group.
+template <typename T>
+static ChainGeom chain_geom(const ConvParams& p1, const ConvParams& p2, int xg, int nw, int nraw)
+{
+    using Tr = TcTraits<T>;
+    const int es = int(sizeof(T));
+    const int ns = std::min(FA_TM / p1.P, FA_TM / p2.P);
+    ChainGeom cg;
+    cg.g1 = fwd_geom<T>(p1, xg, nw, nraw);
+    cg.g1.packed = 1;
+    cg.g1.nsmax = std::min(ns, p1.B);
+    cg.g1.raw_bytes = round_up(cg.g1.nsmax * cg.g1.xs, 128);
+    cg.ns = ns;
+    cg.ngroups = ceil_div(p1.B, ns);
+    cg.OTp2 = round_up(p2.OC, 16);
+    cg.oc_tiles2 = 1;
+    cg.nchunks2 = round_up(p2.Kred, Tr::KC) / Tr::KC;
+    cg.w_bytes2 = cg.OTp2 * ROWB * (Tr::split ? 2 : 1);
+    cg.stage_bytes = std::max(cg.g1.w_bytes, cg.w_bytes2);
+    cg.dcols = std::max(cg.g1.dcols, cg.OTp2 * (Tr::split ? 2 : 1));
+    cg.acol0 = round_up(cg.dcols, 32);
+    cg.g1.na = std::min(FA_MAXA, (FA_TMEM_COLS - cg.acol0) / cg.g1.acols);
+    cg.xs2 = round_up(p2.IHW * es, 16) + 16;  // a sample of conv2's input, 16-byte padded
+    cg.slab_bytes = round_up(ns * cg.xs2, 128);
+    cg.wpack2_off = round_up(size_t(cg.g1.oc_tiles) * cg.g1.nchunks * cg.g1.w_bytes, size_t(256));
+    cg.relu1 = p1.relu;
+    cg.relu2 = p2.relu;
+    return cg;
+}
+
+template <typename T>
+static bool pick_chain(const ConvParams& p1, const ConvParams& p2, const DevInfo& d, ChainGeom& out)
+{
+    using Tr = TcTraits<T>;
+    const int otmax = Tr::split ? 128 : 256;
+    if (d.cc_major != 10 || p1.B <= 0 || p1.P > FA_TM || p2.P > FA_TM || p1.OC > otmax || p2.OC > otmax) return false;
+    static const int cfgs[][3] = {{4, 8, 2}, {4, 4, 2}, {4, 2, 2}, {3, 4, 2}, {3, 2, 2}, {2, 2, 2}, {2, 1, 2}};
+    for (const auto& c : cfgs) {
+        const ChainGeom cg = chain_geom<T>(p1, p2, c[1], c[0], c[2]);
+        if (cg.g1.na < 2 || chain_smem<T>(p1, p2, cg) > d.smem_optin) continue;
+        out = cg;
+        return true;
+    }
+    return false;
+}
+
+bool tc_chain_ok(const ConvParams& p1, const ConvParams& p2, int dt, const DevInfo& d)
+{
+    ChainGeom cg;
+    return dt == DT_BF16 ? pick_chain<__nv_bfloat16>(p1, p2, d, cg) : pick_chain<float>(p1, p2, d, cg);
+}
+
+Plan plan_chain_tc(const ConvParams& p1, const ConvParams& p2, int dt, const DevInfo& d)
+{
+    ChainGeom cg;
+    if (dt == DT_BF16) pick_chain<__nv_bfloat16>(p1, p2, d, cg);
+    else pick_chain<float>(p1, p2, d, cg);
+    Plan pl;
+    pl.algo = ALGO_TC;
+    pl.launches = 3;  // pack W1, pack W2, the chain
+    pl.block = CH_THREADS;
+    pl.grid = std::min(cg.ngroups, d.sms);
+    pl.smem = dt == DT_BF16 ? chain_smem<__nv_bfloat16>(p1, p2, cg) : chain_smem<float>(p1, p2, cg);
+    pl.variant = (cg.g1.xg * 16 + cg.g1.nw) * 8 + cg.g1.nraw;
+    pl.workspace = cg.wpack2_off + size_t(cg.nchunks2) * cg.w_bytes2;
+    return pl;
+}
+
+template <typename T>
+static cudaError_t chain_tc_t(const Plan& pl, const ConvParams& p1, const ConvParams& p2, const void* x,
+                              const void* w1, const void* b1, const void* w2, const void* b2, void* y1, void* y2,
+                              void* ws, cudaStream_t s)
+{
+    const int v = pl.variant;
+    const ChainGeom cg = chain_geom<T>(p1, p2, (v / 128) % 16, (v / 8) % 16, v % 8);
+    unsigned char* wsb = static_cast<unsigned char*>(ws);
+    const dim3 pg1(ceil_div(cg.g1.OTp * 8, 256), cg.g1.nchunks, cg.g1.oc_tiles);
+    pack_fwd_w_kernel<T><<<pg1, 256, 0, s>>>(p1, (const T*)w1, wsb, cg.g1.nchunks, cg.g1.OTp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const dim3 pg2(ceil_div(cg.OTp2 * 8, 256), cg.nchunks2, 1);
+    pack_fwd_w_kernel<T><<<pg2, 256, 0, s>>>(p2, (const T*)w2, wsb + cg.wpack2_off, cg.nchunks2, cg.OTp2);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = ensure_smem<fwd_chain_kernel<T>>(pl.smem);
+    if (e == cudaSuccess)
+        e = launch_ex(fwd_chain_kernel<T>, dim3(pl.grid), dim3(pl.block), pl.smem, s, 1, true, p1, p2, (const T*)x,
+                      (const unsigned char*)wsb, (const T*)b1, (const T*)b2, (T*)y1, (T*)y2, cg);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t run_chain_tc(const Plan& pl, const ConvParams& p1, const ConvParams& p2, int dt, const void* x,
+                         const void* w1, const void* b1, const void* w2, const void* b2, void* y1, void* y2, void* ws,
+                         cudaStream_t s)
+{
+    return dt == DT_F32 ? chain_tc_t<float>(pl, p1, p2, x, w1, b1, w2, b2, y1, y2, ws, s)
+                        : chain_tc_t<__nv_bfloat16>(pl, p1, p2, x, w1, b1, w2, b2, y1, y2, ws, s);
 }
 
 cudaError_t tc_read_status(unsigned* out, bool reset)

@@ -196,6 +196,31 @@ int conv_bwd_filter_bias(const conv_desc_t* desc, const void* x, const void* dy,
 int conv_bwd_bias(const conv_desc_t* desc, const void* dy, const void* y, void* db,
                   conv_stream_t stream);
 
+/* Two-layer forward chain:  y1 = act1(conv1(x, w1) + bias1),  y2 = act2(conv2(y1, w2) + bias2),
+ * where layer 2's input is layer 1's output (d2->IC = d1->OC, d2->H x d2->W = layer 1's
+ * OH x OW, same B and dtype) -- the encoder of PufferLib PR #522, whose layer-1 (11x15, K=5,
+ * S=3, ReLU -> 3x4) and layer-2 (3x4, K=3, S=1 -> 1x2) bench blocks are its two halves.  act1 /
+ * act2 follow d1->relu / d2->relu; bias1 / bias2 may be NULL (no bias).  y1 is written too
+ * (the backward needs it as a mask source and as layer 2's input).  Results: y1 as conv_fwd /
+ * conv_fwd_bias on layer 1 and y2 as conv_fwd on y1 -- bit for bit where those calls sum K in
+ * one range, else up to summation order (they split K when their column tiles are few).
+ * On the tensor-core path one kernel computes both layers per group of whole samples: layer 1's
+ * output tile goes to y1 and into shared memory, where layer 2 gathers its input from, so y1
+ * makes no round trip through memory between the layers and layer 2 needs no launch of its
+ * own; both weight images are packed into the workspace first (two small kernels).  Shapes the
+ * fused kernel does not take (a layer with more than 128 output positions, or more output
+ * channels than one tensor-core tile: 128 fp32 / 256 bf16) run as two conv_fwd calls, and the
+ * workspace size is 0.
+ *   workspace: at least conv_fwd_chain2_workspace_size(d1, d2) bytes, 16-byte aligned, owned
+ *   by the caller; contents ignored on entry and unspecified on return.
+ * conv_query_chain2 reports the plan (algo CONV_ALGO_TC when fused, CONV_ALGO_AUTO when it runs
+ * as two forward calls); conv_set_algo(CONV_OP_FWD, ...) other than AUTO / TC disables the
+ * fused kernel. */
+size_t conv_fwd_chain2_workspace_size(const conv_desc_t* d1, const conv_desc_t* d2);
+int conv_fwd_chain2(const conv_desc_t* d1, const conv_desc_t* d2, const void* x, const void* w1, const void* bias1,
+                    const void* w2, const void* bias2, void* y1, void* y2, void* workspace, size_t workspace_bytes,
+                    conv_stream_t stream);
+
 /* Weight gradient that allocates nothing (PufferLib PR #522 has no counterpart; this
  * entry point exists for callers of this library that cannot allocate device
  * memory: hosts that hand the library only the input and output buffers and own
@@ -240,6 +265,8 @@ typedef struct {
     size_t workspace;     /* wgrad: workspace bytes (else 0)                  */
 } conv_plan_info_t;
 int conv_query(int op, const conv_desc_t* desc, conv_plan_info_t* info);
+/* The plan of conv_fwd_chain2 for these two descriptors (see there). */
+int conv_query_chain2(const conv_desc_t* d1, const conv_desc_t* d2, conv_plan_info_t* info);
 
 /* The same plan for a device described by its properties instead of the current one,
  * computed on the host with no CUDA call (capacity planning; tests without a GPU).

@@ -69,6 +69,9 @@ def test_invalid_descriptor(L, bad):
     assert L.conv_fwd_ws(ctypes.byref(d), fake, fake, None, fake, fake, 1 << 30, None) == -2
     assert L.conv_bwd_data_ws(ctypes.byref(d), fake, fake, fake, fake, fake, 1 << 30, None) == -2
     assert L.conv_bwd_filter_bias(ctypes.byref(d), fake, fake, fake, fake, fake, fake, 1 << 30, None) == -2
+    assert L.conv_fwd_chain2(ctypes.byref(d), ctypes.byref(d), fake, fake, None, fake, None, fake, fake, fake,
+                             1 << 30, None) == -2
+    assert L.conv_fwd_chain2_workspace_size(ctypes.byref(d), ctypes.byref(d)) == 0
     assert L.conv_fwd_workspace_size(ctypes.byref(d)) == 0
     assert L.conv_bwd_data_workspace_size(ctypes.byref(d)) == 0
     oh, ow = ctypes.c_int32(), ctypes.c_int32()
@@ -116,6 +119,24 @@ def test_null_and_alignment_checked_before_cuda(L):
     assert L.conv_fwd_ws(ctypes.byref(d), ok, ok, odd, ok, ok, 1 << 30, None) == -4
     assert L.conv_bwd_data_ws(ctypes.byref(d), ok, ok, None, ok, ok, 1 << 30, None) == -1  # relu needs y
     assert L.conv_bwd_data_ws(ctypes.byref(d), ok, ok, ok, ok, odd, 1 << 30, None) == -4
+
+
+def test_chain_descriptors_checked_before_cuda(L):
+    d1 = desc()
+    d2 = desc(IC=128, H=3, W=4, K=3, S=1, relu=0)
+    ok = ctypes.c_void_p(0x1000)
+    fake = ctypes.c_void_p(0x1000)
+    # layer 2's input must be layer 1's output
+    for bad in (desc(IC=64, H=3, W=4, K=3, S=1), desc(IC=128, H=4, W=4, K=3, S=1), desc(B=7, IC=128, H=3, W=4, K=3, S=1),
+                desc(IC=128, H=3, W=4, K=3, S=1, dtype=1)):
+        assert L.conv_fwd_chain2(ctypes.byref(d1), ctypes.byref(bad), fake, fake, None, fake, None, fake, fake, fake,
+                                 1 << 30, None) == -2
+    assert L.conv_fwd_chain2(None, ctypes.byref(d2), ok, ok, None, ok, None, ok, ok, ok, 1 << 30, None) == -1
+    assert L.conv_fwd_chain2(ctypes.byref(d1), ctypes.byref(d2), None, ok, None, ok, None, ok, ok, ok, 1 << 30,
+                             None) == -1
+    odd = ctypes.c_void_p(0x1008)
+    assert L.conv_fwd_chain2(ctypes.byref(d1), ctypes.byref(d2), ok, ok, None, ok, None, ok, odd, ok, 1 << 30,
+                             None) == -4
 
 
 def test_empty_batch_is_a_no_op(L):

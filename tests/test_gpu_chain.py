@@ -81,3 +81,88 @@ def test_two_layer_chain_bf16(B):
     ref, den = oracle.conv_bwd_filter(x1n, dy1n[:, chans], y1n[:, chans], 5, 3, True)
     _check(to_np(dw1)[chans], ref, den, f"B={B} layer1 wgrad")
     assert np.isfinite(dx1s).all()
+
+
+def _bits(t):
+    return t.view(torch.int16 if t.dtype == torch.bfloat16 else torch.int32)
+
+
+@pytest.mark.parametrize("dtype,B", [("bf16", 256), ("bf16", 1024), ("bf16", 4096), ("bf16", 16384),
+                                     ("f32", 256), ("f32", 1024), ("f32", 4096)])
+def test_fused_forward_chain(dtype, B):
+    """conv_fwd_chain2: both layers' forward in one kernel, layer 1's output tile kept in shared
+    memory as layer 2's input.  Checked stage by stage against the oracle (layer 2 fed the
+    GPU's y1), y1 bit for bit against conv_fwd, and y2 against conv_fwd on that y1."""
+    from .gpu_cases import TORCH_DT
+    tdt = TORCH_DT[dtype]
+    i1 = synth.conv_inputs(B, L1["IC"], L1["OC"], L1["H"], L1["W"], L1["K"], L1["S"], dtype=dtype,
+                           need=("x", "w", "bias"))
+    w2 = synth.conv_inputs(1, L2["IC"], L2["OC"], L2["H"], L2["W"], L2["K"], L2["S"], dtype=dtype,
+                           w_stream=synth.STREAM_W2, need=("w",))["w"]
+    x1, W1, W2, b1 = to_dev(i1["x"], dtype), to_dev(i1["w"], dtype), to_dev(w2, dtype), to_dev(i1["bias"], dtype)
+    d1 = binding.make_desc(B, **L1, relu=1, dtype=tdt)
+    d2 = binding.make_desc(B, **L2, relu=0, dtype=tdt)
+    q = binding.conv_query_chain2(d1, d2)
+    assert q["algo"] == binding.ALGO_TC and q["launches"] == 3, q
+    ws = torch.empty(binding.conv_fwd_chain2_workspace_size(d1, d2), dtype=torch.uint8, device="cuda")
+    y1 = torch.full((B, 128, 3, 4), float("nan"), dtype=tdt, device="cuda")
+    y2 = torch.full((B, 128, 1, 2), float("nan"), dtype=tdt, device="cuda")
+    binding.conv_fwd_chain2(d1, d2, x1, W1, b1, W2, None, y1, y2, ws)
+    y1_ref = torch.empty_like(y1)
+    binding.conv_fwd_bias(d1, x1, W1, b1, y1_ref)
+    y2_ref = torch.empty_like(y2)
+    binding.conv_fwd(d2, y1, W2, y2_ref)
+    torch.cuda.synchronize()
+    assert binding.conv_device_status(reset=True) == 0
+    # The chain's layer 1 sums K in one range; so does conv_fwd_bias unless its plan splits K
+    # (fewer column tiles than half the SMs), in which case the two agree within tolerance.
+    if binding.conv_query(binding.OP_FWD, d1)["splits"] == 1:
+        assert torch.equal(_bits(y1), _bits(y1_ref)), "y1 differs from conv_fwd_bias"
+    rng = np.random.default_rng(B + 7)
+    samples = np.arange(B) if B <= 1024 else np.sort(rng.choice(B, 256, replace=False))
+    y1n, y2n = to_np(y1), to_np(y2)
+    assert np.isfinite(y2n).all() and np.isfinite(y1n).all()
+    ref, den = oracle.conv_fwd(i1["x"][samples], i1["w"], 3, True, bias=i1["bias"])
+    e1 = oracle.normalised_error(y1n[samples], ref, den)
+    assert e1 <= TOL[dtype], f"B={B} {dtype} chain layer1: {e1:.3e}"
+    ref, den = oracle.conv_fwd(y1n[samples], w2, 1, False)
+    e2 = oracle.normalised_error(y2n[samples], ref, den)
+    assert e2 <= TOL[dtype], f"B={B} {dtype} chain layer2: {e2:.3e}"
+    e3 = oracle.normalised_error(y2n, to_np(y2_ref), oracle.conv_fwd(y1n, w2, 1, False)[1])
+    assert e3 <= TOL[dtype], f"B={B} {dtype} chain layer2 vs conv_fwd: {e3:.3e}"
+    e4 = oracle.normalised_error(y1n, to_np(y1_ref), oracle.conv_fwd(i1["x"], i1["w"], 3, True, bias=i1["bias"])[1])
+    assert e4 <= TOL[dtype], f"B={B} {dtype} chain layer1 vs conv_fwd_bias: {e4:.3e}"
+
+
+def test_fused_forward_chain_ragged_and_run_to_run():
+    """A batch that leaves the last group partial (37 = 3 groups of 10 + 7), twice: bit-identical."""
+    B, dtype = 37, "f32"
+    i1 = synth.conv_inputs(B, L1["IC"], L1["OC"], L1["H"], L1["W"], L1["K"], L1["S"], dtype=dtype, need=("x", "w"))
+    w2 = synth.conv_inputs(1, L2["IC"], L2["OC"], L2["H"], L2["W"], L2["K"], L2["S"], dtype=dtype,
+                           w_stream=synth.STREAM_W2, need=("w",))["w"]
+    x1, W1, W2 = to_dev(i1["x"], dtype), to_dev(i1["w"], dtype), to_dev(w2, dtype)
+    d1 = binding.make_desc(B, **L1, relu=1, dtype=torch.float32)
+    d2 = binding.make_desc(B, **L2, relu=0, dtype=torch.float32)
+    ws = torch.empty(binding.conv_fwd_chain2_workspace_size(d1, d2), dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(2):
+        y1 = torch.full((B, 128, 3, 4), float("nan"), device="cuda")
+        y2 = torch.full((B, 128, 1, 2), float("nan"), device="cuda")
+        binding.conv_fwd_chain2(d1, d2, x1, W1, None, W2, None, y1, y2, ws)
+        outs.append((y1, y2))
+    torch.cuda.synchronize()
+    for a, b in zip(*outs):
+        assert torch.equal(_bits(a), _bits(b))
+    y1n, y2n = to_np(outs[0][0]), to_np(outs[0][1])
+    ref, den = oracle.conv_fwd(i1["x"], i1["w"], 3, True)
+    assert oracle.normalised_error(y1n, ref, den) <= TOL[dtype]
+    ref, den = oracle.conv_fwd(y1n, w2, 1, False)
+    assert oracle.normalised_error(y2n, ref, den) <= TOL[dtype]
+
+
+def test_chain_descriptors_must_chain():
+    d1 = binding.make_desc(8, **L1, relu=1, dtype=torch.float32)
+    bad = binding.make_desc(8, 64, 128, 3, 4, 3, 1, 0, torch.float32)  # IC != layer 1's OC
+    with pytest.raises(binding.ConvError) as ei:
+        binding.conv_query_chain2(d1, bad)
+    assert ei.value.status == -2
