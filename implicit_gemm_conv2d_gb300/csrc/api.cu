@@ -422,15 +422,28 @@ int chain_params(const conv_desc_t* d1, const conv_desc_t* d2, ConvParams& p1, C
     return CONV_OK;
 }
 
+// Fused when every CTA gets at most one group of samples (measured on a GB300: with more groups
+// per CTA the layer-2 phase, which cannot overlap the next group's layer-1 tile, costs more than
+// layer 2's own forward call); otherwise the two forward calls with the workspace path, sharing
+// one workspace of the larger size.
 int chain_plan(const ConvParams& p1, const ConvParams& p2, int dt, const DevInfo& d, Plan& pl)
 {
     const int f = g_force[CONV_OP_FWD].load();
     if ((f == ALGO_AUTO || f == ALGO_TC) && tc_chain_ok(p1, p2, dt, d)) {
         pl = plan_chain_tc(p1, p2, dt, d);
-        return CONV_OK;
+        if (chain_groups(p1, p2) <= d.sms) return CONV_OK;  // at most one group per CTA
     }
+    Plan a, b;
+    int rc = choose_fwd(p1, dt, d, true, a);
+    if (rc == CONV_OK) rc = choose_fwd(p2, dt, d, true, b);
+    if (rc != CONV_OK) return rc;
     pl = Plan();
     pl.algo = ALGO_AUTO;  // not fused: two forward calls
+    pl.launches = a.launches + b.launches;
+    pl.grid = std::max(a.grid, b.grid);
+    pl.block = std::max(a.block, b.block);
+    pl.smem = std::max(a.smem, b.smem);
+    pl.workspace = std::max(a.workspace, b.workspace);
     return CONV_OK;
 }
 
@@ -443,7 +456,7 @@ size_t conv_fwd_chain2_workspace_size(const conv_desc_t* d1, const conv_desc_t* 
     DevInfo d;
     if (device_info(d) != CONV_OK) return 0;
     Plan pl;
-    chain_plan(p1, p2, d1->dtype, d, pl);
+    if (chain_plan(p1, p2, d1->dtype, d, pl) != CONV_OK) return 0;
     return pl.workspace;
 }
 
@@ -463,10 +476,11 @@ int conv_fwd_chain2(const conv_desc_t* d1, const conv_desc_t* d2, const void* x,
     DevInfo d;
     if ((rc = device_info(d)) != CONV_OK) return rc;
     Plan pl;
-    chain_plan(p1, p2, d1->dtype, d, pl);
-    if (pl.algo != ALGO_TC) {  // the two layers one after the other
-        if ((rc = fwd_impl(d1, x, w1, bias1, y1, nullptr, 0, false, stream)) != CONV_OK) return rc;
-        return fwd_impl(d2, y1, w2, bias2, y2, nullptr, 0, false, stream);
+    if ((rc = chain_plan(p1, p2, d1->dtype, d, pl)) != CONV_OK) return rc;
+    if (pl.algo != ALGO_TC) {  // the two layers one after the other, through the workspace path
+        if (pl.workspace > 0 && (!workspace || workspace_bytes < pl.workspace)) return CONV_ERR_WORKSPACE;
+        if ((rc = fwd_impl(d1, x, w1, bias1, y1, workspace, workspace_bytes, true, stream)) != CONV_OK) return rc;
+        return fwd_impl(d2, y1, w2, bias2, y2, workspace, workspace_bytes, true, stream);
     }
     if (!workspace || workspace_bytes < pl.workspace) return CONV_ERR_WORKSPACE;
     return cuda_status(run_chain_tc(pl, p1, p2, d1->dtype, x, w1, bias1, w2, bias2, y1, y2, workspace,
@@ -482,7 +496,7 @@ int conv_query_chain2(const conv_desc_t* d1, const conv_desc_t* d2, conv_plan_in
     DevInfo d;
     if ((rc = device_info(d)) != CONV_OK) return rc;
     Plan pl;
-    chain_plan(p1, p2, d1->dtype, d, pl);
+    if ((rc = chain_plan(p1, p2, d1->dtype, d, pl)) != CONV_OK) return rc;
     info->algo = pl.algo;
     info->launches = pl.launches;
     info->grid = pl.grid;

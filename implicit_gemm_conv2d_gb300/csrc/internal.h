@@ -161,6 +161,7 @@ cudaError_t run_dgrad_tc(const Plan&, const ConvParams&, int dt, const void* dy,
 // Two-layer forward chain (layer 2's input = layer 1's output), one kernel after packing both
 // weight images into the workspace.
 bool tc_chain_ok(const ConvParams& p1, const ConvParams& p2, int dt, const DevInfo& d);
+int chain_groups(const ConvParams& p1, const ConvParams& p2);  // groups of whole samples the fused kernel runs
 Plan plan_chain_tc(const ConvParams& p1, const ConvParams& p2, int dt, const DevInfo& d);
 cudaError_t run_chain_tc(const Plan&, const ConvParams& p1, const ConvParams& p2, int dt, const void* x,
                          const void* w1, const void* b1, const void* w2, const void* b2, void* y1, void* y2, void* ws,

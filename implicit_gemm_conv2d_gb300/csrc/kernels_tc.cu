@@ -2115,24 +2115,32 @@ dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const T* __restric
 // Two-layer forward chain: y1 = act1(conv1(x) + b1), y2 = act2(conv2(y1) + b2), where conv2's
 // input is conv1's output (IC2 = OC1, H2 x W2 = OH1 x OW1) -- the encoder of PufferLib PR #522
 // (layer 1 -> 3x4 -> layer 2).  A work item is a group of NS whole samples (NS*P1 <= 128
-// layer-1 columns).  Phase 1 is layer 1's forward tile for the group, as in fwd_tc_kernel;
-// its epilogue writes y1 to global memory (the backward needs it) and into a shared-memory
-// slab laid out as conv2's NCHW input.  Phase 2 is layer 2's forward for the same samples
-// (NS*P2 columns), gathered from that slab: y1 never makes a round trip through memory between
-// the layers, and one launch does both.  Both phases share the weight ring (packed images in
-// the caller's workspace, one bulk copy per chunk), the TMEM operand ring and the accumulator.
+// layer-1 columns).  Phase 1 is layer 1's forward tile for the group, as in fwd_tc_kernel
+// (gathered patches in TMEM, weight stages bulk-copied from the packed W1 image); its epilogue
+// writes y1 to global memory (the backward needs it) and into a shared-memory slab laid out as
+// conv2's NCHW input.  Phase 2 is layer 2's forward for the same samples, with the operands'
+// roles swapped because the group has only NS*P2 columns (20 for the encoder): W2 is the TMEM
+// operand (M = 128 output channels) -- the weight producer bulk-copies its packed chunks into
+// the weight ring, well ahead, and the formatter warps move each landed chunk's rows into TMEM
+// -- and the group's layer-2 patches, gathered from the slab into a small ring of patch stages
+// (one per TMEM operand stage, released with it), are the shared-memory operand (N = N2p, the
+// columns rounded up to 16).  y1 never makes a round trip through memory between the layers,
+// layer 2 needs no launch of its own and its MMAs are N2p wide instead of 128.
 // Warp roles (608 threads): warp 0 x producer (phase 1), warp 1 weight producer (W1 chunks,
-// then W2 chunks), warp 2 MMA, warps 3-18 formatters (gather + epilogue of both phases).
+// then W2 chunks), warp 2 MMA, warps 3-18 formatters (phase 1: gather + epilogue; phase 2: W2
+// rows into TMEM, patch stages, epilogue).
 // ======================================================================================
 constexpr int CH_THREADS = 96 + 32 * FA_FMTW;
 
 struct ChainGeom {
     FwdGeom g1;              // layer 1 (tile = NS*P1 columns, OTp1 rows); nw / nraw / xg of the ring
     int ns, ngroups;         // samples per group, groups
-    int OTp2, oc_tiles2;     // layer 2 rows (a single oc tile)
+    int OTp2, oc_tiles2;     // layer 2 output channels (a single tile: the TMEM lanes)
+    int N2p;                 // layer 2 columns of a group, rounded up to 16 (the MMA's N)
     int nchunks2;            // layer 2 K-chunks
     int w_bytes2;            // one layer-2 weight stage
     int stage_bytes;         // weight ring stage = max(w_bytes1, w_bytes2)
+    int patch_bytes;         // one patch stage (N2p rows x 128 bytes, x2 for fp32); na of them
     int dcols;               // accumulator columns = max of the two layers'
     int acol0;               // first TMEM column of the operand stages
     int xs2;                 // bytes per sample in the y1 slab
@@ -2155,8 +2163,8 @@ template <typename T>
 inline int chain_smem(const ConvParams& p1, const ConvParams& p2, const ChainGeom& c)
 {
     using Tr = TcTraits<T>;
-    return 1024 + c.g1.nw * c.stage_bytes + c.g1.nraw * c.g1.raw_bytes + c.slab_bytes + round_up(p1.Kred, Tr::KC) * 4 +
-           round_up(p2.Kred, Tr::KC) * 4 + int(sizeof(ChainBars)) + 16;
+    return 1024 + c.g1.nw * c.stage_bytes + c.g1.nraw * c.g1.raw_bytes + 1024 + c.g1.na * c.patch_bytes + c.slab_bytes +
+           round_up(p1.Kred, Tr::KC) * 4 + round_up(p2.Kred, Tr::KC) * 4 + int(sizeof(ChainBars)) + 16;
 }
 
 template <typename T>
@@ -2174,10 +2182,11 @@ fwd_chain_kernel(const ConvParams p1, const ConvParams p2, const T* __restrict__
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = align1024(smem_raw);
     const int kred1 = round_up(p1.Kred, Tr::KC), kred2 = round_up(p2.Kred, Tr::KC);
-    // Layout: weight stages | raw x slots | y1 slab | k offsets (layer 1, layer 2) | barriers
+    // Layout: weight stages | raw x slots | patch stages | y1 slab | k offsets (layer 1, layer 2) | barriers
     unsigned char* wring = smem;
     unsigned char* raw = wring + g1.nw * cg.stage_bytes;
-    unsigned char* slab = raw + g1.nraw * g1.raw_bytes;
+    unsigned char* pring = align1024(raw + g1.nraw * g1.raw_bytes);  // swizzled MMA operand: 1024-aligned
+    unsigned char* slab = pring + g1.na * cg.patch_bytes;
     int* offk1 = reinterpret_cast<int*>(slab + cg.slab_bytes);
     int* offk2 = offk1 + kred1;
     ChainBars* bars = reinterpret_cast<ChainBars*>(offk2 + kred2);
@@ -2269,7 +2278,7 @@ fwd_chain_kernel(const ConvParams p1, const ConvParams p2, const T* __restrict__
             RingPos wp;
             bool ok = true;
             for (int grp = blockIdx.x; grp < cg.ngroups && ok && !*abort_flag; grp += gridDim.x) {
-                for (int ph = 0; ph < 2 && ok; ++ph) {
+                for (int ph = 0; ph < 2 && ok; ++ph) {  // W1 chunks, then W2 chunks
                     const int n = ph == 0 ? g1.nchunks : cg.nchunks2;
                     const int wb = ph == 0 ? g1.w_bytes : cg.w_bytes2;
                     const unsigned char* src = wpack + (ph == 0 ? size_t(0) : cg.wpack2_off);
@@ -2296,9 +2305,9 @@ fwd_chain_kernel(const ConvParams p1, const ConvParams p2, const T* __restrict__
             bool ok = true;
             for (int grp = blockIdx.x; grp < cg.ngroups && ok && !*abort_flag; grp += gridDim.x) {
                 for (int ph = 0; ph < 2 && ok; ++ph, ++t) {
-                    const int OTp = ph == 0 ? g1.OTp : cg.OTp2;
-                    const uint32_t idesc2 = instr_desc(Tr::fmt, FA_TM, Tr::split ? 2 * OTp : OTp);
-                    const uint32_t idesc1 = instr_desc(Tr::fmt, FA_TM, OTp);
+                    const int N = ph == 0 ? g1.OTp : cg.N2p;  // phase 2: the group's columns
+                    const uint32_t idesc2 = instr_desc(Tr::fmt, FA_TM, Tr::split ? 2 * N : N);
+                    const uint32_t idesc1 = instr_desc(Tr::fmt, FA_TM, N);
                     const int n = ph == 0 ? g1.nchunks : cg.nchunks2;
                     if (t >= 1 && !mbar_wait_or_abort(smem_u32(&bars->acc_empty), (t - 1) & 1, abort_flag)) {
                         report(const_cast<int*>(abort_flag), 8u);
@@ -2314,7 +2323,10 @@ fwd_chain_kernel(const ConvParams p1, const ConvParams p2, const T* __restrict__
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t wa = w_u32 + wp.i * cg.stage_bytes;
+                        // phase 1: B = the W1 chunk in the weight ring; phase 2: B = the patch stage
+                        // (the W2 chunk in the weight ring was moved into the TMEM operand stage)
+                        const uint32_t wa = ph == 0 ? w_u32 + wp.i * cg.stage_bytes
+                                                    : smem_u32(pring) + uint32_t(ap.i * cg.patch_bytes);
                         const uint32_t aa = tmem + uint32_t(cg.acol0 + ap.i * g1.acols);
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
@@ -2345,40 +2357,28 @@ fwd_chain_kernel(const ConvParams p1, const ConvParams p2, const T* __restrict__
         const uint32_t lane_bits = uint32_t(qd * 32) << 16;
         const uint32_t raw_u32 = smem_u32(raw), slab_u32 = smem_u32(slab);
         const uint32_t offk1_u32 = smem_u32(offk1) + uint32_t(sub * KQ * 4);
-        const uint32_t offk2_u32 = smem_u32(offk2) + uint32_t(sub * KQ * 4);
-        RingPos ap, rp;
+        RingPos ap, rp, wp;
         uint32_t t = 0, sph = 0;
         bool ok = true;
+        const int ft = tid - 96;  // formatter thread 0 .. 511
         for (int grp = blockIdx.x; grp < cg.ngroups && ok; grp += gridDim.x) {
             const int b_first = grp * cg.ns, nsamp = min(cg.ns, p1.B - b_first);
-            for (int ph = 0; ph < 2 && ok; ++ph, ++t) {
-                const ConvParams& p = ph == 0 ? p1 : p2;
-                const int n = ph == 0 ? g1.nchunks : cg.nchunks2;
-                const int cols = nsamp * p.P;  // valid columns of this phase
-                // This thread's column within the group (columns past `cols` gather the last
-                // valid column's values: their accumulator rows are computed but never stored).
-                int boff, bmis = 0;
+            // ================= phase 1: layer 1's tile (gathered patches in TMEM) =================
+            {
+                const int cols = nsamp * p1.P;
+                int boff, bmis;
                 {
                     uint32_t bq, pq, oh, ow;
-                    p.dm_P.divmod(uint32_t(min(m, cols - 1)), bq, pq);
-                    p.dm_OW.divmod(pq, oh, ow);
-                    boff = int(bq) * (ph == 0 ? g1.xs : cg.xs2) + (int(oh) * p.S * p.W + int(ow) * p.S) * ES;
-                    if (ph == 0) bmis = int((size_t(b_first + int(bq)) * p1.IHW * ES) & 15);
+                    p1.dm_P.divmod(uint32_t(min(m, cols - 1)), bq, pq);
+                    p1.dm_OW.divmod(pq, oh, ow);
+                    boff = int(bq) * g1.xs + (int(oh) * p1.S * p1.W + int(ow) * p1.S) * ES;
+                    bmis = int((size_t(b_first + int(bq)) * p1.IHW * ES) & 15);
                 }
-                if (ph == 1) {
-                    // the slab holds this group's y1: wait for every formatter warp's writes
-                    if (!mbar_wait_or_abort(smem_u32(&bars->slab_full), sph, abort_flag)) {
-                        report(const_cast<int*>(abort_flag), 32u);
-                        ok = false;
-                        break;
-                    }
-                    sph ^= 1u;
-                }
-                const bool ragged_k = (p.Kred % Tr::KC) != 0;
+                const bool ragged_k = (p1.Kred % Tr::KC) != 0;
                 uint32_t sbase = 0;
                 int xc = 0;
-                for (int kc = 0; kc < n; ++kc, ap.next(g1.na)) {
-                    if (ph == 0 && xc == 0) {
+                for (int kc = 0; kc < g1.nchunks; ++kc, ap.next(g1.na), wp.next(g1.nw)) {
+                    if (xc == 0) {
                         if (!mbar_wait_or_abort(smem_u32(&bars->raw_full[rp.i]), rp.ph, abort_flag)) {
                             report(const_cast<int*>(abort_flag), 1u);
                             ok = false;
@@ -2388,16 +2388,15 @@ fwd_chain_kernel(const ConvParams p1, const ConvParams p2, const T* __restrict__
                         const int cmis = (ic_lo * p1.HW * ES) & 15;
                         sbase = raw_u32 + uint32_t(rp.i * g1.raw_bytes + boff + ((bmis + cmis) & 15));
                     }
-                    if (ph == 1) sbase = slab_u32 + uint32_t(boff);
                     if (ap.wrapped && !mbar_wait_or_abort(smem_u32(&bars->a_empty[ap.i]), ap.ph ^ 1u, abort_flag)) {
                         report(const_cast<int*>(abort_flag), 1u);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t oaddr = (ph == 0 ? offk1_u32 : offk2_u32) + uint32_t(kc * Tr::KC * 4);
+                    const uint32_t oaddr = offk1_u32 + uint32_t(kc * Tr::KC * 4);
                     const uint32_t col = tmem + lane_bits + uint32_t(cg.acol0 + ap.i * g1.acols + sub * KQC);
-                    const int kvalid = (ragged_k && kc == n - 1) ? p.Kred - (kc * Tr::KC + sub * KQ) : KQ;
+                    const int kvalid = (ragged_k && kc == g1.nchunks - 1) ? p1.Kred - (kc * Tr::KC + sub * KQ) : KQ;
                     int o[KQ];
 #pragma unroll
                     for (int i = 0; i < KQ / 4; ++i) {
@@ -2431,7 +2430,7 @@ fwd_chain_kernel(const ConvParams p1, const ConvParams p2, const T* __restrict__
                     tmem_st_wait();
                     tc_fence_before();
                     __syncwarp();
-                    const bool sc_end = ph == 0 && ((++xc == g1.xg) || kc == n - 1);
+                    const bool sc_end = (++xc == g1.xg) || kc == g1.nchunks - 1;
                     if (lane == 0) {
                         mbar_arrive(smem_u32(&bars->a_full[ap.i]));
                         if (sc_end) mbar_arrive(smem_u32(&bars->raw_empty[rp.i]));
@@ -2442,33 +2441,27 @@ fwd_chain_kernel(const ConvParams p1, const ConvParams p2, const T* __restrict__
                     }
                 }
                 if (!ok) break;
-                // Epilogue: TMEM -> bias -> activation -> y (and, in phase 1, the y1 slab).
+                // Epilogue: TMEM -> bias -> activation -> y1 and the y1 slab.
                 if (!mbar_wait_or_abort(smem_u32(&bars->acc_full), t & 1, abort_flag)) {
                     report(const_cast<int*>(abort_flag), 2u);
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const int OTp = ph == 0 ? g1.OTp : cg.OTp2;
-                const T* bias = ph == 0 ? bias1 : bias2;
-                const bool relu = (ph == 0 ? cg.relu1 : cg.relu2) != 0;
                 T* yc = nullptr;
                 uint32_t srow = 0;
                 if (m < cols) {
-                    const int nglob = b_first * p.P + m;
-                    yc = (ph == 0 ? y1 : y2) + col_out(p, nglob);
-                    if (ph == 0) {
-                        uint32_t s1, q1;
-                        p1.dm_P.divmod(uint32_t(m), s1, q1);
-                        srow = slab_u32 + uint32_t(int(s1) * cg.xs2 + int(q1) * ES);  // + oc * P1 * ES
-                    }
+                    yc = y1 + col_out(p1, b_first * p1.P + m);
+                    uint32_t s1, q1;
+                    p1.dm_P.divmod(uint32_t(m), s1, q1);
+                    srow = slab_u32 + uint32_t(int(s1) * cg.xs2 + int(q1) * ES);  // + oc * P1 * ES
                 }
-                for (int cb = sub * 8; cb < OTp; cb += 8 * FA_KSPLIT) {
+                for (int cb = sub * 8; cb < g1.OTp; cb += 8 * FA_KSPLIT) {
                     uint32_t r[8];
                     tmem_ld8(tmem + lane_bits + uint32_t(cb), r);
                     if constexpr (Tr::split) {
                         uint32_t r2[8];
-                        tmem_ld8(tmem + lane_bits + uint32_t(OTp + cb), r2);
+                        tmem_ld8(tmem + lane_bits + uint32_t(g1.OTp + cb), r2);
                         tmem_ld_wait();
 #pragma unroll
                         for (int e = 0; e < 8; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(r2[e]));
@@ -2479,17 +2472,15 @@ fwd_chain_kernel(const ConvParams p1, const ConvParams p2, const T* __restrict__
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
                             const int oc = cb + e;
-                            if (oc < p.OC) {
+                            if (oc < p1.OC) {
                                 float f = __uint_as_float(r[e]);
-                                if (bias) f += Elem<T>::ldg(bias + oc);
-                                if (relu) f = f > 0.f ? f : 0.f;
-                                Elem<T>::st(yc + size_t(oc) * p.P, f);
-                                if (ph == 0) {
-                                    // the slab holds exactly the value y1 holds (rounded to T)
-                                    const uint32_t a = srow + uint32_t(oc * p1.P * ES);
-                                    if constexpr (ES == 4) sts32(a, __float_as_uint(f));
-                                    else sts16(a, __bfloat16_as_ushort(__float2bfloat16_rn(f)));
-                                }
+                                if (bias1) f += Elem<T>::ldg(bias1 + oc);
+                                if (cg.relu1) f = f > 0.f ? f : 0.f;
+                                Elem<T>::st(yc + size_t(oc) * p1.P, f);
+                                // the slab holds exactly the value y1 holds (rounded to T)
+                                const uint32_t a = srow + uint32_t(oc * p1.P * ES);
+                                if constexpr (ES == 4) sts32(a, __float_as_uint(f));
+                                else sts16(a, __bfloat16_as_ushort(__float2bfloat16_rn(f)));
                             }
                         }
                     }
@@ -2498,8 +2489,124 @@ fwd_chain_kernel(const ConvParams p1, const ConvParams p2, const T* __restrict__
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(smem_u32(&bars->acc_empty));
-                    if (ph == 0) mbar_arrive(smem_u32(&bars->slab_full));  // this warp's slab writes are done
+                    mbar_arrive(smem_u32(&bars->slab_full));  // this warp's slab writes are done
                 }
+                ++t;
+            }
+            // ================= phase 2: layer 2 (W2 rows in TMEM, patches in a ring slot) =================
+            {
+                const int cols = nsamp * p2.P;
+                // the slab holds this group's y1: wait for every formatter warp's writes
+                if (!mbar_wait_or_abort(smem_u32(&bars->slab_full), sph, abort_flag)) {
+                    report(const_cast<int*>(abort_flag), 32u);
+                    ok = false;
+                    break;
+                }
+                sph ^= 1u;
+                // W2 rows: this thread's row m (an output channel) and quarter `sub` of each chunk's K
+                // -- two 16-byte units of the chunk in the weight ring (hi, and lo for fp32).
+                const bool wrow = m < cg.OTp2;
+                // Patch stage: this thread's 16-byte unit (row r = a layer-2 column, unit c) if ft < N2p*8.
+                const int prow = ft >> 3, pc = ft & 7;
+                const bool punit = ft < cg.N2p * 8;
+                const bool pvalid = prow < cols;
+                int pboff = 0;
+                {
+                    uint32_t s2, q2, oh, ow;
+                    p2.dm_P.divmod(uint32_t(min(prow, cols - 1)), s2, q2);
+                    p2.dm_OW.divmod(q2, oh, ow);
+                    pboff = int(s2) * cg.xs2 + (int(oh) * p2.S * p2.W + int(ow) * p2.S) * ES;
+                }
+                const uint32_t pst = unit_off<1>(prow, pc);
+                for (int kc = 0; kc < cg.nchunks2; ++kc, ap.next(g1.na), wp.next(g1.nw)) {
+                    if (!mbar_wait_or_abort(smem_u32(&bars->w_full[wp.i]), wp.ph, abort_flag) ||
+                        (ap.wrapped && !mbar_wait_or_abort(smem_u32(&bars->a_empty[ap.i]), ap.ph ^ 1u, abort_flag))) {
+                        report(const_cast<int*>(abort_flag), 1u);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // (a) W2 rows: weight-ring slot -> TMEM operand stage (the columns phase 1's patches use)
+                    const uint32_t col = tmem + lane_bits + uint32_t(cg.acol0 + ap.i * g1.acols + sub * KQC);
+                    {
+                        const uint32_t wslot = smem_u32(wring) + uint32_t(wp.i * cg.stage_bytes);
+                        uint32_t hw[8] = {0, 0, 0, 0, 0, 0, 0, 0}, lw[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                        if (wrow) {
+#pragma unroll
+                            for (int q = 0; q < 2; ++q) {
+                                const int4 h = lds128(wslot + unit_off<1>(m, 2 * sub + q));
+                                hw[4 * q] = h.x; hw[4 * q + 1] = h.y; hw[4 * q + 2] = h.z; hw[4 * q + 3] = h.w;
+                                if constexpr (Tr::split) {
+                                    const int4 l = lds128(wslot + uint32_t(cg.OTp2 * ROWB) + unit_off<1>(m, 2 * sub + q));
+                                    lw[4 * q] = l.x; lw[4 * q + 1] = l.y; lw[4 * q + 2] = l.z; lw[4 * q + 3] = l.w;
+                                }
+                            }
+                        }
+                        tmem_st8(col, hw);
+                        if constexpr (Tr::split) tmem_st8(col + Tr::KC, lw);
+                    }
+                    // (b) this chunk's patch stage (the one of TMEM operand stage ap.i): rows = the
+                    // group's layer-2 columns (zero past `cols`), K-major, 128-byte swizzled; fp32 as
+                    // hi rows then lo rows
+                    if (punit) {
+                        uint32_t pv[Tr::E];
+                        const int k0 = kc * Tr::KC + pc * Tr::E;
+#pragma unroll
+                        for (int e = 0; e < Tr::E; ++e) {
+                            const int k = k0 + e;
+                            pv[e] = 0u;
+                            if (pvalid && k < p2.Kred) {
+                                const uint32_t a = slab_u32 + uint32_t(pboff) + uint32_t(lds32(smem_u32(offk2) + 4u * uint32_t(k)));
+                                pv[e] = ES == 4 ? lds32(a) : lds16(a);
+                            }
+                        }
+                        unsigned char* stage = pring + ap.i * cg.patch_bytes;
+                        put_unit<T>(stage, stage + cg.N2p * ROWB, pst, pv);
+                    }
+                    fence_proxy_async_smem();  // the patch stage, for the tensor core
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&bars->a_full[ap.i]));  // W2 rows and patches ready
+                }
+                if (!ok) break;
+                // Epilogue: lanes = output channels, columns = the group's layer-2 columns.
+                if (!mbar_wait_or_abort(smem_u32(&bars->acc_full), t & 1, abort_flag)) {
+                    report(const_cast<int*>(abort_flag), 2u);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int oc = m;
+                const float bv = (bias2 && oc < p2.OC) ? Elem<T>::ldg(bias2 + oc) : 0.f;
+                for (int cb = sub * 8; cb < cg.N2p; cb += 8 * FA_KSPLIT) {
+                    uint32_t r[8];
+                    tmem_ld8(tmem + lane_bits + uint32_t(cb), r);
+                    if constexpr (Tr::split) {
+                        uint32_t r2[8];
+                        tmem_ld8(tmem + lane_bits + uint32_t(cg.N2p + cb), r2);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(r2[e]));
+                    } else {
+                        tmem_ld_wait();
+                    }
+                    if (oc < p2.OC) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int n2 = cb + e;
+                            if (n2 < cols) {
+                                float f = __uint_as_float(r[e]) + bv;
+                                if (cg.relu2) f = f > 0.f ? f : 0.f;
+                                Elem<T>::st(y2 + col_out(p2, b_first * p2.P + n2) + size_t(oc) * p2.P, f);
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty));
+                ++t;
             }
         }
     }
@@ -2828,10 +2935,12 @@ static ChainGeom chain_geom(const ConvParams& p1, const ConvParams& p2, int xg, 
     cg.ngroups = ceil_div(p1.B, ns);
     cg.OTp2 = round_up(p2.OC, 16);
     cg.oc_tiles2 = 1;
+    cg.N2p = round_up(ns * p2.P, 16);
     cg.nchunks2 = round_up(p2.Kred, Tr::KC) / Tr::KC;
-    cg.w_bytes2 = cg.OTp2 * ROWB * (Tr::split ? 2 : 1);
-    cg.stage_bytes = std::max(cg.g1.w_bytes, cg.w_bytes2);
-    cg.dcols = std::max(cg.g1.dcols, cg.OTp2 * (Tr::split ? 2 : 1));
+    cg.w_bytes2 = cg.OTp2 * ROWB * (Tr::split ? 2 : 1);  // one chunk of the packed W2 image
+    cg.stage_bytes = std::max(cg.g1.w_bytes, cg.w_bytes2);  // a W1 or a W2 chunk
+    cg.patch_bytes = cg.N2p * ROWB * (Tr::split ? 2 : 1);
+    cg.dcols = std::max(cg.g1.dcols, cg.N2p * (Tr::split ? 2 : 1));
     cg.acol0 = round_up(cg.dcols, 32);
     cg.g1.na = std::min(FA_MAXA, (FA_TMEM_COLS - cg.acol0) / cg.g1.acols);
     cg.xs2 = round_up(p2.IHW * es, 16) + 16;  // a sample of conv2's input, 16-byte padded
@@ -2847,7 +2956,10 @@ static bool pick_chain(const ConvParams& p1, const ConvParams& p2, const DevInfo
 {
     using Tr = TcTraits<T>;
     const int otmax = Tr::split ? 128 : 256;
-    if (d.cc_major != 10 || p1.B <= 0 || p1.P > FA_TM || p2.P > FA_TM || p1.OC > otmax || p2.OC > otmax) return false;
+    // layer 2's output channels are the TMEM lanes of its accumulator; its columns (a group's
+    // samples) the MMA's N, twice over for the fp32 hi / lo pair
+    if (d.cc_major != 10 || p1.B <= 0 || p1.P > FA_TM || p2.P > FA_TM || p1.OC > otmax || p2.OC > FA_TM) return false;
+    if (round_up(std::min(FA_TM / p1.P, FA_TM / p2.P) * p2.P, 16) * (Tr::split ? 2 : 1) > 256) return false;
     static const int cfgs[][3] = {{4, 8, 2}, {4, 4, 2}, {4, 2, 2}, {3, 4, 2}, {3, 2, 2}, {2, 2, 2}, {2, 1, 2}};
     for (const auto& c : cfgs) {
         const ChainGeom cg = chain_geom<T>(p1, p2, c[1], c[0], c[2]);
@@ -2856,6 +2968,11 @@ static bool pick_chain(const ConvParams& p1, const ConvParams& p2, const DevInfo
         return true;
     }
     return false;
+}
+
+int chain_groups(const ConvParams& p1, const ConvParams& p2)
+{
+    return ceil_div(p1.B, std::max(1, std::min(FA_TM / p1.P, FA_TM / p2.P)));
 }
 
 bool tc_chain_ok(const ConvParams& p1, const ConvParams& p2, int dt, const DevInfo& d)

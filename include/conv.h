@@ -207,15 +207,17 @@ int conv_bwd_bias(const conv_desc_t* desc, const void* dy, const void* y, void* 
  * On the tensor-core path one kernel computes both layers per group of whole samples: layer 1's
  * output tile goes to y1 and into shared memory, where layer 2 gathers its input from, so y1
  * makes no round trip through memory between the layers and layer 2 needs no launch of its
- * own; both weight images are packed into the workspace first (two small kernels).  Shapes the
- * fused kernel does not take (a layer with more than 128 output positions, or more output
- * channels than one tensor-core tile: 128 fp32 / 256 bf16) run as two conv_fwd calls, and the
- * workspace size is 0.
+ * own; both weight images are packed into the workspace first (two small kernels).  The fused
+ * kernel runs when every CTA gets at most one group of whole samples (the encoder: B up to
+ * about 1500 on 152 SMs); larger batches, and shapes the fused kernel does not take (a layer with
+ * more than 128 output positions, layer 1 with more output channels than one tensor-core tile --
+ * 128 fp32 / 256 bf16 --, layer 2 with more than 128), run as two conv_fwd_ws calls sharing the
+ * workspace.
  *   workspace: at least conv_fwd_chain2_workspace_size(d1, d2) bytes, 16-byte aligned, owned
  *   by the caller; contents ignored on entry and unspecified on return.
  * conv_query_chain2 reports the plan (algo CONV_ALGO_TC when fused, CONV_ALGO_AUTO when it runs
  * as two forward calls); conv_set_algo(CONV_OP_FWD, ...) other than AUTO / TC disables the
- * fused kernel. */
+ * fused kernel (and forces that family for the two calls). */
 size_t conv_fwd_chain2_workspace_size(const conv_desc_t* d1, const conv_desc_t* d2);
 int conv_fwd_chain2(const conv_desc_t* d1, const conv_desc_t* d2, const void* x, const void* w1, const void* bias1,
                     const void* w2, const void* bias2, void* y1, void* y2, void* workspace, size_t workspace_bytes,

@@ -103,7 +103,9 @@ def test_fused_forward_chain(dtype, B):
     d1 = binding.make_desc(B, **L1, relu=1, dtype=tdt)
     d2 = binding.make_desc(B, **L2, relu=0, dtype=tdt)
     q = binding.conv_query_chain2(d1, d2)
-    assert q["algo"] == binding.ALGO_TC and q["launches"] == 3, q
+    # fused while every CTA gets at most one group of 10 samples, else two forward calls
+    fused = (B + 9) // 10 <= torch.cuda.get_device_properties(0).multi_processor_count
+    assert (q["algo"] == binding.ALGO_TC and q["launches"] == 3) if fused else q["algo"] == binding.ALGO_AUTO, q
     ws = torch.empty(binding.conv_fwd_chain2_workspace_size(d1, d2), dtype=torch.uint8, device="cuda")
     y1 = torch.full((B, 128, 3, 4), float("nan"), dtype=tdt, device="cuda")
     y2 = torch.full((B, 128, 1, 2), float("nan"), dtype=tdt, device="cuda")
