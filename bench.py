@@ -49,6 +49,7 @@ PR522_BIAS_GRAD_US = {"layer1": 136.5968, "layer2": 40.9008}
 BIAS_GRAD_BATCH = 32768
 FLUSH_BYTES = 512 << 20
 OPS = ("fwd", "dgrad", "wgrad")
+STEP_OPS = ("fwd", "bwd")  # the timed step: the forward, then the whole backward in one call
 
 
 def flops(B, IC, OC, H, W, K, S, **_):
@@ -57,16 +58,24 @@ def flops(B, IC, OC, H, W, K, S, **_):
 
 
 def alg_bytes(op, B, IC, OC, H, W, K, S, relu, esize):
-    """Algorithmic HBM bytes of one operation: each tensor read or written once."""
+    """Algorithmic HBM bytes of one operation: each tensor read or written once ("bwd": d_input and
+    wgrad in one call read x, dy, w and y once and write dx and dw)."""
     OH, OW = (H - K) // S + 1, (W - K) // S + 1
     nx, ny, nw = B * IC * H * W, B * OC * OH * OW, OC * IC * K * K
     if op == "fwd":
         n = nx + nw + ny
     elif op == "dgrad":
         n = ny + nw + nx + (ny if relu else 0)
+    elif op == "bwd":
+        n = nx + ny + nw + nx + nw + (ny if relu else 0)
     else:
         n = nx + ny + nw + (ny if relu else 0)
     return n * esize
+
+
+def op_flops(op, flops_per_op):
+    """The fused backward does d_input's and wgrad's FLOPs."""
+    return 2 * flops_per_op if op == "bwd" else flops_per_op
 
 
 def parse():
@@ -85,6 +94,8 @@ def parse():
                     help="launch each operation eagerly instead of replaying a captured CUDA graph")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the other-config table, e2e and CPU baseline")
+    ap.add_argument("--step", choices=("fused", "split"), default="fused",
+                    help="fused: conv_fwd_ws then conv_bwd; split: the three operations one call each")
     ap.add_argument("--chain-only", action="store_true",
                     help="time only the fused two-layer forward chain against the two forward calls")
     return ap.parse_args()
@@ -355,6 +366,9 @@ class Workload:
         self.plans = {name: binding.conv_query(op, self.desc) for op, name in zip(step_ops, OPS)}
         self.plans["fwd_plain"] = binding.conv_query(binding.OP_FWD, self.desc)
         self.plans["dgrad_plain"] = binding.conv_query(binding.OP_BWD_DATA, self.desc)
+        self.plans["bwd"] = binding.conv_query(binding.OP_BWD, self.desc)
+        self.ws_bwd = torch.empty(max(16, binding.conv_bwd_workspace_size(self.desc)), dtype=torch.uint8, device=device)
+        self.step_launches = self.plans["fwd"]["launches"] + self.plans["bwd"]["launches"]
 
     def capture(self):
         """One CUDA graph per operation (captured after a warm-up call), so that
@@ -364,11 +378,11 @@ class Workload:
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
-            for o in OPS + ("fwd_plain", "dgrad_plain"):
+            for o in OPS + ("fwd_plain", "dgrad_plain", "bwd"):
                 self.op(o)
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
-        for o in OPS + ("fwd_plain", "dgrad_plain"):
+        for o in OPS + ("fwd_plain", "dgrad_plain", "bwd"):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=s):
                 self.op(o)
@@ -393,6 +407,8 @@ class Workload:
             binding.conv_fwd(self.desc, self.x, self.w, self.y, stream)
         elif name == "dgrad_plain":
             binding.conv_bwd_data(self.desc, self.dy, self.w, relu_y, self.dx, stream)
+        elif name == "bwd":
+            binding.conv_bwd(self.desc, self.x, self.dy, self.w, relu_y, self.dx, self.dw, None, self.ws_bwd, stream)
         else:
             binding.conv_bwd_filter(self.desc, self.x, self.dy, relu_y, self.dw, self.ws, stream)
 
@@ -426,6 +442,30 @@ def time_step(wl, flush_buf, steps, warmup, flush=True):
             per[o].append(e[j].elapsed_time(e[j + 1]))
         total.append(e[0].elapsed_time(e[3]))
     return per, total
+
+
+def time_fused_step(wl, flush_buf, steps, warmup):
+    """Device times (ms) of the step the bench reports: the forward, then conv_bwd (d_input and
+    wgrad in one call); L2 flushed before each step, outside the timed region."""
+    import torch
+    from implicit_gemm_conv2d_gb300 import binding
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        for o in STEP_OPS:
+            wl.run(o)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for i in range(steps):
+        binding.conv_l2_flush(flush_buf)
+        e = ev[i]
+        e[0].record(stream)
+        wl.run("fwd")
+        e[1].record(stream)
+        wl.run("bwd")
+        e[2].record(stream)
+    torch.cuda.synchronize()
+    per = {o: [e[j].elapsed_time(e[j + 1]) for e in ev] for j, o in enumerate(STEP_OPS)}
+    return per, [e[0].elapsed_time(e[2]) for e in ev]
 
 
 def warm_us(wl, iters=200, warmup=50):
@@ -725,13 +765,14 @@ def roofline_of(wl, op, t_ms, sms, sm_mhz, peaks):
     plan = wl.plans[op]
     esz = 4 if wl.dtype == "f32" else 2
     ab = alg_bytes(op, B=wl.B, esize=esz, **wl.shape)
+    fl = op_flops(op, wl.flops)
     pk, src = pipe_peak(plan["algo_name"], wl.dtype, sms, sm_mhz, peaks)
-    t_flop = wl.flops / (pk * 1e12)
+    t_flop = fl / (pk * 1e12)
     t_mem = ab / (peaks["hbm_gbs"] * 1e9)
     t = t_ms * 1e-3
     if t_flop >= t_mem:
         bound = "alu" if plan["algo_name"] != "tc" else "tensor"
-        r = {"bound": bound, "achieved": wl.flops / t / 1e12, "peak": pk, "unit": "TFLOP/s"}
+        r = {"bound": bound, "achieved": fl / t / 1e12, "peak": pk, "unit": "TFLOP/s"}
         src_s = src
     else:
         r = {"bound": "hbm", "achieved": ab / t / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
@@ -739,7 +780,7 @@ def roofline_of(wl, op, t_ms, sms, sm_mhz, peaks):
     r["frac"] = r["achieved"] / r["peak"]
     r["roofline_us"] = max(t_flop, t_mem) * 1e6
     r["algorithmic_bytes"] = ab
-    r["flops"] = wl.flops
+    r["flops"] = fl
     r["peak_source"] = src_s
     return r
 
@@ -774,8 +815,9 @@ def run_ours(args):
         wl.capture()
 
     # ---- the timed region ----
+    step = STEP_OPS if args.step == "fused" else OPS
     for _ in range(args.warmup):
-        for o in OPS:
+        for o in step:
             wl.run(o)
     torch.cuda.synchronize()
     if world > 1:
@@ -783,7 +825,10 @@ def run_ours(args):
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         clk.mark_start()
-        per, total = time_step(wl, flush_buf, args.steps, 0)
+        if args.step == "fused":
+            per, total = time_fused_step(wl, flush_buf, args.steps, 0)
+        else:
+            per, total = time_step(wl, flush_buf, args.steps, 0)
         torch.cuda.synchronize()
         clk.mark_end()
     if world > 1:
@@ -799,12 +844,19 @@ def run_ours(args):
         return 0
 
     # ---- per-op summary and roofline of the dominant kernel ----
-    op_ms = {o: statistics.mean(per[o]) for o in OPS}
     clocks = clk.summary()
     sm_mhz = clocks["sm_max_mhz"] or peaks.get("sm_max_mhz", 2070.0)
-    dom = max(OPS, key=lambda o: op_ms[o])
+    step_ms = {o: statistics.mean(per[o]) for o in step}
+    dom = max(step, key=lambda o: step_ms[o])
+    # the three operations one call each (cold L2), for the per-operation table
+    if args.step == "fused":
+        per3, _ = time_step(wl, flush_buf, 50, 3)
+        op_ms = {o: statistics.mean(per3[o]) for o in OPS}
+        op_ms["bwd"] = step_ms["bwd"]
+    else:
+        op_ms = dict(step_ms)
     plan = wl.plans[dom]
-    roofline = roofline_of(wl, dom, op_ms[dom], sms, sm_mhz, peaks)
+    roofline = roofline_of(wl, dom, step_ms[dom], sms, sm_mhz, peaks)
     roofline["kernel"] = f"{dom} ({plan['algo_name']}, {plan['launches']} launch(es))"
     roofline["traffic"] = read_traffic(f"{dom}:{args.layer}:{args.dtype}:B{args.batch}")
     roofline["traffic_note"] = ("dram__bytes_read.sum + dram__bytes_write.sum per call (sum over its launches) from "
@@ -812,9 +864,9 @@ def run_ours(args):
                                 "lines still dirty in L2 when the kernel ends are not in dram__bytes_write, so "
                                 "the figure is mostly reads; null when the kernel source changed since")
     ops = {}
-    for o in OPS:
+    for o in op_ms:
         r = roofline_of(wl, o, op_ms[o], sms, sm_mhz, peaks)
-        ops[o] = {"us": op_ms[o] * 1e3, "gflops": wl.flops / (op_ms[o] * 1e-3) / 1e9,
+        ops[o] = {"us": op_ms[o] * 1e3, "gflops": op_flops(o, wl.flops) / (op_ms[o] * 1e-3) / 1e9,
                   "algo": wl.plans[o]["algo_name"], "launches": wl.plans[o]["launches"],
                   "bound": r["bound"], "frac": r["frac"], "roofline_us": r["roofline_us"]}
     # The no-workspace entry points (weights formatted inside the kernels), same workload, cold L2.
@@ -833,14 +885,16 @@ def run_ours(args):
         "dtype": args.dtype, "data": "synthetic",
         "config": dict(workload_config(args.layer, args.dtype, args.batch),
                        l2="flushed (512 MiB write) between timed steps, outside the timed region",
-                       calls="conv_fwd_ws, conv_bwd_data_ws (caller-owned workspaces), conv_bwd_filter",
+                       calls=("step: conv_fwd_ws, then conv_bwd (d_input + wgrad in one launch), caller-owned "
+                              "workspaces" if args.step == "fused" else
+                              "step: conv_fwd_ws, conv_bwd_data_ws, conv_bwd_filter (caller-owned workspaces)"),
                        launch=("each operation replayed from a captured CUDA graph" if not args.no_graphs
                                else "eager launches"),
                        algo=args.algo),
         "ops": ops,
         "ops_no_workspace": plain,
         "roofline": roofline,
-        "gpu_launches": wl.launches * args.steps,
+        "gpu_launches": (wl.step_launches if args.step == "fused" else wl.launches) * args.steps,
         "clocks": clocks,
         "peaks": {"source": peaks_kind, "hbm_gbs": peaks["hbm_gbs"], "bf16_tflops": peaks.get("bf16_tflops")},
     }

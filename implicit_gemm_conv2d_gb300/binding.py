@@ -22,7 +22,7 @@ from . import build as _build
 
 F32, BF16 = 0, 1
 ALGO_AUTO, ALGO_DIRECT, ALGO_FFMA, ALGO_TC = 0, 1, 2, 3
-OP_FWD, OP_BWD_DATA, OP_BWD_FILTER, OP_BWD_BIAS, OP_FWD_WS, OP_BWD_DATA_WS = 0, 1, 2, 3, 4, 5
+OP_FWD, OP_BWD_DATA, OP_BWD_FILTER, OP_BWD_BIAS, OP_FWD_WS, OP_BWD_DATA_WS, OP_BWD = 0, 1, 2, 3, 4, 5, 6
 ALGO_NAMES = {0: "auto", 1: "direct", 2: "ffma", 3: "tc"}
 
 _DT = {torch.float32: F32, torch.bfloat16: BF16}
@@ -55,7 +55,8 @@ EXPORTS = ["conv_fwd", "conv_bwd_data", "conv_bwd_filter_workspace_size", "conv_
            "conv_device_status", "conv_fwd_bias", "conv_bwd_bias",
            "conv_wait_selftest", "conv_query_for_device", "conv_fwd_workspace_size", "conv_fwd_ws",
            "conv_bwd_data_workspace_size", "conv_bwd_data_ws", "conv_bwd_filter_bias",
-           "conv_fwd_chain2_workspace_size", "conv_fwd_chain2", "conv_query_chain2"]
+           "conv_fwd_chain2_workspace_size", "conv_fwd_chain2", "conv_query_chain2", "conv_bwd_workspace_size",
+           "conv_bwd"]
 STATUS_WAIT_SELFTEST = 1 << 30
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -107,6 +108,9 @@ def lib():
         L.conv_fwd_chain2_workspace_size.restype = sz
         L.conv_fwd_chain2.argtypes = [dp, dp] + [vp] * 8 + [sz, vp]
         L.conv_query_chain2.argtypes = [dp, dp, ctypes.POINTER(PlanInfo)]
+        L.conv_bwd_workspace_size.argtypes = [dp]
+        L.conv_bwd_workspace_size.restype = sz
+        L.conv_bwd.argtypes = [dp] + [vp] * 8 + [sz, vp]
         _lib = L
         return L
 
@@ -221,6 +225,17 @@ def conv_query_chain2(d1: ConvDesc, d2: ConvDesc) -> dict:
     d = info.as_dict()
     d["algo_name"] = ALGO_NAMES.get(d["algo"], "?")
     return d
+
+
+def conv_bwd_workspace_size(desc: ConvDesc) -> int:
+    return int(lib().conv_bwd_workspace_size(ctypes.byref(desc)))
+
+
+def conv_bwd(desc: ConvDesc, x, dy, w, y, dx, dw, db, workspace, stream=None) -> None:
+    """The whole backward: dx, dw and (db not None) db, d_input and wgrad in one launch."""
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().conv_bwd(ctypes.byref(desc), _ptr(x), _ptr(dy), _ptr(w), _ptr(y), _ptr(dx), _ptr(dw), _ptr(db),
+                          _ptr(workspace), nbytes, _stream(stream)), "conv_bwd")
 
 
 def conv_bwd_filter_noalloc(desc: ConvDesc, x, dy, y, dw, stream=None) -> None:

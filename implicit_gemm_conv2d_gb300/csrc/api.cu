@@ -141,6 +141,29 @@ int choose_bgrad(const ConvParams& p, int dt, const DevInfo& d, Plan& pl)
     return CONV_OK;
 }
 
+// The fused backward when both operations run on the tensor cores, else d_input (workspace path)
+// then wgrad, one after the other, sharing the workspace (laid out one after the other).
+int choose_bwd(const ConvParams& p, int dt, const DevInfo& d, Plan& pl)
+{
+    Plan a, b;
+    int rc = choose_dgrad(p, dt, d, true, a);
+    if (rc == CONV_OK) rc = choose_wgrad(p, dt, d, b);
+    if (rc != CONV_OK) return rc;
+    if (a.algo == ALGO_TC && b.algo == ALGO_TC && tc_bwd_ok(p, dt, d)) {
+        pl = plan_bwd_tc(p, dt, d);
+        return CONV_OK;
+    }
+    pl = Plan();
+    pl.algo = ALGO_AUTO;  // two calls
+    pl.launches = a.launches + b.launches;
+    pl.grid = std::max(a.grid, b.grid);
+    pl.block = std::max(a.block, b.block);
+    pl.smem = std::max(a.smem, b.smem);
+    pl.splits = b.splits;
+    pl.workspace = (a.workspace + 255) / 256 * 256 + b.workspace;
+    return CONV_OK;
+}
+
 int choose(int op, const ConvParams& p, int dt, const DevInfo& d, Plan& pl)
 {
     switch (op) {
@@ -150,6 +173,7 @@ int choose(int op, const ConvParams& p, int dt, const DevInfo& d, Plan& pl)
     case CONV_OP_BWD_BIAS: return choose_bgrad(p, dt, d, pl);
     case CONV_OP_FWD_WS: return choose_fwd(p, dt, d, true, pl);
     case CONV_OP_BWD_DATA_WS: return choose_dgrad(p, dt, d, true, pl);
+    case CONV_OP_BWD: return choose_bwd(p, dt, d, pl);
     default: return CONV_ERR_UNSUPPORTED;
     }
 }
@@ -244,7 +268,7 @@ int conv_out_dims(const conv_desc_t* desc, int32_t* OH, int32_t* OW)
 
 int conv_set_algo(int op, int algo)
 {
-    if (op < 0 || op > 5 || algo < ALGO_AUTO || algo > ALGO_TC) return CONV_ERR_UNSUPPORTED;
+    if (op < 0 || op > 5 || algo < ALGO_AUTO || algo > ALGO_TC) return CONV_ERR_UNSUPPORTED;  // op 6: ops 1, 2
     if (op == CONV_OP_BWD_BIAS && algo != ALGO_AUTO && algo != ALGO_DIRECT) return CONV_ERR_UNSUPPORTED;
     // the workspace-taking entry points share the choice of their operation
     if (op == CONV_OP_FWD_WS) op = CONV_OP_FWD;
@@ -259,7 +283,7 @@ static int query_on(int op, const conv_desc_t* desc, const DevInfo& d, conv_plan
     int rc = make_params(desc, p);
     if (rc != CONV_OK) return rc;
     if (!info) return CONV_ERR_NULL;
-    if (op < 0 || op > 5) return CONV_ERR_UNSUPPORTED;
+    if (op < 0 || op > 6) return CONV_ERR_UNSUPPORTED;
     Plan pl;
     if ((rc = choose(op, p, desc->dtype, d, pl)) != CONV_OK) return rc;
     info->algo = pl.algo;
@@ -278,7 +302,7 @@ int conv_query(int op, const conv_desc_t* desc, conv_plan_info_t* info)
     int rc = make_params(desc, p);
     if (rc != CONV_OK) return rc;
     if (!info) return CONV_ERR_NULL;
-    if (op < 0 || op > 5) return CONV_ERR_UNSUPPORTED;
+    if (op < 0 || op > 6) return CONV_ERR_UNSUPPORTED;
     DevInfo d;
     if ((rc = device_info(d)) != CONV_OK) return rc;
     return query_on(op, desc, d, info);
@@ -505,6 +529,36 @@ int conv_query_chain2(const conv_desc_t* d1, const conv_desc_t* d2, conv_plan_in
     info->splits = pl.splits;
     info->workspace = pl.workspace;
     return CONV_OK;
+}
+
+size_t conv_bwd_workspace_size(const conv_desc_t* desc) { return plan_workspace(CONV_OP_BWD, desc); }
+
+int conv_bwd(const conv_desc_t* desc, const void* x, const void* dy, const void* w, const void* y, void* dx,
+             void* dw, void* db, void* workspace, size_t workspace_bytes, conv_stream_t stream)
+{
+    ConvParams p;
+    int rc = make_params(desc, p);
+    if (rc != CONV_OK) return rc;
+    if (!dw || !w) return CONV_ERR_NULL;
+    if (p.B > 0 && (!x || !dy || !dx || (p.relu && !y))) return CONV_ERR_NULL;
+    if (!aligned16(dw) || !aligned16(w) || (db && !aligned16(db)) || (workspace && !aligned16(workspace)) ||
+        (p.B > 0 && (!aligned16(x) || !aligned16(dy) || !aligned16(dx) || (p.relu && !aligned16(y)))))
+        return CONV_ERR_ALIGN;
+    DevInfo d;
+    if ((rc = device_info(d)) != CONV_OK) return rc;
+    Plan pl;
+    if ((rc = choose_bwd(p, desc->dtype, d, pl)) != CONV_OK) return rc;
+    if (pl.workspace > 0 && (!workspace || workspace_bytes < pl.workspace)) return CONV_ERR_WORKSPACE;
+    if (pl.algo == ALGO_TC)
+        return cuda_status(run_bwd_tc(pl, p, desc->dtype, d, x, dy, w, y, dx, dw, db, workspace,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+    // two calls: d_input's workspace first, wgrad's after it
+    Plan a;
+    if ((rc = choose_dgrad(p, desc->dtype, d, true, a)) != CONV_OK) return rc;
+    const size_t off = (a.workspace + 255) / 256 * 256;
+    if ((rc = dgrad_impl(desc, dy, w, y, dx, workspace, a.workspace, true, stream)) != CONV_OK) return rc;
+    unsigned char* wws = workspace ? static_cast<unsigned char*>(workspace) + off : nullptr;
+    return wgrad_impl(desc, x, dy, y, dw, db, wws, workspace_bytes > off ? workspace_bytes - off : 0, stream);
 }
 
 uint64_t conv_fastdivmod_check(uint32_t d, uint32_t lo, uint32_t hi)

@@ -158,6 +158,12 @@ bool tc_dgrad_ok(const ConvParams& p, int dt, const DevInfo& d, bool packed);
 Plan plan_dgrad_tc(const ConvParams& p, int dt, const DevInfo& d, bool packed);
 cudaError_t run_dgrad_tc(const Plan&, const ConvParams&, int dt, const void* dy, const void* w,
                          const void* y, void* dx, void* ws, cudaStream_t s);
+// Fused backward: d_input and wgrad (and with db the bias gradient) in one launch after packing
+// W^T; the split reduction follows.
+bool tc_bwd_ok(const ConvParams& p, int dt, const DevInfo& d);
+Plan plan_bwd_tc(const ConvParams& p, int dt, const DevInfo& d);
+cudaError_t run_bwd_tc(const Plan&, const ConvParams& p, int dt, const DevInfo& d, const void* x, const void* dy,
+                       const void* w, const void* y, void* dx, void* dw, void* db, void* ws, cudaStream_t s);
 // Two-layer forward chain (layer 2's input = layer 1's output), one kernel after packing both
 // weight images into the workspace.
 bool tc_chain_ok(const ConvParams& p1, const ConvParams& p2, int dt, const DevInfo& d);

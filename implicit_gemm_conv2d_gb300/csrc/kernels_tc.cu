@@ -1082,10 +1082,13 @@ inline int wgrad_smem(const TcWgradGeom& g)
     return 1024 + g.nbs * g.b_bytes + g.raws * g.raw_bytes + int(sizeof(WgBars)) + 8 * g.cnp + 16;
 }
 
+// The wgrad CTA's work: tiles item0, item0 + istride, ... (its own kernel passes the block
+// index and the grid size; the fused backward kernel its own numbering of the wgrad CTAs).
 template <typename T, bool RELU>
-__global__ void __launch_bounds__(WG_THREADS, 1)
-wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict__ dy,
-                const T* __restrict__ y, float* __restrict__ ws, float* __restrict__ bpart, const TcWgradGeom geo)
+__device__ __forceinline__ void wgrad_tc_body(const ConvParams& p, const T* __restrict__ x, const T* __restrict__ dy,
+                                              const T* __restrict__ y, float* __restrict__ ws,
+                                              float* __restrict__ bpart, const TcWgradGeom& geo, const int item0,
+                                              const int istride)
 {
     using Tr = TcTraits<T>;
     constexpr int ES = int(sizeof(T));
@@ -1185,7 +1188,7 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
                 return bulk;
             };
             RingPos rp;
-            for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+            for (int tile = item0; tile < total && !*abort_flag; tile += istride) {
                 const TileInfo ti = decode(tile);
                 const int xbytes = (ti.ic_hi - ti.ic_lo + 1) * p.HW * ES;
                 for (int kc = 0; kc < ti.nchunks; ++kc, rp.next(geo.raws)) {
@@ -1242,7 +1245,7 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
             const int ksteps = geo.cnp / KS;
             RingPos ap, bp;
             uint32_t t = 0;
-            for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x, ++t) {
+            for (int tile = item0; tile < total && !*abort_flag; tile += istride, ++t) {
                 const TileInfo ti = decode(tile);
                 bool ok = true;
                 if (t >= 1 && !mbar_wait_or_abort(smem_u32(&bars->acc_empty), (t - 1) & 1, abort_flag)) {
@@ -1343,7 +1346,7 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
                 }
             RingPos rp, ap;
             uint32_t t = 0;
-            for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++t) {
+            for (int tile = item0; tile < total; tile += istride, ++t) {
                 const TileInfo ti = decode(tile);
                 // The bias gradient rides on the first k-tile of each split (one per (split, oc
                 // tile)): the sum of this thread's masked g values, chunk by chunk in ascending
@@ -1487,7 +1490,7 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
             for (int i = 0; i < XMAXR; ++i) uo[i] = unit_off<1>(rbase + i * rstep, cfix);
             RingPos rp, bp;
             uint32_t t = 0;
-            for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++t) {
+            for (int tile = item0; tile < total; tile += istride, ++t) {
                 const TileInfo ti = decode(tile);
                 // Byte offsets of this thread's rows k = k0 + rbase + i*rstep (-1: past Kred).
                 int ko[XMAXR];
@@ -1563,6 +1566,14 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+}
+
+template <typename T, bool RELU>
+__global__ void __launch_bounds__(WG_THREADS, 1)
+wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict__ dy,
+                const T* __restrict__ y, float* __restrict__ ws, float* __restrict__ bpart, const TcWgradGeom geo)
+{
+    wgrad_tc_body<T, RELU>(p, x, dy, y, ws, bpart, geo, int(blockIdx.x), int(gridDim.x));
 }
 
 // ======================================================================================
@@ -1677,11 +1688,12 @@ inline int dgrad_smem(const ConvParams& p, const TcDgradGeom& g)
            16 + p.HW * DG_PROW * 4 + int(sizeof(DgBars)) + 16;
 }
 
+// The d_input CTA's work: work items item0, item0 + istride, ... (see wgrad_tc_body).
 template <typename T, bool RELU>
-__global__ void __launch_bounds__(DG_THREADS, 1)
-dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const T* __restrict__ w,
-                const unsigned char* __restrict__ wpack, const T* __restrict__ y, T* __restrict__ dx,
-                const TcDgradGeom geo)
+__device__ __forceinline__ void dgrad_tc_body(const ConvParams& p, const T* __restrict__ dy, const T* __restrict__ w,
+                                              const unsigned char* __restrict__ wpack, const T* __restrict__ y,
+                                              T* __restrict__ dx, const TcDgradGeom& geo, const int item0,
+                                              const int istride)
 {
     using Tr = TcTraits<T>;
     extern __shared__ unsigned char smem_raw[];
@@ -1766,7 +1778,7 @@ dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const T* __restric
         if (warp == DG_WF0 && lane == 0) {
             RingPos wp;
             bool ok = true;
-            for (int wi = blockIdx.x; wi < nwork && ok && !*abort_flag; wi += gridDim.x) {
+            for (int wi = item0; wi < nwork && ok && !*abort_flag; wi += istride) {
                 int kt_lo, kt_hi;
                 ktrange(wi, kt_lo, kt_hi);
                 const unsigned char* src = wpack + size_t(kt_lo) * geo.nch * geo.w_tile;
@@ -1804,11 +1816,11 @@ dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const T* __restric
         auto advance = [&](Seq& s) -> bool {
             if (++s.ch < geo.nch) return true;
             s.ch = 0;
-            return ++s.kt < s.kt_hi || first(s, s.wi + int(gridDim.x));
+            return ++s.kt < s.kt_hi || first(s, s.wi + istride);
         };
         auto k0_of = [&](const Seq& s) { return s.kt * geo.CIC * p.KK; };
         Seq cur;
-        bool have = first(cur, int(blockIdx.x));
+        bool have = first(cur, item0);
         if (have) stage_wt_dgrad<T>(slot0, w, p, k0_of(cur), cur.ch * Tr::KC, geo.KTp, wf, lane);
         cp_async_commit();
         uint32_t slot = 0;
@@ -1846,7 +1858,7 @@ dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const T* __restric
             const uint32_t w_u32 = smem_u32(wring);
             RingPos wp, abp, dbp;
             bool ok = true;
-            for (int wi = blockIdx.x; wi < nwork && ok && !*abort_flag; wi += gridDim.x, abp.next(geo.nab)) {
+            for (int wi = item0; wi < nwork && ok && !*abort_flag; wi += istride, abp.next(geo.nab)) {
                 int kt_lo, kt_hi;
                 ktrange(wi, kt_lo, kt_hi);
                 if (!mbar_wait_or_abort(smem_u32(&bars->a_full[abp.i]), abp.ph, abort_flag)) {
@@ -1983,15 +1995,15 @@ dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const T* __restric
         };
         RingPos abp, dbp;
         bool ok = true;
-        const int first = blockIdx.x;
+        const int first = item0;
         if (first < nwork) ok = build_g(first % geo.ntiles, abp);
-        for (int wi = first; wi < nwork && ok; wi += gridDim.x) {
+        for (int wi = first; wi < nwork && ok; wi += istride) {
             const int tile = wi % geo.ntiles;
             int kt_lo, kt_hi;
             ktrange(wi, kt_lo, kt_hi);
             RingPos nab = abp;
             nab.next(geo.nab);
-            const int next = wi + int(gridDim.x);
+            const int next = wi + istride;
             // With two G buffers the next tile's G is written before this tile's k-tiles
             // are read out, so the MMAs move on to it without waiting.
             if (geo.nab == 2 && next < nwork && !(ok = build_g(next % geo.ntiles, nab))) break;
@@ -2109,6 +2121,38 @@ dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const T* __restric
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+}
+
+template <typename T, bool RELU>
+__global__ void __launch_bounds__(DG_THREADS, 1)
+dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const T* __restrict__ w,
+                const unsigned char* __restrict__ wpack, const T* __restrict__ y, T* __restrict__ dx,
+                const TcDgradGeom geo)
+{
+    dgrad_tc_body<T, RELU>(p, dy, w, wpack, y, dx, geo, int(blockIdx.x), int(gridDim.x));
+}
+
+// ======================================================================================
+// Fused backward: d_input and wgrad in one launch, one work item per CTA.  CTAs [0, n_wg) run
+// one wgrad tile each (the long items, started first); the CTAs after them run d_input's work
+// items, cut into k-tile ranges (disjoint dx channels: no reduction) so that they are short.
+// The block scheduler starts the CTAs in index order as SMs free up, so the short d_input items
+// fill the SMs the wgrad tiles leave idle and backfill the others as the wgrad tiles finish.
+// Both operations compute exactly as in their own kernels.
+// ======================================================================================
+static_assert(DG_THREADS == WG_THREADS, "one block shape for both operations");
+
+template <typename T, bool RELU>
+__global__ void __launch_bounds__(DG_THREADS, 1)
+bwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict__ dy, const T* __restrict__ w,
+              const unsigned char* __restrict__ wpack, const T* __restrict__ y, T* __restrict__ dx,
+              float* __restrict__ ws, float* __restrict__ bpart, const TcDgradGeom dgeo, const TcWgradGeom wgeo,
+              const int n_wg)
+{
+    if (int(blockIdx.x) < n_wg)
+        wgrad_tc_body<T, RELU>(p, x, dy, y, ws, bpart, wgeo, int(blockIdx.x), n_wg);
+    else
+        dgrad_tc_body<T, RELU>(p, dy, w, wpack, y, dx, dgeo, int(blockIdx.x) - n_wg, int(gridDim.x) - n_wg);
 }
 
 // ======================================================================================
@@ -2914,6 +2958,99 @@ cudaError_t run_dgrad_tc(const Plan& pl, const ConvParams& p, int dt, const void
 {
     return dt == DT_F32 ? dgrad_tc_t<float>(pl, p, dy, w, y, dx, ws, s)
                         : dgrad_tc_t<__nv_bfloat16>(pl, p, dy, w, y, dx, ws, s);
+}
+
+// ---- fused backward (d_input + wgrad in one launch) -----------------------------------------
+// wgrad's own geometry (its tiles are the long items) and d_input's workspace-path geometry with
+// its k-tiles cut into DG_BWD_RANGES ranges per sample tile (short items that backfill).
+constexpr int DG_BWD_RANGES = 3;
+
+template <typename T>
+static bool pick_bwd(const ConvParams& p, const DevInfo& d, TcDgradGeom& dg, TcWgradGeom& wg)
+{
+    if (d.cc_major != 10 || p.B <= 0) return false;
+    if (!pick_dgrad<T>(p, d, true, dg) || !pick_wgrad<T>(p, d, wg)) return false;
+    dg.kt_per = ceil_div(dg.nkt, std::min(dg.nkt, DG_BWD_RANGES));
+    dg.ktsplit = ceil_div(dg.nkt, dg.kt_per);
+    return true;
+}
+
+template <typename T>
+static size_t bwd_wgrad_offset(const TcDgradGeom& dg)
+{
+    return round_up(size_t(dg.nkt) * dg.nch * dg.w_tile, size_t(256));
+}
+
+bool tc_bwd_ok(const ConvParams& p, int dt, const DevInfo& d)
+{
+    TcDgradGeom dg;
+    TcWgradGeom wg;
+    return dt == DT_BF16 ? pick_bwd<__nv_bfloat16>(p, d, dg, wg) : pick_bwd<float>(p, d, dg, wg);
+}
+
+Plan plan_bwd_tc(const ConvParams& p, int dt, const DevInfo& d)
+{
+    TcDgradGeom dg;
+    TcWgradGeom wg;
+    Plan pl;
+    if (dt == DT_BF16) {
+        pick_bwd<__nv_bfloat16>(p, d, dg, wg);
+        pl.smem = std::max(dgrad_smem<__nv_bfloat16>(p, dg), wgrad_smem<__nv_bfloat16>(wg));
+        pl.workspace = bwd_wgrad_offset<__nv_bfloat16>(dg);
+    } else {
+        pick_bwd<float>(p, d, dg, wg);
+        pl.smem = std::max(dgrad_smem<float>(p, dg), wgrad_smem<float>(wg));
+        pl.workspace = bwd_wgrad_offset<float>(dg);
+    }
+    pl.algo = ALGO_TC;
+    pl.launches = 3;  // pack W^T, the fused kernel, the split reduction
+    pl.block = DG_THREADS;
+    pl.splits = wg.splits;
+    const int n_wg = wg.k_tiles * wg.oc_tiles * wg.splits;
+    pl.grid = n_wg + dg.ntiles * dg.ktsplit;  // one work item per CTA
+    pl.variant = n_wg;
+    // packed W^T | split-K partials | bias partial channel sums (two G lane groups per split at most)
+    pl.workspace += size_t(wg.splits) * p.OC * wg.kpad * sizeof(float) + size_t(wg.splits) * 2 * p.OC * sizeof(float);
+    return pl;
+}
+
+template <typename T>
+static cudaError_t bwd_tc_t(const Plan& pl, const ConvParams& p, const DevInfo& d, const void* x, const void* dy,
+                            const void* w, const void* y, void* dx, void* dw, void* db, void* ws, cudaStream_t s)
+{
+    TcDgradGeom dg;
+    TcWgradGeom wg;
+    if (!pick_bwd<T>(p, d, dg, wg)) return cudaErrorInvalidValue;
+    const int n_wg = pl.variant;
+    unsigned char* wsb = static_cast<unsigned char*>(ws);
+    float* part = reinterpret_cast<float*>(wsb + bwd_wgrad_offset<T>(dg));
+    float* bpart = db ? part + size_t(wg.splits) * p.OC * wg.kpad : nullptr;
+    const dim3 pgrid(ceil_div(dg.KTp * 8, 256), dg.nch, dg.nkt);
+    pack_dgrad_w_kernel<T><<<pgrid, 256, 0, s>>>(p, (const T*)w, wsb, dg.nch, dg.CIC, dg.KTp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+#define IG_LAUNCH_BWD_TC(R)                                                                                  \
+    do {                                                                                                     \
+        e = ensure_smem<bwd_tc_kernel<T, R>>(pl.smem);                                                       \
+        if (e == cudaSuccess)                                                                                \
+            e = launch_ex(bwd_tc_kernel<T, R>, dim3(pl.grid), dim3(pl.block), pl.smem, s, 1, true, p,        \
+                          (const T*)x, (const T*)dy, (const T*)w, (const unsigned char*)wsb, (const T*)y,    \
+                          (T*)dx, part, bpart, dg, wg, n_wg);                                                 \
+    } while (0)
+    if (p.relu) IG_LAUNCH_BWD_TC(true);
+    else IG_LAUNCH_BWD_TC(false);
+#undef IG_LAUNCH_BWD_TC
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return run_wgrad_reduce(p, dt_of_tc<T>(), part, wg.splits, wg.kpad, dw, s, true, bpart,
+                            wg.splits * (WgRoles<T>::g_warps / 4), db);
+}
+
+cudaError_t run_bwd_tc(const Plan& pl, const ConvParams& p, int dt, const DevInfo& d, const void* x, const void* dy,
+                       const void* w, const void* y, void* dx, void* dw, void* db, void* ws, cudaStream_t s)
+{
+    return dt == DT_F32 ? bwd_tc_t<float>(pl, p, d, x, dy, w, y, dx, dw, db, ws, s)
+                        : bwd_tc_t<__nv_bfloat16>(pl, p, d, x, dy, w, y, dx, dw, db, ws, s);
 }
 
 // ---- two-layer forward chain ----------------------------------------------------------

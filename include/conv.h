@@ -101,7 +101,8 @@ typedef enum {
 typedef enum {
     CONV_OP_FWD = 0, CONV_OP_BWD_DATA = 1, CONV_OP_BWD_FILTER = 2, CONV_OP_BWD_BIAS = 3,
     CONV_OP_FWD_WS = 4,      /* conv_fwd_ws / conv_fwd_bias with a workspace (conv_query only) */
-    CONV_OP_BWD_DATA_WS = 5  /* conv_bwd_data_ws (conv_query only)                           */
+    CONV_OP_BWD_DATA_WS = 5, /* conv_bwd_data_ws (conv_query only)                           */
+    CONV_OP_BWD = 6          /* conv_bwd, the fused backward (conv_query only)              */
 } conv_op_t;
 
 /* Forward:  y = act(conv(x, w)).
@@ -177,6 +178,22 @@ int conv_bwd_filter(const conv_desc_t* desc, const void* x, const void* dy, cons
  *   conv_bwd_filter_workspace_size, serves both)   db: (OC), written. */
 int conv_bwd_filter_bias(const conv_desc_t* desc, const void* x, const void* dy, const void* y, void* dw,
                          void* db, void* workspace, size_t workspace_bytes, conv_stream_t stream);
+
+/* The whole backward in one call:  dx as conv_bwd_data, dw as conv_bwd_filter and, when db is
+ * not NULL, db as conv_bwd_filter_bias -- PufferLib PR #522 times "backward" as wgrad plus
+ * d_input together.  On the tensor-core path d_input and wgrad run in ONE launch (after W^T is
+ * packed into the workspace, and before the split reduction), one work item per CTA: first the
+ * wgrad tiles (the long items), then d_input's work items cut into k-tile ranges (short items:
+ * disjoint dx channels, no reduction), so that d_input fills the SMs the wgrad tiles leave idle
+ * and backfills the others as they finish.  Each operation computes exactly as in its own
+ * kernel: dx is bit for bit conv_bwd_data's and dw conv_bwd_filter's.  Otherwise the two calls
+ * run one after the other.
+ *   x, dy, w, y (required when relu): inputs; dx, dw, db (may be NULL): written.
+ *   workspace: at least conv_bwd_workspace_size(desc) bytes, 16-byte aligned, owned by the
+ *   caller, contents ignored on entry and unspecified on return. */
+size_t conv_bwd_workspace_size(const conv_desc_t* desc);
+int conv_bwd(const conv_desc_t* desc, const void* x, const void* dy, const void* w, const void* y, void* dx,
+             void* dw, void* db, void* workspace, size_t workspace_bytes, conv_stream_t stream);
 
 /* Bias gradient:  db[oc] = sum over b, oh, ow of g (g = dy masked by y > 0 when
  * relu), accumulated in fp32 and rounded once to the dtype.  One kernel: the

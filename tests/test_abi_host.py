@@ -72,6 +72,8 @@ def test_invalid_descriptor(L, bad):
     assert L.conv_fwd_chain2(ctypes.byref(d), ctypes.byref(d), fake, fake, None, fake, None, fake, fake, fake,
                              1 << 30, None) == -2
     assert L.conv_fwd_chain2_workspace_size(ctypes.byref(d), ctypes.byref(d)) == 0
+    assert L.conv_bwd(ctypes.byref(d), fake, fake, fake, fake, fake, fake, None, fake, 1 << 30, None) == -2
+    assert L.conv_bwd_workspace_size(ctypes.byref(d)) == 0
     assert L.conv_fwd_workspace_size(ctypes.byref(d)) == 0
     assert L.conv_bwd_data_workspace_size(ctypes.byref(d)) == 0
     oh, ow = ctypes.c_int32(), ctypes.c_int32()
@@ -109,6 +111,11 @@ def test_null_and_alignment_checked_before_cuda(L):
     assert L.conv_bwd_bias(ctypes.byref(d), ok, ok, odd, None) == -4
     assert L.conv_bwd_bias(ctypes.byref(d), odd, ok, ok, None) == -4
     assert L.conv_bwd_bias(ctypes.byref(d), ok, odd, ok, None) == -4
+    # The fused backward: dw and w required, y with relu, everything aligned.
+    assert L.conv_bwd(ctypes.byref(d), ok, ok, ok, ok, ok, None, None, ok, 1 << 30, None) == -1
+    assert L.conv_bwd(ctypes.byref(d), ok, ok, ok, None, ok, ok, None, ok, 1 << 30, None) == -1
+    assert L.conv_bwd(ctypes.byref(d), ok, ok, ok, ok, ok, ok, odd, ok, 1 << 30, None) == -4
+    assert L.conv_bwd(ctypes.byref(d), ok, ok, ok, ok, odd, ok, None, ok, 1 << 30, None) == -4
     # The fused weight + bias gradients: db required and aligned.
     assert L.conv_bwd_filter_bias(ctypes.byref(d), ok, ok, ok, ok, None, ok, 1 << 30, None) == -1
     assert L.conv_bwd_filter_bias(ctypes.byref(d), ok, ok, ok, ok, odd, ok, 1 << 30, None) == -4

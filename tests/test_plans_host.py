@@ -12,8 +12,8 @@ from implicit_gemm_conv2d_gb300 import binding
 GB300 = binding.GB300
 MAX_CLUSTER = 8
 OPS = (binding.OP_FWD, binding.OP_BWD_DATA, binding.OP_BWD_FILTER, binding.OP_BWD_BIAS, binding.OP_FWD_WS,
-       binding.OP_BWD_DATA_WS)
-WS_OPS = (binding.OP_BWD_FILTER, binding.OP_FWD_WS, binding.OP_BWD_DATA_WS)
+       binding.OP_BWD_DATA_WS, binding.OP_BWD)
+WS_OPS = (binding.OP_BWD_FILTER, binding.OP_FWD_WS, binding.OP_BWD_DATA_WS, binding.OP_BWD)
 
 SHAPES = {
     "L1": (59, 128, 11, 15, 5, 3, 1),
@@ -33,7 +33,8 @@ BATCHES = (1, 37, 256, 1024, 4096, 16384, 32768)
 def _restore_algo():
     yield
     for op in OPS:
-        binding.conv_set_algo(op, binding.ALGO_AUTO)
+        if op != binding.OP_BWD:  # set through d_input's and wgrad's choices
+            binding.conv_set_algo(op, binding.ALGO_AUTO)
 
 
 def plan(op, B, shape, dtype, dev=GB300):
@@ -56,8 +57,10 @@ def test_plans_within_limits(name, dtype):
             assert 32 <= q["block"] <= 1024 and q["block"] % 32 == 0, where
             assert 0 <= q["smem_bytes"] <= GB300["smem_optin"], where
             assert q["grid"] >= 1, where
-            if q["algo"] == binding.ALGO_TC:
-                assert q["grid"] <= GB300["sms"], where
+            if q["algo"] == binding.ALGO_TC and op != binding.OP_BWD:
+                assert q["grid"] <= GB300["sms"], where  # persistent (the fused backward adds one CTA per wgrad tile)
+            if op == binding.OP_BWD and q["algo"] == binding.ALGO_TC:
+                assert q["launches"] == 3 and q["workspace"] > 0 and q["splits"] >= 1, where
             if op not in WS_OPS:
                 assert q["workspace"] == 0, where
             if op in (binding.OP_FWD_WS, binding.OP_BWD_DATA_WS):
@@ -132,9 +135,15 @@ def test_workspace_path_matches_the_plain_plan():
 
 def test_forced_family_is_honoured():
     for op in OPS:
+        if op == binding.OP_BWD:
+            continue  # set through its two operations
         binding.conv_set_algo(op, binding.ALGO_DIRECT)
         assert plan(op, 1024, SHAPES["L1"], binding.F32)["algo"] == binding.ALGO_DIRECT
         binding.conv_set_algo(op, binding.ALGO_AUTO)
+    binding.conv_set_algo(binding.OP_BWD_DATA, binding.ALGO_FFMA)
+    assert plan(binding.OP_BWD, 1024, SHAPES["L1"], binding.F32)["algo"] == binding.ALGO_AUTO  # two calls
+    binding.conv_set_algo(binding.OP_BWD_DATA, binding.ALGO_AUTO)
+    assert plan(binding.OP_BWD, 1024, SHAPES["L1"], binding.F32)["algo"] == binding.ALGO_TC
     binding.conv_set_algo(binding.OP_FWD, binding.ALGO_TC)
     with pytest.raises(binding.ConvError):  # no tensor cores on this device: the forced family cannot run
         plan(binding.OP_FWD, 1024, SHAPES["L1"], binding.F32, dict(sms=132, smem_optin=232448, cc_major=9,
