@@ -2961,15 +2961,26 @@ cudaError_t run_dgrad_tc(const Plan& pl, const ConvParams& p, int dt, const void
 }
 
 // ---- fused backward (d_input + wgrad in one launch) -----------------------------------------
-// wgrad's own geometry (its tiles are the long items) and d_input's workspace-path geometry with
-// its k-tiles cut into DG_BWD_RANGES ranges per sample tile (short items that backfill).
-constexpr int DG_BWD_RANGES = 3;
+// Fused only while d_input's own launch has fewer than two waves of work items: then its last
+// wave leaves SMs idle that the wgrad tiles can fill.  With more items the tail is a small part
+// of the launch, and one CTA per item (each with its own prologue) loses to the persistent
+// standalone kernels.  Fused: wgrad's stages with the split count that gives about half as many
+// tiles as SMs (the long items: half the SMs run them, the other half d_input's items and then
+// the rest), and d_input's workspace-path geometry with its k-tiles cut into DG_BWD_RANGES
+// ranges per sample tile (short items that backfill).  Measured on a GB300 at both encoder
+// layers and both dtypes (B = 1024, 4096, 16384), against wgrad tiles on a third, two thirds and
+// all of the SMs and two to four ranges.
+constexpr int DG_BWD_RANGES = 2;
 
 template <typename T>
 static bool pick_bwd(const ConvParams& p, const DevInfo& d, TcDgradGeom& dg, TcWgradGeom& wg)
 {
     if (d.cc_major != 10 || p.B <= 0) return false;
     if (!pick_dgrad<T>(p, d, true, dg) || !pick_wgrad<T>(p, d, wg)) return false;
+    if (dg.ntiles * dg.ktsplit >= 2 * d.sms) return false;
+    const int tiles = wg.k_tiles * wg.oc_tiles;
+    const int splits = std::min(std::max(1, (d.sms / 2 + tiles / 2) / tiles), std::max(1, p.B / (2 * wg.nsc)));
+    wg = wgrad_geom<T>(p, wg.KTp, wg.raws, wg.nbs, splits);
     dg.kt_per = ceil_div(dg.nkt, std::min(dg.nkt, DG_BWD_RANGES));
     dg.ktsplit = ceil_div(dg.nkt, dg.kt_per);
     return true;

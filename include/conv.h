@@ -181,13 +181,17 @@ int conv_bwd_filter_bias(const conv_desc_t* desc, const void* x, const void* dy,
 
 /* The whole backward in one call:  dx as conv_bwd_data, dw as conv_bwd_filter and, when db is
  * not NULL, db as conv_bwd_filter_bias -- PufferLib PR #522 times "backward" as wgrad plus
- * d_input together.  On the tensor-core path d_input and wgrad run in ONE launch (after W^T is
- * packed into the workspace, and before the split reduction), one work item per CTA: first the
- * wgrad tiles (the long items), then d_input's work items cut into k-tile ranges (short items:
- * disjoint dx channels, no reduction), so that d_input fills the SMs the wgrad tiles leave idle
- * and backfills the others as they finish.  Each operation computes exactly as in its own
- * kernel: dx is bit for bit conv_bwd_data's and dw conv_bwd_filter's.  Otherwise the two calls
- * run one after the other.
+ * d_input together.  On the tensor-core path, while d_input's own launch would have fewer than
+ * two waves of work items (the encoder layers up to a few thousand samples), d_input and wgrad
+ * run in ONE launch (after W^T is packed into the workspace, and before the split reduction), one
+ * work item per CTA: first the wgrad tiles (the long items), then d_input's work items cut into
+ * k-tile ranges (short items: disjoint dx channels, no reduction), so that d_input fills the SMs
+ * the wgrad tiles leave idle and backfills the others as they finish.  Each operation computes
+ * exactly as in its own kernel, but wgrad splits the batch into about half as many ranges as
+ * conv_bwd_filter (its tiles then fill half the SMs), so dw may differ from conv_bwd_filter's in
+ * the last bits (same tolerance, deterministic); dx is bit for bit conv_bwd_data's.  Otherwise
+ * (conv_query(CONV_OP_BWD) reports algo CONV_ALGO_AUTO) conv_bwd_data's workspace path and
+ * conv_bwd_filter run one after the other, each with its own part of the workspace.
  *   x, dy, w, y (required when relu): inputs; dx, dw, db (may be NULL): written.
  *   workspace: at least conv_bwd_workspace_size(desc) bytes, 16-byte aligned, owned by the
  *   caller, contents ignored on entry and unspecified on return. */

@@ -1,8 +1,10 @@
 """conv_bwd: the whole backward of the layer -- d_input, wgrad and optionally the bias
 gradient -- in one launch (PufferLib PR #522 times "backward" as wgrad plus d_input).  Checked
-through the C ABI: dx bit for bit against conv_bwd_data and dw against conv_bwd_filter; dw and
-db against the fp64 oracle; run to run bit identity; the two-call path when a family other than the tensor cores is forced; an
-undersized workspace rejected."""
+through the C ABI: dx bit for bit against conv_bwd_data; dw and db against the fp64 oracle and
+dw against conv_bwd_filter within the tolerance (conv_bwd splits the batch into fewer ranges);
+run to run bit identity; the two-call path, both where the batch is large enough for the
+standalone kernels (layer 1 from 4096 samples) and when a family other than the tensor cores is
+forced; an undersized workspace rejected."""
 import numpy as np
 import pytest
 import torch
@@ -44,7 +46,11 @@ def run_bwd(c: Case, y, with_bias):
 def test_fused_backward(layer, B, dtype):
     c = Case(B, **SHAPES[layer], dtype=dtype)
     q = binding.conv_query(binding.OP_BWD, c.desc)
-    assert q["algo"] == binding.ALGO_TC and q["launches"] == 3 and q["workspace"] > 0, q
+    fused = not (layer == "L1" and B >= 4096)  # fewer than two waves of d_input items
+    if fused:
+        assert q["algo"] == binding.ALGO_TC and q["launches"] == 3 and q["workspace"] > 0, q
+    else:
+        assert q["algo"] == binding.ALGO_AUTO and q["workspace"] > 0, q
     y = c.gpu_fwd()
     dx, dw, db = run_bwd(c, y, with_bias=True)
     dx0 = c.gpu_dgrad(y)
@@ -58,7 +64,7 @@ def test_fused_backward(layer, B, dtype):
         check(to_np(dx), ref, den, dtype, f"{layer} B={B} {dtype} fused dx")
     ref, den = c.ref_wgrad(yn)
     check(to_np(dw), ref, den, dtype, f"{layer} B={B} {dtype} fused dw")
-    assert torch.equal(_bits(dw), _bits(dw0)), "dw differs from conv_bwd_filter"
+    check(to_np(dw), to_np(dw0), den, dtype, f"{layer} B={B} {dtype} fused dw vs conv_bwd_filter")
     ref, den = oracle.conv_bwd_bias(c.inp["dy"], yn if c.relu else None, c.relu)
     check(to_np(db), ref, den, dtype, f"{layer} B={B} {dtype} fused db")
     # run to run

@@ -121,6 +121,28 @@ def test_no_tensor_core_plan_without_the_hardware():
                 assert q["algo"] != binding.ALGO_TC, (op, name, q)
 
 
+def test_backward_fused_only_below_two_waves_of_d_input_items():
+    # layer 1: d_input has one sample tile of 10 samples per work item, 152 SMs: fused below
+    # 3040 samples, two calls from there on; layer 2 (64 samples per tile) fuses to 16384
+    for dtype in (binding.F32, binding.BF16):
+        for B, want in ((1, binding.ALGO_TC), (1024, binding.ALGO_TC), (3000, binding.ALGO_TC),
+                        (4096, binding.ALGO_AUTO), (16384, binding.ALGO_AUTO)):
+            q = plan(binding.OP_BWD, B, SHAPES["L1"], dtype)
+            assert q["algo"] == want, (dtype, B, q)
+        for B, want in ((1024, binding.ALGO_TC), (16384, binding.ALGO_TC), (32768, binding.ALGO_AUTO)):
+            assert plan(binding.OP_BWD, B, SHAPES["L2"], dtype)["algo"] == want, (dtype, B)
+        # fused: the wgrad tiles fill about half the SMs
+        q = plan(binding.OP_BWD, 1024, SHAPES["L1"], dtype)
+        w = plan(binding.OP_BWD_FILTER, 1024, SHAPES["L1"], dtype)
+        tiles = w["grid"] // w["splits"]
+        assert abs(tiles * q["splits"] - GB300["sms"] // 2) <= tiles // 2 + 1, (q, w)
+        # two calls: the workspace holds both operations' parts
+        q = plan(binding.OP_BWD, 16384, SHAPES["L1"], dtype)
+        a = plan(binding.OP_BWD_DATA_WS, 16384, SHAPES["L1"], dtype)
+        w = plan(binding.OP_BWD_FILTER, 16384, SHAPES["L1"], dtype)
+        assert q["workspace"] >= a["workspace"] + w["workspace"] and q["splits"] == w["splits"], (q, a, w)
+
+
 def test_workspace_path_matches_the_plain_plan():
     # the same family (the packed stages need no raw w slots, so the workspace path may pick a
     # deeper ring), with a workspace for the packed image
