@@ -98,6 +98,14 @@ def parse():
                     help="fused: conv_fwd_ws then conv_bwd; split: the three operations one call each")
     ap.add_argument("--chain-only", action="store_true",
                     help="time only the fused two-layer forward chain against the two forward calls")
+    ap.add_argument("--profile-ops", default=None, metavar="OPS",
+                    help="comma-separated operations (" + ", ".join(PROFILE_OPS) + "): run each --warmup + "
+                    "--steps times, eagerly, each call after an L2 flush, and exit -- the launch sequence an ncu "
+                    "capture of the whole run reads (see --write-traffic)")
+    ap.add_argument("--write-traffic", default=None, metavar="CSV",
+                    help="host only: from `ncu --csv --metrics gpu__time_duration.sum,dram__bytes_read.sum,"
+                    "dram__bytes_write.sum` of a --profile-ops run (same --profile-ops, --steps, --warmup, --layer, "
+                    "--dtype, --batch), write each operation's DRAM bytes per call into profiles/dram_traffic.txt")
     return ap.parse_args()
 
 
@@ -303,6 +311,101 @@ def source_sha(paths):
         with open(path, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+TRAFFIC_SOURCES = ("kernels_tc.cu", "tc_ptx.cuh", "common.cuh", "kernels_ffma.cu")
+PROFILE_OPS = ("fwd", "dgrad", "wgrad", "bwd", "fwd_plain", "dgrad_plain")
+FLUSH_KERNEL = "l2_flush_kernel"
+
+
+def ncu_launches(csv_path):
+    """[(kernel name, us, DRAM bytes read + written)] in launch order from an ncu --csv log."""
+    import csv
+    with open(csv_path) as f:
+        rows = list(csv.reader(line for line in f if not line.startswith("==")))
+    hdr = rows[0]
+    col = {k: hdr.index(k) for k in ("ID", "Kernel Name", "Metric Name", "Metric Value", "Metric Unit")}
+    scale = {"nsecond": 1e-3, "ns": 1e-3, "usecond": 1.0, "us": 1.0, "msecond": 1e3, "ms": 1e3, "byte": 1.0,
+             "Kbyte": 1e3, "KB": 1e3, "Mbyte": 1e6, "MB": 1e6, "Gbyte": 1e9, "GB": 1e9}
+    per = {}
+    for r in rows[1:]:
+        if len(r) <= col["Metric Value"]:
+            continue
+        lid = int(r[col["ID"]])
+        name = r[col["Kernel Name"]].replace("<unnamed>", "").replace("(anonymous namespace)", "")
+        name = name.split("(")[0].split("<")[0].split("::")[-1].replace("void ", "").strip()
+        v = float(r[col["Metric Value"]].replace(",", "")) * scale.get(r[col["Metric Unit"]], 1.0)
+        e = per.setdefault(lid, [name, 0.0, 0.0])
+        if r[col["Metric Name"]] == "gpu__time_duration.sum":
+            e[1] += v
+        elif r[col["Metric Name"]].startswith("dram__bytes_"):
+            e[2] += v
+    return [tuple(per[k]) for k in sorted(per)]
+
+
+def write_traffic(args):
+    """Per-call DRAM bytes of each --profile-ops operation, from the ncu capture of that run:
+    the launches between two L2 flushes are one call; an operation's --warmup first calls are
+    dropped and the rest averaged.  Replaces the table's lines for the same keys and stamps
+    them with the hash of the kernel sources they were taken from."""
+    ops = args.profile_ops.split(",")
+    launches = ncu_launches(args.write_traffic)
+    first = next(i for i, l in enumerate(launches) if l[0] == FLUSH_KERNEL)
+    calls, cur = [], None
+    for name, us, nbytes in launches[first:]:
+        if name == FLUSH_KERNEL:
+            cur = [0.0, 0.0, []]
+            calls.append(cur)
+        else:
+            cur[0] += us
+            cur[1] += nbytes
+            cur[2].append(name)
+    per_op = args.warmup + args.steps
+    if len(calls) != len(ops) * per_op:
+        raise SystemExit(f"{len(calls)} flush-separated calls in the capture, expected {len(ops)} x {per_op}")
+    srcs = [os.path.join(ROOT, "implicit_gemm_conv2d_gb300", "csrc", n) for n in TRAFFIC_SOURCES]
+    stamp = "+".join(TRAFFIC_SOURCES) + ":" + source_sha(srcs)
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    lines = open(path).read().splitlines() if os.path.exists(path) else []
+    new = {}
+    for i, op in enumerate(ops):
+        timed = calls[i * per_op + args.warmup:(i + 1) * per_op]
+        key = f"{op}:{args.layer}:{args.dtype}:B{args.batch}"
+        nbytes = statistics.mean(c[1] for c in timed)
+        us = statistics.mean(c[0] for c in timed)
+        new[key] = f"{key} {int(round(nbytes))} {us:.1f} {stamp}"
+        print(f"{key}: {nbytes / 1e6:.2f} MB, {us:.1f} us under ncu, kernels {' + '.join(timed[0][2])}")
+    out = [l for l in lines if not (l.split() and l.split()[0] in new)]
+    if not any(l.startswith("#") for l in out):
+        out = ["# DRAM bytes per operation call: the sum over the call's launches of dram__bytes_read.sum +",
+               "# dram__bytes_write.sum, L2 flushed before the call.  Columns: key  bytes  us_under_ncu",
+               "# sources:sha16 (the kernel sources the capture was taken from, '+'-joined, and the first 16",
+               "# hex digits of the SHA-256 of their concatenation).  Written by bench.py --write-traffic;",
+               "# the commands are in profiles/traffic_b1024.md."] + out
+    out += [new[k] for k in new]
+    with open(path, "w") as f:
+        f.write("\n".join(out) + "\n")
+    return 0
+
+
+def run_profile_ops(args, wl, flush_buf):
+    """The launch sequence --write-traffic reads: each operation --warmup + --steps times,
+    eagerly, an L2 flush before each call."""
+    import torch
+    from implicit_gemm_conv2d_gb300 import binding
+    ops = args.profile_ops.split(",")
+    for op in ops:
+        if op not in PROFILE_OPS:
+            raise SystemExit(f"unknown operation {op!r}")
+    for op in ops:
+        for _ in range(args.warmup + args.steps):
+            binding.conv_l2_flush(flush_buf)
+            wl.op(op)
+    torch.cuda.synchronize()
+    assert binding.conv_device_status(reset=True) == 0
+    print(json.dumps({"profile_ops": ops, "calls_each": args.warmup + args.steps,
+                      "launches": {o: wl.plans[o]["launches"] for o in ops}}))
+    return 0
 
 
 def read_traffic(kernel_key):
@@ -811,6 +914,8 @@ def run_ours(args):
         print(json.dumps({"chain_fwd": chain_extras(flush_buf, device)}))
         return 0
     wl = Workload(args.layer, args.dtype, args.batch, device)
+    if args.profile_ops:
+        return run_profile_ops(args, wl, flush_buf)
     if not args.no_graphs:
         wl.capture()
 
@@ -917,6 +1022,12 @@ def run_ours(args):
                     entry[o] = {"us_cold_l2": t_ms * 1e3, "us_warm": warm[o],
                                 "gflops": w2.flops / (t_ms * 1e-3) / 1e9, "algo": w2.plans[o]["algo_name"],
                                 "bound": r["bound"], "frac": r["frac"], "roofline_us": r["roofline_us"]}
+                if getattr(w2, "graphs", None):
+                    t_ms = time_graph(w2.graphs["bwd"], flush_buf, 50, 5)
+                    r = roofline_of(w2, "bwd", t_ms, sms, sm_mhz, peaks)
+                    entry["bwd"] = {"us_cold_l2": t_ms * 1e3, "gflops": 2 * w2.flops / (t_ms * 1e-3) / 1e9,
+                                    "algo": w2.plans["bwd"]["algo_name"], "bound": r["bound"], "frac": r["frac"],
+                                    "roofline_us": r["roofline_us"]}
                 if args.batch == 1024:
                     f, b = PR522_US[(layer, dt)]
                     entry["pr522_us"] = {"fwd": f, "bwd": b}
@@ -936,6 +1047,8 @@ def run_ours(args):
 
 def main():
     args = parse()
+    if args.write_traffic:
+        return write_traffic(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -2,6 +2,7 @@
 behind the roofline, the DRAM-traffic table lookup (valid only while the kernel sources
 it was captured from are unchanged), and the pipe peaks."""
 import os
+import types
 import sys
 
 import pytest
@@ -44,7 +45,7 @@ def test_traffic_lookup_follows_the_source_hash(tmp_path, monkeypatch):
 
 def test_committed_traffic_table_names_existing_sources():
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-    keys = 0
+    keys = set()
     for line in open(path):
         line = line.split("#", 1)[0].split()
         if not line:
@@ -54,8 +55,58 @@ def test_committed_traffic_table_names_existing_sources():
         assert len(sha) == 16
         for n in names.split("+"):
             assert os.path.exists(os.path.join(ROOT, "implicit_gemm_conv2d_gb300", "csrc", n)), n
-        keys += 1
-    assert keys == 6
+        keys.add(line[0])
+    # the fused step's two operations for both encoder layers and both dtypes at the bench batch
+    for layer in ("layer1", "layer2"):
+        for dt in ("f32", "bf16"):
+            for op in ("fwd", "bwd"):
+                assert f"{op}:{layer}:{dt}:B1024" in keys
+
+
+def _ncu_csv(path, launches):
+    """An ncu --csv log of the three metrics for [(kernel name, us, read bytes, write bytes)]."""
+    rows = ['==PROF== Connected to process 1',
+            '"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream","Block Size",'
+            '"Grid Size","Device","CC","Section Name","Metric Name","Metric Unit","Metric Value"']
+    for i, (name, us, rd, wr) in enumerate(launches):
+        for metric, unit, v in (("dram__bytes_read.sum", "byte", rd), ("dram__bytes_write.sum", "Kbyte", wr / 1e3),
+                                ("gpu__time_duration.sum", "us", us)):
+            rows.append(f'"{i}","1","python3","h","{name}","1","7","(256, 1, 1)","(1, 1, 1)","0","10.3",'
+                        f'"Command line profiler metrics","{metric}","{unit}","{v:,}"')
+    path.write_text("\n".join(rows) + "\n")
+
+
+def test_write_traffic_groups_calls_between_flushes(tmp_path, monkeypatch):
+    # two operations, warmup 1 + steps 2 each: flush-separated calls; warm-up calls dropped
+    flush = ("igc::<unnamed>::l2_flush_kernel(float4 *, unsigned long, float)", 70.0, 0, 5e8)
+    pack = "void igc::<unnamed>::pack_fwd_w_kernel<float>(ConvParams, const T1 *, unsigned char *, int, int)"
+    fwd = "void igc::<unnamed>::fwd_tc_kernel<float, 1>(ConvParams, const T1 *)"
+    bwd = "void igc::<unnamed>::bwd_tc_kernel<float, 1>(ConvParams, const T1 *)"
+    seq = [("void at::vectorized_elementwise_kernel<4, at::copy>(int)", 3.0, 1e6, 0)]
+    for rd in (9e6, 1e6, 3e6):                  # fwd: warm-up, then 1 and 3 MB in its main kernel
+        seq += [flush, (pack, 4.0, 1e5, 0), (fwd, 40.0, rd, 2e3)]
+    for rd in (9e6, 5e6, 7e6):                  # bwd
+        seq += [flush, (pack, 4.0, 0, 0), (bwd, 90.0, rd, 0)]
+    csv = tmp_path / "t.csv"
+    _ncu_csv(csv, seq)
+    (tmp_path / "profiles").mkdir()
+    csrc = tmp_path / "implicit_gemm_conv2d_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for n in bench.TRAFFIC_SOURCES:
+        (csrc / n).write_text(n)
+    (tmp_path / "profiles" / "dram_traffic.txt").write_text("# header\nfwd:layer1:f32:B1024 1 1.0 a.cu:0000000000000000\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    args = types.SimpleNamespace(write_traffic=str(csv), profile_ops="fwd,bwd", warmup=1, steps=2, layer="layer1",
+                                 dtype="f32", batch=1024)
+    assert bench.write_traffic(args) == 0
+    assert bench.read_traffic("fwd:layer1:f32:B1024") == pytest.approx(1e5 + 2e6 + 2e3, abs=1)
+    assert bench.read_traffic("bwd:layer1:f32:B1024") == pytest.approx(6e6, abs=1)
+    lines = [l for l in (tmp_path / "profiles" / "dram_traffic.txt").read_text().splitlines() if l.startswith("fwd:")]
+    assert len(lines) == 1  # the stale line was replaced
+    # a capture with the wrong number of calls is refused
+    args.steps = 3
+    with pytest.raises(SystemExit):
+        bench.write_traffic(args)
 
 
 def test_pipe_peaks():
