@@ -128,8 +128,15 @@ bias_grad_kernel(const ConvParams p, const T* __restrict__ dy, const T* __restri
     if (rank == 0) {
         const uint32_t cs = tc::smem_u32(csum);
         for (int j = threadIdx.x; j < noc; j += blockDim.x) {
+            // All R loads in flight first (R <= kMaxCluster), then the sum in ascending rank order.
+            float v[kMaxCluster];
+#pragma unroll
+            for (int r = 0; r < kMaxCluster; ++r)
+                if (r < R) v[r] = tc::ld_dsmem_f32(tc::dsmem_addr(cs + uint32_t(4 * j), uint32_t(r)));
             float t = 0.f;
-            for (int r = 0; r < R; ++r) t += tc::ld_dsmem_f32(tc::dsmem_addr(cs + uint32_t(4 * j), uint32_t(r)));
+#pragma unroll
+            for (int r = 0; r < kMaxCluster; ++r)
+                if (r < R) t += v[r];
             Elem<T>::st(db + oc0 + j, t);
         }
     }

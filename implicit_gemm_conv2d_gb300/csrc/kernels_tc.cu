@@ -952,12 +952,16 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict__
             const int n = ntile * FA_TM + mm;
             if (n >= p.N) continue;
             const uint32_t off = uint32_t((mm * RS + g4 * 4) * 4);
+            // All R loads in flight first, then the sum in ascending rank order.
+            float4 v[kMaxCluster];
+#pragma unroll
+            for (int q = 0; q < kMaxCluster; ++q)
+                if (q < R) v[q] = ld_dsmem_f4(peer[q] + off);
             float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int q = 0; q < kMaxCluster; ++q) {
                 if (q >= R) break;
-                const float4 v = ld_dsmem_f4(peer[q] + off);
-                s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+                s.x += v[q].x; s.y += v[q].y; s.z += v[q].z; s.w += v[q].w;
             }
             const float f4[4] = {s.x, s.y, s.z, s.w};
             T* yc = y + col_out(p, n);
