@@ -80,11 +80,20 @@ def test_plans_within_limits(name, dtype):
                 assert q["workspace"] >= q["splits"] * OC * IC * K * K * 4, where
             if op == binding.OP_BWD_BIAS:
                 if q["algo"] == binding.ALGO_FFMA:
-                    assert q["block"] <= 256 and q["smem_bytes"] <= 48 * 1024, where
+                    assert 256 <= q["block"] <= 1024 and q["smem_bytes"] <= 48 * 1024, where
                     assert q["splits"] in (1, 2, 4, 8) and q["grid"] % q["splits"] == 0, where
                     assert q["launches"] == 1, where
                 else:
                     assert q["algo"] == binding.ALGO_DIRECT and OH * OW > 12288, where
+
+
+def test_bias_gradient_threads_grow_with_rows_per_range():
+    # 256 threads while the sample ranges are short (B = 1024: 8 ranges of 128 rows), up to
+    # 1024 threads (about 8 rows per row lane) at the PR's bias-gradient batch
+    for name in ("L1", "L2"):
+        for dtype in (binding.F32, binding.BF16):
+            assert plan(binding.OP_BWD_BIAS, 1024, SHAPES[name], dtype)["block"] == 256
+            assert plan(binding.OP_BWD_BIAS, 32768, SHAPES[name], dtype)["block"] == 1024
 
 
 def test_encoder_layers_use_tensor_cores_on_gb300():
