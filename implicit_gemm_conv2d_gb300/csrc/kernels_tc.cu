@@ -20,6 +20,7 @@
 // g_tc_status, all threads leave their loops together and the CTA frees its
 // tensor memory before returning.
 #include <algorithm>
+#include <climits>
 #include <cstdlib>
 
 #include "internal.h"
@@ -411,6 +412,60 @@ struct FwdBars {
 // first words fall 4 banks apart.
 inline __host__ __device__ int fwd_red_stride(int OTp) { return OTp + 4; }
 
+// Shared-memory wavefronts of one gather load of the forward's formatters: the 32 lanes of a warp
+// are 32 consecutive columns n = (b, oh, ow) of a tile, all reading the same k; lane n reads the
+// word at (b - b_first) * xs + (its slab's 16-byte misalignment) + its pixel's offset.  A bank
+// serves one word per wavefront (equal words broadcast).
+inline int fwd_gather_wavefronts(const ConvParams& p, int es, int xs, int n0, int b_first, int cmis)
+{
+    int word[32], bank_words[32] = {0};
+    for (int m = 0; m < 32; ++m) {
+        const int n = std::min(n0 + m, p.N - 1);
+        const int b = n / p.P, pq = n % p.P, oh = pq / p.OW, ow = pq % p.OW;
+        const long long mis = ((long long)b * p.IHW * es + cmis) & 15;
+        word[m] = int(((long long)(b - b_first) * xs + mis + (oh * p.S * p.W + ow * p.S) * es) >> 2);
+        bool seen = false;
+        for (int i = 0; i < m && !seen; ++i) seen = word[i] == word[m];
+        if (!seen) ++bank_words[word[m] & 31];
+    }
+    int w = 0;
+    for (int b = 0; b < 32; ++b) w = std::max(w, bank_words[b]);
+    return w;
+}
+
+// Per-sample stride of the forward's raw x slots (a multiple of 16 bytes, at least xs0): of the
+// eight residues modulo 128 bytes, the one whose gather loads need the fewest wavefronts, counted
+// over the warps of the first tiles and the misalignments (in steps of the element size, at
+// least 4 bytes) a super-chunk's first channel can add.  Each sample's slab sits 0-15 bytes into its slot (its source's misalignment),
+// which is why a fixed residue does not serve every shape.  Remembered per shape (per thread).
+inline int fwd_sample_stride(const ConvParams& p, int es, int xs0)
+{
+    struct Entry { int P, OW, S, W, IHW, N, es, xs0, xs; };
+    constexpr int NCACHE = 64;
+    static thread_local Entry cache[NCACHE];
+    static thread_local int next = 0;
+    for (const Entry& e : cache)
+        if (e.xs0 == xs0 && e.P == p.P && e.OW == p.OW && e.S == p.S && e.W == p.W && e.IHW == p.IHW &&
+            e.es == es && e.N == std::min(p.N, 3 * FA_TM))
+            return e.xs;
+    int best = xs0, best_cost = INT_MAX;
+    for (int i = 0; i < 8; ++i) {
+        const int xs = xs0 + 16 * i;
+        int cost = 0;
+        for (int t = 0; t < 3 && t * FA_TM < p.N; ++t)
+            for (int q = 0; q < 4; ++q)
+                for (int cmis = 0; cmis < 16; cmis += std::min(es, 4))
+                    cost += fwd_gather_wavefronts(p, es, xs, t * FA_TM + q * 32, (t * FA_TM) / p.P, cmis);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = xs;
+        }
+    }
+    cache[next] = Entry{p.P, p.OW, p.S, p.W, p.IHW, std::min(p.N, 3 * FA_TM), es, xs0, best};
+    next = (next + 1) % NCACHE;
+    return best;
+}
+
 template <typename T>
 inline FwdGeom fwd_geom(const ConvParams& p, int xg, int nw, int nraw)
 {
@@ -427,10 +482,7 @@ inline FwdGeom fwd_geom(const ConvParams& p, int xg, int nw, int nraw)
     g.nraw = nraw;
     g.nsmax = std::min(p.B, (FA_TM - 1) / p.P + 2);
     const int chmax = std::min(p.IC, (xg * Tr::KC - 1) / p.KK + 2);
-    g.xs = round_up(chmax * p.HW * es + 16, 16);
-    // Sample stride = 12 words mod 32: the columns of consecutive samples fall on
-    // different banks when a warp gathers one k for 32 columns.
-    while ((g.xs / 4) % 32 != 12) g.xs += 16;
+    g.xs = fwd_sample_stride(p, es, round_up(chmax * p.HW * es + 16, 16));
     g.raw_bytes = round_up(g.nsmax * g.xs, 128);
     g.w_bytes = g.OTp * ROWB * (Tr::split ? 2 : 1);
     g.dcols = g.OTp * (Tr::split ? 2 : 1);
