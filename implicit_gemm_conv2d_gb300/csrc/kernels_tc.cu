@@ -2785,7 +2785,8 @@ Plan plan_fwd_tc(const ConvParams& p, int dt, const DevInfo& d, bool packed)
     pl.launches = packed ? 2 : 1;
     pl.block = FA_THREADS;
     pl.splits = g.splits;
-    pl.variant = ((g.kc_per * 16 + g.xg) * 16 + g.nw) * 8 + g.nraw;
+    static_assert(FV_MAXRAWS < 8 && FA_MAXW < 16, "forward plan: ring depths in 3 and 4 bits");
+    pl.variant = ((g.kc_per * 16 + g.xg) * 16 + g.nw) * 8 + g.nraw;  // xg <= 8
     pl.grid = g.splits > 1 ? g.n_tiles * g.oc_tiles * g.splits : std::min(g.n_tiles * g.oc_tiles, d.sms);
     pl.smem = dt == DT_BF16 ? fwd_smem<__nv_bfloat16>(p, g) : fwd_smem<float>(p, g);
     if (packed) pl.workspace = size_t(g.oc_tiles) * g.nchunks * g.w_bytes;
@@ -2884,7 +2885,8 @@ Plan plan_wgrad_tc(const ConvParams& p, int dt, const DevInfo& d)
     else pick_wgrad<float>(p, d, g);
     pl.smem = dt == DT_BF16 ? wgrad_smem<__nv_bfloat16>(g) : wgrad_smem<float>(g);
     pl.splits = g.splits;
-    pl.variant = (g.KTp * 8 + g.raws) * 4 + g.nbs;
+    static_assert(WG_MAXR < 8 && WG_MAXB < 8, "wgrad plan: ring depths in 3 bits each");
+    pl.variant = (g.KTp * 8 + g.raws) * 8 + g.nbs;
     pl.launches = 2;
     pl.grid = std::min(g.k_tiles * g.oc_tiles * g.splits, d.sms);
     // the split-K partials, then room for the bias gradient's partial channel sums (two G lane
@@ -2905,7 +2907,7 @@ static cudaError_t wgrad_tc_t(const Plan& pl, const ConvParams& p, const void* x
     const int nbp = pl.splits * (WgRoles<T>::g_warps / 4);
     if (pl.splits > 0) {
         const int v = pl.variant;
-        const TcWgradGeom g = wgrad_geom<T>(p, v / 32, (v / 4) % 8, v % 4, pl.splits);
+        const TcWgradGeom g = wgrad_geom<T>(p, v / 64, (v / 8) % 8, v % 8, pl.splits);
 #define IG_LAUNCH_WG_TC(R)                                                                                 \
     do {                                                                                                   \
         e = ensure_smem<wgrad_tc_kernel<T, R>>(pl.smem);                                                   \
@@ -2975,7 +2977,8 @@ Plan plan_dgrad_tc(const ConvParams& p, int dt, const DevInfo& d, bool packed)
     // packs W^T into the workspace
     pl.launches = packed ? 2 : 1;
     pl.block = DG_THREADS;
-    pl.variant = (g.kt_per * 128 + g.CIC) * 8 + g.nw;
+    static_assert(DG_MAXW < 8, "d_input plan: weight stages in 3 bits");
+    pl.variant = (g.kt_per * 256 + g.CIC) * 8 + g.nw;  // CIC <= 128 (KTp <= 128 rows)
     pl.grid = std::min(g.ntiles * g.ktsplit, d.sms);
     pl.smem = dt == DT_BF16 ? dgrad_smem<__nv_bfloat16>(p, g) : dgrad_smem<float>(p, g);
     if (packed) pl.workspace = size_t(g.nkt) * g.nch * g.w_tile;
@@ -2986,8 +2989,8 @@ template <typename T>
 static cudaError_t dgrad_tc_t(const Plan& pl, const ConvParams& p, const void* dy, const void* w,
                               const void* y, void* dx, void* ws, cudaStream_t s)
 {
-    TcDgradGeom g = dgrad_geom<T>(p, (pl.variant / 8) % 128, pl.variant % 8);
-    g.kt_per = pl.variant / 1024;
+    TcDgradGeom g = dgrad_geom<T>(p, (pl.variant / 8) % 256, pl.variant % 8);
+    g.kt_per = pl.variant / 2048;
     g.ktsplit = ceil_div(g.nkt, g.kt_per);
     g.packed = ws ? 1 : 0;
     cudaError_t e = cudaSuccess;

@@ -22,6 +22,8 @@ SHAPES = {
     "wide_oc_p16": dict(IC=4, OC=200, H=6, W=6, K=3, S=1, relu=False),
     "kk_above_128": dict(IC=2, OC=8, H=13, W=12, K=12, S=1, relu=True),
     "k1": dict(IC=16, OC=24, H=3, W=5, K=1, S=1, relu=False),
+    # 1x1 with 128 channels per d_input k-tile (the widest its plan encodes)
+    "k1_wide": dict(IC=160, OC=64, H=4, W=5, K=1, S=1, relu=True),
     "k_eq_input": dict(IC=7, OC=33, H=5, W=5, K=5, S=2, relu=True),
     "stride_gt_k": dict(IC=5, OC=20, H=10, W=11, K=2, S=3, relu=False),
 }

@@ -25,6 +25,7 @@ SHAPES = {
     "k_eq_input": (7, 33, 5, 5, 5, 2, 1),
     "stride_gt_k": (5, 20, 10, 11, 2, 3, 0),
     "long_rows": (1, 3, 120, 120, 1, 1, 0),
+    "k1_wide": (160, 64, 4, 5, 1, 1, 1),
 }
 BATCHES = (1, 37, 256, 1024, 4096, 16384, 32768)
 
