@@ -832,6 +832,17 @@ def chain_extras(flush_buf, device, batches=(256, 1024, 4096, 16384)):
             out[f"{dt}_B{B}"] = {"chain_us_cold_l2": tc, "layer1_fwd_us_cold_l2": t1, "layer2_fwd_us_cold_l2": t2,
                                  "unfused_us": t1 + t2, "layer2_share_of_chain_us": tc - t1,
                                  "chain_plan": {k: q[k] for k in ("algo_name", "launches", "grid", "block")}}
+            # fp32 runs unfused by default; the fused kernel, forced, for the record
+            binding.conv_set_algo(binding.OP_FWD, binding.ALGO_TC)
+            try:
+                if q["algo"] == binding.ALGO_AUTO and binding.conv_query_chain2(d1, d2)["algo"] == binding.ALGO_TC:
+                    wsf = torch.empty(max(16, binding.conv_fwd_chain2_workspace_size(d1, d2)), dtype=torch.uint8,
+                                      device=device)
+                    gf = graphed(lambda: binding.conv_fwd_chain2(d1, d2, x, w1, None, w2, None, y1, y2, wsf))
+                    out[f"{dt}_B{B}"]["fused_forced_us_cold_l2"] = time_graph(gf, flush_buf, 30, 3) * 1e3
+                    del gf
+            finally:
+                binding.conv_set_algo(binding.OP_FWD, binding.ALGO_AUTO)
             del gc, g1, g2, x, y1, y2
             torch.cuda.empty_cache()
     return out

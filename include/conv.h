@@ -229,8 +229,10 @@ int conv_bwd_bias(const conv_desc_t* desc, const void* dy, const void* y, void* 
  * output tile goes to y1 and into shared memory, where layer 2 gathers its input from, so y1
  * makes no round trip through memory between the layers and layer 2 needs no launch of its
  * own; both weight images are packed into the workspace first (two small kernels).  The fused
- * kernel runs when every CTA gets at most one group of whole samples (the encoder: B up to
- * about 1500 on 152 SMs); larger batches, and shapes the fused kernel does not take (a layer with
+ * kernel runs in bf16 when every CTA gets at most one group of whole samples (the encoder: B up
+ * to about 1500 on 152 SMs).  In fp32 the two forward calls were measured faster, so it runs
+ * there only when conv_set_algo(CONV_OP_FWD, CONV_ALGO_TC) forces it.  Larger batches, fp32
+ * unforced, and shapes the fused kernel does not take (a layer with
  * more than 128 output positions, layer 1 with more output channels than one tensor-core tile --
  * 128 fp32 / 256 bf16 --, layer 2 with more than 128), run as two conv_fwd_ws calls sharing the
  * workspace.

@@ -83,6 +83,13 @@ def test_two_layer_chain_bf16(B):
     assert np.isfinite(dx1s).all()
 
 
+@pytest.fixture(autouse=True)
+def _restore_algo():
+    yield
+    for op in range(6):
+        binding.conv_set_algo(op, binding.ALGO_AUTO)
+
+
 def _bits(t):
     return t.view(torch.int16 if t.dtype == torch.bfloat16 else torch.int32)
 
@@ -102,8 +109,12 @@ def test_fused_forward_chain(dtype, B):
     x1, W1, W2, b1 = to_dev(i1["x"], dtype), to_dev(i1["w"], dtype), to_dev(w2, dtype), to_dev(i1["bias"], dtype)
     d1 = binding.make_desc(B, **L1, relu=1, dtype=tdt)
     d2 = binding.make_desc(B, **L2, relu=0, dtype=tdt)
+    # bf16: fused while every CTA gets at most one group of 10 samples, else two forward calls;
+    # fp32: two forward calls unless the tensor-core family is forced (then fused likewise)
+    if dtype == "f32":
+        assert binding.conv_query_chain2(d1, d2)["algo"] == binding.ALGO_AUTO
+        binding.conv_set_algo(binding.OP_FWD, binding.ALGO_TC)
     q = binding.conv_query_chain2(d1, d2)
-    # fused while every CTA gets at most one group of 10 samples, else two forward calls
     fused = (B + 9) // 10 <= torch.cuda.get_device_properties(0).multi_processor_count
     assert (q["algo"] == binding.ALGO_TC and q["launches"] == 3) if fused else q["algo"] == binding.ALGO_AUTO, q
     ws = torch.empty(binding.conv_fwd_chain2_workspace_size(d1, d2), dtype=torch.uint8, device="cuda")
