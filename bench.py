@@ -265,17 +265,32 @@ def cpu_baseline(shape, b_sample, min_seconds):
                       f"(same shapes and seeded inputs), fp64 direct loops, {el:.1f} s"}
 
 
+def arm_config(args):
+    """The `config` both arms report: the workload of the timed step and how it is run."""
+    return dict(workload_config(args.layer, args.dtype, args.batch),
+                l2="flushed (512 MiB write) between timed steps, outside the timed region",
+                calls=("step: conv_fwd_ws, then conv_bwd (d_input + wgrad in one launch), caller-owned "
+                       "workspaces, captured together as one CUDA graph" if args.step == "fused" else
+                       "step: conv_fwd_ws, conv_bwd_data_ws, conv_bwd_filter (caller-owned workspaces)"),
+                launch=("each operation replayed from a captured CUDA graph" if not args.no_graphs
+                        else "eager launches"),
+                algo=args.algo)
+
+
 def run_reference(args):
+    """The oracle on the host cores, on our arm's config (the same `config` object), each step a
+    bounded sample of its workload: B_SAMPLE of its samples, the same shapes, dtype and seeded
+    inputs; the value counts the sample's FLOPs (the `sample` fields say so)."""
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
-    shape = LAYERS["layer1"]
-    b_sample = 8
+    shape = LAYERS[args.layer]
+    b_sample = min(8, args.batch)
     from implicit_gemm_conv2d_gb300 import synth
     import oracle
     oracle.build()
     inp = synth.conv_inputs(b_sample, shape["IC"], shape["OC"], shape["H"], shape["W"], shape["K"],
-                            shape["S"], dtype="f32")
+                            shape["S"], dtype=args.dtype)
     for _ in range(args.warmup):
         oracle_step(inp, shape)
     t0 = time.perf_counter()
@@ -288,13 +303,13 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": dict(workload_config("layer1", "f32", b_sample),
-                       sample=f"each step runs the fp64 oracle on B={b_sample} samples of the B=1024 "
-                              "workload (same shapes, seeded inputs); the value counts those samples' FLOPs"),
+        "config": arm_config(args),
+        "sample": (f"each step runs the fp64 oracle on {b_sample} of the workload's {args.batch} samples (same "
+                   "shapes, dtype and seeded inputs); the value counts those samples' FLOPs"),
         "cpu_baseline": {"value": value, "unit": "GFLOP/s", "cores": oracle.default_threads(),
                          "kind": "oracle",
-                         "sample": f"each step the fp64 oracle on {b_sample} of the 1024 samples (the same "
-                                   "shapes and seeded inputs); GFLOP/s counts the sample's FLOPs"},
+                         "sample": f"each step the fp64 oracle on {b_sample} of the {args.batch} samples (the same "
+                                   "shapes, dtype and seeded inputs); GFLOP/s counts the sample's FLOPs"},
         "e2e": {"value": value, "unit": "GFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -1023,14 +1038,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": (value / world / pr_gflops) if pr_gflops else None,
         "dtype": args.dtype, "data": "synthetic",
-        "config": dict(workload_config(args.layer, args.dtype, args.batch),
-                       l2="flushed (512 MiB write) between timed steps, outside the timed region",
-                       calls=("step: conv_fwd_ws, then conv_bwd (d_input + wgrad in one launch), caller-owned "
-                              "workspaces, captured together as one CUDA graph" if args.step == "fused" else
-                              "step: conv_fwd_ws, conv_bwd_data_ws, conv_bwd_filter (caller-owned workspaces)"),
-                       launch=("each operation replayed from a captured CUDA graph" if not args.no_graphs
-                               else "eager launches"),
-                       algo=args.algo),
+        "config": arm_config(args),
         "ops": ops,
         "ops_no_workspace": plain,
         "roofline": roofline,

@@ -137,3 +137,7 @@ def test_reference_arm_prints_one_contract_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["e2e"]["value"] == d["value"]
+    # the same config object our arm reports for the default workload
+    args = types.SimpleNamespace(layer="layer1", dtype="f32", batch=1024, step="fused", no_graphs=False, algo="auto")
+    assert d["config"] == bench.arm_config(args)
+    assert "B=1024" in d["config"]["workload"] and "8 of the workload's 1024 samples" in d["sample"]
