@@ -329,7 +329,7 @@ def source_sha(paths):
 
 
 TRAFFIC_SOURCES = ("kernels_tc.cu", "tc_ptx.cuh", "common.cuh", "kernels_ffma.cu")
-PROFILE_OPS = ("fwd", "dgrad", "wgrad", "bwd", "fwd_plain", "dgrad_plain")
+PROFILE_OPS = ("fwd", "dgrad", "wgrad", "bwd", "fwd_plain", "dgrad_plain", "bias_grad", "chain")
 FLUSH_KERNEL = "l2_flush_kernel"
 
 
@@ -487,6 +487,31 @@ class Workload:
         self.plans["bwd"] = binding.conv_query(binding.OP_BWD, self.desc)
         self.ws_bwd = torch.empty(max(16, binding.conv_bwd_workspace_size(self.desc)), dtype=torch.uint8, device=device)
         self.step_launches = self.plans["fwd"]["launches"] + self.plans["bwd"]["launches"]
+        self.plans["bias_grad"] = binding.conv_query(binding.OP_BWD_BIAS, self.desc)
+        self.db = torch.empty((s["OC"],), dtype=self.tdt, device=device)
+        self.chain = None  # the layer-2 half of the encoder chain, made on first use (layer 1 only)
+
+    def _chain(self):
+        """Layer 2's weights, descriptor, output and the chain's workspace (for "chain")."""
+        import torch
+        from implicit_gemm_conv2d_gb300 import binding
+        if self.chain is None:
+            if self.layer != "layer1":
+                raise SystemExit("the chain op takes the layer-1 workload (its output feeds layer 2)")
+            s2 = LAYERS["layer2"]
+            g = torch.Generator(device=self.x.device)
+            g.manual_seed(7)
+            w2 = ((torch.rand((s2["OC"], s2["IC"], s2["K"], s2["K"]), generator=g, device=self.x.device) * 2 - 1)
+                  / math.sqrt(s2["IC"] * s2["K"] ** 2)).to(self.tdt)
+            d2 = binding.make_desc(self.B, *(s2[k] for k in ("IC", "OC", "H", "W", "K", "S", "relu")), self.tdt)
+            OH2, OW2 = binding.out_dims(d2)
+            y2 = torch.empty((self.B, s2["OC"], OH2, OW2), dtype=self.tdt, device=self.x.device)
+            ws = torch.empty(max(16, binding.conv_fwd_chain2_workspace_size(self.desc, d2)), dtype=torch.uint8,
+                             device=self.x.device)
+            self.chain = (d2, w2, y2, ws)
+            q = binding.conv_query_chain2(self.desc, d2)
+            self.plans["chain"] = q
+        return self.chain
 
     def capture(self):
         """One CUDA graph per operation (captured after a warm-up call), so that
@@ -534,6 +559,11 @@ class Workload:
             binding.conv_bwd_data(self.desc, self.dy, self.w, relu_y, self.dx, stream)
         elif name == "bwd":
             binding.conv_bwd(self.desc, self.x, self.dy, self.w, relu_y, self.dx, self.dw, None, self.ws_bwd, stream)
+        elif name == "bias_grad":
+            binding.conv_bwd_bias(self.desc, self.dy, relu_y, self.db, stream)
+        elif name == "chain":
+            d2, w2, y2, ws = self._chain()
+            binding.conv_fwd_chain2(self.desc, d2, self.x, self.w, None, w2, None, self.y, y2, ws, stream)
         else:
             binding.conv_bwd_filter(self.desc, self.x, self.dy, relu_y, self.dw, self.ws, stream)
 
@@ -963,7 +993,8 @@ def run_ours(args):
     if args.chain_only:
         print(json.dumps({"chain_fwd": chain_extras(flush_buf, device)}))
         return 0
-    wl = Workload(args.layer, args.dtype, args.batch, device)
+    # Above 4096 samples the inputs are drawn on the device (host generation would take minutes).
+    wl = Workload(args.layer, args.dtype, args.batch, device, on_device=args.batch > 4096)
     if args.profile_ops:
         return run_profile_ops(args, wl, flush_buf)
     if not args.no_graphs:
