@@ -1033,38 +1033,44 @@ fwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict__
 }
 
 // ======================================================================================
-// wgrad partials: tile = (128 output channels, KTp reduction indices k, one split range of
-// samples); the GEMM's K runs over the split's columns n = (b, oh, ow), a chunk being NSC
-// whole samples (NSC*P columns, zero-padded to the MMA step):
-//   D[oc, k] = sum_{n in split} G[n, oc] * X[n, k]
-// G (dy masked by y > 0) is the MMA's A operand in tensor memory (lane = output channel,
-// K = n along the columns); X (the patches) is the shared-memory B operand (N = KTp rows
-// of k, K-major along n; fp32 as tf32 hi rows then lo rows, so one N = 2*KTp MMA forms
-// G_hi*X_hi and G_hi*X_lo and an N = KTp MMA adds G_lo*X_hi).
+// wgrad partials: tile = (128 output channels, KTp <= 128 reduction indices k, one split
+// range of samples); the GEMM's K runs over the split's columns n = (b, oh, ow), a chunk
+// being NSC whole samples (NSC*P columns, zero-padded to the MMA step):
+//   D[k, oc] = sum_{n in split} X[n, k] * G[n, oc]
+// X (the patches) is the MMA's A operand in tensor memory (lane = k row, K = n along the
+// columns), written by the X formatters with tcgen05.st: consecutive lanes gather
+// consecutive k, mostly consecutive words of the raw x slab.  G (dy masked by y > 0) is the
+// shared-memory B operand (N = 128 output-channel rows, K-major along n; fp32 as tf32 hi
+// rows then lo rows, so one N = 256 MMA forms X_hi*G_hi and X_hi*G_lo and an N = 128 MMA adds
+// X_lo*G_hi), built by the G formatters with conflict-free 16-byte stores.  (With the
+// operands the other way round the patch stage's swizzled stores made the kernel
+// shared-memory bound: ~1600 wavefronts per 2-sample chunk at layer 1 fp32.)
 // Warp roles (608 threads):
 //   warps 0, 1  bulk-copy producers (lane 0 each): per chunk, the contiguous slab
 //               dy[b0 : b0+nb] (and y, the ReLU mask source) by warp 0, and x[b, ic_lo :
 //               ic_hi] (the k-tile's input channels) of each sample by warp 1, into a raw slot.
 //   warp 2      MMA.
-//   G warps     (the first 8 formatter warps for fp32, 4 for bf16) lane = output channel;
-//               the chunk's columns, masked and split, into a TMEM operand stage with
-//               tcgen05.st.
-//   X warps     (the other formatter warps) 16-byte units (row k, 4 or 8 columns) of the
-//               B stage.
-//   warps 3-18  epilogue: the fp32 tile to ws[split][oc][k] (row stride kpad).
+//   G warps     (the first 8 formatter warps for fp32, 4 for bf16) thread = output channel
+//               row; the chunk's columns, masked and split, as 16-byte units of the
+//               shared-memory stage.
+//   X warps     (the other formatter warps, the same number per TMEM lane quarter) thread =
+//               k row; groups of the chunk's columns into the TMEM operand stage.
+//   warps 3-18  epilogue: D[k][oc] to ws[split][oc][k] (row stride kpad; lanes store
+//               consecutive k).
 // ======================================================================================
 constexpr int WG_MMA_WARP = 2;
 constexpr int WG_FMT0 = 96;  // first formatter thread (warp 3)
 constexpr int WG_THREADS = WG_FMT0 + 32 * 16;
 constexpr int WG_MAXA = 8, WG_MAXB = 4, WG_MAXR = 5;
-// Formatter roles: G warps (a multiple of 4, one or more per TMEM lane quarter) and X
-// warps; the column groups of 8 words one G thread writes; the B-stage rows one X thread
-// builds (its k offsets stay in registers).  fp32 splits the warps evenly (G and X are
-// both 128 rows); bf16 gives X three quarters (its KTp is up to 256 rows).
+// Formatter roles: G warps (a multiple of 4; thread = output channel row of the shared-memory
+// stage) and X warps (the rest, a multiple of 4: each TMEM lane quarter gets the same number;
+// thread = k row of the tensor-memory stage); the column groups (two 16-byte units, or one
+// 8-word tcgen05.st) one thread of each builds.  Both get half the warps: each builds as many
+// elements per chunk as the other.
 template <typename T> struct WgRoles {
-    static constexpr int g_warps = TcTraits<T>::split ? 8 : 4;
-    static constexpr int g_groups = TcTraits<T>::split ? 2 : 4;
-    static constexpr int x_rows = TcTraits<T>::split ? 4 : 6;
+    static constexpr int g_warps = 8;
+    static constexpr int g_groups = 2;
+    static constexpr int x_groups = 2;
 };
 
 struct TcWgradGeom {
@@ -1124,9 +1130,9 @@ inline TcWgradGeom wgrad_geom(const ConvParams& p, int KTp, int raws, int nbs, i
     const int chk = std::min(p.IC, (KTp - 1) / p.KK + 2);
     g.xsb = round_up(chk * p.HW * es + 16, 16);
     g.raw_bytes = round_up(g.nsc * (g.gs * (p.relu ? 2 : 1) + g.xsb) + 32, 128);
-    g.b_bytes = KTp * ROWB * (Tr::split ? 2 : 1);
+    g.b_bytes = TC_M * ROWB * (Tr::split ? 2 : 1);  // g: TC_M output-channel rows (x2: tf32 hi, lo)
     g.nbs = nbs;
-    g.dcols = KTp * (Tr::split ? 2 : 1);
+    g.dcols = TC_M * (Tr::split ? 2 : 1);           // D[k][oc]: oc columns (x2: hi, lo products)
     g.acols = Tr::split ? 2 * Tr::KC : Tr::KC / 2;
     g.na = std::min(WG_MAXA, (512 - round_up(g.dcols, 32)) / g.acols);
     return g;
@@ -1135,7 +1141,7 @@ inline TcWgradGeom wgrad_geom(const ConvParams& p, int KTp, int raws, int nbs, i
 template <typename T>
 inline int wgrad_smem(const TcWgradGeom& g)
 {
-    return 1024 + g.nbs * g.b_bytes + g.raws * g.raw_bytes + int(sizeof(WgBars)) + 8 * g.cnp + 16;
+    return 1024 + g.nbs * g.b_bytes + g.raws * g.raw_bytes + int(sizeof(WgBars)) + 16 * g.cnp + 16;
 }
 
 // The wgrad CTA's work: tiles item0, item0 + istride, ... (its own kernel passes the block
@@ -1164,10 +1170,15 @@ __device__ __forceinline__ void wgrad_tc_body(const ConvParams& p, const T* __re
     const int acol0 = round_up(geo.dcols, 32);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // Column table of the x gather: column n -> (sample j, byte offset of its pixel from the
+    // sample's channel ic_lo in the x region), right after the dy table.
     for (int n = tid; n < geo.cnp; n += WG_THREADS) {
         const int j = n / p.P, pq = n % p.P;
         gtab[2 * n] = n < geo.nsc * p.P ? j : 1 << 20;
         gtab[2 * n + 1] = (j * p.OCP + pq) * ES;
+        const int oh = pq / p.OW, ow = pq % p.OW;
+        gtab[2 * geo.cnp + 2 * n] = n < geo.nsc * p.P ? j : 1 << 20;
+        gtab[2 * geo.cnp + 2 * n + 1] = (oh * p.S * p.W + ow * p.S) * ES;
     }
     if (tid == 0) {
         for (int i = 0; i < geo.raws; ++i) {
@@ -1175,11 +1186,11 @@ __device__ __forceinline__ void wgrad_tc_body(const ConvParams& p, const T* __re
             mbar_init(smem_u32(&bars->raw_empty[i]), 16);
         }
         for (int i = 0; i < geo.na; ++i) {
-            mbar_init(smem_u32(&bars->a_full[i]), WgRoles<T>::g_warps);
+            mbar_init(smem_u32(&bars->a_full[i]), 16 - WgRoles<T>::g_warps);  // the X warps
             mbar_init(smem_u32(&bars->a_empty[i]), 1);
         }
         for (int i = 0; i < geo.nbs; ++i) {
-            mbar_init(smem_u32(&bars->b_full[i]), 16 - WgRoles<T>::g_warps);
+            mbar_init(smem_u32(&bars->b_full[i]), WgRoles<T>::g_warps);  // the G warps
             mbar_init(smem_u32(&bars->b_empty[i]), 1);
         }
         mbar_init(smem_u32(&bars->acc_full), 1);
@@ -1295,8 +1306,10 @@ __device__ __forceinline__ void wgrad_tc_body(const ConvParams& p, const T* __re
     } else if (warp == WG_MMA_WARP) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
+            // A = the x patches (TMEM, M = TC_M k rows), B = g (shared memory, N = TC_M output
+            // channels, fp32: N = 2*TC_M over [g_hi; g_lo], then N = TC_M over g_hi).
             const uint32_t idesc2 = instr_desc(Tr::fmt, TC_M, geo.dcols);
-            const uint32_t idesc1 = instr_desc(Tr::fmt, TC_M, KTp);
+            const uint32_t idesc1 = instr_desc(Tr::fmt, TC_M, TC_M);
             const uint32_t b_u32 = smem_u32(bring);
             const int ksteps = geo.cnp / KS;
             RingPos ap, bp;
@@ -1339,39 +1352,39 @@ __device__ __forceinline__ void wgrad_tc_body(const ConvParams& p, const T* __re
         __syncwarp();
     } else if (warp >= 3) {
         const int fw = warp - 3;            // 0 .. 15
-        const int qd = warp & 3;            // TMEM lane quarter
+        const int qd = warp & 3;            // TMEM lane quarter (X formatters, epilogue)
         const uint32_t lane_bits = uint32_t(qd * 32) << 16;
         constexpr int NGW = WgRoles<T>::g_warps;
-        const int m = qd * 32 + lane;       // output channel within the tile (G, epilogue)
-        // Epilogue of tile t: D[oc][k] -> ws; this warp's lanes, a quarter of the k columns.
+        constexpr int NXS = (16 - NGW) / 4;  // X warps per TMEM lane quarter
+        const int2* xtab = reinterpret_cast<const int2*>(gtab + 2 * geo.cnp);
+        // Epilogue of tile t: D[k][oc] -> ws[split][oc][k]; lane = k row of this warp's quarter,
+        // 32 of the oc columns per warp of the quarter (consecutive lanes store consecutive k).
         auto epilogue = [&](const TileInfo& ti, uint32_t t) -> bool {
             if (!mbar_wait_or_abort(smem_u32(&bars->acc_full), t & 1, abort_flag)) {
                 report(const_cast<int*>(abort_flag), 2u);
                 return false;
             }
             tc_fence_after();
-            const int oc = ti.oc0 + m;
-            const int kq = KTp / 4, c0 = (fw >> 2) * kq;
-            for (int cb = c0; cb < c0 + kq; cb += 8) {
+            const int k = ti.k0 + qd * 32 + lane;
+            const bool kin = qd * 32 + lane < KTp && k < p.Kred;
+            const int c0 = (fw >> 2) * (TC_M / 4);
+            for (int cb = c0; cb < c0 + TC_M / 4; cb += 8) {
                 uint32_t r[8];
                 tmem_ld8(tmem + lane_bits + uint32_t(cb), r);
                 if constexpr (Tr::split) {
                     uint32_t r2[8];
-                    tmem_ld8(tmem + lane_bits + uint32_t(KTp + cb), r2);
+                    tmem_ld8(tmem + lane_bits + uint32_t(TC_M + cb), r2);
                     tmem_ld_wait();
 #pragma unroll
                     for (int e = 0; e < 8; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(r2[e]));
                 } else {
                     tmem_ld_wait();
                 }
-                const int k = ti.k0 + cb;
-                if (oc < p.OC && m < ti.rows && k < geo.kpad) {
-                    float* dst = ws + (size_t(ti.split) * p.OC + oc) * geo.kpad + k;
-                    *reinterpret_cast<float4*>(dst) = make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]),
-                                                                  __uint_as_float(r[2]), __uint_as_float(r[3]));
-                    if (k + 4 < geo.kpad)
-                        *reinterpret_cast<float4*>(dst + 4) = make_float4(
-                            __uint_as_float(r[4]), __uint_as_float(r[5]), __uint_as_float(r[6]), __uint_as_float(r[7]));
+                if (kin) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        if (cb + e < ti.rows)
+                            ws[(size_t(ti.split) * p.OC + ti.oc0 + cb + e) * geo.kpad + k] = __uint_as_float(r[e]);
                 }
             }
             tc_fence_before();
@@ -1380,9 +1393,13 @@ __device__ __forceinline__ void wgrad_tc_body(const ConvParams& p, const T* __re
             return true;
         };
         if (fw < NGW) {
-            // ---------------- G formatters ----------------
+            // ---------------- G formatters: the shared-memory operand ----------------
+            // Thread = output channel row m of the B stage (oc0 + m); its column groups of NG
+            // columns, each two 16-byte units of the K-major, 128-byte-swizzled row (fp32: the
+            // tf32 hi rows, then the lo rows TC_M rows further).
+            const int m = qd * 32 + lane;
             const int gsub = fw >> 2;           // which of the NGW/4 warps of its lane quarter
-            constexpr int NG = ES == 4 ? 8 : 16;       // columns per tcgen05.st of 8 words
+            constexpr int NG = ES == 4 ? 8 : 16;       // columns per group: two 16-byte units
             constexpr int MAXG = WgRoles<T>::g_groups;  // column groups per thread
             const int ngroups = geo.cnp / NG;
             // Fast path: P a multiple of 4 -> runs of 4 positions of one
@@ -1400,7 +1417,7 @@ __device__ __forceinline__ void wgrad_tc_body(const ConvParams& p, const T* __re
                     goff[gi][vi] = (int(j) * p.OCP + int(pq)) * ES;
                     gsj[gi][vi] = n < geo.nsc * p.P ? int(j) : 1 << 20;  // padding: never a real sample
                 }
-            RingPos rp, ap;
+            RingPos rp, bp;
             uint32_t t = 0;
             for (int tile = item0; tile < total; tile += istride, ++t) {
                 const TileInfo ti = decode(tile);
@@ -1419,16 +1436,15 @@ __device__ __forceinline__ void wgrad_tc_body(const ConvParams& p, const T* __re
                     const int b0 = ti.s_lo + ti.chunk(kc) * geo.nsc;
                     const int nb = min(geo.nsc, ti.s_hi - b0);
                     const uint32_t slot = smem_u32(raw + rp.i * geo.raw_bytes);
-                    if (ap.wrapped && !mbar_wait_or_abort(smem_u32(&bars->a_empty[ap.i]), ap.ph ^ 1u, abort_flag)) {
+                    if (bp.wrapped && !mbar_wait_or_abort(smem_u32(&bars->b_empty[bp.i]), bp.ph ^ 1u, abort_flag)) {
                         report(const_cast<int*>(abort_flag), 1u);
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
+                    unsigned char* op = bring + bp.i * geo.b_bytes;
                     // Element (sample j, channel m, position pq) of the dy region; y is gregion further.
                     const int dg0 = int(((size_t(b0) * p.OCP + size_t(ti.oc0) * p.P) * ES) & 15);
                     const bool live = m < ti.rows;
-                    const uint32_t col = tmem + lane_bits + uint32_t(acol0 + ap.i * geo.acols);
                     const uint32_t gbase = slot + uint32_t(dg0 + m * p.P * ES);
                     const uint32_t gtab_u32 = smem_u32(gtab);
 #pragma unroll
@@ -1495,16 +1511,95 @@ __device__ __forceinline__ void wgrad_tc_body(const ConvParams& p, const T* __re
                             for (int e = 0; e < NG; ++e) bsum += __uint_as_float(ES == 4 ? v[e] : (v[e] << 16));
                         }
                         if constexpr (Tr::split) {
-                            uint32_t hi[8], lo[8];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) split_tf32(v[e], hi[e], lo[e]);
-                            tmem_st8(col + uint32_t(g * NG), hi);
-                            tmem_st8(col + uint32_t(Tr::KC + g * NG), lo);
+                            put_raw_unit<T, 1>(op, op + TC_M * ROWB, unit_off<1>(m, 2 * g), make_uint4(v[0], v[1], v[2], v[3]));
+                            put_raw_unit<T, 1>(op, op + TC_M * ROWB, unit_off<1>(m, 2 * g + 1),
+                                               make_uint4(v[4], v[5], v[6], v[7]));
                         } else {
                             uint32_t wv[8];
 #pragma unroll
                             for (int e = 0; e < 8; ++e) wv[e] = __byte_perm(v[2 * e], v[2 * e + 1], 0x5410);
-                            tmem_st8(col + uint32_t(g * NG / 2), wv);
+                            put_raw_unit<T, 1>(op, op, unit_off<1>(m, 2 * g), make_uint4(wv[0], wv[1], wv[2], wv[3]));
+                            put_raw_unit<T, 1>(op, op, unit_off<1>(m, 2 * g + 1), make_uint4(wv[4], wv[5], wv[6], wv[7]));
+                        }
+                    }
+                    fence_proxy_async_smem();  // the generic-proxy stores, for the tensor core
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(smem_u32(&bars->b_full[bp.i]));
+                        mbar_arrive(smem_u32(&bars->raw_empty[rp.i]));
+                    }
+                    bp.next(geo.nbs);
+                }
+                if (ok && bias_tile && m < ti.rows)
+                    bpart[(size_t(ti.split) * (NGW / 4) + gsub) * p.OC + ti.oc0 + m] = bsum;
+                if (!ok || !epilogue(ti, t)) break;
+            }
+        } else {
+            // ---------------- X formatters: the tensor-memory operand ----------------
+            // Thread = k row of the tile (TMEM lane qd*32 + lane); its column groups of XG
+            // columns (one tcgen05.st of 8 words each), the values gathered from the raw x slab:
+            // column n = (sample j, position) reads x at the sample's slab + the position's
+            // pixel offset + the row's k offset.  Consecutive lanes are consecutive k, i.e.
+            // mostly consecutive words of the slab.
+            const int xsub = (fw - NGW) >> 2;  // which of the NXS warps of its lane quarter
+            constexpr int XG = ES == 4 ? 8 : 16;
+            constexpr int XMAXG = WgRoles<T>::x_groups;
+            const int xgroups = geo.cnp / XG;
+            const int kr = qd * 32 + lane;
+            RingPos rp, ap;
+            uint32_t t = 0;
+            for (int tile = item0; tile < total; tile += istride, ++t) {
+                const TileInfo ti = decode(tile);
+                const int k = ti.k0 + kr;
+                const int ko = (kr < KTp && k < p.Kred) ? (k_offset(p, k) - ti.ic_lo * p.HW) * ES : -1;
+                bool ok = true;
+                for (int kc = 0; kc < ti.nchunks; ++kc, rp.next(geo.raws)) {
+                    if (!mbar_wait_or_abort(smem_u32(&bars->raw_full[rp.i]), rp.ph, abort_flag)) {
+                        report(const_cast<int*>(abort_flag), 1u);
+                        ok = false;
+                        break;
+                    }
+                    const int b0 = ti.s_lo + ti.chunk(kc) * geo.nsc;
+                    const int nb = min(geo.nsc, ti.s_hi - b0);
+                    const uint32_t slot = smem_u32(raw + rp.i * geo.raw_bytes);
+                    if (ap.wrapped && !mbar_wait_or_abort(smem_u32(&bars->a_empty[ap.i]), ap.ph ^ 1u, abort_flag)) {
+                        report(const_cast<int*>(abort_flag), 1u);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // Sample j's slab sits (m0 + j * mstep) mod 16 bytes into its slot (its source's
+                    // 16-byte misalignment).
+                    const int m0 = int(((size_t(b0) * p.IHW + size_t(ti.ic_lo) * p.HW) * ES) & 15);
+                    const int mstep = int((size_t(p.IHW) * ES) & 15);
+                    const uint32_t xbase = slot + uint32_t(xoff + (ko >= 0 ? ko : 0));
+                    const uint32_t col = tmem + lane_bits + uint32_t(acol0 + ap.i * geo.acols);
+#pragma unroll
+                    for (int gi = 0; gi < XMAXG; ++gi) {
+                        const int g = xsub + gi * NXS;
+                        if (g >= xgroups) break;
+                        uint32_t v[XG];
+#pragma unroll
+                        for (int e = 0; e < XG; ++e) {
+                            const int2 c = xtab[g * XG + e];  // (sample, pixel byte offset); the same for the warp
+                            v[e] = 0u;
+                            if (ko >= 0 && c.x < nb) {
+                                const int mj = (m0 + c.x * mstep) & 15;
+                                const uint32_t a = xbase + uint32_t(c.x * geo.xsb + mj + c.y);
+                                v[e] = ES == 4 ? lds32(a) : lds16(a);
+                            }
+                        }
+                        if constexpr (Tr::split) {
+                            uint32_t hi[8], lo[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) split_tf32(v[e], hi[e], lo[e]);
+                            tmem_st8(col + uint32_t(g * 8), hi);
+                            tmem_st8(col + uint32_t(Tr::KC + g * 8), lo);
+                        } else {
+                            uint32_t wv[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) wv[e] = __byte_perm(v[2 * e], v[2 * e + 1], 0x5410);
+                            tmem_st8(col + uint32_t(g * 8), wv);
                         }
                     }
                     tmem_st_wait();
@@ -1516,102 +1611,6 @@ __device__ __forceinline__ void wgrad_tc_body(const ConvParams& p, const T* __re
                     }
                     ap.next(geo.na);
                 }
-                if (ok && bias_tile && m < ti.rows)
-                    bpart[(size_t(ti.split) * (NGW / 4) + gsub) * p.OC + ti.oc0 + m] = bsum;
-                if (!ok || !epilogue(ti, t)) break;
-            }
-        } else {
-            // ---------------- X formatters ----------------
-            // 16-byte unit column c (E columns) of rows rbase + i*rstep.
-            const int xthreads = 32 * (16 - NGW);
-            const int xt = tid - WG_FMT0 - 32 * NGW;
-            const int upr = geo.cnp / Tr::E;     // units per row
-            const int cfix = xt % upr;
-            const int rbase = xt / upr;
-            const int rstep = xthreads / upr;
-            const bool xact = xt < rstep * upr;
-            constexpr int XMAXR = WgRoles<T>::x_rows;  // rows per thread (checked by the planner)
-            int po[Tr::E], jj[Tr::E];            // column offset and sample of this thread's columns
-#pragma unroll
-            for (int e = 0; e < Tr::E; ++e) {
-                const int n = cfix * Tr::E + e;
-                uint32_t j, r, oh, ow;
-                p.dm_P.divmod(uint32_t(n), j, r);
-                p.dm_OW.divmod(r, oh, ow);
-                jj[e] = n < geo.nsc * p.P ? int(j) : 1 << 20;  // padding columns: never a real sample
-                po[e] = (int(oh) * p.S * p.W + int(ow) * p.S) * ES;
-            }
-            uint32_t uo[XMAXR];                  // unit offsets of this thread's rows in a B stage
-#pragma unroll
-            for (int i = 0; i < XMAXR; ++i) uo[i] = unit_off<1>(rbase + i * rstep, cfix);
-            RingPos rp, bp;
-            uint32_t t = 0;
-            for (int tile = item0; tile < total; tile += istride, ++t) {
-                const TileInfo ti = decode(tile);
-                // Byte offsets of this thread's rows k = k0 + rbase + i*rstep (-1: past Kred).
-                int ko[XMAXR];
-#pragma unroll
-                for (int i = 0; i < XMAXR; ++i) {
-                    const int r = rbase + i * rstep;
-                    const int k = ti.k0 + r;
-                    ko[i] = (xact && r < KTp && k < p.Kred) ? (k_offset(p, k) - ti.ic_lo * p.HW) * ES : -1;
-                }
-                bool ok = true;
-                for (int kc = 0; kc < ti.nchunks; ++kc, rp.next(geo.raws)) {
-                    if (!mbar_wait_or_abort(smem_u32(&bars->raw_full[rp.i]), rp.ph, abort_flag)) {
-                        report(const_cast<int*>(abort_flag), 1u);
-                        ok = false;
-                        break;
-                    }
-                    const int b0 = ti.s_lo + ti.chunk(kc) * geo.nsc;
-                    const int nb = min(geo.nsc, ti.s_hi - b0);
-                    const uint32_t slot = smem_u32(raw + rp.i * geo.raw_bytes);
-                    if (bp.wrapped && !mbar_wait_or_abort(smem_u32(&bars->b_empty[bp.i]), bp.ph ^ 1u, abort_flag)) {
-                        report(const_cast<int*>(abort_flag), 1u);
-                        ok = false;
-                        break;
-                    }
-                    unsigned char* op = bring + bp.i * geo.b_bytes;
-                    if (xact) {
-                        // Sample bases of this thread's columns in the x region (with the slack
-                        // of each sample's 16-byte-rounded copy).
-                        uint32_t xs[Tr::E];
-#pragma unroll
-                        for (int e = 0; e < Tr::E; ++e) {
-                            const int j = min(jj[e], geo.nsc - 1);
-                            const size_t b = size_t(b0 + j);
-                            xs[e] = slot + uint32_t(xoff + j * geo.xsb +
-                                                    int(((b * p.IHW + size_t(ti.ic_lo) * p.HW) * ES) & 15) + po[e]);
-                        }
-#pragma unroll
-                        for (int i = 0; i < XMAXR; ++i) {
-                            const int r = rbase + i * rstep;
-                            if (r >= KTp) break;
-                            uint32_t wv[4] = {0, 0, 0, 0};
-                            if (ko[i] >= 0) {
-#pragma unroll
-                                for (int e = 0; e < Tr::E; ++e) {
-                                    if (jj[e] < nb) {
-                                        if constexpr (ES == 2) {
-                                            const uint32_t h = lds16(xs[e] + uint32_t(ko[i]));
-                                            wv[e >> 1] |= (e & 1) ? (h << 16) : h;
-                                        } else {
-                                            wv[e] = lds32(xs[e] + uint32_t(ko[i]));
-                                        }
-                                    }
-                                }
-                            }
-                            put_raw_unit<T, 1>(op, op + KTp * ROWB, uo[i], make_uint4(wv[0], wv[1], wv[2], wv[3]));
-                        }
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(smem_u32(&bars->b_full[bp.i]));
-                        mbar_arrive(smem_u32(&bars->raw_empty[rp.i]));
-                    }
-                    bp.next(geo.nbs);
-                                }
                 if (!ok || !epilogue(ti, t)) break;
             }
         }
@@ -2840,13 +2839,11 @@ static bool pick_wgrad(const ConvParams& p, const DevInfo& d, TcWgradGeom& out)
 {
     using Tr = TcTraits<T>;
     if (p.P > Tr::KC || p.B <= 0 || p.OC > TC_M) return false;  // one dy range of all OC per chunk
-    const int ktmax = Tr::split ? 128 : 256;
-    const int ktp = std::min(ktmax, round_up(p.Kred, 32));  // epilogue quarters of 8-column loads
+    const int ktp = std::min(TC_M, round_up(p.Kred, 32));  // k rows per tile: the TMEM lanes
     const int cnp = round_up(wgrad_nsc(p.P, Tr::KC, Tr::KC / 4) * p.P, Tr::KC / 4);
-    const int upr = cnp / Tr::E;
-    if (ceil_div(ktp, 32 * (16 - WgRoles<T>::g_warps) / upr) > WgRoles<T>::x_rows) return false;  // rows per X thread
-    const int ng = Tr::split ? 8 : 16;  // G columns per group
+    const int ng = Tr::split ? 8 : 16;  // columns per G / X group
     if (ceil_div(cnp / ng, WgRoles<T>::g_warps / 4) > WgRoles<T>::g_groups) return false;
+    if (ceil_div(cnp / ng, (16 - WgRoles<T>::g_warps) / 4) > WgRoles<T>::x_groups) return false;
     const int tiles = ceil_div(p.Kred, ktp) * ceil_div(p.OC, TC_M);
     const int nsc = wgrad_nsc(p.P, Tr::KC, Tr::KC / 4);
     int splits = std::max(1, d.sms / tiles);
@@ -3026,13 +3023,13 @@ cudaError_t run_dgrad_tc(const Plan& pl, const ConvParams& p, int dt, const void
 // Fused only while d_input's own launch has fewer than two waves of work items: then its last
 // wave leaves SMs idle that the wgrad tiles can fill.  With more items the tail is a small part
 // of the launch, and one CTA per item (each with its own prologue) loses to the persistent
-// standalone kernels.  Fused: wgrad's stages with the split count that gives about half as many
-// tiles as SMs (the long items: half the SMs run them, the other half d_input's items and then
-// the rest), and d_input's workspace-path geometry with its k-tiles cut into DG_BWD_RANGES
-// ranges per sample tile (short items that backfill).  Measured on a GB300 at both encoder
-// layers and both dtypes (B = 1024, 4096, 16384), against wgrad tiles on a third, two thirds and
-// all of the SMs and two to four ranges.
-constexpr int DG_BWD_RANGES = 2;
+// standalone kernels.  Fused: wgrad's stages with the split count that gives about two thirds as
+// many tiles as SMs (the long items: two thirds of the SMs run them, the rest d_input's items and
+// then everything), and d_input's workspace-path geometry with its k-tiles cut into two ranges
+// per sample tile, three when the sample tiles fill fewer than a quarter of the SMs (short items
+// that backfill).  Measured on a GB300 at both encoder layers and both dtypes (B = 1024: wgrad
+// tiles on 35, 50, 65, 80 and 95 % of the SMs, two and three ranges; B = 4096, 16384 for the
+// fusion rule).
 
 template <typename T>
 static bool pick_bwd(const ConvParams& p, const DevInfo& d, TcDgradGeom& dg, TcWgradGeom& wg)
@@ -3041,9 +3038,10 @@ static bool pick_bwd(const ConvParams& p, const DevInfo& d, TcDgradGeom& dg, TcW
     if (!pick_dgrad<T>(p, d, true, dg) || !pick_wgrad<T>(p, d, wg)) return false;
     if (dg.ntiles * dg.ktsplit >= 2 * d.sms) return false;
     const int tiles = wg.k_tiles * wg.oc_tiles;
-    const int splits = std::min(std::max(1, (d.sms / 2 + tiles / 2) / tiles), std::max(1, p.B / (2 * wg.nsc)));
+    const int splits = std::min(std::max(1, (2 * d.sms / 3 + tiles / 2) / tiles), std::max(1, p.B / (2 * wg.nsc)));
     wg = wgrad_geom<T>(p, wg.KTp, wg.raws, wg.nbs, splits);
-    dg.kt_per = ceil_div(dg.nkt, std::min(dg.nkt, DG_BWD_RANGES));
+    const int ranges = 4 * dg.ntiles < d.sms ? 3 : 2;
+    dg.kt_per = ceil_div(dg.nkt, std::min(dg.nkt, ranges));
     dg.ktsplit = ceil_div(dg.nkt, dg.kt_per);
     return true;
 }

@@ -187,9 +187,10 @@ int conv_bwd_filter_bias(const conv_desc_t* desc, const void* x, const void* dy,
  * work item per CTA: first the wgrad tiles (the long items), then d_input's work items cut into
  * k-tile ranges (short items: disjoint dx channels, no reduction), so that d_input fills the SMs
  * the wgrad tiles leave idle and backfills the others as they finish.  Each operation computes
- * exactly as in its own kernel, but wgrad splits the batch into about half as many ranges as
- * conv_bwd_filter (its tiles then fill half the SMs), so dw may differ from conv_bwd_filter's in
- * the last bits (same tolerance, deterministic); dx is bit for bit conv_bwd_data's.  Otherwise
+ * exactly as in its own kernel, but wgrad splits the batch into fewer ranges than
+ * conv_bwd_filter (its tiles then fill about two thirds of the SMs), so dw may differ from
+ * conv_bwd_filter's in the last bits (same tolerance, deterministic); dx is bit for bit
+ * conv_bwd_data's.  Otherwise
  * (conv_query(CONV_OP_BWD) reports algo CONV_ALGO_AUTO) conv_bwd_data's workspace path and
  * conv_bwd_filter run one after the other, each with its own part of the workspace.
  *   x, dy, w, y (required when relu): inputs; dx, dw, db (may be NULL): written.
