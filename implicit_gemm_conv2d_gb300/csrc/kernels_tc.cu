@@ -1072,6 +1072,15 @@ template <typename T> struct WgRoles {
     static constexpr int g_groups = 2;
     static constexpr int x_groups = 2;
 };
+// The other layout (wgrad_tc_body_gt): g in tensor memory (lane = output channel) and the
+// patches as the shared-memory operand, k-tiles up to 256 rows in bf16.  G warps (thread =
+// output channel lane, its column groups of 8 words) and X warps (16-byte units of the
+// patch stage, x_rows rows per thread).
+template <typename T> struct WgRolesGt {
+    static constexpr int g_warps = TcTraits<T>::split ? 8 : 4;
+    static constexpr int g_groups = TcTraits<T>::split ? 2 : 4;
+    static constexpr int x_rows = TcTraits<T>::split ? 4 : 6;
+};
 
 struct TcWgradGeom {
     int KTp;       // k rows per tile (multiple of 32): <= 128 (fp32), <= 256 (bf16)
@@ -1089,6 +1098,7 @@ struct TcWgradGeom {
     int nbs;       // B stages
     int dcols;     // accumulator columns
     int acols, na; // TMEM columns per A stage, A stages
+    int layout;    // 0: patches in TMEM (wgrad_tc_body); 1: g in TMEM (wgrad_tc_body_gt)
 };
 
 struct WgBars {
@@ -1109,7 +1119,7 @@ inline int wgrad_nsc(int P, int KC, int ks)
 }
 
 template <typename T>
-inline TcWgradGeom wgrad_geom(const ConvParams& p, int KTp, int raws, int nbs, int splits)
+inline TcWgradGeom wgrad_geom(const ConvParams& p, int KTp, int raws, int nbs, int splits, int layout)
 {
     using Tr = TcTraits<T>;
     const int es = int(sizeof(T));
@@ -1130,9 +1140,14 @@ inline TcWgradGeom wgrad_geom(const ConvParams& p, int KTp, int raws, int nbs, i
     const int chk = std::min(p.IC, (KTp - 1) / p.KK + 2);
     g.xsb = round_up(chk * p.HW * es + 16, 16);
     g.raw_bytes = round_up(g.nsc * (g.gs * (p.relu ? 2 : 1) + g.xsb) + 32, 128);
-    g.b_bytes = TC_M * ROWB * (Tr::split ? 2 : 1);  // g: TC_M output-channel rows (x2: tf32 hi, lo)
+    // Shared-memory stage: g's TC_M output-channel rows (layout 0) or the KTp patch rows (layout
+    // 1), x2 for the tf32 hi and lo rows; accumulator columns: D[k][oc]'s TC_M oc columns or
+    // D[oc][k]'s KTp k columns, x2 for the hi and lo products.
+    g.layout = layout;
+    const int brows = layout ? KTp : TC_M;
+    g.b_bytes = brows * ROWB * (Tr::split ? 2 : 1);
     g.nbs = nbs;
-    g.dcols = TC_M * (Tr::split ? 2 : 1);           // D[k][oc]: oc columns (x2: hi, lo products)
+    g.dcols = brows * (Tr::split ? 2 : 1);
     g.acols = Tr::split ? 2 * Tr::KC : Tr::KC / 2;
     g.na = std::min(WG_MAXA, (512 - round_up(g.dcols, 32)) / g.acols);
     return g;
@@ -1624,11 +1639,503 @@ __device__ __forceinline__ void wgrad_tc_body(const ConvParams& p, const T* __re
 }
 
 template <typename T, bool RELU>
+__device__ __forceinline__ void wgrad_tc_body_gt(const ConvParams& p, const T* __restrict__ x, const T* __restrict__ dy,
+                                              const T* __restrict__ y, float* __restrict__ ws,
+                                              float* __restrict__ bpart, const TcWgradGeom& geo, const int item0,
+                                              const int istride)
+{
+    using Tr = TcTraits<T>;
+    constexpr int ES = int(sizeof(T));
+    constexpr int KS = Tr::KC / 4;  // columns per MMA K-step
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = align1024(smem_raw);
+    const int KTp = geo.KTp;
+    unsigned char* bring = smem;
+    unsigned char* raw = bring + geo.nbs * geo.b_bytes;
+    WgBars* bars = reinterpret_cast<WgBars*>(raw + geo.raws * geo.raw_bytes);
+    // Column table of a chunk: column n -> (sample j, byte offset of (j, pq) in the dy
+    // region from channel row 0); padding columns get a sample no chunk has.
+    int* gtab = reinterpret_cast<int*>(bars + 1);
+    volatile int* abort_flag = &bars->abort_flag;
+    const int gregion = geo.nsc * geo.gs + 16;              // bytes of the dy (and of the y) region
+    const int xoff = gregion * (RELU ? 2 : 1);              // start of the x region in a slot
+    const int acol0 = round_up(geo.dcols, 32);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int n = tid; n < geo.cnp; n += WG_THREADS) {
+        const int j = n / p.P, pq = n % p.P;
+        gtab[2 * n] = n < geo.nsc * p.P ? j : 1 << 20;
+        gtab[2 * n + 1] = (j * p.OCP + pq) * ES;
+    }
+    if (tid == 0) {
+        for (int i = 0; i < geo.raws; ++i) {
+            mbar_init(smem_u32(&bars->raw_full[i]), 2);  // the two producers' arrivals
+            mbar_init(smem_u32(&bars->raw_empty[i]), 16);
+        }
+        for (int i = 0; i < geo.na; ++i) {
+            mbar_init(smem_u32(&bars->a_full[i]), WgRolesGt<T>::g_warps);
+            mbar_init(smem_u32(&bars->a_empty[i]), 1);
+        }
+        for (int i = 0; i < geo.nbs; ++i) {
+            mbar_init(smem_u32(&bars->b_full[i]), 16 - WgRolesGt<T>::g_warps);
+            mbar_init(smem_u32(&bars->b_empty[i]), 1);
+        }
+        mbar_init(smem_u32(&bars->acc_full), 1);
+        mbar_init(smem_u32(&bars->acc_empty), 16);
+        fence_mbar_init();
+        bars->abort_flag = 0;
+    }
+    if (warp == 0) tmem_alloc(smem_u32(&bars->tslot), 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tslot;
+    // Nothing above touches global memory: the previous kernel on the stream may still run.
+    grid_dep_wait();
+    const int per_split = geo.k_tiles * geo.oc_tiles;
+    const int total = per_split * geo.splits;
+
+    // Tile decode shared by all roles.
+    // The k-tiles of one split read the same dy / y chunks: each starts at a different
+    // chunk (a fixed rotation, so the summation order is fixed) so that they do not all
+    // request the same lines at once.
+    struct TileInfo {
+        int split, k0, oc0, rows, s_lo, s_hi, nchunks, ic_lo, ic_hi, rot;
+        __device__ int chunk(int kc) const { return kc + rot < nchunks ? kc + rot : kc + rot - nchunks; }
+    };
+    auto decode = [&](int tile) {
+        TileInfo ti;
+        ti.split = tile / per_split;
+        const int rem = tile % per_split;
+        ti.k0 = (rem % geo.k_tiles) * KTp;
+        ti.oc0 = (rem / geo.k_tiles) * TC_M;
+        ti.rows = min(TC_M, p.OC - ti.oc0);
+        ti.s_lo = int((long long)p.B * ti.split / geo.splits);
+        ti.s_hi = int((long long)p.B * (ti.split + 1) / geo.splits);
+        ti.nchunks = (ti.s_hi - ti.s_lo + geo.nsc - 1) / geo.nsc;
+        ti.ic_lo = ti.k0 / p.KK;
+        ti.ic_hi = min(p.IC - 1, (min(ti.k0 + KTp, p.Kred) - 1) / p.KK);
+        ti.rot = (rem % geo.k_tiles) * ti.nchunks / geo.k_tiles;
+        return ti;
+    };
+
+    if (warp <= 1) {
+        // ---------------- bulk-copy producers ----------------
+        // Lane 0 of warp 0 copies dy[b0 : b0+nb] (all channels, contiguous) and y; lane 0
+        // of warp 1 copies x[b, ic_lo : ic_hi] of each sample: two threads on two SM
+        // sub-partitions, each arriving once (with its transaction bytes) on the slot's
+        // barrier.  Sources are rounded down to 16 bytes (the slack is skipped when read);
+        // bytes of a last 16-byte block past the end of a tensor are copied by plain loads
+        // before the arrival that releases them.
+        if (lane == 0) {
+            const bool gside = warp == 0;
+            const unsigned char* xb = reinterpret_cast<const unsigned char*>(x);
+            const unsigned char* gb = reinterpret_cast<const unsigned char*>(dy);
+            const unsigned char* yb = reinterpret_cast<const unsigned char*>(y);
+            const unsigned char* x_end = xb + size_t(p.B) * p.IHW * ES;
+            const unsigned char* g_end = gb + size_t(p.B) * p.OCP * ES;
+            const unsigned char* y_end = yb + size_t(p.B) * p.OCP * ES;
+            const size_t xstride = size_t(p.IHW) * ES, gstride = size_t(p.OCP) * ES;
+            auto tail = [&](unsigned char* dstp, const unsigned char* src, int bytes, const unsigned char* end) -> int {
+                const int bulk = slab_bytes_bulk(src, bytes, end);
+                for (const unsigned char* t = src + bulk; t < src + bytes && t < end; ++t) dstp[int(t - src)] = *t;
+                return bulk;
+            };
+            RingPos rp;
+            for (int tile = item0; tile < total && !*abort_flag; tile += istride) {
+                const TileInfo ti = decode(tile);
+                const int xbytes = (ti.ic_hi - ti.ic_lo + 1) * p.HW * ES;
+                for (int kc = 0; kc < ti.nchunks; ++kc, rp.next(geo.raws)) {
+                    const int s = rp.i;
+                    if (rp.wrapped && !mbar_wait_or_abort(smem_u32(&bars->raw_empty[s]), rp.ph ^ 1u, abort_flag)) {
+                        report(const_cast<int*>(abort_flag), 4u);
+                        break;
+                    }
+                    unsigned char* slot = raw + s * geo.raw_bytes;
+                    const uint32_t slot_u32 = smem_u32(slot), bar = smem_u32(&bars->raw_full[s]);
+                    const int b0 = ti.s_lo + ti.chunk(kc) * geo.nsc, nb = min(geo.nsc, ti.s_hi - b0);
+                    if (gside) {
+                        const size_t goff = size_t(b0) * gstride;
+                        const int gd = int(goff & 15);
+                        const int gbytes = round_up(gd + nb * int(gstride), 16);
+                        const bool at_end = b0 + nb == p.B;  // only then can a copy reach dy's end
+                        const int gbulk = at_end ? tail(slot, gb + goff - gd, gbytes, g_end) : gbytes;
+                        if (RELU && at_end) tail(slot + gregion, yb + goff - gd, gbytes, y_end);
+                        mbar_arrive_expect_tx(bar, uint32_t(gbulk * (RELU ? 2 : 1)));
+                        if (gbulk > 0) {
+                            bulk_g2s(slot_u32, gb + goff - gd, uint32_t(gbulk), bar);
+                            if (RELU) bulk_g2s(slot_u32 + gregion, yb + goff - gd, uint32_t(gbulk), bar);
+                        }
+                    } else {
+                        const unsigned char* xs = xb + size_t(b0) * xstride + size_t(ti.ic_lo) * p.HW * ES;
+                        const bool at_end = b0 + nb == p.B;  // only then can a copy reach x's end
+                        int tx = 0;
+                        for (int j = 0; j < nb; ++j) {
+                            const int xd = int(reinterpret_cast<uintptr_t>(xs + size_t(j) * xstride) & 15);
+                            const int bytes = round_up(xd + xbytes, 16);
+                            tx += at_end ? tail(slot + xoff + j * geo.xsb, xs + size_t(j) * xstride - xd, bytes, x_end)
+                                         : bytes;
+                        }
+                        mbar_arrive_expect_tx(bar, uint32_t(tx));
+                        for (int j = 0; j < nb; ++j) {
+                            const unsigned char* src = xs + size_t(j) * xstride;
+                            const int xd = int(reinterpret_cast<uintptr_t>(src) & 15);
+                            const int bytes = round_up(xd + xbytes, 16);
+                            const int xbulk = at_end ? slab_bytes_bulk(src - xd, bytes, x_end) : bytes;
+                            if (xbulk > 0)
+                                bulk_g2s(slot_u32 + uint32_t(xoff + j * geo.xsb), src - xd, uint32_t(xbulk), bar);
+                        }
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == WG_MMA_WARP) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            const uint32_t idesc2 = instr_desc(Tr::fmt, TC_M, geo.dcols);
+            const uint32_t idesc1 = instr_desc(Tr::fmt, TC_M, KTp);
+            const uint32_t b_u32 = smem_u32(bring);
+            const int ksteps = geo.cnp / KS;
+            RingPos ap, bp;
+            uint32_t t = 0;
+            for (int tile = item0; tile < total && !*abort_flag; tile += istride, ++t) {
+                const TileInfo ti = decode(tile);
+                bool ok = true;
+                if (t >= 1 && !mbar_wait_or_abort(smem_u32(&bars->acc_empty), (t - 1) & 1, abort_flag)) {
+                    report(const_cast<int*>(abort_flag), 8u);
+                    break;
+                }
+                tc_fence_after();
+                for (int kc = 0; kc < ti.nchunks; ++kc, ap.next(geo.na), bp.next(geo.nbs)) {
+                    if (!mbar_wait_or_abort(smem_u32(&bars->a_full[ap.i]), ap.ph, abort_flag) ||
+                        !mbar_wait_or_abort(smem_u32(&bars->b_full[bp.i]), bp.ph, abort_flag)) {
+                        report(const_cast<int*>(abort_flag), 8u);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t ba = b_u32 + bp.i * geo.b_bytes;
+                    const uint32_t aa = tmem + uint32_t(acol0 + ap.i * geo.acols);
+                    for (int j = 0; j < ksteps; ++j) {
+                        const uint64_t bd = op_desc<1>(ba + kstep_off<1>(j));
+                        const uint32_t acc = (kc == 0 && j == 0) ? 0u : 1u;
+                        if constexpr (Tr::split) {
+                            mma_tf32_ta(tmem, aa + 8 * j, bd, idesc2, acc);           // hi * [hi; lo]
+                            mma_tf32_ta(tmem, aa + Tr::KC + 8 * j, bd, idesc1, 1u);  // lo * hi
+                        } else {
+                            mma_f16_ta(tmem, aa + 8 * j, bd, idesc1, acc);
+                        }
+                    }
+                    mma_commit(smem_u32(&bars->a_empty[ap.i]));
+                    mma_commit(smem_u32(&bars->b_empty[bp.i]));
+                }
+                if (!ok) break;
+                mma_commit(smem_u32(&bars->acc_full));
+            }
+        }
+        __syncwarp();
+    } else if (warp >= 3) {
+        const int fw = warp - 3;            // 0 .. 15
+        const int qd = warp & 3;            // TMEM lane quarter
+        const uint32_t lane_bits = uint32_t(qd * 32) << 16;
+        constexpr int NGW = WgRolesGt<T>::g_warps;
+        const int m = qd * 32 + lane;       // output channel within the tile (G, epilogue)
+        // Epilogue of tile t: D[oc][k] -> ws; this warp's lanes, a quarter of the k columns.
+        auto epilogue = [&](const TileInfo& ti, uint32_t t) -> bool {
+            if (!mbar_wait_or_abort(smem_u32(&bars->acc_full), t & 1, abort_flag)) {
+                report(const_cast<int*>(abort_flag), 2u);
+                return false;
+            }
+            tc_fence_after();
+            const int oc = ti.oc0 + m;
+            const int kq = KTp / 4, c0 = (fw >> 2) * kq;
+            for (int cb = c0; cb < c0 + kq; cb += 8) {
+                uint32_t r[8];
+                tmem_ld8(tmem + lane_bits + uint32_t(cb), r);
+                if constexpr (Tr::split) {
+                    uint32_t r2[8];
+                    tmem_ld8(tmem + lane_bits + uint32_t(KTp + cb), r2);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(r2[e]));
+                } else {
+                    tmem_ld_wait();
+                }
+                const int k = ti.k0 + cb;
+                if (oc < p.OC && m < ti.rows && k < geo.kpad) {
+                    float* dst = ws + (size_t(ti.split) * p.OC + oc) * geo.kpad + k;
+                    *reinterpret_cast<float4*>(dst) = make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]),
+                                                                  __uint_as_float(r[2]), __uint_as_float(r[3]));
+                    if (k + 4 < geo.kpad)
+                        *reinterpret_cast<float4*>(dst + 4) = make_float4(
+                            __uint_as_float(r[4]), __uint_as_float(r[5]), __uint_as_float(r[6]), __uint_as_float(r[7]));
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty));
+            return true;
+        };
+        if (fw < NGW) {
+            // ---------------- G formatters ----------------
+            const int gsub = fw >> 2;           // which of the NGW/4 warps of its lane quarter
+            constexpr int NG = ES == 4 ? 8 : 16;       // columns per tcgen05.st of 8 words
+            constexpr int MAXG = WgRolesGt<T>::g_groups;  // column groups per thread
+            const int ngroups = geo.cnp / NG;
+            // Fast path: P a multiple of 4 -> runs of 4 positions of one
+            // sample are one vector load; per group of NG columns the byte offsets (from the
+            // thread's channel row) and samples of its NG/4 vectors never change.
+            const bool gfast = p.P % 4 == 0;
+            int goff[MAXG][NG / 4], gsj[MAXG][NG / 4];
+#pragma unroll
+            for (int gi = 0; gi < MAXG; ++gi)
+#pragma unroll
+                for (int vi = 0; vi < NG / 4; ++vi) {
+                    const int n = (gsub + gi * (NGW / 4)) * NG + vi * 4;
+                    uint32_t j, pq;
+                    p.dm_P.divmod(uint32_t(n), j, pq);
+                    goff[gi][vi] = (int(j) * p.OCP + int(pq)) * ES;
+                    gsj[gi][vi] = n < geo.nsc * p.P ? int(j) : 1 << 20;  // padding: never a real sample
+                }
+            RingPos rp, ap;
+            uint32_t t = 0;
+            for (int tile = item0; tile < total; tile += istride, ++t) {
+                const TileInfo ti = decode(tile);
+                // The bias gradient rides on the first k-tile of each split (one per (split, oc
+                // tile)): the sum of this thread's masked g values, chunk by chunk in ascending
+                // order (k-tile 0 starts at chunk 0), each chunk's values in ascending column.
+                const bool bias_tile = bpart != nullptr && ti.k0 == 0;
+                float bsum = 0.f;
+                bool ok = true;
+                for (int kc = 0; kc < ti.nchunks; ++kc, rp.next(geo.raws)) {
+                    if (!mbar_wait_or_abort(smem_u32(&bars->raw_full[rp.i]), rp.ph, abort_flag)) {
+                        report(const_cast<int*>(abort_flag), 1u);
+                        ok = false;
+                        break;
+                    }
+                    const int b0 = ti.s_lo + ti.chunk(kc) * geo.nsc;
+                    const int nb = min(geo.nsc, ti.s_hi - b0);
+                    const uint32_t slot = smem_u32(raw + rp.i * geo.raw_bytes);
+                    if (ap.wrapped && !mbar_wait_or_abort(smem_u32(&bars->a_empty[ap.i]), ap.ph ^ 1u, abort_flag)) {
+                        report(const_cast<int*>(abort_flag), 1u);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // Element (sample j, channel m, position pq) of the dy region; y is gregion further.
+                    const int dg0 = int(((size_t(b0) * p.OCP + size_t(ti.oc0) * p.P) * ES) & 15);
+                    const bool live = m < ti.rows;
+                    const uint32_t col = tmem + lane_bits + uint32_t(acol0 + ap.i * geo.acols);
+                    const uint32_t gbase = slot + uint32_t(dg0 + m * p.P * ES);
+                    const uint32_t gtab_u32 = smem_u32(gtab);
+#pragma unroll
+                    for (int gi = 0; gi < MAXG; ++gi) {
+                        const int g = gsub + gi * (NGW / 4);
+                        if (g >= ngroups) break;
+                        uint32_t v[NG];
+                        if (gfast) {
+                            uint32_t d[NG], w[NG];
+#pragma unroll
+                            for (int vi = 0; vi < NG / 4; ++vi) {
+                                // Only real rows and samples are read (the rest of the
+                                // region may lie past the slot).
+                                const uint32_t a = gbase + uint32_t(goff[gi][vi]);
+                                d[4 * vi] = d[4 * vi + 1] = d[4 * vi + 2] = d[4 * vi + 3] = 0u;
+                                w[4 * vi] = w[4 * vi + 1] = w[4 * vi + 2] = w[4 * vi + 3] = 0u;
+                                if (!live || gsj[gi][vi] >= nb) continue;
+                                if constexpr (ES == 4) {
+                                    const int4 q = lds128(a);
+                                    d[4 * vi] = q.x; d[4 * vi + 1] = q.y; d[4 * vi + 2] = q.z; d[4 * vi + 3] = q.w;
+                                    if (RELU) {
+                                        const int4 r = lds128(a + gregion);
+                                        w[4 * vi] = r.x; w[4 * vi + 1] = r.y; w[4 * vi + 2] = r.z; w[4 * vi + 3] = r.w;
+                                    }
+                                } else {
+                                    const uint2 q = lds64(a);
+                                    d[4 * vi] = q.x & 0xFFFFu; d[4 * vi + 1] = q.x >> 16;
+                                    d[4 * vi + 2] = q.y & 0xFFFFu; d[4 * vi + 3] = q.y >> 16;
+                                    if (RELU) {
+                                        const uint2 r = lds64(a + gregion);
+                                        w[4 * vi] = r.x << 16; w[4 * vi + 1] = r.x & 0xFFFF0000u;
+                                        w[4 * vi + 2] = r.y << 16; w[4 * vi + 3] = r.y & 0xFFFF0000u;
+                                    }
+                                }
+                            }
+#pragma unroll
+                            for (int e = 0; e < NG; ++e) {
+                                // mask words are fp32 patterns (bf16 y in the high half)
+                                const bool keep = live && gsj[gi][e / 4] < nb && (!RELU || __uint_as_float(w[e]) > 0.f);
+                                v[e] = keep ? d[e] : 0u;
+                            }
+                        } else {
+                            // Element by element through the column table (sample, byte offset).
+#pragma unroll
+                            for (int e = 0; e < NG; ++e) {
+                                const int n = g * NG + e;
+                                const int j = int(lds32(gtab_u32 + 8 * n)), off = int(lds32(gtab_u32 + 8 * n + 4));
+                                uint32_t d = 0u;
+                                if (live && j < nb) {
+                                    const uint32_t a = gbase + uint32_t(off);
+                                    if constexpr (ES == 4) {
+                                        d = lds32(a);
+                                        if (RELU && !(__uint_as_float(lds32(a + gregion)) > 0.f)) d = 0u;
+                                    } else {
+                                        d = lds16(a);
+                                        if (RELU && !(__uint_as_float(lds16(a + gregion) << 16) > 0.f)) d = 0u;
+                                    }
+                                }
+                                v[e] = d;
+                            }
+                        }
+                        if (bias_tile) {
+#pragma unroll
+                            for (int e = 0; e < NG; ++e) bsum += __uint_as_float(ES == 4 ? v[e] : (v[e] << 16));
+                        }
+                        if constexpr (Tr::split) {
+                            uint32_t hi[8], lo[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) split_tf32(v[e], hi[e], lo[e]);
+                            tmem_st8(col + uint32_t(g * NG), hi);
+                            tmem_st8(col + uint32_t(Tr::KC + g * NG), lo);
+                        } else {
+                            uint32_t wv[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) wv[e] = __byte_perm(v[2 * e], v[2 * e + 1], 0x5410);
+                            tmem_st8(col + uint32_t(g * NG / 2), wv);
+                        }
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(smem_u32(&bars->a_full[ap.i]));
+                        mbar_arrive(smem_u32(&bars->raw_empty[rp.i]));
+                    }
+                    ap.next(geo.na);
+                }
+                if (ok && bias_tile && m < ti.rows)
+                    bpart[(size_t(ti.split) * (NGW / 4) + gsub) * p.OC + ti.oc0 + m] = bsum;
+                if (!ok || !epilogue(ti, t)) break;
+            }
+        } else {
+            // ---------------- X formatters ----------------
+            // 16-byte unit column c (E columns) of rows rbase + i*rstep.
+            const int xthreads = 32 * (16 - NGW);
+            const int xt = tid - WG_FMT0 - 32 * NGW;
+            const int upr = geo.cnp / Tr::E;     // units per row
+            const int cfix = xt % upr;
+            const int rbase = xt / upr;
+            const int rstep = xthreads / upr;
+            const bool xact = xt < rstep * upr;
+            constexpr int XMAXR = WgRolesGt<T>::x_rows;  // rows per thread (checked by the planner)
+            int po[Tr::E], jj[Tr::E];            // column offset and sample of this thread's columns
+#pragma unroll
+            for (int e = 0; e < Tr::E; ++e) {
+                const int n = cfix * Tr::E + e;
+                uint32_t j, r, oh, ow;
+                p.dm_P.divmod(uint32_t(n), j, r);
+                p.dm_OW.divmod(r, oh, ow);
+                jj[e] = n < geo.nsc * p.P ? int(j) : 1 << 20;  // padding columns: never a real sample
+                po[e] = (int(oh) * p.S * p.W + int(ow) * p.S) * ES;
+            }
+            uint32_t uo[XMAXR];                  // unit offsets of this thread's rows in a B stage
+#pragma unroll
+            for (int i = 0; i < XMAXR; ++i) uo[i] = unit_off<1>(rbase + i * rstep, cfix);
+            RingPos rp, bp;
+            uint32_t t = 0;
+            for (int tile = item0; tile < total; tile += istride, ++t) {
+                const TileInfo ti = decode(tile);
+                // Byte offsets of this thread's rows k = k0 + rbase + i*rstep (-1: past Kred).
+                int ko[XMAXR];
+#pragma unroll
+                for (int i = 0; i < XMAXR; ++i) {
+                    const int r = rbase + i * rstep;
+                    const int k = ti.k0 + r;
+                    ko[i] = (xact && r < KTp && k < p.Kred) ? (k_offset(p, k) - ti.ic_lo * p.HW) * ES : -1;
+                }
+                bool ok = true;
+                for (int kc = 0; kc < ti.nchunks; ++kc, rp.next(geo.raws)) {
+                    if (!mbar_wait_or_abort(smem_u32(&bars->raw_full[rp.i]), rp.ph, abort_flag)) {
+                        report(const_cast<int*>(abort_flag), 1u);
+                        ok = false;
+                        break;
+                    }
+                    const int b0 = ti.s_lo + ti.chunk(kc) * geo.nsc;
+                    const int nb = min(geo.nsc, ti.s_hi - b0);
+                    const uint32_t slot = smem_u32(raw + rp.i * geo.raw_bytes);
+                    if (bp.wrapped && !mbar_wait_or_abort(smem_u32(&bars->b_empty[bp.i]), bp.ph ^ 1u, abort_flag)) {
+                        report(const_cast<int*>(abort_flag), 1u);
+                        ok = false;
+                        break;
+                    }
+                    unsigned char* op = bring + bp.i * geo.b_bytes;
+                    if (xact) {
+                        // Sample bases of this thread's columns in the x region (with the slack
+                        // of each sample's 16-byte-rounded copy).
+                        uint32_t xs[Tr::E];
+#pragma unroll
+                        for (int e = 0; e < Tr::E; ++e) {
+                            const int j = min(jj[e], geo.nsc - 1);
+                            const size_t b = size_t(b0 + j);
+                            xs[e] = slot + uint32_t(xoff + j * geo.xsb +
+                                                    int(((b * p.IHW + size_t(ti.ic_lo) * p.HW) * ES) & 15) + po[e]);
+                        }
+#pragma unroll
+                        for (int i = 0; i < XMAXR; ++i) {
+                            const int r = rbase + i * rstep;
+                            if (r >= KTp) break;
+                            uint32_t wv[4] = {0, 0, 0, 0};
+                            if (ko[i] >= 0) {
+#pragma unroll
+                                for (int e = 0; e < Tr::E; ++e) {
+                                    if (jj[e] < nb) {
+                                        if constexpr (ES == 2) {
+                                            const uint32_t h = lds16(xs[e] + uint32_t(ko[i]));
+                                            wv[e >> 1] |= (e & 1) ? (h << 16) : h;
+                                        } else {
+                                            wv[e] = lds32(xs[e] + uint32_t(ko[i]));
+                                        }
+                                    }
+                                }
+                            }
+                            put_raw_unit<T, 1>(op, op + KTp * ROWB, uo[i], make_uint4(wv[0], wv[1], wv[2], wv[3]));
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(smem_u32(&bars->b_full[bp.i]));
+                        mbar_arrive(smem_u32(&bars->raw_empty[rp.i]));
+                    }
+                    bp.next(geo.nbs);
+                                }
+                if (!ok || !epilogue(ti, t)) break;
+            }
+        }
+    }
+    grid_dep_launch();  // the split reduction may be scheduled now (it waits for this grid)
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// Bias partial channel sums per split: one per G warp of a TMEM lane quarter.
+template <typename T>
+__host__ __device__ inline int wgrad_bias_parts(const TcWgradGeom& g)
+{
+    return g.splits * (g.layout ? WgRolesGt<T>::g_warps / 4 : WgRoles<T>::g_warps / 4);
+}
+
+template <typename T, bool RELU>
 __global__ void __launch_bounds__(WG_THREADS, 1)
 wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict__ dy,
                 const T* __restrict__ y, float* __restrict__ ws, float* __restrict__ bpart, const TcWgradGeom geo)
 {
-    wgrad_tc_body<T, RELU>(p, x, dy, y, ws, bpart, geo, int(blockIdx.x), int(gridDim.x));
+    if (geo.layout) wgrad_tc_body_gt<T, RELU>(p, x, dy, y, ws, bpart, geo, int(blockIdx.x), int(gridDim.x));
+    else wgrad_tc_body<T, RELU>(p, x, dy, y, ws, bpart, geo, int(blockIdx.x), int(gridDim.x));
 }
 
 // ======================================================================================
@@ -2204,9 +2711,10 @@ bwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict__
               float* __restrict__ ws, float* __restrict__ bpart, const TcDgradGeom dgeo, const TcWgradGeom wgeo,
               const int n_wg)
 {
-    if (int(blockIdx.x) < n_wg)
-        wgrad_tc_body<T, RELU>(p, x, dy, y, ws, bpart, wgeo, int(blockIdx.x), n_wg);
-    else
+    if (int(blockIdx.x) < n_wg) {
+        if (wgeo.layout) wgrad_tc_body_gt<T, RELU>(p, x, dy, y, ws, bpart, wgeo, int(blockIdx.x), n_wg);
+        else wgrad_tc_body<T, RELU>(p, x, dy, y, ws, bpart, wgeo, int(blockIdx.x), n_wg);
+    } else
         dgrad_tc_body<T, RELU>(p, dy, w, wpack, y, dx, dgeo, int(blockIdx.x) - n_wg, int(gridDim.x) - n_wg);
 }
 
@@ -2831,19 +3339,33 @@ cudaError_t run_fwd_tc(const Plan& pl, const ConvParams& p, int dt, const void* 
 }
 
 // ---- wgrad ------------------------------------------------------------------------------
-// k rows per tile: the largest the accumulator allows (128 for fp32 hi + lo, 256 for
-// bf16), shrunk to K*K*IC rounded up to 32; splits: enough tiles to cover the SMs, at least two
-// chunks per split; then the deepest raw / B rings that fit.
+// Layout: the patches in tensor memory (k-tiles of at most 128 rows, the TMEM lanes) except
+// for bf16 from WG_GT_MIN_B samples on, which keeps g in tensor memory and the patches in
+// shared memory with k-tiles of up to 256 rows: per k row it formats g half as often, which
+// decides at large batches (layer 1 bf16 at B = 16384: 305 against 401 us; at B = 1024 both
+// 42.7 us; layer 2 bf16 at B = 1024 26.4 against 34.6 us for the patches-in-TMEM layout).
+// k rows per tile: the most the layout allows, shrunk to K*K*IC rounded up to 32; splits:
+// enough tiles to cover the SMs, at least two chunks per split; then the deepest raw / B rings
+// that fit.
+constexpr int WG_GT_MIN_B = 2048;
+
 template <typename T>
 static bool pick_wgrad(const ConvParams& p, const DevInfo& d, TcWgradGeom& out)
 {
     using Tr = TcTraits<T>;
     if (p.P > Tr::KC || p.B <= 0 || p.OC > TC_M) return false;  // one dy range of all OC per chunk
-    const int ktp = std::min(TC_M, round_up(p.Kred, 32));  // k rows per tile: the TMEM lanes
+    const int layout = (!Tr::split && p.B >= WG_GT_MIN_B) ? 1 : 0;
+    const int ktp = std::min(layout ? 256 : TC_M, round_up(p.Kred, 32));
     const int cnp = round_up(wgrad_nsc(p.P, Tr::KC, Tr::KC / 4) * p.P, Tr::KC / 4);
     const int ng = Tr::split ? 8 : 16;  // columns per G / X group
-    if (ceil_div(cnp / ng, WgRoles<T>::g_warps / 4) > WgRoles<T>::g_groups) return false;
-    if (ceil_div(cnp / ng, (16 - WgRoles<T>::g_warps) / 4) > WgRoles<T>::x_groups) return false;
+    if (layout) {
+        const int upr = cnp / Tr::E;
+        if (ceil_div(ktp, 32 * (16 - WgRolesGt<T>::g_warps) / upr) > WgRolesGt<T>::x_rows) return false;
+        if (ceil_div(cnp / ng, WgRolesGt<T>::g_warps / 4) > WgRolesGt<T>::g_groups) return false;
+    } else {
+        if (ceil_div(cnp / ng, WgRoles<T>::g_warps / 4) > WgRoles<T>::g_groups) return false;
+        if (ceil_div(cnp / ng, (16 - WgRoles<T>::g_warps) / 4) > WgRoles<T>::x_groups) return false;
+    }
     const int tiles = ceil_div(p.Kred, ktp) * ceil_div(p.OC, TC_M);
     const int nsc = wgrad_nsc(p.P, Tr::KC, Tr::KC / 4);
     int splits = std::max(1, d.sms / tiles);
@@ -2852,7 +3374,7 @@ static bool pick_wgrad(const ConvParams& p, const DevInfo& d, TcWgradGeom& out)
     // so it gets the deeper ring; two B stages suffice.
     static const int cfgs[][2] = {{5, 2}, {4, 2}, {3, 3}, {3, 2}, {2, 2}};  // {raws, nbs}
     for (const auto& c : cfgs) {
-        const TcWgradGeom g = wgrad_geom<T>(p, ktp, c[0], c[1], splits);
+        const TcWgradGeom g = wgrad_geom<T>(p, ktp, c[0], c[1], splits, layout);
         if (g.na >= 2 && wgrad_smem<T>(g) <= d.smem_optin) {
             out = g;
             return true;
@@ -2886,7 +3408,7 @@ Plan plan_wgrad_tc(const ConvParams& p, int dt, const DevInfo& d)
     pl.smem = dt == DT_BF16 ? wgrad_smem<__nv_bfloat16>(g) : wgrad_smem<float>(g);
     pl.splits = g.splits;
     static_assert(WG_MAXR < 8 && WG_MAXB < 8, "wgrad plan: ring depths in 3 bits each");
-    pl.variant = (g.KTp * 8 + g.raws) * 8 + g.nbs;
+    pl.variant = ((g.KTp * 8 + g.raws) * 8 + g.nbs) * 2 + g.layout;
     pl.launches = 2;
     pl.grid = std::min(g.k_tiles * g.oc_tiles * g.splits, d.sms);
     // the split-K partials, then room for the bias gradient's partial channel sums (two G lane
@@ -2904,10 +3426,11 @@ static cudaError_t wgrad_tc_t(const Plan& pl, const ConvParams& p, const void* x
     float* bpart = db ? reinterpret_cast<float*>(static_cast<unsigned char*>(ws) +
                                                  size_t(pl.splits) * p.OC * kpad * sizeof(float))
                       : nullptr;
-    const int nbp = pl.splits * (WgRoles<T>::g_warps / 4);
+    int nbp = 0;
     if (pl.splits > 0) {
-        const int v = pl.variant;
-        const TcWgradGeom g = wgrad_geom<T>(p, v / 64, (v / 8) % 8, v % 8, pl.splits);
+        const int v = pl.variant / 2;
+        const TcWgradGeom g = wgrad_geom<T>(p, v / 64, (v / 8) % 8, v % 8, pl.splits, pl.variant % 2);
+        nbp = wgrad_bias_parts<T>(g);
 #define IG_LAUNCH_WG_TC(R)                                                                                 \
     do {                                                                                                   \
         e = ensure_smem<wgrad_tc_kernel<T, R>>(pl.smem);                                                   \
@@ -3039,7 +3562,7 @@ static bool pick_bwd(const ConvParams& p, const DevInfo& d, TcDgradGeom& dg, TcW
     if (dg.ntiles * dg.ktsplit >= 2 * d.sms) return false;
     const int tiles = wg.k_tiles * wg.oc_tiles;
     const int splits = std::min(std::max(1, (2 * d.sms / 3 + tiles / 2) / tiles), std::max(1, p.B / (2 * wg.nsc)));
-    wg = wgrad_geom<T>(p, wg.KTp, wg.raws, wg.nbs, splits);
+    wg = wgrad_geom<T>(p, wg.KTp, wg.raws, wg.nbs, splits, wg.layout);
     const int ranges = 4 * dg.ntiles < d.sms ? 3 : 2;
     dg.kt_per = ceil_div(dg.nkt, std::min(dg.nkt, ranges));
     dg.ktsplit = ceil_div(dg.nkt, dg.kt_per);
@@ -3114,7 +3637,7 @@ static cudaError_t bwd_tc_t(const Plan& pl, const ConvParams& p, const DevInfo& 
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return run_wgrad_reduce(p, dt_of_tc<T>(), part, wg.splits, wg.kpad, dw, s, true, bpart,
-                            wg.splits * (WgRoles<T>::g_warps / 4), db);
+                            wgrad_bias_parts<T>(wg), db);
 }
 
 cudaError_t run_bwd_tc(const Plan& pl, const ConvParams& p, int dt, const DevInfo& d, const void* x, const void* dy,

@@ -207,6 +207,29 @@ def test_tc_wgrad(shape, B, dtype):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("B", [2048, 2051])
+@pytest.mark.parametrize("shape", list(SHAPES))
+def test_tc_wgrad_large_batch(shape, B, dtype):
+    """From 2048 samples bf16 wgrad keeps g in tensor memory and the patches in shared memory
+    (k-tiles of up to 256 rows); fp32 keeps the patches in tensor memory.  Both against the
+    oracle, a full and a ragged last chunk, and run to run bit identity."""
+    binding.conv_set_algo(binding.OP_BWD_FILTER, binding.ALGO_TC)
+    c = Case(B, **SHAPES[shape], dtype=dtype)
+    try:
+        binding.conv_query(binding.OP_BWD_FILTER, c.desc)
+    except binding.ConvError:
+        pytest.skip("shape outside the tensor-core wgrad kernel's limits")
+    y = c.gpu_fwd()
+    dw = c.gpu_wgrad(y)
+    dw2 = c.gpu_wgrad(y)
+    torch.cuda.synchronize()
+    assert binding.conv_device_status(reset=True) == 0
+    ref, den = c.ref_wgrad(to_np(y))
+    check(to_np(dw), ref, den, dtype, f"tc wgrad {shape} B={B} {dtype}")
+    assert torch.equal(_bits(dw), _bits(dw2))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("B", [3, 200, 1024])
 @pytest.mark.parametrize("shape", list(SHAPES))
 def test_tc_dgrad(shape, B, dtype):

@@ -187,3 +187,17 @@ def test_device_properties_checked():
     for bad in (dict(GB300, sms=0), dict(GB300, smem_optin=0), dict(GB300, cc_major=0), dict(GB300, cc_minor=-1)):
         with pytest.raises(binding.ConvError):
             binding.conv_query_for_device(binding.OP_FWD, d, **bad)
+
+
+def test_wgrad_k_tile_rows_per_dtype_and_batch():
+    # fp32 and small-batch bf16 keep the patches in tensor memory (k-tiles of 128 rows, the TMEM
+    # lanes); bf16 from 2048 samples keeps g there instead and takes k-tiles of 256 rows
+    for name in ("L1", "L2"):
+        IC, OC, H, W, K, S, relu = SHAPES[name]
+        kred = IC * K * K
+        for dtype in (binding.F32, binding.BF16):
+            for B in (37, 1024, 2047, 2048, 4096, 16384):
+                w = plan(binding.OP_BWD_FILTER, B, SHAPES[name], dtype)
+                rows = 256 if (dtype == binding.BF16 and B >= 2048) else 128
+                want = -(-kred // min(rows, -(-kred // 32) * 32)) * -(-OC // 128)
+                assert w["algo"] == binding.ALGO_TC and w["grid"] == want * w["splits"], (name, dtype, B, w)
