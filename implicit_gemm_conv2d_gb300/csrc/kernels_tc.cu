@@ -2129,12 +2129,13 @@ __host__ __device__ inline int wgrad_bias_parts(const TcWgradGeom& g)
     return g.splits * (g.layout ? WgRolesGt<T>::g_warps / 4 : WgRoles<T>::g_warps / 4);
 }
 
-template <typename T, bool RELU>
+// One kernel per operand layout (GT: g in tensor memory), so that each holds one body.
+template <typename T, bool RELU, bool GT>
 __global__ void __launch_bounds__(WG_THREADS, 1)
 wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict__ dy,
                 const T* __restrict__ y, float* __restrict__ ws, float* __restrict__ bpart, const TcWgradGeom geo)
 {
-    if (geo.layout) wgrad_tc_body_gt<T, RELU>(p, x, dy, y, ws, bpart, geo, int(blockIdx.x), int(gridDim.x));
+    if constexpr (GT) wgrad_tc_body_gt<T, RELU>(p, x, dy, y, ws, bpart, geo, int(blockIdx.x), int(gridDim.x));
     else wgrad_tc_body<T, RELU>(p, x, dy, y, ws, bpart, geo, int(blockIdx.x), int(gridDim.x));
 }
 
@@ -2147,9 +2148,10 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
 // once per sample tile; the W^T tiles are the shared-memory B operand, formatted in the
 // kernel from w.
 // Warp roles (608 threads):
-//   warp 0      MMA: per k-tile, the oc-chunk MMAs into an accumulator buffer, then a
-//               commit to that buffer's barrier (two buffers for bf16: the MMAs of k-tile
-//               kt+1 run while k-tile kt is read out).
+//   warp 0      MMA: per k-tile, the oc-chunk MMAs into an accumulator buffer of KTp columns
+//               (fp32: hi*hi, hi*lo and lo*hi into the same one), then a commit to that
+//               buffer's barrier (two buffers: the MMAs of k-tile kt+1 run while k-tile kt is
+//               read out).
 //   warps 1-2   weight formatters: the W^T tiles (kt, oc chunk) from w into a ring of
 //               stages (stage_wt_dgrad, format_wt_dgrad).
 //   warps 3-18  formatters: per sample tile, load dy (and y) of their lane's column and
@@ -2176,7 +2178,8 @@ struct TcDgradGeom {
     int taps;        // max (kh, kw) taps landing on one input pixel
     int nw;          // weight ring stages
     int w_tile;      // bytes of one packed tile: KTp rows x 128 (x2 for split fp32)
-    int dcols;       // accumulator columns per buffer: KTp (x2 for split fp32)
+    int dcols;       // accumulator columns per buffer: KTp
+    int dstr;        // Ds row stride in floats (see dgrad_ds_stride)
     int ndb;         // accumulator buffers
     int acol0;       // first TMEM column of the G buffers
     int acols;       // TMEM columns of one G buffer
@@ -2194,6 +2197,77 @@ struct DgBars {
     int abort_flag;
 };
 
+constexpr int DG_TMAX = 4;          // taps per input pixel handled by the fast gather
+constexpr int DG_PROW = 8;          // ints per pixel row of the tap table (32 bytes, int4-aligned)
+
+// Shared-memory wavefronts of the fast col2im gather's first pass for Ds row stride `dstr`:
+// thread it handles pixel it % HW of sample it / HW (channel 0; later samples and channels
+// shift every address of a warp alike), one 4-byte load per tap the pixel has.
+inline int dgrad_gather_wavefronts(const ConvParams& p, int NS, int dstr)
+{
+    const int nsplit = std::max(1, 512 / p.HW);
+    const int items = p.HW * std::min(nsplit, NS);
+    int total = 0;
+    for (int w0 = 0; w0 < items; w0 += 32) {
+        for (int t = 0; t < DG_TMAX; ++t) {
+            int word[32], n = 0, bank_words[32] = {0};
+            for (int it = w0; it < std::min(items, w0 + 32); ++it) {
+                const int hw = it % p.HW, sI = it / p.HW, h = hw / p.W, c = hw % p.W;
+                int k = 0, found = -1;
+                for (int oh = 0; oh < p.OH && found < 0; ++oh) {
+                    const int kh = h - oh * p.S;
+                    if (kh < 0 || kh >= p.K) continue;
+                    for (int ow = 0; ow < p.OW; ++ow) {
+                        const int kw = c - ow * p.S;
+                        if (kw < 0 || kw >= p.K) continue;
+                        if (k++ == t) {
+                            found = (sI * p.P + oh * p.OW + ow) * dstr + kh * p.K + kw;
+                            break;
+                        }
+                    }
+                }
+                if (found < 0) continue;
+                bool seen = false;
+                for (int i = 0; i < n && !seen; ++i) seen = word[i] == found;
+                if (!seen) {
+                    word[n++] = found;
+                    ++bank_words[found & 31];
+                }
+            }
+            int wf = 0;
+            for (int b = 0; b < 32; ++b) wf = std::max(wf, bank_words[b]);
+            total += wf;
+        }
+    }
+    return total;
+}
+
+// Ds row stride: DG_TM + 4 + 8i floats (i < 4), each an odd number of 16-byte units so that
+// the 16-byte stores of eight consecutive rows hit eight different bank groups; of these, the
+// one whose gather loads need the fewest wavefronts (layer 1, 11x15 with K=5, S=3: 148 floats,
+// about 28 % fewer than at 132).  Remembered per shape (per thread).
+inline int dgrad_ds_stride(const ConvParams& p, int NS)
+{
+    struct Entry { int H, W, K, S, NS, dstr; };
+    constexpr int NCACHE = 64;
+    static thread_local Entry cache[NCACHE];
+    static thread_local int next = 0;
+    for (const Entry& e : cache)
+        if (e.H == p.H && e.W == p.W && e.K == p.K && e.S == p.S && e.NS == NS && e.dstr > 0) return e.dstr;
+    int best = DG_TM + 4, best_cost = INT_MAX;
+    for (int i = 0; i < 4; ++i) {
+        const int dstr = DG_TM + 4 + 8 * i;
+        const int cost = dgrad_gather_wavefronts(p, NS, dstr);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = dstr;
+        }
+    }
+    cache[next] = Entry{p.H, p.W, p.K, p.S, NS, best};
+    next = (next + 1) % NCACHE;
+    return best;
+}
+
 template <typename T>
 inline TcDgradGeom dgrad_geom(const ConvParams& p, int CIC, int nw)
 {
@@ -2207,7 +2281,7 @@ inline TcDgradGeom dgrad_geom(const ConvParams& p, int CIC, int nw)
     g.rmax = (p.K + p.S - 1) / p.S;
     g.nw = nw;
     g.w_tile = g.KTp * ROWB * (Tr::split ? 2 : 1);
-    g.dcols = g.KTp * (Tr::split ? 2 : 1);
+    g.dcols = g.KTp;
     g.acols = Tr::split ? 2 * g.nch * Tr::KC : g.nch * Tr::KC / 2;
     // Two accumulator and two G buffers when they fit in the 512 TMEM columns.
     g.ndb = 2;
@@ -2229,12 +2303,9 @@ inline TcDgradGeom dgrad_geom(const ConvParams& p, int CIC, int nw)
         return m;
     };
     g.taps = axis_max(p.H, p.K, p.S, p.OH) * axis_max(p.W, p.K, p.S, p.OW);
+    g.dstr = g.taps <= DG_TMAX ? dgrad_ds_stride(p, g.NS) : DG_TM + 4;
     return g;
 }
-
-constexpr int DG_DSTR = DG_TM + 4;  // Ds row stride (floats): 16-byte rows, 4 banks apart
-constexpr int DG_TMAX = 4;          // taps per input pixel handled by the fast gather
-constexpr int DG_PROW = 8;          // ints per pixel row of the tap table (32 bytes, int4-aligned)
 
 // Raw w slots of the weight formatters (none on the workspace path).
 template <typename T>
@@ -2246,12 +2317,26 @@ inline __host__ __device__ int dgrad_wraw_bytes(const TcDgradGeom& g)
 template <typename T>
 inline int dgrad_smem(const ConvParams& p, const TcDgradGeom& g)
 {
-    return 1024 + g.nw * g.w_tile + dgrad_wraw_bytes<T>(g) + DG_TM * DG_DSTR * 4 + 16 + (p.H + p.W) * (1 + g.rmax) * 8 +
+    return 1024 + g.nw * g.w_tile + dgrad_wraw_bytes<T>(g) + DG_TM * (g.dstr + 1) * 4 + (p.H + p.W) * (1 + g.rmax) * 8 +
            16 + p.HW * DG_PROW * 4 + int(sizeof(DgBars)) + 16;
 }
 
+// Compile-time constants of the col2im gather (K*K, H*W, CIC; 0: read from the parameters).
+// SH = 1: 11x15 input, K = 5, S = 3, CIC = 5 for 128-row k-tiles -- layer 1 of the PufferLib
+// PR #522 encoder, where the gather sets the pace (B = 1024: fp32 51.9 -> 49.9 us, bf16 45.8 ->
+// 41.8 us).  Its layer 2 (two k-tiles per sample tile, bound by building G) gains nothing from it.
+template <int SH> struct DgShape { static constexpr int KK = 0, HW = 0, CIC = 0; };
+template <> struct DgShape<1> { static constexpr int KK = 25, HW = 165, CIC = 5; };
+
+inline int dgrad_shape(const ConvParams& p, const TcDgradGeom& g)
+{
+    if (g.taps > DG_TMAX) return 0;
+    if (p.KK == DgShape<1>::KK && p.HW == DgShape<1>::HW && g.CIC == DgShape<1>::CIC) return 1;
+    return 0;
+}
+
 // The d_input CTA's work: work items item0, item0 + istride, ... (see wgrad_tc_body).
-template <typename T, bool RELU>
+template <typename T, bool RELU, int SH>
 __device__ __forceinline__ void dgrad_tc_body(const ConvParams& p, const T* __restrict__ dy, const T* __restrict__ w,
                                               const unsigned char* __restrict__ wpack, const T* __restrict__ y,
                                               T* __restrict__ dx, const TcDgradGeom& geo, const int item0,
@@ -2265,7 +2350,8 @@ __device__ __forceinline__ void dgrad_tc_body(const ConvParams& p, const T* __re
     unsigned char* wraw = wring + geo.nw * geo.w_tile;
     float* Ds = reinterpret_cast<float*>(wraw + dgrad_wraw_bytes<T>(geo));
     const int R1 = 1 + geo.rmax;
-    int2* rtab = reinterpret_cast<int2*>(Ds + DG_TM * DG_DSTR + 4);  // 4 floats: the zero word
+    const int dstr = geo.dstr;
+    int2* rtab = reinterpret_cast<int2*>(Ds + DG_TM * dstr + DG_TM);  // after the zero row
     int2* ctab = rtab + p.H * R1;
     // Per input pixel hw: its contributing (p, kh*K + kw) as Ds offsets p*DSTR + kh*K + kw,
     // then the count (only used when every pixel has <= DG_TMAX taps).
@@ -2274,7 +2360,7 @@ __device__ __forceinline__ void dgrad_tc_body(const ConvParams& p, const T* __re
     volatile int* abort_flag = &bars->abort_flag;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (tid < 4) Ds[DG_TM * DG_DSTR + tid] = 0.f;
+    if (tid < DG_TM) Ds[DG_TM * dstr + tid] = 0.f;
     for (int h = tid; h < p.H; h += DG_THREADS) {
         int n = 0;
         for (int oh = 0; oh < p.OH; ++oh) {
@@ -2301,7 +2387,7 @@ __device__ __forceinline__ void dgrad_tc_body(const ConvParams& p, const T* __re
             int n = 0;
             for (int a = 1; a <= rr[0].x; ++a)
                 for (int bq = 1; bq <= cc[0].x; ++bq)
-                    ptab[hw * DG_PROW + n++] = (rr[a].x + cc[bq].x) * DG_DSTR + rr[a].y + cc[bq].y;
+                    ptab[hw * DG_PROW + n++] = (rr[a].x + cc[bq].x) * dstr + rr[a].y + cc[bq].y;
             for (int i = n; i < DG_TMAX; ++i) ptab[hw * DG_PROW + i] = -1;
             ptab[hw * DG_PROW + DG_TMAX] = n;
         }
@@ -2415,9 +2501,8 @@ __device__ __forceinline__ void dgrad_tc_body(const ConvParams& p, const T* __re
     } else if (warp == DG_MMA_WARP) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
-            const uint32_t idesc2 = instr_desc(Tr::fmt, DG_TM, geo.dcols);
             const uint32_t idesc1 = instr_desc(Tr::fmt, DG_TM, geo.KTp);
-            const uint32_t w_u32 = smem_u32(wring);
+            const uint32_t w_u32 = smem_u32(wring), lo_off = uint32_t(geo.KTp * ROWB);
             RingPos wp, abp, dbp;
             bool ok = true;
             for (int wi = item0; wi < nwork && ok && !*abort_flag; wi += istride, abp.next(geo.nab)) {
@@ -2451,8 +2536,11 @@ __device__ __forceinline__ void dgrad_tc_body(const ConvParams& p, const T* __re
                             const uint32_t first = (ch == 0 && j == 0) ? 0u : 1u;
                             const uint32_t col = uint32_t(ch * 32 + 8 * j);  // oc columns of this step
                             if constexpr (Tr::split) {
-                                mma_tf32_ta(acc, ga + col, bd, idesc2, first);                          // hi*[hi;lo]
-                                mma_tf32_ta(acc, ga + uint32_t(geo.nch * Tr::KC) + col, bd, idesc1, 1u);  // lo*hi
+                                const uint64_t bl = op_desc<1>(wa + lo_off + kstep_off<1>(j));
+                                const uint32_t glo = ga + uint32_t(geo.nch * Tr::KC) + col;
+                                mma_tf32_ta(acc, ga + col, bd, idesc1, first);  // hi*hi
+                                mma_tf32_ta(acc, ga + col, bl, idesc1, 1u);     // hi*lo
+                                mma_tf32_ta(acc, glo, bd, idesc1, 1u);          // lo*hi
                             } else {
                                 mma_f16_ta(acc, ga + col, bd, idesc1, first);
                             }
@@ -2480,16 +2568,16 @@ __device__ __forceinline__ void dgrad_tc_body(const ConvParams& p, const T* __re
         // G rows of sample tile `tile` into G buffer `ab`: dy (masked) of column m, channels
         // [sub*ocq, (sub+1)*ocq); zeros past the batch or past OC.
         auto build_g = [&](int tile, const RingPos& ab) -> bool {
-            if (ab.wrapped && !mbar_wait_or_abort(smem_u32(&bars->a_empty[ab.i]), ab.ph ^ 1u, abort_flag)) {
-                report(const_cast<int*>(abort_flag), 1u);
-                return false;
-            }
-            tc_fence_after();
             const int b0 = tile * geo.NS, ns = min(geo.NS, p.B - b0);
             const bool valid = m < ns * p.P;
             uint32_t si = 0, pq = 0;
             p.dm_P.divmod(uint32_t(valid ? m : 0), si, pq);
             const size_t base = (size_t(b0) + si) * p.OCP + pq;  // si = 0, pq = 0 for invalid lanes
+            if (ab.wrapped && !mbar_wait_or_abort(smem_u32(&bars->a_empty[ab.i]), ab.ph ^ 1u, abort_flag)) {
+                report(const_cast<int*>(abort_flag), 1u);
+                return false;
+            }
+            tc_fence_after();
             const uint32_t gcol = tmem + lane_bits + uint32_t(geo.acol0 + ab.i * geo.acols);
             // Batches of 16 channels: every load of a batch is issued before the first use.
             for (int o0 = sub * ocq; o0 < (sub + 1) * ocq; o0 += 16) {
@@ -2582,25 +2670,16 @@ __device__ __forceinline__ void dgrad_tc_body(const ConvParams& p, const T* __re
                 {
                     const uint32_t acc = tmem + lane_bits + uint32_t(dbp.i * geo.dcols);
                     const int kq = geo.KTp / 4, c0 = sub * kq;
-                    const uint32_t drow = ds_u32 + uint32_t((m * DG_DSTR + c0) * 4);
+                    const uint32_t drow = ds_u32 + uint32_t((m * dstr + c0) * 4);
                     for (int c = 0; c < kq; c += 16) {
                         const bool two = c + 8 < kq;
-                        uint32_t r[2][8], r2[2][8];
+                        uint32_t r[2][8];
                         tmem_ld8(acc + uint32_t(c0 + c), r[0]);
                         if (two) tmem_ld8(acc + uint32_t(c0 + c + 8), r[1]);
-                        if constexpr (Tr::split) {
-                            tmem_ld8(acc + uint32_t(geo.KTp + c0 + c), r2[0]);
-                            if (two) tmem_ld8(acc + uint32_t(geo.KTp + c0 + c + 8), r2[1]);
-                        }
                         tmem_ld_wait();
 #pragma unroll
                         for (int i = 0; i < 2; ++i) {
                             if (i == 1 && !two) break;
-                            if constexpr (Tr::split) {
-#pragma unroll
-                                for (int e = 0; e < 8; ++e)
-                                    r[i][e] = __float_as_uint(__uint_as_float(r[i][e]) + __uint_as_float(r2[i][e]));
-                            }
                             sts128(drow + uint32_t(4 * (c + 8 * i)), r[i][0], r[i][1], r[i][2], r[i][3]);
                             sts128(drow + uint32_t(4 * (c + 8 * i)) + 16, r[i][4], r[i][5], r[i][6], r[i][7]);
                         }
@@ -2616,34 +2695,48 @@ __device__ __forceinline__ void dgrad_tc_body(const ConvParams& p, const T* __re
                 const int ic0 = kt * geo.CIC, nic = min(geo.CIC, p.IC - ic0);
                 if (fast_taps) {
                     // Thread owns (pixel hw, a subset of the samples); its <= 4 tap offsets
-                    // stay in registers while it walks the chunk's channels.
-                    const int nsplit = max(1, DG_NFT / p.HW);
-                    for (int it = ft; it < p.HW * nsplit; it += DG_NFT) {
-                        const int hw = it % p.HW, part = it / p.HW;
+                    // stay in registers while it walks the k-tile's channels.  Absent taps read
+                    // the zero row past the Ds rows (as long as a k-tile's K*K*CIC words), so
+                    // every tap moves by one channel's K*K words.  For the shapes DgShape names,
+                    // K*K, H*W and CIC are constants: the channel loop unrolls with fixed load
+                    // and store offsets.
+                    constexpr int KKc = DgShape<SH>::KK, HWc = DgShape<SH>::HW, CICc = DgShape<SH>::CIC;
+                    const int KK = KKc ? KKc : p.KK, HW = HWc ? HWc : p.HW;
+                    const int nsplit = max(1, DG_NFT / HW);
+                    const uint32_t zrow = ds_u32 + uint32_t(DG_TM * dstr * 4);
+                    for (int it = ft; it < HW * nsplit; it += DG_NFT) {
+                        const int hw = it % HW, part = it / HW;
                         const int4 o = *reinterpret_cast<const int4*>(ptab + hw * DG_PROW);
-                        // Absent taps read the zero word kept past the Ds rows and do not move
-                        // with the channel; present ones step by one channel's K*K values.
-                        const uint32_t zero = ds_u32 + uint32_t(DG_TM * DG_DSTR * 4);
-                        const uint32_t kstep = uint32_t(p.KK * 4);
-                        const uint32_t d0 = o.x >= 0 ? kstep : 0u, d1 = o.y >= 0 ? kstep : 0u;
-                        const uint32_t d2 = o.z >= 0 ? kstep : 0u, d3 = o.w >= 0 ? kstep : 0u;
                         for (int sI = part; sI < ns; sI += nsplit) {
-                            T* dxs = dx + size_t(b0 + sI) * p.IHW + size_t(ic0) * p.HW + hw;
-                            const uint32_t ds = ds_u32 + uint32_t(sI * p.P * DG_DSTR * 4);
-                            uint32_t a0 = o.x >= 0 ? ds + uint32_t(o.x * 4) : zero;
-                            uint32_t a1 = o.y >= 0 ? ds + uint32_t(o.y * 4) : zero;
-                            uint32_t a2 = o.z >= 0 ? ds + uint32_t(o.z * 4) : zero;
-                            uint32_t a3 = o.w >= 0 ? ds + uint32_t(o.w * 4) : zero;
+                            T* dxs = dx + size_t(b0 + sI) * p.IHW + size_t(ic0) * HW + hw;
+                            const uint32_t ds = ds_u32 + uint32_t(sI * p.P * dstr * 4);
+                            uint32_t a0 = o.x >= 0 ? ds + uint32_t(o.x * 4) : zrow;
+                            uint32_t a1 = o.y >= 0 ? ds + uint32_t(o.y * 4) : zrow;
+                            uint32_t a2 = o.z >= 0 ? ds + uint32_t(o.z * 4) : zrow;
+                            uint32_t a3 = o.w >= 0 ? ds + uint32_t(o.w * 4) : zrow;
+                            if (CICc > 0 && nic == CICc) {
+#pragma unroll
+                                for (int icl = 0; icl < (CICc > 0 ? CICc : 1); ++icl) {
+                                    const uint32_t off = uint32_t(icl * KK * 4);
+                                    const float v0 = __uint_as_float(lds32(a0 + off));
+                                    const float v1 = __uint_as_float(lds32(a1 + off));
+                                    const float v2 = __uint_as_float(lds32(a2 + off));
+                                    const float v3 = __uint_as_float(lds32(a3 + off));
+                                    Elem<T>::st(dxs + icl * HW, ((v0 + v1) + v2) + v3);
+                                }
+                            } else {
+                                const uint32_t kstep = uint32_t(KK * 4);
 #pragma unroll 4
-                            for (int icl = 0; icl < nic; ++icl) {
-                                const float v0 = __uint_as_float(lds32(a0)), v1 = __uint_as_float(lds32(a1));
-                                const float v2 = __uint_as_float(lds32(a2)), v3 = __uint_as_float(lds32(a3));
-                                Elem<T>::st(dxs, ((v0 + v1) + v2) + v3);
-                                dxs += p.HW;
-                                a0 += d0;
-                                a1 += d1;
-                                a2 += d2;
-                                a3 += d3;
+                                for (int icl = 0; icl < nic; ++icl) {
+                                    const float v0 = __uint_as_float(lds32(a0)), v1 = __uint_as_float(lds32(a1));
+                                    const float v2 = __uint_as_float(lds32(a2)), v3 = __uint_as_float(lds32(a3));
+                                    Elem<T>::st(dxs, ((v0 + v1) + v2) + v3);
+                                    dxs += HW;
+                                    a0 += kstep;
+                                    a1 += kstep;
+                                    a2 += kstep;
+                                    a3 += kstep;
+                                }
                             }
                         }
                     }
@@ -2651,7 +2744,7 @@ __device__ __forceinline__ void dgrad_tc_body(const ConvParams& p, const T* __re
                     const int span = nic * p.HW;
                     for (int sI = 0; sI < ns; ++sI) {
                         T* dxs = dx + size_t(b0 + sI) * p.IHW + size_t(ic0) * p.HW;
-                        const float* ds = Ds + sI * p.P * DG_DSTR;
+                        const float* ds = Ds + sI * p.P * dstr;
                         for (int t = ft; t < span; t += DG_NFT) {
                             uint32_t icl, hw, h, ww;
                             p.dm_HW.divmod(uint32_t(t), icl, hw);
@@ -2663,7 +2756,7 @@ __device__ __forceinline__ void dgrad_tc_body(const ConvParams& p, const T* __re
                             float sum = 0.f;
                             for (int a = 1; a <= nr; ++a)
                                 for (int bq = 1; bq <= ncc; ++bq)
-                                    sum += ds[(rr[a].x + cc[bq].x) * DG_DSTR + kb + rr[a].y + cc[bq].y];
+                                    sum += ds[(rr[a].x + cc[bq].x) * dstr + kb + rr[a].y + cc[bq].y];
                             Elem<T>::st(dxs + t, sum);
                         }
                     }
@@ -2685,13 +2778,13 @@ __device__ __forceinline__ void dgrad_tc_body(const ConvParams& p, const T* __re
     }
 }
 
-template <typename T, bool RELU>
+template <typename T, bool RELU, int SH>
 __global__ void __launch_bounds__(DG_THREADS, 1)
 dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const T* __restrict__ w,
                 const unsigned char* __restrict__ wpack, const T* __restrict__ y, T* __restrict__ dx,
                 const TcDgradGeom geo)
 {
-    dgrad_tc_body<T, RELU>(p, dy, w, wpack, y, dx, geo, int(blockIdx.x), int(gridDim.x));
+    dgrad_tc_body<T, RELU, SH>(p, dy, w, wpack, y, dx, geo, int(blockIdx.x), int(gridDim.x));
 }
 
 // ======================================================================================
@@ -2704,7 +2797,7 @@ dgrad_tc_kernel(const ConvParams p, const T* __restrict__ dy, const T* __restric
 // ======================================================================================
 static_assert(DG_THREADS == WG_THREADS, "one block shape for both operations");
 
-template <typename T, bool RELU>
+template <typename T, bool RELU, bool GT, int SH>
 __global__ void __launch_bounds__(DG_THREADS, 1)
 bwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict__ dy, const T* __restrict__ w,
               const unsigned char* __restrict__ wpack, const T* __restrict__ y, T* __restrict__ dx,
@@ -2712,10 +2805,10 @@ bwd_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict__
               const int n_wg)
 {
     if (int(blockIdx.x) < n_wg) {
-        if (wgeo.layout) wgrad_tc_body_gt<T, RELU>(p, x, dy, y, ws, bpart, wgeo, int(blockIdx.x), n_wg);
+        if constexpr (GT) wgrad_tc_body_gt<T, RELU>(p, x, dy, y, ws, bpart, wgeo, int(blockIdx.x), n_wg);
         else wgrad_tc_body<T, RELU>(p, x, dy, y, ws, bpart, wgeo, int(blockIdx.x), n_wg);
     } else
-        dgrad_tc_body<T, RELU>(p, dy, w, wpack, y, dx, dgeo, int(blockIdx.x) - n_wg, int(gridDim.x) - n_wg);
+        dgrad_tc_body<T, RELU, SH>(p, dy, w, wpack, y, dx, dgeo, int(blockIdx.x) - n_wg, int(gridDim.x) - n_wg);
 }
 
 // ======================================================================================
@@ -3431,15 +3524,23 @@ static cudaError_t wgrad_tc_t(const Plan& pl, const ConvParams& p, const void* x
         const int v = pl.variant / 2;
         const TcWgradGeom g = wgrad_geom<T>(p, v / 64, (v / 8) % 8, v % 8, pl.splits, pl.variant % 2);
         nbp = wgrad_bias_parts<T>(g);
-#define IG_LAUNCH_WG_TC(R)                                                                                 \
+#define IG_LAUNCH_WG_TC(R, GT)                                                                             \
     do {                                                                                                   \
-        e = ensure_smem<wgrad_tc_kernel<T, R>>(pl.smem);                                                   \
+        e = ensure_smem<wgrad_tc_kernel<T, R, GT>>(pl.smem);                                               \
         if (e == cudaSuccess)                                                                              \
-            e = launch_ex(wgrad_tc_kernel<T, R>, dim3(pl.grid), dim3(pl.block), pl.smem, s, 1, true, p,       \
+            e = launch_ex(wgrad_tc_kernel<T, R, GT>, dim3(pl.grid), dim3(pl.block), pl.smem, s, 1, true, p,   \
                           (const T*)x, (const T*)dy, (const T*)y, (float*)ws, bpart, g);                   \
     } while (0)
-        if (p.relu) IG_LAUNCH_WG_TC(true);
-        else IG_LAUNCH_WG_TC(false);
+        if constexpr (!TcTraits<T>::split) {  // the g-in-TMEM layout is a bf16 plan only
+            if (g.layout) {
+                if (p.relu) IG_LAUNCH_WG_TC(true, true);
+                else IG_LAUNCH_WG_TC(false, true);
+            }
+        }
+        if (!g.layout) {
+            if (p.relu) IG_LAUNCH_WG_TC(true, false);
+            else IG_LAUNCH_WG_TC(false, false);
+        }
 #undef IG_LAUNCH_WG_TC
         if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -3522,15 +3623,19 @@ static cudaError_t dgrad_tc_t(const Plan& pl, const ConvParams& p, const void* d
         pack_dgrad_w_kernel<T><<<pgrid, 256, 0, s>>>(p, (const T*)w, (unsigned char*)ws, g.nch, g.CIC, g.KTp);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-#define IG_LAUNCH_DG_TC(R)                                                                                   \
+#define IG_LAUNCH_DG_TC(R, SH)                                                                               \
     do {                                                                                                     \
-        e = ensure_smem<dgrad_tc_kernel<T, R>>(pl.smem);                                                     \
+        e = ensure_smem<dgrad_tc_kernel<T, R, SH>>(pl.smem);                                                 \
         if (e == cudaSuccess)                                                                                \
-            e = launch_ex(dgrad_tc_kernel<T, R>, dim3(pl.grid), dim3(pl.block), pl.smem, s, 1, true, p,      \
+            e = launch_ex(dgrad_tc_kernel<T, R, SH>, dim3(pl.grid), dim3(pl.block), pl.smem, s, 1, true, p,  \
                           (const T*)dy, (const T*)w, (const unsigned char*)ws, (const T*)y, (T*)dx, g);      \
     } while (0)
-    if (p.relu) IG_LAUNCH_DG_TC(true);
-    else IG_LAUNCH_DG_TC(false);
+    switch (dgrad_shape(p, g) * 2 + (p.relu ? 1 : 0)) {
+    case 2: IG_LAUNCH_DG_TC(false, 1); break;
+    case 3: IG_LAUNCH_DG_TC(true, 1); break;
+    case 1: IG_LAUNCH_DG_TC(true, 0); break;
+    default: IG_LAUNCH_DG_TC(false, 0); break;
+    }
 #undef IG_LAUNCH_DG_TC
     return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -3623,16 +3728,32 @@ static cudaError_t bwd_tc_t(const Plan& pl, const ConvParams& p, const DevInfo& 
     pack_dgrad_w_kernel<T><<<pgrid, 256, 0, s>>>(p, (const T*)w, wsb, dg.nch, dg.CIC, dg.KTp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-#define IG_LAUNCH_BWD_TC(R)                                                                                  \
+#define IG_LAUNCH_BWD_TC(R, GT, SH)                                                                          \
     do {                                                                                                     \
-        e = ensure_smem<bwd_tc_kernel<T, R>>(pl.smem);                                                       \
+        e = ensure_smem<bwd_tc_kernel<T, R, GT, SH>>(pl.smem);                                               \
         if (e == cudaSuccess)                                                                                \
-            e = launch_ex(bwd_tc_kernel<T, R>, dim3(pl.grid), dim3(pl.block), pl.smem, s, 1, true, p,        \
-                          (const T*)x, (const T*)dy, (const T*)w, (const unsigned char*)wsb, (const T*)y,    \
+            e = launch_ex(bwd_tc_kernel<T, R, GT, SH>, dim3(pl.grid), dim3(pl.block), pl.smem, s, 1, true,   \
+                          p, (const T*)x, (const T*)dy, (const T*)w, (const unsigned char*)wsb, (const T*)y, \
                           (T*)dx, part, bpart, dg, wg, n_wg);                                                 \
     } while (0)
-    if (p.relu) IG_LAUNCH_BWD_TC(true);
-    else IG_LAUNCH_BWD_TC(false);
+#define IG_LAUNCH_BWD_SH(R, GT)                 \
+    do {                                        \
+        if (dgrad_shape(p, dg) == 1)            \
+            IG_LAUNCH_BWD_TC(R, GT, 1);         \
+        else                                    \
+            IG_LAUNCH_BWD_TC(R, GT, 0);         \
+    } while (0)
+    if constexpr (!TcTraits<T>::split) {
+        if (wg.layout) {
+            if (p.relu) IG_LAUNCH_BWD_SH(true, true);
+            else IG_LAUNCH_BWD_SH(false, true);
+        }
+    }
+    if (!wg.layout) {
+        if (p.relu) IG_LAUNCH_BWD_SH(true, false);
+        else IG_LAUNCH_BWD_SH(false, false);
+    }
+#undef IG_LAUNCH_BWD_SH
 #undef IG_LAUNCH_BWD_TC
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;

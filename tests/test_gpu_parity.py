@@ -26,6 +26,9 @@ SHAPES = {
     "k1_wide": dict(IC=160, OC=64, H=4, W=5, K=1, S=1, relu=True),
     "k_eq_input": dict(IC=7, OC=33, H=5, W=5, K=5, S=2, relu=True),
     "stride_gt_k": dict(IC=5, OC=20, H=10, W=11, K=2, S=3, relu=False),
+    # layer 1's input size, kernel and stride (the d_input gather compiled for them) without the
+    # ReLU, one full k-tile of 5 channels and a ragged one of 2
+    "l1_geometry_ic7": dict(IC=7, OC=16, H=11, W=15, K=5, S=3, relu=False),
 }
 
 
