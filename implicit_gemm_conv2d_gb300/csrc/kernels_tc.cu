@@ -2180,6 +2180,8 @@ struct TcDgradGeom {
     int w_tile;      // bytes of one packed tile: KTp rows x 128 (x2 for split fp32)
     int dcols;       // accumulator columns per buffer: KTp
     int dstr;        // Ds row stride in floats (see dgrad_ds_stride)
+    int grounds;     // channel blocks of the staged G build (0: not staged; see dgrad_tc_body)
+    int gstride;     // bytes per sample block of the staged dy (and y) in the Ds rows
     int ndb;         // accumulator buffers
     int acol0;       // first TMEM column of the G buffers
     int acols;       // TMEM columns of one G buffer
@@ -2193,6 +2195,7 @@ struct TcDgradGeom {
 struct DgBars {
     uint64_t w_full[DG_MAXW], w_empty[DG_MAXW], a_full[2], a_empty[2], acc_full[2], acc_empty[2];
     uint64_t fbar;  // formatter-warp barrier (Ds written / Ds read)
+    uint64_t gbar;  // staged G build: a channel block's bulk copies landed
     uint32_t tslot;
     int abort_flag;
 };
@@ -2268,6 +2271,40 @@ inline int dgrad_ds_stride(const ConvParams& p, int NS)
     return best;
 }
 
+// Byte stride of the sample blocks of the staged G build (a block: gch channels x P positions
+// of one sample, `bytes` long): `bytes` plus 0-28 pad words in steps of 16 bytes, at most
+// `max_st`, the one whose reads by the formatter warps (lane = column (sample, position), one
+// channel at a time) hit the fewest words per bank; 0 if none fits.
+inline int dgrad_stage_stride(int P, int es, int bytes, int max_st)
+{
+    int best = 0, best_cost = INT_MAX;
+    for (int pad = 0; pad < 32; pad += 4) {
+        const int st = bytes + 4 * pad;
+        if (st > max_st) break;
+        int cost = 0;
+        for (int w0 = 0; w0 < 128; w0 += 32) {
+            int word[32], n = 0, bank_words[32] = {0};
+            for (int l = w0; l < w0 + 32; ++l) {
+                const int wd = ((l / P) * st + (l % P) * es) / 4;
+                bool seen = false;
+                for (int i = 0; i < n && !seen; ++i) seen = word[i] == wd;
+                if (!seen) {
+                    word[n++] = wd;
+                    ++bank_words[wd & 31];
+                }
+            }
+            int wf = 0;
+            for (int b = 0; b < 32; ++b) wf = std::max(wf, bank_words[b]);
+            cost += wf;
+        }
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = st;
+        }
+    }
+    return best;
+}
+
 template <typename T>
 inline TcDgradGeom dgrad_geom(const ConvParams& p, int CIC, int nw)
 {
@@ -2304,6 +2341,25 @@ inline TcDgradGeom dgrad_geom(const ConvParams& p, int CIC, int nw)
     };
     g.taps = axis_max(p.H, p.K, p.S, p.OH) * axis_max(p.W, p.K, p.S, p.OW);
     g.dstr = g.taps <= DG_TMAX ? dgrad_ds_stride(p, g.NS) : DG_TM + 4;
+    // Staged G build, where a warp's 32 columns span 8 or more samples (P <= 4), so that the
+    // strided loads of build_g touch a line per sample for a few bytes each (layer 2 of the
+    // PufferLib PR #522 encoder, P = 2, B = 1024: d_input 23.4 -> 21.3 us fp32, 21.1 -> 19.1 us
+    // bf16; layer 1, P = 12, gained nothing in fp32 and lost 2 us in bf16): the fewest channel
+    // blocks (up to 4) whose dy (and y) slabs for a whole sample tile fit in the Ds rows, each
+    // block a whole number of 16-channel groups per formatter quarter, every slab a run of whole
+    // 16-byte units.
+    g.grounds = 0;
+    g.gstride = 0;
+    const int es = int(sizeof(T));
+    for (int r = 1; r <= 4 && g.grounds == 0 && p.P <= 4 && p.OC == g.nch * Tr::KC; ++r) {
+        if (p.OC % (64 * r) != 0) continue;
+        const int bytes = p.OC / r * p.P * es;
+        if (bytes % 16 != 0 || (p.OCP * es) % 16 != 0) continue;
+        const int st = dgrad_stage_stride(p.P, es, bytes, DG_TM * g.dstr * 4 / (g.NS * (p.relu ? 2 : 1)));
+        if (st == 0) continue;
+        g.grounds = r;
+        g.gstride = st;
+    }
     return g;
 }
 
@@ -2343,6 +2399,7 @@ __device__ __forceinline__ void dgrad_tc_body(const ConvParams& p, const T* __re
                                               const int istride)
 {
     using Tr = TcTraits<T>;
+    constexpr int ES = int(sizeof(T));
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = align1024(smem_raw);
     // Layout: weight stages | raw w slots (DG_NWF warps x WRAW) | Ds | row, column, pixel tap tables | barriers
@@ -2404,6 +2461,7 @@ __device__ __forceinline__ void dgrad_tc_body(const ConvParams& p, const T* __re
             mbar_init(smem_u32(&bars->acc_empty[i]), DG_FMTW);
         }
         mbar_init(smem_u32(&bars->fbar), DG_FMTW);
+        mbar_init(smem_u32(&bars->gbar), 1);
         fence_mbar_init();
         bars->abort_flag = 0;
     }
@@ -2565,6 +2623,103 @@ __device__ __forceinline__ void dgrad_tc_body(const ConvParams& p, const T* __re
         const int m = qd * 32 + lane;       // column within the tile
         const uint32_t lane_bits = uint32_t(qd * 32) << 16;
         const int ocq = geo.nch * Tr::KC / 4;  // output channels per formatter warp
+        // Barrier of the 16 formatter warps (bounded wait, unlike bar.sync).
+        uint32_t fph = 0;
+        auto fmt_sync = [&]() -> bool {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->fbar));
+            const bool done = mbar_wait_or_abort(smem_u32(&bars->fbar), fph, abort_flag);
+            fph ^= 1u;
+            if (!done) report(const_cast<int*>(abort_flag), 2u);
+            return done;
+        };
+        // G values of channels [o0, o0 + nb) (nb = 8 or 16) of this thread's column into the G
+        // buffer at TMEM column gcol: tf32 hi and lo parts (fp32) or bf16 pairs.
+        auto store_g16 = [&](uint32_t gcol, int o0, int nb, const float* v) {
+            if constexpr (Tr::split) {
+#pragma unroll
+                for (int g8 = 0; g8 < 2; ++g8) {
+                    if (8 * g8 >= nb) break;
+                    uint32_t hi[8], lo[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float f = v[8 * g8 + e];
+                        const float h = to_tf32(f);
+                        hi[e] = __float_as_uint(h);
+                        lo[e] = __float_as_uint(f - h);
+                    }
+                    tmem_st8(gcol + uint32_t(o0 + 8 * g8), hi);
+                    tmem_st8(gcol + uint32_t(geo.nch * Tr::KC + o0 + 8 * g8), lo);
+                }
+            } else {
+                uint32_t wv[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    wv[e] = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(v[2 * e]))) |
+                            (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(v[2 * e + 1]))) << 16);
+                tmem_st8(gcol + uint32_t(o0 / 2), wv);
+            }
+        };
+        // Staged build of the CTA's first sample tile (the Ds rows are not in use yet): per
+        // block of gch = OC / grounds channels, formatter warp 0 bulk-copies each sample's
+        // contiguous dy (and y) slab of the block into the Ds rows (sample blocks gstride bytes
+        // apart, the y slabs after the dy slabs), and every formatter thread reads its column's
+        // gch / 4 channels from there.  The same values as build_g, in whole-tile copies
+        // instead of strided 4-byte loads.
+        uint32_t gph = 0;
+        auto build_g_staged = [&](int tile, const RingPos& ab) -> bool {
+            tc_fence_after();
+            const int b0 = tile * geo.NS, ns = min(geo.NS, p.B - b0);
+            const bool valid = m < ns * p.P;
+            uint32_t si = 0, pq = 0;
+            p.dm_P.divmod(uint32_t(valid ? m : 0), si, pq);
+            const int gch = p.OC / geo.grounds, gq = gch / 4;
+            const int bytes = gch * p.P * ES;
+            const uint32_t ybase = ds_u32 + uint32_t(ns * geo.gstride);
+            const uint32_t mine = uint32_t(int(si) * geo.gstride + int(pq) * ES);
+            const uint32_t gcol = tmem + lane_bits + uint32_t(geo.acol0 + ab.i * geo.acols);
+            const uint32_t gbar = smem_u32(&bars->gbar);
+            for (int r = 0; r < geo.grounds; ++r) {
+                if (ft < 32) {
+                    if (ft == 0) mbar_arrive_expect_tx(gbar, uint32_t(ns * bytes * (RELU ? 2 : 1)));
+                    __syncwarp();
+                    for (int sI = ft; sI < ns; sI += 32) {
+                        const size_t e0 = size_t(b0 + sI) * p.OCP + size_t(r) * gch * p.P;
+                        bulk_g2s(ds_u32 + uint32_t(sI * geo.gstride), dy + e0, uint32_t(bytes), gbar);
+                        if (RELU) bulk_g2s(ybase + uint32_t(sI * geo.gstride), y + e0, uint32_t(bytes), gbar);
+                    }
+                }
+                if (!mbar_wait_or_abort(gbar, gph, abort_flag)) {
+                    report(const_cast<int*>(abort_flag), 1u);
+                    return false;
+                }
+                gph ^= 1u;
+                for (int c0 = sub * gq; c0 < (sub + 1) * gq; c0 += 16) {
+                    float v[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const uint32_t a = mine + uint32_t((c0 + e) * p.P * ES);
+                        float d = 0.f;
+                        if (valid) {
+                            d = ES == 4 ? __uint_as_float(lds32(ds_u32 + a)) : __uint_as_float(lds16(ds_u32 + a) << 16);
+                            if (RELU) {
+                                const float yv = ES == 4 ? __uint_as_float(lds32(ybase + a))
+                                                         : __uint_as_float(lds16(ybase + a) << 16);
+                                if (!(yv > 0.f)) d = 0.f;
+                            }
+                        }
+                        v[e] = d;
+                    }
+                    store_g16(gcol, r * gch + c0, 16, v);
+                }
+                if (!fmt_sync()) return false;  // the block's slabs are consumed
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->a_full[ab.i]));
+            return true;
+        };
         // G rows of sample tile `tile` into G buffer `ab`: dy (masked) of column m, channels
         // [sub*ocq, (sub+1)*ocq); zeros past the batch or past OC.
         auto build_g = [&](int tile, const RingPos& ab) -> bool {
@@ -2599,33 +2754,7 @@ __device__ __forceinline__ void dgrad_tc_body(const ConvParams& p, const T* __re
                     if (RELU) keep = keep && yv[e] > 0.f;
                     if (!keep) v[e] = 0.f;
                 }
-                const int nb = min(16, (sub + 1) * ocq - o0);  // multiple of 8 (fp32) / 16 (bf16)
-                if constexpr (Tr::split) {
-#pragma unroll
-                    for (int g8 = 0; g8 < 2; ++g8) {
-                        if (8 * g8 >= nb) break;
-                        uint32_t hi[8], lo[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const float f = v[8 * g8 + e];
-                            const float h = to_tf32(f);
-                            hi[e] = __float_as_uint(h);
-                            lo[e] = __float_as_uint(f - h);
-                        }
-                        tmem_st8(gcol + uint32_t(o0 + 8 * g8), hi);
-                        tmem_st8(gcol + uint32_t(geo.nch * Tr::KC + o0 + 8 * g8), lo);
-                    }
-                } else {
-#pragma unroll
-                    for (int g16 = 0; g16 < 1; ++g16) {
-                        uint32_t wv[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            wv[e] = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(v[16 * g16 + 2 * e]))) |
-                                    (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(v[16 * g16 + 2 * e + 1]))) << 16);
-                        tmem_st8(gcol + uint32_t((o0 + 16 * g16) / 2), wv);
-                    }
-                }
+                store_g16(gcol, o0, min(16, (sub + 1) * ocq - o0), v);  // multiple of 8 (fp32) / 16 (bf16)
             }
             tmem_st_wait();
             tc_fence_before();
@@ -2633,20 +2762,16 @@ __device__ __forceinline__ void dgrad_tc_body(const ConvParams& p, const T* __re
             if (lane == 0) mbar_arrive(smem_u32(&bars->a_full[ab.i]));
             return true;
         };
-        // Barrier of the 16 formatter warps (bounded wait, unlike bar.sync).
-        uint32_t fph = 0;
-        auto fmt_sync = [&]() -> bool {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&bars->fbar));
-            const bool done = mbar_wait_or_abort(smem_u32(&bars->fbar), fph, abort_flag);
-            fph ^= 1u;
-            if (!done) report(const_cast<int*>(abort_flag), 2u);
-            return done;
-        };
         RingPos abp, dbp;
         bool ok = true;
         const int first = item0;
-        if (first < nwork) ok = build_g(first % geo.ntiles, abp);
+        // (Staging needs P <= 4: not compiled into the instances for a named shape.)
+        const bool staged = SH == 0 && geo.grounds > 0 &&
+                            ((reinterpret_cast<uintptr_t>(dy) | (RELU ? reinterpret_cast<uintptr_t>(y) : 0)) & 15) == 0;
+        if (first < nwork) {
+            if constexpr (SH == 0) ok = staged ? build_g_staged(first % geo.ntiles, abp) : build_g(first % geo.ntiles, abp);
+            else ok = build_g(first % geo.ntiles, abp);
+        }
         for (int wi = first; wi < nwork && ok; wi += istride) {
             const int tile = wi % geo.ntiles;
             int kt_lo, kt_hi;

@@ -17,7 +17,8 @@ from .gpu_cases import L1, L2, TOL, Case, check, to_np
 pytestmark = pytest.mark.gpu
 
 SHAPES = {"L1": L1, "L2": L2, "odd": dict(IC=3, OC=5, H=7, W=9, K=2, S=2, relu=True),
-          "k_eq_input": dict(IC=7, OC=33, H=5, W=5, K=5, S=2, relu=True)}
+          "k_eq_input": dict(IC=7, OC=33, H=5, W=5, K=5, S=2, relu=True),
+          "p1_relu_oc64": dict(IC=16, OC=64, H=4, W=4, K=3, S=2, relu=True)}
 
 
 @pytest.fixture(autouse=True)
@@ -74,7 +75,7 @@ def test_fused_backward(layer, B, dtype):
         assert torch.equal(_bits(a), _bits(b))
 
 
-@pytest.mark.parametrize("shape", ["odd", "k_eq_input"])
+@pytest.mark.parametrize("shape", ["odd", "k_eq_input", "p1_relu_oc64"])
 def test_fused_backward_odd_shapes(shape):
     c = Case(5, **SHAPES[shape], dtype="f32")
     y = c.gpu_fwd()

@@ -29,6 +29,10 @@ SHAPES = {
     # layer 1's input size, kernel and stride (the d_input gather compiled for them) without the
     # ReLU, one full k-tile of 5 channels and a ragged one of 2
     "l1_geometry_ic7": dict(IC=7, OC=16, H=11, W=15, K=5, S=3, relu=False),
+    # one output position per sample and 64 channels: d_input stages dy and y (ReLU) of a sample
+    # tile through shared memory by bulk copies (128 samples per tile: B = 200 is one full tile
+    # and a ragged one)
+    "p1_relu_oc64": dict(IC=16, OC=64, H=4, W=4, K=3, S=2, relu=True),
 }
 
 
