@@ -2155,9 +2155,10 @@ wgrad_tc_kernel(const ConvParams p, const T* __restrict__ x, const T* __restrict
 //   warps 1-2   weight formatters: the W^T tiles (kt, oc chunk) from w into a ring of
 //               stages (stage_wt_dgrad, format_wt_dgrad).
 //   warps 3-18  formatters: per sample tile, load dy (and y) of their lane's column and
-//               a quarter of the output channels from global memory, mask, split (fp32)
-//               and store G to TMEM; per k-tile, TMEM -> Ds (fp32 [n][k] in shared
-//               memory), then the col2im gather into dx with all 512 threads.
+//               a quarter of the output channels from global memory (with P <= 4 the
+//               CTA's first tile from whole sample slabs bulk-copied into the Ds rows), mask,
+//               split (fp32) and store G to TMEM; per k-tile, TMEM -> Ds (fp32 [n][k] in
+//               shared memory), then the col2im gather into dx with all 512 threads.
 // ======================================================================================
 constexpr int DG_MMA_WARP = 0;
 constexpr int DG_WF0 = 1;                     // first weight-formatter warp
