@@ -761,7 +761,7 @@ _SIDE = []
 
 def graphed(fn):
     """Capture fn (a sequence of library calls) into a CUDA graph on a side stream, after
-    a warm-up call there (the library's per-stream scratch exists before capture)."""
+    a warm-up call there (kernel attributes and lazy module loading happen outside capture)."""
     import torch
     if not _SIDE:
         _SIDE.append(torch.cuda.Stream())
@@ -907,6 +907,52 @@ def chain_extras(flush_buf, device, batches=(256, 1024, 4096, 16384)):
     return out
 
 
+def chain_bwd_extras(flush_buf, device, batches=(256, 1024, 4096)):
+    """The encoder's two-layer backward (conv_bwd_chain2: layer 2's dx kept in the workspace and
+    fed to layer 1's backward) with and without layer 1's input gradient, against the two
+    layers' conv_bwd calls one after the other, cold L2."""
+    import torch
+    from implicit_gemm_conv2d_gb300 import binding
+    out = {}
+    s1, s2 = LAYERS["layer1"], LAYERS["layer2"]
+    for dt in ("f32", "bf16"):
+        tdt = torch.float32 if dt == "f32" else torch.bfloat16
+        for B in batches:
+            g = torch.Generator(device=device)
+            g.manual_seed(11)
+            x = torch.randn((B, s1["IC"], s1["H"], s1["W"]), generator=g, device=device).to(tdt)
+            w1 = ((torch.rand((s1["OC"], s1["IC"], s1["K"], s1["K"]), generator=g, device=device) * 2 - 1)
+                  / math.sqrt(s1["IC"] * s1["K"] ** 2)).to(tdt)
+            w2 = ((torch.rand((s2["OC"], s2["IC"], s2["K"], s2["K"]), generator=g, device=device) * 2 - 1)
+                  / math.sqrt(s2["IC"] * s2["K"] ** 2)).to(tdt)
+            dy2 = torch.randn((B, 128, 1, 2), generator=g, device=device).to(tdt)
+            d1 = binding.make_desc(B, *(s1[k] for k in ("IC", "OC", "H", "W", "K", "S", "relu")), tdt)
+            d2 = binding.make_desc(B, *(s2[k] for k in ("IC", "OC", "H", "W", "K", "S", "relu")), tdt)
+            y1 = torch.empty((B, 128, 3, 4), dtype=tdt, device=device)
+            y2 = torch.empty((B, 128, 1, 2), dtype=tdt, device=device)
+            binding.conv_fwd(d1, x, w1, y1)
+            binding.conv_fwd(d2, y1, w2, y2)
+            dx1, dx2 = torch.empty_like(x), torch.empty_like(y1)
+            dw1, dw2 = torch.empty_like(w1), torch.empty_like(w2)
+            wsc = torch.empty(max(16, binding.conv_bwd_chain2_workspace_size(d1, d2)), dtype=torch.uint8,
+                              device=device)
+            ws1 = torch.empty(max(16, binding.conv_bwd_workspace_size(d1)), dtype=torch.uint8, device=device)
+            ws2 = torch.empty(max(16, binding.conv_bwd_workspace_size(d2)), dtype=torch.uint8, device=device)
+            gc = graphed(lambda: binding.conv_bwd_chain2(d1, d2, x, w1, y1, w2, y2, dy2, dx1, dw1, None, dw2, None, wsc))
+            gn = graphed(lambda: binding.conv_bwd_chain2(d1, d2, x, w1, y1, w2, y2, dy2, None, dw1, None, dw2, None,
+                                                         wsc))
+
+            def two_calls():
+                binding.conv_bwd(d2, y1, dy2, w2, y2, dx2, dw2, None, ws2)
+                binding.conv_bwd(d1, x, dx2, w1, y1, dx1, dw1, None, ws1)
+            gu = graphed(two_calls)
+            tc, tn, tu = (time_graph(gg, flush_buf, 30, 3) * 1e3 for gg in (gc, gn, gu))
+            out[f"{dt}_B{B}"] = {"chain_us_cold_l2": tc, "chain_no_dx1_us_cold_l2": tn, "two_conv_bwd_us_cold_l2": tu}
+            del gc, gn, gu, x, y1, y2, dx1, dx2
+            torch.cuda.empty_cache()
+    return out
+
+
 SWEEP_BATCHES = (256, 1024, 4096, 16384)
 
 
@@ -1005,7 +1051,7 @@ def run_ours(args):
 
     flush_buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     if args.chain_only:
-        print(json.dumps({"chain_fwd": chain_extras(flush_buf, device)}))
+        print(json.dumps({"chain_fwd": chain_extras(flush_buf, device), "chain_bwd": chain_bwd_extras(flush_buf, device)}))
         return 0
     # Above 4096 samples the inputs are drawn on the device (host generation would take minutes).
     wl = Workload(args.layer, args.dtype, args.batch, device, on_device=args.batch > 4096)
@@ -1123,6 +1169,7 @@ def run_ours(args):
         line["configs_b%d" % args.batch] = others
         line["bias"] = bias_extras(wls, flush_buf, peaks, device)
         line["chain_fwd"] = chain_extras(flush_buf, device)
+        line["chain_bwd"] = chain_bwd_extras(flush_buf, device)
         line["batch_sweep"] = batch_sweep(flush_buf, sms, sm_mhz, peaks, device)
         if world == 1:
             line["cpu_baseline"] = cpu_baseline(LAYERS[args.layer], 128, 10.0)

@@ -55,7 +55,8 @@ EXPORTS = ["conv_fwd", "conv_bwd_data", "conv_bwd_filter_workspace_size", "conv_
            "conv_device_status", "conv_fwd_bias", "conv_bwd_bias",
            "conv_wait_selftest", "conv_query_for_device", "conv_fwd_workspace_size", "conv_fwd_ws",
            "conv_bwd_data_workspace_size", "conv_bwd_data_ws", "conv_bwd_filter_bias",
-           "conv_fwd_chain2_workspace_size", "conv_fwd_chain2", "conv_query_chain2", "conv_bwd_workspace_size",
+           "conv_fwd_chain2_workspace_size", "conv_fwd_chain2", "conv_query_chain2",
+           "conv_bwd_chain2_workspace_size", "conv_bwd_chain2", "conv_bwd_workspace_size",
            "conv_bwd"]
 STATUS_WAIT_SELFTEST = 1 << 30
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -108,6 +109,9 @@ def lib():
         L.conv_fwd_chain2_workspace_size.restype = sz
         L.conv_fwd_chain2.argtypes = [dp, dp] + [vp] * 8 + [sz, vp]
         L.conv_query_chain2.argtypes = [dp, dp, ctypes.POINTER(PlanInfo)]
+        L.conv_bwd_chain2_workspace_size.argtypes = [dp, dp]
+        L.conv_bwd_chain2_workspace_size.restype = sz
+        L.conv_bwd_chain2.argtypes = [dp, dp] + [vp] * 11 + [vp, sz, vp]
         L.conv_bwd_workspace_size.argtypes = [dp]
         L.conv_bwd_workspace_size.restype = sz
         L.conv_bwd.argtypes = [dp] + [vp] * 8 + [sz, vp]
@@ -217,6 +221,20 @@ def conv_fwd_chain2(d1: ConvDesc, d2: ConvDesc, x, w1, bias1, w2, bias2, y1, y2,
     _check(lib().conv_fwd_chain2(ctypes.byref(d1), ctypes.byref(d2), _ptr(x), _ptr(w1), _ptr(bias1), _ptr(w2),
                                  _ptr(bias2), _ptr(y1), _ptr(y2), _ptr(workspace), nbytes, _stream(stream)),
            "conv_fwd_chain2")
+
+
+def conv_bwd_chain2_workspace_size(d1: ConvDesc, d2: ConvDesc) -> int:
+    return int(lib().conv_bwd_chain2_workspace_size(ctypes.byref(d1), ctypes.byref(d2)))
+
+
+def conv_bwd_chain2(d1: ConvDesc, d2: ConvDesc, x1, w1, y1, w2, y2, dy2, dx1, dw1, db1, dw2, db2, workspace,
+                    stream=None) -> None:
+    """Backward of the two-layer stack (dx1, db1, db2 may be None: not computed)."""
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().conv_bwd_chain2(ctypes.byref(d1), ctypes.byref(d2), _ptr(x1), _ptr(w1), _ptr(y1), _ptr(w2),
+                                 _ptr(y2), _ptr(dy2), _ptr(dx1), _ptr(dw1), _ptr(db1), _ptr(dw2), _ptr(db2),
+                                 _ptr(workspace), nbytes, _stream(stream)),
+           "conv_bwd_chain2")
 
 
 def conv_query_chain2(d1: ConvDesc, d2: ConvDesc) -> dict:

@@ -563,6 +563,56 @@ int conv_bwd(const conv_desc_t* desc, const void* x, const void* dy, const void*
     return wgrad_impl(desc, x, dy, y, dw, db, wws, workspace_bytes > off ? workspace_bytes - off : 0, stream);
 }
 
+namespace {
+
+// The backward chain's workspace: layer 2's dx (layer 1's dy) first, then the larger of the
+// workspaces its calls need (layer 2's conv_bwd, layer 1's conv_bwd or conv_bwd_filter), used
+// one call after the other.
+size_t bwd_chain_dx2_bytes(const conv_desc_t* d2)
+{
+    const size_t es = d2->dtype == CONV_BF16 ? 2 : 4;
+    return (size_t(d2->B) * d2->IC * d2->H * d2->W * es + 255) / 256 * 256;
+}
+
+size_t bwd_chain_call_ws(const conv_desc_t* d1, const conv_desc_t* d2)
+{
+    return std::max(plan_workspace(CONV_OP_BWD, d2),
+                    std::max(plan_workspace(CONV_OP_BWD, d1), plan_workspace(CONV_OP_BWD_FILTER, d1)));
+}
+
+}  // namespace
+
+size_t conv_bwd_chain2_workspace_size(const conv_desc_t* d1, const conv_desc_t* d2)
+{
+    ConvParams p1, p2;
+    if (chain_params(d1, d2, p1, p2) != CONV_OK) return 0;
+    return bwd_chain_dx2_bytes(d2) + bwd_chain_call_ws(d1, d2);
+}
+
+int conv_bwd_chain2(const conv_desc_t* d1, const conv_desc_t* d2, const void* x1, const void* w1, const void* y1,
+                    const void* w2, const void* y2, const void* dy2, void* dx1, void* dw1, void* db1, void* dw2,
+                    void* db2, void* workspace, size_t workspace_bytes, conv_stream_t stream)
+{
+    if (!d1 || !d2) return CONV_ERR_NULL;
+    ConvParams p1, p2;
+    int rc = chain_params(d1, d2, p1, p2);
+    if (rc != CONV_OK) return rc;
+    if (!w1 || !w2 || !dw1 || !dw2) return CONV_ERR_NULL;
+    if (p1.B > 0 && (!x1 || !y1 || !dy2 || (p2.relu && !y2))) return CONV_ERR_NULL;
+    if (workspace && !aligned16(workspace)) return CONV_ERR_ALIGN;
+    const size_t dx2_bytes = bwd_chain_dx2_bytes(d2), need = dx2_bytes + bwd_chain_call_ws(d1, d2);
+    if (need > 0 && (!workspace || workspace_bytes < need)) return CONV_ERR_WORKSPACE;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    void* dx2 = ws;
+    void* rest = ws ? ws + dx2_bytes : nullptr;
+    const size_t rest_bytes = ws ? workspace_bytes - dx2_bytes : 0;
+    // layer 2: x = y1, the mask source y2
+    if ((rc = conv_bwd(d2, y1, dy2, w2, y2, dx2, dw2, db2, rest, rest_bytes, stream)) != CONV_OK) return rc;
+    // layer 1 on dy = dx2, masked by y1; its d_input only when dx1 is wanted
+    if (dx1) return conv_bwd(d1, x1, dx2, w1, y1, dx1, dw1, db1, rest, rest_bytes, stream);
+    return wgrad_impl(d1, x1, dx2, y1, dw1, db1, rest, rest_bytes, stream);
+}
+
 uint64_t conv_fastdivmod_check(uint32_t d, uint32_t lo, uint32_t hi)
 {
     if (d < 1 || d >= (1u << 31)) return ~uint64_t(0);

@@ -247,6 +247,29 @@ int conv_fwd_chain2(const conv_desc_t* d1, const conv_desc_t* d2, const void* x,
                     const void* w2, const void* bias2, void* y1, void* y2, void* workspace, size_t workspace_bytes,
                     conv_stream_t stream);
 
+/* Two-layer backward chain, the backward of conv_fwd_chain2's stack (d1, d2 as there):
+ *   g2 = dy2 masked by y2 > 0 when d2->relu;  dx2 = conv_bwd_data(g2, w2);  dw2, db2 from g2;
+ *   g1 = dx2 masked by y1 > 0 when d1->relu;  dw1, db1 from g1;  dx1 = conv_bwd_data(g1, w1).
+ * Layer 2 runs as conv_bwd (d_input and wgrad of the layer in one launch where that call fuses
+ * them) with dx2 written into the workspace, not to a caller buffer: it is layer 1's dy and is
+ * read back at once (6.3 MB in fp32 at the encoder's B = 1024, so it stays in L2).  Layer 1
+ * runs as conv_bwd when dx1 is wanted, else as conv_bwd_filter / conv_bwd_filter_bias only --
+ * the input gradient of a network's first layer is not needed.  Layer 1's wgrad reduces g1
+ * over the whole batch, so dx2 has to be complete before it starts: the two layers are two
+ * fused calls, one after the other on the stream, not one kernel.  Results as those calls.
+ *   x1: layer 1's input  w1, w2: weights  y1: layer 1's output (layer 2's input and layer 1's
+ *   mask source; required)  y2: layer 2's output (required when d2->relu, else may be NULL)
+ *   dy2: (B, OC2, OH2, OW2)  dx1: NCHW like x1, or NULL (not computed)  dw1, dw2: written
+ *   db1, db2: the bias gradients, or NULL (not computed).
+ *   workspace: at least conv_bwd_chain2_workspace_size(d1, d2) bytes, 16-byte aligned, owned
+ *   by the caller; contents ignored on entry and unspecified on return.
+ * Errors: CONV_ERR_DESC when the descriptors do not chain (checked before any CUDA call), then
+ * as conv_bwd. */
+size_t conv_bwd_chain2_workspace_size(const conv_desc_t* d1, const conv_desc_t* d2);
+int conv_bwd_chain2(const conv_desc_t* d1, const conv_desc_t* d2, const void* x1, const void* w1, const void* y1,
+                    const void* w2, const void* y2, const void* dy2, void* dx1, void* dw1, void* db1, void* dw2,
+                    void* db2, void* workspace, size_t workspace_bytes, conv_stream_t stream);
+
 /* Weight gradient that allocates nothing (PufferLib PR #522 has no counterpart; this
  * entry point exists for callers of this library that cannot allocate device
  * memory: hosts that hand the library only the input and output buffers and own

@@ -72,6 +72,8 @@ def test_invalid_descriptor(L, bad):
     assert L.conv_fwd_chain2(ctypes.byref(d), ctypes.byref(d), fake, fake, None, fake, None, fake, fake, fake,
                              1 << 30, None) == -2
     assert L.conv_fwd_chain2_workspace_size(ctypes.byref(d), ctypes.byref(d)) == 0
+    assert L.conv_bwd_chain2(ctypes.byref(d), ctypes.byref(d), *([fake] * 11), fake, 1 << 30, None) == -2
+    assert L.conv_bwd_chain2_workspace_size(ctypes.byref(d), ctypes.byref(d)) == 0
     assert L.conv_bwd(ctypes.byref(d), fake, fake, fake, fake, fake, fake, None, fake, 1 << 30, None) == -2
     assert L.conv_bwd_workspace_size(ctypes.byref(d)) == 0
     assert L.conv_fwd_workspace_size(ctypes.byref(d)) == 0
@@ -144,6 +146,16 @@ def test_chain_descriptors_checked_before_cuda(L):
     odd = ctypes.c_void_p(0x1008)
     assert L.conv_fwd_chain2(ctypes.byref(d1), ctypes.byref(d2), ok, ok, None, ok, None, ok, odd, ok, 1 << 30,
                              None) == -4
+    # the backward chain: the same descriptor check, then the required pointers
+    for bad in (desc(IC=64, H=3, W=4, K=3, S=1), desc(B=7, IC=128, H=3, W=4, K=3, S=1)):
+        assert L.conv_bwd_chain2(ctypes.byref(d1), ctypes.byref(bad), *([fake] * 11), fake, 1 << 30, None) == -2
+        assert L.conv_bwd_chain2_workspace_size(ctypes.byref(d1), ctypes.byref(bad)) == 0
+    args = [ok] * 11  # x1 w1 y1 w2 y2 dy2 dx1 dw1 db1 dw2 db2
+    for i in (1, 2, 3, 5, 7, 9):  # w1, y1, w2, dy2, dw1, dw2 are required
+        a = list(args)
+        a[i] = None
+        assert L.conv_bwd_chain2(ctypes.byref(d1), ctypes.byref(d2), *a, ok, 1 << 30, None) == -1, i
+    assert L.conv_bwd_chain2(ctypes.byref(d1), ctypes.byref(d2), *args, odd, 1 << 30, None) == -4
 
 
 def test_empty_batch_is_a_no_op(L):

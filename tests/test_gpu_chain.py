@@ -179,3 +179,63 @@ def test_chain_descriptors_must_chain():
     with pytest.raises(binding.ConvError) as ei:
         binding.conv_query_chain2(d1, bad)
     assert ei.value.status == -2
+
+
+@pytest.mark.parametrize("dtype,B", [("f32", 37), ("f32", 1024), ("bf16", 37), ("bf16", 1024)])
+def test_backward_chain(dtype, B):
+    """conv_bwd_chain2: layer 2's backward with dx2 kept in the workspace, then layer 1's on it.
+    Stage by stage against the oracle: layer 2 on the GPU's y1 / y2, layer 1 on dx2 as
+    conv_bwd_data computes it (the same kernels, bit for bit); without dx1 only layer 1's wgrad
+    runs.  Biases' gradients included."""
+    from .gpu_cases import TORCH_DT
+    tdt = TORCH_DT[dtype]
+    i1 = synth.conv_inputs(B, L1["IC"], L1["OC"], L1["H"], L1["W"], L1["K"], L1["S"], dtype=dtype, need=("x", "w"))
+    w2 = synth.conv_inputs(1, L2["IC"], L2["OC"], L2["H"], L2["W"], L2["K"], L2["S"], dtype=dtype,
+                           w_stream=synth.STREAM_W2, need=("w",))["w"]
+    dy2 = synth.conv_inputs(B, L2["IC"], L2["OC"], L2["H"], L2["W"], L2["K"], L2["S"], dtype=dtype,
+                            need=("dy",))["dy"]
+    x1, W1, W2, DY2 = to_dev(i1["x"], dtype), to_dev(i1["w"], dtype), to_dev(w2, dtype), to_dev(dy2, dtype)
+    d1 = binding.make_desc(B, **L1, relu=1, dtype=tdt)
+    d2 = binding.make_desc(B, **L2, relu=1, dtype=tdt)  # a ReLU on layer 2 too: both masks
+    y1 = torch.empty((B, 128, 3, 4), dtype=tdt, device="cuda")
+    y2 = torch.empty((B, 128, 1, 2), dtype=tdt, device="cuda")
+    binding.conv_fwd(d1, x1, W1, y1)
+    binding.conv_fwd(d2, y1, W2, y2)
+    ws = torch.empty(binding.conv_bwd_chain2_workspace_size(d1, d2), dtype=torch.uint8, device="cuda")
+    nan = float("nan")
+    dx1 = torch.full_like(x1, nan)
+    dw1, dw2 = torch.full_like(W1, nan), torch.full_like(W2, nan)
+    db1 = torch.full((128,), nan, dtype=tdt, device="cuda")
+    db2 = torch.full((128,), nan, dtype=tdt, device="cuda")
+    binding.conv_bwd_chain2(d1, d2, x1, W1, y1, W2, y2, DY2, dx1, dw1, db1, dw2, db2, ws)
+    # without dx1 (and without the biases): layer 1's wgrad only
+    dw1b = torch.full_like(W1, nan)
+    dw2b = torch.full_like(W2, nan)
+    binding.conv_bwd_chain2(d1, d2, x1, W1, y1, W2, y2, DY2, None, dw1b, None, dw2b, None, ws)
+    dx2 = torch.empty_like(y1)
+    binding.conv_bwd_data(d2, DY2, W2, y2, dx2)
+    torch.cuda.synchronize()
+    assert binding.conv_device_status(reset=True) == 0
+    y1n, y2n, dx2n = to_np(y1), to_np(y2), to_np(dx2)
+    # layer 2
+    ref, den = oracle.conv_bwd_filter(y1n, dy2, y2n, 3, 1, True)
+    for out in (dw2, dw2b):
+        _check_dt(to_np(out), ref, den, dtype, f"B={B} {dtype} chain dw2")
+    ref, den = oracle.conv_bwd_bias(dy2, y2n, True)
+    _check_dt(to_np(db2), ref, den, dtype, f"B={B} {dtype} chain db2")
+    ref, den = oracle.conv_bwd_data(dy2, w2, y2n, 3, 4, 1, True)
+    _check_dt(dx2n, ref, den, dtype, f"B={B} {dtype} layer-2 dx (conv_bwd_data)")
+    # layer 1 on that dx2, masked by y1
+    ref, den = oracle.conv_bwd_filter(i1["x"], dx2n, y1n, 5, 3, True)
+    for out in (dw1, dw1b):
+        _check_dt(to_np(out), ref, den, dtype, f"B={B} {dtype} chain dw1")
+    ref, den = oracle.conv_bwd_bias(dx2n, y1n, True)
+    _check_dt(to_np(db1), ref, den, dtype, f"B={B} {dtype} chain db1")
+    ref, den = oracle.conv_bwd_data(dx2n, i1["w"], y1n, 11, 15, 3, True)
+    _check_dt(to_np(dx1), ref, den, dtype, f"B={B} {dtype} chain dx1")
+
+
+def _check_dt(out, ref, den, dtype, what):
+    assert np.isfinite(out).all(), what
+    err = oracle.normalised_error(out, ref, den)
+    assert err <= TOL[dtype], f"{what}: normalised error {err:.3e}"
